@@ -1,0 +1,121 @@
+"""Seeded synthetic inputs for the linear-attention layer.
+
+This module draws random numbers and nothing else: it holds none of the
+layer's arithmetic, so both the CUDA path and the CPU oracle can take their
+inputs from it.  Every tensor comes from a ``torch.Generator`` seeded by the
+caller, on the device the caller names.
+
+Workloads (the distributions are those of the configurations this library is
+measured on; "N(m, s)" means mean m, standard deviation s):
+
+* ``worked_example``  -- gated linear attention, one head, T=64, d=16, fp32:
+  q, k ~ N(0,1)/4, v ~ N(0,1), alpha = sigmoid(N(0,1) + 3), drawn in that order
+  from seed 0 (the worked example of "Inference for linear attention and
+  hybrid architectures", section "Two ways to write the same computation").
+* ``gla_prefill``     -- q, k ~ N(0,1)/sqrt(d), v ~ N(0,1) in bf16; alpha =
+  sigmoid(N(0,1) + 3) fp32 per token and head; zero start state.
+* ``gdn_prefill``     -- raw q, k with every row scaled to unit L2 norm and
+  v ~ N(0,1), in bf16; beta = sigmoid(N(0,1)); alpha = sigmoid(N(0,1) + 3);
+  conv weights N(0,1)/2 over the [q | k | v] channels; S0 ~ N(0, 0.01).
+* ``gdn_decode``      -- N requests x H heads, one token each; a pool of P
+  fp32 states ~ N(0, 0.01) and bf16 conv caches ~ N(0, 1); slot ids = the
+  first N entries of a random permutation of the P slots.
+* ``spec_drafts``     -- D draft tokens per request and an accepted prefix
+  length drawn uniformly from 0..D.
+"""
+from __future__ import annotations
+
+import torch
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def _randn(shape, g, device, scale=1.0, dtype=torch.float32):
+    x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if scale != 1.0:
+        x = x * scale
+    return x.to(dtype)
+
+
+def _unit_rows(x: torch.Tensor) -> torch.Tensor:
+    """Scale each last-axis row to unit Euclidean length (input recipe)."""
+    return x / x.norm(dim=-1, keepdim=True)
+
+
+def worked_example(device="cpu"):
+    """Seed 0, T=64, DK=DV=16, drawn in the page's order; shapes [1,T,1,d]."""
+    T, DK, DV = 64, 16, 16
+    g = _gen(0, device)
+    q = torch.randn(T, DK, generator=g, device=device) / 4
+    k = torch.randn(T, DK, generator=g, device=device) / 4
+    v = torch.randn(T, DV, generator=g, device=device)
+    alpha = torch.sigmoid(torch.randn(T, generator=g, device=device) + 3)
+    return dict(q=q[None, :, None], k=k[None, :, None], v=v[None, :, None],
+                alpha=alpha[None, :, None], chunk=16)
+
+
+def gla_prefill(B, H, T, d, seed=0, device="cpu", dtype=torch.bfloat16, s0_std=0.0):
+    g = _gen(seed, device)
+    q = _randn((B, T, H, d), g, device, d ** -0.5, dtype)
+    k = _randn((B, T, H, d), g, device, d ** -0.5, dtype)
+    v = _randn((B, T, H, d), g, device, 1.0, dtype)
+    alpha = torch.sigmoid(_randn((B, T, H), g, device) + 3.0)
+    S0 = _randn((B, H, d, d), g, device, s0_std) if s0_std > 0 else None
+    return dict(q=q, k=k, v=v, alpha=alpha, beta=None, S0=S0)
+
+
+def gdn_prefill(B, H, T, d, seed=0, device="cpu", dtype=torch.bfloat16, s0_std=0.01,
+                conv=True):
+    g = _gen(seed, device)
+    q = _unit_rows(_randn((B, T, H, d), g, device)).to(dtype)
+    k = _unit_rows(_randn((B, T, H, d), g, device)).to(dtype)
+    v = _randn((B, T, H, d), g, device, 1.0, dtype)
+    beta = torch.sigmoid(_randn((B, T, H), g, device))
+    alpha = torch.sigmoid(_randn((B, T, H), g, device) + 3.0)
+    conv_w = _randn((3 * H * d, 4), g, device, 0.5) if conv else None
+    S0 = _randn((B, H, d, d), g, device, s0_std) if s0_std > 0 else None
+    return dict(q=q, k=k, v=v, alpha=alpha, beta=beta, S0=S0, conv_w=conv_w)
+
+
+def gdn_decode(N, H, d, P, seed=0, device="cpu", dtype=torch.bfloat16, conv=True,
+               variant_gdn=True):
+    g = _gen(seed, device)
+    pool = _randn((P, H, d, d), g, device, 0.01)
+    conv_pool = _randn((P, 3, 3 * H * d), g, device, 1.0, dtype) if conv else None
+    perm = torch.randperm(P, generator=g, device=device)
+    slot_ids = perm[:N].to(torch.int32)
+    if variant_gdn:
+        q = _unit_rows(_randn((N, H, d), g, device)).to(dtype)
+        k = _unit_rows(_randn((N, H, d), g, device)).to(dtype)
+    else:
+        q = _randn((N, H, d), g, device, d ** -0.5, dtype)
+        k = _randn((N, H, d), g, device, d ** -0.5, dtype)
+    v = _randn((N, H, d), g, device, 1.0, dtype)
+    beta = torch.sigmoid(_randn((N, H), g, device)) if variant_gdn else None
+    alpha = torch.sigmoid(_randn((N, H), g, device) + 3.0)
+    conv_w = _randn((3 * H * d, 4), g, device, 0.5) if conv else None
+    return dict(q=q, k=k, v=v, alpha=alpha, beta=beta, pool=pool, conv_pool=conv_pool,
+                slot_ids=slot_ids, conv_w=conv_w)
+
+
+def spec_drafts(N, D, H, d, seed=0, device="cpu", dtype=torch.bfloat16):
+    """Draft-token inputs [N,D,H,*] and accepted prefix lengths a in 0..D."""
+    g = _gen(seed, device)
+    q = _unit_rows(_randn((N, D, H, d), g, device)).to(dtype)
+    k = _unit_rows(_randn((N, D, H, d), g, device)).to(dtype)
+    v = _randn((N, D, H, d), g, device, 1.0, dtype)
+    beta = torch.sigmoid(_randn((N, D, H), g, device))
+    alpha = torch.sigmoid(_randn((N, D, H), g, device) + 3.0)
+    accept = torch.randint(0, D + 1, (N,), generator=g, device=device, dtype=torch.int32)
+    return dict(q=q, k=k, v=v, alpha=alpha, beta=beta, accept=accept)
+
+
+def segment_lengths(T: int, fractions=(0.20, 0.35)):
+    """Split T into segments of floor(f*T) tokens for each fraction, and the rest."""
+    out = [int(T * f) for f in fractions]
+    out.append(T - sum(out))
+    return out
