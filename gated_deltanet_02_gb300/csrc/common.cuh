@@ -1,0 +1,38 @@
+// common.cuh -- small internals shared by the glinattn CUDA translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "glinattn.h"
+
+namespace glinattn {
+
+// Kernel parameters of the token-serial recurrent kernel (decode, speculative
+// decode and the fp32 prefill path).  A "unit" is one (request, head) pair;
+// every unit consumes `steps` tokens laid out [N, steps, H, d].
+struct RecurParams {
+  int variant, in_bf16, out_bf16, qk_l2norm;
+  int N, steps, H, pool_slots;  // pool_slots = 0 when states are not pooled
+  int Cch;                      // conv channels per request, H * 3d
+  const void *q, *k, *v;
+  const float *alpha, *beta;
+  // state source: S_src + (slot or n) * H*d*d + h*d*d; NULL means zeros
+  const float *S_src;
+  const int32_t *src_slot;  // [N] or NULL (index by n)
+  // state destination(s)
+  float *S_dst;
+  const int32_t *dst_slot;  // [N] (final) or [N*steps] (per step) or NULL (index by n)
+  int dst_per_step;
+  void *o;
+  // short convolution: weights [Cch, 4]; caches [.., 3, Cch] indexed like the states
+  const float *conv_w;
+  const void *conv_src;  // NULL = zero history
+  void *conv_dst;        // NULL = not written
+  uint32_t *dev_status;
+};
+
+glinattn_status launch_recurrent(const RecurParams &p, int d, cudaStream_t stream);
+
+}  // namespace glinattn

@@ -1,0 +1,204 @@
+// glinattn_api.cu -- the extern "C" boundary: host-side argument validation
+// and dispatch to the kernels.  Nothing is launched when validation fails.
+#include <stdio.h>
+#include <stdlib.h>
+
+#include "common.cuh"
+#include "prefill_tc.cuh"
+
+namespace {
+
+using glinattn::RecurParams;
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool supported_head(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+// [a, a+na) and [b, b+nb) overlap without being the same buffer
+bool partial_overlap(const void *a, size_t na, const void *b, size_t nb) {
+  if (!a || !b || a == b) return false;
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + nb && y < x + na;
+}
+
+glinattn_status check_common(int variant, int in_dtype, int out_dtype, int dk, int dv,
+                             int heads) {
+  if (variant != GLINATTN_GLA && variant != GLINATTN_GDN) return GLINATTN_ERR_INVALID_ARG;
+  if ((in_dtype != GLINATTN_F32 && in_dtype != GLINATTN_BF16) ||
+      (out_dtype != GLINATTN_F32 && out_dtype != GLINATTN_BF16))
+    return GLINATTN_ERR_INVALID_ARG;
+  if (heads <= 0 || dk <= 0 || dv <= 0) return GLINATTN_ERR_INVALID_ARG;
+  if (dk != dv || !supported_head(dk)) return GLINATTN_ERR_UNSUPPORTED;
+  return GLINATTN_OK;
+}
+
+template <typename... P>
+bool all_aligned(P... ptrs) {
+  const void *list[] = {ptrs...};
+  for (const void *p : list)
+    if (p && !aligned16(p)) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *glinattn_status_string(glinattn_status s) {
+  switch (s) {
+    case GLINATTN_OK: return "ok";
+    case GLINATTN_ERR_INVALID_ARG: return "invalid argument";
+    case GLINATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case GLINATTN_ERR_CUDA: return "CUDA error";
+    case GLINATTN_ERR_DEVICE_STATUS: return "device reported an error status";
+    case GLINATTN_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+int glinattn_version(void) { return 100; /* 0.1.0 */ }
+
+size_t glinattn_state_bytes(int heads, int dk, int dv) {
+  if (heads <= 0 || dk <= 0 || dv <= 0) return 0;
+  return (size_t)heads * dk * dv * sizeof(float);
+}
+
+glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream_t stream) {
+  if (!a) return GLINATTN_ERR_INVALID_ARG;
+  glinattn_status st = check_common(a->variant, a->in_dtype, a->out_dtype, a->dk, a->dv, a->heads);
+  if (st != GLINATTN_OK) return st;
+  if (a->batch < 0 || a->seqlen < 0) return GLINATTN_ERR_INVALID_ARG;
+  const int B = a->batch, T = a->seqlen, H = a->heads, d = a->dk;
+  if ((long long)B * H > (1ll << 30) || (long long)T > (1ll << 30)) return GLINATTN_ERR_INVALID_ARG;
+  if (B == 0) return GLINATTN_OK;
+  const size_t act = a->in_dtype == GLINATTN_BF16 ? 2 : 4;
+  const size_t state_bytes = (size_t)B * H * d * d * sizeof(float);
+  if (!a->S_T) return GLINATTN_ERR_INVALID_ARG;
+  if (T > 0) {
+    if (!a->q || !a->k || !a->v || !a->alpha || !a->o) return GLINATTN_ERR_INVALID_ARG;
+    if (a->variant == GLINATTN_GDN && !a->beta) return GLINATTN_ERR_INVALID_ARG;
+  }
+  if (!all_aligned(a->q, a->k, a->v, a->alpha, a->beta, a->S0, a->S_T, a->o, a->conv_w,
+                   a->conv_in, a->conv_out))
+    return GLINATTN_ERR_INVALID_ARG;
+  if (partial_overlap(a->S0, state_bytes, a->S_T, state_bytes)) return GLINATTN_ERR_INVALID_ARG;
+  const int Cch = H * 3 * d;
+  if (a->conv_w) {
+    const size_t cb = (size_t)B * 3 * Cch * act;
+    if (partial_overlap(a->conv_in, cb, a->conv_out, cb)) return GLINATTN_ERR_INVALID_ARG;
+  }
+
+  if (a->in_dtype == GLINATTN_BF16 && d == 128 && T > 0 && glinattn::prefill_tc_available()) {
+    return glinattn::launch_prefill_tc(*a, (cudaStream_t)stream);
+  }
+
+  RecurParams p = {};
+  p.variant = a->variant;
+  p.in_bf16 = a->in_dtype == GLINATTN_BF16;
+  p.out_bf16 = a->out_dtype == GLINATTN_BF16;
+  p.qk_l2norm = a->qk_l2norm != 0;
+  p.N = B;
+  p.steps = T;
+  p.H = H;
+  p.pool_slots = 0;
+  p.Cch = Cch;
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.alpha = a->alpha;
+  p.beta = a->beta;
+  p.S_src = a->S0;
+  p.S_dst = a->S_T;
+  p.o = a->o;
+  p.conv_w = a->conv_w;
+  p.conv_src = a->conv_w ? a->conv_in : nullptr;
+  p.conv_dst = a->conv_w ? a->conv_out : nullptr;
+  p.dev_status = a->dev_status;
+  return glinattn::launch_recurrent(p, d, (cudaStream_t)stream);
+}
+
+glinattn_status glinattn_decode(const glinattn_decode_args *a, glinattn_stream_t stream) {
+  if (!a) return GLINATTN_ERR_INVALID_ARG;
+  glinattn_status st = check_common(a->variant, a->in_dtype, a->out_dtype, a->dk, a->dv, a->heads);
+  if (st != GLINATTN_OK) return st;
+  if (a->num_req < 0 || a->pool_slots <= 0) return GLINATTN_ERR_INVALID_ARG;
+  if ((long long)a->num_req * a->heads > (1ll << 30)) return GLINATTN_ERR_INVALID_ARG;
+  if (a->num_req == 0) return GLINATTN_OK;
+  if (!a->q || !a->k || !a->v || !a->alpha || !a->o || !a->state_pool || !a->slot_ids)
+    return GLINATTN_ERR_INVALID_ARG;
+  if (a->variant == GLINATTN_GDN && !a->beta) return GLINATTN_ERR_INVALID_ARG;
+  if (a->conv_w && !a->conv_pool) return GLINATTN_ERR_INVALID_ARG;
+  if (!all_aligned(a->q, a->k, a->v, a->alpha, a->beta, a->state_pool, a->o, a->conv_w, a->conv_pool))
+    return GLINATTN_ERR_INVALID_ARG;
+  RecurParams p = {};
+  p.variant = a->variant;
+  p.in_bf16 = a->in_dtype == GLINATTN_BF16;
+  p.out_bf16 = a->out_dtype == GLINATTN_BF16;
+  p.qk_l2norm = a->qk_l2norm != 0;
+  p.N = a->num_req;
+  p.steps = 1;
+  p.H = a->heads;
+  p.pool_slots = a->pool_slots;
+  p.Cch = a->heads * 3 * a->dk;
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.alpha = a->alpha;
+  p.beta = a->beta;
+  p.S_src = a->state_pool;
+  p.src_slot = a->slot_ids;
+  p.S_dst = a->state_pool;
+  p.dst_slot = a->slot_ids;
+  p.dst_per_step = 0;
+  p.o = a->o;
+  p.conv_w = a->conv_w;
+  p.conv_src = a->conv_w ? a->conv_pool : nullptr;
+  p.conv_dst = a->conv_w ? a->conv_pool : nullptr;
+  p.dev_status = a->dev_status;
+  return glinattn::launch_recurrent(p, a->dk, (cudaStream_t)stream);
+}
+
+glinattn_status glinattn_spec_decode(const glinattn_spec_args *a, glinattn_stream_t stream) {
+  if (!a) return GLINATTN_ERR_INVALID_ARG;
+  glinattn_status st = check_common(a->variant, a->in_dtype, a->out_dtype, a->dk, a->dv, a->heads);
+  if (st != GLINATTN_OK) return st;
+  if (a->num_req < 0 || a->draft_len <= 0 || a->pool_slots <= 0) return GLINATTN_ERR_INVALID_ARG;
+  if ((long long)a->num_req * a->heads > (1ll << 30) || a->draft_len > (1 << 20))
+    return GLINATTN_ERR_INVALID_ARG;
+  if (a->num_req == 0) return GLINATTN_OK;
+  if (!a->q || !a->k || !a->v || !a->alpha || !a->o || !a->state_pool || !a->src_slots ||
+      !a->dst_slots)
+    return GLINATTN_ERR_INVALID_ARG;
+  if (a->variant == GLINATTN_GDN && !a->beta) return GLINATTN_ERR_INVALID_ARG;
+  if (a->conv_w && !a->conv_pool) return GLINATTN_ERR_INVALID_ARG;
+  if (!all_aligned(a->q, a->k, a->v, a->alpha, a->beta, a->state_pool, a->o, a->conv_w, a->conv_pool))
+    return GLINATTN_ERR_INVALID_ARG;
+  RecurParams p = {};
+  p.variant = a->variant;
+  p.in_bf16 = a->in_dtype == GLINATTN_BF16;
+  p.out_bf16 = a->out_dtype == GLINATTN_BF16;
+  p.qk_l2norm = a->qk_l2norm != 0;
+  p.N = a->num_req;
+  p.steps = a->draft_len;
+  p.H = a->heads;
+  p.pool_slots = a->pool_slots;
+  p.Cch = a->heads * 3 * a->dk;
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.alpha = a->alpha;
+  p.beta = a->beta;
+  p.S_src = a->state_pool;
+  p.src_slot = a->src_slots;
+  p.S_dst = a->state_pool;
+  p.dst_slot = a->dst_slots;
+  p.dst_per_step = 1;
+  p.o = a->o;
+  p.conv_w = a->conv_w;
+  p.conv_src = a->conv_w ? a->conv_pool : nullptr;
+  p.conv_dst = a->conv_w ? a->conv_pool : nullptr;
+  p.dev_status = a->dev_status;
+  return glinattn::launch_recurrent(p, a->dk, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,16 @@
+// prefill_tc.cuh -- tensor-core (tcgen05 / TMEM / TMA) chunked prefill.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "glinattn.h"
+
+namespace glinattn {
+
+// True when the chunked tensor-core kernels are built into this library.
+bool prefill_tc_available();
+
+// bf16 activations, dk == dv == 128, chunk 64.  Arguments already validated.
+glinattn_status launch_prefill_tc(const glinattn_prefill_args &a, cudaStream_t stream);
+
+}  // namespace glinattn

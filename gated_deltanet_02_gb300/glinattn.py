@@ -1,0 +1,253 @@
+"""Thin Python binding of the glinattn C ABI (``include/glinattn.h``).
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels of
+``libglinattn.so``.  PyTorch supplies device memory and streams.  There is no
+CPU fallback: if the library cannot be built or loaded, every call raises.
+
+The three entry points keep the C names:
+
+* ``glinattn_prefill``     -- chunked prefill of a segment (state hand-over in/out)
+* ``glinattn_decode``      -- one recurrent step per request, state pool by slot id
+* ``glinattn_spec_decode`` -- D draft steps, one state per draft position
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import build as _build
+
+GLA, GDN = 0, 1
+F32, BF16 = 0, 1
+
+DEV_BAD_SLOT = 0x1
+DEV_BAD_GATE = 0x2
+DEV_WAIT_TIMEOUT = 0x4
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
+           4: "device reported an error status", 5: "device wait timed out"}
+
+
+class GlinattnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {_STATUS.get(status, status)} (status {status})")
+        self.status = status
+
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+
+
+class PrefillArgs(ctypes.Structure):
+    _fields_ = [("variant", _i32), ("in_dtype", _i32), ("out_dtype", _i32), ("qk_l2norm", _i32),
+                ("batch", _i32), ("seqlen", _i32), ("heads", _i32), ("dk", _i32), ("dv", _i32),
+                ("reserved0", _i32),
+                ("q", _vp), ("k", _vp), ("v", _vp), ("alpha", _vp), ("beta", _vp), ("S0", _vp),
+                ("S_T", _vp), ("o", _vp), ("conv_w", _vp), ("conv_in", _vp), ("conv_out", _vp),
+                ("dev_status", _vp)]
+
+
+class DecodeArgs(ctypes.Structure):
+    _fields_ = [("variant", _i32), ("in_dtype", _i32), ("out_dtype", _i32), ("qk_l2norm", _i32),
+                ("num_req", _i32), ("heads", _i32), ("dk", _i32), ("dv", _i32),
+                ("pool_slots", _i32), ("reserved0", _i32),
+                ("q", _vp), ("k", _vp), ("v", _vp), ("alpha", _vp), ("beta", _vp),
+                ("state_pool", _vp), ("slot_ids", _vp), ("o", _vp), ("conv_w", _vp),
+                ("conv_pool", _vp), ("dev_status", _vp)]
+
+
+class SpecArgs(ctypes.Structure):
+    _fields_ = [("variant", _i32), ("in_dtype", _i32), ("out_dtype", _i32), ("qk_l2norm", _i32),
+                ("num_req", _i32), ("draft_len", _i32), ("heads", _i32), ("dk", _i32),
+                ("dv", _i32), ("pool_slots", _i32),
+                ("q", _vp), ("k", _vp), ("v", _vp), ("alpha", _vp), ("beta", _vp),
+                ("state_pool", _vp), ("src_slots", _vp), ("dst_slots", _vp), ("o", _vp),
+                ("conv_w", _vp), ("conv_pool", _vp), ("dev_status", _vp)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """Load ``libglinattn.so`` (building it first when its sources are newer)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            lib = ctypes.CDLL(path)
+            for name, argt in (("glinattn_prefill", PrefillArgs), ("glinattn_decode", DecodeArgs),
+                               ("glinattn_spec_decode", SpecArgs)):
+                f = getattr(lib, name)
+                f.argtypes = [ctypes.POINTER(argt), _vp]
+                f.restype = ctypes.c_int
+            lib.glinattn_status_string.argtypes = [ctypes.c_int]
+            lib.glinattn_status_string.restype = ctypes.c_char_p
+            lib.glinattn_version.restype = ctypes.c_int
+            lib.glinattn_state_bytes.argtypes = [ctypes.c_int] * 3
+            lib.glinattn_state_bytes.restype = ctypes.c_size_t
+            _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"activations must be bf16 or fp32, got {t.dtype}")
+
+
+def _need(t, name, dtype=None, shape=None, device=None):
+    if t is None:
+        return
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _call(name, args, stream_handle):
+    rc = getattr(library(), name)(ctypes.byref(args), stream_handle)
+    if rc != 0:
+        raise GlinattnError(rc, name)
+
+
+def glinattn_prefill(q, k, v, alpha, beta=None, S0=None, *, variant=GLA, conv_w=None,
+                     conv_in=None, qk_l2norm=False, out_dtype=None, o=None, S_T=None,
+                     conv_out=None, dev_status=None, stream=None):
+    """Prefill one segment.  q, k [B,T,H,dk], v [B,T,H,dv] (bf16 or fp32);
+    alpha/beta [B,T,H] fp32; S0 [B,H,dk,dv] fp32 or None.  Outputs are
+    allocated when not given.  Returns (o, S_T, conv_out)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    act = q.dtype
+    _need(q, "q", act, (B, T, H, dk), dev)
+    _need(k, "k", act, (B, T, H, dk), dev)
+    _need(v, "v", act, (B, T, H, dv), dev)
+    _need(alpha, "alpha", torch.float32, (B, T, H), dev)
+    _need(beta, "beta", torch.float32, (B, T, H), dev)
+    _need(S0, "S0", torch.float32, (B, H, dk, dv), dev)
+    out_dtype = act if out_dtype is None else out_dtype
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=out_dtype, device=dev)
+    if S_T is None:
+        S_T = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+    Cch = H * (2 * dk + dv)
+    if conv_w is not None:
+        _need(conv_w, "conv_w", torch.float32, (Cch, 4), dev)
+        _need(conv_in, "conv_in", act, (B, 3, Cch), dev)
+        if conv_out is None:
+            conv_out = torch.empty((B, 3, Cch), dtype=act, device=dev)
+        _need(conv_out, "conv_out", act, (B, 3, Cch), dev)
+    _need(o, "o", out_dtype, (B, T, H, dv), dev)
+    _need(S_T, "S_T", torch.float32, (B, H, dk, dv), dev)
+    a = PrefillArgs(variant=variant, in_dtype=_dtype_code(q), out_dtype=_dtype_code(o),
+                    qk_l2norm=int(bool(qk_l2norm)), batch=B, seqlen=T, heads=H, dk=dk, dv=dv,
+                    q=_ptr(q), k=_ptr(k), v=_ptr(v), alpha=_ptr(alpha), beta=_ptr(beta),
+                    S0=_ptr(S0), S_T=_ptr(S_T), o=_ptr(o), conv_w=_ptr(conv_w),
+                    conv_in=_ptr(conv_in), conv_out=_ptr(conv_out), dev_status=_ptr(dev_status))
+    _call("glinattn_prefill", a, _stream_handle(stream, dev))
+    return o, S_T, conv_out
+
+
+def glinattn_decode(q, k, v, alpha, beta, state_pool, slot_ids, *, variant=GDN, conv_w=None,
+                    conv_pool=None, qk_l2norm=False, out_dtype=None, o=None, dev_status=None,
+                    stream=None):
+    """One decode step.  q, k [N,H,dk], v [N,H,dv]; alpha/beta [N,H];
+    state_pool [P,H,dk,dv] fp32 and conv_pool [P,3,Cch] updated in place at
+    slot_ids [N] int32.  Returns o [N,H,dv]."""
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    act = q.dtype
+    P = state_pool.shape[0]
+    _need(q, "q", act, (N, H, dk), dev)
+    _need(k, "k", act, (N, H, dk), dev)
+    _need(v, "v", act, (N, H, dv), dev)
+    _need(alpha, "alpha", torch.float32, (N, H), dev)
+    _need(beta, "beta", torch.float32, (N, H), dev)
+    _need(state_pool, "state_pool", torch.float32, (P, H, dk, dv), dev)
+    _need(slot_ids, "slot_ids", torch.int32, (N,), dev)
+    Cch = H * (2 * dk + dv)
+    if conv_w is not None:
+        _need(conv_w, "conv_w", torch.float32, (Cch, 4), dev)
+        _need(conv_pool, "conv_pool", act, (P, 3, Cch), dev)
+    out_dtype = act if out_dtype is None else out_dtype
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=out_dtype, device=dev)
+    _need(o, "o", out_dtype, (N, H, dv), dev)
+    a = DecodeArgs(variant=variant, in_dtype=_dtype_code(q), out_dtype=_dtype_code(o),
+                   qk_l2norm=int(bool(qk_l2norm)), num_req=N, heads=H, dk=dk, dv=dv,
+                   pool_slots=P, q=_ptr(q), k=_ptr(k), v=_ptr(v), alpha=_ptr(alpha),
+                   beta=_ptr(beta), state_pool=_ptr(state_pool), slot_ids=_ptr(slot_ids),
+                   o=_ptr(o), conv_w=_ptr(conv_w), conv_pool=_ptr(conv_pool) if conv_w is not None else None,
+                   dev_status=_ptr(dev_status))
+    _call("glinattn_decode", a, _stream_handle(stream, dev))
+    return o
+
+
+def glinattn_spec_decode(q, k, v, alpha, beta, state_pool, src_slots, dst_slots, *, variant=GDN,
+                         conv_w=None, conv_pool=None, qk_l2norm=False, out_dtype=None, o=None,
+                         dev_status=None, stream=None):
+    """D draft steps per request.  q, k [N,D,H,dk], v [N,D,H,dv];
+    alpha/beta [N,D,H]; src_slots [N], dst_slots [N,D] int32.  The state after
+    draft i is written to state_pool[dst_slots[n, i]].  Returns o [N,D,H,dv]."""
+    N, D, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    act = q.dtype
+    P = state_pool.shape[0]
+    _need(q, "q", act, (N, D, H, dk), dev)
+    _need(k, "k", act, (N, D, H, dk), dev)
+    _need(v, "v", act, (N, D, H, dv), dev)
+    _need(alpha, "alpha", torch.float32, (N, D, H), dev)
+    _need(beta, "beta", torch.float32, (N, D, H), dev)
+    _need(state_pool, "state_pool", torch.float32, (P, H, dk, dv), dev)
+    _need(src_slots, "src_slots", torch.int32, (N,), dev)
+    _need(dst_slots, "dst_slots", torch.int32, (N, D), dev)
+    Cch = H * (2 * dk + dv)
+    if conv_w is not None:
+        _need(conv_w, "conv_w", torch.float32, (Cch, 4), dev)
+        _need(conv_pool, "conv_pool", act, (P, 3, Cch), dev)
+    out_dtype = act if out_dtype is None else out_dtype
+    if o is None:
+        o = torch.empty((N, D, H, dv), dtype=out_dtype, device=dev)
+    _need(o, "o", out_dtype, (N, D, H, dv), dev)
+    a = SpecArgs(variant=variant, in_dtype=_dtype_code(q), out_dtype=_dtype_code(o),
+                 qk_l2norm=int(bool(qk_l2norm)), num_req=N, draft_len=D, heads=H, dk=dk, dv=dv,
+                 pool_slots=P, q=_ptr(q), k=_ptr(k), v=_ptr(v), alpha=_ptr(alpha), beta=_ptr(beta),
+                 state_pool=_ptr(state_pool), src_slots=_ptr(src_slots), dst_slots=_ptr(dst_slots),
+                 o=_ptr(o), conv_w=_ptr(conv_w), conv_pool=_ptr(conv_pool) if conv_w is not None else None,
+                 dev_status=_ptr(dev_status))
+    _call("glinattn_spec_decode", a, _stream_handle(stream, dev))
+    return o
+
+
+def version() -> int:
+    return library().glinattn_version()
+
+
+def status_string(code: int) -> str:
+    return library().glinattn_status_string(code).decode()
+
+
+def state_bytes(heads: int, dk: int, dv: int) -> int:
+    return library().glinattn_state_bytes(heads, dk, dv)

@@ -1,0 +1,185 @@
+/*
+ * glinattn.h -- C ABI of the GB300 (sm_103a) state-passing linear-attention
+ * layer: gated linear attention (GLA) and Gated DeltaNet (GDN).
+ *
+ * Source: "Inference for linear attention and hybrid architectures"
+ * (ai-infra-handbooks):
+ *   - section "Two ways to write the same computation": the two recurrences,
+ *       GLA  S_t = alpha_t S_{t-1} + k_t^T v_t
+ *       GDN  S_t = alpha_t (I - beta_t k_t^T k_t) S_{t-1} + beta_t k_t^T v_t
+ *     with o_t = q_t S_t read after the update; the chunked form used for
+ *     prefill; the hand-over of the state between prefill segments; the short
+ *     causal convolution in front of the layer and its per-request cache;
+ *   - section "A new memory ledger": a per-request state pool, states in fp32;
+ *   - section "Speculative decoding and PD disaggregation": one state per
+ *     draft position for rollback; batched kernels read and write the state
+ *     pool by slot index.
+ *
+ * Conventions shared by every call
+ *   - All tensor arguments are DEVICE pointers to caller-owned memory,
+ *     contiguous row-major in the layout stated (innermost index last), with
+ *     the base address 16-byte aligned.  The library keeps no pointer after
+ *     the call returns and allocates no device memory.
+ *   - Calls are asynchronous on the given stream (0 = legacy default stream).
+ *     Argument errors are detected on the host before anything is launched and
+ *     returned as a status; the output buffers are then untouched.
+ *   - dev_status (nullable) is a device word the kernels OR error bits into
+ *     (GLINATTN_DEV_*); a unit that raises a bit skips its writes.  The caller
+ *     zeroes it and reads it after synchronising.
+ *   - Head sizes: dk == dv, one of 16, 32, 64, 128.  Activations (q, k, v,
+ *     conv cache) are all GLINATTN_BF16 or all GLINATTN_F32; gates alpha and
+ *     beta, states and conv weights are fp32.  alpha must lie in (0, 1],
+ *     beta in [0, 1].
+ *   - The short convolution is depthwise, width 4, over the channels
+ *     [q | k | v] of every head, Cch = H * (2 dk + dv) channels, channel index
+ *     part_offset + h * d + i.  Weight w[c][j] multiplies input x_{t-3+j}
+ *     (tap 3 is the current token); no bias, no activation.  The conv cache
+ *     holds the last 3 RAW inputs per channel, oldest first: [.., 3, Cch].
+ *   - qk_l2norm != 0 rescales each q and k row of each head to
+ *     x / sqrt(sum x^2 + 1e-6) after the convolution.  With bf16 activations
+ *     the convolved / normalised values are rounded to bf16 before use.
+ */
+#ifndef GLINATTN_H
+#define GLINATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *glinattn_stream_t; /* a cudaStream_t */
+
+typedef enum {
+  GLINATTN_OK = 0,
+  GLINATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, aliasing */
+  GLINATTN_ERR_UNSUPPORTED = 2, /* valid but not built: head size, dtype combination */
+  GLINATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, attribute) */
+  GLINATTN_ERR_DEVICE_STATUS = 4, /* reserved for host helpers that read dev_status */
+  GLINATTN_ERR_TIMEOUT = 5      /* reserved: a bounded device wait gave up */
+} glinattn_status;
+
+typedef enum { GLINATTN_GLA = 0, GLINATTN_GDN = 1 } glinattn_variant;
+typedef enum { GLINATTN_F32 = 0, GLINATTN_BF16 = 1 } glinattn_dtype;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define GLINATTN_DEV_BAD_SLOT 0x1u    /* slot id outside [0, pool_slots): unit skipped */
+#define GLINATTN_DEV_BAD_GATE 0x2u    /* alpha outside (0, 1] or not finite: unit skipped */
+#define GLINATTN_DEV_WAIT_TIMEOUT 0x4u /* an on-chip barrier wait exceeded its bound */
+
+/*
+ * glinattn_prefill -- chunked prefill of one segment for B sequences.
+ *   Computes o_t = q_t S_t for t = 1..T and the final state S_T of every
+ *   (sequence, head), starting from S0 (or zeros) and the conv cache conv_in
+ *   (or zero history).  Feeding S_T and conv_out of one call as S0 and
+ *   conv_in of the next continues the sequence exactly (segmented prefill).
+ *
+ *   q, k   [B, T, H, dk]   v [B, T, H, dv]       activations (in_dtype)
+ *   alpha  [B, T, H]       beta [B, T, H] (GDN only, else NULL)       fp32
+ *   S0     [B, H, dk, dv]  fp32 or NULL (zero state)
+ *   S_T    [B, H, dk, dv]  fp32 output; may alias S0 exactly
+ *   o      [B, T, H, dv]   output (out_dtype)
+ *   conv_w [Cch, 4] fp32 or NULL (no convolution; conv_in/conv_out ignored)
+ *   conv_in  [B, 3, Cch] (in_dtype) or NULL (zero history)
+ *   conv_out [B, 3, Cch] (in_dtype) or NULL; may alias conv_in exactly
+ *   T may be any value >= 0 (a ragged last chunk is handled); T == 0 copies
+ *   S0 to S_T and conv_in to conv_out.
+ *   bf16 activations with dk == dv == 128 run the tensor-core chunked kernels
+ *   (chunk 64); every other supported combination runs the fp32 token-serial
+ *   kernel, which is exact to fp32 rounding but not fast.
+ */
+typedef struct {
+  int32_t variant;   /* glinattn_variant */
+  int32_t in_dtype;  /* glinattn_dtype of q, k, v, conv cache */
+  int32_t out_dtype; /* glinattn_dtype of o */
+  int32_t qk_l2norm;
+  int32_t batch, seqlen, heads, dk, dv;
+  int32_t reserved0;
+  const void *q, *k, *v;
+  const float *alpha, *beta;
+  const float *S0;
+  float *S_T;
+  void *o;
+  const float *conv_w;
+  const void *conv_in;
+  void *conv_out;
+  uint32_t *dev_status;
+} glinattn_prefill_args;
+
+glinattn_status glinattn_prefill(const glinattn_prefill_args *args, glinattn_stream_t stream);
+
+/*
+ * glinattn_decode -- one recurrent decode step for N requests.
+ *   For request n with slot s = slot_ids[n]: runs the conv step against
+ *   conv_pool[s] (then shifts it), reads state_pool[s], applies one rank-one
+ *   update, writes the state back IN PLACE and writes o[n].  Slots not named
+ *   in slot_ids are not touched.  slot_ids must be distinct (not checked on
+ *   the device: duplicates race); ids outside [0, pool_slots) set
+ *   GLINATTN_DEV_BAD_SLOT and skip that request.
+ *
+ *   q, k [N, H, dk]   v [N, H, dv]   alpha, beta [N, H]   slot_ids [N] int32
+ *   state_pool [P, H, dk, dv] fp32 (read/write)   o [N, H, dv]
+ *   conv_w [Cch, 4] or NULL;  conv_pool [P, 3, Cch] (in_dtype, read/write)
+ */
+typedef struct {
+  int32_t variant, in_dtype, out_dtype, qk_l2norm;
+  int32_t num_req, heads, dk, dv, pool_slots;
+  int32_t reserved0;
+  const void *q, *k, *v;
+  const float *alpha, *beta;
+  float *state_pool;
+  const int32_t *slot_ids;
+  void *o;
+  const float *conv_w;
+  void *conv_pool;
+  uint32_t *dev_status;
+} glinattn_decode_args;
+
+glinattn_status glinattn_decode(const glinattn_decode_args *args, glinattn_stream_t stream);
+
+/*
+ * glinattn_spec_decode -- speculative decode of D draft tokens per request,
+ *   keeping one state per draft position.  Starting from state_pool[src_slots[n]]
+ *   (and its conv cache), step i = 0..D-1 consumes draft token i and writes the
+ *   state after it to state_pool[dst_slots[n*D + i]] (and the conv cache to the
+ *   same slot of conv_pool); o[n, i] is its output.  The source slot is only
+ *   read.  Rolling back to an accepted prefix of length a is the caller's
+ *   choice of slot: src_slots[n] for a = 0, else dst_slots[n*D + a - 1]; the
+ *   state there is bit-identical to a decode steps of glinattn_decode.
+ *   All destination slots of all requests must be distinct from each other
+ *   and from every source slot (not checked on the device).
+ *
+ *   q, k [N, D, H, dk]   v [N, D, H, dv]   alpha, beta [N, D, H]
+ *   src_slots [N]  dst_slots [N, D]  int32    o [N, D, H, dv]
+ */
+typedef struct {
+  int32_t variant, in_dtype, out_dtype, qk_l2norm;
+  int32_t num_req, draft_len, heads, dk, dv, pool_slots;
+  const void *q, *k, *v;
+  const float *alpha, *beta;
+  float *state_pool;
+  const int32_t *src_slots;
+  const int32_t *dst_slots;
+  void *o;
+  const float *conv_w;
+  void *conv_pool;
+  uint32_t *dev_status;
+} glinattn_spec_args;
+
+glinattn_status glinattn_spec_decode(const glinattn_spec_args *args, glinattn_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *glinattn_status_string(glinattn_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int glinattn_version(void);
+
+/* Bytes of one request's state in one layer: heads * dk * dv * 4. */
+size_t glinattn_state_bytes(int heads, int dk, int dv);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GLINATTN_H */

@@ -1,0 +1,160 @@
+"""The C-ABI library: loads, exports every declared symbol, matches the
+header's struct layout, and rejects bad arguments on the host (no launch)."""
+import ctypes
+import json
+import os
+import re
+import subprocess
+
+import pytest
+
+from gated_deltanet_02_gb300 import glinattn as G
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "glinattn.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(glinattn_\w+)\s*\(", text, re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = G.library()
+    names = _declared_functions()
+    assert {"glinattn_prefill", "glinattn_decode", "glinattn_spec_decode",
+            "glinattn_status_string", "glinattn_version"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", G._build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    for name in names:
+        assert re.search(rf"\bT {name}$", out, re.M), name
+
+
+def test_struct_layout_matches_header(tmp_path):
+    src = tmp_path / "layout.c"
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "glinattn.h"', "int main(void){"]
+    for ct, cname in ((G.PrefillArgs, "glinattn_prefill_args"), (G.DecodeArgs, "glinattn_decode_args"),
+                      (G.SpecArgs, "glinattn_spec_args")):
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in ct._fields_:
+            lines.append(f'printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines.append("return 0;}")
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n"):
+        if line:
+            s, f, v = line.split()
+            got[(s, f)] = int(v)
+    for ct, cname in ((G.PrefillArgs, "glinattn_prefill_args"), (G.DecodeArgs, "glinattn_decode_args"),
+                      (G.SpecArgs, "glinattn_spec_args")):
+        assert got[(cname, "size")] == ctypes.sizeof(ct)
+        for fname, _ in ct._fields_:
+            assert got[(cname, fname)] == getattr(ct, fname).offset, (cname, fname)
+
+
+def test_version_status_and_state_size():
+    lib = G.library()
+    assert lib.glinattn_version() >= 100
+    for code in range(6):
+        assert G.status_string(code) != "unknown status"
+    assert G.status_string(99) == "unknown status"
+    ledger = json.load(open(os.path.join(ROOT, "tests", "golden", "memory_ledger.json")))
+    d = ledger["head_state_shape"][0]
+    assert G.state_bytes(1, d, d) == ledger["head_state_bytes_fp32"]
+    per_layer = G.state_bytes(ledger["heads_per_linear_layer"], d, d)
+    assert per_layer * ledger["linear_layers"] == ledger["state_bytes_per_request"]
+    # the conv cache of one layer: [q | k | v] channels of every head
+    assert ledger["heads_per_linear_layer"] * 3 * d == ledger["conv_channels_per_layer"]
+    assert G.state_bytes(0, 128, 128) == 0
+
+
+# Fake, aligned device addresses: validation must reject before any dereference.
+A = 0x10000
+
+
+def _prefill(**kw):
+    base = dict(variant=G.GDN, in_dtype=G.BF16, out_dtype=G.F32, qk_l2norm=1, batch=2, seqlen=100,
+                heads=4, dk=128, dv=128, q=A, k=A * 2, v=A * 3, alpha=A * 4, beta=A * 5, S0=None,
+                S_T=A * 6, o=A * 7)
+    base.update(kw)
+    return G.PrefillArgs(**base)
+
+
+def _decode(**kw):
+    base = dict(variant=G.GDN, in_dtype=G.BF16, out_dtype=G.F32, num_req=4, heads=2, dk=64, dv=64,
+                pool_slots=8, q=A, k=A * 2, v=A * 3, alpha=A * 4, beta=A * 5, state_pool=A * 6,
+                slot_ids=A * 7, o=A * 8)
+    base.update(kw)
+    return G.DecodeArgs(**base)
+
+
+def _spec(**kw):
+    base = dict(variant=G.GDN, in_dtype=G.BF16, out_dtype=G.F32, num_req=4, draft_len=3, heads=2,
+                dk=64, dv=64, pool_slots=32, q=A, k=A * 2, v=A * 3, alpha=A * 4, beta=A * 5,
+                state_pool=A * 6, src_slots=A * 7, dst_slots=A * 8, o=A * 9)
+    base.update(kw)
+    return G.SpecArgs(**base)
+
+
+INVALID, UNSUPPORTED = 1, 2
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(variant=7), INVALID),
+    (dict(in_dtype=5), INVALID),
+    (dict(out_dtype=-1), INVALID),
+    (dict(dk=96, dv=96), UNSUPPORTED),
+    (dict(dk=128, dv=64), UNSUPPORTED),
+    (dict(heads=0), INVALID),
+    (dict(batch=-1), INVALID),
+    (dict(seqlen=-5), INVALID),
+    (dict(q=None), INVALID),
+    (dict(beta=None), INVALID),          # Gated DeltaNet needs beta
+    (dict(S_T=None), INVALID),
+    (dict(o=None), INVALID),
+    (dict(q=A + 8), INVALID),            # 16-byte alignment
+    (dict(S0=A * 6 + 64), INVALID),      # S0 partially overlaps S_T
+])
+def test_prefill_rejects(kw, code):
+    rc = G.library().glinattn_prefill(ctypes.byref(_prefill(**kw)), None)
+    assert rc == code
+
+
+def test_prefill_null_args_and_empty_batch():
+    lib = G.library()
+    assert lib.glinattn_prefill(None, None) == INVALID
+    # B = 0 is a no-op that launches nothing, even with null tensors
+    assert lib.glinattn_prefill(ctypes.byref(_prefill(batch=0, q=None, o=None)), None) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(pool_slots=0), INVALID),
+    (dict(slot_ids=None), INVALID),
+    (dict(state_pool=None), INVALID),
+    (dict(state_pool=A * 6 + 4), INVALID),
+    (dict(dk=48, dv=48), UNSUPPORTED),
+    (dict(conv_w=A * 9, conv_pool=None), INVALID),
+    (dict(num_req=-1), INVALID),
+])
+def test_decode_rejects(kw, code):
+    assert G.library().glinattn_decode(ctypes.byref(_decode(**kw)), None) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(draft_len=0), INVALID),
+    (dict(dst_slots=None), INVALID),
+    (dict(src_slots=None), INVALID),
+    (dict(variant=G.GDN, beta=None), INVALID),
+])
+def test_spec_rejects(kw, code):
+    assert G.library().glinattn_spec_decode(ctypes.byref(_spec(**kw)), None) == code
+
+
+def test_zero_requests_is_a_noop():
+    lib = G.library()
+    assert lib.glinattn_decode(ctypes.byref(_decode(num_req=0, q=None)), None) == 0
+    assert lib.glinattn_spec_decode(ctypes.byref(_spec(num_req=0, q=None)), None) == 0

@@ -1,0 +1,155 @@
+"""GPU parity of prefill against the oracle.
+
+"Inference for linear attention and hybrid architectures", section "Two ways
+to write the same computation": the chunked form equals the recurrence, and a
+prompt prefilled in segments (the state handed from one segment to the next)
+equals one prefill; section "Checking on a real model" checks the same on a
+real model with a three-segment prefill.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_02_gb300 import GDN, GLA, glinattn_prefill, inputs
+from oracle.chunked import chunked
+
+from helpers import TOL_F32, TOL_O_BF16, TOL_S_BF16, f64, relerr, to
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def _gpu_prefill(g, variant, conv, S0=None, conv_in=None, out_dtype=torch.float32):
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o, S, c = glinattn_prefill(g["q"], g["k"], g["v"], g["alpha"], g.get("beta"), S0,
+                               variant=variant, conv_w=g.get("conv_w") if conv else None,
+                               conv_in=conv_in, qk_l2norm=conv, out_dtype=out_dtype,
+                               dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return o, S, c
+
+
+def _oracle_prefill(ex, variant, conv, S0=None, conv_in=None, sl=slice(None), heads=slice(None)):
+    def cut(t):
+        return None if t is None else f64(t[:, sl, heads] if t.dim() >= 3 else t)
+    q, k, v = cut(ex["q"]), cut(ex["k"]), cut(ex["v"])
+    a = cut(ex["alpha"])
+    b = cut(ex.get("beta")) if variant == GDN else None
+    return oracle.layer_prefill(variant, q, k, v, a, b, S0, f64(ex.get("conv_w")) if conv else None,
+                                conv_in, conv, nthreads=8)
+
+
+def test_worked_example_fp32():
+    """T=64, d=16, fp32: the GPU matches the oracle to 1e-5 and, like the
+    page's chunked form, agrees with the recurrence under allclose(atol=1e-5)."""
+    ex = inputs.worked_example()
+    g = to(ex, DEV)
+    o, S, _ = _gpu_prefill(g, GLA, False)
+    o_ref, S_ref = oracle.recurrence(GLA, f64(ex["q"]), f64(ex["k"]), f64(ex["v"]), f64(ex["alpha"]))
+    assert relerr(o, o_ref) <= TOL_F32 and relerr(S, S_ref) <= TOL_F32
+    o_c, S_c = chunked(GLA, f64(ex["q"]), f64(ex["k"]), f64(ex["v"]), f64(ex["alpha"]), C=ex["chunk"])
+    assert np.allclose(f64(o), o_c, atol=1e-5) and np.allclose(f64(S), S_c, atol=1e-5)
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 200, 300])
+def test_gla_bf16_small(T):
+    ex = inputs.gla_prefill(2, 3, T, 128, seed=T, s0_std=0.05)
+    g = to(ex, DEV)
+    o, S, _ = _gpu_prefill(g, GLA, False, S0=g["S0"])
+    o_ref, S_ref, _ = _oracle_prefill(ex, GLA, False, S0=f64(ex["S0"]))
+    assert relerr(o, o_ref) <= TOL_O_BF16
+    assert relerr(S, S_ref) <= TOL_S_BF16
+
+
+@pytest.mark.parametrize("T", [2, 64, 130, 257])
+def test_gdn_bf16_conv_small(T):
+    ex = inputs.gdn_prefill(2, 2, T, 128, seed=T)
+    g = to(ex, DEV)
+    o, S, c = _gpu_prefill(g, GDN, True, S0=g["S0"])
+    o_ref, S_ref, c_ref = _oracle_prefill(ex, GDN, True, S0=f64(ex["S0"]))
+    assert relerr(o, o_ref) <= TOL_O_BF16
+    assert relerr(S, S_ref) <= TOL_S_BF16
+    assert np.array_equal(f64(c), c_ref)
+
+
+@pytest.mark.parametrize("d", [16, 32, 64])
+def test_other_head_sizes(d):
+    ex = inputs.gdn_prefill(1, 2, 77, d, seed=d)
+    g = to(ex, DEV)
+    o, S, c = _gpu_prefill(g, GDN, True, S0=g["S0"])
+    o_ref, S_ref, c_ref = _oracle_prefill(ex, GDN, True, S0=f64(ex["S0"]))
+    assert relerr(o, o_ref) <= TOL_O_BF16 and relerr(S, S_ref) <= TOL_S_BF16
+    assert np.array_equal(f64(c), c_ref)
+
+
+@pytest.mark.parametrize("variant", [GLA, GDN])
+def test_segmented_equals_one_shot(variant):
+    """Three ragged segments carrying S and the conv cache equal one call."""
+    T = 333
+    ex = (inputs.gdn_prefill if variant == GDN else inputs.gla_prefill)(1, 2, T, 128, seed=21)
+    g = to(ex, DEV)
+    conv = variant == GDN
+    o_all, S_all, c_all = _gpu_prefill(g, variant, conv, S0=g.get("S0"))
+    S, c, outs = g.get("S0"), None, []
+    for s, e in ((0, 70), (70, 72), (72, T)):
+        seg = {k: (v[:, s:e].contiguous() if k in ("q", "k", "v", "alpha", "beta") and v is not None
+                   else v) for k, v in g.items()}
+        o, S, c = _gpu_prefill(seg, variant, conv, S0=S, conv_in=c)
+        outs.append(o)
+    o_seg = torch.cat(outs, dim=1)
+    o_ref, S_ref, c_ref = _oracle_prefill(ex, variant, conv, S0=f64(ex.get("S0")))
+    assert relerr(o_seg, o_ref) <= TOL_O_BF16 and relerr(S, S_ref) <= TOL_S_BF16
+    assert relerr(o_seg, f64(o_all)) <= TOL_O_BF16 and relerr(S, f64(S_all)) <= TOL_S_BF16
+    if conv:
+        assert torch.equal(c, c_all)
+        assert np.array_equal(f64(c), c_ref)
+
+
+def test_zero_length_segment_hands_state_on():
+    ex = inputs.gdn_prefill(2, 2, 0, 128, seed=3)
+    g = to(ex, DEV)
+    cin = torch.randn(2, 3, 2 * 3 * 128, device=DEV).to(torch.bfloat16)
+    o, S, c = _gpu_prefill(g, GDN, True, S0=g["S0"], conv_in=cin)
+    assert o.numel() == 0
+    assert torch.equal(S, g["S0"]) and torch.equal(c, cin)
+
+
+def test_bf16_output():
+    ex = inputs.gla_prefill(1, 2, 150, 128, seed=5)
+    g = to(ex, DEV)
+    o, _, _ = _gpu_prefill(g, GLA, False, out_dtype=torch.bfloat16)
+    o_ref, _, _ = _oracle_prefill(ex, GLA, False)
+    err = np.abs(f64(o) - o_ref)
+    assert (err <= np.abs(o_ref) * 2.0 ** -8 + TOL_O_BF16 * np.abs(o_ref).max()).all()
+
+
+def _sampled_full(ex, variant, conv, heads):
+    """Run the full workload on the GPU; check the listed (b, h) units in full
+    against the oracle."""
+    g = to(ex, DEV)
+    o, S, c = _gpu_prefill(g, variant, conv, S0=g.get("S0"), out_dtype=torch.float32)
+    for b, h in heads:
+        sub = {k: (v[b:b + 1, :, h:h + 1] if k in ("q", "k", "v", "alpha", "beta") and v is not None
+                   else v) for k, v in ex.items()}
+        S0 = None if ex.get("S0") is None else f64(ex["S0"][b:b + 1, h:h + 1])
+        if conv:  # the conv weights of head h only
+            H, d = ex["q"].shape[2], ex["q"].shape[3]
+            w = ex["conv_w"].view(3, H, d, 4)[:, h].reshape(3 * d, 4)
+            sub["conv_w"] = w
+        o_ref, S_ref, _ = _oracle_prefill(sub, variant, conv, S0=S0)
+        assert relerr(o[b:b + 1, :, h:h + 1], o_ref) <= TOL_O_BF16, (b, h)
+        assert relerr(S[b:b + 1, h:h + 1], S_ref) <= TOL_S_BF16, (b, h)
+
+
+def test_gla_prefill_full_size_sampled():
+    """B=4, H=16, T=4096, d=128, bf16; units (0,0) and (3,15) in full."""
+    ex = inputs.gla_prefill(4, 16, 4096, 128, seed=0, device=DEV)
+    _sampled_full(ex, GLA, False, [(0, 0), (3, 15)])
+
+
+def test_gdn_prefill_full_size_sampled():
+    """B=2, H=16, T=8192, d=128, conv + L2 norm, S0 ~ N(0, 0.01)."""
+    ex = inputs.gdn_prefill(2, 16, 8192, 128, seed=0, device=DEV)
+    _sampled_full(ex, GDN, True, [(0, 5), (1, 15)])
