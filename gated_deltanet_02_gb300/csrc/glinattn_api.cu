@@ -88,7 +88,7 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
     if (partial_overlap(a->conv_in, cb, a->conv_out, cb)) return GLINATTN_ERR_INVALID_ARG;
   }
 
-  if (a->in_dtype == GLINATTN_BF16 && d == 128 && T > 0 && glinattn::prefill_tc_available()) {
+  if (glinattn::prefill_tc_supports(*a) && glinattn::prefill_tc_available()) {
     return glinattn::launch_prefill_tc(*a, (cudaStream_t)stream);
   }
 

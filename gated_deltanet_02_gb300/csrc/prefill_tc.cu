@@ -1,9 +1,537 @@
-// prefill_tc.cu -- placeholder until the tensor-core kernels land.
+// prefill_tc.cu -- chunked prefill on the 5th-generation tensor cores.
+//
+// "Inference for linear attention and hybrid architectures", section "Two
+// ways to write the same computation": prefill splits the sequence into chunks
+// of C tokens; inside a chunk the work is a C x C decay-masked "attention"
+// done with matrix multiplies, and only the d_k x d_v state passes from one
+// chunk to the next.  With g the cumulative log decay inside the chunk,
+// gamma = exp(g), D_ij = exp(g_i - g_j) [j <= i] and r_j = exp(g_C - g_j):
+//
+//   O      = diag(gamma) Q S + ((Q K^T) * D) V
+//   S_next = gamma_C S + K^T diag(r) V
+//
+// (the page's chunked gated linear attention; the decay of the state update
+// is applied to V's rows here instead of K's, which is the same product).
+//
+// Kernel design (sm_103a):
+//   * one CTA per (batch, head, 64-wide slice of d_v); the state slice
+//     S[128 x 64] is fp32 and lives in the registers of the epilogue warps
+//     for the whole sequence, one d_k row per thread;
+//   * warp 0 streams Q, K (64 x 128) and V (64 x 64) chunk tiles with TMA
+//     (128-byte swizzle, 2-stage ring, out-of-range rows of a ragged last
+//     chunk are zero-filled by the copy engine);
+//   * warp 1 (one thread) issues tcgen05.mma: QK^T, K^T V~, P V and Q S into
+//     double-buffered TMEM accumulators (4 x 64 columns per chunk);
+//   * warps 2-5 form P = (QK^T)*D, V~ = diag(r) V and the next state, and
+//     write the outputs.  Operands derived in fp32 (P, V~, S) are split into
+//     a bf16 high part and a bf16 remainder and multiplied twice, so the
+//     products keep ~16 bits instead of bf16's 8 (one bf16 rounding of these
+//     operands alone costs ~2e-3 relative error in o and S).
+//   Every mbarrier wait is bounded; on timeout the CTA raises
+//   GLINATTN_DEV_WAIT_TIMEOUT and all roles leave their loops.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "common.cuh"
 #include "prefill_tc.cuh"
+#include "sm100.cuh"
 
 namespace glinattn {
-bool prefill_tc_available() { return false; }
-glinattn_status launch_prefill_tc(const glinattn_prefill_args &, cudaStream_t) {
-  return GLINATTN_ERR_UNSUPPORTED;
+namespace {
+
+using namespace sm100;
+
+constexpr int kC = 64;    // chunk length
+constexpr int kDK = 128;  // key / value head size
+constexpr int kBV = 64;   // d_v columns per CTA
+constexpr int kStages = 2;
+constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kEpiThreads = 128;
+
+// ---- shared memory map (offsets from a 1024-byte aligned base) -------------
+constexpr uint32_t kTileQ = kC * kDK * 2;  // 16 KiB: two 64-column swizzled blocks
+constexpr uint32_t kTileK = kC * kDK * 2;  // 16 KiB
+constexpr uint32_t kTileV = kC * kBV * 2;  // 8 KiB
+constexpr uint32_t kStageBytes = kTileQ + kTileK + kTileV;
+constexpr uint32_t kTileP = kC * kC * 2;   // 8 KiB, one of hi / lo
+constexpr uint32_t kTileS = kDK * kBV * 2; // 16 KiB, one of hi / lo
+constexpr uint32_t kOffStage = 0;
+constexpr uint32_t kOffP = kOffStage + kStages * kStageBytes;  // P[buf][hi, lo]
+constexpr uint32_t kOffVt = kOffP + 4 * kTileP;                // V~[buf][hi, lo]
+constexpr uint32_t kOffS = kOffVt + 4 * kTileV;                // S[buf][hi, lo]
+constexpr uint32_t kOffBar = kOffS + 4 * kTileS;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+// TMEM columns per accumulator buffer (two buffers of 256 columns).
+constexpr uint32_t kTmCols = 512;
+constexpr uint32_t kColQK = 0, kColO1 = 64, kColO2 = 128, kColDS = 192;
+
+struct GlaParams {
+  int B, T, H, nchunks, out_bf16;
+  const float *alpha;
+  const float *S0;
+  float *S_T;
+  void *o;
+  uint32_t *dev_status;
+};
+
+struct Bars {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t qk_ready[2], ds_ready[2], o_ready[2], p_ready[2], s_ready[2], tmem_free[2];
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      return false;
+    }
+  }
 }
+
+// Warp-uniform version for warps that go on to warp-collective tcgen05.ld.
+__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort) {
+  const bool ok = wait_bar(bar, parity, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk16) {
+  return row * 128u + ((chunk16 ^ (row & 7u)) << 4);
+}
+
+// 8 fp32 -> bf16 high parts and bf16 remainders, packed as 16 bytes each.
+__device__ __forceinline__ uint32_t bits(__nv_bfloat162 v) {
+  uint32_t u;
+  memcpy(&u, &v, 4);
+  return u;
+}
+
+__device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * k], x[2 * k + 1]);
+    const float2 hf = __bfloat1622float2(hb);
+    h[k] = bits(hb);
+    l[k] = bits(__floats2bfloat162_rn(x[2 * k] - hf.x, x[2 * k + 1] - hf.y));
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float *x) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    __nv_bfloat162 b;
+    memcpy(&b, &w[k], 4);
+    const float2 f = __bfloat1622float2(b);
+    x[2 * k] = f.x;
+    x[2 * k + 1] = f.y;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gla_prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv, const GlaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  Bars *bars = reinterpret_cast<Bars *>(smem + kOffBar);
+  volatile int *abort = &bars->abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int vblk = blockIdx.x & 1;
+  const int bh = blockIdx.x >> 1;
+  const int b = bh / p.H, h = bh - b * p.H;
+  const int T = p.T, nchunks = p.nchunks;
+
+  // ---- the unit is skipped when a gate is outside (0, 1] ---------------------
+  {
+    int bad = 0;
+    for (int t = tid; t < T; t += kThreads) {
+      const float a = p.alpha[((size_t)b * T + t) * p.H + h];
+      bad |= !(a > 0.f && a <= 1.f);
+    }
+    if (__syncthreads_or(bad)) {
+      if (tid == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_BAD_GATE);
+      return;
+    }
+  }
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->qk_ready[i], 1);
+      mbar_init(&bars->ds_ready[i], 1);
+      mbar_init(&bars->o_ready[i], 1);
+      mbar_init(&bars->p_ready[i], kEpiThreads);
+      mbar_init(&bars->s_ready[i], kEpiThreads);
+      mbar_init(&bars->tmem_free[i], kEpiThreads);
+    }
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      prefetch_tensormap(&tq);
+      prefetch_tensormap(&tk);
+      prefetch_tensormap(&tv);
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % kStages;
+        const uint32_t use = (uint32_t)(c / kStages);
+        if (!wait_bar(&bars->empty[s], (use & 1u) ^ 1u, abort)) break;
+        uint8_t *st = smem + kOffStage + s * kStageBytes;
+        mbar_arrive_expect_tx(&bars->full[s], kStageBytes);
+        const int t0 = c * kC;
+        tma_load_4d(st, &tq, &bars->full[s], 0, h, t0, b);
+        tma_load_4d(st + kTileQ / 2, &tq, &bars->full[s], 64, h, t0, b);
+        tma_load_4d(st + kTileQ, &tk, &bars->full[s], 0, h, t0, b);
+        tma_load_4d(st + kTileQ + kTileK / 2, &tk, &bars->full[s], 64, h, t0, b);
+        tma_load_4d(st + kTileQ + kTileK, &tv, &bars->full[s], vblk * kBV, h, t0, b);
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);   // Q K^T
+      constexpr uint32_t id_qs = idesc_bf16(64, kBV, false, true);   // Q S
+      constexpr uint32_t id_pv = idesc_bf16(64, kBV, false, true);   // P V
+      constexpr uint32_t id_ds = idesc_bf16(128, kBV, true, true);   // K^T V~
+      const uint32_t sbase = smem_u32(smem);
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % kStages;
+        const uint32_t sph = (uint32_t)(c / kStages) & 1u;
+        const int tb = c & 1;
+        const uint32_t ph = (uint32_t)(c >> 1) & 1u;
+        if (!wait_bar(&bars->full[s], sph, abort)) break;
+        if (!wait_bar(&bars->tmem_free[tb], ph ^ 1u, abort)) break;
+        tc_fence_after();
+        const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
+        const uint32_t aK = aQ + kTileQ;
+        const uint32_t aV = aK + kTileK;
+        const uint32_t dcol = tmem + tb * 256;
+        // Q K^T: M = 64 tokens, N = 64 tokens, K = d_k (2 swizzle blocks x 4 steps)
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = (ks >> 2) * (kTileQ / 2) + (ks & 3) * 32;
+          umma_bf16(dcol + kColQK, desc_sw128(aQ + off, 16, 1024), desc_sw128(aK + off, 16, 1024),
+                    id_qk, ks > 0);
+        }
+        umma_commit(&bars->qk_ready[tb]);
+        if (!wait_bar(&bars->p_ready[tb], ph, abort)) break;
+        tc_fence_after();
+        const uint32_t aP = sbase + kOffP + tb * 2 * kTileP;
+        const uint32_t aVt = sbase + kOffVt + tb * 2 * kTileV;
+        // dS = K^T (V~hi + V~lo): M = d_k (K tile read M-major), N = 64, K = 64 tokens
+        for (int part = 0; part < 2; ++part)
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(dcol + kColDS, desc_sw128(aK + ks * 2048, kTileK / 2, 1024),
+                      desc_sw128(aVt + part * kTileV + ks * 2048, 16, 1024), id_ds,
+                      (part | ks) != 0);
+        umma_commit(&bars->ds_ready[tb]);
+        // O2 = (Phi + Plo) V: M = 64, N = 64, K = 64 tokens
+        for (int part = 0; part < 2; ++part)
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(dcol + kColO2, desc_sw128(aP + part * kTileP + ks * 32, 16, 1024),
+                      desc_sw128(aV + ks * 2048, 16, 1024), id_pv, (part | ks) != 0);
+        const int sb = c & 1;
+        if (!wait_bar(&bars->s_ready[sb], (uint32_t)(c >> 1) & 1u, abort)) break;
+        tc_fence_after();
+        const uint32_t aS = sbase + kOffS + sb * 2 * kTileS;
+        // O1 = Q (Shi + Slo): M = 64, N = 64, K = d_k (S tile rows = d_k, MN-major)
+        for (int part = 0; part < 2; ++part)
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t qoff = (ks >> 2) * (kTileQ / 2) + (ks & 3) * 32;
+            umma_bf16(dcol + kColO1, desc_sw128(aQ + qoff, 16, 1024),
+                      desc_sw128(aS + part * kTileS + ks * 2048, 16, 1024), id_qs, (part | ks) != 0);
+          }
+        umma_commit(&bars->o_ready[tb]);
+        umma_commit(&bars->empty[s]);
+      }
+    }
+  } else {
+    // ======================= epilogue warpgroup =======================
+    const int q4 = warp & 3;               // TMEM lane quarter of this warp
+    const int e = tid - 64;                // 0..127
+    const int srow = 32 * q4 + lane;       // d_k row of the state held by this thread
+    const bool has_tok = lane < 16;        // holds a token row of the M = 64 tiles
+    const int tok = 16 * q4 + lane;        // that token row
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+
+    // the state slice S[srow, vblk*64 .. +64) in fp32 registers
+    float S[kBV];
+    {
+      const float *src = p.S0 ? p.S0 + (((size_t)b * p.H + h) * kDK + srow) * kDK + vblk * kBV : nullptr;
+#pragma unroll
+      for (int j = 0; j < kBV; j += 4) {
+        const float4 v4 = src ? *reinterpret_cast<const float4 *>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
+      }
+    }
+    auto write_state = [&](int sb) {
+      uint8_t *hi = smem + kOffS + sb * 2 * kTileS;
+      uint8_t *lo = hi + kTileS;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        uint4 uh, ul;
+        split8(&S[8 * ch], uh, ul);
+        *reinterpret_cast<uint4 *>(hi + swz(srow, ch)) = uh;
+        *reinterpret_cast<uint4 *>(lo + swz(srow, ch)) = ul;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->s_ready[sb]);
+    };
+    write_state(0);
+
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int s = c % kStages;
+      const uint32_t sph = (uint32_t)(c / kStages) & 1u;
+      const int tb = c & 1;
+      const uint32_t ph = (uint32_t)(c >> 1) & 1u;
+      const int t0 = c * kC;
+      const uint32_t dcol = tmem + tb * 256 + lane_base;
+
+      // ---- gates: g = cumsum(log alpha) inside the chunk (lane holds 2 tokens)
+      float g0, g1;
+      {
+        const int ta = t0 + 2 * lane, tb2 = ta + 1;
+        const float a0 = ta < T ? p.alpha[((size_t)b * T + ta) * p.H + h] : 1.f;
+        const float a1 = tb2 < T ? p.alpha[((size_t)b * T + tb2) * p.H + h] : 1.f;
+        const float l0 = logf(a0), l1 = logf(a1);
+        float incl = l0 + l1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) excl = 0.f;
+        g0 = excl + l0;
+        g1 = g0 + l1;
+      }
+      auto g_at = [&](int j) {  // warp-uniform j
+        const float x0 = __shfl_sync(0xffffffffu, g0, j >> 1);
+        const float x1 = __shfl_sync(0xffffffffu, g1, j >> 1);
+        return (j & 1) ? x1 : x0;
+      };
+      const float gC = __shfl_sync(0xffffffffu, g1, 31);
+      const float gt_even = __shfl_sync(0xffffffffu, g0, (tok >> 1) & 31);
+      const float gt_odd = __shfl_sync(0xffffffffu, g1, (tok >> 1) & 31);
+      const float g_tok = (tok & 1) ? gt_odd : gt_even;  // garbage for lanes >= 16, never stored
+
+      // ---- P = (Q K^T) * D, split into hi / lo --------------------------------
+      if (!wait_bar_warp(&bars->qk_ready[tb], ph, abort)) { ok = false; break; }
+      tc_fence_after();
+      {
+        uint8_t *phi = smem + kOffP + tb * 2 * kTileP;
+        uint8_t *plo = phi + kTileP;
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+          float qk[16];
+          tmem_ld16(dcol + kColQK + 16 * blk, qk);
+          float pv[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = 16 * blk + jj;
+            const float gj = g_at(j);
+            pv[jj] = (j <= tok) ? qk[jj] * expf(g_tok - gj) : 0.f;
+          }
+          if (has_tok) {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              uint4 uh, ul;
+              split8(&pv[8 * half], uh, ul);
+              const uint32_t ch = 2 * blk + half;
+              *reinterpret_cast<uint4 *>(phi + swz(tok, ch)) = uh;
+              *reinterpret_cast<uint4 *>(plo + swz(tok, ch)) = ul;
+            }
+          }
+        }
+      }
+      // ---- V~ = diag(exp(gC - g)) V, split into hi / lo ------------------------
+      if (!wait_bar_warp(&bars->full[s], sph, abort)) { ok = false; break; }
+      {
+        const uint8_t *vt = smem + kOffStage + s * kStageBytes + kTileQ + kTileK;
+        uint8_t *vhi = smem + kOffVt + tb * 2 * kTileV;
+        uint8_t *vlo = vhi + kTileV;
+        const int t = e >> 1, half = e & 1;
+        // token t's decay: lanes hold g for tokens 2*lane, 2*lane+1
+        const float gt0 = __shfl_sync(0xffffffffu, g0, (t >> 1) & 31);
+        const float gt1 = __shfl_sync(0xffffffffu, g1, (t >> 1) & 31);
+        const float r = expf(gC - ((t & 1) ? gt1 : gt0));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t ch = 4 * half + k;
+          float x[8];
+          unpack8(*reinterpret_cast<const uint4 *>(vt + swz(t, ch)), x);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] *= r;
+          uint4 uh, ul;
+          split8(x, uh, ul);
+          *reinterpret_cast<uint4 *>(vhi + swz(t, ch)) = uh;
+          *reinterpret_cast<uint4 *>(vlo + swz(t, ch)) = ul;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->p_ready[tb]);
+
+      // ---- S <- gamma_C S + K^T V~ --------------------------------------------
+      if (!wait_bar_warp(&bars->ds_ready[tb], ph, abort)) { ok = false; break; }
+      tc_fence_after();
+      {
+        const float gam = expf(gC);
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+          float ds[16];
+          tmem_ld16(dcol + kColDS + 16 * blk, ds);
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) S[16 * blk + jj] = gam * S[16 * blk + jj] + ds[jj];
+        }
+      }
+      if (c + 1 < nchunks) write_state((c + 1) & 1);
+
+      // ---- o = gamma_i (Q S) + P V ----------------------------------------------
+      if (!wait_bar_warp(&bars->o_ready[tb], ph, abort)) { ok = false; break; }
+      tc_fence_after();
+      {
+        const float gi = expf(g_tok);
+        const int t = t0 + tok;
+        const bool store = has_tok && t < T;
+        const size_t obase = (((size_t)b * T + t) * p.H + h) * kDK + vblk * kBV;
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+          float o1[16], o2[16];
+          tmem_ld16(dcol + kColO1 + 16 * blk, o1);
+          tmem_ld16(dcol + kColO2 + 16 * blk, o2);
+          float ov[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) ov[jj] = gi * o1[jj] + o2[jj];
+          if (store) {
+            if (p.out_bf16) {
+              uint32_t pk[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) pk[k] = bits(__floats2bfloat162_rn(ov[2 * k], ov[2 * k + 1]));
+              uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + obase + 16 * blk);
+              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            } else {
+              float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + obase + 16 * blk);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                dst[k] = make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->tmem_free[tb]);
+    }
+    if (ok) {
+      float *dst = p.S_T + (((size_t)b * p.H + h) * kDK + srow) * kDK + vblk * kBV;
+#pragma unroll
+      for (int j = 0; j < kBV; j += 4)
+        *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort && tid == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_WAIT_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmCols);
+  }
+}
+
+// ---- host side ----------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (EncodeTiledFn) nullptr;
+    return (EncodeTiledFn)f;
+  }();
+  return fn;
+}
+
+// [B, T, H, d] bf16 activations as a 4-D map (d, H, T, B), box 64 x 1 x 64 x 1.
+bool make_act_map(CUtensorMap *m, const void *base, int B, int T, int H, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)T * H * d * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)kC, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool prefill_tc_available() { return encode_fn() != nullptr; }
+
+bool prefill_tc_supports(const glinattn_prefill_args &a) {
+  return a.variant == GLINATTN_GLA && a.in_dtype == GLINATTN_BF16 && a.dk == kDK && a.dv == kDK &&
+         a.conv_w == nullptr && !a.qk_l2norm && a.seqlen > 0;
+}
+
+glinattn_status launch_prefill_tc(const glinattn_prefill_args &a, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  if (!make_act_map(&tq, a.q, a.batch, a.seqlen, a.heads, kDK) ||
+      !make_act_map(&tk, a.k, a.batch, a.seqlen, a.heads, kDK) ||
+      !make_act_map(&tv, a.v, a.batch, a.seqlen, a.heads, kDK))
+    return GLINATTN_ERR_CUDA;
+  GlaParams p;
+  p.B = a.batch;
+  p.T = a.seqlen;
+  p.H = a.heads;
+  p.nchunks = (a.seqlen + kC - 1) / kC;
+  p.out_bf16 = a.out_dtype == GLINATTN_BF16;
+  p.alpha = a.alpha;
+  p.S0 = a.S0;
+  p.S_T = a.S_T;
+  p.o = a.o;
+  p.dev_status = a.dev_status;
+  if (cudaFuncSetAttribute(gla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kSmemBytes) != cudaSuccess)
+    return GLINATTN_ERR_CUDA;
+  const unsigned grid = (unsigned)a.batch * (unsigned)a.heads * (kDK / kBV);
+  gla_prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? GLINATTN_OK : GLINATTN_ERR_CUDA;
+}
+
 }  // namespace glinattn
