@@ -1,0 +1,427 @@
+"""Benchmark of the linear-attention hot path on GB300.
+
+One JSON line on rank 0.  The headline ``value`` is gated-linear-attention
+prefill throughput (tokens/s) on B=4, H=16, T=4096, d_k=d_v=128, chunk 64,
+bf16 activations, fp32 state; a step is one prefill call over the whole batch.
+Sub-objects report Gated DeltaNet decode at batch 256 (16 heads, 512-slot
+fp32 state pool, conv cache), Gated DeltaNet prefill (B=2, H=16, T=8192, conv
++ L2 norm) and the long-context run (B=1, H=32, T=32768 in three segments,
+then 64 requests x 4-token speculative decode), each with its roofline.
+
+Timing: W untimed warm-up steps, then K steps between a barrier and
+torch.cuda.synchronize() on both sides, CUDA events on the launching stream,
+max over ranks.  Every input set is larger than L2 (129 MB), so no flush is
+needed.  Multi-GPU runs are replicas: each rank runs the same per-GPU workload
+("scaling": "weak"); there is no data-path collective.
+
+``--impl reference`` times the plain fp64 CPU oracle on the host cores on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill tokens/s (%tensor peak); decode tokens/s at batch 256 (%HBM BW)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return dist, rank, ws, local
+    return None, 0, 1, 0
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float, device):
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def timed_steps(fn, steps, warmup, dist, device):
+    """Returns (ms per step over the timed region, [per-step event ms])."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for i in range(steps):
+        fn()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    total = ev[0].elapsed_time(ev[steps])
+    return max_over_ranks(dist, total / steps, device), per
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "gated_deltanet_02_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, src_files, units_scale=1.0):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    ent = d.get(kernel)
+    if not ent or ent.get("source_hash") != source_hash(*src_files):
+        return None
+    return ent["dram_bytes_per_launch"] * units_scale
+
+
+# ----------------------------------------------------------------------------
+# workloads
+# ----------------------------------------------------------------------------
+
+GLA_CFG = dict(B=4, H=16, T=4096, d=128)
+GDN_CFG = dict(B=2, H=16, T=8192, d=128)
+DEC_CFG = dict(N=256, H=16, d=128, P=512)
+
+
+def gla_bytes_flops(B, H, T, d):
+    bt = B * T * H
+    bytes_ = bt * d * 2 * 3 + bt * 4 + bt * d * 2 + B * H * d * d * 4  # q k v, alpha, o (bf16), S_T
+    flops = bt * (4 * 64 * d + 4 * d * d)  # QK^T, PV, QS, K^T V per head-token
+    return bytes_, flops
+
+
+def gdn_bytes_flops(B, H, T, d):
+    bt = B * T * H
+    bytes_ = bt * d * 2 * 3 + bt * 8 + bt * d * 2 + 2 * B * H * d * d * 4 + 3 * H * d * 16
+    flops = bt * (10 * 64 * d + 6 * d * d + 64 * 64 // 3)
+    return bytes_, flops
+
+
+def decode_state_bytes(N, H, d):
+    return N * H * d * d * 4 * 2  # read + write of every touched fp32 state
+
+
+def run_ours(args):
+    import torch
+
+    from gated_deltanet_02_gb300 import GDN, GLA, glinattn_decode, glinattn_prefill, inputs
+    dist, rank, ws, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk, pk_kind = peaks()
+    hbm, tc = pk["hbm_gbs"], pk["bf16_tflops"]
+
+    # ---- GLA prefill (headline) ------------------------------------------------
+    c = GLA_CFG
+    ex = inputs.gla_prefill(c["B"], c["H"], c["T"], c["d"], seed=rank, device=dev)
+    o = torch.empty(c["B"], c["T"], c["H"], c["d"], dtype=torch.bfloat16, device=dev)
+    S = torch.empty(c["B"], c["H"], c["d"], c["d"], dtype=torch.float32, device=dev)
+
+    def step_gla():
+        glinattn_prefill(ex["q"], ex["k"], ex["v"], ex["alpha"], None, None, variant=GLA, o=o, S_T=S)
+
+    with ClockSampler(local) as clk:
+        ms, per = timed_steps(step_gla, args.steps, args.warmup, dist, dev)
+    tokens = c["B"] * c["T"]
+    gbytes, gflops = gla_bytes_flops(**c)
+    kern_ms = statistics.mean(per)
+    value = tokens * ws / (ms / 1e3)
+
+    # ---- end to end through the C ABI with host buffers -------------------------
+    host = {k: ex[k].cpu().pin_memory() for k in ("q", "k", "v", "alpha")}
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    S_h = torch.empty(S.shape, dtype=S.dtype).pin_memory()
+    dbuf = {k: torch.empty_like(ex[k]) for k in host}
+
+    def step_e2e():
+        for k in host:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        glinattn_prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["alpha"], None, None, variant=GLA,
+                         o=o, S_T=S)
+        o_h.copy_(o, non_blocking=True)
+        S_h.copy_(S, non_blocking=True)
+
+    e2e_ms, _ = timed_steps(step_e2e, max(2, args.steps // 2), 2, dist, dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_h.numel() * o_h.element_size() + S_h.numel() * S_h.element_size()
+
+    # ---- Gated DeltaNet decode, batch 256 -----------------------------------------
+    dc = DEC_CFG
+    dx = inputs.gdn_decode(dc["N"], dc["H"], dc["d"], dc["P"], seed=rank, device=dev)
+    od = torch.empty(dc["N"], dc["H"], dc["d"], dtype=torch.bfloat16, device=dev)
+
+    def step_dec():
+        glinattn_decode(dx["q"], dx["k"], dx["v"], dx["alpha"], dx["beta"], dx["pool"], dx["slot_ids"],
+                        variant=GDN, conv_w=dx["conv_w"], conv_pool=dx["conv_pool"], qk_l2norm=True, o=od)
+
+    dec_ms, dec_per = timed_steps(step_dec, max(args.steps, 20), max(args.warmup, 3), dist, dev)
+    dsb = decode_state_bytes(dc["N"], dc["H"], dc["d"])
+    dec_kms = statistics.mean(dec_per)
+
+    # ---- Gated DeltaNet prefill -------------------------------------------------------
+    g = GDN_CFG
+    gx = inputs.gdn_prefill(g["B"], g["H"], g["T"], g["d"], seed=rank, device=dev)
+    og = torch.empty(g["B"], g["T"], g["H"], g["d"], dtype=torch.bfloat16, device=dev)
+    Sg = torch.empty(g["B"], g["H"], g["d"], g["d"], dtype=torch.float32, device=dev)
+
+    def step_gdn():
+        glinattn_prefill(gx["q"], gx["k"], gx["v"], gx["alpha"], gx["beta"], gx["S0"], variant=GDN,
+                         conv_w=gx["conv_w"], qk_l2norm=True, o=og, S_T=Sg)
+
+    gdn_ms, gdn_per = timed_steps(step_gdn, max(2, min(args.steps, 5)), 1, dist, dev)
+    gdn_bytes, gdn_flops = gdn_bytes_flops(**g)
+
+    # ---- CPU baseline: the oracle on this host's cores (rank 0) -----------------------
+    cpu = cpu_baseline_run(ex, budget_s=args.cpu_seconds) if rank == 0 and not args.no_cpu else None
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    traffic = profiled_traffic("gla_prefill_kernel", ["prefill_tc.cu", "sm100.cuh"])
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; q,k ~ N(0,1)/sqrt(d), v ~ N(0,1), alpha = sigmoid(N(0,1)+3))",
+        "config": {"workload": "gated linear attention prefill, B=4 H=16 T=4096 d_k=d_v=128 C=64, "
+                               "bf16 q/k/v/o, fp32 alpha and state, S0 = 0",
+                   "global_batch": c["B"] * ws, "seq_len": c["T"], "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2 (no flush needed)"},
+        "roofline": {"bound": "hbm", "achieved": gbytes / (kern_ms / 1e3) / 1e9, "peak": hbm,
+                     "unit": "GB/s", "frac": gbytes / (kern_ms / 1e3) / 1e9 / hbm,
+                     "traffic": traffic, "peak_kind": f"{pk_kind} burst copy",
+                     "algorithmic_bytes": gbytes, "kernel": "gla_prefill_kernel"},
+        "tensor": {"flops": gflops, "achieved_tflops": gflops / (kern_ms / 1e3) / 1e12,
+                   "peak_tflops": tc, "frac": gflops / (kern_ms / 1e3) / 1e12 / tc,
+                   "peak_kind": f"{pk_kind} bf16 burst"},
+        "e2e": {"value": tokens * ws / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "decode": {"value": dc["N"] * ws / (dec_ms / 1e3), "unit": "tokens/s",
+                   "config": "Gated DeltaNet decode, 256 requests x 16 heads, d=128, 512-slot fp32 pool, "
+                             "conv cache + L2 norm, in place",
+                   "ms_per_step": dec_ms,
+                   "roofline": {"bound": "hbm", "achieved": dsb / (dec_kms / 1e3) / 1e9, "peak": hbm,
+                                "unit": "GB/s", "frac": dsb / (dec_kms / 1e3) / 1e9 / hbm,
+                                "traffic": profiled_traffic("recurrent_kernel", ["recurrent.cu", "sm100.cuh"]),
+                                "algorithmic_bytes": dsb, "kernel": "recurrent_kernel<128>"}},
+        "gdn_prefill": {"value": g["B"] * g["T"] * ws / (gdn_ms / 1e3), "unit": "tokens/s",
+                        "config": "Gated DeltaNet prefill, B=2 H=16 T=8192 d=128, conv + L2 norm",
+                        "ms_per_step": gdn_ms,
+                        "roofline": {"bound": "hbm",
+                                     "achieved": gdn_bytes / (statistics.mean(gdn_per) / 1e3) / 1e9,
+                                     "peak": hbm, "unit": "GB/s",
+                                     "frac": gdn_bytes / (statistics.mean(gdn_per) / 1e3) / 1e9 / hbm},
+                        "tensor_frac": gdn_flops / (statistics.mean(gdn_per) / 1e3) / 1e12 / tc},
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# the oracle on the host cores
+# ----------------------------------------------------------------------------
+
+def cpu_baseline_run(ex, budget_s=10.0):
+    """Times the fp64 oracle recurrence on a bounded sample of the GLA prefill
+    workload: whole sequences (T = 4096) of as many (batch, head) units as fit
+    the time budget, on all host cores.  Throughput is layer tokens/s: the
+    head-tokens processed divided by the H heads of a token."""
+    import oracle
+    cores = os.cpu_count() or 1
+    q, k, v, a = (ex[n] for n in ("q", "k", "v", "alpha"))
+    B, T, H, d = q.shape
+
+    def run(nu):
+        bs, hs = (nu // H, H) if nu >= H else (1, nu)
+        qs, ks, vs = (x[:bs, :, :hs].double().cpu().numpy() for x in (q, k, v))
+        al = a[:bs, :, :hs].double().cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.recurrence(oracle.GLA, qs, ks, vs, al, nthreads=cores)
+        return time.perf_counter() - t0, bs * hs
+
+    dt, nu = run(1)
+    target = int(budget_s * cores / max(dt / nu, 1e-9))
+    target = max(1, min(B * H, target))
+    dt, nu = run(target)
+    return {"value": nu * T / H / dt, "unit": "tokens/s", "cores": min(cores, nu), "kind": "oracle",
+            "sample": f"fp64 recurrence over {nu} of {B * H} (batch, head) units, full T={T}, "
+                      f"of the GLA prefill workload ({dt:.1f} s)"}
+
+
+def run_reference(args):
+    """The oracle arm: rank 0 times the fp64 CPU oracle; other ranks exit."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+
+    from gated_deltanet_02_gb300 import inputs
+    import oracle
+    cores = os.cpu_count() or 1
+    c = GLA_CFG
+    ex = inputs.gla_prefill(c["B"], c["H"], c["T"], c["d"], seed=0, device="cpu")
+    # per step: a bounded sample of (batch, head) units of the workload
+    nu = max(1, min(c["B"] * c["H"], cores))
+    hs = min(nu, c["H"])
+    bs = max(1, nu // c["H"])
+    qs, ks, vs = (ex[n][:bs, :, :hs].double().numpy() for n in ("q", "k", "v"))
+    al = ex["alpha"][:bs, :, :hs].double().numpy()
+    for _ in range(args.warmup):
+        oracle.recurrence(oracle.GLA, qs[:, :256], ks[:, :256], vs[:, :256], al[:, :256], nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.recurrence(oracle.GLA, qs, ks, vs, al, nthreads=cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    # tokens/s of the whole layer: head-tokens processed / heads per token
+    value = bs * hs * c["T"] / c["H"] / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "gated linear attention prefill, B=4 H=16 T=4096 d_k=d_v=128 C=64"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": min(cores, bs * hs),
+                             "kind": "oracle",
+                             "sample": f"{bs * hs} of {c['B'] * c['H']} (batch, head) units per step, "
+                                       f"full T={c['T']}, fp64 recurrence"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

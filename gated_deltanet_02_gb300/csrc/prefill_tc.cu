@@ -47,8 +47,8 @@ constexpr int kC = 64;    // chunk length
 constexpr int kDK = 128;  // key / value head size
 constexpr int kBV = 64;   // d_v columns per CTA
 constexpr int kStages = 2;
-constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kEpiThreads = 128;
+constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-5 and 6-9 epilogue
+constexpr int kEpiThreads = 128;  // threads per epilogue warpgroup
 
 // ---- shared memory map (offsets from a 1024-byte aligned base) -------------
 constexpr uint32_t kTileQ = kC * kDK * 2;  // 16 KiB: two 64-column swizzled blocks
@@ -61,7 +61,8 @@ constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffP = kOffStage + kStages * kStageBytes;  // P[buf][hi, lo]
 constexpr uint32_t kOffVt = kOffP + 4 * kTileP;                // V~[buf][hi, lo]
 constexpr uint32_t kOffS = kOffVt + 4 * kTileV;                // S[buf][hi, lo]
-constexpr uint32_t kOffBar = kOffS + 4 * kTileS;
+constexpr uint32_t kOffG = kOffS + 4 * kTileS;                 // gate rows [warp][64]
+constexpr uint32_t kOffBar = kOffG + (kThreads / 32) * kC * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
@@ -80,7 +81,8 @@ struct GlaParams {
 
 struct Bars {
   uint64_t full[kStages], empty[kStages];
-  uint64_t qk_ready[2], ds_ready[2], o_ready[2], p_ready[2], s_ready[2], tmem_free[2];
+  uint64_t qk_ready[2], qk_free[2], p_ready[2], p_free[2];
+  uint64_t ds_ready[2], o_ready[2], o_free[2], s_ready[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -142,12 +144,48 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float *x) {
   }
 }
 
+// Per-chunk gates of one warp: g2 = cumsum(log2 alpha) over the chunk's 64
+// tokens (2 per lane, alpha = 1 past the end of the sequence), published in
+// the warp's shared row so any lane can read any g2_j by broadcast.
+struct Gates {
+  float a0n, a1n;  // next chunk's alphas, prefetched one chunk ahead
+};
+
+__device__ __forceinline__ void gates_prefetch(Gates &G, const GlaParams &p, int b, int h, int c,
+                                               int lane) {
+  const int ta = c * kC + 2 * lane, tb2 = ta + 1;
+  G.a0n = ta < p.T ? p.alpha[((size_t)b * p.T + ta) * p.H + h] : 1.f;
+  G.a1n = tb2 < p.T ? p.alpha[((size_t)b * p.T + tb2) * p.H + h] : 1.f;
+}
+
+// Consumes the prefetched alphas of chunk c, writes g2[0..63] to `row`,
+// prefetches chunk c+1.  Returns g2 of the chunk's last token.
+__device__ __forceinline__ float gates_chunk(Gates &G, const GlaParams &p, int b, int h, int c,
+                                             int lane, float *row) {
+  const float l0 = log2f(G.a0n), l1 = log2f(G.a1n);
+  gates_prefetch(G, p, b, h, c + 1, lane);
+  float incl = l0 + l1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) excl = 0.f;
+  __syncwarp();
+  row[2 * lane] = excl + l0;
+  row[2 * lane + 1] = excl + l0 + l1;
+  __syncwarp();
+  return row[kC - 1];
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gla_prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, const GlaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Bars *bars = reinterpret_cast<Bars *>(smem + kOffBar);
+  float *s_g = reinterpret_cast<float *>(smem + kOffG);  // [warp][64] per-warp gate rows
   volatile int *abort = &bars->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -178,9 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->qk_ready[i], 1);
       mbar_init(&bars->ds_ready[i], 1);
       mbar_init(&bars->o_ready[i], 1);
+      mbar_init(&bars->p_free[i], 1);
+      mbar_init(&bars->qk_free[i], kEpiThreads);
       mbar_init(&bars->p_ready[i], kEpiThreads);
+      mbar_init(&bars->o_free[i], kEpiThreads);
       mbar_init(&bars->s_ready[i], kEpiThreads);
-      mbar_init(&bars->tmem_free[i], kEpiThreads);
     }
     bars->abort = 0;
     fence_mbar_init();
@@ -222,64 +262,157 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_pv = idesc_bf16(64, kBV, false, true);   // P V
       constexpr uint32_t id_ds = idesc_bf16(128, kBV, true, true);   // K^T V~
       const uint32_t sbase = smem_u32(smem);
-      for (int c = 0; c < nchunks; ++c) {
+      // Q K^T of chunk c: M = 64 tokens, N = 64 tokens, K = d_k (2 swizzle blocks x 4 steps)
+      auto issue_qk = [&](int c) -> bool {
+        const int s = c % kStages, tb = c & 1;
+        if (!wait_bar(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) return false;
+        if (!wait_bar(&bars->qk_free[tb], ((uint32_t)(c >> 1) & 1u) ^ 1u, abort)) return false;
+        tc_fence_after();
+        const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
+        const uint64_t dQ = desc_sw128(aQ, 16, 1024), dK = desc_sw128(aQ + kTileQ, 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = ((ks >> 2) * (kTileQ / 2) + (ks & 3) * 32) >> 4;
+          umma_bf16(tmem + tb * 256 + kColQK, dQ + off, dK + off, id_qk, ks > 0);
+        }
+        umma_commit(&bars->qk_ready[tb]);
+        return true;
+      };
+      bool ok = issue_qk(0);
+      for (int c = 0; c < nchunks && ok; ++c) {
         const int s = c % kStages;
-        const uint32_t sph = (uint32_t)(c / kStages) & 1u;
         const int tb = c & 1;
         const uint32_t ph = (uint32_t)(c >> 1) & 1u;
-        if (!wait_bar(&bars->full[s], sph, abort)) break;
-        if (!wait_bar(&bars->tmem_free[tb], ph ^ 1u, abort)) break;
+        if (c + 1 < nchunks && !issue_qk(c + 1)) break;
+        if (!wait_bar(&bars->p_ready[tb], ph, abort)) break;
+        if (!wait_bar(&bars->o_free[tb], ph ^ 1u, abort)) break;
         tc_fence_after();
         const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
         const uint32_t aK = aQ + kTileQ;
         const uint32_t aV = aK + kTileK;
         const uint32_t dcol = tmem + tb * 256;
-        // Q K^T: M = 64 tokens, N = 64 tokens, K = d_k (2 swizzle blocks x 4 steps)
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = (ks >> 2) * (kTileQ / 2) + (ks & 3) * 32;
-          umma_bf16(dcol + kColQK, desc_sw128(aQ + off, 16, 1024), desc_sw128(aK + off, 16, 1024),
-                    id_qk, ks > 0);
-        }
-        umma_commit(&bars->qk_ready[tb]);
-        if (!wait_bar(&bars->p_ready[tb], ph, abort)) break;
-        tc_fence_after();
-        const uint32_t aP = sbase + kOffP + tb * 2 * kTileP;
-        const uint32_t aVt = sbase + kOffVt + tb * 2 * kTileV;
+        // descriptors built once; the k-steps only move the start-address field
+        const uint64_t dKm = desc_sw128(aK, kTileK / 2, 1024);
+        const uint64_t dVt = desc_sw128(sbase + kOffVt + tb * 2 * kTileV, 16, 1024);
+        const uint64_t dP = desc_sw128(sbase + kOffP + tb * 2 * kTileP, 16, 1024);
+        const uint64_t dV = desc_sw128(aV, 16, 1024);
+        const uint64_t dQ = desc_sw128(aQ, 16, 1024);
         // dS = K^T (V~hi + V~lo): M = d_k (K tile read M-major), N = 64, K = 64 tokens
+#pragma unroll
         for (int part = 0; part < 2; ++part)
+#pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(dcol + kColDS, desc_sw128(aK + ks * 2048, kTileK / 2, 1024),
-                      desc_sw128(aVt + part * kTileV + ks * 2048, 16, 1024), id_ds,
-                      (part | ks) != 0);
+            umma_bf16(dcol + kColDS, dKm + ((ks * 2048) >> 4),
+                      dVt + ((part * kTileV + ks * 2048) >> 4), id_ds, (part | ks) != 0);
         umma_commit(&bars->ds_ready[tb]);
         // O2 = (Phi + Plo) V: M = 64, N = 64, K = 64 tokens
+#pragma unroll
         for (int part = 0; part < 2; ++part)
+#pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(dcol + kColO2, desc_sw128(aP + part * kTileP + ks * 32, 16, 1024),
-                      desc_sw128(aV + ks * 2048, 16, 1024), id_pv, (part | ks) != 0);
+            umma_bf16(dcol + kColO2, dP + ((part * kTileP + ks * 32) >> 4), dV + ((ks * 2048) >> 4),
+                      id_pv, (part | ks) != 0);
         const int sb = c & 1;
-        if (!wait_bar(&bars->s_ready[sb], (uint32_t)(c >> 1) & 1u, abort)) break;
+        if (!wait_bar(&bars->s_ready[sb], ph, abort)) break;
         tc_fence_after();
-        const uint32_t aS = sbase + kOffS + sb * 2 * kTileS;
+        const uint64_t dS = desc_sw128(sbase + kOffS + sb * 2 * kTileS, 16, 1024);
         // O1 = Q (Shi + Slo): M = 64, N = 64, K = d_k (S tile rows = d_k, MN-major)
+#pragma unroll
         for (int part = 0; part < 2; ++part)
+#pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t qoff = (ks >> 2) * (kTileQ / 2) + (ks & 3) * 32;
-            umma_bf16(dcol + kColO1, desc_sw128(aQ + qoff, 16, 1024),
-                      desc_sw128(aS + part * kTileS + ks * 2048, 16, 1024), id_qs, (part | ks) != 0);
+            const uint32_t qoff = ((ks >> 2) * (kTileQ / 2) + (ks & 3) * 32) >> 4;
+            umma_bf16(dcol + kColO1, dQ + qoff, dS + ((part * kTileS + ks * 2048) >> 4), id_qs,
+                      (part | ks) != 0);
           }
         umma_commit(&bars->o_ready[tb]);
+        umma_commit(&bars->p_free[tb]);
         umma_commit(&bars->empty[s]);
       }
     }
-  } else {
-    // ======================= epilogue warpgroup =======================
-    const int q4 = warp & 3;               // TMEM lane quarter of this warp
-    const int e = tid - 64;                // 0..127
-    const int srow = 32 * q4 + lane;       // d_k row of the state held by this thread
-    const bool has_tok = lane < 16;        // holds a token row of the M = 64 tiles
-    const int tok = 16 * q4 + lane;        // that token row
+  } else if (warp < 6) {
+    // ============ warpgroup A: P = (Q K^T) * D and V~ = diag(r) V ============
+    const int q4 = warp & 3;
+    const int e = tid - 64;               // 0..127
+    const bool has_tok = lane < 16;       // holds a token row of the M = 64 tiles
+    const int tok = 16 * q4 + lane;       // that token row (valid when has_tok)
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    float *grow = s_g + warp * kC;
+    Gates G;
+    gates_prefetch(G, p, b, h, 0, lane);
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % kStages;
+      const uint32_t sph = (uint32_t)(c / kStages) & 1u;
+      const int tb = c & 1;
+      const uint32_t ph = (uint32_t)(c >> 1) & 1u;
+      const float gC = gates_chunk(G, p, b, h, c, lane, grow);
+
+      if (!wait_bar_warp(&bars->qk_ready[tb], ph, abort)) break;
+      tc_fence_after();
+      float qk[64];
+      {
+        float part[32];
+        tmem_ld32(tmem + tb * 256 + kColQK + lane_base, part);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) qk[j] = part[j];
+        tmem_ld32(tmem + tb * 256 + kColQK + 32 + lane_base, part);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) qk[32 + j] = part[j];
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->qk_free[tb]);
+      if (!wait_bar_warp(&bars->p_free[tb], ph ^ 1u, abort)) break;
+      if (has_tok) {
+        uint8_t *phi = smem + kOffP + tb * 2 * kTileP;
+        uint8_t *plo = phi + kTileP;
+        const float gi = grow[tok];
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          float pv[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int j = 8 * ch + jj;
+            pv[jj] = (j <= tok) ? qk[j] * exp2f(gi - grow[j]) : 0.f;
+          }
+          uint4 uh, ul;
+          split8(pv, uh, ul);
+          *reinterpret_cast<uint4 *>(phi + swz(tok, ch)) = uh;
+          *reinterpret_cast<uint4 *>(plo + swz(tok, ch)) = ul;
+        }
+      }
+      if (!wait_bar_warp(&bars->full[s], sph, abort)) break;
+      {
+        const uint8_t *vt = smem + kOffStage + s * kStageBytes + kTileQ + kTileK;
+        uint8_t *vhi = smem + kOffVt + tb * 2 * kTileV;
+        uint8_t *vlo = vhi + kTileV;
+        const int t = e >> 1, half = e & 1;
+        const float r = exp2f(gC - grow[t]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t ch = 4 * half + k;
+          float x[8];
+          unpack8(*reinterpret_cast<const uint4 *>(vt + swz(t, ch)), x);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[i] *= r;
+          uint4 uh, ul;
+          split8(x, uh, ul);
+          *reinterpret_cast<uint4 *>(vhi + swz(t, ch)) = uh;
+          *reinterpret_cast<uint4 *>(vlo + swz(t, ch)) = ul;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->p_ready[tb]);
+    }
+  } else {
+    // ============ warpgroup B: the state chain and the outputs ============
+    const int q4 = warp & 3;
+    const int srow = 32 * q4 + lane;      // d_k row of the state held by this thread
+    const bool has_tok = lane < 16;
+    const int tok = 16 * q4 + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    float *grow = s_g + warp * kC;
+    Gates G;
+    gates_prefetch(G, p, b, h, 0, lane);
 
     // the state slice S[srow, vblk*64 .. +64) in fp32 registers
     float S[kBV];
@@ -308,108 +441,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
-      const int s = c % kStages;
-      const uint32_t sph = (uint32_t)(c / kStages) & 1u;
       const int tb = c & 1;
       const uint32_t ph = (uint32_t)(c >> 1) & 1u;
       const int t0 = c * kC;
       const uint32_t dcol = tmem + tb * 256 + lane_base;
-
-      // ---- gates: g = cumsum(log alpha) inside the chunk (lane holds 2 tokens)
-      float g0, g1;
-      {
-        const int ta = t0 + 2 * lane, tb2 = ta + 1;
-        const float a0 = ta < T ? p.alpha[((size_t)b * T + ta) * p.H + h] : 1.f;
-        const float a1 = tb2 < T ? p.alpha[((size_t)b * T + tb2) * p.H + h] : 1.f;
-        const float l0 = logf(a0), l1 = logf(a1);
-        float incl = l0 + l1;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-        if (lane == 0) excl = 0.f;
-        g0 = excl + l0;
-        g1 = g0 + l1;
-      }
-      auto g_at = [&](int j) {  // warp-uniform j
-        const float x0 = __shfl_sync(0xffffffffu, g0, j >> 1);
-        const float x1 = __shfl_sync(0xffffffffu, g1, j >> 1);
-        return (j & 1) ? x1 : x0;
-      };
-      const float gC = __shfl_sync(0xffffffffu, g1, 31);
-      const float gt_even = __shfl_sync(0xffffffffu, g0, (tok >> 1) & 31);
-      const float gt_odd = __shfl_sync(0xffffffffu, g1, (tok >> 1) & 31);
-      const float g_tok = (tok & 1) ? gt_odd : gt_even;  // garbage for lanes >= 16, never stored
-
-      // ---- P = (Q K^T) * D, split into hi / lo --------------------------------
-      if (!wait_bar_warp(&bars->qk_ready[tb], ph, abort)) { ok = false; break; }
-      tc_fence_after();
-      {
-        uint8_t *phi = smem + kOffP + tb * 2 * kTileP;
-        uint8_t *plo = phi + kTileP;
-#pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-          float qk[16];
-          tmem_ld16(dcol + kColQK + 16 * blk, qk);
-          float pv[16];
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int j = 16 * blk + jj;
-            const float gj = g_at(j);
-            pv[jj] = (j <= tok) ? qk[jj] * expf(g_tok - gj) : 0.f;
-          }
-          if (has_tok) {
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              uint4 uh, ul;
-              split8(&pv[8 * half], uh, ul);
-              const uint32_t ch = 2 * blk + half;
-              *reinterpret_cast<uint4 *>(phi + swz(tok, ch)) = uh;
-              *reinterpret_cast<uint4 *>(plo + swz(tok, ch)) = ul;
-            }
-          }
-        }
-      }
-      // ---- V~ = diag(exp(gC - g)) V, split into hi / lo ------------------------
-      if (!wait_bar_warp(&bars->full[s], sph, abort)) { ok = false; break; }
-      {
-        const uint8_t *vt = smem + kOffStage + s * kStageBytes + kTileQ + kTileK;
-        uint8_t *vhi = smem + kOffVt + tb * 2 * kTileV;
-        uint8_t *vlo = vhi + kTileV;
-        const int t = e >> 1, half = e & 1;
-        // token t's decay: lanes hold g for tokens 2*lane, 2*lane+1
-        const float gt0 = __shfl_sync(0xffffffffu, g0, (t >> 1) & 31);
-        const float gt1 = __shfl_sync(0xffffffffu, g1, (t >> 1) & 31);
-        const float r = expf(gC - ((t & 1) ? gt1 : gt0));
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t ch = 4 * half + k;
-          float x[8];
-          unpack8(*reinterpret_cast<const uint4 *>(vt + swz(t, ch)), x);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) x[i] *= r;
-          uint4 uh, ul;
-          split8(x, uh, ul);
-          *reinterpret_cast<uint4 *>(vhi + swz(t, ch)) = uh;
-          *reinterpret_cast<uint4 *>(vlo + swz(t, ch)) = ul;
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&bars->p_ready[tb]);
+      const float gC = gates_chunk(G, p, b, h, c, lane, grow);
 
       // ---- S <- gamma_C S + K^T V~ --------------------------------------------
       if (!wait_bar_warp(&bars->ds_ready[tb], ph, abort)) { ok = false; break; }
       tc_fence_after();
       {
-        const float gam = expf(gC);
+        const float gam = exp2f(gC);
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-          float ds[16];
-          tmem_ld16(dcol + kColDS + 16 * blk, ds);
+        for (int half = 0; half < 2; ++half) {
+          float ds[32];
+          tmem_ld32(dcol + kColDS + 32 * half, ds);
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) S[16 * blk + jj] = gam * S[16 * blk + jj] + ds[jj];
+          for (int jj = 0; jj < 32; ++jj) S[32 * half + jj] = gam * S[32 * half + jj] + ds[jj];
         }
       }
       if (c + 1 < nchunks) write_state((c + 1) & 1);
@@ -418,37 +466,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_bar_warp(&bars->o_ready[tb], ph, abort)) { ok = false; break; }
       tc_fence_after();
       {
-        const float gi = expf(g_tok);
+        const float gi = exp2f(grow[tok & (kC - 1)]);
         const int t = t0 + tok;
         const bool store = has_tok && t < T;
         const size_t obase = (((size_t)b * T + t) * p.H + h) * kDK + vblk * kBV;
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-          float o1[16], o2[16];
-          tmem_ld16(dcol + kColO1 + 16 * blk, o1);
-          tmem_ld16(dcol + kColO2 + 16 * blk, o2);
-          float ov[16];
+        for (int half = 0; half < 2; ++half) {
+          float o1[32], o2[32];
+          tmem_ld32(dcol + kColO1 + 32 * half, o1);
+          tmem_ld32(dcol + kColO2 + 32 * half, o2);
+          float ov[32];
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) ov[jj] = gi * o1[jj] + o2[jj];
+          for (int jj = 0; jj < 32; ++jj) ov[jj] = gi * o1[jj] + o2[jj];
           if (store) {
             if (p.out_bf16) {
-              uint32_t pk[8];
+              uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + obase + 32 * half);
 #pragma unroll
-              for (int k = 0; k < 8; ++k) pk[k] = bits(__floats2bfloat162_rn(ov[2 * k], ov[2 * k + 1]));
-              uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + obase + 16 * blk);
-              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+              for (int k = 0; k < 4; ++k) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                  pk[m] = bits(__floats2bfloat162_rn(ov[8 * k + 2 * m], ov[8 * k + 2 * m + 1]));
+                dst[k] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              }
             } else {
-              float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + obase + 16 * blk);
+              float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + obase + 32 * half);
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
+              for (int k = 0; k < 8; ++k)
                 dst[k] = make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
             }
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars->tmem_free[tb]);
+      mbar_arrive(&bars->o_free[tb]);
     }
     if (ok) {
       float *dst = p.S_T + (((size_t)b * p.H + h) * kDK + srow) * kDK + vblk * kBV;

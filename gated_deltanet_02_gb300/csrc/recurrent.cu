@@ -13,18 +13,25 @@
 // and PD disaggregation": one state is kept per draft position, and batched
 // kernels read and write the state pool by slot index.
 //
-// One CTA owns one (request, head) state, d x d fp32, held in registers for
-// all of its steps: thread (rg, cg) holds rows rg + ROWG*i of column group cg
-// (4 consecutive columns, one 16-byte vector), so every warp-wide load or
-// store of a state row is contiguous.  k S and q S are reduced in one pass
-// over the registers, across row groups through shared memory in a fixed
-// order (deterministic, no atomics).  Decode (1 step, in place) and
-// speculative decode (D steps, a write after each) run this same code, so a
-// draft state equals the state of repeated decode steps bit for bit.
+// One CTA owns one (request, head) state, d x d fp32.  Its source is fetched
+// into shared memory by a single bulk copy (cp.async.bulk) issued as soon as
+// the slot id is known, so the copy engine moves the 64 KiB while the threads
+// run the front end (short convolution, L2 norm); registers stay low enough
+// for two CTAs per SM, i.e. two states in flight per SM besides the stores.
+// Thread (rg, cg) owns rows rg + ROWG*i of column group cg (4 consecutive
+// columns, one 16-byte vector), so every warp-wide access to a state row is
+// contiguous, in shared and in global memory.  k S and q S are reduced in one
+// pass, across row groups through shared memory in a fixed order
+// (deterministic, no atomics).  Decode (1 step, in place) and speculative
+// decode (D steps, a write after each) run this same code, so a draft state
+// equals the state of repeated decode steps bit for bit.
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace glinattn {
 namespace {
+
+using namespace sm100;
 
 template <int D>
 struct Shape {
@@ -61,35 +68,54 @@ template <int D>
 __global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurParams p) {
   using Sh = Shape<D>;
   constexpr int NW = (Sh::NT + 31) / 32;
+  constexpr uint32_t kStateBytes = D * D * 4;
   const int unit = blockIdx.x;
   const int n = unit / p.H, h = unit - n * p.H;
   const int tid = threadIdx.x;
   const int cg = tid % Sh::COLG, rg = tid / Sh::COLG;
   const size_t DD = (size_t)D * D;
 
-  __shared__ float s_act[3 * D];      // q | k | v of the current token after the front end
-  __shared__ float s_raw[3 * D];      // raw inputs of the current token
-  __shared__ float s_hist[3][3 * D];  // conv history, oldest first
+  extern __shared__ __align__(128) float4 s_state4[];  // the d x d state, row-major
+  __shared__ float s_act[3 * D];                        // q | k | v after the front end
+  __shared__ float s_raw[3 * D];                        // raw inputs of the current token
+  __shared__ float s_hist[3][3 * D];                    // conv history, oldest first
   __shared__ float s_red[Sh::ROWG][2][D];
   __shared__ float s_wsum[2][NW];
   __shared__ float s_qk;
-  __shared__ int s_bad;
+  __shared__ int s_bad, s_has_src;
+  __shared__ __align__(8) uint64_t s_bar;
 
-  // ---- unit validation: slots in range, gates in (0, 1] ----------------------
-  if (tid == 0) s_bad = 0;
-  __syncthreads();
-  int bad = 0;
-  if (p.pool_slots > 0) {
-    if (p.src_slot && tid == 0) {
-      const int s = p.src_slot[n];
-      if (s < 0 || s >= p.pool_slots) bad |= GLINATTN_DEV_BAD_SLOT;
-    }
-    if (p.dst_slot) {
-      const int nd = p.dst_per_step ? p.steps : 1;
-      for (int t = tid; t < nd; t += Sh::NT) {
-        const int s = p.dst_slot[(size_t)n * nd + t];
-        if (s < 0 || s >= p.pool_slots) bad |= GLINATTN_DEV_BAD_SLOT;
+  // ---- thread 0 checks the source slot and starts the state copy at once ----
+  if (tid == 0) {
+    int bad0 = 0;
+    const float *src = nullptr;
+    if (p.S_src) {
+      size_t slot = (size_t)n;
+      if (p.src_slot) {
+        const int s = p.src_slot[n];
+        if (p.pool_slots > 0 && (s < 0 || s >= p.pool_slots)) bad0 = GLINATTN_DEV_BAD_SLOT;
+        slot = (size_t)s;
       }
+      if (!bad0) src = p.S_src + (slot * p.H + h) * DD;
+    }
+    mbar_init(&s_bar, 1);
+    fence_mbar_init();
+    if (src) {
+      mbar_arrive_expect_tx(&s_bar, kStateBytes);
+      bulk_load(s_state4, src, kStateBytes, &s_bar);
+    }
+    s_bad = bad0;
+    s_has_src = src != nullptr;
+  }
+  __syncthreads();
+
+  // ---- the rest of the unit validation: destination slots, gates in (0, 1] --
+  int bad = 0;
+  if (p.pool_slots > 0 && p.dst_slot) {
+    const int nd = p.dst_per_step ? p.steps : 1;
+    for (int t = tid; t < nd; t += Sh::NT) {
+      const int s = p.dst_slot[(size_t)n * nd + t];
+      if (s < 0 || s >= p.pool_slots) bad |= GLINATTN_DEV_BAD_SLOT;
     }
   }
   for (int t = tid; t < p.steps; t += Sh::NT) {
@@ -98,25 +124,16 @@ __global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurPara
   }
   if (bad) atomicOr(&s_bad, bad);
   __syncthreads();
+  const bool has_src = s_has_src != 0;
   if (s_bad) {
+    if (has_src) mbar_wait(&s_bar, 0);  // let the copy land before the CTA exits
     if (tid == 0 && p.dev_status) atomicOr(p.dev_status, (uint32_t)s_bad);
     return;
   }
-
-  // ---- load the state into registers ------------------------------------------
-  float4 S[Sh::RPT];
-  {
-    const float *src = nullptr;
-    if (p.S_src) {
-      const size_t slot = p.src_slot ? (size_t)p.src_slot[n] : (size_t)n;
-      src = p.S_src + (slot * p.H + h) * DD;
-    }
+  if (!has_src) {
 #pragma unroll
-    for (int i = 0; i < Sh::RPT; ++i) {
-      const int r = rg + Sh::ROWG * i;
-      S[i] = src ? *reinterpret_cast<const float4 *>(src + (size_t)r * D + 4 * cg)
-                 : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    for (int i = 0; i < Sh::RPT; ++i)
+      s_state4[(rg + Sh::ROWG * i) * Sh::COLG + cg] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
   // channel of this head for local channel c = part * D + i
@@ -187,7 +204,15 @@ __global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurPara
       __syncthreads();
       for (int c = tid; c < 3 * D; c += Sh::NT) s_act[c] = round_bf16(s_act[c]);
     }
-    __syncthreads();
+    if (t == 0 && has_src) {  // the state copy must have landed
+      const bool ok = mbar_wait(&s_bar, 0);
+      if (!__syncthreads_and(ok)) {
+        if (tid == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_WAIT_TIMEOUT);
+        return;
+      }
+    } else {
+      __syncthreads();
+    }
 
     // ---- q.k (one warp, fixed order) and the partial k S, q S ------------------
     if (tid < 32) {
@@ -201,9 +226,10 @@ __global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurPara
 #pragma unroll
     for (int i = 0; i < Sh::RPT; ++i) {
       const int r = rg + Sh::ROWG * i;
+      const float4 S = s_state4[r * Sh::COLG + cg];
       const float kr = sk[r], qr = sq[r];
-      x.x += kr * S[i].x; x.y += kr * S[i].y; x.z += kr * S[i].z; x.w += kr * S[i].w;
-      y.x += qr * S[i].x; y.y += qr * S[i].y; y.z += qr * S[i].z; y.w += qr * S[i].w;
+      x.x += kr * S.x; x.y += kr * S.y; x.z += kr * S.z; x.w += kr * S.w;
+      y.x += qr * S.x; y.y += qr * S.y; y.z += qr * S.z; y.w += qr * S.w;
     }
     *reinterpret_cast<float4 *>(&s_red[rg][0][4 * cg]) = x;
     *reinterpret_cast<float4 *>(&s_red[rg][1][4 * cg]) = y;
@@ -218,7 +244,7 @@ __global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurPara
       y.x += b.x; y.y += b.y; y.z += b.z; y.w += b.w;
     }
 
-    // ---- update -----------------------------------------------------------------
+    // ---- update: shared memory copy for the next step, global copy if due ------
     const float a = p.alpha[row];
     const float4 vv = *reinterpret_cast<const float4 *>(sv + 4 * cg);
     float4 u = vv;
@@ -229,13 +255,26 @@ __global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurPara
       u.z = b * (vv.z - a * x.z);
       u.w = b * (vv.w - a * x.w);
     }
+    const bool last = (t == p.steps - 1);
+    const bool emit = p.dst_per_step || last;
+    float *dst = nullptr;
+    size_t dslot = (size_t)n;
+    if (emit) {
+      if (p.dst_slot)
+        dslot = (size_t)p.dst_slot[(size_t)n * (p.dst_per_step ? p.steps : 1) + (p.dst_per_step ? t : 0)];
+      dst = p.S_dst + (dslot * p.H + h) * DD;
+    }
 #pragma unroll
     for (int i = 0; i < Sh::RPT; ++i) {
-      const float kr = sk[rg + Sh::ROWG * i];
-      S[i].x = a * S[i].x + kr * u.x;
-      S[i].y = a * S[i].y + kr * u.y;
-      S[i].z = a * S[i].z + kr * u.z;
-      S[i].w = a * S[i].w + kr * u.w;
+      const int r = rg + Sh::ROWG * i;
+      const float kr = sk[r];
+      float4 S = s_state4[r * Sh::COLG + cg];
+      S.x = a * S.x + kr * u.x;
+      S.y = a * S.y + kr * u.y;
+      S.z = a * S.z + kr * u.z;
+      S.w = a * S.w + kr * u.w;
+      if (!last) s_state4[r * Sh::COLG + cg] = S;
+      if (emit) *reinterpret_cast<float4 *>(dst + (size_t)r * D + 4 * cg) = S;
     }
     if (rg == 0) {
       const float qk = s_qk;
@@ -245,33 +284,28 @@ __global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurPara
       store_act(p.o, ob + 2, a * y.z + qk * u.z, p.out_bf16);
       store_act(p.o, ob + 3, a * y.w + qk * u.w, p.out_bf16);
     }
-
-    // ---- per-step destination (one state per draft position) ------------------
-    const bool last = (t == p.steps - 1);
-    if (p.dst_per_step || last) {
-      const size_t slot = p.dst_slot ? (size_t)p.dst_slot[(size_t)n * (p.dst_per_step ? p.steps : 1) +
-                                                          (p.dst_per_step ? t : 0)]
-                                     : (size_t)n;
-      float *dst = p.S_dst + (slot * p.H + h) * DD;
+    if (emit && conv && p.conv_dst) {
+      __syncthreads();  // s_hist shift complete
+      for (int c = tid; c < 3 * D; c += Sh::NT)
 #pragma unroll
-      for (int i = 0; i < Sh::RPT; ++i)
-        *reinterpret_cast<float4 *>(dst + (size_t)(rg + Sh::ROWG * i) * D + 4 * cg) = S[i];
-      if (conv && p.conv_dst) {
-        __syncthreads();  // s_hist shift complete
-        for (int c = tid; c < 3 * D; c += Sh::NT)
-#pragma unroll
-          for (int j = 0; j < 3; ++j)
-            store_act(p.conv_dst, (slot * 3 + j) * p.Cch + chan(c), s_hist[j][c], p.in_bf16);
-      }
+        for (int j = 0; j < 3; ++j)
+          store_act(p.conv_dst, (dslot * 3 + j) * p.Cch + chan(c), s_hist[j][c], p.in_bf16);
     }
     __syncthreads();  // shared buffers are rewritten by the next step
   }
 
   if (p.steps == 0) {  // a zero-length segment hands its inputs straight on
+    if (has_src && !mbar_wait(&s_bar, 0)) {
+      if (tid == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_WAIT_TIMEOUT);
+      return;
+    }
+    __syncthreads();
     float *dst = p.S_dst + ((size_t)n * p.H + h) * DD;
 #pragma unroll
-    for (int i = 0; i < Sh::RPT; ++i)
-      *reinterpret_cast<float4 *>(dst + (size_t)(rg + Sh::ROWG * i) * D + 4 * cg) = S[i];
+    for (int i = 0; i < Sh::RPT; ++i) {
+      const int r = rg + Sh::ROWG * i;
+      *reinterpret_cast<float4 *>(dst + (size_t)r * D + 4 * cg) = s_state4[r * Sh::COLG + cg];
+    }
     if (conv && p.conv_dst)
       for (int c = tid; c < 3 * D; c += Sh::NT)
 #pragma unroll
@@ -283,7 +317,12 @@ __global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurPara
 template <int D>
 cudaError_t launch(const RecurParams &p, cudaStream_t stream) {
   const unsigned units = (unsigned)p.N * (unsigned)p.H;
-  recurrent_kernel<D><<<units, Shape<D>::NT, 0, stream>>>(p);
+  constexpr int smem = D * D * 4;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(recurrent_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  recurrent_kernel<D><<<units, Shape<D>::NT, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
