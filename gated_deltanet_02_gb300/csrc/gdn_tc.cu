@@ -1,0 +1,890 @@
+// gdn_tc.cu -- chunked Gated DeltaNet prefill on the 5th-generation tensor cores.
+//
+// "Inference for linear attention and hybrid architectures", section "Two
+// ways to write the same computation": DeltaNet's chunked form must first
+// write the error-correcting updates inside a chunk in matrix form.  With the
+// recurrence S_t = alpha_t S_{t-1} + k_t^T u_t, u_t = beta_t (v_t - alpha_t k_t
+// S_{t-1}) and, inside a chunk with start state S, g = cumulative log decay,
+// gamma = exp(g), D_ij = exp(g_i - g_j) [j <= i], r_j = exp(g_C - g_j):
+//
+//   (I + A) U = diag(beta) V - diag(beta gamma) K S,
+//        A_ij = beta_i D_ij (k_i . k_j) for j < i
+//   U = U~ - W S,  U~ = (I+A)^-1 diag(beta) V,  W = (I+A)^-1 diag(beta gamma) K
+//   O      = diag(gamma) Q S + ((Q K^T) * D) U
+//   S_next = gamma_C S + K^T diag(r) U
+//
+// Everything but U - W S is independent of the state, so the work is split:
+//
+//   pass A (gdn_prep_kernel), one CTA per (batch, head, chunk), all chunks in
+//     parallel: the front end (short causal convolution, L2 norm of q and k,
+//     rounding to bf16), [Q; K] K^T as one M = 128 MMA, A, the unit-lower
+//     inverse (I + A)^-1 in fp32, and W and U~ as MMAs.  Q', K', W (bf16), U~
+//     (fp32) and the log2 gates go to a caller-provided workspace.
+//   pass B (gdn_scan_kernel), one CTA per (batch, head, 64-wide d_v slice),
+//     serial over chunks with the fp32 state in registers: U = U~ - W S, the
+//     outputs and the state carry, with the same warp roles as the gated
+//     linear attention kernel.
+//
+// Operands derived in fp32 (S, P, U, r U, the inverse) enter the MMAs as a
+// bf16 high part plus a bf16 remainder.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "prefill_tc.cuh"
+#include "sm100.cuh"
+#include "tc_common.cuh"
+
+namespace glinattn {
+namespace {
+
+using namespace sm100;
+using namespace tc;
+
+constexpr int kC = 64;   // chunk length
+constexpr int kD = 128;  // head size (d_k = d_v)
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+  return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+}
+
+// bf16 round-to-nearest-even of 8 floats, packed as 16 bytes.
+__device__ __forceinline__ uint4 pack8_rn(const float *x) {
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) w[k] = bits(__floats2bfloat162_rn(x[2 * k], x[2 * k + 1]));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ================================ pass A ====================================
+
+constexpr int kPrepThreads = 256;
+constexpr int kRawRows = kC + 3;                 // the chunk and 3 tokens of conv history
+constexpr uint32_t kRawRowBytes = 3 * kD * 2;    // q | k | v of one token, bf16
+constexpr uint32_t kOffRaw = 0;                  // raw [67][384] bf16 (51456 B)
+constexpr uint32_t kOffAmat = 0;                 // after the front end: A [64][65] fp32
+constexpr uint32_t kOffTm = 17408;               // then (I+A)^-1 diag(beta gamma) hi, lo and
+                                                 // (I+A)^-1 diag(beta) hi, lo: 4 x 8 KiB
+constexpr uint32_t kOffW4 = 52224;               // conv weights [384][4] fp32
+constexpr uint32_t kOffQK = 58368;               // stacked [Q'; K']: 2 column blocks x 128 rows x 128 B
+constexpr uint32_t kOffVp = kOffQK + 32768;      // V': 2 column blocks x 64 rows x 128 B
+constexpr uint32_t kOffMisc = kOffVp + 16384;    // g2[64], beta[64], barrier, TMEM slot
+constexpr uint32_t kPrepSmem = kOffMisc + 1024 + 1024;
+static_assert(kOffRaw + kRawRows * kRawRowBytes <= kOffW4, "raw tile");
+static_assert(kOffAmat + 64 * 65 * 4 <= kOffTm && kOffTm + 4 * 8192 <= kOffW4, "aliases");
+static_assert(kOffQK % 1024 == 0 && kOffVp % 1024 == 0 && kOffTm % 1024 == 0, "alignment");
+
+struct PrepParams {
+  int B, T, H, nchunks, Tp, qk_l2norm, has_conv;
+  const __nv_bfloat16 *q, *k, *v;
+  const float *alpha, *beta, *conv_w;
+  const __nv_bfloat16 *conv_in;
+  __nv_bfloat16 *Qp, *Kp, *Wp;  // [B*H, Tp, 128]
+  float *Up;                    // [B*H, Tp, 128]
+  float *Gp;                    // [B*H, Tp]
+  uint32_t *dev_status;
+};
+
+__global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = c * kC, H = p.H, T = p.T;
+  const int Cch = 3 * H * kD;
+  const size_t unit = (size_t)b * H + h;
+  float *g2s = reinterpret_cast<float *>(smem + kOffMisc);
+  float *betas = g2s + kC;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffMisc + 512);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffMisc + 520);
+
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tslot, 256);
+    tmem_relinquish();
+  }
+
+  // ---- raw tile: tokens t0-3 .. t0+63, history from conv_in (or zero) ---------
+  uint8_t *raw = smem + kOffRaw;
+  for (int it = tid; it < kRawRows * 48; it += kPrepThreads) {
+    const int r = it / 48, rem = it - r * 48, part = rem >> 4, q16 = rem & 15;
+    const int t = t0 - 3 + r;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (t >= 0 && t < T) {
+      const __nv_bfloat16 *src = part == 0 ? p.q : (part == 1 ? p.k : p.v);
+      val = *reinterpret_cast<const uint4 *>(src + (((size_t)b * T + t) * H + h) * kD + q16 * 8);
+    } else if (t < 0 && p.has_conv && p.conv_in) {
+      val = *reinterpret_cast<const uint4 *>(p.conv_in + ((size_t)b * 3 + (t + 3)) * Cch + part * H * kD +
+                                             h * kD + q16 * 8);
+    }
+    *reinterpret_cast<uint4 *>(raw + r * kRawRowBytes + part * 256 + q16 * 16) = val;
+  }
+  float *w4 = reinterpret_cast<float *>(smem + kOffW4);
+  if (p.has_conv)
+    for (int i = tid; i < 3 * kD; i += kPrepThreads) {
+      const int part = i / kD, ch = i - part * kD;
+      *reinterpret_cast<float4 *>(w4 + i * 4) =
+          *reinterpret_cast<const float4 *>(p.conv_w + ((size_t)part * H * kD + h * kD + ch) * 4);
+    }
+  // ---- gates of the chunk (warp 0): g2 = cumsum(log2 alpha); alpha = 1, beta = 0 past T
+  if (warp == 0) {
+    const int ta = t0 + 2 * lane, tb = ta + 1;
+    const size_t ia = ((size_t)b * T + ta) * H + h, ib = ((size_t)b * T + tb) * H + h;
+    const float a0 = ta < T ? p.alpha[ia] : 1.f, a1 = tb < T ? p.alpha[ib] : 1.f;
+    const float l0 = log2f(a0), l1 = log2f(a1);
+    float incl = l0 + l1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0.f;
+    const float ga = excl + l0, gb = ga + l1;
+    g2s[2 * lane] = ga;
+    g2s[2 * lane + 1] = gb;
+    betas[2 * lane] = ta < T ? p.beta[ia] : 0.f;
+    betas[2 * lane + 1] = tb < T ? p.beta[ib] : 0.f;
+    p.Gp[unit * p.Tp + t0 + 2 * lane] = ga;
+    p.Gp[unit * p.Tp + t0 + 2 * lane + 1] = gb;
+  }
+  __syncthreads();
+
+  // ---- front end: y_t = sum_j w_j x_{t-3+j}; L2 norm of q, k rows; bf16 -------
+  uint8_t *qk = smem + kOffQK;
+  uint8_t *vp = smem + kOffVp;
+  for (int task = tid; task < kC * 3 * 8; task += kPrepThreads) {  // 6 rounds, uniform
+    const int g = task & 7, tp = task >> 3, part = tp % 3, t = tp / 3;
+    const int ch0 = g * 16;
+    float y[16];
+    if (p.has_conv) {
+      const float *w = w4 + (part * kD + ch0) * 4;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) y[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint8_t *src = raw + (t + j) * kRawRowBytes + part * 256 + ch0 * 2;
+        float x[16];
+        unpack8(*reinterpret_cast<const uint4 *>(src), x);
+        unpack8(*reinterpret_cast<const uint4 *>(src + 16), x + 8);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[i] += w[i * 4 + j] * x[i];
+      }
+    } else {
+      const uint8_t *src = raw + (t + 3) * kRawRowBytes + part * 256 + ch0 * 2;
+      unpack8(*reinterpret_cast<const uint4 *>(src), y);
+      unpack8(*reinterpret_cast<const uint4 *>(src + 16), y + 8);
+    }
+    if (part < 2 && p.qk_l2norm) {
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ss += y[i] * y[i];
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+      const float inv = 1.f / sqrtf(ss + 1e-6f);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) y[i] *= inv;
+    }
+    if (t0 + t >= T) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) y[i] = 0.f;
+    }
+    const uint4 lo8 = pack8_rn(y), hi8 = pack8_rn(y + 8);
+    const int blk = g >> 2, chunk = (g & 3) * 2;
+    if (part < 2) {
+      const int row = part * kC + t;
+      uint8_t *tile = qk + blk * 16384;
+      *reinterpret_cast<uint4 *>(tile + swz(row, chunk)) = lo8;
+      *reinterpret_cast<uint4 *>(tile + swz(row, chunk + 1)) = hi8;
+      __nv_bfloat16 *dst = (part == 0 ? p.Qp : p.Kp) + (unit * p.Tp + t0 + t) * kD + ch0;
+      reinterpret_cast<uint4 *>(dst)[0] = lo8;
+      reinterpret_cast<uint4 *>(dst)[1] = hi8;
+    } else {
+      uint8_t *tile = vp + blk * 8192;
+      *reinterpret_cast<uint4 *>(tile + swz(t, chunk)) = lo8;
+      *reinterpret_cast<uint4 *>(tile + swz(t, chunk + 1)) = hi8;
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tslot;
+
+  // ---- [Q'; K'] K'^T: M = 128 (rows 0-63 Q'K'^T, rows 64-127 K'K'^T), N = 64
+  if (tid == 0) {
+    const uint64_t dA = desc_sw128(smem_u32(qk), 16, 1024);
+    const uint64_t dB = desc_sw128(smem_u32(qk + 8192), 16, 1024);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+      umma_bf16(tm, dA + off, dB + off, idesc_bf16(128, 64, false, false), ks > 0);
+    }
+    umma_commit(bar);
+  }
+  bool ok = __syncthreads_and(mbar_wait(bar, 0));
+  tc_fence_after();
+
+  // ---- A_ij = beta_i 2^(g_i - g_j) (k_i . k_j) for j < i (rows from TMEM lanes 64..127)
+  float *A = reinterpret_cast<float *>(smem + kOffAmat);
+  if (ok && (warp == 2 || warp == 3)) {
+    const int i = 32 * (warp - 2) + lane;
+    float kk[64];
+    {
+      float part[32];
+      tmem_ld32(tm + ((uint32_t)(32 * warp) << 16), part);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) kk[j] = part[j];
+      tmem_ld32(tm + ((uint32_t)(32 * warp) << 16) + 32, part);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) kk[32 + j] = part[j];
+    }
+    const float gi = g2s[i], bi = betas[i];
+#pragma unroll
+    for (int j = 0; j < 64; ++j) A[i * 65 + j] = (j < i) ? bi * exp2f(gi - g2s[j]) * kk[j] : 0.f;
+  }
+  __syncthreads();
+
+  // ---- (I + A)^-1 by forward substitution, thread k solves column k ------------
+  if (ok && tid < 64) {
+    const int k = tid;
+    float x[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < i; ++j) s += A[i * 65 + j] * x[j];
+      x[i] = (i == k ? 1.f : 0.f) - s;
+    }
+    const float bk = betas[k], bgk = bk * exp2f(g2s[k]);
+    uint8_t *tm1 = smem + kOffTm;  // (I+A)^-1 diag(beta gamma): hi, lo
+    uint8_t *tm2 = tm1 + 16384;    // (I+A)^-1 diag(beta): hi, lo
+    const uint32_t colb = (uint32_t)(k & 7) * 2;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const float w1 = x[i] * bgk, w2 = x[i] * bk;
+      const __nv_bfloat16 h1 = __float2bfloat16_rn(w1), h2 = __float2bfloat16_rn(w2);
+      const __nv_bfloat16 l1 = __float2bfloat16_rn(w1 - __bfloat162float(h1));
+      const __nv_bfloat16 l2 = __float2bfloat16_rn(w2 - __bfloat162float(h2));
+      const uint32_t off = swz(i, k >> 3) + colb;
+      *reinterpret_cast<__nv_bfloat16 *>(tm1 + off) = h1;
+      *reinterpret_cast<__nv_bfloat16 *>(tm1 + 8192 + off) = l1;
+      *reinterpret_cast<__nv_bfloat16 *>(tm2 + off) = h2;
+      *reinterpret_cast<__nv_bfloat16 *>(tm2 + 8192 + off) = l2;
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  // ---- W = Tm1 K' (TMEM cols 0-127), U~ = Tm2 V' (cols 128-255): M = 64, N = 128
+  if (ok && tid == 0) {
+    const uint32_t id = idesc_bf16(64, 128, false, true);
+    const uint64_t dT1 = desc_sw128(smem_u32(smem + kOffTm), 16, 1024);
+    const uint64_t dT2 = desc_sw128(smem_u32(smem + kOffTm + 16384), 16, 1024);
+    const uint64_t dK = desc_sw128(smem_u32(qk + 8192), 16384, 1024);
+    const uint64_t dV = desc_sw128(smem_u32(vp), 8192, 1024);
+#pragma unroll
+    for (int part = 0; part < 2; ++part)
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint32_t aoff = (part * 8192 + ks * 32) >> 4, boff = (ks * 2048) >> 4;
+        umma_bf16(tm, dT1 + aoff, dK + boff, id, (part | ks) != 0);
+        umma_bf16(tm + 128, dT2 + aoff, dV + boff, id, (part | ks) != 0);
+      }
+    umma_commit(bar);
+  }
+  if (ok) ok = __syncthreads_and(mbar_wait(bar, 1));
+  tc_fence_after();
+
+  // ---- W (bf16) and U~ (fp32) rows to the workspace ----------------------------
+  if (ok) {
+    const int q4 = warp & 3, i = 16 * q4 + lane;
+    const uint32_t base = tm + ((uint32_t)(32 * q4) << 16) + (warp < 4 ? 0u : 128u);
+    const size_t row = unit * p.Tp + t0 + i;
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+      float v[32];
+      tmem_ld32(base + 32 * blk, v);
+      if (lane < 16) {
+        if (warp < 4) {
+          uint4 *dst = reinterpret_cast<uint4 *>(p.Wp + row * kD + 32 * blk);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) dst[k] = pack8_rn(v + 8 * k);
+        } else {
+          float4 *dst = reinterpret_cast<float4 *>(p.Up + row * kD + 32 * blk);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (!ok && tid == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_WAIT_TIMEOUT);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tm, 256);
+  }
+}
+
+// ================================ pass B ====================================
+
+constexpr int kBV = 64;
+constexpr int kStages = 2;
+constexpr int kThreads = 320;    // warp 0 TMA, warp 1 MMA, warps 2-5 (P), 6-9 (state, outputs)
+constexpr int kEpiThreads = 128;
+constexpr uint32_t kTile = kC * kD * 2;        // Q', K' or W tile: 16 KiB (2 column blocks)
+constexpr uint32_t kTileU = kC * kBV * 4;      // U~ slice, fp32: 16 KiB
+constexpr uint32_t kStageBytes = 3 * kTile + kTileU;
+constexpr uint32_t kTileP = kC * kC * 2;       // 8 KiB (one of hi / lo)
+constexpr uint32_t kTileV = kC * kBV * 2;      // 8 KiB
+constexpr uint32_t kTileS = kD * kBV * 2;      // 16 KiB
+constexpr uint32_t kOffStage = 0;
+constexpr uint32_t kOffP = kStages * kStageBytes;   // P hi, lo
+constexpr uint32_t kOffU = kOffP + 2 * kTileP;      // U hi, lo
+constexpr uint32_t kOffRU = kOffU + 2 * kTileV;     // r U hi, lo
+constexpr uint32_t kOffS = kOffRU + 2 * kTileV;     // S hi, lo
+constexpr uint32_t kOffG = kOffS + 2 * kTileS;      // gate rows [warp][2][64]
+constexpr uint32_t kOffBar = kOffG + (kThreads / 32) * 2 * kC * 4;
+constexpr uint32_t kScanSmem = kOffBar + 256 + 1024;
+static_assert(kScanSmem <= 232448, "shared memory budget");
+constexpr uint32_t kColQK = 0, kColWS = 128, kColDS = 192, kColQS = 256, kColPU = 384;
+
+struct ScanParams {
+  int B, T, H, nchunks, Tp, out_bf16;
+  const float *alpha;
+  const float *Gp;
+  const float *S0;
+  float *S_T;
+  void *o;
+  // conv cache hand-over (written by the vblk-0 CTA of each (b, h))
+  int has_conv;
+  const __nv_bfloat16 *q, *k, *v, *conv_in;
+  __nv_bfloat16 *conv_out;
+  uint32_t *dev_status;
+};
+
+struct ScanBars {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t qk_ready[2], qk_free[2], p_ready[2], o_ready[2], o_free[2];
+  uint64_t ws_ready, u_ready, ds_ready, s_ready, p_free;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(ScanBars) <= 256, "barrier block");
+
+struct GateRow {
+  float g0n, g1n;  // next chunk's g2 values, prefetched
+};
+
+__device__ __forceinline__ void grow_prefetch(GateRow &G, const ScanParams &p, size_t unit, int c,
+                                              int lane) {
+  const size_t base = unit * p.Tp + (size_t)c * kC + 2 * lane;
+  const bool in = c < p.nchunks;
+  G.g0n = in ? p.Gp[base] : 0.f;
+  G.g1n = in ? p.Gp[base + 1] : 0.f;
+}
+
+__device__ __forceinline__ float grow_chunk(GateRow &G, const ScanParams &p, size_t unit, int c,
+                                            int lane, float *row) {
+  const float a = G.g0n, b = G.g1n;
+  grow_prefetch(G, p, unit, c + 1, lane);
+  __syncwarp();
+  row[2 * lane] = a;
+  row[2 * lane + 1] = b;
+  __syncwarp();
+  return row[kC - 1];
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gdn_scan_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tu,
+                    const ScanParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  ScanBars *bars = reinterpret_cast<ScanBars *>(smem + kOffBar);
+  float *s_g = reinterpret_cast<float *>(smem + kOffG);
+  volatile int *abort = &bars->abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int vblk = blockIdx.x & 1;
+  const int bh = blockIdx.x >> 1;
+  const int b = bh / p.H, h = bh - b * p.H;
+  const size_t unit = (size_t)bh;
+  const int T = p.T, nchunks = p.nchunks;
+
+  // ---- the unit is skipped when a gate is outside (0, 1] ---------------------
+  {
+    int bad = 0;
+    for (int t = tid; t < T; t += kThreads) {
+      const float a = p.alpha[((size_t)b * T + t) * p.H + h];
+      bad |= !(a > 0.f && a <= 1.f);
+    }
+    if (__syncthreads_or(bad)) {
+      if (tid == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_BAD_GATE);
+      return;
+    }
+  }
+  // ---- conv cache hand-over: the last 3 raw inputs of this head's channels -----
+  if (p.has_conv && p.conv_out && vblk == 0) {
+    const int Cch = 3 * p.H * kD;
+    __nv_bfloat16 vals[6];  // up to 2 (row, channel) items per thread: 3 x 384 / 320
+    int n = 0;
+    for (int it = tid; it < 3 * 3 * kD; it += kThreads, ++n) {
+      const int j = it / (3 * kD), rem = it - j * 3 * kD, part = rem / kD, ch = rem - part * kD;
+      const int t = T - 3 + j;
+      __nv_bfloat16 x = __float2bfloat16_rn(0.f);
+      if (t >= 0) {
+        const __nv_bfloat16 *src = part == 0 ? p.q : (part == 1 ? p.k : p.v);
+        x = src[(((size_t)b * T + t) * p.H + h) * kD + ch];
+      } else if (p.conv_in) {
+        x = p.conv_in[((size_t)b * 3 + (t + 3)) * Cch + part * p.H * kD + h * kD + ch];
+      }
+      vals[n] = x;
+    }
+    __syncthreads();  // every read of conv_in precedes the writes (they may alias)
+    n = 0;
+    for (int it = tid; it < 3 * 3 * kD; it += kThreads, ++n) {
+      const int j = it / (3 * kD), rem = it - j * 3 * kD, part = rem / kD, ch = rem - part * kD;
+      p.conv_out[((size_t)b * 3 + j) * Cch + part * p.H * kD + h * kD + ch] = vals[n];
+    }
+  }
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->qk_ready[i], 1);
+      mbar_init(&bars->o_ready[i], 1);
+      mbar_init(&bars->qk_free[i], kEpiThreads);
+      mbar_init(&bars->p_ready[i], kEpiThreads);
+      mbar_init(&bars->o_free[i], kEpiThreads);
+    }
+    mbar_init(&bars->ws_ready, 1);
+    mbar_init(&bars->ds_ready, 1);
+    mbar_init(&bars->p_free, 1);
+    mbar_init(&bars->u_ready, kEpiThreads);
+    mbar_init(&bars->s_ready, kEpiThreads);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      prefetch_tensormap(&tq);
+      prefetch_tensormap(&tk);
+      prefetch_tensormap(&tw);
+      prefetch_tensormap(&tu);
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % kStages;
+        if (!wait_bar(&bars->empty[s], ((uint32_t)(c / kStages) & 1u) ^ 1u, abort)) break;
+        uint8_t *st = smem + kOffStage + s * kStageBytes;
+        uint64_t *fb = &bars->full[s];
+        mbar_arrive_expect_tx(fb, kStageBytes);
+        const int r0 = c * kC;
+        tma_load_3d(st, &tq, fb, 0, r0, (int)unit);
+        tma_load_3d(st + kTile / 2, &tq, fb, 64, r0, (int)unit);
+        tma_load_3d(st + kTile, &tk, fb, 0, r0, (int)unit);
+        tma_load_3d(st + kTile + kTile / 2, &tk, fb, 64, r0, (int)unit);
+        tma_load_3d(st + 2 * kTile, &tw, fb, 0, r0, (int)unit);
+        tma_load_3d(st + 2 * kTile + kTile / 2, &tw, fb, 64, r0, (int)unit);
+        tma_load_3d(st + 3 * kTile, &tu, fb, vblk * kBV, r0, (int)unit);
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);   // Q' K'^T
+      constexpr uint32_t id_xs = idesc_bf16(64, kBV, false, true);   // W S, Q' S
+      constexpr uint32_t id_ds = idesc_bf16(128, kBV, true, true);   // K'^T (r U)
+      constexpr uint32_t id_pu = idesc_bf16(64, kBV, false, true);   // P U
+      const uint32_t sbase = smem_u32(smem);
+      auto issue_qk = [&](int c) -> bool {
+        const int s = c % kStages, tb = c & 1;
+        if (!wait_bar(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) return false;
+        if (!wait_bar(&bars->qk_free[tb], ((uint32_t)(c >> 1) & 1u) ^ 1u, abort)) return false;
+        tc_fence_after();
+        const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
+        const uint64_t dQ = desc_sw128(aQ, 16, 1024), dK = desc_sw128(aQ + kTile, 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
+          umma_bf16(tmem + kColQK + tb * 64, dQ + off, dK + off, id_qk, ks > 0);
+        }
+        umma_commit(&bars->qk_ready[tb]);
+        return true;
+      };
+      bool ok = issue_qk(0);
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int s = c % kStages, tb = c & 1;
+        const uint32_t ph = (uint32_t)(c >> 1) & 1u, pc = (uint32_t)c & 1u;
+        if (c + 1 < nchunks && !issue_qk(c + 1)) break;
+        const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
+        const uint64_t dQ = desc_sw128(aQ, 16, 1024);
+        const uint64_t dKm = desc_sw128(aQ + kTile, kTile / 2, 1024);
+        const uint64_t dW = desc_sw128(aQ + 2 * kTile, 16, 1024);
+        const uint64_t dS = desc_sw128(sbase + kOffS, 16, 1024);
+        const uint64_t dP = desc_sw128(sbase + kOffP, 16, 1024);
+        const uint64_t dU = desc_sw128(sbase + kOffU, 16, 1024);
+        const uint64_t dRU = desc_sw128(sbase + kOffRU, 16, 1024);
+        if (!wait_bar(&bars->s_ready, pc, abort)) break;
+        if (!wait_bar(&bars->o_free[tb], ph ^ 1u, abort)) break;
+        tc_fence_after();
+        // W S: M = 64, N = 64, K = d_k (W tile K-major, S tile MN-major)
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t aoff = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
+            umma_bf16(tmem + kColWS, dW + aoff, dS + ((part * kTileS + ks * 2048) >> 4), id_xs,
+                      (part | ks) != 0);
+          }
+        umma_commit(&bars->ws_ready);
+        // Q' S
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t aoff = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
+            umma_bf16(tmem + kColQS + tb * 64, dQ + aoff, dS + ((part * kTileS + ks * 2048) >> 4),
+                      id_xs, (part | ks) != 0);
+          }
+        if (!wait_bar(&bars->u_ready, pc, abort)) break;
+        if (!wait_bar(&bars->p_ready[tb], ph, abort)) break;
+        tc_fence_after();
+        // dS = K'^T (rU hi + rU lo): M = d_k (K' tile read M-major), N = 64, K = 64 tokens
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tmem + kColDS, dKm + ((ks * 2048) >> 4), dRU + ((part * kTileV + ks * 2048) >> 4),
+                      id_ds, (part | ks) != 0);
+        umma_commit(&bars->ds_ready);
+        // P U = Phi Uhi + Phi Ulo + Plo Uhi: M = 64, N = 64, K = 64 tokens
+#pragma unroll
+        for (int part = 0; part < 3; ++part)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const int pp = part == 2 ? 1 : 0, up = part == 1 ? 1 : 0;
+            umma_bf16(tmem + kColPU + tb * 64, dP + ((pp * kTileP + ks * 32) >> 4),
+                      dU + ((up * kTileV + ks * 2048) >> 4), id_pu, (part | ks) != 0);
+          }
+        umma_commit(&bars->o_ready[tb]);
+        umma_commit(&bars->p_free);
+        umma_commit(&bars->empty[s]);
+      }
+    }
+  } else if (warp < 6) {
+    // ============ warpgroup A: P = (Q' K'^T) * D ============
+    const int q4 = warp & 3;
+    const bool has_tok = lane < 16;
+    const int tok = 16 * q4 + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    float *grow = s_g + warp * 2 * kC;
+    GateRow G;
+    grow_prefetch(G, p, unit, 0, lane);
+    for (int c = 0; c < nchunks; ++c) {
+      const int tb = c & 1;
+      const uint32_t ph = (uint32_t)(c >> 1) & 1u;
+      const float gC = grow_chunk(G, p, unit, c, lane, grow);
+      if (!wait_bar_warp(&bars->qk_ready[tb], ph, abort)) break;
+      tc_fence_after();
+      float qk[64];
+      {
+        float part[32];
+        tmem_ld32(tmem + kColQK + tb * 64 + lane_base, part);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) qk[j] = part[j];
+        tmem_ld32(tmem + kColQK + tb * 64 + 32 + lane_base, part);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) qk[32 + j] = part[j];
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->qk_free[tb]);
+      const bool factored = gC > -100.f;
+      float *cfrow = grow + kC;
+      if (factored) {
+        cfrow[2 * lane] = exp2f(-grow[2 * lane]);
+        cfrow[2 * lane + 1] = exp2f(-grow[2 * lane + 1]);
+      }
+      __syncwarp();
+      if (!wait_bar_warp(&bars->p_free, ((uint32_t)c & 1u) ^ 1u, abort)) break;
+      if (has_tok) {
+        const uint32_t phi = smem_u32(smem + kOffP), plo = phi + kTileP;
+        const float gi = grow[tok];
+        if (factored) {
+          const float rf = exp2f(gi);
+#pragma unroll
+          for (int j = 0; j < kC; ++j) qk[j] = (j <= tok) ? qk[j] * rf * cfrow[j] : 0.f;
+        } else {
+#pragma unroll
+          for (int j = 0; j < kC; ++j) qk[j] = (j <= tok) ? qk[j] * exp2f(gi - grow[j]) : 0.f;
+        }
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint4 uh, ul;
+          split8(&qk[8 * ch], uh, ul);
+          sts128(phi + swz(tok, ch), uh);
+          sts128(plo + swz(tok, ch), ul);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->p_ready[tb]);
+    }
+  } else {
+    // ============ warpgroup B: U, the state chain and the outputs ============
+    const int q4 = warp & 3;
+    const int srow = 32 * q4 + lane;
+    const bool has_tok = lane < 16;
+    const int tok = 16 * q4 + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    float *grow = s_g + warp * 2 * kC;
+    GateRow G;
+    grow_prefetch(G, p, unit, 0, lane);
+    float S[kBV];
+    {
+      const float *src = p.S0 ? p.S0 + ((unit * kD) + srow) * kD + vblk * kBV : nullptr;
+#pragma unroll
+      for (int j = 0; j < kBV; j += 4) {
+        const float4 v4 = src ? *reinterpret_cast<const float4 *>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
+      }
+    }
+    auto write_state = [&]() {
+      const uint32_t hi = smem_u32(smem + kOffS), lo = hi + kTileS;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        uint4 uh, ul;
+        split8(&S[8 * ch], uh, ul);
+        sts128(hi + swz(srow, ch), uh);
+        sts128(lo + swz(srow, ch), ul);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->s_ready);
+    };
+    write_state();
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int s = c % kStages, tb = c & 1;
+      const uint32_t ph = (uint32_t)(c >> 1) & 1u, pc = (uint32_t)c & 1u;
+      const uint32_t sph = (uint32_t)(c / kStages) & 1u;
+      const int t0 = c * kC;
+      const float gC = grow_chunk(G, p, unit, c, lane, grow);
+      const float g_tok = grow[tok & (kC - 1)];
+
+      // ---- U = U~ - W S (rows), U and r U split into smem --------------------
+      if (!wait_bar_warp(&bars->ws_ready, pc, abort)) { ok = false; break; }
+      tc_fence_after();
+      float u[kBV];
+      {
+        float part[32];
+        tmem_ld32(tmem + kColWS + lane_base, part);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) u[j] = part[j];
+        tmem_ld32(tmem + kColWS + 32 + lane_base, part);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) u[32 + j] = part[j];
+      }
+      if (!wait_bar_warp(&bars->full[s], sph, abort)) { ok = false; break; }
+      if (!wait_bar_warp(&bars->p_free, pc ^ 1u, abort)) { ok = false; break; }
+      if (has_tok) {
+        const float *ut = reinterpret_cast<const float *>(smem + kOffStage + s * kStageBytes + 3 * kTile) +
+                          tok * kBV;
+#pragma unroll
+        for (int j = 0; j < kBV; j += 4) {
+          const float4 v4 = *reinterpret_cast<const float4 *>(ut + j);
+          u[j] = v4.x - u[j];
+          u[j + 1] = v4.y - u[j + 1];
+          u[j + 2] = v4.z - u[j + 2];
+          u[j + 3] = v4.w - u[j + 3];
+        }
+        const float r = exp2f(gC - g_tok);
+        const uint32_t uhi = smem_u32(smem + kOffU), ulo = uhi + kTileV;
+        const uint32_t rhi = smem_u32(smem + kOffRU), rlo = rhi + kTileV;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint4 uh, ul;
+          split8(&u[8 * ch], uh, ul);
+          sts128(uhi + swz(tok, ch), uh);
+          sts128(ulo + swz(tok, ch), ul);
+          float ru[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) ru[i] = r * u[8 * ch + i];
+          split8(ru, uh, ul);
+          sts128(rhi + swz(tok, ch), uh);
+          sts128(rlo + swz(tok, ch), ul);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->u_ready);
+
+      // ---- S <- gamma_C S + K'^T diag(r) U ----------------------------------------
+      if (!wait_bar_warp(&bars->ds_ready, pc, abort)) { ok = false; break; }
+      tc_fence_after();
+      {
+        const float gam = exp2f(gC);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float ds[32];
+          tmem_ld32(tmem + kColDS + 32 * half + lane_base, ds);
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) S[32 * half + jj] = gam * S[32 * half + jj] + ds[jj];
+        }
+      }
+      if (c + 1 < nchunks) write_state();
+
+      // ---- o = gamma_i (Q' S) + P U ------------------------------------------------
+      if (!wait_bar_warp(&bars->o_ready[tb], ph, abort)) { ok = false; break; }
+      tc_fence_after();
+      {
+        const float gi = exp2f(g_tok);
+        const int t = t0 + tok;
+        const bool store = has_tok && t < T;
+        const size_t obase = (((size_t)b * T + t) * p.H + h) * kD + vblk * kBV;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float o1[32], o2[32];
+          tmem_ld32(tmem + kColQS + tb * 64 + 32 * half + lane_base, o1);
+          tmem_ld32(tmem + kColPU + tb * 64 + 32 * half + lane_base, o2);
+          float ov[32];
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) ov[jj] = gi * o1[jj] + o2[jj];
+          if (store) {
+            if (p.out_bf16) {
+              uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + obase + 32 * half);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) dst[k] = pack8_rn(ov + 8 * k);
+            } else {
+              float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + obase + 32 * half);
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                dst[k] = make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->o_free[tb]);
+    }
+    if (ok) {
+      float *dst = p.S_T + ((unit * kD) + srow) * kD + vblk * kBV;
+#pragma unroll
+      for (int j = 0; j < kBV; j += 4)
+        *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort && tid == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_WAIT_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================ host ======================================
+
+struct Workspace {
+  __nv_bfloat16 *Qp, *Kp, *Wp;
+  float *Up, *Gp;
+  size_t bytes;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+Workspace carve(void *base, int B, int H, int Tp) {
+  Workspace w;
+  const size_t rows = (size_t)B * H * Tp;
+  size_t off = 0;
+  uint8_t *p = reinterpret_cast<uint8_t *>(base);
+  w.Qp = reinterpret_cast<__nv_bfloat16 *>(p + off);
+  off = align256(off + rows * kD * 2);
+  w.Kp = reinterpret_cast<__nv_bfloat16 *>(p + off);
+  off = align256(off + rows * kD * 2);
+  w.Wp = reinterpret_cast<__nv_bfloat16 *>(p + off);
+  off = align256(off + rows * kD * 2);
+  w.Up = reinterpret_cast<float *>(p + off);
+  off = align256(off + rows * kD * 4);
+  w.Gp = reinterpret_cast<float *>(p + off);
+  off = align256(off + rows * 4);
+  w.bytes = off;
+  return w;
+}
+
+}  // namespace
+
+bool gdn_tc_supports(const glinattn_prefill_args &a) {
+  return a.variant == GLINATTN_GDN && a.in_dtype == GLINATTN_BF16 && a.dk == kD && a.dv == kD &&
+         a.seqlen > 0;
+}
+
+size_t gdn_tc_workspace_bytes(const glinattn_prefill_args &a) {
+  const int Tp = (a.seqlen + kC - 1) / kC * kC;
+  return carve(nullptr, a.batch, a.heads, Tp).bytes;
+}
+
+glinattn_status launch_gdn_tc(const glinattn_prefill_args &a, cudaStream_t stream) {
+  const int B = a.batch, T = a.seqlen, H = a.heads;
+  const int nchunks = (T + kC - 1) / kC, Tp = nchunks * kC;
+  const Workspace w = carve(a.workspace, B, H, Tp);
+  if (!a.workspace || a.workspace_bytes < w.bytes) return GLINATTN_ERR_INVALID_ARG;
+
+  PrepParams pp;
+  pp.B = B; pp.T = T; pp.H = H; pp.nchunks = nchunks; pp.Tp = Tp;
+  pp.qk_l2norm = a.qk_l2norm != 0;
+  pp.has_conv = a.conv_w != nullptr;
+  pp.q = static_cast<const __nv_bfloat16 *>(a.q);
+  pp.k = static_cast<const __nv_bfloat16 *>(a.k);
+  pp.v = static_cast<const __nv_bfloat16 *>(a.v);
+  pp.alpha = a.alpha; pp.beta = a.beta; pp.conv_w = a.conv_w;
+  pp.conv_in = static_cast<const __nv_bfloat16 *>(a.conv_in);
+  pp.Qp = w.Qp; pp.Kp = w.Kp; pp.Wp = w.Wp; pp.Up = w.Up; pp.Gp = w.Gp;
+  pp.dev_status = a.dev_status;
+  if (cudaFuncSetAttribute(gdn_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kPrepSmem) != cudaSuccess)
+    return GLINATTN_ERR_CUDA;
+  gdn_prep_kernel<<<dim3(nchunks, H, B), kPrepThreads, kPrepSmem, stream>>>(pp);
+  if (cudaGetLastError() != cudaSuccess) return GLINATTN_ERR_CUDA;
+
+  CUtensorMap tq, tk, tw, tu;
+  const int rows_bh = B * H;
+  if (!encode_rows_map(&tq, w.Qp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, Tp, rows_bh, 64, true) ||
+      !encode_rows_map(&tk, w.Kp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, Tp, rows_bh, 64, true) ||
+      !encode_rows_map(&tw, w.Wp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, Tp, rows_bh, 64, true) ||
+      !encode_rows_map(&tu, w.Up, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kD, Tp, rows_bh, 64, false))
+    return GLINATTN_ERR_CUDA;
+  ScanParams sp;
+  sp.B = B; sp.T = T; sp.H = H; sp.nchunks = nchunks; sp.Tp = Tp;
+  sp.out_bf16 = a.out_dtype == GLINATTN_BF16;
+  sp.alpha = a.alpha; sp.Gp = w.Gp; sp.S0 = a.S0; sp.S_T = a.S_T; sp.o = a.o;
+  sp.has_conv = a.conv_w != nullptr;
+  sp.q = pp.q; sp.k = pp.k; sp.v = pp.v; sp.conv_in = pp.conv_in;
+  sp.conv_out = static_cast<__nv_bfloat16 *>(a.conv_out);
+  sp.dev_status = a.dev_status;
+  if (cudaFuncSetAttribute(gdn_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kScanSmem) != cudaSuccess)
+    return GLINATTN_ERR_CUDA;
+  gdn_scan_kernel<<<(unsigned)(B * H * 2), kThreads, kScanSmem, stream>>>(tq, tk, tw, tu, sp);
+  return cudaGetLastError() == cudaSuccess ? GLINATTN_OK : GLINATTN_ERR_CUDA;
+}
+
+}  // namespace glinattn

@@ -88,8 +88,14 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
     if (partial_overlap(a->conv_in, cb, a->conv_out, cb)) return GLINATTN_ERR_INVALID_ARG;
   }
 
-  if (glinattn::prefill_tc_supports(*a) && glinattn::prefill_tc_available()) {
-    return glinattn::launch_prefill_tc(*a, (cudaStream_t)stream);
+  if (glinattn::prefill_tc_available()) {
+    if (glinattn::prefill_tc_supports(*a)) return glinattn::launch_prefill_tc(*a, (cudaStream_t)stream);
+    if (glinattn::gdn_tc_supports(*a)) {
+      if (!a->workspace || a->workspace_bytes < glinattn::gdn_tc_workspace_bytes(*a) ||
+          !aligned16(a->workspace))
+        return GLINATTN_ERR_INVALID_ARG;
+      return glinattn::launch_gdn_tc(*a, (cudaStream_t)stream);
+    }
   }
 
   RecurParams p = {};
@@ -115,6 +121,13 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
   p.conv_dst = a->conv_w ? a->conv_out : nullptr;
   p.dev_status = a->dev_status;
   return glinattn::launch_recurrent(p, d, (cudaStream_t)stream);
+}
+
+size_t glinattn_prefill_workspace_size(const glinattn_prefill_args *a) {
+  if (!a || a->batch <= 0 || a->seqlen <= 0 || a->heads <= 0) return 0;
+  if (check_common(a->variant, a->in_dtype, a->out_dtype, a->dk, a->dv, a->heads) != GLINATTN_OK) return 0;
+  if (!glinattn::gdn_tc_supports(*a)) return 0;
+  return glinattn::gdn_tc_workspace_bytes(*a);
 }
 
 glinattn_status glinattn_decode(const glinattn_decode_args *a, glinattn_stream_t stream) {

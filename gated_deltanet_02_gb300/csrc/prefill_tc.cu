@@ -37,16 +37,18 @@
 #include "common.cuh"
 #include "prefill_tc.cuh"
 #include "sm100.cuh"
+#include "tc_common.cuh"
 
 namespace glinattn {
 namespace {
 
 using namespace sm100;
+using namespace tc;
 
 constexpr int kC = 64;    // chunk length
 constexpr int kDK = 128;  // key / value head size
 constexpr int kBV = 64;   // d_v columns per CTA
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-5 and 6-9 epilogue
 constexpr int kEpiThreads = 128;  // threads per epilogue warpgroup
 
@@ -58,13 +60,13 @@ constexpr uint32_t kStageBytes = kTileQ + kTileK + kTileV;
 constexpr uint32_t kTileP = kC * kC * 2;   // 8 KiB, one of hi / lo
 constexpr uint32_t kTileS = kDK * kBV * 2; // 16 KiB, one of hi / lo
 constexpr uint32_t kOffStage = 0;
-constexpr uint32_t kOffP = kOffStage + kStages * kStageBytes;  // P[buf][hi, lo]
-constexpr uint32_t kOffVt = kOffP + 4 * kTileP;                // V~[buf][hi, lo]
-constexpr uint32_t kOffS = kOffVt + 4 * kTileV;                // S[buf][hi, lo]
+constexpr uint32_t kOffP = kOffStage + kStages * kStageBytes;  // P[hi, lo]
+constexpr uint32_t kOffVt = kOffP + 2 * kTileP;                // V~[hi, lo]
+constexpr uint32_t kOffS = kOffVt + 2 * kTileV;                // S[buf][hi, lo]
 constexpr uint32_t kOffG = kOffS + 4 * kTileS;                 // gate rows [warp][64]
-constexpr uint32_t kOffBar = kOffG + (kThreads / 32) * kC * 4;
+constexpr uint32_t kOffBar = kOffG + (kThreads / 32) * 2 * kC * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // TMEM columns per accumulator buffer (two buffers of 256 columns).
 constexpr uint32_t kTmCols = 512;
@@ -81,68 +83,12 @@ struct GlaParams {
 
 struct Bars {
   uint64_t full[kStages], empty[kStages];
-  uint64_t qk_ready[2], qk_free[2], p_ready[2], p_free[2];
+  uint64_t qk_ready[2], qk_free[2], p_ready[2], p_free;
   uint64_t ds_ready[2], o_ready[2], o_free[2], s_ready[2];
   uint32_t tmem_base;
   int abort;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
-
-// Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      return false;
-    }
-  }
-}
-
-// Warp-uniform version for warps that go on to warp-collective tcgen05.ld.
-__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort) {
-  const bool ok = wait_bar(bar, parity, abort);
-  return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk16) {
-  return row * 128u + ((chunk16 ^ (row & 7u)) << 4);
-}
-
-// 8 fp32 -> bf16 high parts and bf16 remainders, packed as 16 bytes each.
-__device__ __forceinline__ uint32_t bits(__nv_bfloat162 v) {
-  uint32_t u;
-  memcpy(&u, &v, 4);
-  return u;
-}
-
-__device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * k], x[2 * k + 1]);
-    const float2 hf = __bfloat1622float2(hb);
-    h[k] = bits(hb);
-    l[k] = bits(__floats2bfloat162_rn(x[2 * k] - hf.x, x[2 * k + 1] - hf.y));
-  }
-  hi = make_uint4(h[0], h[1], h[2], h[3]);
-  lo = make_uint4(l[0], l[1], l[2], l[3]);
-}
-
-__device__ __forceinline__ void unpack8(const uint4 &u, float *x) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    __nv_bfloat162 b;
-    memcpy(&b, &w[k], 4);
-    const float2 f = __bfloat1622float2(b);
-    x[2 * k] = f.x;
-    x[2 * k + 1] = f.y;
-  }
-}
 
 // Per-chunk gates of one warp: g2 = cumsum(log2 alpha) over the chunk's 64
 // tokens (2 per lane, alpha = 1 past the end of the sequence), published in
@@ -185,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Bars *bars = reinterpret_cast<Bars *>(smem + kOffBar);
-  float *s_g = reinterpret_cast<float *>(smem + kOffG);  // [warp][64] per-warp gate rows
+  float *s_g = reinterpret_cast<float *>(smem + kOffG);  // [warp][2][64] gate rows
   volatile int *abort = &bars->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -216,12 +162,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->qk_ready[i], 1);
       mbar_init(&bars->ds_ready[i], 1);
       mbar_init(&bars->o_ready[i], 1);
-      mbar_init(&bars->p_free[i], 1);
       mbar_init(&bars->qk_free[i], kEpiThreads);
       mbar_init(&bars->p_ready[i], kEpiThreads);
       mbar_init(&bars->o_free[i], kEpiThreads);
       mbar_init(&bars->s_ready[i], kEpiThreads);
     }
+    mbar_init(&bars->p_free, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -293,8 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dcol = tmem + tb * 256;
         // descriptors built once; the k-steps only move the start-address field
         const uint64_t dKm = desc_sw128(aK, kTileK / 2, 1024);
-        const uint64_t dVt = desc_sw128(sbase + kOffVt + tb * 2 * kTileV, 16, 1024);
-        const uint64_t dP = desc_sw128(sbase + kOffP + tb * 2 * kTileP, 16, 1024);
+        const uint64_t dVt = desc_sw128(sbase + kOffVt, 16, 1024);
+        const uint64_t dP = desc_sw128(sbase + kOffP, 16, 1024);
         const uint64_t dV = desc_sw128(aV, 16, 1024);
         const uint64_t dQ = desc_sw128(aQ, 16, 1024);
         // dS = K^T (V~hi + V~lo): M = d_k (K tile read M-major), N = 64, K = 64 tokens
@@ -312,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ks = 0; ks < 4; ++ks)
             umma_bf16(dcol + kColO2, dP + ((part * kTileP + ks * 32) >> 4), dV + ((ks * 2048) >> 4),
                       id_pv, (part | ks) != 0);
+        umma_commit(&bars->p_free);  // P and V~ may be rewritten once these are done
         const int sb = c & 1;
         if (!wait_bar(&bars->s_ready[sb], ph, abort)) break;
         tc_fence_after();
@@ -326,7 +273,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (part | ks) != 0);
           }
         umma_commit(&bars->o_ready[tb]);
-        umma_commit(&bars->p_free[tb]);
         umma_commit(&bars->empty[s]);
       }
     }
@@ -337,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool has_tok = lane < 16;       // holds a token row of the M = 64 tiles
     const int tok = 16 * q4 + lane;       // that token row (valid when has_tok)
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-    float *grow = s_g + warp * kC;
+    float *grow = s_g + warp * 2 * kC;
     Gates G;
     gates_prefetch(G, p, b, h, 0, lane);
     for (int c = 0; c < nchunks; ++c) {
@@ -361,43 +307,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&bars->qk_free[tb]);
-      if (!wait_bar_warp(&bars->p_free[tb], ph ^ 1u, abort)) break;
+      if (!wait_bar_warp(&bars->p_free, ((uint32_t)c & 1u) ^ 1u, abort)) break;
+      // D_ij = 2^(g_i - g_j).  When the chunk's total decay is moderate the
+      // factors 2^g_i and 2^-g_j cannot overflow and D is their product (one
+      // exp2 per token instead of one per pair); otherwise pairwise exp2.
+      const bool factored = gC > -100.f;  // warp-uniform
+      float *cfrow = grow + kC;           // 2^-g_j of this chunk
+      if (factored) {
+        cfrow[2 * lane] = exp2f(-grow[2 * lane]);
+        cfrow[2 * lane + 1] = exp2f(-grow[2 * lane + 1]);
+      }
+      __syncwarp();
       if (has_tok) {
-        uint8_t *phi = smem + kOffP + tb * 2 * kTileP;
-        uint8_t *plo = phi + kTileP;
+        const uint32_t phi = smem_u32(smem + kOffP);
+        const uint32_t plo = phi + kTileP;
         const float gi = grow[tok];
+        if (factored) {
+          const float rf = exp2f(gi);
+#pragma unroll
+          for (int j = 0; j < kC; ++j) qk[j] = (j <= tok) ? qk[j] * rf * cfrow[j] : 0.f;
+        } else {
+#pragma unroll
+          for (int j = 0; j < kC; ++j) qk[j] = (j <= tok) ? qk[j] * exp2f(gi - grow[j]) : 0.f;
+        }
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
-          float pv[8];
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int j = 8 * ch + jj;
-            pv[jj] = (j <= tok) ? qk[j] * exp2f(gi - grow[j]) : 0.f;
-          }
           uint4 uh, ul;
-          split8(pv, uh, ul);
-          *reinterpret_cast<uint4 *>(phi + swz(tok, ch)) = uh;
-          *reinterpret_cast<uint4 *>(plo + swz(tok, ch)) = ul;
+          split8(&qk[8 * ch], uh, ul);
+          sts128(phi + swz(tok, ch), uh);
+          sts128(plo + swz(tok, ch), ul);
         }
       }
       if (!wait_bar_warp(&bars->full[s], sph, abort)) break;
       {
-        const uint8_t *vt = smem + kOffStage + s * kStageBytes + kTileQ + kTileK;
-        uint8_t *vhi = smem + kOffVt + tb * 2 * kTileV;
-        uint8_t *vlo = vhi + kTileV;
+        const uint32_t vt = smem_u32(smem + kOffStage + s * kStageBytes + kTileQ + kTileK);
+        const uint32_t vhi = smem_u32(smem + kOffVt);
+        const uint32_t vlo = vhi + kTileV;
         const int t = e >> 1, half = e & 1;
         const float r = exp2f(gC - grow[t]);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t ch = 4 * half + k;
           float x[8];
-          unpack8(*reinterpret_cast<const uint4 *>(vt + swz(t, ch)), x);
+          unpack8(lds128(vt + swz(t, ch)), x);
 #pragma unroll
           for (int i = 0; i < 8; ++i) x[i] *= r;
           uint4 uh, ul;
           split8(x, uh, ul);
-          *reinterpret_cast<uint4 *>(vhi + swz(t, ch)) = uh;
-          *reinterpret_cast<uint4 *>(vlo + swz(t, ch)) = ul;
+          sts128(vhi + swz(t, ch), uh);
+          sts128(vlo + swz(t, ch), ul);
         }
       }
       fence_proxy_async_smem();
@@ -410,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool has_tok = lane < 16;
     const int tok = 16 * q4 + lane;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-    float *grow = s_g + warp * kC;
+    float *grow = s_g + warp * 2 * kC;
     Gates G;
     gates_prefetch(G, p, b, h, 0, lane);
 
@@ -425,14 +383,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     auto write_state = [&](int sb) {
-      uint8_t *hi = smem + kOffS + sb * 2 * kTileS;
-      uint8_t *lo = hi + kTileS;
+      const uint32_t hi = smem_u32(smem + kOffS + sb * 2 * kTileS);
+      const uint32_t lo = hi + kTileS;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {
         uint4 uh, ul;
         split8(&S[8 * ch], uh, ul);
-        *reinterpret_cast<uint4 *>(hi + swz(srow, ch)) = uh;
-        *reinterpret_cast<uint4 *>(lo + swz(srow, ch)) = ul;
+        sts128(hi + swz(srow, ch), uh);
+        sts128(lo + swz(srow, ch), ul);
       }
       fence_proxy_async_smem();
       mbar_arrive(&bars->s_ready[sb]);
@@ -552,6 +510,19 @@ bool make_act_map(CUtensorMap *m, const void *base, int B, int T, int H, int d) 
 }
 
 }  // namespace
+
+bool encode_rows_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, int elem_bytes,
+                     int inner, int rows, int planes, int box_inner, bool swizzle) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)planes};
+  const cuuint64_t strides[2] = {(cuuint64_t)inner * elem_bytes, (cuuint64_t)rows * inner * elem_bytes};
+  const cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)kC, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, type, 3, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool prefill_tc_available() { return encode_fn() != nullptr; }
 

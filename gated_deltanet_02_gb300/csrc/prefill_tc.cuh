@@ -1,7 +1,9 @@
 // prefill_tc.cuh -- tensor-core (tcgen05 / TMEM / TMA) chunked prefill.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 
 #include "glinattn.h"
 
@@ -15,5 +17,15 @@ bool prefill_tc_supports(const glinattn_prefill_args &a);
 
 // bf16 activations, dk == dv == 128, chunk 64.  Arguments already validated.
 glinattn_status launch_prefill_tc(const glinattn_prefill_args &a, cudaStream_t stream);
+
+// Chunked Gated DeltaNet (two passes through a caller-provided workspace).
+bool gdn_tc_supports(const glinattn_prefill_args &a);
+size_t gdn_tc_workspace_bytes(const glinattn_prefill_args &a);
+glinattn_status launch_gdn_tc(const glinattn_prefill_args &a, cudaStream_t stream);
+
+// 3-D tiled map over rows of `inner` elements: dims (inner, rows, planes),
+// box (box_inner, 64, 1); 128-byte swizzle when `swizzle` is set.
+bool encode_rows_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, int elem_bytes,
+                     int inner, int rows, int planes, int box_inner, bool swizzle);
 
 }  // namespace glinattn

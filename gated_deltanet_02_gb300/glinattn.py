@@ -46,7 +46,7 @@ class PrefillArgs(ctypes.Structure):
                 ("reserved0", _i32),
                 ("q", _vp), ("k", _vp), ("v", _vp), ("alpha", _vp), ("beta", _vp), ("S0", _vp),
                 ("S_T", _vp), ("o", _vp), ("conv_w", _vp), ("conv_in", _vp), ("conv_out", _vp),
-                ("dev_status", _vp)]
+                ("dev_status", _vp), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class DecodeArgs(ctypes.Structure):
@@ -88,6 +88,8 @@ def library() -> ctypes.CDLL:
             lib.glinattn_version.restype = ctypes.c_int
             lib.glinattn_state_bytes.argtypes = [ctypes.c_int] * 3
             lib.glinattn_state_bytes.restype = ctypes.c_size_t
+            lib.glinattn_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs)]
+            lib.glinattn_prefill_workspace_size.restype = ctypes.c_size_t
             _lib = lib
     return _lib
 
@@ -131,10 +133,11 @@ def _call(name, args, stream_handle):
 
 def glinattn_prefill(q, k, v, alpha, beta=None, S0=None, *, variant=GLA, conv_w=None,
                      conv_in=None, qk_l2norm=False, out_dtype=None, o=None, S_T=None,
-                     conv_out=None, dev_status=None, stream=None):
+                     conv_out=None, dev_status=None, stream=None, workspace=None):
     """Prefill one segment.  q, k [B,T,H,dk], v [B,T,H,dv] (bf16 or fp32);
-    alpha/beta [B,T,H] fp32; S0 [B,H,dk,dv] fp32 or None.  Outputs are
-    allocated when not given.  Returns (o, S_T, conv_out)."""
+    alpha/beta [B,T,H] fp32; S0 [B,H,dk,dv] fp32 or None.  Outputs, and the
+    scratch space the chunked Gated DeltaNet kernels need, are allocated when
+    not given.  Returns (o, S_T, conv_out)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     dev = q.device
@@ -164,6 +167,15 @@ def glinattn_prefill(q, k, v, alpha, beta=None, S0=None, *, variant=GLA, conv_w=
                     q=_ptr(q), k=_ptr(k), v=_ptr(v), alpha=_ptr(alpha), beta=_ptr(beta),
                     S0=_ptr(S0), S_T=_ptr(S_T), o=_ptr(o), conv_w=_ptr(conv_w),
                     conv_in=_ptr(conv_in), conv_out=_ptr(conv_out), dev_status=_ptr(dev_status))
+    ws_bytes = library().glinattn_prefill_workspace_size(ctypes.byref(a))
+    ws = None
+    if ws_bytes:
+        if workspace is not None and workspace.numel() * workspace.element_size() >= ws_bytes:
+            ws = workspace
+        else:
+            ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        a.workspace = _ptr(ws)
+        a.workspace_bytes = ws_bytes
     _call("glinattn_prefill", a, _stream_handle(stream, dev))
     return o, S_T, conv_out
 
@@ -251,3 +263,9 @@ def status_string(code: int) -> str:
 
 def state_bytes(heads: int, dk: int, dv: int) -> int:
     return library().glinattn_state_bytes(heads, dk, dv)
+
+
+def prefill_workspace_size(batch, seqlen, heads, d, variant=GDN, in_dtype=BF16, out_dtype=F32) -> int:
+    a = PrefillArgs(variant=variant, in_dtype=in_dtype, out_dtype=out_dtype, batch=batch,
+                    seqlen=seqlen, heads=heads, dk=d, dv=d)
+    return library().glinattn_prefill_workspace_size(ctypes.byref(a))

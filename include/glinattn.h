@@ -19,7 +19,8 @@
  *   - All tensor arguments are DEVICE pointers to caller-owned memory,
  *     contiguous row-major in the layout stated (innermost index last), with
  *     the base address 16-byte aligned.  The library keeps no pointer after
- *     the call returns and allocates no device memory.
+ *     the call returns and allocates no device memory; scratch space, where a
+ *     kernel needs it, is passed in by the caller (glinattn_prefill_workspace_size).
  *   - Calls are asynchronous on the given stream (0 = legacy default stream).
  *     Argument errors are detected on the host before anything is launched and
  *     returned as a status; the output buffers are then untouched.
@@ -86,8 +87,9 @@ typedef enum { GLINATTN_F32 = 0, GLINATTN_BF16 = 1 } glinattn_dtype;
  *   T may be any value >= 0 (a ragged last chunk is handled); T == 0 copies
  *   S0 to S_T and conv_in to conv_out.
  *   bf16 activations with dk == dv == 128 run the tensor-core chunked kernels
- *   (chunk 64); every other supported combination runs the fp32 token-serial
- *   kernel, which is exact to fp32 rounding but not fast.
+ *   (chunk 64; Gated DeltaNet also needs `workspace`, see below, else
+ *   GLINATTN_ERR_INVALID_ARG); every other supported combination runs the
+ *   fp32 token-serial kernel, which is exact to fp32 rounding but not fast.
  */
 typedef struct {
   int32_t variant;   /* glinattn_variant */
@@ -105,9 +107,23 @@ typedef struct {
   const void *conv_in;
   void *conv_out;
   uint32_t *dev_status;
+  void *workspace;        /* device scratch, >= glinattn_prefill_workspace_size() bytes */
+  size_t workspace_bytes; /* its size; may be 0 when the size query returns 0 */
 } glinattn_prefill_args;
 
 glinattn_status glinattn_prefill(const glinattn_prefill_args *args, glinattn_stream_t stream);
+
+/*
+ * glinattn_prefill_workspace_size -- bytes of device scratch the call needs
+ *   for these arguments (only sizes, variant and dtypes are read).  The
+ *   chunked Gated DeltaNet kernels run in two passes: a parallel pass over all
+ *   chunks stores the front-end outputs q', k', the state-independent chunk
+ *   products W = (I+A)^-1 diag(beta gamma) K' and U~ = (I+A)^-1 diag(beta) V'
+ *   and the gates there, about 1.3 KB per (batch, head, token); the serial
+ *   pass reads them.  Every other configuration needs 0 bytes.  The caller
+ *   owns the buffer; calls on one stream may reuse it.
+ */
+size_t glinattn_prefill_workspace_size(const glinattn_prefill_args *args);
 
 /*
  * glinattn_decode -- one recurrent decode step for N requests.
