@@ -126,6 +126,35 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *args, glinattn_str
 size_t glinattn_prefill_workspace_size(const glinattn_prefill_args *args);
 
 /*
+ * glinattn_prefill_static_scratch -- glinattn_prefill for callers that cannot
+ *   allocate device memory.  The source pages have no counterpart: this is a
+ *   deployment interface, not part of the method.  A serving engine that plans
+ *   all of its device memory up front (the paged KV pool and the per-request
+ *   state pool, sized together against the request-length mix) has no spare
+ *   buffer to pass as `workspace` and does not let a library call cudaMalloc;
+ *   this entry point takes its scratch from a fixed 32 MiB array in the
+ *   library's device image instead.
+ *
+ *   - args->workspace and args->workspace_bytes are ignored; every other field
+ *     means what it means for glinattn_prefill, with the same validation and
+ *     the same results.
+ *   - A call whose glinattn_prefill_workspace_size() exceeds 32 MiB (about
+ *     26,000 batch x head x token positions of chunked Gated DeltaNet prefill)
+ *     returns GLINATTN_ERR_UNSUPPORTED and launches nothing.
+ *   - It calls no cudaMalloc or cudaFree.  The array exists once per GPU that
+ *     loads the library and stays allocated until the process exits.  The
+ *     first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress, with the device current); make that first
+ *     call before any stream capture.
+ *   - Every call shares the one array, which keeps the previous call's
+ *     contents (the kernels overwrite every byte they read, so nothing needs
+ *     clearing).  Calls that may overlap on the GPU -- on different streams,
+ *     or from different host threads -- race on it: serialise them.
+ */
+glinattn_status glinattn_prefill_static_scratch(const glinattn_prefill_args *args,
+                                                glinattn_stream_t stream);
+
+/*
  * glinattn_decode -- one recurrent decode step for N requests.
  *   For request n with slot s = slot_ids[n]: runs the conv step against
  *   conv_pool[s] (then shifts it), reads state_pool[s], applies one rank-one
