@@ -276,6 +276,9 @@ def run_ours(args):
     gdn_ms, gdn_per = timed_steps(step_gdn, max(2, min(args.steps, 5)), 1, dist, dev)
     gdn_bytes, gdn_flops = gdn_bytes_flops(**g)
 
+    # ---- long context: 3-segment prefill, then 64 x 4 speculative decode -------------
+    lc = long_context_run(args, dist, dev, rank)
+
     # ---- CPU baseline: the oracle on this host's cores (rank 0) -----------------------
     cpu = cpu_baseline_run(ex, budget_s=args.cpu_seconds) if rank == 0 and not args.no_cpu else None
 
@@ -328,11 +331,71 @@ def run_ours(args):
                                      "peak": hbm, "unit": "GB/s",
                                      "frac": gdn_bytes / (statistics.mean(gdn_per) / 1e3) / 1e9 / hbm},
                         "tensor_frac": gdn_flops / (statistics.mean(gdn_per) / 1e3) / 1e12 / tc},
+        "long_context": lc,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
+
+
+def long_context_run(args, dist, dev, rank):
+    """Gated DeltaNet, B=1, H=32, T=32768 prefilled as segments of 6553 / 11468
+    / 14747 tokens (state and conv cache handed on), then 64 requests each
+    decoding 4 draft tokens from their own copy of the state, one state kept
+    per draft position."""
+    import torch
+
+    from gated_deltanet_02_gb300 import GDN, glinattn_prefill, glinattn_spec_decode, inputs
+    pk, _ = peaks()
+    B, H, T, d = 1, 32, 32768, 128
+    ex = inputs.gdn_prefill(B, H, T, d, seed=rank, device=dev, s0_std=0.0)
+    segs = inputs.segment_lengths(T)
+    parts, s0 = [], 0
+    for L in segs:
+        sl = slice(s0, s0 + L)
+        parts.append({k: ex[k][:, sl].contiguous() for k in ("q", "k", "v", "alpha", "beta")})
+        s0 += L
+    outs = [torch.empty(B, L, H, d, dtype=torch.bfloat16, device=dev) for L in segs]
+    S = torch.empty(B, H, d, d, device=dev)
+    conv = [torch.empty(B, 3, 3 * H * d, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    from gated_deltanet_02_gb300.glinattn import prefill_workspace_size
+    ws = torch.empty(prefill_workspace_size(B, max(segs), H, d), dtype=torch.uint8, device=dev)
+
+    def step_prefill():
+        for i, part in enumerate(parts):
+            glinattn_prefill(part["q"], part["k"], part["v"], part["alpha"], part["beta"],
+                             None if i == 0 else S, variant=GDN, conv_w=ex["conv_w"],
+                             conv_in=None if i == 0 else conv[(i - 1) % 2], conv_out=conv[i % 2],
+                             qk_l2norm=True, o=outs[i], S_T=S, workspace=ws)
+
+    pre_ms, _ = timed_steps(step_prefill, 2, 1, dist, dev)
+    N, D = 64, 4
+    P = N * (1 + D)
+    pool = torch.zeros(P, H, d, d, device=dev)
+    cpool = torch.zeros(P, 3, 3 * H * d, dtype=torch.bfloat16, device=dev)
+    pool[:N] = S[0]
+    cpool[:N] = conv[(len(segs) - 1) % 2][0]
+    src = torch.arange(N, dtype=torch.int32, device=dev)
+    dst = (N + torch.arange(N * D, dtype=torch.int32, device=dev)).view(N, D)
+    dr = inputs.spec_drafts(N, D, H, d, seed=rank + 1, device=dev)
+    od = torch.empty(N, D, H, d, dtype=torch.bfloat16, device=dev)
+
+    def step_spec():
+        glinattn_spec_decode(dr["q"], dr["k"], dr["v"], dr["alpha"], dr["beta"], pool, src, dst,
+                             variant=GDN, conv_w=ex["conv_w"], conv_pool=cpool, qk_l2norm=True, o=od)
+
+    spec_ms, spec_per = timed_steps(step_spec, max(10, args.steps), 3, dist, dev)
+    spec_bytes = N * H * (1 + D) * d * d * 4
+    k_ms = statistics.mean(spec_per)
+    return {"config": "Gated DeltaNet, B=1 H=32 T=32768 in segments 6553/11468/14747 (conv + L2 norm), "
+                      "then 64 requests x 4 draft tokens, one fp32 state per draft position",
+            "prefill_tokens_per_s": T / (pre_ms / 1e3), "prefill_ms": pre_ms,
+            "spec_draft_tokens_per_s": N * D / (spec_ms / 1e3), "spec_ms_per_round": spec_ms,
+            "spec_roofline": {"bound": "hbm", "achieved": spec_bytes / (k_ms / 1e3) / 1e9,
+                              "peak": pk["hbm_gbs"], "unit": "GB/s",
+                              "frac": spec_bytes / (k_ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                              "algorithmic_bytes": spec_bytes}}
 
 
 # ----------------------------------------------------------------------------
