@@ -511,6 +511,19 @@ bool make_act_map(CUtensorMap *m, const void *base, int B, int T, int H, int d) 
 
 }  // namespace
 
+bool encode_3d_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, int elem_bytes,
+                   const long long dims[3], const int box[3], bool swizzle) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t gd[3] = {(cuuint64_t)dims[0], (cuuint64_t)dims[1], (cuuint64_t)dims[2]};
+  const cuuint64_t st[2] = {(cuuint64_t)dims[0] * elem_bytes, (cuuint64_t)dims[0] * dims[1] * elem_bytes};
+  const cuuint32_t bx[3] = {(cuuint32_t)box[0], (cuuint32_t)box[1], (cuuint32_t)box[2]};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, type, 3, const_cast<void *>(base), gd, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_rows_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, int elem_bytes,
                      int inner, int rows, int planes, int box_inner, bool swizzle) {
   EncodeTiledFn enc = encode_fn();

@@ -23,6 +23,10 @@ bool gdn_tc_supports(const glinattn_prefill_args &a);
 size_t gdn_tc_workspace_bytes(const glinattn_prefill_args &a);
 glinattn_status launch_gdn_tc(const glinattn_prefill_args &a, cudaStream_t stream);
 
+// General 3-D tiled map: dims (innermost first) and box in elements.
+bool encode_3d_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, int elem_bytes,
+                   const long long dims[3], const int box[3], bool swizzle);
+
 // 3-D tiled map over rows of `inner` elements: dims (inner, rows, planes),
 // box (box_inner, 64, 1); 128-byte swizzle when `swizzle` is set.
 bool encode_rows_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, int elem_bytes,

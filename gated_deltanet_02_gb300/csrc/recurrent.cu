@@ -13,19 +13,23 @@
 // and PD disaggregation": one state is kept per draft position, and batched
 // kernels read and write the state pool by slot index.
 //
-// One CTA owns one (request, head) state, d x d fp32.  Its source is fetched
-// into shared memory by a single bulk copy (cp.async.bulk) issued as soon as
-// the slot id is known, so the copy engine moves the 64 KiB while the threads
-// run the front end (short convolution, L2 norm); registers stay low enough
-// for two CTAs per SM, i.e. two states in flight per SM besides the stores.
-// Thread (rg, cg) owns rows rg + ROWG*i of column group cg (4 consecutive
-// columns, one 16-byte vector), so every warp-wide access to a state row is
-// contiguous, in shared and in global memory.  k S and q S are reduced in one
-// pass, across row groups through shared memory in a fixed order
-// (deterministic, no atomics).  Decode (1 step, in place) and speculative
-// decode (D steps, a write after each) run this same code, so a draft state
-// equals the state of repeated decode steps bit for bit.
+// The columns of S evolve independently (both updates left-multiply S by a
+// matrix of k, alpha, beta only), so one CTA owns one column slice of one
+// (request, head) state: the 128 x 64 half for d = 128, the whole state for
+// smaller heads.  The slice is fetched into shared memory by one TMA tile
+// load issued as soon as the slot id is known, while the threads run the
+// front end (short convolution, L2 norm); each CTA needs 44 KB of shared
+// memory at d = 128, so five slices per SM are in flight.  Thread (rg, cg)
+// owns rows rg + ROWG*i of column group cg (4 consecutive columns, one
+// 16-byte vector): every warp access to a state row is contiguous.  k S and
+// q S are reduced in one pass, across row groups through shared memory in a
+// fixed order (deterministic, no atomics).  Decode (1 step, in place) and
+// speculative decode (D steps, a write after each) run this same code, so a
+// draft state equals the state of repeated decode steps bit for bit.
+#include <string.h>
+
 #include "common.cuh"
+#include "prefill_tc.cuh"
 #include "sm100.cuh"
 
 namespace glinattn {
@@ -35,10 +39,13 @@ using namespace sm100;
 
 template <int D>
 struct Shape {
-  static constexpr int NT = (D * D / 4 < 256) ? D * D / 4 : 256;  // threads per CTA
-  static constexpr int COLG = D / 4;                               // 16-byte column groups
-  static constexpr int ROWG = NT / COLG;                           // row groups
-  static constexpr int RPT = D / ROWG;                             // rows per thread
+  static constexpr int NSPLIT = D == 128 ? 2 : 1;  // column slices per state
+  static constexpr int DC = D / NSPLIT;             // columns per CTA
+  static constexpr int NT = D == 128 ? 128 : ((D * D / 4 < 256) ? D * D / 4 : 256);
+  static constexpr int COLG = DC / 4;               // 16-byte column groups
+  static constexpr int ROWG = NT / COLG;            // row groups
+  static constexpr int RPT = D / ROWG;              // rows per thread
+  static constexpr int NCH = 2 * D + DC;            // front-end channels: q, k, own v slice
   static_assert(RPT >= 1 && ROWG * RPT == D, "shape");
 };
 
@@ -65,52 +72,86 @@ __device__ __forceinline__ float warp_sum(float x) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurParams p) {
+__global__ void __launch_bounds__(Shape<D>::NT)
+    recurrent_kernel(const __grid_constant__ CUtensorMap tstate, const RecurParams p) {
   using Sh = Shape<D>;
   constexpr int NW = (Sh::NT + 31) / 32;
-  constexpr uint32_t kStateBytes = D * D * 4;
-  const int unit = blockIdx.x;
+  constexpr int NCH = Sh::NCH;
+  constexpr int MAXC = (NCH + Sh::NT - 1) / Sh::NT;  // front-end channels per thread
+  constexpr uint32_t kSliceBytes = D * Sh::DC * 4;
+  const int half = blockIdx.x % Sh::NSPLIT;
+  const int unit = blockIdx.x / Sh::NSPLIT;
   const int n = unit / p.H, h = unit - n * p.H;
   const int tid = threadIdx.x;
   const int cg = tid % Sh::COLG, rg = tid / Sh::COLG;
+  const int col0 = half * Sh::DC;  // first state column of this CTA
   const size_t DD = (size_t)D * D;
 
-  extern __shared__ __align__(128) float4 s_state4[];  // the d x d state, row-major
-  __shared__ float s_act[3 * D];                        // q | k | v after the front end
-  __shared__ float s_raw[3 * D];                        // raw inputs of the current token
-  __shared__ float s_hist[3][3 * D];                    // conv history, oldest first
-  __shared__ float s_red[Sh::ROWG][2][D];
+  extern __shared__ __align__(128) float4 s_state4[];  // D rows x DC columns, row-major
+  __shared__ float s_act[NCH];                          // q | k | own v slice after the front end
+  __shared__ float s_red[Sh::ROWG][2][Sh::DC];
   __shared__ float s_wsum[2][NW];
   __shared__ float s_qk;
-  __shared__ int s_bad, s_has_src;
+  __shared__ int s_bad;
   __shared__ __align__(8) uint64_t s_bar;
 
-  // ---- thread 0 checks the source slot and starts the state copy at once ----
+  // global channel of local front-end channel c: q (0..D-1), k (D..2D-1), own v slice
+  auto chan = [&](int c) {
+    if (c < 2 * D) return (c / D) * p.H * D + h * D + (c % D);
+    return 2 * p.H * D + h * D + col0 + (c - 2 * D);
+  };
+  // input element of local channel c for token row `row` (index of (n, t, h))
+  auto act_at = [&](int c, size_t row) {
+    const void *src = c < D ? p.q : (c < 2 * D ? p.k : p.v);
+    const int i = c < 2 * D ? (c % D) : col0 + (c - 2 * D);
+    return load_act(src, row * D + i, p.in_bf16);
+  };
+  // conv-cache channels written by this CTA: q and k by slice 0, each v slice by its owner
+  auto writes_chan = [&](int c) { return c >= 2 * D || half == 0; };
+
+  // ---- every independent load is issued first ----------------------------------
+  int slot = n;
+  bool slot_ok = true;
+  if (p.src_slot) {
+    slot = p.src_slot[n];
+    slot_ok = !(p.pool_slots > 0 && (slot < 0 || slot >= p.pool_slots));
+  }
+  const bool has_src = p.S_src != nullptr && slot_ok;
   if (tid == 0) {
-    int bad0 = 0;
-    const float *src = nullptr;
-    if (p.S_src) {
-      size_t slot = (size_t)n;
-      if (p.src_slot) {
-        const int s = p.src_slot[n];
-        if (p.pool_slots > 0 && (s < 0 || s >= p.pool_slots)) bad0 = GLINATTN_DEV_BAD_SLOT;
-        slot = (size_t)s;
-      }
-      if (!bad0) src = p.S_src + (slot * p.H + h) * DD;
-    }
     mbar_init(&s_bar, 1);
     fence_mbar_init();
-    if (src) {
-      mbar_arrive_expect_tx(&s_bar, kStateBytes);
-      bulk_load(s_state4, src, kStateBytes, &s_bar);
+    if (has_src) {
+      mbar_arrive_expect_tx(&s_bar, kSliceBytes);
+      tma_load_3d(s_state4, &tstate, &s_bar, col0, 0, slot * p.H + h);
     }
-    s_bad = bad0;
-    s_has_src = src != nullptr;
+    s_bad = 0;
   }
-  __syncthreads();
-
-  // ---- the rest of the unit validation: destination slots, gates in (0, 1] --
-  int bad = 0;
+  const bool conv = p.conv_w != nullptr;
+  float xr[MAXC], wr[MAXC][4], hr[MAXC][3];
+  {
+    const size_t row0 = ((size_t)n * p.steps) * p.H + h;
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+      const int c = tid + i * Sh::NT;
+      xr[i] = 0.f;
+      wr[i][0] = wr[i][1] = wr[i][2] = 0.f;
+      wr[i][3] = 1.f;
+      hr[i][0] = hr[i][1] = hr[i][2] = 0.f;
+      if (c < NCH) {
+        if (p.steps > 0) xr[i] = act_at(c, row0);
+        if (conv) {
+          const float4 w = *reinterpret_cast<const float4 *>(p.conv_w + (size_t)chan(c) * 4);
+          wr[i][0] = w.x; wr[i][1] = w.y; wr[i][2] = w.z; wr[i][3] = w.w;
+          if (p.conv_src && slot_ok)
+#pragma unroll
+            for (int j = 0; j < 3; ++j)
+              hr[i][j] = load_act(p.conv_src, ((size_t)slot * 3 + j) * p.Cch + chan(c), p.in_bf16);
+        }
+      }
+    }
+  }
+  // ---- unit validation: slots in range, gates in (0, 1] --------------------------
+  int bad = slot_ok ? 0 : GLINATTN_DEV_BAD_SLOT;
   if (p.pool_slots > 0 && p.dst_slot) {
     const int nd = p.dst_per_step ? p.steps : 1;
     for (int t = tid; t < nd; t += Sh::NT) {
@@ -122,12 +163,12 @@ __global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurPara
     const float a = p.alpha[((size_t)n * p.steps + t) * p.H + h];
     if (!(a > 0.f && a <= 1.f)) bad |= GLINATTN_DEV_BAD_GATE;
   }
+  __syncthreads();  // s_bad initialised, barrier initialised
   if (bad) atomicOr(&s_bad, bad);
   __syncthreads();
-  const bool has_src = s_has_src != 0;
   if (s_bad) {
     if (has_src) mbar_wait(&s_bar, 0);  // let the copy land before the CTA exits
-    if (tid == 0 && p.dev_status) atomicOr(p.dev_status, (uint32_t)s_bad);
+    if (tid == 0 && half == 0 && p.dev_status) atomicOr(p.dev_status, (uint32_t)s_bad);
     return;
   }
   if (!has_src) {
@@ -135,51 +176,38 @@ __global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurPara
     for (int i = 0; i < Sh::RPT; ++i)
       s_state4[(rg + Sh::ROWG * i) * Sh::COLG + cg] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-
-  // channel of this head for local channel c = part * D + i
-  auto chan = [&](int c) { return (c / D) * p.H * D + h * D + (c % D); };
-
-  // ---- conv history ----------------------------------------------------------
-  const bool conv = p.conv_w != nullptr;
-  if (conv) {
-    const size_t cslot = p.src_slot ? (size_t)p.src_slot[n] : (size_t)n;
-    for (int c = tid; c < 3 * D; c += Sh::NT)
-#pragma unroll
-      for (int j = 0; j < 3; ++j)
-        s_hist[j][c] = p.conv_src ? load_act(p.conv_src, (cslot * 3 + j) * p.Cch + chan(c), p.in_bf16)
-                                  : 0.f;
-  }
+  // The slices of one state share the q / k conv history, and slice 0 writes it
+  // back (in place for decode): every slice has read it before any writes it.
+  bool history_released = Sh::NSPLIT == 1;
+  auto release_history = [&]() {
+    if (!history_released) {
+      cluster_wait();
+      history_released = true;
+    }
+  };
+  if (Sh::NSPLIT > 1) cluster_arrive();
 
   for (int t = 0; t < p.steps; ++t) {
     const size_t row = ((size_t)n * p.steps + t) * p.H + h;  // (n, t, h)
-    // ---- front end: conv, L2 norm, bf16 rounding --------------------------------
-    for (int c = tid; c < 3 * D; c += Sh::NT) {
-      const int part = c / D, i = c % D;
-      const void *src = part == 0 ? p.q : (part == 1 ? p.k : p.v);
-      const float x = load_act(src, row * D + i, p.in_bf16);
-      float y = x;
-      if (conv) {
-        const float *w = p.conv_w + (size_t)chan(c) * 4;
-        y = w[0] * s_hist[0][c] + w[1] * s_hist[1][c] + w[2] * s_hist[2][c] + w[3] * x;
-      }
-      s_raw[c] = x;
-      s_act[c] = y;
+    // ---- front end in registers: conv, history shift, next token prefetch -------
+    float yv[MAXC];
+    float sq = 0.f, sk = 0.f;
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+      const int c = tid + i * Sh::NT;
+      const float x = xr[i];
+      const float y = conv ? wr[i][0] * hr[i][0] + wr[i][1] * hr[i][1] + wr[i][2] * hr[i][2] + wr[i][3] * x
+                           : x;
+      yv[i] = y;
+      if (c < D) sq += y * y;
+      else if (c < 2 * D) sk += y * y;
+      hr[i][0] = hr[i][1];
+      hr[i][1] = hr[i][2];
+      hr[i][2] = x;
+      if (c < NCH && t + 1 < p.steps) xr[i] = act_at(c, row + p.H);
     }
-    __syncthreads();
-    if (conv) {
-      for (int c = tid; c < 3 * D; c += Sh::NT) {
-        s_hist[0][c] = s_hist[1][c];
-        s_hist[1][c] = s_hist[2][c];
-        s_hist[2][c] = s_raw[c];
-      }
-    }
+    float iq = 1.f, ik = 1.f;
     if (p.qk_l2norm) {
-      // sum of squares of q (part 0) and k (part 1), fixed order
-      float sq = 0.f, sk = 0.f;
-      for (int i = tid; i < D; i += Sh::NT) {
-        sq += s_act[i] * s_act[i];
-        sk += s_act[D + i] * s_act[D + i];
-      }
       sq = warp_sum(sq);
       sk = warp_sum(sk);
       if ((tid & 31) == 0) {
@@ -193,21 +221,25 @@ __global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurPara
         tq += s_wsum[0][w];
         tk += s_wsum[1][w];
       }
-      const float iq = 1.f / sqrtf(tq + 1e-6f), ik = 1.f / sqrtf(tk + 1e-6f);
-      __syncthreads();  // everyone has read s_wsum before s_act changes
-      for (int i = tid; i < D; i += Sh::NT) {
-        s_act[i] *= iq;
-        s_act[D + i] *= ik;
-      }
+      iq = 1.f / sqrtf(tq + 1e-6f);
+      ik = 1.f / sqrtf(tk + 1e-6f);
     }
-    if (p.in_bf16 && (conv || p.qk_l2norm)) {
-      __syncthreads();
-      for (int c = tid; c < 3 * D; c += Sh::NT) s_act[c] = round_bf16(s_act[c]);
+    const bool round_act = p.in_bf16 && (conv || p.qk_l2norm);
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+      const int c = tid + i * Sh::NT;
+      if (c < NCH) {
+        float y = yv[i];
+        if (c < D) y *= iq;
+        else if (c < 2 * D) y *= ik;
+        s_act[c] = round_act ? round_bf16(y) : y;
+      }
     }
     if (t == 0 && has_src) {  // the state copy must have landed
       const bool ok = mbar_wait(&s_bar, 0);
       if (!__syncthreads_and(ok)) {
         if (tid == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_WAIT_TIMEOUT);
+        release_history();
         return;
       }
     } else {
@@ -221,13 +253,13 @@ __global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurPara
       acc = warp_sum(acc);
       if (tid == 0) s_qk = acc;
     }
-    const float *sq = s_act, *sk = s_act + D, *sv = s_act + 2 * D;
+    const float *sqa = s_act, *ska = s_act + D, *sva = s_act + 2 * D;
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
 #pragma unroll
     for (int i = 0; i < Sh::RPT; ++i) {
       const int r = rg + Sh::ROWG * i;
       const float4 S = s_state4[r * Sh::COLG + cg];
-      const float kr = sk[r], qr = sq[r];
+      const float kr = ska[r], qr = sqa[r];
       x.x += kr * S.x; x.y += kr * S.y; x.z += kr * S.z; x.w += kr * S.w;
       y.x += qr * S.x; y.y += qr * S.y; y.z += qr * S.z; y.w += qr * S.w;
     }
@@ -246,7 +278,7 @@ __global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurPara
 
     // ---- update: shared memory copy for the next step, global copy if due ------
     const float a = p.alpha[row];
-    const float4 vv = *reinterpret_cast<const float4 *>(sv + 4 * cg);
+    const float4 vv = *reinterpret_cast<const float4 *>(sva + 4 * cg);
     float4 u = vv;
     if (p.variant == GLINATTN_GDN) {
       const float b = p.beta[row];
@@ -262,12 +294,12 @@ __global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurPara
     if (emit) {
       if (p.dst_slot)
         dslot = (size_t)p.dst_slot[(size_t)n * (p.dst_per_step ? p.steps : 1) + (p.dst_per_step ? t : 0)];
-      dst = p.S_dst + (dslot * p.H + h) * DD;
+      dst = p.S_dst + (dslot * p.H + h) * DD + col0;
     }
 #pragma unroll
     for (int i = 0; i < Sh::RPT; ++i) {
       const int r = rg + Sh::ROWG * i;
-      const float kr = sk[r];
+      const float kr = ska[r];
       float4 S = s_state4[r * Sh::COLG + cg];
       S.x = a * S.x + kr * u.x;
       S.y = a * S.y + kr * u.y;
@@ -278,52 +310,85 @@ __global__ void __launch_bounds__(Shape<D>::NT) recurrent_kernel(const RecurPara
     }
     if (rg == 0) {
       const float qk = s_qk;
-      const size_t ob = row * D + 4 * cg;
+      const size_t ob = row * D + col0 + 4 * cg;
       store_act(p.o, ob + 0, a * y.x + qk * u.x, p.out_bf16);
       store_act(p.o, ob + 1, a * y.y + qk * u.y, p.out_bf16);
       store_act(p.o, ob + 2, a * y.z + qk * u.z, p.out_bf16);
       store_act(p.o, ob + 3, a * y.w + qk * u.w, p.out_bf16);
     }
     if (emit && conv && p.conv_dst) {
-      __syncthreads();  // s_hist shift complete
-      for (int c = tid; c < 3 * D; c += Sh::NT)
+      release_history();
 #pragma unroll
-        for (int j = 0; j < 3; ++j)
-          store_act(p.conv_dst, (dslot * 3 + j) * p.Cch + chan(c), s_hist[j][c], p.in_bf16);
+      for (int i = 0; i < MAXC; ++i) {
+        const int c = tid + i * Sh::NT;
+        if (c < NCH && writes_chan(c))
+#pragma unroll
+          for (int j = 0; j < 3; ++j)
+            store_act(p.conv_dst, (dslot * 3 + j) * p.Cch + chan(c), hr[i][j], p.in_bf16);
+      }
     }
-    __syncthreads();  // shared buffers are rewritten by the next step
   }
 
   if (p.steps == 0) {  // a zero-length segment hands its inputs straight on
-    if (has_src && !mbar_wait(&s_bar, 0)) {
+    if (has_src && !__syncthreads_and(mbar_wait(&s_bar, 0))) {
       if (tid == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_WAIT_TIMEOUT);
+      release_history();
       return;
     }
     __syncthreads();
-    float *dst = p.S_dst + ((size_t)n * p.H + h) * DD;
+    release_history();
+    float *dst = p.S_dst + ((size_t)n * p.H + h) * DD + col0;
 #pragma unroll
     for (int i = 0; i < Sh::RPT; ++i) {
       const int r = rg + Sh::ROWG * i;
       *reinterpret_cast<float4 *>(dst + (size_t)r * D + 4 * cg) = s_state4[r * Sh::COLG + cg];
     }
-    if (conv && p.conv_dst)
-      for (int c = tid; c < 3 * D; c += Sh::NT)
+    if (conv && p.conv_dst) {
 #pragma unroll
-        for (int j = 0; j < 3; ++j)
-          store_act(p.conv_dst, ((size_t)n * 3 + j) * p.Cch + chan(c), s_hist[j][c], p.in_bf16);
+      for (int i = 0; i < MAXC; ++i) {
+        const int c = tid + i * Sh::NT;
+        if (c < NCH && writes_chan(c))
+#pragma unroll
+          for (int j = 0; j < 3; ++j)
+            store_act(p.conv_dst, ((size_t)n * 3 + j) * p.Cch + chan(c), hr[i][j], p.in_bf16);
+      }
+    }
   }
+  release_history();
 }
 
 template <int D>
 cudaError_t launch(const RecurParams &p, cudaStream_t stream) {
-  const unsigned units = (unsigned)p.N * (unsigned)p.H;
-  constexpr int smem = D * D * 4;
+  using Sh = Shape<D>;
+  const unsigned grid = (unsigned)p.N * (unsigned)p.H * Sh::NSPLIT;
+  constexpr int smem = D * Sh::DC * 4;
+  CUtensorMap tmap;
+  memset(&tmap, 0, sizeof(tmap));
+  if (p.S_src) {
+    // the state source as (columns, rows, slot * H + head) planes; box = one column slice
+    const long long planes = (long long)(p.src_slot ? p.pool_slots : p.N) * p.H;
+    const long long dims[3] = {D, D, planes};
+    const int box[3] = {Sh::DC, D, 1};
+    if (!encode_3d_map(&tmap, p.S_src, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dims, box, false))
+      return cudaErrorInvalidValue;
+  }
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(recurrent_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
-  recurrent_kernel<D><<<units, Shape<D>::NT, smem, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(Sh::NT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = Sh::NSPLIT;  // the slices of one state run as one cluster
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, recurrent_kernel<D>, tmap, p);
 }
 
 }  // namespace
