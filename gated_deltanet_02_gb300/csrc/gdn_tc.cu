@@ -61,13 +61,14 @@ __device__ __forceinline__ uint4 pack8_rn(const float *x) {
 
 constexpr int kPrepThreads = 256;
 constexpr int kRawRows = kC + 3;                 // the chunk and 3 tokens of conv history
-constexpr uint32_t kRawRowBytes = 3 * kD * 2;    // q | k | v of one token, bf16
-constexpr uint32_t kOffRaw = 0;                  // raw [67][384] bf16 (51456 B)
+constexpr uint32_t kRawPartBytes = kD * 2 + 16;  // one part (q, k or v) of a token, padded
+constexpr uint32_t kRawRowBytes = 3 * kRawPartBytes;  // padding spreads rows and parts over banks
+constexpr uint32_t kOffRaw = 0;                  // raw [67][3][136] bf16
 constexpr uint32_t kOffAmat = 0;                 // after the front end: A [64][65] fp32
 constexpr uint32_t kOffTm = 17408;               // then (I+A)^-1 diag(beta gamma) hi, lo and
                                                  // (I+A)^-1 diag(beta) hi, lo: 4 x 8 KiB
-constexpr uint32_t kOffW4 = 52224;               // conv weights [384][4] fp32
-constexpr uint32_t kOffQK = 58368;               // stacked [Q'; K']: 2 column blocks x 128 rows x 128 B
+constexpr uint32_t kOffW4 = 55296;               // conv weights [384][4] fp32
+constexpr uint32_t kOffQK = 61440;               // stacked [Q'; K']: 2 column blocks x 128 rows x 128 B
 constexpr uint32_t kOffVp = kOffQK + 32768;      // V': 2 column blocks x 64 rows x 128 B
 constexpr uint32_t kOffMisc = kOffVp + 16384;    // g2[64], beta[64], barrier, TMEM slot
 constexpr uint32_t kPrepSmem = kOffMisc + 1024 + 1024;
@@ -110,18 +111,34 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
 
   // ---- raw tile: tokens t0-3 .. t0+63, history from conv_in (or zero) ---------
   uint8_t *raw = smem + kOffRaw;
-  for (int it = tid; it < kRawRows * 48; it += kPrepThreads) {
-    const int r = it / 48, rem = it - r * 48, part = rem >> 4, q16 = rem & 15;
-    const int t = t0 - 3 + r;
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (t >= 0 && t < T) {
-      const __nv_bfloat16 *src = part == 0 ? p.q : (part == 1 ? p.k : p.v);
-      val = *reinterpret_cast<const uint4 *>(src + (((size_t)b * T + t) * H + h) * kD + q16 * 8);
-    } else if (t < 0 && p.has_conv && p.conv_in) {
-      val = *reinterpret_cast<const uint4 *>(p.conv_in + ((size_t)b * 3 + (t + 3)) * Cch + part * H * kD +
-                                             h * kD + q16 * 8);
+  {
+    // every load of the tile is issued before the first store
+    constexpr int kItems = kRawRows * 48, kRounds = (kItems + kPrepThreads - 1) / kPrepThreads;
+    uint4 vals[kRounds];
+#pragma unroll
+    for (int m = 0; m < kRounds; ++m) {
+      const int it = tid + m * kPrepThreads;
+      vals[m] = make_uint4(0u, 0u, 0u, 0u);
+      if (it < kItems) {
+        const int r = it / 48, rem = it - r * 48, part = rem >> 4, q16 = rem & 15;
+        const int t = t0 - 3 + r;
+        if (t >= 0 && t < T) {
+          const __nv_bfloat16 *src = part == 0 ? p.q : (part == 1 ? p.k : p.v);
+          vals[m] = *reinterpret_cast<const uint4 *>(src + (((size_t)b * T + t) * H + h) * kD + q16 * 8);
+        } else if (t < 0 && p.has_conv && p.conv_in) {
+          vals[m] = *reinterpret_cast<const uint4 *>(p.conv_in + ((size_t)b * 3 + (t + 3)) * Cch +
+                                                     part * H * kD + h * kD + q16 * 8);
+        }
+      }
     }
-    *reinterpret_cast<uint4 *>(raw + r * kRawRowBytes + part * 256 + q16 * 16) = val;
+#pragma unroll
+    for (int m = 0; m < kRounds; ++m) {
+      const int it = tid + m * kPrepThreads;
+      if (it < kItems) {
+        const int r = it / 48, rem = it - r * 48, part = rem >> 4, q16 = rem & 15;
+        *reinterpret_cast<uint4 *>(raw + r * kRawRowBytes + part * kRawPartBytes + q16 * 16) = vals[m];
+      }
+    }
   }
   float *w4 = reinterpret_cast<float *>(smem + kOffW4);
   if (p.has_conv)
@@ -155,29 +172,32 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
   __syncthreads();
 
   // ---- front end: y_t = sum_j w_j x_{t-3+j}; L2 norm of q, k rows; bf16 -------
+  // task = (token t, part, lane l of 8): channels l, l+8, ..., l+120, so the 8
+  // lanes of a task group read consecutive weights and raw elements.
   uint8_t *qk = smem + kOffQK;
   uint8_t *vp = smem + kOffVp;
   for (int task = tid; task < kC * 3 * 8; task += kPrepThreads) {  // 6 rounds, uniform
-    const int g = task & 7, tp = task >> 3, part = tp % 3, t = tp / 3;
-    const int ch0 = g * 16;
+    const int l = task & 7, tp = task >> 3, part = tp % 3, t = tp / 3;
     float y[16];
     if (p.has_conv) {
-      const float *w = w4 + (part * kD + ch0) * 4;
 #pragma unroll
       for (int i = 0; i < 16; ++i) y[i] = 0.f;
+      const float *w = w4 + (part * kD + l) * 4;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint8_t *src = raw + (t + j) * kRawRowBytes + part * 256 + ch0 * 2;
-        float x[16];
-        unpack8(*reinterpret_cast<const uint4 *>(src), x);
-        unpack8(*reinterpret_cast<const uint4 *>(src + 16), x + 8);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) y[i] += w[i * 4 + j] * x[i];
+      for (int i = 0; i < 16; ++i) {
+        const float4 wc = *reinterpret_cast<const float4 *>(w + i * 32);
+        const uint8_t *src = raw + t * kRawRowBytes + part * kRawPartBytes + (l + 8 * i) * 2;
+        const float x0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(src));
+        const float x1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(src + kRawRowBytes));
+        const float x2 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(src + 2 * kRawRowBytes));
+        const float x3 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(src + 3 * kRawRowBytes));
+        y[i] = wc.x * x0 + wc.y * x1 + wc.z * x2 + wc.w * x3;
       }
     } else {
-      const uint8_t *src = raw + (t + 3) * kRawRowBytes + part * 256 + ch0 * 2;
-      unpack8(*reinterpret_cast<const uint4 *>(src), y);
-      unpack8(*reinterpret_cast<const uint4 *>(src + 16), y + 8);
+      const uint8_t *src = raw + (t + 3) * kRawRowBytes + part * kRawPartBytes + l * 2;
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        y[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(src + 16 * i));
     }
     if (part < 2 && p.qk_l2norm) {
       float ss = 0.f;
@@ -190,24 +210,21 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
 #pragma unroll
       for (int i = 0; i < 16; ++i) y[i] *= inv;
     }
-    if (t0 + t >= T) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] = 0.f;
-    }
-    const uint4 lo8 = pack8_rn(y), hi8 = pack8_rn(y + 8);
-    const int blk = g >> 2, chunk = (g & 3) * 2;
+    const bool valid = t0 + t < T;
+    // element l of every 16-byte chunk i (= channels 8i .. 8i+7) of the row
     if (part < 2) {
       const int row = part * kC + t;
-      uint8_t *tile = qk + blk * 16384;
-      *reinterpret_cast<uint4 *>(tile + swz(row, chunk)) = lo8;
-      *reinterpret_cast<uint4 *>(tile + swz(row, chunk + 1)) = hi8;
-      __nv_bfloat16 *dst = (part == 0 ? p.Qp : p.Kp) + (unit * p.Tp + t0 + t) * kD + ch0;
-      reinterpret_cast<uint4 *>(dst)[0] = lo8;
-      reinterpret_cast<uint4 *>(dst)[1] = hi8;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const __nv_bfloat16 v = __float2bfloat16_rn(valid ? y[i] : 0.f);
+        *reinterpret_cast<__nv_bfloat16 *>(qk + (i >> 3) * 16384 + swz(row, i & 7) + l * 2) = v;
+      }
     } else {
-      uint8_t *tile = vp + blk * 8192;
-      *reinterpret_cast<uint4 *>(tile + swz(t, chunk)) = lo8;
-      *reinterpret_cast<uint4 *>(tile + swz(t, chunk + 1)) = hi8;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const __nv_bfloat16 v = __float2bfloat16_rn(valid ? y[i] : 0.f);
+        *reinterpret_cast<__nv_bfloat16 *>(vp + (i >> 3) * 8192 + swz(t, i & 7) + l * 2) = v;
+      }
     }
   }
   fence_proxy_async_smem();
@@ -215,6 +232,13 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
+  // Q', K' rows to the workspace: 2 x 64 rows x 16 chunks of 16 bytes
+  for (int it = tid; it < 2 * kC * 16; it += kPrepThreads) {
+    const int part = it >> 10, rem = it & 1023, t = rem >> 4, ch = rem & 15;
+    const uint4 v = *reinterpret_cast<const uint4 *>(qk + (ch >> 3) * 16384 + swz(part * kC + t, ch & 7));
+    __nv_bfloat16 *dst = (part == 0 ? p.Qp : p.Kp) + (unit * p.Tp + t0 + t) * kD + ch * 8;
+    *reinterpret_cast<uint4 *>(dst) = v;
+  }
 
   // ---- [Q'; K'] K'^T: M = 128 (rows 0-63 Q'K'^T, rows 64-127 K'K'^T), N = 64
   if (tid == 0) {
@@ -250,24 +274,35 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
   }
   __syncthreads();
 
-  // ---- (I + A)^-1 by forward substitution, thread k solves column k ------------
-  if (ok && tid < 64) {
-    const int k = tid;
-    float x[64];
+  // ---- (I + A)^-1 by forward substitution: 4 lanes solve column k = tid / 4 ----
+  // x_i = [i == k] - sum_{j < i} A_ij x_j; lane `sub` holds x_j for j = sub (mod 4)
+  // and the partial sums over its j are combined with two shuffles per row.
+  if (ok) {
+    const int k = tid >> 2, sub = tid & 3;
+    float xs[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) xs[m] = 0.f;
 #pragma unroll
     for (int i = 0; i < 64; ++i) {
-      float s = 0.f;
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-      for (int j = 0; j < i; ++j) s += A[i * 65 + j] * x[j];
-      x[i] = (i == k ? 1.f : 0.f) - s;
+      for (int m = 0; 4 * m + sub < i && m < 16; m += 2) {
+        s0 += A[i * 65 + 4 * m + sub] * xs[m];
+        if (4 * (m + 1) + sub < i) s1 += A[i * 65 + 4 * (m + 1) + sub] * xs[m + 1];
+      }
+      float sum = s0 + s1;
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      if ((i & 3) == sub) xs[i >> 2] = (i == k ? 1.f : 0.f) - sum;
     }
     const float bk = betas[k], bgk = bk * exp2f(g2s[k]);
     uint8_t *tm1 = smem + kOffTm;  // (I+A)^-1 diag(beta gamma): hi, lo
     uint8_t *tm2 = tm1 + 16384;    // (I+A)^-1 diag(beta): hi, lo
     const uint32_t colb = (uint32_t)(k & 7) * 2;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      const float w1 = x[i] * bgk, w2 = x[i] * bk;
+    for (int m = 0; m < 16; ++m) {
+      const int i = 4 * m + sub;
+      const float w1 = xs[m] * bgk, w2 = xs[m] * bk;
       const __nv_bfloat16 h1 = __float2bfloat16_rn(w1), h2 = __float2bfloat16_rn(w2);
       const __nv_bfloat16 l1 = __float2bfloat16_rn(w1 - __bfloat162float(h1));
       const __nv_bfloat16 l2 = __float2bfloat16_rn(w2 - __bfloat162float(h2));

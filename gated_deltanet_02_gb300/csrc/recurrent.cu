@@ -127,6 +127,15 @@ __global__ void __launch_bounds__(Shape<D>::NT)
     s_bad = 0;
   }
   const bool conv = p.conv_w != nullptr;
+  // gates and destination slot of step 0 (prefetched one step ahead afterwards)
+  float a_next = 1.f, b_next = 0.f;
+  int dslot_next = n;
+  if (p.steps > 0) {
+    const size_t row0 = ((size_t)n * p.steps) * p.H + h;
+    a_next = p.alpha[row0];
+    if (p.variant == GLINATTN_GDN) b_next = p.beta[row0];
+    if (p.dst_slot) dslot_next = p.dst_slot[(size_t)n * (p.dst_per_step ? p.steps : 1)];
+  }
   float xr[MAXC], wr[MAXC][4], hr[MAXC][3];
   {
     const size_t row0 = ((size_t)n * p.steps) * p.H + h;
@@ -189,6 +198,13 @@ __global__ void __launch_bounds__(Shape<D>::NT)
 
   for (int t = 0; t < p.steps; ++t) {
     const size_t row = ((size_t)n * p.steps + t) * p.H + h;  // (n, t, h)
+    const float a = a_next, bgate = b_next;
+    const int dslot_t = dslot_next;
+    if (t + 1 < p.steps) {
+      a_next = p.alpha[row + p.H];
+      if (p.variant == GLINATTN_GDN) b_next = p.beta[row + p.H];
+      if (p.dst_slot && p.dst_per_step) dslot_next = p.dst_slot[(size_t)n * p.steps + t + 1];
+    }
     // ---- front end in registers: conv, history shift, next token prefetch -------
     float yv[MAXC];
     float sq = 0.f, sk = 0.f;
@@ -277,11 +293,10 @@ __global__ void __launch_bounds__(Shape<D>::NT)
     }
 
     // ---- update: shared memory copy for the next step, global copy if due ------
-    const float a = p.alpha[row];
     const float4 vv = *reinterpret_cast<const float4 *>(sva + 4 * cg);
     float4 u = vv;
     if (p.variant == GLINATTN_GDN) {
-      const float b = p.beta[row];
+      const float b = bgate;
       u.x = b * (vv.x - a * x.x);
       u.y = b * (vv.y - a * x.y);
       u.z = b * (vv.z - a * x.z);
@@ -290,12 +305,8 @@ __global__ void __launch_bounds__(Shape<D>::NT)
     const bool last = (t == p.steps - 1);
     const bool emit = p.dst_per_step || last;
     float *dst = nullptr;
-    size_t dslot = (size_t)n;
-    if (emit) {
-      if (p.dst_slot)
-        dslot = (size_t)p.dst_slot[(size_t)n * (p.dst_per_step ? p.steps : 1) + (p.dst_per_step ? t : 0)];
-      dst = p.S_dst + (dslot * p.H + h) * DD + col0;
-    }
+    const size_t dslot = (size_t)dslot_t;
+    if (emit) dst = p.S_dst + (dslot * p.H + h) * DD + col0;
 #pragma unroll
     for (int i = 0; i < Sh::RPT; ++i) {
       const int r = rg + Sh::ROWG * i;
