@@ -373,6 +373,7 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
 
 constexpr int kBV = 64;
 constexpr int kStages = 2;
+constexpr int kPrefetch = 3;  // chunks prefetched into L2 beyond the shared-memory ring
 constexpr int kThreads = 320;    // warp 0 TMA, warp 1 MMA, warps 2-5 (P), 6-9 (state, outputs)
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kTile = kC * kD * 2;        // Q', K' or W tile: 16 KiB (2 column blocks)
@@ -390,7 +391,8 @@ constexpr uint32_t kOffG = kOffS + 2 * kTileS;      // gate rows [warp][2][64]
 constexpr uint32_t kOffBar = kOffG + (kThreads / 32) * 2 * kC * 4;
 constexpr uint32_t kScanSmem = kOffBar + 256 + 1024;
 static_assert(kScanSmem <= 232448, "shared memory budget");
-constexpr uint32_t kColQK = 0, kColWS = 128, kColDS = 192, kColQS = 256, kColPU = 384;
+// TMEM: Q'K'^T (64), W[S_hi|S_lo] (128), K'^T[rU_hi|rU_lo] (128), Q'[S_hi|S_lo] (128), P U (64)
+constexpr uint32_t kColQK = 0, kColWS = 64, kColDS = 192, kColQS = 320, kColPU = 448;
 
 struct ScanParams {
   int B, T, H, nchunks, Tp, out_bf16;
@@ -408,7 +410,7 @@ struct ScanParams {
 
 struct ScanBars {
   uint64_t full[kStages], empty[kStages];
-  uint64_t qk_ready[2], qk_free[2], p_ready[2], o_ready[2], o_free[2];
+  uint64_t qk_ready, qk_free, p_ready, o_ready, o_free;
   uint64_t ws_ready, u_ready, ds_ready, s_ready, p_free;
   uint32_t tmem_base;
   int abort;
@@ -497,13 +499,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->qk_ready[i], 1);
-      mbar_init(&bars->o_ready[i], 1);
-      mbar_init(&bars->qk_free[i], kEpiThreads);
-      mbar_init(&bars->p_ready[i], kEpiThreads);
-      mbar_init(&bars->o_free[i], kEpiThreads);
-    }
+    mbar_init(&bars->qk_ready, 1);
+    mbar_init(&bars->o_ready, 1);
+    mbar_init(&bars->qk_free, kEpiThreads);
+    mbar_init(&bars->p_ready, kEpiThreads);
+    mbar_init(&bars->o_free, kEpiThreads);
     mbar_init(&bars->ws_ready, 1);
     mbar_init(&bars->ds_ready, 1);
     mbar_init(&bars->p_free, 1);
@@ -528,8 +528,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tk);
       prefetch_tensormap(&tw);
       prefetch_tensormap(&tu);
+      auto prefetch = [&](int c) {  // chunk c's tiles into L2, ahead of the ring
+        if (c >= nchunks) return;
+        const int r0 = c * kC;
+        tma_prefetch_l2_3d(&tq, 0, r0, (int)unit);
+        tma_prefetch_l2_3d(&tq, 64, r0, (int)unit);
+        tma_prefetch_l2_3d(&tk, 0, r0, (int)unit);
+        tma_prefetch_l2_3d(&tk, 64, r0, (int)unit);
+        tma_prefetch_l2_3d(&tw, 0, r0, (int)unit);
+        tma_prefetch_l2_3d(&tw, 64, r0, (int)unit);
+        tma_prefetch_l2_3d(&tu, vblk * kBV, r0, (int)unit);
+      };
+      for (int c = 0; c < kPrefetch; ++c) prefetch(kStages + c);
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % kStages;
+        prefetch(c + kStages + kPrefetch);
         if (!wait_bar(&bars->empty[s], ((uint32_t)(c / kStages) & 1u) ^ 1u, abort)) break;
         uint8_t *st = smem + kOffStage + s * kStageBytes;
         uint64_t *fb = &bars->full[s];
@@ -547,71 +560,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
     if (lane == 0) {
-      constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);   // Q' K'^T
-      constexpr uint32_t id_xs = idesc_bf16(64, kBV, false, true);   // W S, Q' S
-      constexpr uint32_t id_ds = idesc_bf16(128, kBV, true, true);   // K'^T (r U)
-      constexpr uint32_t id_pu = idesc_bf16(64, kBV, false, true);   // P U
+      constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);        // Q' K'^T
+      constexpr uint32_t id_xs = idesc_bf16(64, 2 * kBV, false, true);    // W [S_hi|S_lo], Q' [..]
+      constexpr uint32_t id_ds = idesc_bf16(128, 2 * kBV, true, true);    // K'^T [rU_hi|rU_lo]
+      constexpr uint32_t id_pu = idesc_bf16(64, kBV, false, true);        // P U
       const uint32_t sbase = smem_u32(smem);
-      auto issue_qk = [&](int c) -> bool {
-        const int s = c % kStages, tb = c & 1;
-        if (!wait_bar(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) return false;
-        if (!wait_bar(&bars->qk_free[tb], ((uint32_t)(c >> 1) & 1u) ^ 1u, abort)) return false;
-        tc_fence_after();
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % kStages;
+        const uint32_t pc = (uint32_t)c & 1u;
         const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
         const uint64_t dQ = desc_sw128(aQ, 16, 1024), dK = desc_sw128(aQ + kTile, 16, 1024);
+        const uint64_t dKm = desc_sw128(aQ + kTile, kTile / 2, 1024);
+        const uint64_t dW = desc_sw128(aQ + 2 * kTile, 16, 1024);
+        const uint64_t dS = desc_sw128(sbase + kOffS, kTileS, 1024);    // [S_hi | S_lo]
+        const uint64_t dP = desc_sw128(sbase + kOffP, 16, 1024);
+        const uint64_t dU = desc_sw128(sbase + kOffU, 16, 1024);
+        const uint64_t dRU = desc_sw128(sbase + kOffRU, kTileV, 1024);  // [rU_hi | rU_lo]
+        // Q' K'^T: M = 64 tokens, N = 64 tokens, K = d_k
+        if (!wait_bar(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) break;
+        if (!wait_bar(&bars->qk_free, pc ^ 1u, abort)) break;
+        tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t off = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
-          umma_bf16(tmem + kColQK + tb * 64, dQ + off, dK + off, id_qk, ks > 0);
+          umma_bf16(tmem + kColQK, dQ + off, dK + off, id_qk, ks > 0);
         }
-        umma_commit(&bars->qk_ready[tb]);
-        return true;
-      };
-      bool ok = issue_qk(0);
-      for (int c = 0; c < nchunks && ok; ++c) {
-        const int s = c % kStages, tb = c & 1;
-        const uint32_t ph = (uint32_t)(c >> 1) & 1u, pc = (uint32_t)c & 1u;
-        if (c + 1 < nchunks && !issue_qk(c + 1)) break;
-        const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
-        const uint64_t dQ = desc_sw128(aQ, 16, 1024);
-        const uint64_t dKm = desc_sw128(aQ + kTile, kTile / 2, 1024);
-        const uint64_t dW = desc_sw128(aQ + 2 * kTile, 16, 1024);
-        const uint64_t dS = desc_sw128(sbase + kOffS, 16, 1024);
-        const uint64_t dP = desc_sw128(sbase + kOffP, 16, 1024);
-        const uint64_t dU = desc_sw128(sbase + kOffU, 16, 1024);
-        const uint64_t dRU = desc_sw128(sbase + kOffRU, 16, 1024);
+        umma_commit(&bars->qk_ready);
+        // W [S_hi | S_lo]: M = 64, N = 128, K = d_k (W tile K-major, S tiles MN-major)
         if (!wait_bar(&bars->s_ready, pc, abort)) break;
-        if (!wait_bar(&bars->o_free[tb], ph ^ 1u, abort)) break;
         tc_fence_after();
-        // W S: M = 64, N = 64, K = d_k (W tile K-major, S tile MN-major)
 #pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t aoff = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
-            umma_bf16(tmem + kColWS, dW + aoff, dS + ((part * kTileS + ks * 2048) >> 4), id_xs,
-                      (part | ks) != 0);
-          }
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t aoff = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
+          umma_bf16(tmem + kColWS, dW + aoff, dS + ((ks * 2048) >> 4), id_xs, ks > 0);
+        }
         umma_commit(&bars->ws_ready);
-        // Q' S
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t aoff = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
-            umma_bf16(tmem + kColQS + tb * 64, dQ + aoff, dS + ((part * kTileS + ks * 2048) >> 4),
-                      id_xs, (part | ks) != 0);
-          }
-        if (!wait_bar(&bars->u_ready, pc, abort)) break;
-        if (!wait_bar(&bars->p_ready[tb], ph, abort)) break;
+        // Q' [S_hi | S_lo] (its accumulator is read by the previous chunk's outputs)
+        if (!wait_bar(&bars->o_free, pc ^ 1u, abort)) break;
         tc_fence_after();
-        // dS = K'^T (rU hi + rU lo): M = d_k (K' tile read M-major), N = 64, K = 64 tokens
 #pragma unroll
-        for (int part = 0; part < 2; ++part)
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t aoff = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
+          umma_bf16(tmem + kColQS, dQ + aoff, dS + ((ks * 2048) >> 4), id_xs, ks > 0);
+        }
+        if (!wait_bar(&bars->u_ready, pc, abort)) break;
+        if (!wait_bar(&bars->p_ready, pc, abort)) break;
+        tc_fence_after();
+        // dS = K'^T [rU_hi | rU_lo]: M = d_k (K' tile read M-major), N = 128, K = 64 tokens
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(tmem + kColDS, dKm + ((ks * 2048) >> 4), dRU + ((part * kTileV + ks * 2048) >> 4),
-                      id_ds, (part | ks) != 0);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tmem + kColDS, dKm + ((ks * 2048) >> 4), dRU + ((ks * 2048) >> 4), id_ds, ks > 0);
         umma_commit(&bars->ds_ready);
         // P U = Phi Uhi + Phi Ulo + Plo Uhi: M = 64, N = 64, K = 64 tokens
 #pragma unroll
@@ -619,10 +617,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const int pp = part == 2 ? 1 : 0, up = part == 1 ? 1 : 0;
-            umma_bf16(tmem + kColPU + tb * 64, dP + ((pp * kTileP + ks * 32) >> 4),
+            umma_bf16(tmem + kColPU, dP + ((pp * kTileP + ks * 32) >> 4),
                       dU + ((up * kTileV + ks * 2048) >> 4), id_pu, (part | ks) != 0);
           }
-        umma_commit(&bars->o_ready[tb]);
+        umma_commit(&bars->o_ready);
         umma_commit(&bars->p_free);
         umma_commit(&bars->empty[s]);
       }
@@ -630,30 +628,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 6) {
     // ============ warpgroup A: P = (Q' K'^T) * D ============
     const int q4 = warp & 3;
-    const bool has_tok = lane < 16;
-    const int tok = 16 * q4 + lane;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     float *grow = s_g + warp * 2 * kC;
     GateRow G;
     grow_prefetch(G, p, unit, 0, lane);
     for (int c = 0; c < nchunks; ++c) {
-      const int tb = c & 1;
-      const uint32_t ph = (uint32_t)(c >> 1) & 1u;
+      const uint32_t pc = (uint32_t)c & 1u;
       const float gC = grow_chunk(G, p, unit, c, lane, grow);
-      if (!wait_bar_warp(&bars->qk_ready[tb], ph, abort)) break;
+      if (!wait_bar_warp(&bars->qk_ready, pc, abort)) break;
       tc_fence_after();
-      float qk[64];
+      // lane l < 16 holds row 16*q4 + l (M = 64 layout); it keeps columns 0..31
+      // and hands columns 32..63 to lane l + 16
+      float qk[32];
       {
-        float part[32];
-        tmem_ld32(tmem + kColQK + tb * 64 + lane_base, part);
+        float lo32[32], hi32[32];
+        tmem_ld32(tmem + kColQK + lane_base, lo32);
+        tmem_ld32(tmem + kColQK + 32 + lane_base, hi32);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) qk[j] = part[j];
-        tmem_ld32(tmem + kColQK + tb * 64 + 32 + lane_base, part);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) qk[32 + j] = part[j];
+        for (int j = 0; j < 32; ++j) {
+          const float x = __shfl_sync(0xffffffffu, hi32[j], lane & 15);
+          qk[j] = lane < 16 ? lo32[j] : x;
+        }
       }
       tc_fence_before();
-      mbar_arrive(&bars->qk_free[tb]);
+      mbar_arrive(&bars->qk_free);
       const bool factored = gC > -100.f;
       float *cfrow = grow + kC;
       if (factored) {
@@ -661,28 +659,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         cfrow[2 * lane + 1] = exp2f(-grow[2 * lane + 1]);
       }
       __syncwarp();
-      if (!wait_bar_warp(&bars->p_free, ((uint32_t)c & 1u) ^ 1u, abort)) break;
-      if (has_tok) {
+      if (!wait_bar_warp(&bars->p_free, pc ^ 1u, abort)) break;
+      {
+        const int row = 16 * q4 + (lane & 15), jb = 32 * (lane >> 4);
         const uint32_t phi = smem_u32(smem + kOffP), plo = phi + kTileP;
-        const float gi = grow[tok];
+        const float gi = grow[row];
         if (factored) {
           const float rf = exp2f(gi);
 #pragma unroll
-          for (int j = 0; j < kC; ++j) qk[j] = (j <= tok) ? qk[j] * rf * cfrow[j] : 0.f;
+          for (int jj = 0; jj < 32; ++jj) {
+            const int j = jb + jj;
+            qk[jj] = (j <= row) ? qk[jj] * rf * cfrow[j] : 0.f;
+          }
         } else {
 #pragma unroll
-          for (int j = 0; j < kC; ++j) qk[j] = (j <= tok) ? qk[j] * exp2f(gi - grow[j]) : 0.f;
+          for (int jj = 0; jj < 32; ++jj) {
+            const int j = jb + jj;
+            qk[jj] = (j <= row) ? qk[jj] * exp2f(gi - grow[j]) : 0.f;
+          }
         }
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int c4 = 0; c4 < 4; ++c4) {
           uint4 uh, ul;
-          split8(&qk[8 * ch], uh, ul);
-          sts128(phi + swz(tok, ch), uh);
-          sts128(plo + swz(tok, ch), ul);
+          split8(&qk[8 * c4], uh, ul);
+          const int ch = 4 * (lane >> 4) + c4;
+          sts128(phi + swz(row, ch), uh);
+          sts128(plo + swz(row, ch), ul);
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(&bars->p_ready[tb]);
+      mbar_arrive(&bars->p_ready);
     }
   } else {
     // ============ warpgroup B: U, the state chain and the outputs ============
@@ -690,6 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int srow = 32 * q4 + lane;
     const bool has_tok = lane < 16;
     const int tok = 16 * q4 + lane;
+    const int urow = 16 * q4 + (lane & 15), ub = 32 * (lane >> 4);  // U row / column half
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     float *grow = s_g + warp * 2 * kC;
     GateRow G;
@@ -718,76 +725,85 @@ __global__ void __launch_bounds__(kThreads, 1)
     write_state();
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
-      const int s = c % kStages, tb = c & 1;
-      const uint32_t ph = (uint32_t)(c >> 1) & 1u, pc = (uint32_t)c & 1u;
+      const int s = c % kStages;
+      const uint32_t pc = (uint32_t)c & 1u;
       const uint32_t sph = (uint32_t)(c / kStages) & 1u;
       const int t0 = c * kC;
       const float gC = grow_chunk(G, p, unit, c, lane, grow);
       const float g_tok = grow[tok & (kC - 1)];
 
-      // ---- U = U~ - W S (rows), U and r U split into smem --------------------
+      // ---- U = U~ - W S: lane l < 16 takes columns 0..31 of row 16*q4 + l,
+      // lane l + 16 columns 32..63; the W S hi and lo halves are summed
       if (!wait_bar_warp(&bars->ws_ready, pc, abort)) { ok = false; break; }
       tc_fence_after();
-      float u[kBV];
-      {
-        float part[32];
-        tmem_ld32(tmem + kColWS + lane_base, part);
+      float u[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) u[j] = part[j];
-        tmem_ld32(tmem + kColWS + 32 + lane_base, part);
+      for (int q = 0; q < 2; ++q) {
+        float hi[16], lo[16];
+        tmem_ld16(tmem + kColWS + 16 * q + lane_base, hi);        // columns 16q.. of the hi half
+        tmem_ld16(tmem + kColWS + kBV + 16 * q + lane_base, lo);  // and of the lo half
 #pragma unroll
-        for (int j = 0; j < 32; ++j) u[32 + j] = part[j];
+        for (int j = 0; j < 16; ++j) u[16 * q + j] = hi[j] + lo[j];
+        tmem_ld16(tmem + kColWS + 32 + 16 * q + lane_base, hi);   // columns 32 + 16q..
+        tmem_ld16(tmem + kColWS + kBV + 32 + 16 * q + lane_base, lo);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float x = __shfl_sync(0xffffffffu, hi[j] + lo[j], lane & 15);
+          if (lane >= 16) u[16 * q + j] = x;
+        }
       }
       if (!wait_bar_warp(&bars->full[s], sph, abort)) { ok = false; break; }
       if (!wait_bar_warp(&bars->p_free, pc ^ 1u, abort)) { ok = false; break; }
-      if (has_tok) {
+      {
         const float *ut = reinterpret_cast<const float *>(smem + kOffStage + s * kStageBytes + 3 * kTile) +
-                          tok * kBV;
+                          urow * kBV + ub;
 #pragma unroll
-        for (int j = 0; j < kBV; j += 4) {
+        for (int j = 0; j < 32; j += 4) {
           const float4 v4 = *reinterpret_cast<const float4 *>(ut + j);
           u[j] = v4.x - u[j];
           u[j + 1] = v4.y - u[j + 1];
           u[j + 2] = v4.z - u[j + 2];
           u[j + 3] = v4.w - u[j + 3];
         }
-        const float r = exp2f(gC - g_tok);
+        const float r = exp2f(gC - grow[urow]);
         const uint32_t uhi = smem_u32(smem + kOffU), ulo = uhi + kTileV;
         const uint32_t rhi = smem_u32(smem + kOffRU), rlo = rhi + kTileV;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int ch = 4 * (lane >> 4) + c4;
           uint4 uh, ul;
-          split8(&u[8 * ch], uh, ul);
-          sts128(uhi + swz(tok, ch), uh);
-          sts128(ulo + swz(tok, ch), ul);
+          split8(&u[8 * c4], uh, ul);
+          sts128(uhi + swz(urow, ch), uh);
+          sts128(ulo + swz(urow, ch), ul);
           float ru[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) ru[i] = r * u[8 * ch + i];
+          for (int i = 0; i < 8; ++i) ru[i] = r * u[8 * c4 + i];
           split8(ru, uh, ul);
-          sts128(rhi + swz(tok, ch), uh);
-          sts128(rlo + swz(tok, ch), ul);
+          sts128(rhi + swz(urow, ch), uh);
+          sts128(rlo + swz(urow, ch), ul);
         }
       }
       fence_proxy_async_smem();
       mbar_arrive(&bars->u_ready);
 
-      // ---- S <- gamma_C S + K'^T diag(r) U ----------------------------------------
+      // ---- S <- gamma_C S + K'^T diag(r) U (hi and lo halves summed) -------------
       if (!wait_bar_warp(&bars->ds_ready, pc, abort)) { ok = false; break; }
       tc_fence_after();
       {
         const float gam = exp2f(gC);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float ds[32];
-          tmem_ld32(tmem + kColDS + 32 * half + lane_base, ds);
+        for (int q = 0; q < 4; ++q) {
+          float dh[16], dl[16];
+          tmem_ld16(tmem + kColDS + 16 * q + lane_base, dh);
+          tmem_ld16(tmem + kColDS + kBV + 16 * q + lane_base, dl);
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) S[32 * half + jj] = gam * S[32 * half + jj] + ds[jj];
+          for (int jj = 0; jj < 16; ++jj) S[16 * q + jj] = gam * S[16 * q + jj] + (dh[jj] + dl[jj]);
         }
       }
       if (c + 1 < nchunks) write_state();
 
       // ---- o = gamma_i (Q' S) + P U ------------------------------------------------
-      if (!wait_bar_warp(&bars->o_ready[tb], ph, abort)) { ok = false; break; }
+      if (!wait_bar_warp(&bars->o_ready, pc, abort)) { ok = false; break; }
       tc_fence_after();
       {
         const float gi = exp2f(g_tok);
@@ -795,29 +811,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool store = has_tok && t < T;
         const size_t obase = (((size_t)b * T + t) * p.H + h) * kD + vblk * kBV;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float o1[32], o2[32];
-          tmem_ld32(tmem + kColQS + tb * 64 + 32 * half + lane_base, o1);
-          tmem_ld32(tmem + kColPU + tb * 64 + 32 * half + lane_base, o2);
-          float ov[32];
+        for (int qt = 0; qt < 4; ++qt) {
+          float o1[16], o1l[16], o2[16];
+          tmem_ld16(tmem + kColQS + 16 * qt + lane_base, o1);
+          tmem_ld16(tmem + kColQS + kBV + 16 * qt + lane_base, o1l);
+          tmem_ld16(tmem + kColPU + 16 * qt + lane_base, o2);
+          float ov[16];
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) ov[jj] = gi * o1[jj] + o2[jj];
+          for (int jj = 0; jj < 16; ++jj) ov[jj] = gi * (o1[jj] + o1l[jj]) + o2[jj];
           if (store) {
             if (p.out_bf16) {
-              uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + obase + 32 * half);
+              uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + obase + 16 * qt);
 #pragma unroll
-              for (int k = 0; k < 4; ++k) dst[k] = pack8_rn(ov + 8 * k);
+              for (int k = 0; k < 2; ++k) dst[k] = pack8_rn(ov + 8 * k);
             } else {
-              float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + obase + 32 * half);
+              float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + obase + 16 * qt);
 #pragma unroll
-              for (int k = 0; k < 8; ++k)
+              for (int k = 0; k < 4; ++k)
                 dst[k] = make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
             }
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(&bars->o_free[tb]);
+      mbar_arrive(&bars->o_free);
     }
     if (ok) {
       float *dst = p.S_T + ((unit * kD) + srow) * kD + vblk * kBV;

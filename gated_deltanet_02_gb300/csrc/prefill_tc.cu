@@ -49,6 +49,7 @@ constexpr int kC = 64;    // chunk length
 constexpr int kDK = 128;  // key / value head size
 constexpr int kBV = 64;   // d_v columns per CTA
 constexpr int kStages = 3;
+constexpr int kPrefetch = 3;  // chunks prefetched into L2 beyond the shared-memory ring
 constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-5 and 6-9 epilogue
 constexpr int kEpiThreads = 128;  // threads per epilogue warpgroup
 
@@ -68,9 +69,10 @@ constexpr uint32_t kOffBar = kOffG + (kThreads / 32) * 2 * kC * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-// TMEM columns per accumulator buffer (two buffers of 256 columns).
+// TMEM columns: QK^T double-buffered (64 each), Q[S_hi|S_lo] (128), P V
+// double-buffered (64 each), K^T[V~hi|V~lo] (128).
 constexpr uint32_t kTmCols = 512;
-constexpr uint32_t kColQK = 0, kColO1 = 64, kColO2 = 128, kColDS = 192;
+constexpr uint32_t kColQK = 0, kColO1 = 128, kColO2 = 256, kColDS = 384;
 
 struct GlaParams {
   int B, T, H, nchunks, out_bf16;
@@ -84,7 +86,7 @@ struct GlaParams {
 struct Bars {
   uint64_t full[kStages], empty[kStages];
   uint64_t qk_ready[2], qk_free[2], p_ready[2], p_free;
-  uint64_t ds_ready[2], o_ready[2], o_free[2], s_ready[2];
+  uint64_t ds_ready, ds_free, o_ready[2], o_free[2], s_ready[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -160,7 +162,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->qk_ready[i], 1);
-      mbar_init(&bars->ds_ready[i], 1);
       mbar_init(&bars->o_ready[i], 1);
       mbar_init(&bars->qk_free[i], kEpiThreads);
       mbar_init(&bars->p_ready[i], kEpiThreads);
@@ -168,6 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_ready[i], kEpiThreads);
     }
     mbar_init(&bars->p_free, 1);
+    mbar_init(&bars->ds_ready, 1);
+    mbar_init(&bars->ds_free, kEpiThreads);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -186,9 +189,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tq);
       prefetch_tensormap(&tk);
       prefetch_tensormap(&tv);
+      auto prefetch = [&](int c) {  // chunk c's tiles into L2, ahead of the ring
+        if (c >= nchunks) return;
+        const int t0 = c * kC;
+        tma_prefetch_l2_4d(&tq, 0, h, t0, b);
+        tma_prefetch_l2_4d(&tq, 64, h, t0, b);
+        tma_prefetch_l2_4d(&tk, 0, h, t0, b);
+        tma_prefetch_l2_4d(&tk, 64, h, t0, b);
+        tma_prefetch_l2_4d(&tv, vblk * kBV, h, t0, b);
+      };
+      for (int c = 0; c < kPrefetch; ++c) prefetch(kStages + c);
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % kStages;
         const uint32_t use = (uint32_t)(c / kStages);
+        prefetch(c + kStages + kPrefetch);
         if (!wait_bar(&bars->empty[s], (use & 1u) ^ 1u, abort)) break;
         uint8_t *st = smem + kOffStage + s * kStageBytes;
         mbar_arrive_expect_tx(&bars->full[s], kStageBytes);
@@ -204,9 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================= MMA issuer =======================
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);   // Q K^T
-      constexpr uint32_t id_qs = idesc_bf16(64, kBV, false, true);   // Q S
+      constexpr uint32_t id_qs = idesc_bf16(64, 2 * kBV, false, true);  // Q [S_hi | S_lo]
       constexpr uint32_t id_pv = idesc_bf16(64, kBV, false, true);   // P V
-      constexpr uint32_t id_ds = idesc_bf16(128, kBV, true, true);   // K^T V~
+      constexpr uint32_t id_ds = idesc_bf16(128, 2 * kBV, true, true);  // K^T [V~hi | V~lo]
       const uint32_t sbase = smem_u32(smem);
       // Q K^T of chunk c: M = 64 tokens, N = 64 tokens, K = d_k (2 swizzle blocks x 4 steps)
       auto issue_qk = [&](int c) -> bool {
@@ -219,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t off = ((ks >> 2) * (kTileQ / 2) + (ks & 3) * 32) >> 4;
-          umma_bf16(tmem + tb * 256 + kColQK, dQ + off, dK + off, id_qk, ks > 0);
+          umma_bf16(tmem + kColQK + tb * 64, dQ + off, dK + off, id_qk, ks > 0);
         }
         umma_commit(&bars->qk_ready[tb]);
         return true;
@@ -231,47 +245,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = (uint32_t)(c >> 1) & 1u;
         if (c + 1 < nchunks && !issue_qk(c + 1)) break;
         if (!wait_bar(&bars->p_ready[tb], ph, abort)) break;
-        if (!wait_bar(&bars->o_free[tb], ph ^ 1u, abort)) break;
+        if (!wait_bar(&bars->o_free[tb], ph ^ 1u, abort)) break;   // P V buffer tb
+        if (!wait_bar(&bars->ds_free, ((uint32_t)c & 1u) ^ 1u, abort)) break;
         tc_fence_after();
         const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
         const uint32_t aK = aQ + kTileQ;
         const uint32_t aV = aK + kTileK;
-        const uint32_t dcol = tmem + tb * 256;
         // descriptors built once; the k-steps only move the start-address field
         const uint64_t dKm = desc_sw128(aK, kTileK / 2, 1024);
-        const uint64_t dVt = desc_sw128(sbase + kOffVt, 16, 1024);
+        const uint64_t dVt = desc_sw128(sbase + kOffVt, kTileV, 1024);  // [hi | lo] as N = 128
         const uint64_t dP = desc_sw128(sbase + kOffP, 16, 1024);
         const uint64_t dV = desc_sw128(aV, 16, 1024);
         const uint64_t dQ = desc_sw128(aQ, 16, 1024);
-        // dS = K^T (V~hi + V~lo): M = d_k (K tile read M-major), N = 64, K = 64 tokens
+        // dS = K^T [V~hi | V~lo]: M = d_k (K tile read M-major), N = 128, K = 64 tokens
 #pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(dcol + kColDS, dKm + ((ks * 2048) >> 4),
-                      dVt + ((part * kTileV + ks * 2048) >> 4), id_ds, (part | ks) != 0);
-        umma_commit(&bars->ds_ready[tb]);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tmem + kColDS, dKm + ((ks * 2048) >> 4), dVt + ((ks * 2048) >> 4), id_ds, ks > 0);
+        umma_commit(&bars->ds_ready);
         // O2 = (Phi + Plo) V: M = 64, N = 64, K = 64 tokens
 #pragma unroll
         for (int part = 0; part < 2; ++part)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(dcol + kColO2, dP + ((part * kTileP + ks * 32) >> 4), dV + ((ks * 2048) >> 4),
-                      id_pv, (part | ks) != 0);
+            umma_bf16(tmem + kColO2 + tb * 64, dP + ((part * kTileP + ks * 32) >> 4),
+                      dV + ((ks * 2048) >> 4), id_pv, (part | ks) != 0);
         umma_commit(&bars->p_free);  // P and V~ may be rewritten once these are done
         const int sb = c & 1;
         if (!wait_bar(&bars->s_ready[sb], ph, abort)) break;
+        // Q S accumulator is single: the previous chunk's outputs must be read
+        if (c > 0 && !wait_bar(&bars->o_free[(c - 1) & 1], (uint32_t)((c - 1) >> 1) & 1u, abort)) break;
         tc_fence_after();
-        const uint64_t dS = desc_sw128(sbase + kOffS + sb * 2 * kTileS, 16, 1024);
-        // O1 = Q (Shi + Slo): M = 64, N = 64, K = d_k (S tile rows = d_k, MN-major)
+        const uint64_t dS = desc_sw128(sbase + kOffS + sb * 2 * kTileS, kTileS, 1024);  // [hi | lo]
+        // O1 = Q [S_hi | S_lo]: M = 64, N = 128, K = d_k (S tile rows = d_k, MN-major)
 #pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t qoff = ((ks >> 2) * (kTileQ / 2) + (ks & 3) * 32) >> 4;
-            umma_bf16(dcol + kColO1, dQ + qoff, dS + ((part * kTileS + ks * 2048) >> 4), id_qs,
-                      (part | ks) != 0);
-          }
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t qoff = ((ks >> 2) * (kTileQ / 2) + (ks & 3) * 32) >> 4;
+          umma_bf16(tmem + kColO1, dQ + qoff, dS + ((ks * 2048) >> 4), id_qs, ks > 0);
+        }
         umma_commit(&bars->o_ready[tb]);
         umma_commit(&bars->empty[s]);
       }
@@ -280,8 +290,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============ warpgroup A: P = (Q K^T) * D and V~ = diag(r) V ============
     const int q4 = warp & 3;
     const int e = tid - 64;               // 0..127
-    const bool has_tok = lane < 16;       // holds a token row of the M = 64 tiles
-    const int tok = 16 * q4 + lane;       // that token row (valid when has_tok)
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     float *grow = s_g + warp * 2 * kC;
     Gates G;
@@ -295,15 +303,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if (!wait_bar_warp(&bars->qk_ready[tb], ph, abort)) break;
       tc_fence_after();
-      float qk[64];
+      // lane l < 16 holds row 16*q4 + l of QK^T (M = 64 layout); it keeps
+      // columns 0..31 and hands columns 32..63 to lane l + 16
+      float qk[32];
       {
-        float part[32];
-        tmem_ld32(tmem + tb * 256 + kColQK + lane_base, part);
+        float lo32[32], hi32[32];
+        tmem_ld32(tmem + kColQK + tb * 64 + lane_base, lo32);
+        tmem_ld32(tmem + kColQK + tb * 64 + 32 + lane_base, hi32);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) qk[j] = part[j];
-        tmem_ld32(tmem + tb * 256 + kColQK + 32 + lane_base, part);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) qk[32 + j] = part[j];
+        for (int j = 0; j < 32; ++j) {
+          const float x = __shfl_sync(0xffffffffu, hi32[j], lane & 15);
+          qk[j] = lane < 16 ? lo32[j] : x;
+        }
       }
       tc_fence_before();
       mbar_arrive(&bars->qk_free[tb]);
@@ -318,24 +329,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         cfrow[2 * lane + 1] = exp2f(-grow[2 * lane + 1]);
       }
       __syncwarp();
-      if (has_tok) {
+      {
+        const int row = 16 * q4 + (lane & 15), jb = 32 * (lane >> 4);
         const uint32_t phi = smem_u32(smem + kOffP);
         const uint32_t plo = phi + kTileP;
-        const float gi = grow[tok];
+        const float gi = grow[row];
         if (factored) {
           const float rf = exp2f(gi);
 #pragma unroll
-          for (int j = 0; j < kC; ++j) qk[j] = (j <= tok) ? qk[j] * rf * cfrow[j] : 0.f;
+          for (int jj = 0; jj < 32; ++jj) {
+            const int j = jb + jj;
+            qk[jj] = (j <= row) ? qk[jj] * rf * cfrow[j] : 0.f;
+          }
         } else {
 #pragma unroll
-          for (int j = 0; j < kC; ++j) qk[j] = (j <= tok) ? qk[j] * exp2f(gi - grow[j]) : 0.f;
+          for (int jj = 0; jj < 32; ++jj) {
+            const int j = jb + jj;
+            qk[jj] = (j <= row) ? qk[jj] * exp2f(gi - grow[j]) : 0.f;
+          }
         }
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int c4 = 0; c4 < 4; ++c4) {
           uint4 uh, ul;
-          split8(&qk[8 * ch], uh, ul);
-          sts128(phi + swz(tok, ch), uh);
-          sts128(plo + swz(tok, ch), ul);
+          split8(&qk[8 * c4], uh, ul);
+          const int ch = 4 * (lane >> 4) + c4;
+          sts128(phi + swz(row, ch), uh);
+          sts128(plo + swz(row, ch), ul);
         }
       }
       if (!wait_bar_warp(&bars->full[s], sph, abort)) break;
@@ -402,22 +421,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tb = c & 1;
       const uint32_t ph = (uint32_t)(c >> 1) & 1u;
       const int t0 = c * kC;
-      const uint32_t dcol = tmem + tb * 256 + lane_base;
       const float gC = gates_chunk(G, p, b, h, c, lane, grow);
 
-      // ---- S <- gamma_C S + K^T V~ --------------------------------------------
-      if (!wait_bar_warp(&bars->ds_ready[tb], ph, abort)) { ok = false; break; }
+      // ---- S <- gamma_C S + K^T V~ (the hi and lo column halves summed) -------
+      if (!wait_bar_warp(&bars->ds_ready, (uint32_t)c & 1u, abort)) { ok = false; break; }
       tc_fence_after();
       {
         const float gam = exp2f(gC);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          float ds[32];
-          tmem_ld32(dcol + kColDS + 32 * half, ds);
+          float dh[32], dl[32];
+          tmem_ld32(tmem + kColDS + 32 * half + lane_base, dh);
+          tmem_ld32(tmem + kColDS + kBV + 32 * half + lane_base, dl);
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) S[32 * half + jj] = gam * S[32 * half + jj] + ds[jj];
+          for (int jj = 0; jj < 32; ++jj) S[32 * half + jj] = gam * S[32 * half + jj] + (dh[jj] + dl[jj]);
         }
       }
+      tc_fence_before();
+      mbar_arrive(&bars->ds_free);
       if (c + 1 < nchunks) write_state((c + 1) & 1);
 
       // ---- o = gamma_i (Q S) + P V ----------------------------------------------
@@ -429,18 +450,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool store = has_tok && t < T;
         const size_t obase = (((size_t)b * T + t) * p.H + h) * kDK + vblk * kBV;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float o1[32], o2[32];
-          tmem_ld32(dcol + kColO1 + 32 * half, o1);
-          tmem_ld32(dcol + kColO2 + 32 * half, o2);
-          float ov[32];
+        for (int qt = 0; qt < 4; ++qt) {
+          float o1[16], o1l[16], o2[16];
+          tmem_ld16(tmem + kColO1 + 16 * qt + lane_base, o1);
+          tmem_ld16(tmem + kColO1 + kBV + 16 * qt + lane_base, o1l);
+          tmem_ld16(tmem + kColO2 + tb * 64 + 16 * qt + lane_base, o2);
+          float ov[16];
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) ov[jj] = gi * o1[jj] + o2[jj];
+          for (int jj = 0; jj < 16; ++jj) ov[jj] = gi * (o1[jj] + o1l[jj]) + o2[jj];
           if (store) {
             if (p.out_bf16) {
-              uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + obase + 32 * half);
+              uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + obase + 16 * qt);
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
+              for (int k = 0; k < 2; ++k) {
                 uint32_t pk[4];
 #pragma unroll
                 for (int m = 0; m < 4; ++m)
@@ -448,9 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dst[k] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
               }
             } else {
-              float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + obase + 32 * half);
+              float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + obase + 16 * qt);
 #pragma unroll
-              for (int k = 0; k < 8; ++k)
+              for (int k = 0; k < 4; ++k)
                 dst[k] = make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
             }
           }
