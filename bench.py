@@ -469,8 +469,54 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def run_profile(args):
+    """One workload alone, for a profiler: `launches` calls of the chosen hot
+    kernel on the bench's own inputs, nothing timed, no JSON line."""
+    import torch
+
+    from gated_deltanet_02_gb300 import GDN, GLA, glinattn_decode, glinattn_prefill, inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.profile == "gla":
+        c = GLA_CFG
+        ex = inputs.gla_prefill(c["B"], c["H"], c["T"], c["d"], seed=0, device=dev)
+        o = torch.empty(c["B"], c["T"], c["H"], c["d"], dtype=torch.bfloat16, device=dev)
+        S = torch.empty(c["B"], c["H"], c["d"], c["d"], dtype=torch.float32, device=dev)
+
+        def step():
+            glinattn_prefill(ex["q"], ex["k"], ex["v"], ex["alpha"], None, None, variant=GLA, o=o, S_T=S)
+    elif args.profile == "decode":
+        dc = DEC_CFG
+        dx = inputs.gdn_decode(dc["N"], dc["H"], dc["d"], dc["P"], seed=0, device=dev)
+        od = torch.empty(dc["N"], dc["H"], dc["d"], dtype=torch.bfloat16, device=dev)
+
+        def step():
+            glinattn_decode(dx["q"], dx["k"], dx["v"], dx["alpha"], dx["beta"], dx["pool"], dx["slot_ids"],
+                            variant=GDN, conv_w=dx["conv_w"], conv_pool=dx["conv_pool"], qk_l2norm=True,
+                            o=od)
+    else:
+        g = GDN_CFG
+        gx = inputs.gdn_prefill(g["B"], g["H"], g["T"], g["d"], seed=0, device=dev)
+        og = torch.empty(g["B"], g["T"], g["H"], g["d"], dtype=torch.bfloat16, device=dev)
+        Sg = torch.empty(g["B"], g["H"], g["d"], g["d"], dtype=torch.float32, device=dev)
+        from gated_deltanet_02_gb300.glinattn import prefill_workspace_size
+        wsb = torch.empty(prefill_workspace_size(g["B"], g["T"], g["H"], g["d"]), dtype=torch.uint8,
+                          device=dev)
+
+        def step():
+            glinattn_prefill(gx["q"], gx["k"], gx["v"], gx["alpha"], gx["beta"], gx["S0"], variant=GDN,
+                             conv_w=gx["conv_w"], qk_l2norm=True, o=og, S_T=Sg, workspace=wsb)
+    for _ in range(args.launches):
+        step()
+    torch.cuda.synchronize()
+    print(f"profile {args.profile}: {args.launches} launches done")
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile", choices=["gla", "decode", "gdn"], default=None,
+                    help="run one workload's kernel a few times for a profiler, then exit")
+    ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
@@ -480,7 +526,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
