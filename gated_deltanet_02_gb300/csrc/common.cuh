@@ -35,4 +35,8 @@ struct RecurParams {
 
 glinattn_status launch_recurrent(const RecurParams &p, int d, cudaStream_t stream);
 
+// Persistent pipelined decode / speculative decode for 128 x 128 pooled states.
+bool decode128_supports(const RecurParams &p, int d);
+cudaError_t launch_decode128(const RecurParams &p, cudaStream_t stream);
+
 }  // namespace glinattn

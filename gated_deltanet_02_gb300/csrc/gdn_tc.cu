@@ -45,8 +45,10 @@ using namespace tc;
 constexpr int kC = 64;   // chunk length
 constexpr int kD = 128;  // head size (d_k = d_v)
 
+// 1024-byte aligned pointer into the shared array, derived by pointer
+// arithmetic so the compiler keeps accesses through it in the shared space.
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
-  return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+  return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
 }
 
 // bf16 round-to-nearest-even of 8 floats, packed as 16 bytes.

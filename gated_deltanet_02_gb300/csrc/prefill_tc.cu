@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gla_prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, const GlaParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // stays in the shared space
   Bars *bars = reinterpret_cast<Bars *>(smem + kOffBar);
   float *s_g = reinterpret_cast<float *>(smem + kOffG);  // [warp][2][64] gate rows
   volatile int *abort = &bars->abort;

@@ -406,6 +406,8 @@ cudaError_t launch(const RecurParams &p, cudaStream_t stream) {
 
 glinattn_status launch_recurrent(const RecurParams &p, int d, cudaStream_t stream) {
   if ((long long)p.N * p.H == 0) return GLINATTN_OK;
+  if (decode128_supports(p, d))
+    return launch_decode128(p, stream) == cudaSuccess ? GLINATTN_OK : GLINATTN_ERR_CUDA;
   cudaError_t e;
   switch (d) {
     case 16: e = launch<16>(p, stream); break;

@@ -76,6 +76,13 @@ __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
+// Arrive without release semantics: orders nothing, so it does not wait for
+// this thread's earlier global stores to drain.  For a partner that only needs
+// to know that this CTA has passed a point (here: a copy it waited on landed).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }

@@ -52,8 +52,9 @@ def test_decode_matches_oracle_bf16(d, variant):
         assert np.array_equal(f64(cpool), cpool_ref)
 
 
-def test_decode_fp32_inputs_tight():
-    ex = inputs.gdn_decode(6, 2, 64, 10, seed=3, dtype=torch.float32)
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_fp32_inputs_tight(d):
+    ex = inputs.gdn_decode(6, 2, d, 10, seed=3, dtype=torch.float32)
     o, pool, cpool, st = _run_decode(ex, GDN, True, True)
     o_ref, pool_ref, cpool_ref = oracle.decode(
         GDN, f64(ex["q"]), f64(ex["k"]), f64(ex["v"]), f64(ex["alpha"]), f64(ex["beta"]),
@@ -114,6 +115,56 @@ def test_bad_slot_and_gate_are_flagged_and_skipped():
     assert not torch.equal(pool[s0, 0].cpu(), ex["pool"][s0, 0])
 
 
+def test_decode128_bad_slot_and_gate_are_flagged_and_skipped():
+    ex = inputs.gdn_decode(6, 3, 128, 12, seed=21)
+    ex["slot_ids"] = ex["slot_ids"].clone()
+    ex["slot_ids"][1] = 12  # out of range
+    ex["alpha"] = ex["alpha"].clone()
+    ex["alpha"][2, 1] = 1.5  # gate outside (0, 1]
+    o, pool, cpool, st = _run_decode(ex, GDN, True, True)
+    assert st == DEV_BAD_SLOT | DEV_BAD_GATE
+    s2 = int(ex["slot_ids"][2])
+    assert torch.equal(pool[s2, 1].cpu(), ex["pool"][s2, 1])
+    hd = [c for part in range(3) for c in range(part * 3 * 128 + 128, part * 3 * 128 + 256)]
+    assert torch.equal(cpool[s2][:, hd].cpu(), ex["conv_pool"][s2][:, hd])
+    # every other unit is updated as the oracle says
+    good = [0, 3, 4, 5]
+    sl = ex["slot_ids"][good].long()
+    o_ref, pool_ref, cpool_ref = oracle.decode(
+        GDN, f64(ex["q"][good]), f64(ex["k"][good]), f64(ex["v"][good]), f64(ex["alpha"][good]),
+        f64(ex["beta"][good]), f64(ex["pool"][sl]), list(range(len(good))), f64(ex["conv_w"]),
+        f64(ex["conv_pool"][sl]), True)
+    assert relerr(o[good], o_ref) <= TOL_O_BF16
+    assert relerr(pool[sl.to(DEV)], pool_ref) <= TOL_S_BF16
+    assert np.array_equal(f64(cpool[sl.to(DEV)]), cpool_ref)
+    # request 2: heads 0 and 2 are updated (the oracle run gets a valid gate for head 1)
+    a2 = ex["alpha"][2:3].clone()
+    a2[0, 1] = 0.5
+    s2t = torch.tensor([s2])
+    _, p2_ref, _ = oracle.decode(
+        GDN, f64(ex["q"][2:3]), f64(ex["k"][2:3]), f64(ex["v"][2:3]), f64(a2), f64(ex["beta"][2:3]),
+        f64(ex["pool"][s2t]), [0], f64(ex["conv_w"]), f64(ex["conv_pool"][s2t]), True)
+    for h in (0, 2):
+        assert relerr(pool[s2, h], p2_ref[0, h]) <= TOL_S_BF16
+
+
+def test_decode128_many_units_per_cluster():
+    """3 requests x 600 heads: each persistent cluster walks several units in
+    turn, and the head (hence the conv weights) changes every 3 units."""
+    N, H, d, P = 3, 600, 128, 4
+    ex = inputs.gdn_decode(N, H, d, P, seed=13)
+    o, pool, cpool, st = _run_decode(ex, GDN, True, True, out_dtype=torch.bfloat16)
+    assert st == 0
+    o_ref, pool_ref, cpool_ref = oracle.decode(
+        GDN, f64(ex["q"]), f64(ex["k"]), f64(ex["v"]), f64(ex["alpha"]), f64(ex["beta"]),
+        f64(ex["pool"]), ex["slot_ids"].tolist(), f64(ex["conv_w"]), f64(ex["conv_pool"]), True)
+    err = np.abs(f64(o) - o_ref)
+    assert (err <= np.abs(o_ref) * 2.0 ** -8 + TOL_O_BF16 * np.abs(o_ref).max()).all()
+    sl = ex["slot_ids"].long()
+    assert relerr(pool[sl.to(DEV)], pool_ref[sl.numpy()]) <= TOL_S_BF16
+    assert np.array_equal(f64(cpool), cpool_ref)
+
+
 def _spec_setup(N, D, H, d, P, seed):
     base = inputs.gdn_decode(N, H, d, P, seed=seed)
     dr = inputs.spec_drafts(N, D, H, d, seed=seed + 100)
@@ -123,8 +174,11 @@ def _spec_setup(N, D, H, d, P, seed):
     return base, dr, src, dst
 
 
-def test_spec_decode_matches_oracle_and_repeated_decode():
-    N, D, H, d, P = 6, 4, 3, 128, 64
+@pytest.mark.parametrize("D,P", [(4, 64), (10, 80)])
+def test_spec_decode_matches_oracle_and_repeated_decode(D, P):
+    """D = 10 drafts also covers steps whose gates and slots are read past the
+    per-unit table of the d = 128 kernel."""
+    N, H, d = 6, 3, 128
     base, dr, src, dst = _spec_setup(N, D, H, d, P, 7)
     pool, cpool = base["pool"].to(DEV), base["conv_pool"].to(DEV)
     g = to(dr, DEV)
