@@ -62,20 +62,16 @@ __device__ __forceinline__ uint4 pack8_rn(const float *x) {
 // ================================ pass A ====================================
 
 constexpr int kPrepThreads = 256;
-constexpr int kRawRows = kC + 3;                 // the chunk and 3 tokens of conv history
-constexpr uint32_t kRawPartBytes = kD * 2 + 16;  // one part (q, k or v) of a token, padded
-constexpr uint32_t kRawRowBytes = 3 * kRawPartBytes;  // padding spreads rows and parts over banks
-constexpr uint32_t kOffRaw = 0;                  // raw [67][3][136] bf16
-constexpr uint32_t kOffAmat = 0;                 // after the front end: A [64][65] fp32
-constexpr uint32_t kOffTm = 17408;               // then (I+A)^-1 diag(beta gamma) hi, lo and
-                                                 // (I+A)^-1 diag(beta) hi, lo: 4 x 8 KiB
-constexpr uint32_t kOffW4 = 55296;               // conv weights [384][4] fp32
+constexpr int kBlk = 32;                         // the inverse works on 32 x 32 blocks
+constexpr uint32_t kBlkBytes = kBlk * (kBlk + 1) * 4;  // one fp32 block, rows padded to 33
+constexpr uint32_t kOffA = 0;                    // A00, A10, A11 (A00 later holds X = A10 T00)
+constexpr uint32_t kOffT = 3 * kBlkBytes;        // T00, T10, T11 of T = (I + A)^-1
+constexpr uint32_t kOffTm = 25600;               // T diag(beta gamma) hi, lo and T diag(beta) hi, lo: 4 x 8 KiB
 constexpr uint32_t kOffQK = 61440;               // stacked [Q'; K']: 2 column blocks x 128 rows x 128 B
 constexpr uint32_t kOffVp = kOffQK + 32768;      // V': 2 column blocks x 64 rows x 128 B
 constexpr uint32_t kOffMisc = kOffVp + 16384;    // g2[64], beta[64], barrier, TMEM slot
 constexpr uint32_t kPrepSmem = kOffMisc + 1024 + 1024;
-static_assert(kOffRaw + kRawRows * kRawRowBytes <= kOffW4, "raw tile");
-static_assert(kOffAmat + 64 * 65 * 4 <= kOffTm && kOffTm + 4 * 8192 <= kOffW4, "aliases");
+static_assert(kOffT + 3 * kBlkBytes <= kOffTm && kOffTm + 4 * 8192 <= kOffQK, "pass A layout");
 static_assert(kOffQK % 1024 == 0 && kOffVp % 1024 == 0 && kOffTm % 1024 == 0, "alignment");
 
 struct PrepParams {
@@ -111,44 +107,77 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
     tmem_relinquish();
   }
 
-  // ---- raw tile: tokens t0-3 .. t0+63, history from conv_in (or zero) ---------
-  uint8_t *raw = smem + kOffRaw;
-  {
-    // every load of the tile is issued before the first store
-    constexpr int kItems = kRawRows * 48, kRounds = (kItems + kPrepThreads - 1) / kPrepThreads;
-    uint4 vals[kRounds];
+  // ---- front end: y_t = sum_j w_j x_{t-3+j}; L2 norm of q, k rows; bf16 -------
+  // A task is (part, 8 consecutive tokens) of the chunk: a warp slides the
+  // 4-tap window along its tokens, lane l owning channels 4l .. 4l+3, so every
+  // load and store is 8 bytes per lane and the L2 norm is one warp reduction.
+  // Each warp has three tasks; the next task's rows are loaded before the
+  // current one is computed.  History before the sequence comes from conv_in
+  // (or is zero).
+  struct FeTask {
+    uint2 x[11];  // rows r0 - 3 .. r0 + 7 of the part: 4 bf16 channels each
+    float4 w[4];  // the 4 taps of channels 4l .. 4l+3
+  };
+  auto fe_load = [&](int task, FeTask &f) {
+    const int part = task % 3, r0 = (task / 3) * 8;
+    const __nv_bfloat16 *src = part == 0 ? p.q : (part == 1 ? p.k : p.v);
 #pragma unroll
-    for (int m = 0; m < kRounds; ++m) {
-      const int it = tid + m * kPrepThreads;
-      vals[m] = make_uint4(0u, 0u, 0u, 0u);
-      if (it < kItems) {
-        const int r = it / 48, rem = it - r * 48, part = rem >> 4, q16 = rem & 15;
-        const int t = t0 - 3 + r;
-        if (t >= 0 && t < T) {
-          const __nv_bfloat16 *src = part == 0 ? p.q : (part == 1 ? p.k : p.v);
-          vals[m] = *reinterpret_cast<const uint4 *>(src + (((size_t)b * T + t) * H + h) * kD + q16 * 8);
-        } else if (t < 0 && p.has_conv && p.conv_in) {
-          vals[m] = *reinterpret_cast<const uint4 *>(p.conv_in + ((size_t)b * 3 + (t + 3)) * Cch +
-                                                     part * H * kD + h * kD + q16 * 8);
-        }
-      }
+    for (int m = 0; m < 11; ++m) {
+      const int t = t0 + r0 - 3 + m;
+      uint2 v = make_uint2(0u, 0u);
+      if (t >= 0 && t < T)
+        v = *reinterpret_cast<const uint2 *>(src + (((size_t)b * T + t) * H + h) * kD + 4 * lane);
+      else if (t < 0 && p.has_conv && p.conv_in)
+        v = *reinterpret_cast<const uint2 *>(p.conv_in + ((size_t)b * 3 + (t + 3)) * Cch + part * H * kD +
+                                             h * kD + 4 * lane);
+      f.x[m] = v;
     }
 #pragma unroll
-    for (int m = 0; m < kRounds; ++m) {
-      const int it = tid + m * kPrepThreads;
-      if (it < kItems) {
-        const int r = it / 48, rem = it - r * 48, part = rem >> 4, q16 = rem & 15;
-        *reinterpret_cast<uint4 *>(raw + r * kRawRowBytes + part * kRawPartBytes + q16 * 16) = vals[m];
+    for (int c2 = 0; c2 < 4; ++c2)
+      f.w[c2] = p.has_conv ? *reinterpret_cast<const float4 *>(
+                                 p.conv_w + ((size_t)part * H * kD + h * kD + 4 * lane + c2) * 4)
+                           : make_float4(0.f, 0.f, 0.f, 1.f);
+  };
+  uint8_t *qk = smem + kOffQK;
+  uint8_t *vp = smem + kOffVp;
+  auto fe_compute = [&](int task, const FeTask &f) {
+    const int part = task % 3, r0 = (task / 3) * 8;
+    // channels 4l .. 4l+3: column block l / 16, 16-byte chunk (l % 16) / 2, half l % 2
+    const uint32_t cb = (uint32_t)(lane >> 4), ch = (uint32_t)((lane & 15) >> 1), hb = (uint32_t)(lane & 1) * 8;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      float y[4];
+#pragma unroll
+      for (int c2 = 0; c2 < 4; ++c2) {
+        // bf16 channel c2 of row m: low or high half of word c2 / 2
+        auto xv = [&](int m) {
+          const uint32_t wd = (c2 >> 1) ? f.x[m].y : f.x[m].x;
+          return __uint_as_float((c2 & 1) ? (wd & 0xffff0000u) : (wd << 16));
+        };
+        const float4 wc = f.w[c2];
+        y[c2] = wc.x * xv(r) + wc.y * xv(r + 1) + wc.z * xv(r + 2) + wc.w * xv(r + 3);
       }
+      if (part < 2 && p.qk_l2norm) {
+        float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float inv = 1.f / sqrtf(ss + 1e-6f);
+#pragma unroll
+        for (int c2 = 0; c2 < 4; ++c2) y[c2] *= inv;
+      }
+      const bool valid = t0 + r0 + r < T;
+      uint2 pk;
+      pk.x = bits(__floats2bfloat162_rn(valid ? y[0] : 0.f, valid ? y[1] : 0.f));
+      pk.y = bits(__floats2bfloat162_rn(valid ? y[2] : 0.f, valid ? y[3] : 0.f));
+      const int t = r0 + r;
+      if (part < 2)
+        *reinterpret_cast<uint2 *>(qk + cb * 16384 + swz(part * kC + t, ch) + hb) = pk;
+      else
+        *reinterpret_cast<uint2 *>(vp + cb * 8192 + swz(t, ch) + hb) = pk;
     }
-  }
-  float *w4 = reinterpret_cast<float *>(smem + kOffW4);
-  if (p.has_conv)
-    for (int i = tid; i < 3 * kD; i += kPrepThreads) {
-      const int part = i / kD, ch = i - part * kD;
-      *reinterpret_cast<float4 *>(w4 + i * 4) =
-          *reinterpret_cast<const float4 *>(p.conv_w + ((size_t)part * H * kD + h * kD + ch) * 4);
-    }
+  };
+  FeTask fa, fb;
+  fe_load(warp, fa);  // 24 tasks, three per warp
   // ---- gates of the chunk (warp 0): g2 = cumsum(log2 alpha); alpha = 1, beta = 0 past T
   if (warp == 0) {
     const int ta = t0 + 2 * lane, tb = ta + 1;
@@ -171,64 +200,12 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
     p.Gp[unit * p.Tp + t0 + 2 * lane] = ga;
     p.Gp[unit * p.Tp + t0 + 2 * lane + 1] = gb;
   }
-  __syncthreads();
 
-  // ---- front end: y_t = sum_j w_j x_{t-3+j}; L2 norm of q, k rows; bf16 -------
-  // task = (token t, part, lane l of 8): channels l, l+8, ..., l+120, so the 8
-  // lanes of a task group read consecutive weights and raw elements.
-  uint8_t *qk = smem + kOffQK;
-  uint8_t *vp = smem + kOffVp;
-  for (int task = tid; task < kC * 3 * 8; task += kPrepThreads) {  // 6 rounds, uniform
-    const int l = task & 7, tp = task >> 3, part = tp % 3, t = tp / 3;
-    float y[16];
-    if (p.has_conv) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] = 0.f;
-      const float *w = w4 + (part * kD + l) * 4;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float4 wc = *reinterpret_cast<const float4 *>(w + i * 32);
-        const uint8_t *src = raw + t * kRawRowBytes + part * kRawPartBytes + (l + 8 * i) * 2;
-        const float x0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(src));
-        const float x1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(src + kRawRowBytes));
-        const float x2 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(src + 2 * kRawRowBytes));
-        const float x3 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(src + 3 * kRawRowBytes));
-        y[i] = wc.x * x0 + wc.y * x1 + wc.z * x2 + wc.w * x3;
-      }
-    } else {
-      const uint8_t *src = raw + (t + 3) * kRawRowBytes + part * kRawPartBytes + l * 2;
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        y[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(src + 16 * i));
-    }
-    if (part < 2 && p.qk_l2norm) {
-      float ss = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) ss += y[i] * y[i];
-      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-      ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-      const float inv = 1.f / sqrtf(ss + 1e-6f);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] *= inv;
-    }
-    const bool valid = t0 + t < T;
-    // element l of every 16-byte chunk i (= channels 8i .. 8i+7) of the row
-    if (part < 2) {
-      const int row = part * kC + t;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const __nv_bfloat16 v = __float2bfloat16_rn(valid ? y[i] : 0.f);
-        *reinterpret_cast<__nv_bfloat16 *>(qk + (i >> 3) * 16384 + swz(row, i & 7) + l * 2) = v;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const __nv_bfloat16 v = __float2bfloat16_rn(valid ? y[i] : 0.f);
-        *reinterpret_cast<__nv_bfloat16 *>(vp + (i >> 3) * 8192 + swz(t, i & 7) + l * 2) = v;
-      }
-    }
-  }
+  fe_load(warp + 8, fb);
+  fe_compute(warp, fa);
+  fe_load(warp + 16, fa);
+  fe_compute(warp + 8, fb);
+  fe_compute(warp + 16, fa);
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -257,7 +234,14 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
   tc_fence_after();
 
   // ---- A_ij = beta_i 2^(g_i - g_j) (k_i . k_j) for j < i (rows from TMEM lanes 64..127)
-  float *A = reinterpret_cast<float *>(smem + kOffAmat);
+  // stored as the blocks A00, A10, A11 of 32 x 32 (A01 is zero)
+  float *A00 = reinterpret_cast<float *>(smem + kOffA);
+  float *A10 = A00 + kBlk * (kBlk + 1);
+  float *A11 = A10 + kBlk * (kBlk + 1);
+  float *T00 = reinterpret_cast<float *>(smem + kOffT);
+  float *T10 = T00 + kBlk * (kBlk + 1);
+  float *T11 = T10 + kBlk * (kBlk + 1);
+  constexpr int kLd = kBlk + 1;
   if (ok && (warp == 2 || warp == 3)) {
     const int i = 32 * (warp - 2) + lane;
     float kk[64];
@@ -271,48 +255,102 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
       for (int j = 0; j < 32; ++j) kk[32 + j] = part[j];
     }
     const float gi = g2s[i], bi = betas[i];
+    if (warp == 2) {
 #pragma unroll
-    for (int j = 0; j < 64; ++j) A[i * 65 + j] = (j < i) ? bi * exp2f(gi - g2s[j]) * kk[j] : 0.f;
+      for (int j = 0; j < 32; ++j) A00[lane * kLd + j] = (j < i) ? bi * exp2f(gi - g2s[j]) * kk[j] : 0.f;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) A10[lane * kLd + j] = bi * exp2f(gi - g2s[j]) * kk[j];
+#pragma unroll
+      for (int j = 32; j < 64; ++j) A11[lane * kLd + j - 32] = (j < i) ? bi * exp2f(gi - g2s[j]) * kk[j] : 0.f;
+    }
   }
   __syncthreads();
 
-  // ---- (I + A)^-1 by forward substitution: 4 lanes solve column k = tid / 4 ----
-  // x_i = [i == k] - sum_{j < i} A_ij x_j; lane `sub` holds x_j for j = sub (mod 4)
-  // and the partial sums over its j are combined with two shuffles per row.
+  // ---- T = (I + A)^-1 in 32 x 32 blocks ---------------------------------------
+  // T00 = (I + A00)^-1 and T11 = (I + A11)^-1 by forward substitution, both at
+  // once: 4 lanes solve column kc of one block, lane `sub` holding x_j for
+  // j = sub (mod 4), the partial sums combined with two shuffles per row.
+  // Then T10 = -T11 A10 T00 as two fp32 products (T01 = 0).
   if (ok) {
-    const int k = tid >> 2, sub = tid & 3;
-    float xs[16];
+    const int k = tid >> 2, sub = tid & 3, blk = k >> 5, kc = k & 31;
+    const float *Ab = blk ? A11 : A00;
+    float xs[8];
 #pragma unroll
-    for (int m = 0; m < 16; ++m) xs[m] = 0.f;
+    for (int m = 0; m < 8; ++m) xs[m] = 0.f;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
+    for (int i = 0; i < kBlk; ++i) {
       float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-      for (int m = 0; 4 * m + sub < i && m < 16; m += 2) {
-        s0 += A[i * 65 + 4 * m + sub] * xs[m];
-        if (4 * (m + 1) + sub < i) s1 += A[i * 65 + 4 * (m + 1) + sub] * xs[m + 1];
+      for (int m = 0; 4 * m + sub < i && m < 8; m += 2) {
+        s0 += Ab[i * kLd + 4 * m + sub] * xs[m];
+        if (4 * (m + 1) + sub < i) s1 += Ab[i * kLd + 4 * (m + 1) + sub] * xs[m + 1];
       }
       float sum = s0 + s1;
       sum += __shfl_xor_sync(0xffffffffu, sum, 1);
       sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-      if ((i & 3) == sub) xs[i >> 2] = (i == k ? 1.f : 0.f) - sum;
+      if ((i & 3) == sub) xs[i >> 2] = (i == kc ? 1.f : 0.f) - sum;
     }
-    const float bk = betas[k], bgk = bk * exp2f(g2s[k]);
-    uint8_t *tm1 = smem + kOffTm;  // (I+A)^-1 diag(beta gamma): hi, lo
-    uint8_t *tm2 = tm1 + 16384;    // (I+A)^-1 diag(beta): hi, lo
-    const uint32_t colb = (uint32_t)(k & 7) * 2;
+    float *Tb = blk ? T11 : T00;
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const int i = 4 * m + sub;
-      const float w1 = xs[m] * bgk, w2 = xs[m] * bk;
-      const __nv_bfloat16 h1 = __float2bfloat16_rn(w1), h2 = __float2bfloat16_rn(w2);
-      const __nv_bfloat16 l1 = __float2bfloat16_rn(w1 - __bfloat162float(h1));
-      const __nv_bfloat16 l2 = __float2bfloat16_rn(w2 - __bfloat162float(h2));
-      const uint32_t off = swz(i, k >> 3) + colb;
-      *reinterpret_cast<__nv_bfloat16 *>(tm1 + off) = h1;
-      *reinterpret_cast<__nv_bfloat16 *>(tm1 + 8192 + off) = l1;
-      *reinterpret_cast<__nv_bfloat16 *>(tm2 + off) = h2;
-      *reinterpret_cast<__nv_bfloat16 *>(tm2 + 8192 + off) = l2;
+    for (int m = 0; m < 8; ++m) Tb[(4 * m + sub) * kLd + kc] = xs[m];
+  }
+  __syncthreads();
+  float *X = A00;  // A00 is no longer needed: X = A10 T00 takes its place
+  if (ok) {
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int i = warp + 8 * rr;
+      float acc = 0.f;
+#pragma unroll 8
+      for (int j = 0; j < kBlk; ++j) acc += A10[i * kLd + j] * T00[j * kLd + lane];
+      X[i * kLd + lane] = acc;
+    }
+  }
+  __syncthreads();
+  if (ok) {
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int i = warp + 8 * rr;
+      float acc = 0.f;
+#pragma unroll 8
+      for (int j = 0; j < kBlk; ++j) acc += T11[i * kLd + j] * X[j * kLd + lane];
+      T10[i * kLd + lane] = -acc;
+    }
+  }
+  __syncthreads();
+  // ---- T diag(beta gamma) and T diag(beta) as bf16 hi / lo MMA tiles ------------
+  if (ok) {
+    uint8_t *tm1 = smem + kOffTm;  // T diag(beta gamma): hi, lo
+    uint8_t *tm2 = tm1 + 16384;    // T diag(beta): hi, lo
+    for (int it = tid; it < kC * 8; it += kPrepThreads) {  // (row i, 8-column chunk)
+      const int i = it >> 3, chk = it & 7;
+      float w1[8], w2[8];
+#pragma unroll
+      for (int e2 = 0; e2 < 8; ++e2) {
+        const int k = 8 * chk + e2;
+        float tv;
+        if (i < kBlk) tv = k < kBlk ? T00[i * kLd + k] : 0.f;
+        else tv = k < kBlk ? T10[(i - kBlk) * kLd + k] : T11[(i - kBlk) * kLd + (k - kBlk)];
+        const float bk = betas[k];
+        w1[e2] = tv * (bk * exp2f(g2s[k]));
+        w2[e2] = tv * bk;
+      }
+      uint32_t h1[4], l1[4], h2[4], l2[4];
+#pragma unroll
+      for (int q2 = 0; q2 < 4; ++q2) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(w1[2 * q2], w1[2 * q2 + 1]);
+        const __nv_bfloat162 c2 = __floats2bfloat162_rn(w2[2 * q2], w2[2 * q2 + 1]);
+        h1[q2] = bits(a);
+        h2[q2] = bits(c2);
+        l1[q2] = bits(__floats2bfloat162_rn(w1[2 * q2] - __low2float(a), w1[2 * q2 + 1] - __high2float(a)));
+        l2[q2] = bits(__floats2bfloat162_rn(w2[2 * q2] - __low2float(c2), w2[2 * q2 + 1] - __high2float(c2)));
+      }
+      const uint32_t off = swz(i, chk);
+      *reinterpret_cast<uint4 *>(tm1 + off) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+      *reinterpret_cast<uint4 *>(tm1 + 8192 + off) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
+      *reinterpret_cast<uint4 *>(tm2 + off) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+      *reinterpret_cast<uint4 *>(tm2 + 8192 + off) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
     }
   }
   fence_proxy_async_smem();
