@@ -411,28 +411,33 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
 
 // ================================ pass B ====================================
 
-constexpr int kBV = 64;
+constexpr int kBV = 32;          // d_v columns per CTA
+constexpr int kNV = kD / kBV;    // CTAs per (batch, head)
 constexpr int kStages = 2;
 constexpr int kPrefetch = 3;  // chunks prefetched into L2 beyond the shared-memory ring
 constexpr int kThreads = 320;    // warp 0 TMA, warp 1 MMA, warps 2-5 (P), 6-9 (state, outputs)
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kTile = kC * kD * 2;        // Q', K' or W tile: 16 KiB (2 column blocks)
-constexpr uint32_t kTileU = kC * kBV * 4;      // U~ slice, fp32: 16 KiB
+constexpr uint32_t kTileU = kC * kBV * 4;      // U~ slice, fp32: 8 KiB
 constexpr uint32_t kStageBytes = 3 * kTile + kTileU;
 constexpr uint32_t kTileP = kC * kC * 2;       // 8 KiB (one of hi / lo)
-constexpr uint32_t kTileV = kC * kBV * 2;      // 8 KiB
-constexpr uint32_t kTileS = kD * kBV * 2;      // 16 KiB
+// A d_v slice of 32 bf16 high parts and its 32 remainders share one 128-byte
+// swizzled row, so [hi | lo] is a single 64-wide MMA operand.
+constexpr uint32_t kTileHL = kC * 128;         // [U_hi | U_lo] or [rU_hi | rU_lo]: 8 KiB
+constexpr uint32_t kTileS = kD * 128;          // [S_hi | S_lo]: 16 KiB
 constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffP = kStages * kStageBytes;   // P hi, lo
-constexpr uint32_t kOffU = kOffP + 2 * kTileP;      // U hi, lo
-constexpr uint32_t kOffRU = kOffU + 2 * kTileV;     // r U hi, lo
-constexpr uint32_t kOffS = kOffRU + 2 * kTileV;     // S hi, lo
-constexpr uint32_t kOffG = kOffS + 2 * kTileS;      // gate rows [warp][2][64]
+constexpr uint32_t kOffU = kOffP + 2 * kTileP;      // [U_hi | U_lo]
+constexpr uint32_t kOffRU = kOffU + kTileHL;        // [rU_hi | rU_lo]
+constexpr uint32_t kOffS = kOffRU + kTileHL;        // [S_hi | S_lo]
+constexpr uint32_t kOffG = kOffS + kTileS;          // gate rows [warp][2][64]
 constexpr uint32_t kOffBar = kOffG + (kThreads / 32) * 2 * kC * 4;
 constexpr uint32_t kScanSmem = kOffBar + 256 + 1024;
 static_assert(kScanSmem <= 232448, "shared memory budget");
-// TMEM: Q'K'^T (64), W[S_hi|S_lo] (128), K'^T[rU_hi|rU_lo] (128), Q'[S_hi|S_lo] (128), P U (64)
-constexpr uint32_t kColQK = 0, kColWS = 64, kColDS = 192, kColQS = 320, kColPU = 448;
+static_assert(kOffP % 1024 == 0 && kOffU % 1024 == 0 && kOffRU % 1024 == 0 && kOffS % 1024 == 0, "alignment");
+// TMEM (64 columns each, the hi and lo products side by side): Q'K'^T,
+// W[S_hi|S_lo], K'^T[rU_hi|rU_lo], Q'[S_hi|S_lo], P[U_hi|U_lo]
+constexpr uint32_t kColQK = 0, kColWS = 64, kColDS = 128, kColQS = 192, kColPU = 256;
 
 struct ScanParams {
   int B, T, H, nchunks, Tp, out_bf16;
@@ -491,8 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort = &bars->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int vblk = blockIdx.x & 1;
-  const int bh = blockIdx.x >> 1;
+  const int vblk = blockIdx.x % kNV;
+  const int bh = blockIdx.x / kNV;
   const int b = bh / p.H, h = bh - b * p.H;
   const size_t unit = (size_t)bh;
   const int T = p.T, nchunks = p.nchunks;
@@ -603,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);        // Q' K'^T
       constexpr uint32_t id_xs = idesc_bf16(64, 2 * kBV, false, true);    // W [S_hi|S_lo], Q' [..]
       constexpr uint32_t id_ds = idesc_bf16(128, 2 * kBV, true, true);    // K'^T [rU_hi|rU_lo]
-      constexpr uint32_t id_pu = idesc_bf16(64, kBV, false, true);        // P U
+      constexpr uint32_t id_pu = idesc_bf16(64, 2 * kBV, false, true);    // P [U_hi|U_lo]
       const uint32_t sbase = smem_u32(smem);
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % kStages;
@@ -612,10 +617,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dQ = desc_sw128(aQ, 16, 1024), dK = desc_sw128(aQ + kTile, 16, 1024);
         const uint64_t dKm = desc_sw128(aQ + kTile, kTile / 2, 1024);
         const uint64_t dW = desc_sw128(aQ + 2 * kTile, 16, 1024);
-        const uint64_t dS = desc_sw128(sbase + kOffS, kTileS, 1024);    // [S_hi | S_lo]
+        const uint64_t dS = desc_sw128(sbase + kOffS, 16, 1024);    // [S_hi | S_lo], one 64-wide block
         const uint64_t dP = desc_sw128(sbase + kOffP, 16, 1024);
-        const uint64_t dU = desc_sw128(sbase + kOffU, 16, 1024);
-        const uint64_t dRU = desc_sw128(sbase + kOffRU, kTileV, 1024);  // [rU_hi | rU_lo]
+        const uint64_t dU = desc_sw128(sbase + kOffU, 16, 1024);    // [U_hi | U_lo]
+        const uint64_t dRU = desc_sw128(sbase + kOffRU, 16, 1024);  // [rU_hi | rU_lo]
         // Q' K'^T: M = 64 tokens, N = 64 tokens, K = d_k
         if (!wait_bar(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) break;
         if (!wait_bar(&bars->qk_free, pc ^ 1u, abort)) break;
@@ -626,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16(tmem + kColQK, dQ + off, dK + off, id_qk, ks > 0);
         }
         umma_commit(&bars->qk_ready);
-        // W [S_hi | S_lo]: M = 64, N = 128, K = d_k (W tile K-major, S tiles MN-major)
+        // W [S_hi | S_lo]: M = 64, N = 64, K = d_k (W tile K-major, S tile MN-major)
         if (!wait_bar(&bars->s_ready, pc, abort)) break;
         tc_fence_after();
 #pragma unroll
@@ -646,20 +651,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bar(&bars->u_ready, pc, abort)) break;
         if (!wait_bar(&bars->p_ready, pc, abort)) break;
         tc_fence_after();
-        // dS = K'^T [rU_hi | rU_lo]: M = d_k (K' tile read M-major), N = 128, K = 64 tokens
+        // dS = K'^T [rU_hi | rU_lo]: M = d_k (K' tile read M-major), N = 64, K = 64 tokens
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           umma_bf16(tmem + kColDS, dKm + ((ks * 2048) >> 4), dRU + ((ks * 2048) >> 4), id_ds, ks > 0);
         umma_commit(&bars->ds_ready);
-        // P U = Phi Uhi + Phi Ulo + Plo Uhi: M = 64, N = 64, K = 64 tokens
+        // (Phi + Plo) [U_hi | U_lo]: M = 64, N = 64, K = 64 tokens
 #pragma unroll
-        for (int part = 0; part < 3; ++part)
+        for (int part = 0; part < 2; ++part)
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const int pp = part == 2 ? 1 : 0, up = part == 1 ? 1 : 0;
-            umma_bf16(tmem + kColPU, dP + ((pp * kTileP + ks * 32) >> 4),
-                      dU + ((up * kTileV + ks * 2048) >> 4), id_pu, (part | ks) != 0);
-          }
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tmem + kColPU, dP + ((part * kTileP + ks * 32) >> 4), dU + ((ks * 2048) >> 4), id_pu,
+                      (part | ks) != 0);
         umma_commit(&bars->o_ready);
         umma_commit(&bars->p_free);
         umma_commit(&bars->empty[s]);
@@ -736,7 +739,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int srow = 32 * q4 + lane;
     const bool has_tok = lane < 16;
     const int tok = 16 * q4 + lane;
-    const int urow = 16 * q4 + (lane & 15), ub = 32 * (lane >> 4);  // U row / column half
+    // U rows: lane l < 16 takes columns 0..15 of row 16*q4 + l, lane l + 16 columns 16..31
+    const int urow = 16 * q4 + (lane & 15), uh = lane >> 4;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     float *grow = s_g + warp * 2 * kC;
     GateRow G;
@@ -750,14 +754,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         S[j] = v4.x; S[j + 1] = v4.y; S[j + 2] = v4.z; S[j + 3] = v4.w;
       }
     }
+    // S row srow as [hi | lo]: 16-byte chunks 0-3 hold the high parts, 4-7 the remainders
     auto write_state = [&]() {
-      const uint32_t hi = smem_u32(smem + kOffS), lo = hi + kTileS;
+      const uint32_t sb = smem_u32(smem + kOffS);
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint4 uh, ul;
-        split8(&S[8 * ch], uh, ul);
-        sts128(hi + swz(srow, ch), uh);
-        sts128(lo + swz(srow, ch), ul);
+      for (int ch = 0; ch < 4; ++ch) {
+        uint4 vh, vl;
+        split8(&S[8 * ch], vh, vl);
+        sts128(sb + swz(srow, ch), vh);
+        sts128(sb + swz(srow, 4 + ch), vl);
       }
       fence_proxy_async_smem();
       mbar_arrive(&bars->s_ready);
@@ -772,33 +777,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float gC = grow_chunk(G, p, unit, c, lane, grow);
       const float g_tok = grow[tok & (kC - 1)];
 
-      // ---- U = U~ - W S: lane l < 16 takes columns 0..31 of row 16*q4 + l,
-      // lane l + 16 columns 32..63; the W S hi and lo halves are summed
+      // ---- U = U~ - W S (the hi and lo products summed) ---------------------------
       if (!wait_bar_warp(&bars->ws_ready, pc, abort)) { ok = false; break; }
       tc_fence_after();
-      float u[32];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
+      float u[16];
+      {
         float hi[16], lo[16];
-        tmem_ld16(tmem + kColWS + 16 * q + lane_base, hi);        // columns 16q.. of the hi half
-        tmem_ld16(tmem + kColWS + kBV + 16 * q + lane_base, lo);  // and of the lo half
+        tmem_ld16(tmem + kColWS + lane_base, hi);        // W S_hi, columns 0..15
+        tmem_ld16(tmem + kColWS + kBV + lane_base, lo);  // W S_lo, columns 0..15
 #pragma unroll
-        for (int j = 0; j < 16; ++j) u[16 * q + j] = hi[j] + lo[j];
-        tmem_ld16(tmem + kColWS + 32 + 16 * q + lane_base, hi);   // columns 32 + 16q..
-        tmem_ld16(tmem + kColWS + kBV + 32 + 16 * q + lane_base, lo);
+        for (int j = 0; j < 16; ++j) u[j] = hi[j] + lo[j];
+        tmem_ld16(tmem + kColWS + 16 + lane_base, hi);        // columns 16..31
+        tmem_ld16(tmem + kColWS + kBV + 16 + lane_base, lo);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const float x = __shfl_sync(0xffffffffu, hi[j] + lo[j], lane & 15);
-          if (lane >= 16) u[16 * q + j] = x;
+          if (lane >= 16) u[j] = x;
         }
       }
       if (!wait_bar_warp(&bars->full[s], sph, abort)) { ok = false; break; }
       if (!wait_bar_warp(&bars->p_free, pc ^ 1u, abort)) { ok = false; break; }
       {
         const float *ut = reinterpret_cast<const float *>(smem + kOffStage + s * kStageBytes + 3 * kTile) +
-                          urow * kBV + ub;
+                          urow * kBV + 16 * uh;
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
+        for (int j = 0; j < 16; j += 4) {
           const float4 v4 = *reinterpret_cast<const float4 *>(ut + j);
           u[j] = v4.x - u[j];
           u[j + 1] = v4.y - u[j + 1];
@@ -806,43 +809,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           u[j + 3] = v4.w - u[j + 3];
         }
         const float r = exp2f(gC - grow[urow]);
-        const uint32_t uhi = smem_u32(smem + kOffU), ulo = uhi + kTileV;
-        const uint32_t rhi = smem_u32(smem + kOffRU), rlo = rhi + kTileV;
+        const uint32_t ub = smem_u32(smem + kOffU), rb = smem_u32(smem + kOffRU);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const int ch = 4 * (lane >> 4) + c4;
-          uint4 uh, ul;
-          split8(&u[8 * c4], uh, ul);
-          sts128(uhi + swz(urow, ch), uh);
-          sts128(ulo + swz(urow, ch), ul);
+        for (int c8 = 0; c8 < 2; ++c8) {
+          const int ch = 2 * uh + c8;  // columns 16*uh + 8*c8 .. +7 of the slice
+          uint4 vh, vl;
+          split8(&u[8 * c8], vh, vl);
+          sts128(ub + swz(urow, ch), vh);
+          sts128(ub + swz(urow, 4 + ch), vl);
           float ru[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) ru[i] = r * u[8 * c4 + i];
-          split8(ru, uh, ul);
-          sts128(rhi + swz(urow, ch), uh);
-          sts128(rlo + swz(urow, ch), ul);
+          for (int i = 0; i < 8; ++i) ru[i] = r * u[8 * c8 + i];
+          split8(ru, vh, vl);
+          sts128(rb + swz(urow, ch), vh);
+          sts128(rb + swz(urow, 4 + ch), vl);
         }
       }
       fence_proxy_async_smem();
       mbar_arrive(&bars->u_ready);
 
-      // ---- S <- gamma_C S + K'^T diag(r) U (hi and lo halves summed) -------------
+      // ---- S <- gamma_C S + K'^T diag(r) U (hi and lo products summed) -----------
       if (!wait_bar_warp(&bars->ds_ready, pc, abort)) { ok = false; break; }
       tc_fence_after();
       {
         const float gam = exp2f(gC);
+        float dh[32], dl[32];
+        tmem_ld32(tmem + kColDS + lane_base, dh);
+        tmem_ld32(tmem + kColDS + kBV + lane_base, dl);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float dh[16], dl[16];
-          tmem_ld16(tmem + kColDS + 16 * q + lane_base, dh);
-          tmem_ld16(tmem + kColDS + kBV + 16 * q + lane_base, dl);
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) S[16 * q + jj] = gam * S[16 * q + jj] + (dh[jj] + dl[jj]);
-        }
+        for (int jj = 0; jj < kBV; ++jj) S[jj] = gam * S[jj] + (dh[jj] + dl[jj]);
       }
       if (c + 1 < nchunks) write_state();
 
-      // ---- o = gamma_i (Q' S) + P U ------------------------------------------------
+      // ---- o = gamma_i (Q' S) + P U -------------------------------------------------
       if (!wait_bar_warp(&bars->o_ready, pc, abort)) { ok = false; break; }
       tc_fence_after();
       {
@@ -851,14 +850,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool store = has_tok && t < T;
         const size_t obase = (((size_t)b * T + t) * p.H + h) * kD + vblk * kBV;
 #pragma unroll
-        for (int qt = 0; qt < 4; ++qt) {
-          float o1[16], o1l[16], o2[16];
-          tmem_ld16(tmem + kColQS + 16 * qt + lane_base, o1);
-          tmem_ld16(tmem + kColQS + kBV + 16 * qt + lane_base, o1l);
-          tmem_ld16(tmem + kColPU + 16 * qt + lane_base, o2);
+        for (int qt = 0; qt < 2; ++qt) {
+          float a1[16], a2[16], b1[16], b2[16];
+          tmem_ld16(tmem + kColQS + 16 * qt + lane_base, a1);
+          tmem_ld16(tmem + kColQS + kBV + 16 * qt + lane_base, a2);
+          tmem_ld16(tmem + kColPU + 16 * qt + lane_base, b1);
+          tmem_ld16(tmem + kColPU + kBV + 16 * qt + lane_base, b2);
           float ov[16];
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) ov[jj] = gi * (o1[jj] + o1l[jj]) + o2[jj];
+          for (int jj = 0; jj < 16; ++jj) ov[jj] = gi * (a1[jj] + a2[jj]) + (b1[jj] + b2[jj]);
           if (store) {
             if (p.out_bf16) {
               uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + obase + 16 * qt);
@@ -962,7 +962,7 @@ glinattn_status launch_gdn_tc(const glinattn_prefill_args &a, cudaStream_t strea
   if (!encode_rows_map(&tq, w.Qp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, Tp, rows_bh, 64, true) ||
       !encode_rows_map(&tk, w.Kp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, Tp, rows_bh, 64, true) ||
       !encode_rows_map(&tw, w.Wp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, Tp, rows_bh, 64, true) ||
-      !encode_rows_map(&tu, w.Up, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kD, Tp, rows_bh, 64, false))
+      !encode_rows_map(&tu, w.Up, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kD, Tp, rows_bh, kBV, false))
     return GLINATTN_ERR_CUDA;
   ScanParams sp;
   sp.B = B; sp.T = T; sp.H = H; sp.nchunks = nchunks; sp.Tp = Tp;
@@ -975,7 +975,7 @@ glinattn_status launch_gdn_tc(const glinattn_prefill_args &a, cudaStream_t strea
   if (cudaFuncSetAttribute(gdn_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kScanSmem) != cudaSuccess)
     return GLINATTN_ERR_CUDA;
-  gdn_scan_kernel<<<(unsigned)(B * H * 2), kThreads, kScanSmem, stream>>>(tq, tk, tw, tu, sp);
+  gdn_scan_kernel<<<(unsigned)(B * H * kNV), kThreads, kScanSmem, stream>>>(tq, tk, tw, tu, sp);
   return cudaGetLastError() == cudaSuccess ? GLINATTN_OK : GLINATTN_ERR_CUDA;
 }
 
