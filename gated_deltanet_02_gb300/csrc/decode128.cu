@@ -55,9 +55,17 @@ constexpr int kTabWords = 32;         // [0] src slot, [1..8] dst slots, [9..16]
 constexpr uint32_t kStateBytes = kD * kDC * 4;
 constexpr uint32_t kMiscBytes = kNCH * 4 + kNW * 2 * kDC * 4 + 3 * kNW * 4 + kTab * kTabWords * 4 + kRing * 8;
 
-__host__ __device__ constexpr uint32_t small_bytes(int esz) { return 4u * kNCH * esz; }
-__host__ __device__ constexpr uint32_t slot_bytes(int esz) { return kStateBytes + small_bytes(esz); }
-__host__ __device__ constexpr uint32_t smem_bytes(int esz) { return 128 + kRing * slot_bytes(esz) + kMiscBytes; }
+constexpr int kRingSteps = 4;         // token rows of a unit carried in its ring slot
+// ring slot: the state half, then the conv history (3 rows) and the first
+// `xrows` token rows of the unit, each row kNCH channels of `esz` bytes
+__host__ __device__ constexpr int ring_xrows(int steps) { return steps < kRingSteps ? steps : kRingSteps; }
+__host__ __device__ constexpr uint32_t small_bytes(int esz, int xrows) { return (3u + xrows) * kNCH * esz; }
+__host__ __device__ constexpr uint32_t slot_bytes(int esz, int xrows) {
+  return kStateBytes + small_bytes(esz, xrows);
+}
+__host__ __device__ constexpr uint32_t smem_bytes(int esz, int xrows) {
+  return 128 + kRing * slot_bytes(esz, xrows) + kMiscBytes;
+}
 
 __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
@@ -92,7 +100,8 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
   uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   const int in_bf16 = p.in_bf16;
   const int esz = in_bf16 ? 2 : 4;
-  const uint32_t sbytes = slot_bytes(esz);
+  const int xrows = ring_xrows(p.steps);
+  const uint32_t sbytes = slot_bytes(esz, xrows);
   float *s_act = reinterpret_cast<float *>(smem + kRing * sbytes);  // q | k | own v slice
   float *s_red = s_act + kNCH;                                      // [warp][k S | q S][kDC]
   float *s_wsum = s_red + kNW * 2 * kDC;                            // [|q|^2, |k|^2, q.k][warp]
@@ -157,7 +166,7 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
     const int n = unit_n(k), h = unit_h(k);
     uint8_t *st = smem + (k % kRing) * sbytes;
     uint8_t *small = st + kStateBytes;
-    const uint32_t bytes = kStateBytes + (conv ? 3u : 0u) * kNCH * esz + (uint32_t)kNCH * esz;
+    const uint32_t bytes = kStateBytes + (conv ? 3u : 0u) * kNCH * esz + (uint32_t)xrows * kNCH * esz;
     mbar_arrive_expect_tx(bar, bytes);
     tma_load_3d(st, &tstate, bar, col0, 0, slot * H + h);
     if (conv) {
@@ -170,11 +179,13 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
         bulk_load(dst + 2 * kD * esz, row + (size_t)(2 * H * kD + h * kD + col0) * esz, kDC * esz, bar);
       }
     }
-    const size_t row0 = ((size_t)n * steps) * H + h;
-    uint8_t *xs = small + 3 * kNCH * esz;
-    bulk_load(xs, (const uint8_t *)p.q + row0 * kD * esz, kD * esz, bar);
-    bulk_load(xs + kD * esz, (const uint8_t *)p.k + row0 * kD * esz, kD * esz, bar);
-    bulk_load(xs + 2 * kD * esz, (const uint8_t *)p.v + (row0 * kD + col0) * esz, kDC * esz, bar);
+    for (int t = 0; t < xrows; ++t) {
+      const size_t row = ((size_t)n * steps + t) * H + h;
+      uint8_t *xs = small + (size_t)(3 + t) * kNCH * esz;
+      bulk_load(xs, (const uint8_t *)p.q + row * kD * esz, kD * esz, bar);
+      bulk_load(xs + kD * esz, (const uint8_t *)p.k + row * kD * esz, kD * esz, bar);
+      bulk_load(xs + 2 * kD * esz, (const uint8_t *)p.v + (row * kD + col0) * esz, kDC * esz, bar);
+    }
   };
 
   if (tid == 0) {
@@ -326,10 +337,14 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
           hr[i][0] = hr[i][1];
           hr[i][1] = hr[i][2];
           hr[i][2] = x;
-          if (c < kNCH && !last) {
-            const void *src = c < kD ? p.q : (c < 2 * kD ? p.k : p.v);
-            const int ci = c < 2 * kD ? (c % kD) : col0 + (c - 2 * kD);
-            xr[i] = ld_act(src, (row + H) * kD + ci, in_bf16);
+          if (c < kNCH && !last) {  // next step's token: from the ring slot, else global memory
+            if (t + 1 < xrows) {
+              xr[i] = ld_act(small, (3 + t + 1) * kNCH + c, in_bf16);
+            } else {
+              const void *src = c < kD ? p.q : (c < 2 * kD ? p.k : p.v);
+              const int ci = c < 2 * kD ? (c % kD) : col0 + (c - 2 * kD);
+              xr[i] = ld_act(src, (row + H) * kD + ci, in_bf16);
+            }
           }
         }
         float iq = 1.f, ik = 1.f;
@@ -494,7 +509,7 @@ bool decode128_supports(const RecurParams &p, int d) {
 
 cudaError_t launch_decode128(const RecurParams &p, cudaStream_t stream) {
   const int esz = p.in_bf16 ? 2 : 4;
-  const int smem = (int)smem_bytes(esz);
+  const int smem = (int)smem_bytes(esz, ring_xrows(p.steps));
   CUtensorMap tmap;
   memset(&tmap, 0, sizeof(tmap));
   {
