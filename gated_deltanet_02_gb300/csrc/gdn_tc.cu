@@ -415,7 +415,9 @@ constexpr int kBV = 32;          // d_v columns per CTA
 constexpr int kNV = kD / kBV;    // CTAs per (batch, head)
 constexpr int kStages = 2;
 constexpr int kPrefetch = 3;  // chunks prefetched into L2 beyond the shared-memory ring
-constexpr int kThreads = 320;    // warp 0 TMA, warp 1 MMA, warps 2-5 (P), 6-9 (state, outputs)
+// warp 0 TMA, warp 1 MMA issuer of the state chain (W S, K'^T r U), warps 2-5 P,
+// warps 6-9 U / state / outputs, warp 10 MMA issuer of Q'K'^T, Q'S and P U
+constexpr int kThreads = 352;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kTile = kC * kD * 2;        // Q', K' or W tile: 16 KiB (2 column blocks)
 constexpr uint32_t kTileU = kC * kBV * 4;      // U~ slice, fp32: 8 KiB
@@ -429,8 +431,8 @@ constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffP = kStages * kStageBytes;   // P hi, lo
 constexpr uint32_t kOffU = kOffP + 2 * kTileP;      // [U_hi | U_lo]
 constexpr uint32_t kOffRU = kOffU + kTileHL;        // [rU_hi | rU_lo]
-constexpr uint32_t kOffS = kOffRU + kTileHL;        // [S_hi | S_lo]
-constexpr uint32_t kOffG = kOffS + kTileS;          // gate rows [warp][2][64]
+constexpr uint32_t kOffS = kOffRU + kTileHL;        // [S_hi | S_lo], double-buffered
+constexpr uint32_t kOffG = kOffS + 2 * kTileS;      // gate rows [warp][2][64]
 constexpr uint32_t kOffBar = kOffG + (kThreads / 32) * 2 * kC * 4;
 constexpr uint32_t kScanSmem = kOffBar + 256 + 1024;
 static_assert(kScanSmem <= 232448, "shared memory budget");
@@ -542,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 1);
+      mbar_init(&bars->empty[s], 2);  // one commit from each MMA issuer
     }
     mbar_init(&bars->qk_ready, 1);
     mbar_init(&bars->o_ready, 1);
@@ -551,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->o_free, kEpiThreads);
     mbar_init(&bars->ws_ready, 1);
     mbar_init(&bars->ds_ready, 1);
-    mbar_init(&bars->p_free, 1);
+    mbar_init(&bars->p_free, 2);
     mbar_init(&bars->u_ready, kEpiThreads);
     mbar_init(&bars->s_ready, kEpiThreads);
     bars->abort = 0;
@@ -603,69 +605,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ======================= MMA issuer =======================
+    // ============ MMA issuer A: the state chain, W S and K'^T r U ============
+    // Its own thread, so these are issued the moment their inputs are ready
+    // instead of queueing behind Q'K'^T, Q'S and P U.  S buffer c & 1 holds
+    // the state before chunk c.
     if (lane == 0) {
-      constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);        // Q' K'^T
-      constexpr uint32_t id_xs = idesc_bf16(64, 2 * kBV, false, true);    // W [S_hi|S_lo], Q' [..]
+      constexpr uint32_t id_xs = idesc_bf16(64, 2 * kBV, false, true);    // W [S_hi|S_lo]
       constexpr uint32_t id_ds = idesc_bf16(128, 2 * kBV, true, true);    // K'^T [rU_hi|rU_lo]
-      constexpr uint32_t id_pu = idesc_bf16(64, 2 * kBV, false, true);    // P [U_hi|U_lo]
       const uint32_t sbase = smem_u32(smem);
+      const uint64_t dRU = desc_sw128(sbase + kOffRU, 16, 1024);  // [rU_hi | rU_lo]
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % kStages;
         const uint32_t pc = (uint32_t)c & 1u;
         const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
-        const uint64_t dQ = desc_sw128(aQ, 16, 1024), dK = desc_sw128(aQ + kTile, 16, 1024);
         const uint64_t dKm = desc_sw128(aQ + kTile, kTile / 2, 1024);
         const uint64_t dW = desc_sw128(aQ + 2 * kTile, 16, 1024);
-        const uint64_t dS = desc_sw128(sbase + kOffS, 16, 1024);    // [S_hi | S_lo], one 64-wide block
-        const uint64_t dP = desc_sw128(sbase + kOffP, 16, 1024);
-        const uint64_t dU = desc_sw128(sbase + kOffU, 16, 1024);    // [U_hi | U_lo]
-        const uint64_t dRU = desc_sw128(sbase + kOffRU, 16, 1024);  // [rU_hi | rU_lo]
-        // Q' K'^T: M = 64 tokens, N = 64 tokens, K = d_k
+        const uint64_t dS = desc_sw128(sbase + kOffS + (c & 1) * kTileS, 16, 1024);  // [S_hi | S_lo]
         if (!wait_bar(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) break;
-        if (!wait_bar(&bars->qk_free, pc ^ 1u, abort)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
-          umma_bf16(tmem + kColQK, dQ + off, dK + off, id_qk, ks > 0);
-        }
-        umma_commit(&bars->qk_ready);
-        // W [S_hi | S_lo]: M = 64, N = 64, K = d_k (W tile K-major, S tile MN-major)
         if (!wait_bar(&bars->s_ready, pc, abort)) break;
         tc_fence_after();
+        // W [S_hi | S_lo]: M = 64, N = 64, K = d_k (W tile K-major, S tile MN-major)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t aoff = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
           umma_bf16(tmem + kColWS, dW + aoff, dS + ((ks * 2048) >> 4), id_xs, ks > 0);
         }
         umma_commit(&bars->ws_ready);
-        // Q' [S_hi | S_lo] (its accumulator is read by the previous chunk's outputs)
-        if (!wait_bar(&bars->o_free, pc ^ 1u, abort)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t aoff = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
-          umma_bf16(tmem + kColQS, dQ + aoff, dS + ((ks * 2048) >> 4), id_xs, ks > 0);
-        }
         if (!wait_bar(&bars->u_ready, pc, abort)) break;
-        if (!wait_bar(&bars->p_ready, pc, abort)) break;
         tc_fence_after();
         // dS = K'^T [rU_hi | rU_lo]: M = d_k (K' tile read M-major), N = 64, K = 64 tokens
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           umma_bf16(tmem + kColDS, dKm + ((ks * 2048) >> 4), dRU + ((ks * 2048) >> 4), id_ds, ks > 0);
         umma_commit(&bars->ds_ready);
-        // (Phi + Plo) [U_hi | U_lo]: M = 64, N = 64, K = 64 tokens
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(tmem + kColPU, dP + ((part * kTileP + ks * 32) >> 4), dU + ((ks * 2048) >> 4), id_pu,
-                      (part | ks) != 0);
-        umma_commit(&bars->o_ready);
-        umma_commit(&bars->p_free);
-        umma_commit(&bars->empty[s]);
+        umma_commit(&bars->p_free);    // r U may be rewritten
+        umma_commit(&bars->empty[s]);  // W and K' of this stage are read
       }
     }
   } else if (warp < 6) {
@@ -733,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(&bars->p_ready);
     }
-  } else {
+  } else if (warp < 10) {
     // ============ warpgroup B: U, the state chain and the outputs ============
     const int q4 = warp & 3;
     const int srow = 32 * q4 + lane;
@@ -755,8 +729,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // S row srow as [hi | lo]: 16-byte chunks 0-3 hold the high parts, 4-7 the remainders
-    auto write_state = [&]() {
-      const uint32_t sb = smem_u32(smem + kOffS);
+    auto write_state = [&](int buf) {
+      const uint32_t sb = smem_u32(smem + kOffS + buf * kTileS);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint4 vh, vl;
@@ -767,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(&bars->s_ready);
     };
-    write_state();
+    write_state(0);
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % kStages;
@@ -839,7 +813,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int jj = 0; jj < kBV; ++jj) S[jj] = gam * S[jj] + (dh[jj] + dl[jj]);
       }
-      if (c + 1 < nchunks) write_state();
+      // buffer (c + 1) & 1 was last read by W S (done: ds_ready of chunk c - 1)
+      // and Q' S (done: o_ready of chunk c - 1) of the previous chunk
+      if (c + 1 < nchunks) write_state((c + 1) & 1);
 
       // ---- o = gamma_i (Q' S) + P U -------------------------------------------------
       if (!wait_bar_warp(&bars->o_ready, pc, abort)) { ok = false; break; }
@@ -881,6 +857,55 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < kBV; j += 4)
         *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+  } else {
+    // ============ MMA issuer B: Q' K'^T, Q' S and P U (off the state chain) ============
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);        // Q' K'^T
+      constexpr uint32_t id_xs = idesc_bf16(64, 2 * kBV, false, true);    // Q' [S_hi|S_lo]
+      constexpr uint32_t id_pu = idesc_bf16(64, 2 * kBV, false, true);    // P [U_hi|U_lo]
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t dP = desc_sw128(sbase + kOffP, 16, 1024);
+      const uint64_t dU = desc_sw128(sbase + kOffU, 16, 1024);    // [U_hi | U_lo]
+      for (int c = 0; c < nchunks; ++c) {
+        const int s = c % kStages;
+        const uint32_t pc = (uint32_t)c & 1u;
+        const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
+        const uint64_t dQ = desc_sw128(aQ, 16, 1024), dK = desc_sw128(aQ + kTile, 16, 1024);
+        const uint64_t dS = desc_sw128(sbase + kOffS + (c & 1) * kTileS, 16, 1024);
+        // Q' K'^T: M = 64 tokens, N = 64 tokens, K = d_k
+        if (!wait_bar(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) break;
+        if (!wait_bar(&bars->qk_free, pc ^ 1u, abort)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
+          umma_bf16(tmem + kColQK, dQ + off, dK + off, id_qk, ks > 0);
+        }
+        umma_commit(&bars->qk_ready);
+        // Q' [S_hi | S_lo] (its accumulator is read by the previous chunk's outputs)
+        if (!wait_bar(&bars->s_ready, pc, abort)) break;
+        if (!wait_bar(&bars->o_free, pc ^ 1u, abort)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t aoff = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
+          umma_bf16(tmem + kColQS, dQ + aoff, dS + ((ks * 2048) >> 4), id_xs, ks > 0);
+        }
+        // (Phi + Plo) [U_hi | U_lo]: M = 64, N = 64, K = 64 tokens
+        if (!wait_bar(&bars->p_ready, pc, abort)) break;
+        if (!wait_bar(&bars->u_ready, pc, abort)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tmem + kColPU, dP + ((part * kTileP + ks * 32) >> 4), dU + ((ks * 2048) >> 4), id_pu,
+                      (part | ks) != 0);
+        umma_commit(&bars->o_ready);
+        umma_commit(&bars->p_free);    // P and U may be rewritten
+        umma_commit(&bars->empty[s]);  // Q' and K' of this stage are read
+      }
     }
   }
 
