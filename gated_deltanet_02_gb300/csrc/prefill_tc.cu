@@ -64,8 +64,9 @@ constexpr uint32_t kOffStage = 0;
 constexpr uint32_t kOffP = kOffStage + kStages * kStageBytes;  // P[hi, lo]
 constexpr uint32_t kOffVt = kOffP + 2 * kTileP;                // V~[hi, lo]
 constexpr uint32_t kOffS = kOffVt + 2 * kTileV;                // S[buf][hi, lo]
-constexpr uint32_t kOffG = kOffS + 4 * kTileS;                 // gate rows [warp][64]
-constexpr uint32_t kOffBar = kOffG + (kThreads / 32) * 2 * kC * 4;
+constexpr uint32_t kOffG = kOffS + 4 * kTileS;                 // gate ring [stage]
+constexpr uint32_t kGateBytes = 1088;                          // one GateRing entry
+constexpr uint32_t kOffBar = kOffG + kStages * kGateBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -92,40 +93,16 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
-// Per-chunk gates of one warp: g2 = cumsum(log2 alpha) over the chunk's 64
-// tokens (2 per lane, alpha = 1 past the end of the sequence), published in
-// the warp's shared row so any lane can read any g2_j by broadcast.
-struct Gates {
-  float a0n, a1n;  // next chunk's alphas, prefetched one chunk ahead
+// The gates of one chunk, computed once by the TMA warp and published with
+// the chunk's tiles: g = cumsum(log2 alpha) over the chunk's tokens (alpha = 1
+// past the end of the sequence), 2^g, 2^-g (when the chunk's total decay g_C
+// is moderate, so the factors cannot overflow), r = 2^(g_C - g) and 2^g_C.
+struct __align__(16) GateRing {
+  float g[kC], eg[kC], ecg[kC], r[kC];
+  float gC, egC;
+  int factored;
 };
-
-__device__ __forceinline__ void gates_prefetch(Gates &G, const GlaParams &p, int b, int h, int c,
-                                               int lane) {
-  const int ta = c * kC + 2 * lane, tb2 = ta + 1;
-  G.a0n = ta < p.T ? p.alpha[((size_t)b * p.T + ta) * p.H + h] : 1.f;
-  G.a1n = tb2 < p.T ? p.alpha[((size_t)b * p.T + tb2) * p.H + h] : 1.f;
-}
-
-// Consumes the prefetched alphas of chunk c, writes g2[0..63] to `row`,
-// prefetches chunk c+1.  Returns g2 of the chunk's last token.
-__device__ __forceinline__ float gates_chunk(Gates &G, const GlaParams &p, int b, int h, int c,
-                                             int lane, float *row) {
-  const float l0 = log2f(G.a0n), l1 = log2f(G.a1n);
-  gates_prefetch(G, p, b, h, c + 1, lane);
-  float incl = l0 + l1;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-  if (lane == 0) excl = 0.f;
-  __syncwarp();
-  row[2 * lane] = excl + l0;
-  row[2 * lane + 1] = excl + l0 + l1;
-  __syncwarp();
-  return row[kC - 1];
-}
+static_assert(sizeof(GateRing) <= kGateBytes, "gate ring entry");
 
 __global__ void __launch_bounds__(kThreads, 1)
     gla_prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -133,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // stays in the shared space
   Bars *bars = reinterpret_cast<Bars *>(smem + kOffBar);
-  float *s_g = reinterpret_cast<float *>(smem + kOffG);  // [warp][2][64] gate rows
+  GateRing *ring = reinterpret_cast<GateRing *>(smem + kOffG);
   volatile int *abort = &bars->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -157,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->full[s], 1 + 32);  // the TMA transaction and the 32 gate lanes
       mbar_init(&bars->empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -184,26 +161,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == 0) {
-    // ======================= TMA producer =======================
+    // ============ TMA producer (lane 0) and the gates of each chunk (all lanes) ============
+    auto prefetch = [&](int c) {  // chunk c's tiles into L2, ahead of the ring
+      if (c >= nchunks) return;
+      const int t0 = c * kC;
+      tma_prefetch_l2_4d(&tq, 0, h, t0, b);
+      tma_prefetch_l2_4d(&tq, 64, h, t0, b);
+      tma_prefetch_l2_4d(&tk, 0, h, t0, b);
+      tma_prefetch_l2_4d(&tk, 64, h, t0, b);
+      tma_prefetch_l2_4d(&tv, vblk * kBV, h, t0, b);
+    };
     if (lane == 0) {
       prefetch_tensormap(&tq);
       prefetch_tensormap(&tk);
       prefetch_tensormap(&tv);
-      auto prefetch = [&](int c) {  // chunk c's tiles into L2, ahead of the ring
-        if (c >= nchunks) return;
-        const int t0 = c * kC;
-        tma_prefetch_l2_4d(&tq, 0, h, t0, b);
-        tma_prefetch_l2_4d(&tq, 64, h, t0, b);
-        tma_prefetch_l2_4d(&tk, 0, h, t0, b);
-        tma_prefetch_l2_4d(&tk, 64, h, t0, b);
-        tma_prefetch_l2_4d(&tv, vblk * kBV, h, t0, b);
-      };
       for (int c = 0; c < kPrefetch; ++c) prefetch(kStages + c);
-      for (int c = 0; c < nchunks; ++c) {
-        const int s = c % kStages;
-        const uint32_t use = (uint32_t)(c / kStages);
-        prefetch(c + kStages + kPrefetch);
-        if (!wait_bar(&bars->empty[s], (use & 1u) ^ 1u, abort)) break;
+    }
+    // lane l holds the alphas of tokens 2l and 2l + 1 of the next chunk
+    auto alphas = [&](int c, float &a0, float &a1) {
+      const int ta = c * kC + 2 * lane, tb2 = ta + 1;
+      a0 = ta < T ? p.alpha[((size_t)b * T + ta) * p.H + h] : 1.f;
+      a1 = tb2 < T ? p.alpha[((size_t)b * T + tb2) * p.H + h] : 1.f;
+    };
+    float a0n, a1n;
+    alphas(0, a0n, a1n);
+    for (int c = 0; c < nchunks; ++c) {
+      const int s = c % kStages;
+      const uint32_t use = (uint32_t)(c / kStages);
+      if (lane == 0) prefetch(c + kStages + kPrefetch);
+      if (!wait_bar_warp(&bars->empty[s], (use & 1u) ^ 1u, abort)) break;
+      if (lane == 0) {
         uint8_t *st = smem + kOffStage + s * kStageBytes;
         mbar_arrive_expect_tx(&bars->full[s], kStageBytes);
         const int t0 = c * kC;
@@ -213,6 +200,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(st + kTileQ + kTileK / 2, &tk, &bars->full[s], 64, h, t0, b);
         tma_load_4d(st + kTileQ + kTileK, &tv, &bars->full[s], vblk * kBV, h, t0, b);
       }
+      const float l0 = log2f(a0n), l1 = log2f(a1n);
+      alphas(c + 1, a0n, a1n);
+      float incl = l0 + l1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+      if (lane == 0) excl = 0.f;
+      const float ga = excl + l0, gb = excl + l0 + l1;
+      const float gC = __shfl_sync(0xffffffffu, gb, 31);
+      const bool factored = gC > -100.f;  // 2^-g <= 2^100: no overflow
+      GateRing &gr = ring[s];
+      gr.g[2 * lane] = ga;
+      gr.g[2 * lane + 1] = gb;
+      gr.eg[2 * lane] = exp2f(ga);
+      gr.eg[2 * lane + 1] = exp2f(gb);
+      gr.ecg[2 * lane] = factored ? exp2f(-ga) : 0.f;
+      gr.ecg[2 * lane + 1] = factored ? exp2f(-gb) : 0.f;
+      gr.r[2 * lane] = exp2f(gC - ga);
+      gr.r[2 * lane + 1] = exp2f(gC - gb);
+      if (lane == 0) {
+        gr.gC = gC;
+        gr.egC = exp2f(gC);
+        gr.factored = factored ? 1 : 0;
+      }
+      mbar_arrive(&bars->full[s]);  // releases this lane's gate writes
     }
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
@@ -291,17 +306,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q4 = warp & 3;
     const int e = tid - 64;               // 0..127
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-    float *grow = s_g + warp * 2 * kC;
-    Gates G;
-    gates_prefetch(G, p, b, h, 0, lane);
     for (int c = 0; c < nchunks; ++c) {
       const int s = c % kStages;
       const uint32_t sph = (uint32_t)(c / kStages) & 1u;
       const int tb = c & 1;
       const uint32_t ph = (uint32_t)(c >> 1) & 1u;
-      const float gC = gates_chunk(G, p, b, h, c, lane, grow);
-
       if (!wait_bar_warp(&bars->qk_ready[tb], ph, abort)) break;
+      if (!wait_bar_warp(&bars->full[s], sph, abort)) break;  // the chunk's gates and V tile
+      const GateRing &gr = ring[s];
       tc_fence_after();
       // lane l < 16 holds row 16*q4 + l of QK^T (M = 64 layout); it keeps
       // columns 0..31 and hands columns 32..63 to lane l + 16
@@ -321,31 +333,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_bar_warp(&bars->p_free, ((uint32_t)c & 1u) ^ 1u, abort)) break;
       // D_ij = 2^(g_i - g_j).  When the chunk's total decay is moderate the
       // factors 2^g_i and 2^-g_j cannot overflow and D is their product (one
-      // exp2 per token instead of one per pair); otherwise pairwise exp2.
-      const bool factored = gC > -100.f;  // warp-uniform
-      float *cfrow = grow + kC;           // 2^-g_j of this chunk
-      if (factored) {
-        cfrow[2 * lane] = exp2f(-grow[2 * lane]);
-        cfrow[2 * lane + 1] = exp2f(-grow[2 * lane + 1]);
-      }
-      __syncwarp();
+      // exp2 per token, done by the TMA warp); otherwise pairwise exp2.
       {
         const int row = 16 * q4 + (lane & 15), jb = 32 * (lane >> 4);
         const uint32_t phi = smem_u32(smem + kOffP);
         const uint32_t plo = phi + kTileP;
-        const float gi = grow[row];
-        if (factored) {
-          const float rf = exp2f(gi);
+        if (gr.factored) {  // warp-uniform
+          const float rf = gr.eg[row];
+          const uint32_t cfa = smem_u32(&gr.ecg[jb]);
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int j = jb + jj;
-            qk[jj] = (j <= row) ? qk[jj] * rf * cfrow[j] : 0.f;
+          for (int q = 0; q < 8; ++q) {
+            const uint4 cw = lds128(cfa + 16 * q);
+            const float cf[4] = {__uint_as_float(cw.x), __uint_as_float(cw.y), __uint_as_float(cw.z),
+                                 __uint_as_float(cw.w)};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const int jj = 4 * q + m, j = jb + jj;
+              qk[jj] = (j <= row) ? qk[jj] * rf * cf[m] : 0.f;
+            }
           }
         } else {
+          const float gi = gr.g[row];
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
             const int j = jb + jj;
-            qk[jj] = (j <= row) ? qk[jj] * exp2f(gi - grow[j]) : 0.f;
+            qk[jj] = (j <= row) ? qk[jj] * exp2f(gi - gr.g[j]) : 0.f;
           }
         }
 #pragma unroll
@@ -357,13 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           sts128(plo + swz(row, ch), ul);
         }
       }
-      if (!wait_bar_warp(&bars->full[s], sph, abort)) break;
       {
         const uint32_t vt = smem_u32(smem + kOffStage + s * kStageBytes + kTileQ + kTileK);
         const uint32_t vhi = smem_u32(smem + kOffVt);
         const uint32_t vlo = vhi + kTileV;
         const int t = e >> 1, half = e & 1;
-        const float r = exp2f(gC - grow[t]);
+        const float r = gr.r[t];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t ch = 4 * half + k;
@@ -387,9 +398,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool has_tok = lane < 16;
     const int tok = 16 * q4 + lane;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-    float *grow = s_g + warp * 2 * kC;
-    Gates G;
-    gates_prefetch(G, p, b, h, 0, lane);
+    // 2^g_C of the chunk and 2^g of this thread's token, read from the gate
+    // ring before the slot can be refilled (the refill needs Q S of the chunk,
+    // which waits for this warpgroup's o_free of the previous chunk)
+    float egC = 1.f, eg_tok = 1.f;
+    auto read_gates = [&](int c) -> bool {
+      const int s = c % kStages;
+      if (!wait_bar_warp(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) return false;
+      egC = ring[s].egC;
+      eg_tok = ring[s].eg[tok & (kC - 1)];
+      return true;
+    };
 
     // the state slice S[srow, vblk*64 .. +64) in fp32 registers
     float S[kBV];
@@ -414,20 +433,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(&bars->s_ready[sb]);
     };
-    write_state(0);
-
-    bool ok = true;
+    bool ok = read_gates(0);
+    if (ok) write_state(0);
     for (int c = 0; c < nchunks && ok; ++c) {
       const int tb = c & 1;
       const uint32_t ph = (uint32_t)(c >> 1) & 1u;
       const int t0 = c * kC;
-      const float gC = gates_chunk(G, p, b, h, c, lane, grow);
 
       // ---- S <- gamma_C S + K^T V~ (the hi and lo column halves summed) -------
       if (!wait_bar_warp(&bars->ds_ready, (uint32_t)c & 1u, abort)) { ok = false; break; }
       tc_fence_after();
       {
-        const float gam = exp2f(gC);
+        const float gam = egC;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float dh[32], dl[32];
@@ -445,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_bar_warp(&bars->o_ready[tb], ph, abort)) { ok = false; break; }
       tc_fence_after();
       {
-        const float gi = exp2f(grow[tok & (kC - 1)]);
+        const float gi = eg_tok;
         const int t = t0 + tok;
         const bool store = has_tok && t < T;
         const size_t obase = (((size_t)b * T + t) * p.H + h) * kDK + vblk * kBV;
@@ -478,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (c + 1 < nchunks && !read_gates(c + 1)) { ok = false; break; }
       tc_fence_before();
       mbar_arrive(&bars->o_free[tb]);
     }
