@@ -772,15 +772,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_bar_warp(&bars->full[s], sph, abort)) { ok = false; break; }
       if (!wait_bar_warp(&bars->p_free, pc ^ 1u, abort)) { ok = false; break; }
       {
-        const float *ut = reinterpret_cast<const float *>(smem + kOffStage + s * kStageBytes + 3 * kTile) +
-                          urow * kBV + 16 * uh;
+        // the U~ slice rows are 128 bytes (32 fp32), loaded with the 128-byte swizzle
+        const uint32_t ut = smem_u32(smem + kOffStage + s * kStageBytes + 3 * kTile);
 #pragma unroll
         for (int j = 0; j < 16; j += 4) {
-          const float4 v4 = *reinterpret_cast<const float4 *>(ut + j);
-          u[j] = v4.x - u[j];
-          u[j + 1] = v4.y - u[j + 1];
-          u[j + 2] = v4.z - u[j + 2];
-          u[j + 3] = v4.w - u[j + 3];
+          const uint4 w4 = lds128(ut + swz(urow, 4 * uh + j / 4));
+          u[j] = __uint_as_float(w4.x) - u[j];
+          u[j + 1] = __uint_as_float(w4.y) - u[j + 1];
+          u[j + 2] = __uint_as_float(w4.z) - u[j + 2];
+          u[j + 3] = __uint_as_float(w4.w) - u[j + 3];
         }
         const float r = exp2f(gC - grow[urow]);
         const uint32_t ub = smem_u32(smem + kOffU), rb = smem_u32(smem + kOffRU);
@@ -987,7 +987,7 @@ glinattn_status launch_gdn_tc(const glinattn_prefill_args &a, cudaStream_t strea
   if (!encode_rows_map(&tq, w.Qp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, Tp, rows_bh, 64, true) ||
       !encode_rows_map(&tk, w.Kp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, Tp, rows_bh, 64, true) ||
       !encode_rows_map(&tw, w.Wp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, Tp, rows_bh, 64, true) ||
-      !encode_rows_map(&tu, w.Up, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kD, Tp, rows_bh, kBV, false))
+      !encode_rows_map(&tu, w.Up, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, kD, Tp, rows_bh, kBV, true))
     return GLINATTN_ERR_CUDA;
   ScanParams sp;
   sp.B = B; sp.T = T; sp.H = H; sp.nchunks = nchunks; sp.Tp = Tp;
