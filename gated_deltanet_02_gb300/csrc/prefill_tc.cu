@@ -50,7 +50,9 @@ constexpr int kDK = 128;  // key / value head size
 constexpr int kBV = 64;   // d_v columns per CTA
 constexpr int kStages = 3;
 constexpr int kPrefetch = 3;  // chunks prefetched into L2 beyond the shared-memory ring
-constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-5 and 6-9 epilogue
+// warp 0 TMA and gates, warp 1 MMA issuer of the state chain (K^T V~, Q S),
+// warps 2-5 and 6-9 epilogue, warp 10 MMA issuer of Q K^T and P V
+constexpr int kThreads = 352;
 constexpr int kEpiThreads = 128;  // threads per epilogue warpgroup
 
 // ---- shared memory map (offsets from a 1024-byte aligned base) -------------
@@ -135,17 +137,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->full[s], 1 + 32);  // the TMA transaction and the 32 gate lanes
-      mbar_init(&bars->empty[s], 1);
+      mbar_init(&bars->empty[s], 2);  // one commit from each MMA issuer
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->qk_ready[i], 1);
-      mbar_init(&bars->o_ready[i], 1);
+      mbar_init(&bars->o_ready[i], 2);  // Q S (issuer A) and P V (issuer B)
       mbar_init(&bars->qk_free[i], kEpiThreads);
       mbar_init(&bars->p_ready[i], kEpiThreads);
       mbar_init(&bars->o_free[i], kEpiThreads);
       mbar_init(&bars->s_ready[i], kEpiThreads);
     }
-    mbar_init(&bars->p_free, 1);
+    mbar_init(&bars->p_free, 2);
     mbar_init(&bars->ds_ready, 1);
     mbar_init(&bars->ds_free, kEpiThreads);
     bars->abort = 0;
@@ -230,61 +232,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars->full[s]);  // releases this lane's gate writes
     }
   } else if (warp == 1) {
-    // ======================= MMA issuer =======================
+    // ============ MMA issuer A: the state chain, K^T V~ and Q S ============
     if (lane == 0) {
-      constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);   // Q K^T
       constexpr uint32_t id_qs = idesc_bf16(64, 2 * kBV, false, true);  // Q [S_hi | S_lo]
-      constexpr uint32_t id_pv = idesc_bf16(64, kBV, false, true);   // P V
       constexpr uint32_t id_ds = idesc_bf16(128, 2 * kBV, true, true);  // K^T [V~hi | V~lo]
       const uint32_t sbase = smem_u32(smem);
-      // Q K^T of chunk c: M = 64 tokens, N = 64 tokens, K = d_k (2 swizzle blocks x 4 steps)
-      auto issue_qk = [&](int c) -> bool {
-        const int s = c % kStages, tb = c & 1;
-        if (!wait_bar(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) return false;
-        if (!wait_bar(&bars->qk_free[tb], ((uint32_t)(c >> 1) & 1u) ^ 1u, abort)) return false;
-        tc_fence_after();
-        const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
-        const uint64_t dQ = desc_sw128(aQ, 16, 1024), dK = desc_sw128(aQ + kTileQ, 16, 1024);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = ((ks >> 2) * (kTileQ / 2) + (ks & 3) * 32) >> 4;
-          umma_bf16(tmem + kColQK + tb * 64, dQ + off, dK + off, id_qk, ks > 0);
-        }
-        umma_commit(&bars->qk_ready[tb]);
-        return true;
-      };
-      bool ok = issue_qk(0);
-      for (int c = 0; c < nchunks && ok; ++c) {
+      const uint64_t dVt = desc_sw128(sbase + kOffVt, kTileV, 1024);  // [hi | lo] as N = 128
+      for (int c = 0; c < nchunks; ++c) {
         const int s = c % kStages;
         const int tb = c & 1;
         const uint32_t ph = (uint32_t)(c >> 1) & 1u;
-        if (c + 1 < nchunks && !issue_qk(c + 1)) break;
-        if (!wait_bar(&bars->p_ready[tb], ph, abort)) break;
-        if (!wait_bar(&bars->o_free[tb], ph ^ 1u, abort)) break;   // P V buffer tb
+        if (!wait_bar(&bars->p_ready[tb], ph, abort)) break;  // V~ of chunk c
         if (!wait_bar(&bars->ds_free, ((uint32_t)c & 1u) ^ 1u, abort)) break;
         tc_fence_after();
         const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
         const uint32_t aK = aQ + kTileQ;
-        const uint32_t aV = aK + kTileK;
         // descriptors built once; the k-steps only move the start-address field
         const uint64_t dKm = desc_sw128(aK, kTileK / 2, 1024);
-        const uint64_t dVt = desc_sw128(sbase + kOffVt, kTileV, 1024);  // [hi | lo] as N = 128
-        const uint64_t dP = desc_sw128(sbase + kOffP, 16, 1024);
-        const uint64_t dV = desc_sw128(aV, 16, 1024);
         const uint64_t dQ = desc_sw128(aQ, 16, 1024);
         // dS = K^T [V~hi | V~lo]: M = d_k (K tile read M-major), N = 128, K = 64 tokens
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           umma_bf16(tmem + kColDS, dKm + ((ks * 2048) >> 4), dVt + ((ks * 2048) >> 4), id_ds, ks > 0);
         umma_commit(&bars->ds_ready);
-        // O2 = (Phi + Plo) V: M = 64, N = 64, K = 64 tokens
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(tmem + kColO2 + tb * 64, dP + ((part * kTileP + ks * 32) >> 4),
-                      dV + ((ks * 2048) >> 4), id_pv, (part | ks) != 0);
-        umma_commit(&bars->p_free);  // P and V~ may be rewritten once these are done
+        umma_commit(&bars->p_free);  // V~ may be rewritten
         const int sb = c & 1;
         if (!wait_bar(&bars->s_ready[sb], ph, abort)) break;
         // Q S accumulator is single: the previous chunk's outputs must be read
@@ -391,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(&bars->p_ready[tb]);
     }
-  } else {
+  } else if (warp < 10) {
     // ============ warpgroup B: the state chain and the outputs ============
     const int q4 = warp & 3;
     const int srow = 32 * q4 + lane;      // d_k row of the state held by this thread
@@ -504,6 +475,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < kBV; j += 4)
         *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+  } else {
+    // ============ MMA issuer B: Q K^T (one chunk ahead) and P V ============
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);  // Q K^T
+      constexpr uint32_t id_pv = idesc_bf16(64, kBV, false, true);  // P V
+      const uint32_t sbase = smem_u32(smem);
+      const uint64_t dP = desc_sw128(sbase + kOffP, 16, 1024);
+      // Q K^T of chunk c: M = 64 tokens, N = 64 tokens, K = d_k (2 swizzle blocks x 4 steps)
+      auto issue_qk = [&](int c) -> bool {
+        const int s = c % kStages, tb = c & 1;
+        if (!wait_bar(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) return false;
+        if (!wait_bar(&bars->qk_free[tb], ((uint32_t)(c >> 1) & 1u) ^ 1u, abort)) return false;
+        tc_fence_after();
+        const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
+        const uint64_t dQ = desc_sw128(aQ, 16, 1024), dK = desc_sw128(aQ + kTileQ, 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = ((ks >> 2) * (kTileQ / 2) + (ks & 3) * 32) >> 4;
+          umma_bf16(tmem + kColQK + tb * 64, dQ + off, dK + off, id_qk, ks > 0);
+        }
+        umma_commit(&bars->qk_ready[tb]);
+        return true;
+      };
+      bool ok = issue_qk(0);
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int s = c % kStages;
+        const int tb = c & 1;
+        const uint32_t ph = (uint32_t)(c >> 1) & 1u;
+        if (c + 1 < nchunks && !issue_qk(c + 1)) break;
+        if (!wait_bar(&bars->p_ready[tb], ph, abort)) break;
+        if (!wait_bar(&bars->o_free[tb], ph ^ 1u, abort)) break;   // P V buffer tb
+        tc_fence_after();
+        const uint64_t dV = desc_sw128(sbase + kOffStage + s * kStageBytes + kTileQ + kTileK, 16, 1024);
+        // O2 = (Phi + Plo) V: M = 64, N = 64, K = 64 tokens
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tmem + kColO2 + tb * 64, dP + ((part * kTileP + ks * 32) >> 4),
+                      dV + ((ks * 2048) >> 4), id_pv, (part | ks) != 0);
+        umma_commit(&bars->o_ready[tb]);
+        umma_commit(&bars->p_free);   // P may be rewritten
+        umma_commit(&bars->empty[s]);  // Q, K (Q K^T) and V of this stage are read
+      }
     }
   }
 
