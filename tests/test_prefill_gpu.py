@@ -153,3 +153,40 @@ def test_gdn_prefill_full_size_sampled():
     """B=2, H=16, T=8192, d=128, conv + L2 norm, S0 ~ N(0, 0.01)."""
     ex = inputs.gdn_prefill(2, 16, 8192, 128, seed=0, device=DEV)
     _sampled_full(ex, GDN, True, [(0, 5), (1, 15)])
+
+
+@pytest.mark.parametrize("variant", [GLA, GDN])
+def test_strong_decay_pairwise_path(variant):
+    """alpha ~ U(0.05, 0.2): a chunk's total decay is far below 2^-100, so the
+    decay mask cannot be factored into row and column factors and every
+    D_ij = 2^(g_i - g_j) is formed pairwise."""
+    T = 200
+    ex = (inputs.gdn_prefill if variant == GDN else inputs.gla_prefill)(1, 2, T, 128, seed=31)
+    gen = torch.Generator().manual_seed(7)
+    ex["alpha"] = (0.05 + 0.15 * torch.rand(ex["alpha"].shape, generator=gen)).to(ex["alpha"].dtype)
+    g = to(ex, DEV)
+    conv = variant == GDN
+    o, S, _ = _gpu_prefill(g, variant, conv, S0=g.get("S0"))
+    o_ref, S_ref, _ = _oracle_prefill(ex, variant, conv, S0=f64(ex.get("S0")))
+    assert relerr(o, o_ref) <= TOL_O_BF16
+    assert relerr(S, S_ref) <= TOL_S_BF16
+
+
+@pytest.mark.parametrize("variant", [GLA, GDN])
+def test_more_units_than_sms(variant):
+    """B=3, H=40: 240 GLA CTAs and 480 GDN scan CTAs, more than one wave."""
+    ex = (inputs.gdn_prefill if variant == GDN else inputs.gla_prefill)(3, 40, 130, 128, seed=41)
+    conv = variant == GDN
+    heads = [(0, 0), (1, 17), (2, 39)]
+    g = to(ex, DEV)
+    o, S, _ = _gpu_prefill(g, variant, conv, S0=g.get("S0"))
+    H, d = 40, 128
+    for b, h in heads:
+        sub = {k: (v[b:b + 1, :, h:h + 1] if k in ("q", "k", "v", "alpha", "beta") and v is not None
+                   else v) for k, v in ex.items()}
+        if conv:
+            sub["conv_w"] = ex["conv_w"].view(3, H, d, 4)[:, h].reshape(3 * d, 4)
+        S0 = None if ex.get("S0") is None else f64(ex["S0"][b:b + 1, h:h + 1])
+        o_ref, S_ref, _ = _oracle_prefill(sub, variant, conv, S0=S0)
+        assert relerr(o[b:b + 1, :, h:h + 1], o_ref) <= TOL_O_BF16, (b, h)
+        assert relerr(S[b:b + 1, h:h + 1], S_ref) <= TOL_S_BF16, (b, h)
