@@ -64,6 +64,8 @@ __device__ __forceinline__ uint4 pack8_rn(const float *x) {
 constexpr int kPrepThreads = 256;
 constexpr int kBlk = 32;                         // the inverse works on 32 x 32 blocks
 constexpr uint32_t kBlkBytes = kBlk * (kBlk + 1) * 4;  // one fp32 block, rows padded to 33
+constexpr uint32_t kOffRaw = 0;                  // the chunk's raw q, k, v rows: 3 x 2 swizzled 8 KiB blocks
+constexpr uint32_t kRawBytes = 3 * 16384;        // (dead after the front end; A, T, Tm reuse it)
 constexpr uint32_t kOffA = 0;                    // A00, A10, A11 (A00 later holds X = A10 T00)
 constexpr uint32_t kOffT = 3 * kBlkBytes;        // T00, T10, T11 of T = (I + A)^-1
 constexpr uint32_t kOffTm = 25600;               // T diag(beta gamma) hi, lo and T diag(beta) hi, lo: 4 x 8 KiB
@@ -72,6 +74,7 @@ constexpr uint32_t kOffVp = kOffQK + 32768;      // V': 2 column blocks x 64 row
 constexpr uint32_t kOffMisc = kOffVp + 16384;    // g2[64], beta[64], barrier, TMEM slot
 constexpr uint32_t kPrepSmem = kOffMisc + 1024 + 1024;
 static_assert(kOffT + 3 * kBlkBytes <= kOffTm && kOffTm + 4 * 8192 <= kOffQK, "pass A layout");
+static_assert(kOffRaw + kRawBytes <= kOffQK, "raw tile");
 static_assert(kOffQK % 1024 == 0 && kOffVp % 1024 == 0 && kOffTm % 1024 == 0, "alignment");
 
 struct PrepParams {
@@ -85,7 +88,9 @@ struct PrepParams {
   uint32_t *dev_status;
 };
 
-__global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams p) {
+__global__ void __launch_bounds__(kPrepThreads)
+    gdn_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const PrepParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -97,40 +102,54 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
   float *betas = g2s + kC;
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffMisc + 512);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffMisc + 520);
+  uint64_t *bar_raw = reinterpret_cast<uint64_t *>(smem + kOffMisc + 528);
+  uint8_t *raw = smem + kOffRaw;
 
+  // the chunk's 64 raw rows of q, k and v by TMA (rows past T arrive as zeros)
   if (tid == 0) {
     mbar_init(bar, 1);
+    mbar_init(bar_raw, 1);
     fence_mbar_init();
+    mbar_arrive_expect_tx(bar_raw, kRawBytes);
+    const CUtensorMap *maps[3] = {&tq, &tk, &tv};
+#pragma unroll
+    for (int part = 0; part < 3; ++part)
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk)
+        tma_load_4d(raw + part * 16384 + blk * 8192, maps[part], bar_raw, 64 * blk, h, t0, b);
   }
   if (warp == 0) {
     tmem_alloc(tslot, 256);
     tmem_relinquish();
   }
+  __syncthreads();  // both mbarriers are initialised before any thread waits on them
 
   // ---- front end: y_t = sum_j w_j x_{t-3+j}; L2 norm of q, k rows; bf16 -------
   // A task is (part, 8 consecutive tokens) of the chunk: a warp slides the
   // 4-tap window along its tokens, lane l owning channels 4l .. 4l+3, so every
-  // load and store is 8 bytes per lane and the L2 norm is one warp reduction.
-  // Each warp has three tasks; the next task's rows are loaded before the
-  // current one is computed.  History before the sequence comes from conv_in
-  // (or is zero).
+  // access is 8 bytes per lane and the L2 norm is one warp reduction.  The
+  // chunk's rows come from the TMA tile; the 3 rows before the chunk (first
+  // task of each part only) from global memory, or conv_in before the
+  // sequence (zero without it).
   struct FeTask {
-    uint2 x[11];  // rows r0 - 3 .. r0 + 7 of the part: 4 bf16 channels each
-    float4 w[4];  // the 4 taps of channels 4l .. 4l+3
+    uint2 hist[3];  // rows -3, -2, -1 of the chunk when r0 == 0
+    float4 w[4];    // the 4 taps of channels 4l .. 4l+3
   };
   auto fe_load = [&](int task, FeTask &f) {
     const int part = task % 3, r0 = (task / 3) * 8;
     const __nv_bfloat16 *src = part == 0 ? p.q : (part == 1 ? p.k : p.v);
 #pragma unroll
-    for (int m = 0; m < 11; ++m) {
-      const int t = t0 + r0 - 3 + m;
+    for (int m = 0; m < 3; ++m) {
+      const int t = t0 - 3 + m;
       uint2 v = make_uint2(0u, 0u);
-      if (t >= 0 && t < T)
-        v = *reinterpret_cast<const uint2 *>(src + (((size_t)b * T + t) * H + h) * kD + 4 * lane);
-      else if (t < 0 && p.has_conv && p.conv_in)
-        v = *reinterpret_cast<const uint2 *>(p.conv_in + ((size_t)b * 3 + (t + 3)) * Cch + part * H * kD +
-                                             h * kD + 4 * lane);
-      f.x[m] = v;
+      if (r0 == 0) {
+        if (t >= 0)
+          v = *reinterpret_cast<const uint2 *>(src + (((size_t)b * T + t) * H + h) * kD + 4 * lane);
+        else if (p.has_conv && p.conv_in)
+          v = *reinterpret_cast<const uint2 *>(p.conv_in + ((size_t)b * 3 + (t + 3)) * Cch + part * H * kD +
+                                               h * kD + 4 * lane);
+      }
+      f.hist[m] = v;
     }
 #pragma unroll
     for (int c2 = 0; c2 < 4; ++c2)
@@ -144,6 +163,13 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
     const int part = task % 3, r0 = (task / 3) * 8;
     // channels 4l .. 4l+3: column block l / 16, 16-byte chunk (l % 16) / 2, half l % 2
     const uint32_t cb = (uint32_t)(lane >> 4), ch = (uint32_t)((lane & 15) >> 1), hb = (uint32_t)(lane & 1) * 8;
+    uint2 xrow[11];  // rows r0 - 3 .. r0 + 7
+#pragma unroll
+    for (int m = 0; m < 11; ++m) {
+      const int tr = r0 - 3 + m;
+      xrow[m] = tr >= 0 ? *reinterpret_cast<const uint2 *>(raw + part * 16384 + cb * 8192 + swz(tr, ch) + hb)
+                        : f.hist[m < 3 ? m : 0];
+    }
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       float y[4];
@@ -151,7 +177,7 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
       for (int c2 = 0; c2 < 4; ++c2) {
         // bf16 channel c2 of row m: low or high half of word c2 / 2
         auto xv = [&](int m) {
-          const uint32_t wd = (c2 >> 1) ? f.x[m].y : f.x[m].x;
+          const uint32_t wd = (c2 >> 1) ? xrow[m].y : xrow[m].x;
           return __uint_as_float((c2 & 1) ? (wd & 0xffff0000u) : (wd << 16));
         };
         const float4 wc = f.w[c2];
@@ -201,6 +227,7 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
     p.Gp[unit * p.Tp + t0 + 2 * lane + 1] = gb;
   }
 
+  const bool raw_ok = mbar_wait(bar_raw, 0);  // visibility of the raw tile to this thread
   fe_load(warp + 8, fb);
   fe_compute(warp, fa);
   fe_load(warp + 16, fa);
@@ -230,7 +257,7 @@ __global__ void __launch_bounds__(kPrepThreads) gdn_prep_kernel(const PrepParams
     }
     umma_commit(bar);
   }
-  bool ok = __syncthreads_and(mbar_wait(bar, 0));
+  bool ok = __syncthreads_and(mbar_wait(bar, 0) && raw_ok);
   tc_fence_after();
 
   // ---- A_ij = beta_i 2^(g_i - g_j) (k_i . k_j) for j < i (rows from TMEM lanes 64..127)
@@ -979,7 +1006,11 @@ glinattn_status launch_gdn_tc(const glinattn_prefill_args &a, cudaStream_t strea
   if (cudaFuncSetAttribute(gdn_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kPrepSmem) != cudaSuccess)
     return GLINATTN_ERR_CUDA;
-  gdn_prep_kernel<<<dim3(nchunks, H, B), kPrepThreads, kPrepSmem, stream>>>(pp);
+  CUtensorMap rq, rk, rv;  // raw activations, 64-token x 64-channel boxes
+  if (!make_act_map(&rq, a.q, B, T, H, kD) || !make_act_map(&rk, a.k, B, T, H, kD) ||
+      !make_act_map(&rv, a.v, B, T, H, kD))
+    return GLINATTN_ERR_CUDA;
+  gdn_prep_kernel<<<dim3(nchunks, H, B), kPrepThreads, kPrepSmem, stream>>>(rq, rk, rv, pp);
   if (cudaGetLastError() != cudaSuccess) return GLINATTN_ERR_CUDA;
 
   CUtensorMap tq, tk, tw, tu;

@@ -552,6 +552,8 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 // [B, T, H, d] bf16 activations as a 4-D map (d, H, T, B), box 64 x 1 x 64 x 1.
 bool make_act_map(CUtensorMap *m, const void *base, int B, int T, int H, int d) {
   EncodeTiledFn enc = encode_fn();
@@ -564,8 +566,6 @@ bool make_act_map(CUtensorMap *m, const void *base, int B, int T, int H, int d) 
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 bool encode_3d_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, int elem_bytes,
                    const long long dims[3], const int box[3], bool swizzle) {

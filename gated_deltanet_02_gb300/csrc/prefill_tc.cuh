@@ -23,6 +23,10 @@ bool gdn_tc_supports(const glinattn_prefill_args &a);
 size_t gdn_tc_workspace_bytes(const glinattn_prefill_args &a);
 glinattn_status launch_gdn_tc(const glinattn_prefill_args &a, cudaStream_t stream);
 
+// [B, T, H, d] bf16 activations as a 4-D map (d, H, T, B); box 64 x 1 x 64 x 1
+// (64 channels of one head for 64 tokens), 128-byte swizzle.
+bool make_act_map(CUtensorMap *m, const void *base, int B, int T, int H, int d);
+
 // General 3-D tiled map: dims (innermost first) and box in elements.
 bool encode_3d_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, int elem_bytes,
                    const long long dims[3], const int box[3], bool swizzle);
