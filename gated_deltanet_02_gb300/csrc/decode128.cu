@@ -55,7 +55,7 @@ constexpr int kTabWords = 32;         // [0] src slot, [1..8] dst slots, [9..16]
 constexpr uint32_t kStateBytes = kD * kDC * 4;
 constexpr uint32_t kMiscBytes = kNCH * 4 + kNW * 2 * kDC * 4 + 3 * kNW * 4 + kTab * kTabWords * 4 + kRing * 8;
 
-constexpr int kRingSteps = 4;         // token rows of a unit carried in its ring slot
+constexpr int kRingSteps = 2;         // token rows of a unit carried in its ring slot (3 CTAs per SM)
 // ring slot: the state half, then the conv history (3 rows) and the first
 // `xrows` token rows of the unit, each row kNCH channels of `esz` bytes
 __host__ __device__ constexpr int ring_xrows(int steps) { return steps < kRingSteps ? steps : kRingSteps; }
@@ -286,15 +286,26 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
       float *sst = reinterpret_cast<float *>(smem + s * sbytes);
       float4 *st4 = reinterpret_cast<float4 *>(sst);
       const uint8_t *small = smem + s * sbytes + kStateBytes;
-      // front-end inputs of step 0 from the ring
-      float xr[kMaxC], hr[kMaxC][3];
+      // raw input of local channel c at step st: the ring slot's rows for the
+      // first xrows steps, global memory after that
+      auto x_at = [&](int st, int c) -> float {
+        if (st < xrows) return ld_act(small, (3 + st) * kNCH + c, in_bf16);
+        const void *src = c < kD ? p.q : (c < 2 * kD ? p.k : p.v);
+        const int ci = c < 2 * kD ? (c % kD) : col0 + (c - 2 * kD);
+        return ld_act(src, (((size_t)n * steps + st) * H + h) * kD + ci, in_bf16);
+      };
+      // inputs of this step (xr) and of the next two (xa, xb): global loads are
+      // issued two steps before their use
+      float xr[kMaxC], xa[kMaxC], xb[kMaxC], hr[kMaxC][3];
 #pragma unroll
       for (int i = 0; i < kMaxC; ++i) {
         const int c = tid + i * kNT;
-        xr[i] = 0.f;
+        xr[i] = xa[i] = xb[i] = 0.f;
         hr[i][0] = hr[i][1] = hr[i][2] = 0.f;
         if (c < kNCH) {
-          xr[i] = ld_act(small, 3 * kNCH + c, in_bf16);
+          xr[i] = x_at(0, c);
+          if (steps > 1) xa[i] = x_at(1, c);
+          if (steps > 2) xb[i] = x_at(2, c);
           if (conv)
 #pragma unroll
             for (int j = 0; j < 3; ++j) hr[i][j] = ld_act(small, j * kNCH + c, in_bf16);
@@ -337,14 +348,10 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
           hr[i][0] = hr[i][1];
           hr[i][1] = hr[i][2];
           hr[i][2] = x;
-          if (c < kNCH && !last) {  // next step's token: from the ring slot, else global memory
-            if (t + 1 < xrows) {
-              xr[i] = ld_act(small, (3 + t + 1) * kNCH + c, in_bf16);
-            } else {
-              const void *src = c < kD ? p.q : (c < 2 * kD ? p.k : p.v);
-              const int ci = c < 2 * kD ? (c % kD) : col0 + (c - 2 * kD);
-              xr[i] = ld_act(src, (row + H) * kD + ci, in_bf16);
-            }
+          if (c < kNCH && !last) {  // shift the input queue; step t + 3 is loaded now
+            xr[i] = xa[i];
+            xa[i] = xb[i];
+            if (t + 3 < steps) xb[i] = x_at(t + 3, c);
           }
         }
         float iq = 1.f, ik = 1.f;
