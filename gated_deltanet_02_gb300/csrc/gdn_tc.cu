@@ -103,6 +103,7 @@ __global__ void __launch_bounds__(kPrepThreads)
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffMisc + 512);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffMisc + 520);
   uint64_t *bar_raw = reinterpret_cast<uint64_t *>(smem + kOffMisc + 528);
+  float *colbg = reinterpret_cast<float *>(smem + kOffMisc + 768);  // beta_k 2^g_k, 64 columns
   uint8_t *raw = smem + kOffRaw;
 
   // the chunk's 64 raw rows of q, k and v by TMA (rows past T arrive as zeros)
@@ -269,6 +270,10 @@ __global__ void __launch_bounds__(kPrepThreads)
   float *T10 = T00 + kBlk * (kBlk + 1);
   float *T11 = T10 + kBlk * (kBlk + 1);
   constexpr int kLd = kBlk + 1;
+  if (ok && warp < 2) {  // column scales of T diag(beta gamma)
+    const int k = 32 * warp + lane;
+    colbg[k] = betas[k] * exp2f(g2s[k]);
+  }
   if (ok && (warp == 2 || warp == 3)) {
     const int i = 32 * (warp - 2) + lane;
     float kk[64];
@@ -324,26 +329,30 @@ __global__ void __launch_bounds__(kPrepThreads)
   }
   __syncthreads();
   float *X = A00;  // A00 is no longer needed: X = A10 T00 takes its place
+  // a warp computes rows warp, warp + 8, +16, +24 of a product, lane = column;
+  // each element of the right factor is loaded once for the four rows
   if (ok) {
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      const int i = warp + 8 * rr;
-      float acc = 0.f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
-      for (int j = 0; j < kBlk; ++j) acc += A10[i * kLd + j] * T00[j * kLd + lane];
-      X[i * kLd + lane] = acc;
+    for (int j = 0; j < kBlk; ++j) {
+      const float t = T00[j * kLd + lane];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) acc[rr] += A10[(warp + 8 * rr) * kLd + j] * t;
     }
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) X[(warp + 8 * rr) * kLd + lane] = acc[rr];
   }
   __syncthreads();
   if (ok) {
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      const int i = warp + 8 * rr;
-      float acc = 0.f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
-      for (int j = 0; j < kBlk; ++j) acc += T11[i * kLd + j] * X[j * kLd + lane];
-      T10[i * kLd + lane] = -acc;
+    for (int j = 0; j < kBlk; ++j) {
+      const float x = X[j * kLd + lane];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) acc[rr] += T11[(warp + 8 * rr) * kLd + j] * x;
     }
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) T10[(warp + 8 * rr) * kLd + lane] = -acc[rr];
   }
   __syncthreads();
   // ---- T diag(beta gamma) and T diag(beta) as bf16 hi / lo MMA tiles ------------
@@ -359,9 +368,8 @@ __global__ void __launch_bounds__(kPrepThreads)
         float tv;
         if (i < kBlk) tv = k < kBlk ? T00[i * kLd + k] : 0.f;
         else tv = k < kBlk ? T10[(i - kBlk) * kLd + k] : T11[(i - kBlk) * kLd + (k - kBlk)];
-        const float bk = betas[k];
-        w1[e2] = tv * (bk * exp2f(g2s[k]));
-        w2[e2] = tv * bk;
+        w1[e2] = tv * colbg[k];
+        w2[e2] = tv * betas[k];
       }
       uint32_t h1[4], l1[4], h2[4], l2[4];
 #pragma unroll
