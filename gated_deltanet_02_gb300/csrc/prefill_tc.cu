@@ -291,8 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float qk[32];
       {
         float lo32[32], hi32[32];
-        tmem_ld32(tmem + kColQK + tb * 64 + lane_base, lo32);
-        tmem_ld32(tmem + kColQK + tb * 64 + 32 + lane_base, hi32);
+        tmem_ld32x2(tmem + kColQK + tb * 64 + lane_base, tmem + kColQK + tb * 64 + 32 + lane_base, lo32, hi32);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const float x = __shfl_sync(0xffffffffu, hi32[j], lane & 15);
@@ -419,8 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           float dh[32], dl[32];
-          tmem_ld32(tmem + kColDS + 32 * half + lane_base, dh);
-          tmem_ld32(tmem + kColDS + kBV + 32 * half + lane_base, dl);
+          tmem_ld32x2(tmem + kColDS + 32 * half + lane_base, tmem + kColDS + kBV + 32 * half + lane_base, dh, dl);
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) S[32 * half + jj] = gam * S[32 * half + jj] + (dh[jj] + dl[jj]);
         }
@@ -440,9 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int qt = 0; qt < 4; ++qt) {
           float o1[16], o1l[16], o2[16];
-          tmem_ld16(tmem + kColO1 + 16 * qt + lane_base, o1);
-          tmem_ld16(tmem + kColO1 + kBV + 16 * qt + lane_base, o1l);
-          tmem_ld16(tmem + kColO2 + tb * 64 + 16 * qt + lane_base, o2);
+          tmem_ld16x3(tmem + kColO1 + 16 * qt + lane_base, tmem + kColO1 + kBV + 16 * qt + lane_base,
+                      tmem + kColO2 + tb * 64 + 16 * qt + lane_base, o1, o1l, o2);
           float ov[16];
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) ov[jj] = gi * (o1[jj] + o1l[jj]) + o2[jj];
