@@ -31,9 +31,15 @@ struct RecurParams {
   const void *conv_src;  // NULL = zero history
   void *conv_dst;        // NULL = not written
   uint32_t *dev_status;
+  // prefill only: the state after every state_every tokens to S_blocks
+  // [N, nblocks, H, d, d] (state_every == 0: none)
+  float *S_blocks;
+  int state_every, nblocks;
 };
 
 glinattn_status launch_recurrent(const RecurParams &p, int d, cudaStream_t stream);
+// conv caches at the emitted block boundaries of a prefill (checkpoint.cu)
+glinattn_status launch_conv_blocks(const glinattn_prefill_args &a, cudaStream_t stream);
 
 // Persistent pipelined decode / speculative decode for 128 x 128 pooled states.
 bool decode128_supports(const RecurParams &p, int d);

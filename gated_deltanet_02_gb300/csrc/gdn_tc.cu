@@ -478,6 +478,8 @@ constexpr uint32_t kColQK = 0, kColWS = 64, kColDS = 128, kColQS = 192, kColPU =
 
 struct ScanParams {
   int B, T, H, nchunks, Tp, out_bf16;
+  int state_every, nblocks;  // states emitted after every state_every tokens (a multiple of 64)
+  float *S_blocks;
   const float *alpha;
   const float *Gp;
   const float *S0;
@@ -851,6 +853,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // buffer (c + 1) & 1 was last read by W S (done: ds_ready of chunk c - 1)
       // and Q' S (done: o_ready of chunk c - 1) of the previous chunk
       if (c + 1 < nchunks) write_state((c + 1) & 1);
+      if (p.state_every && ((c + 1) * kC) % p.state_every == 0 && (c + 1) * kC <= T) {
+        // the state after this chunk closes a block: this thread's row slice goes out
+        float *dst = p.S_blocks +
+                     ((((size_t)b * p.nblocks + (c + 1) * kC / p.state_every - 1) * p.H + h) * kD + srow) * kD +
+                     vblk * kBV;
+#pragma unroll
+        for (int j = 0; j < kBV; j += 4)
+          *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+      }
 
       // ---- o = gamma_i (Q' S) + P U -------------------------------------------------
       if (!wait_bar_warp(&bars->o_ready, pc, abort)) { ok = false; break; }
@@ -1036,6 +1047,9 @@ glinattn_status launch_gdn_tc(const glinattn_prefill_args &a, cudaStream_t strea
   sp.q = pp.q; sp.k = pp.k; sp.v = pp.v; sp.conv_in = pp.conv_in;
   sp.conv_out = static_cast<__nv_bfloat16 *>(a.conv_out);
   sp.dev_status = a.dev_status;
+  sp.state_every = a.state_every > 0 && T / a.state_every > 0 ? a.state_every : 0;
+  sp.nblocks = sp.state_every ? T / sp.state_every : 0;
+  sp.S_blocks = a.S_blocks;
   if (cudaFuncSetAttribute(gdn_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kScanSmem) != cudaSuccess)
     return GLINATTN_ERR_CUDA;

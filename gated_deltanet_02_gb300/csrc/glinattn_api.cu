@@ -74,6 +74,9 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
   const size_t act = a->in_dtype == GLINATTN_BF16 ? 2 : 4;
   const size_t state_bytes = (size_t)B * H * d * d * sizeof(float);
   if (!a->S_T) return GLINATTN_ERR_INVALID_ARG;
+  if (a->state_every < 0) return GLINATTN_ERR_INVALID_ARG;
+  const bool emit_blocks = a->state_every > 0 && T / a->state_every > 0;
+  if (emit_blocks && (!a->S_blocks || !aligned16(a->S_blocks))) return GLINATTN_ERR_INVALID_ARG;
   if (T > 0) {
     if (!a->q || !a->k || !a->v || !a->alpha || !a->o) return GLINATTN_ERR_INVALID_ARG;
     if (a->variant == GLINATTN_GDN && !a->beta) return GLINATTN_ERR_INVALID_ARG;
@@ -88,14 +91,25 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
     if (partial_overlap(a->conv_in, cb, a->conv_out, cb)) return GLINATTN_ERR_INVALID_ARG;
   }
 
-  if (glinattn::prefill_tc_available()) {
+  // the chunked kernels emit states at chunk ends only (checked whatever the device)
+  if ((glinattn::prefill_tc_supports(*a) || glinattn::gdn_tc_supports(*a)) && emit_blocks &&
+      a->state_every % 64 != 0)
+    return GLINATTN_ERR_UNSUPPORTED;
+  const bool tc_device = glinattn::prefill_tc_available();
+  if (tc_device && glinattn::gdn_tc_supports(*a) &&
+      (!a->workspace || a->workspace_bytes < glinattn::gdn_tc_workspace_bytes(*a) || !aligned16(a->workspace)))
+    return GLINATTN_ERR_INVALID_ARG;
+  // conv caches at the block boundaries: taken before the layer runs, since
+  // conv_out may alias conv_in
+  const bool conv_blocks = a->conv_w && a->conv_blocks && emit_blocks;
+  if (conv_blocks) {
+    if (!aligned16(a->conv_blocks)) return GLINATTN_ERR_INVALID_ARG;
+    const glinattn_status st = glinattn::launch_conv_blocks(*a, (cudaStream_t)stream);
+    if (st != GLINATTN_OK) return st;
+  }
+  if (tc_device) {
     if (glinattn::prefill_tc_supports(*a)) return glinattn::launch_prefill_tc(*a, (cudaStream_t)stream);
-    if (glinattn::gdn_tc_supports(*a)) {
-      if (!a->workspace || a->workspace_bytes < glinattn::gdn_tc_workspace_bytes(*a) ||
-          !aligned16(a->workspace))
-        return GLINATTN_ERR_INVALID_ARG;
-      return glinattn::launch_gdn_tc(*a, (cudaStream_t)stream);
-    }
+    if (glinattn::gdn_tc_supports(*a)) return glinattn::launch_gdn_tc(*a, (cudaStream_t)stream);
   }
 
   RecurParams p = {};
@@ -120,6 +134,11 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
   p.conv_src = a->conv_w ? a->conv_in : nullptr;
   p.conv_dst = a->conv_w ? a->conv_out : nullptr;
   p.dev_status = a->dev_status;
+  if (emit_blocks) {
+    p.S_blocks = a->S_blocks;
+    p.state_every = a->state_every;
+    p.nblocks = T / a->state_every;
+  }
   return glinattn::launch_recurrent(p, d, (cudaStream_t)stream);
 }
 

@@ -79,6 +79,8 @@ constexpr uint32_t kColQK = 0, kColO1 = 128, kColO2 = 256, kColDS = 384;
 
 struct GlaParams {
   int B, T, H, nchunks, out_bf16;
+  int state_every, nblocks;  // states emitted after every state_every tokens (a multiple of 64)
+  float *S_blocks;
   const float *alpha;
   const float *S0;
   float *S_T;
@@ -426,6 +428,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->ds_free);
       if (c + 1 < nchunks) write_state((c + 1) & 1);
+      if (p.state_every && ((c + 1) * kC) % p.state_every == 0 && (c + 1) * kC <= T) {
+        // the state after this chunk closes a block: this thread's row slice goes out
+        float *dst = p.S_blocks +
+                     ((((size_t)b * p.nblocks + (c + 1) * kC / p.state_every - 1) * p.H + h) * kDK + srow) * kDK +
+                     vblk * kBV;
+#pragma unroll
+        for (int j = 0; j < kBV; j += 4)
+          *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+      }
 
       // ---- o = gamma_i (Q S) + P V ----------------------------------------------
       if (!wait_bar_warp(&bars->o_ready[tb], ph, abort)) { ok = false; break; }
@@ -614,6 +625,9 @@ glinattn_status launch_prefill_tc(const glinattn_prefill_args &a, cudaStream_t s
   p.S_T = a.S_T;
   p.o = a.o;
   p.dev_status = a.dev_status;
+  p.state_every = a.state_every > 0 && a.seqlen / a.state_every > 0 ? a.state_every : 0;
+  p.nblocks = p.state_every ? a.seqlen / p.state_every : 0;
+  p.S_blocks = a.S_blocks;
   if (cudaFuncSetAttribute(gla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kSmemBytes) != cudaSuccess)
     return GLINATTN_ERR_CUDA;

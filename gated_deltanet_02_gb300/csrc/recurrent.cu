@@ -307,6 +307,9 @@ __global__ void __launch_bounds__(Shape<D>::NT)
     float *dst = nullptr;
     const size_t dslot = (size_t)dslot_t;
     if (emit) dst = p.S_dst + (dslot * p.H + h) * DD + col0;
+    float *bdst = nullptr;  // prefill state emitted at a block boundary
+    if (p.state_every && (t + 1) % p.state_every == 0)
+      bdst = p.S_blocks + (((size_t)n * p.nblocks + (t + 1) / p.state_every - 1) * p.H + h) * DD + col0;
 #pragma unroll
     for (int i = 0; i < Sh::RPT; ++i) {
       const int r = rg + Sh::ROWG * i;
@@ -318,6 +321,7 @@ __global__ void __launch_bounds__(Shape<D>::NT)
       S.w = a * S.w + kr * u.w;
       if (!last) s_state4[r * Sh::COLG + cg] = S;
       if (emit) *reinterpret_cast<float4 *>(dst + (size_t)r * D + 4 * cg) = S;
+      if (bdst) *reinterpret_cast<float4 *>(bdst + (size_t)r * D + 4 * cg) = S;
     }
     if (rg == 0) {
       const float qk = s_qk;

@@ -9,6 +9,7 @@ The three entry points keep the C names:
 * ``glinattn_prefill``     -- chunked prefill of a segment (state hand-over in/out)
 * ``glinattn_decode``      -- one recurrent step per request, state pool by slot id
 * ``glinattn_spec_decode`` -- D draft steps, one state per draft position
+* ``glinattn_state_copy``  -- whole-slot copies inside a state pool (copy on write)
 """
 from __future__ import annotations
 
@@ -43,10 +44,11 @@ _i32 = ctypes.c_int32
 class PrefillArgs(ctypes.Structure):
     _fields_ = [("variant", _i32), ("in_dtype", _i32), ("out_dtype", _i32), ("qk_l2norm", _i32),
                 ("batch", _i32), ("seqlen", _i32), ("heads", _i32), ("dk", _i32), ("dv", _i32),
-                ("reserved0", _i32),
+                ("state_every", _i32),
                 ("q", _vp), ("k", _vp), ("v", _vp), ("alpha", _vp), ("beta", _vp), ("S0", _vp),
                 ("S_T", _vp), ("o", _vp), ("conv_w", _vp), ("conv_in", _vp), ("conv_out", _vp),
-                ("dev_status", _vp), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
+                ("dev_status", _vp), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+                ("S_blocks", _vp), ("conv_blocks", _vp)]
 
 
 class DecodeArgs(ctypes.Structure):
@@ -67,6 +69,12 @@ class SpecArgs(ctypes.Structure):
                 ("conv_w", _vp), ("conv_pool", _vp), ("dev_status", _vp)]
 
 
+class CopyArgs(ctypes.Structure):
+    _fields_ = [("n", _i32), ("pool_slots", _i32), ("heads", _i32), ("dk", _i32), ("dv", _i32),
+                ("in_dtype", _i32), ("state_pool", _vp), ("conv_pool", _vp), ("src_slots", _vp),
+                ("dst_slots", _vp), ("dev_status", _vp)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -79,7 +87,7 @@ def library() -> ctypes.CDLL:
             path = _build.build()
             lib = ctypes.CDLL(path)
             for name, argt in (("glinattn_prefill", PrefillArgs), ("glinattn_decode", DecodeArgs),
-                               ("glinattn_spec_decode", SpecArgs)):
+                               ("glinattn_spec_decode", SpecArgs), ("glinattn_state_copy", CopyArgs)):
                 f = getattr(lib, name)
                 f.argtypes = [ctypes.POINTER(argt), _vp]
                 f.restype = ctypes.c_int
@@ -133,11 +141,15 @@ def _call(name, args, stream_handle):
 
 def glinattn_prefill(q, k, v, alpha, beta=None, S0=None, *, variant=GLA, conv_w=None,
                      conv_in=None, qk_l2norm=False, out_dtype=None, o=None, S_T=None,
-                     conv_out=None, dev_status=None, stream=None, workspace=None):
+                     conv_out=None, dev_status=None, stream=None, workspace=None,
+                     state_every=0, S_blocks=None, conv_blocks=None):
     """Prefill one segment.  q, k [B,T,H,dk], v [B,T,H,dv] (bf16 or fp32);
     alpha/beta [B,T,H] fp32; S0 [B,H,dk,dv] fp32 or None.  Outputs, and the
     scratch space the chunked Gated DeltaNet kernels need, are allocated when
-    not given.  Returns (o, S_T, conv_out)."""
+    not given.  Returns (o, S_T, conv_out); with state_every > 0 also
+    S_blocks [B, T // state_every, H, dk, dv], the state after every
+    state_every tokens of the segment, and conv_blocks [B, T // state_every,
+    3, Cch], the conv cache at the same points (None without a conv)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     dev = q.device
@@ -162,11 +174,26 @@ def glinattn_prefill(q, k, v, alpha, beta=None, S0=None, *, variant=GLA, conv_w=
         _need(conv_out, "conv_out", act, (B, 3, Cch), dev)
     _need(o, "o", out_dtype, (B, T, H, dv), dev)
     _need(S_T, "S_T", torch.float32, (B, H, dk, dv), dev)
+    if state_every < 0:
+        raise ValueError("state_every must be >= 0")
+    nblk = T // state_every if state_every else 0
+    if state_every and S_blocks is None:
+        S_blocks = torch.empty((B, nblk, H, dk, dv), dtype=torch.float32, device=dev)
+    if state_every:
+        _need(S_blocks, "S_blocks", torch.float32, (B, nblk, H, dk, dv), dev)
+        if conv_w is not None:
+            if conv_blocks is None:
+                conv_blocks = torch.empty((B, nblk, 3, Cch), dtype=act, device=dev)
+            _need(conv_blocks, "conv_blocks", act, (B, nblk, 3, Cch), dev)
+        else:
+            conv_blocks = None
     a = PrefillArgs(variant=variant, in_dtype=_dtype_code(q), out_dtype=_dtype_code(o),
                     qk_l2norm=int(bool(qk_l2norm)), batch=B, seqlen=T, heads=H, dk=dk, dv=dv,
                     q=_ptr(q), k=_ptr(k), v=_ptr(v), alpha=_ptr(alpha), beta=_ptr(beta),
                     S0=_ptr(S0), S_T=_ptr(S_T), o=_ptr(o), conv_w=_ptr(conv_w),
-                    conv_in=_ptr(conv_in), conv_out=_ptr(conv_out), dev_status=_ptr(dev_status))
+                    conv_in=_ptr(conv_in), conv_out=_ptr(conv_out), dev_status=_ptr(dev_status),
+                    state_every=state_every, S_blocks=_ptr(S_blocks) if nblk else None,
+                    conv_blocks=_ptr(conv_blocks) if nblk else None)
     ws_bytes = library().glinattn_prefill_workspace_size(ctypes.byref(a))
     ws = None
     if ws_bytes:
@@ -177,6 +204,8 @@ def glinattn_prefill(q, k, v, alpha, beta=None, S0=None, *, variant=GLA, conv_w=
         a.workspace = _ptr(ws)
         a.workspace_bytes = ws_bytes
     _call("glinattn_prefill", a, _stream_handle(stream, dev))
+    if state_every:
+        return o, S_T, conv_out, S_blocks, conv_blocks
     return o, S_T, conv_out
 
 
@@ -251,6 +280,29 @@ def glinattn_spec_decode(q, k, v, alpha, beta, state_pool, src_slots, dst_slots,
                  dev_status=_ptr(dev_status))
     _call("glinattn_spec_decode", a, _stream_handle(stream, dev))
     return o
+
+
+def glinattn_state_copy(state_pool, src_slots, dst_slots, *, conv_pool=None, dev_status=None,
+                        stream=None):
+    """state_pool[dst_slots[i]] = state_pool[src_slots[i]] (and the same for
+    conv_pool [P,3,Cch] when given), in place.  state_pool [P,H,dk,dv] fp32;
+    src_slots, dst_slots [n] int32.  Destination slots must be distinct and
+    must not be a source of another pair of the same call."""
+    P, H, dk, dv = state_pool.shape
+    dev = state_pool.device
+    n = src_slots.shape[0]
+    _need(state_pool, "state_pool", torch.float32, (P, H, dk, dv), dev)
+    _need(src_slots, "src_slots", torch.int32, (n,), dev)
+    _need(dst_slots, "dst_slots", torch.int32, (n,), dev)
+    in_dtype = BF16
+    if conv_pool is not None:
+        _need(conv_pool, "conv_pool", conv_pool.dtype, (P, 3, H * (2 * dk + dv)), dev)
+        in_dtype = _dtype_code(conv_pool)
+    a = CopyArgs(n=n, pool_slots=P, heads=H, dk=dk, dv=dv, in_dtype=in_dtype,
+                 state_pool=_ptr(state_pool), conv_pool=_ptr(conv_pool), src_slots=_ptr(src_slots),
+                 dst_slots=_ptr(dst_slots), dev_status=_ptr(dev_status))
+    _call("glinattn_state_copy", a, _stream_handle(stream, dev))
+    return state_pool
 
 
 def version() -> int:

@@ -86,6 +86,17 @@ typedef enum { GLINATTN_F32 = 0, GLINATTN_BF16 = 1 } glinattn_dtype;
  *   conv_out [B, 3, Cch] (in_dtype) or NULL; may alias conv_in exactly
  *   T may be any value >= 0 (a ragged last chunk is handled); T == 0 copies
  *   S0 to S_T and conv_in to conv_out.
+ *   state_every > 0 also emits the state at block boundaries for prefix
+ *   caching (section "Prefix caching has to be redone": a prefix can be
+ *   reused only where its state was kept): S_blocks [B, T / state_every, H,
+ *   dk, dv] fp32 receives the state after token j * state_every of this
+ *   segment, j = 1 .. T / state_every (rounded down).  The chunked kernels
+ *   need state_every to be a multiple of the chunk (64), else the call returns
+ *   GLINATTN_ERR_UNSUPPORTED; the fp32 token-serial kernel takes any value.
+ *   0 emits nothing and S_blocks is ignored.  With a convolution, conv_blocks
+ *   (when not NULL) [B, T / state_every, 3, Cch] (in_dtype) receives the conv
+ *   cache at the same boundaries, so that (S_blocks[:, j], conv_blocks[:, j])
+ *   is a whole checkpoint a later prefill or decode can start from.
  *   bf16 activations with dk == dv == 128 run the tensor-core chunked kernels
  *   (chunk 64; Gated DeltaNet also needs `workspace`, see below, else
  *   GLINATTN_ERR_INVALID_ARG); every other supported combination runs the
@@ -97,7 +108,7 @@ typedef struct {
   int32_t out_dtype; /* glinattn_dtype of o */
   int32_t qk_l2norm;
   int32_t batch, seqlen, heads, dk, dv;
-  int32_t reserved0;
+  int32_t state_every; /* 0, or the block length of emitted states (see above) */
   const void *q, *k, *v;
   const float *alpha, *beta;
   const float *S0;
@@ -109,6 +120,8 @@ typedef struct {
   uint32_t *dev_status;
   void *workspace;        /* device scratch, >= glinattn_prefill_workspace_size() bytes */
   size_t workspace_bytes; /* its size; may be 0 when the size query returns 0 */
+  float *S_blocks;        /* [B, T / state_every, H, dk, dv] fp32 when state_every > 0 */
+  void *conv_blocks;      /* [B, T / state_every, 3, Cch] (in_dtype) or NULL */
 } glinattn_prefill_args;
 
 glinattn_status glinattn_prefill(const glinattn_prefill_args *args, glinattn_stream_t stream);
@@ -213,6 +226,34 @@ typedef struct {
 } glinattn_spec_args;
 
 glinattn_status glinattn_spec_decode(const glinattn_spec_args *args, glinattn_stream_t stream);
+
+/*
+ * glinattn_state_copy -- copy whole slots of a state pool (and of its conv
+ *   cache pool): for i < n, state_pool[dst_slots[i]] = state_pool[src_slots[i]]
+ *   and, when conv_pool is given, conv_pool[dst_slots[i]] =
+ *   conv_pool[src_slots[i]].  Section "Prefix caching has to be redone": a
+ *   request that reuses a cached prefix starts from a copy of the prefix's
+ *   state, never from the cached slot itself (copy on write); section
+ *   "Speculative decoding and PD disaggregation": an accepted draft's state
+ *   can be copied back to the request's own slot.
+ *
+ *   state_pool [P, H, dk, dv] fp32     conv_pool [P, 3, Cch] (in_dtype) or NULL
+ *   src_slots, dst_slots [n] int32 (device memory)
+ *   A pair whose slot is outside [0, pool_slots) is skipped and raises
+ *   GLINATTN_DEV_BAD_SLOT in *dev_status (when given).  Destination slots must
+ *   be distinct and must not be a source slot of another pair of the same call
+ *   (not checked on the device).
+ */
+typedef struct {
+  int32_t n, pool_slots, heads, dk, dv, in_dtype;
+  float *state_pool;
+  void *conv_pool;
+  const int32_t *src_slots;
+  const int32_t *dst_slots;
+  uint32_t *dev_status;
+} glinattn_copy_args;
+
+glinattn_status glinattn_state_copy(const glinattn_copy_args *args, glinattn_stream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 const char *glinattn_status_string(glinattn_status status);

@@ -22,7 +22,7 @@ def _declared_functions():
 def test_library_exports_every_declared_symbol():
     lib = G.library()
     names = _declared_functions()
-    assert {"glinattn_prefill", "glinattn_decode", "glinattn_spec_decode",
+    assert {"glinattn_prefill", "glinattn_decode", "glinattn_spec_decode", "glinattn_state_copy",
             "glinattn_status_string", "glinattn_version"} <= set(names)
     for name in names:
         assert hasattr(lib, name), name
@@ -32,11 +32,14 @@ def test_library_exports_every_declared_symbol():
         assert re.search(rf"\bT {name}$", out, re.M), name
 
 
+STRUCTS = ((G.PrefillArgs, "glinattn_prefill_args"), (G.DecodeArgs, "glinattn_decode_args"),
+           (G.SpecArgs, "glinattn_spec_args"), (G.CopyArgs, "glinattn_copy_args"))
+
+
 def test_struct_layout_matches_header(tmp_path):
     src = tmp_path / "layout.c"
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "glinattn.h"', "int main(void){"]
-    for ct, cname in ((G.PrefillArgs, "glinattn_prefill_args"), (G.DecodeArgs, "glinattn_decode_args"),
-                      (G.SpecArgs, "glinattn_spec_args")):
+    for ct, cname in STRUCTS:
         lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
         for fname, _ in ct._fields_:
             lines.append(f'printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
@@ -49,8 +52,7 @@ def test_struct_layout_matches_header(tmp_path):
         if line:
             s, f, v = line.split()
             got[(s, f)] = int(v)
-    for ct, cname in ((G.PrefillArgs, "glinattn_prefill_args"), (G.DecodeArgs, "glinattn_decode_args"),
-                      (G.SpecArgs, "glinattn_spec_args")):
+    for ct, cname in STRUCTS:
         assert got[(cname, "size")] == ctypes.sizeof(ct)
         for fname, _ in ct._fields_:
             assert got[(cname, fname)] == getattr(ct, fname).offset, (cname, fname)
@@ -118,6 +120,10 @@ INVALID, UNSUPPORTED = 1, 2
     (dict(o=None), INVALID),
     (dict(q=A + 8), INVALID),            # 16-byte alignment
     (dict(S0=A * 6 + 64), INVALID),      # S0 partially overlaps S_T
+    (dict(state_every=-1), INVALID),
+    (dict(state_every=50), INVALID),     # two blocks to emit but no S_blocks
+    (dict(state_every=50, S_blocks=A * 9 + 4), INVALID),
+    (dict(state_every=50, S_blocks=A * 9), UNSUPPORTED),  # chunked kernels: multiples of 64 only
 ])
 def test_prefill_rejects(kw, code):
     rc = G.library().glinattn_prefill(ctypes.byref(_prefill(**kw)), None)
@@ -158,3 +164,33 @@ def test_zero_requests_is_a_noop():
     lib = G.library()
     assert lib.glinattn_decode(ctypes.byref(_decode(num_req=0, q=None)), None) == 0
     assert lib.glinattn_spec_decode(ctypes.byref(_spec(num_req=0, q=None)), None) == 0
+
+
+def _copy(**kw):
+    base = dict(n=3, pool_slots=8, heads=2, dk=64, dv=64, in_dtype=G.BF16, state_pool=A,
+                conv_pool=A * 2, src_slots=A * 3, dst_slots=A * 4)
+    base.update(kw)
+    return G.CopyArgs(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n=-1), INVALID),
+    (dict(pool_slots=0), INVALID),
+    (dict(heads=0), INVALID),
+    (dict(in_dtype=5), INVALID),
+    (dict(state_pool=None), INVALID),
+    (dict(src_slots=None), INVALID),
+    (dict(dst_slots=None), INVALID),
+    (dict(state_pool=A + 4), INVALID),
+    (dict(conv_pool=A * 2 + 8), INVALID),
+    (dict(n=70000), UNSUPPORTED),
+    (dict(dk=3, dv=3, conv_pool=None), UNSUPPORTED),  # a slot of 18 floats: not whole 16-byte words
+])
+def test_state_copy_rejects(kw, code):
+    assert G.library().glinattn_state_copy(ctypes.byref(_copy(**kw)), None) == code
+
+
+def test_state_copy_zero_pairs_is_a_noop():
+    lib = G.library()
+    assert lib.glinattn_state_copy(None, None) == INVALID
+    assert lib.glinattn_state_copy(ctypes.byref(_copy(n=0, state_pool=None)), None) == 0
