@@ -31,6 +31,10 @@ struct RecurParams {
   const void *conv_src;  // NULL = zero history
   void *conv_dst;        // NULL = not written
   uint32_t *dev_status;
+  // [N] steps applied per request (0 .. steps; NULL: all): the replay of
+  // accepted drafts.  With S_dst == NULL no state or conv cache is written,
+  // with o == NULL no output.
+  const int32_t *step_count;
   // prefill only: the state after every state_every tokens to S_blocks
   // [N, nblocks, H, d, d] (state_every == 0: none)
   float *S_blocks;

@@ -51,7 +51,8 @@ constexpr int kMaxC = (kNCH + kNT - 1) / kNT;
 constexpr int kRing = 2;              // units in flight per CTA
 constexpr int kTab = 4;               // unit table entries
 constexpr int kTabSteps = 8;          // per-step scalars kept in a table entry
-constexpr int kTabWords = 32;         // [0] src slot, [1..8] dst slots, [9..16] alpha, [17..24] beta
+constexpr int kTabWords = 32;         // [0] src slot, [1..8] dst slots, [9..16] alpha, [17..24] beta,
+                                      // [25] steps applied (replay)
 constexpr uint32_t kStateBytes = kD * kDC * 4;
 constexpr uint32_t kMiscBytes = kNCH * 4 + kNW * 2 * kDC * 4 + 3 * kNW * 4 + kTab * kTabWords * 4 + kRing * 8;
 
@@ -142,13 +143,15 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
         cp_async4(&e[0], &p.src_slot[n]);
       } else if (lane <= kTabSteps) {
         const int t = lane - 1;
-        if (t < tsteps && t < ndst) cp_async4(&e[lane], &p.dst_slot[(size_t)n * ndst + t]);
+        if (t < tsteps && t < ndst && p.dst_slot) cp_async4(&e[lane], &p.dst_slot[(size_t)n * ndst + t]);
       } else if (lane <= 2 * kTabSteps) {
         const int t = lane - 1 - kTabSteps;
         if (t < tsteps) cp_async4(&e[lane], &p.alpha[((size_t)n * steps + t) * H + h]);
       } else if (lane <= 3 * kTabSteps) {
         const int t = lane - 1 - 2 * kTabSteps;
         if (t < tsteps && gdn) cp_async4(&e[lane], &p.beta[((size_t)n * steps + t) * H + h]);
+      } else if (lane == 3 * kTabSteps + 1 && p.step_count) {
+        cp_async4(&e[lane], &p.step_count[n]);
       }
     }
     cp_async_commit();  // one group per call, empty past the end
@@ -159,8 +162,9 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
     const int *e = s_tab + (k % kTab) * kTabWords;
     uint64_t *bar = &s_full[k % kRing];
     const int slot = e[0];
-    if (slot < 0 || slot >= p.pool_slots) {  // reported when the unit is computed
-      mbar_arrive(bar);
+    const int su = p.step_count ? e[1 + 3 * kTabSteps] : steps;
+    if (slot < 0 || slot >= p.pool_slots || su <= 0 || su > steps) {  // nothing to load; reported when
+      mbar_arrive(bar);                                              // the unit is computed
       return;
     }
     const int n = unit_n(k), h = unit_h(k);
@@ -254,14 +258,23 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
     // ---- validation from the table (uniform): slots in range, gates in (0, 1] ----
     const int *e = s_tab + (k % kTab) * kTabWords;
     int bad = 0;
+    // steps applied to this unit: all, or the request's accepted length (replay)
+    int su = steps;
+    if (!dead && p.step_count) {
+      su = e[1 + 3 * kTabSteps];
+      if (su < 0 || su > steps) {
+        bad |= GLINATTN_DEV_BAD_COUNT;
+        su = 0;
+      }
+    }
     if (!dead) {
       const int slot = e[0];
       if (slot < 0 || slot >= p.pool_slots) bad |= GLINATTN_DEV_BAD_SLOT;
-      for (int t = 0; t < tsteps && t < ndst; ++t) {
+      for (int t = 0; t < tsteps && t < ndst && p.dst_slot; ++t) {
         const int d = e[1 + t];
         if (d < 0 || d >= p.pool_slots) bad |= GLINATTN_DEV_BAD_SLOT;
       }
-      for (int t = 0; t < tsteps; ++t) {
+      for (int t = 0; t < tsteps && t < su; ++t) {
         const float a = __int_as_float(e[1 + kTabSteps + t]);
         if (!(a > 0.f && a <= 1.f)) bad |= GLINATTN_DEV_BAD_GATE;
       }
@@ -269,8 +282,8 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
         int b2 = 0;
         for (int t = kTabSteps + tid; t < steps; t += kNT) {
           const float a = p.alpha[((size_t)n * steps + t) * H + h];
-          if (!(a > 0.f && a <= 1.f)) b2 |= GLINATTN_DEV_BAD_GATE;
-          if (t < ndst) {
+          if (t < su && !(a > 0.f && a <= 1.f)) b2 |= GLINATTN_DEV_BAD_GATE;
+          if (t < ndst && p.dst_slot) {
             const int d = p.dst_slot[(size_t)n * ndst + t];
             if (d < 0 || d >= p.pool_slots) b2 |= GLINATTN_DEV_BAD_SLOT;
           }
@@ -282,7 +295,7 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
     }
     bool hist_waited = false;
 
-    if (!dead && !bad) {
+    if (!dead && !bad && su > 0) {
       float *sst = reinterpret_cast<float *>(smem + s * sbytes);
       float4 *st4 = reinterpret_cast<float4 *>(sst);
       const uint8_t *small = smem + s * sbytes + kStateBytes;
@@ -304,8 +317,8 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
         hr[i][0] = hr[i][1] = hr[i][2] = 0.f;
         if (c < kNCH) {
           xr[i] = x_at(0, c);
-          if (steps > 1) xa[i] = x_at(1, c);
-          if (steps > 2) xb[i] = x_at(2, c);
+          if (su > 1) xa[i] = x_at(1, c);
+          if (su > 2) xb[i] = x_at(2, c);
           if (conv)
 #pragma unroll
             for (int j = 0; j < 3; ++j) hr[i][j] = ld_act(small, j * kNCH + c, in_bf16);
@@ -315,12 +328,12 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
       float b_nx = gdn ? __int_as_float(e[1 + 2 * kTabSteps]) : 0.f;
       int d_nx = e[1];
 
-      for (int t = 0; t < steps; ++t) {
+      for (int t = 0; t < su; ++t) {
         const size_t row = ((size_t)n * steps + t) * H + h;  // (n, t, h)
         const float a = a_nx, bgate = b_nx;
         const int dslot = d_nx;
-        const bool last = t == steps - 1;
-        const bool emit = p.dst_per_step || last;
+        const bool last = t == su - 1;
+        const bool emit = p.S_dst && (p.dst_per_step || last);
         if (!last) {  // next step's scalars: table, else global memory
           const int t1 = t + 1;
           if (t1 < kTabSteps) {
@@ -330,7 +343,7 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
           } else {
             a_nx = p.alpha[row + H];
             if (gdn) b_nx = p.beta[row + H];
-            if (p.dst_per_step) d_nx = p.dst_slot[(size_t)n * ndst + t1];
+            if (p.dst_per_step && p.dst_slot) d_nx = p.dst_slot[(size_t)n * ndst + t1];
           }
         }
         // ---- front end: conv, history shift, next token prefetch, L2 norms ------
@@ -351,7 +364,7 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
           if (c < kNCH && !last) {  // shift the input queue; step t + 3 is loaded now
             xr[i] = xa[i];
             xa[i] = xb[i];
-            if (t + 3 < steps) xb[i] = x_at(t + 3, c);
+            if (t + 3 < su) xb[i] = x_at(t + 3, c);
           }
         }
         float iq = 1.f, ik = 1.f;
@@ -457,7 +470,7 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
           if (!last) st4[r * kColG + cg] = S;
           if (emit) *reinterpret_cast<float4 *>(dst + (size_t)r * kD + 4 * cg) = S;
         }
-        if (rg == 0) {
+        if (rg == 0 && p.o) {
           const float o0 = a * y.x + qk * u.x, o1 = a * y.y + qk * u.y;
           const float o2 = a * y.z + qk * u.z, o3 = a * y.w + qk * u.w;
           const size_t ob = row * kD + col0 + 4 * cg;
@@ -510,7 +523,7 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
 }  // namespace
 
 bool decode128_supports(const RecurParams &p, int d) {
-  return d == kD && p.src_slot != nullptr && p.dst_slot != nullptr && p.S_src != nullptr &&
+  return d == kD && p.src_slot != nullptr && (p.dst_slot != nullptr || p.S_dst == nullptr) && p.S_src != nullptr &&
          p.steps >= 1 && p.pool_slots > 0 && (p.conv_w == nullptr || p.conv_src != nullptr) &&
          p.S_blocks == nullptr;
 }

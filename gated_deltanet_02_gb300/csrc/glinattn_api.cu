@@ -198,8 +198,7 @@ glinattn_status glinattn_spec_decode(const glinattn_spec_args *a, glinattn_strea
   if ((long long)a->num_req * a->heads > (1ll << 30) || a->draft_len > (1 << 20))
     return GLINATTN_ERR_INVALID_ARG;
   if (a->num_req == 0) return GLINATTN_OK;
-  if (!a->q || !a->k || !a->v || !a->alpha || !a->o || !a->state_pool || !a->src_slots ||
-      !a->dst_slots)
+  if (!a->q || !a->k || !a->v || !a->alpha || !a->o || !a->state_pool || !a->src_slots)
     return GLINATTN_ERR_INVALID_ARG;
   if (a->variant == GLINATTN_GDN && !a->beta) return GLINATTN_ERR_INVALID_ARG;
   if (a->conv_w && !a->conv_pool) return GLINATTN_ERR_INVALID_ARG;
@@ -222,10 +221,53 @@ glinattn_status glinattn_spec_decode(const glinattn_spec_args *a, glinattn_strea
   p.beta = a->beta;
   p.S_src = a->state_pool;
   p.src_slot = a->src_slots;
-  p.S_dst = a->state_pool;
+  const bool verify_only = a->dst_slots == nullptr;  // outputs only, the pool is not written
+  p.S_dst = verify_only ? nullptr : a->state_pool;
   p.dst_slot = a->dst_slots;
-  p.dst_per_step = 1;
+  p.dst_per_step = verify_only ? 0 : 1;
   p.o = a->o;
+  p.conv_w = a->conv_w;
+  p.conv_src = a->conv_w ? a->conv_pool : nullptr;
+  p.conv_dst = a->conv_w && !verify_only ? a->conv_pool : nullptr;
+  p.dev_status = a->dev_status;
+  return glinattn::launch_recurrent(p, a->dk, (cudaStream_t)stream);
+}
+
+glinattn_status glinattn_replay(const glinattn_replay_args *a, glinattn_stream_t stream) {
+  if (!a) return GLINATTN_ERR_INVALID_ARG;
+  glinattn_status st = check_common(a->variant, a->in_dtype, GLINATTN_F32, a->dk, a->dv, a->heads);
+  if (st != GLINATTN_OK) return st;
+  if (a->num_req < 0 || a->draft_len <= 0 || a->pool_slots <= 0) return GLINATTN_ERR_INVALID_ARG;
+  if ((long long)a->num_req * a->heads > (1ll << 30) || a->draft_len > (1 << 20))
+    return GLINATTN_ERR_INVALID_ARG;
+  if (a->num_req == 0) return GLINATTN_OK;
+  if (!a->q || !a->k || !a->v || !a->alpha || !a->state_pool || !a->slot_ids || !a->accept)
+    return GLINATTN_ERR_INVALID_ARG;
+  if (a->variant == GLINATTN_GDN && !a->beta) return GLINATTN_ERR_INVALID_ARG;
+  if (a->conv_w && !a->conv_pool) return GLINATTN_ERR_INVALID_ARG;
+  if (!all_aligned(a->q, a->k, a->v, a->alpha, a->beta, a->state_pool, a->conv_w, a->conv_pool))
+    return GLINATTN_ERR_INVALID_ARG;
+  RecurParams p = {};
+  p.variant = a->variant;
+  p.in_bf16 = a->in_dtype == GLINATTN_BF16;
+  p.qk_l2norm = a->qk_l2norm != 0;
+  p.N = a->num_req;
+  p.steps = a->draft_len;
+  p.H = a->heads;
+  p.pool_slots = a->pool_slots;
+  p.Cch = a->heads * 3 * a->dk;
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.alpha = a->alpha;
+  p.beta = a->beta;
+  p.S_src = a->state_pool;
+  p.src_slot = a->slot_ids;
+  p.S_dst = a->state_pool;  // in place, the final state only
+  p.dst_slot = a->slot_ids;
+  p.dst_per_step = 0;
+  p.step_count = a->accept;
+  p.o = nullptr;
   p.conv_w = a->conv_w;
   p.conv_src = a->conv_w ? a->conv_pool : nullptr;
   p.conv_dst = a->conv_w ? a->conv_pool : nullptr;

@@ -109,6 +109,16 @@ __global__ void __launch_bounds__(Shape<D>::NT)
   // conv-cache channels written by this CTA: q and k by slice 0, each v slice by its owner
   auto writes_chan = [&](int c) { return c >= 2 * D || half == 0; };
 
+  // steps applied by this request: all, or its accepted length (replay)
+  int steps_n = p.steps;
+  if (p.step_count) {
+    steps_n = p.step_count[n];
+    if (steps_n < 0 || steps_n > p.steps) {
+      if (tid == 0 && half == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_BAD_COUNT);
+      return;
+    }
+    if (steps_n == 0) return;  // nothing accepted: the slot stays as it is
+  }
   // ---- every independent load is issued first ----------------------------------
   int slot = n;
   bool slot_ok = true;
@@ -168,7 +178,7 @@ __global__ void __launch_bounds__(Shape<D>::NT)
       if (s < 0 || s >= p.pool_slots) bad |= GLINATTN_DEV_BAD_SLOT;
     }
   }
-  for (int t = tid; t < p.steps; t += Sh::NT) {
+  for (int t = tid; t < steps_n; t += Sh::NT) {
     const float a = p.alpha[((size_t)n * p.steps + t) * p.H + h];
     if (!(a > 0.f && a <= 1.f)) bad |= GLINATTN_DEV_BAD_GATE;
   }
@@ -196,11 +206,11 @@ __global__ void __launch_bounds__(Shape<D>::NT)
   };
   if (Sh::NSPLIT > 1) cluster_arrive();
 
-  for (int t = 0; t < p.steps; ++t) {
+  for (int t = 0; t < steps_n; ++t) {
     const size_t row = ((size_t)n * p.steps + t) * p.H + h;  // (n, t, h)
     const float a = a_next, bgate = b_next;
     const int dslot_t = dslot_next;
-    if (t + 1 < p.steps) {
+    if (t + 1 < steps_n) {
       a_next = p.alpha[row + p.H];
       if (p.variant == GLINATTN_GDN) b_next = p.beta[row + p.H];
       if (p.dst_slot && p.dst_per_step) dslot_next = p.dst_slot[(size_t)n * p.steps + t + 1];
@@ -220,7 +230,7 @@ __global__ void __launch_bounds__(Shape<D>::NT)
       hr[i][0] = hr[i][1];
       hr[i][1] = hr[i][2];
       hr[i][2] = x;
-      if (c < NCH && t + 1 < p.steps) xr[i] = act_at(c, row + p.H);
+      if (c < NCH && t + 1 < steps_n) xr[i] = act_at(c, row + p.H);
     }
     float iq = 1.f, ik = 1.f;
     if (p.qk_l2norm) {
@@ -302,8 +312,8 @@ __global__ void __launch_bounds__(Shape<D>::NT)
       u.z = b * (vv.z - a * x.z);
       u.w = b * (vv.w - a * x.w);
     }
-    const bool last = (t == p.steps - 1);
-    const bool emit = p.dst_per_step || last;
+    const bool last = (t == steps_n - 1);
+    const bool emit = p.S_dst && (p.dst_per_step || last);
     float *dst = nullptr;
     const size_t dslot = (size_t)dslot_t;
     if (emit) dst = p.S_dst + (dslot * p.H + h) * DD + col0;
@@ -323,7 +333,7 @@ __global__ void __launch_bounds__(Shape<D>::NT)
       if (emit) *reinterpret_cast<float4 *>(dst + (size_t)r * D + 4 * cg) = S;
       if (bdst) *reinterpret_cast<float4 *>(bdst + (size_t)r * D + 4 * cg) = S;
     }
-    if (rg == 0) {
+    if (rg == 0 && p.o) {
       const float qk = s_qk;
       const size_t ob = row * D + col0 + 4 * cg;
       store_act(p.o, ob + 0, a * y.x + qk * u.x, p.out_bf16);

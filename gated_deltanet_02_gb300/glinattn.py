@@ -9,6 +9,7 @@ The three entry points keep the C names:
 * ``glinattn_prefill``     -- chunked prefill of a segment (state hand-over in/out)
 * ``glinattn_decode``      -- one recurrent step per request, state pool by slot id
 * ``glinattn_spec_decode`` -- D draft steps, one state per draft position
+* ``glinattn_replay``      -- apply the accepted drafts to the pool in place
 * ``glinattn_state_copy``  -- whole-slot copies inside a state pool (copy on write)
 """
 from __future__ import annotations
@@ -26,6 +27,7 @@ F32, BF16 = 0, 1
 DEV_BAD_SLOT = 0x1
 DEV_BAD_GATE = 0x2
 DEV_WAIT_TIMEOUT = 0x4
+DEV_BAD_COUNT = 0x8
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
            4: "device reported an error status", 5: "device wait timed out"}
@@ -69,6 +71,15 @@ class SpecArgs(ctypes.Structure):
                 ("conv_w", _vp), ("conv_pool", _vp), ("dev_status", _vp)]
 
 
+class ReplayArgs(ctypes.Structure):
+    _fields_ = [("variant", _i32), ("in_dtype", _i32), ("qk_l2norm", _i32), ("num_req", _i32),
+                ("draft_len", _i32), ("heads", _i32), ("dk", _i32), ("dv", _i32), ("pool_slots", _i32),
+                ("reserved0", _i32),
+                ("q", _vp), ("k", _vp), ("v", _vp), ("alpha", _vp), ("beta", _vp),
+                ("state_pool", _vp), ("slot_ids", _vp), ("accept", _vp), ("conv_w", _vp),
+                ("conv_pool", _vp), ("dev_status", _vp)]
+
+
 class CopyArgs(ctypes.Structure):
     _fields_ = [("n", _i32), ("pool_slots", _i32), ("heads", _i32), ("dk", _i32), ("dv", _i32),
                 ("in_dtype", _i32), ("state_pool", _vp), ("conv_pool", _vp), ("src_slots", _vp),
@@ -87,7 +98,8 @@ def library() -> ctypes.CDLL:
             path = _build.build()
             lib = ctypes.CDLL(path)
             for name, argt in (("glinattn_prefill", PrefillArgs), ("glinattn_decode", DecodeArgs),
-                               ("glinattn_spec_decode", SpecArgs), ("glinattn_state_copy", CopyArgs)):
+                               ("glinattn_spec_decode", SpecArgs), ("glinattn_replay", ReplayArgs),
+                               ("glinattn_state_copy", CopyArgs)):
                 f = getattr(lib, name)
                 f.argtypes = [ctypes.POINTER(argt), _vp]
                 f.restype = ctypes.c_int
@@ -250,7 +262,9 @@ def glinattn_spec_decode(q, k, v, alpha, beta, state_pool, src_slots, dst_slots,
                          dev_status=None, stream=None):
     """D draft steps per request.  q, k [N,D,H,dk], v [N,D,H,dv];
     alpha/beta [N,D,H]; src_slots [N], dst_slots [N,D] int32.  The state after
-    draft i is written to state_pool[dst_slots[n, i]].  Returns o [N,D,H,dv]."""
+    draft i is written to state_pool[dst_slots[n, i]]; dst_slots=None only
+    verifies (outputs, no state written: see glinattn_replay).  Returns
+    o [N,D,H,dv]."""
     N, D, H, dk = q.shape
     dv = v.shape[-1]
     dev = q.device
@@ -280,6 +294,42 @@ def glinattn_spec_decode(q, k, v, alpha, beta, state_pool, src_slots, dst_slots,
                  dev_status=_ptr(dev_status))
     _call("glinattn_spec_decode", a, _stream_handle(stream, dev))
     return o
+
+
+def glinattn_replay(k, v, alpha, beta, state_pool, slot_ids, accept, *, q=None, variant=GDN,
+                    conv_w=None, conv_pool=None, qk_l2norm=False, dev_status=None, stream=None):
+    """Apply the first accept[n] recorded draft steps to state_pool[slot_ids[n]]
+    (and its conv cache) in place.  k [N,D,H,dk], v [N,D,H,dv], alpha/beta
+    [N,D,H], q [N,D,H,dk] (its raw values enter the conv cache; defaults to k
+    when there is no conv); slot_ids, accept [N] int32."""
+    N, D, H, dk = k.shape
+    dv = v.shape[-1]
+    dev = k.device
+    act = k.dtype
+    P = state_pool.shape[0]
+    if q is None:
+        if conv_w is not None:
+            raise ValueError("q is needed with a conv: its raw values enter the conv cache")
+        q = k
+    _need(q, "q", act, (N, D, H, dk), dev)
+    _need(k, "k", act, (N, D, H, dk), dev)
+    _need(v, "v", act, (N, D, H, dv), dev)
+    _need(alpha, "alpha", torch.float32, (N, D, H), dev)
+    _need(beta, "beta", torch.float32, (N, D, H), dev)
+    _need(state_pool, "state_pool", torch.float32, (P, H, dk, dv), dev)
+    _need(slot_ids, "slot_ids", torch.int32, (N,), dev)
+    _need(accept, "accept", torch.int32, (N,), dev)
+    Cch = H * (2 * dk + dv)
+    if conv_w is not None:
+        _need(conv_w, "conv_w", torch.float32, (Cch, 4), dev)
+        _need(conv_pool, "conv_pool", act, (P, 3, Cch), dev)
+    a = ReplayArgs(variant=variant, in_dtype=_dtype_code(k), qk_l2norm=int(bool(qk_l2norm)), num_req=N,
+                   draft_len=D, heads=H, dk=dk, dv=dv, pool_slots=P, q=_ptr(q), k=_ptr(k), v=_ptr(v),
+                   alpha=_ptr(alpha), beta=_ptr(beta), state_pool=_ptr(state_pool), slot_ids=_ptr(slot_ids),
+                   accept=_ptr(accept), conv_w=_ptr(conv_w),
+                   conv_pool=_ptr(conv_pool) if conv_w is not None else None, dev_status=_ptr(dev_status))
+    _call("glinattn_replay", a, _stream_handle(stream, dev))
+    return state_pool
 
 
 def glinattn_state_copy(state_pool, src_slots, dst_slots, *, conv_pool=None, dev_status=None,

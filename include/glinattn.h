@@ -68,6 +68,7 @@ typedef enum { GLINATTN_F32 = 0, GLINATTN_BF16 = 1 } glinattn_dtype;
 #define GLINATTN_DEV_BAD_SLOT 0x1u    /* slot id outside [0, pool_slots): unit skipped */
 #define GLINATTN_DEV_BAD_GATE 0x2u    /* alpha outside (0, 1] or not finite: unit skipped */
 #define GLINATTN_DEV_WAIT_TIMEOUT 0x4u /* an on-chip barrier wait exceeded its bound */
+#define GLINATTN_DEV_BAD_COUNT 0x8u   /* accepted length outside [0, draft_len]: request skipped */
 
 /*
  * glinattn_prefill -- chunked prefill of one segment for B sequences.
@@ -207,9 +208,12 @@ glinattn_status glinattn_decode(const glinattn_decode_args *args, glinattn_strea
  *   state there is bit-identical to a decode steps of glinattn_decode.
  *   All destination slots of all requests must be distinct from each other
  *   and from every source slot (not checked on the device).
+ *   dst_slots == NULL verifies only: the outputs are written, no state and no
+ *   conv cache, and the pool keeps one state per request; glinattn_replay
+ *   then applies the accepted drafts (the replay-buffer alternative).
  *
  *   q, k [N, D, H, dk]   v [N, D, H, dv]   alpha, beta [N, D, H]
- *   src_slots [N]  dst_slots [N, D]  int32    o [N, D, H, dv]
+ *   src_slots [N]  dst_slots [N, D] or NULL  int32    o [N, D, H, dv]
  */
 typedef struct {
   int32_t variant, in_dtype, out_dtype, qk_l2norm;
@@ -226,6 +230,40 @@ typedef struct {
 } glinattn_spec_args;
 
 glinattn_status glinattn_spec_decode(const glinattn_spec_args *args, glinattn_stream_t stream);
+
+/*
+ * glinattn_replay -- roll the pool forward over the accepted drafts, the
+ *   alternative to keeping one state per draft position (section "Speculative
+ *   decoding and PD disaggregation": the updates of the draft steps are
+ *   recorded and replayed from a chosen position).  The recorded draft inputs
+ *   of a verify-only glinattn_spec_decode are the replay buffer: for request
+ *   n, the first accept[n] draft steps are applied to state_pool[slot_ids[n]]
+ *   and its conv cache, in place, with the arithmetic of glinattn_decode, so
+ *   the result equals accept[n] decode steps (and the per-draft state of
+ *   glinattn_spec_decode) bit for bit.  accept[n] == 0 leaves the slot as it
+ *   is; a length outside [0, D] sets GLINATTN_DEV_BAD_COUNT and skips the
+ *   request; slot ids outside [0, pool_slots) set GLINATTN_DEV_BAD_SLOT.
+ *   Only the applied steps' gates are checked.  No outputs are written.
+ *
+ *   q, k [N, D, H, dk]   v [N, D, H, dv]   alpha, beta [N, D, H]   (in_dtype / fp32)
+ *   slot_ids [N] int32 (distinct)   accept [N] int32
+ *   state_pool [P, H, dk, dv] fp32 and conv_pool [P, 3, Cch] (read/write)
+ */
+typedef struct {
+  int32_t variant, in_dtype, qk_l2norm;
+  int32_t num_req, draft_len, heads, dk, dv, pool_slots;
+  int32_t reserved0;
+  const void *q, *k, *v;
+  const float *alpha, *beta;
+  float *state_pool;
+  const int32_t *slot_ids;
+  const int32_t *accept;
+  const float *conv_w;
+  void *conv_pool;
+  uint32_t *dev_status;
+} glinattn_replay_args;
+
+glinattn_status glinattn_replay(const glinattn_replay_args *args, glinattn_stream_t stream);
 
 /*
  * glinattn_state_copy -- copy whole slots of a state pool (and of its conv

@@ -23,6 +23,7 @@ def test_library_exports_every_declared_symbol():
     lib = G.library()
     names = _declared_functions()
     assert {"glinattn_prefill", "glinattn_decode", "glinattn_spec_decode", "glinattn_state_copy",
+            "glinattn_replay",
             "glinattn_status_string", "glinattn_version"} <= set(names)
     for name in names:
         assert hasattr(lib, name), name
@@ -33,7 +34,8 @@ def test_library_exports_every_declared_symbol():
 
 
 STRUCTS = ((G.PrefillArgs, "glinattn_prefill_args"), (G.DecodeArgs, "glinattn_decode_args"),
-           (G.SpecArgs, "glinattn_spec_args"), (G.CopyArgs, "glinattn_copy_args"))
+           (G.SpecArgs, "glinattn_spec_args"), (G.ReplayArgs, "glinattn_replay_args"),
+           (G.CopyArgs, "glinattn_copy_args"))
 
 
 def test_struct_layout_matches_header(tmp_path):
@@ -152,7 +154,7 @@ def test_decode_rejects(kw, code):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(draft_len=0), INVALID),
-    (dict(dst_slots=None), INVALID),
+    (dict(o=None), INVALID),             # dst_slots may be NULL (verify only), o may not
     (dict(src_slots=None), INVALID),
     (dict(variant=G.GDN, beta=None), INVALID),
 ])
@@ -194,3 +196,32 @@ def test_state_copy_zero_pairs_is_a_noop():
     lib = G.library()
     assert lib.glinattn_state_copy(None, None) == INVALID
     assert lib.glinattn_state_copy(ctypes.byref(_copy(n=0, state_pool=None)), None) == 0
+
+
+def _replay(**kw):
+    base = dict(variant=G.GDN, in_dtype=G.BF16, qk_l2norm=1, num_req=4, draft_len=3, heads=2, dk=64, dv=64,
+                pool_slots=8, q=A, k=A * 2, v=A * 3, alpha=A * 4, beta=A * 5, state_pool=A * 6,
+                slot_ids=A * 7, accept=A * 8)
+    base.update(kw)
+    return G.ReplayArgs(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(accept=None), INVALID),
+    (dict(slot_ids=None), INVALID),
+    (dict(state_pool=None), INVALID),
+    (dict(draft_len=0), INVALID),
+    (dict(pool_slots=0), INVALID),
+    (dict(variant=G.GDN, beta=None), INVALID),
+    (dict(conv_w=A * 9, conv_pool=None), INVALID),
+    (dict(dk=48, dv=48), UNSUPPORTED),
+    (dict(k=A * 2 + 2), INVALID),
+])
+def test_replay_rejects(kw, code):
+    assert G.library().glinattn_replay(ctypes.byref(_replay(**kw)), None) == code
+
+
+def test_replay_zero_requests_is_a_noop():
+    lib = G.library()
+    assert lib.glinattn_replay(None, None) == INVALID
+    assert lib.glinattn_replay(ctypes.byref(_replay(num_req=0, k=None)), None) == 0
