@@ -276,6 +276,20 @@ def run_ours(args):
     gdn_ms, gdn_per = timed_steps(step_gdn, max(2, min(args.steps, 5)), 1, dist, dev)
     gdn_bytes, gdn_flops = gdn_bytes_flops(**g)
 
+    # the same prefill keeping a prefix-cache checkpoint (state + conv cache) every 1024 tokens
+    every = 1024
+    nblk = g["T"] // every
+    Sb = torch.empty(g["B"], nblk, g["H"], g["d"], g["d"], dtype=torch.float32, device=dev)
+    cb = torch.empty(g["B"], nblk, 3, 3 * g["H"] * g["d"], dtype=torch.bfloat16, device=dev)
+
+    def step_gdn_ck():
+        glinattn_prefill(gx["q"], gx["k"], gx["v"], gx["alpha"], gx["beta"], gx["S0"], variant=GDN,
+                         conv_w=gx["conv_w"], qk_l2norm=True, o=og, S_T=Sg, state_every=every, S_blocks=Sb,
+                         conv_blocks=cb)
+
+    ck_ms, _ = timed_steps(step_gdn_ck, max(2, min(args.steps, 5)), 1, dist, dev)
+    ck_bytes = Sb.numel() * 4 + cb.numel() * 2
+
     # ---- long context: 3-segment prefill, then 64 x 4 speculative decode -------------
     lc = long_context_run(args, dist, dev, rank)
 
@@ -335,7 +349,10 @@ def run_ours(args):
                                      "frac": gdn_bytes / (statistics.mean(gdn_per) / 1e3) / 1e9 / hbm,
                                      "traffic": gdn_traffic, "algorithmic_bytes": gdn_bytes,
                                      "kernels": "gdn_prep_kernel + gdn_scan_kernel"},
-                        "tensor_frac": gdn_flops / (statistics.mean(gdn_per) / 1e3) / 1e12 / tc},
+                        "tensor_frac": gdn_flops / (statistics.mean(gdn_per) / 1e3) / 1e12 / tc,
+                        "with_checkpoints": {"state_every": every, "ms_per_step": ck_ms,
+                                             "checkpoint_bytes": ck_bytes,
+                                             "overhead_frac": ck_ms / gdn_ms - 1.0}},
         "long_context": lc,
         "cpu_baseline": cpu,
     }
@@ -351,7 +368,8 @@ def long_context_run(args, dist, dev, rank):
     per draft position."""
     import torch
 
-    from gated_deltanet_02_gb300 import GDN, glinattn_prefill, glinattn_spec_decode, inputs
+    from gated_deltanet_02_gb300 import (GDN, glinattn_prefill, glinattn_replay, glinattn_spec_decode,
+                                         glinattn_state_copy, inputs)
     pk, _ = peaks()
     B, H, T, d = 1, 32, 32768, 128
     ex = inputs.gdn_prefill(B, H, T, d, seed=rank, device=dev, s0_std=0.0)
@@ -393,6 +411,30 @@ def long_context_run(args, dist, dev, rank):
     spec_ms, spec_per = timed_steps(step_spec, max(10, args.steps), 3, dist, dev)
     spec_bytes = N * H * (1 + D) * d * d * 4
     k_ms = statistics.mean(spec_per)
+
+    # the replay-buffer alternative: verify without per-draft states, then apply
+    # each request's accepted drafts (a ~ U{0..4}) to its own slot in place
+    accept = dr["accept"].to(torch.int32)
+
+    def step_replay():
+        glinattn_spec_decode(dr["q"], dr["k"], dr["v"], dr["alpha"], dr["beta"], pool, src, None,
+                             variant=GDN, conv_w=ex["conv_w"], conv_pool=cpool, qk_l2norm=True, o=od)
+        glinattn_replay(dr["k"], dr["v"], dr["alpha"], dr["beta"], pool, src, accept, q=dr["q"], variant=GDN,
+                        conv_w=ex["conv_w"], conv_pool=cpool, qk_l2norm=True)
+
+    rep_ms, rep_per = timed_steps(step_replay, max(10, args.steps), 3, dist, dev)
+    n_acc = int((accept > 0).sum().item())
+    rep_bytes = N * H * d * d * 4 + 2 * n_acc * H * d * d * 4
+
+    # copy on write: 64 request slots copied whole (state + conv cache) into 64 others
+    csrc = torch.arange(N, dtype=torch.int32, device=dev)
+    cdst = N + csrc
+
+    def step_copy():
+        glinattn_state_copy(pool, csrc, cdst, conv_pool=cpool)
+
+    copy_ms, copy_per = timed_steps(step_copy, max(10, args.steps), 3, dist, dev)
+    copy_bytes = 2 * N * (H * d * d * 4 + 3 * 3 * H * d * 2)
     return {"config": "Gated DeltaNet, B=1 H=32 T=32768 in segments 6553/11468/14747 (conv + L2 norm), "
                       "then 64 requests x 4 draft tokens, one fp32 state per draft position",
             "prefill_tokens_per_s": T / (pre_ms / 1e3), "prefill_ms": pre_ms,
@@ -400,7 +442,23 @@ def long_context_run(args, dist, dev, rank):
             "spec_roofline": {"bound": "hbm", "achieved": spec_bytes / (k_ms / 1e3) / 1e9,
                               "peak": pk["hbm_gbs"], "unit": "GB/s",
                               "frac": spec_bytes / (k_ms / 1e3) / 1e9 / pk["hbm_gbs"],
-                              "algorithmic_bytes": spec_bytes}}
+                              "algorithmic_bytes": spec_bytes},
+            "replay_rollback": {"config": "verify-only speculative decode + replay of the accepted drafts "
+                                          f"({n_acc} of {N} requests accept at least one), in place",
+                                "ms_per_round": rep_ms, "pool_slots_needed": N,
+                                "pool_slots_needed_per_draft_states": N * (1 + D),
+                                "roofline": {"bound": "hbm",
+                                             "achieved": rep_bytes / (statistics.mean(rep_per) / 1e3) / 1e9,
+                                             "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                             "frac": rep_bytes / (statistics.mean(rep_per) / 1e3) / 1e9
+                                             / pk["hbm_gbs"], "algorithmic_bytes": rep_bytes}},
+            "slot_copy": {"config": "64 whole slots (32 heads x 128 x 128 fp32 + bf16 conv cache) copied",
+                          "ms": copy_ms,
+                          "roofline": {"bound": "hbm",
+                                       "achieved": copy_bytes / (statistics.mean(copy_per) / 1e3) / 1e9,
+                                       "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                       "frac": copy_bytes / (statistics.mean(copy_per) / 1e3) / 1e9
+                                       / pk["hbm_gbs"], "algorithmic_bytes": copy_bytes}}}
 
 
 # ----------------------------------------------------------------------------
