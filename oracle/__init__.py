@@ -15,6 +15,7 @@ one state per draft position).  The token-by-token recurrence itself lives in
 gcc on first use and composes the layer from it:
 
 * ``recurrence``   -- the C recurrence, optionally emitting every state;
+* ``expand_groups``-- grouped q / k heads (the SSD form's shared B, C) to one per head;
 * ``frontend``     -- conv (width 4) -> L2 norm of q, k -> bf16 rounding;
 * ``layer_prefill``-- front end + recurrence over a whole segment;
 * ``decode``       -- by definition a one-token prefill from a pool slot;
@@ -95,14 +96,32 @@ def _check(rc: int, what: str):
 # The recurrence
 # --------------------------------------------------------------------------
 
+def expand_groups(x, heads):
+    """q or k [..., Hq, d] -> [..., H, d] when groups of H / Hq consecutive heads
+    share one q / k head: head h reads head h // (H / Hq).  The linear-attention
+    page lists the SSD form of Mamba2 among the gated linear attention
+    recurrences (section "Two ways to write the same computation"); its B and C
+    (k and q here) are shared by the heads of a group, the convention of the
+    Mamba2 layer on the field-notes page (section "Mamba and hybrid SSMs, the
+    real packages")."""
+    x = _f64(x)
+    hq = x.shape[-2]
+    if hq <= 0 or heads % hq:
+        raise ValueError("q / k heads must divide the number of heads")
+    return np.repeat(x, heads // hq, axis=-2)
+
+
 def recurrence(variant, q, k, v, alpha, beta=None, S0=None, return_states=False, nthreads=1):
-    """Token-by-token recurrence over q, k [B,T,H,dk], v [B,T,H,dv],
-    alpha/beta [B,T,H]; S0 [B,H,dk,dv] or None (zeros).
+    """Token-by-token recurrence over q, k [B,T,H,dk] (or [B,T,Hq,dk] shared
+    by groups of heads, see ``expand_groups``), v [B,T,H,dv], alpha/beta
+    [B,T,H]; S0 [B,H,dk,dv] or None (zeros).
 
     Returns (o [B,T,H,dv], S_T [B,H,dk,dv]) and, with ``return_states``, the
     state after every token [B,T,H,dk,dv].
     """
     q, k, v, alpha = _f64(q), _f64(k), _f64(v), _f64(alpha)
+    if q.ndim == 4 and v.ndim == 4 and q.shape[2] != v.shape[2]:
+        q, k = expand_groups(q, v.shape[2]), expand_groups(k, v.shape[2])
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     if k.shape != q.shape or v.shape[:3] != (B, T, H) or alpha.shape != (B, T, H):

@@ -325,3 +325,35 @@ def test_l2norm_and_bf16_rounding():
     f32 = rng.standard_normal(4000).astype(np.float32) * 100
     expect = torch.from_numpy(f32).to(torch.bfloat16).double().numpy()
     np.testing.assert_array_equal(oracle.round_bf16(f32.astype(np.float64)), expect)
+
+
+# ---------------------------------------------------------------------------
+# grouped q / k heads (the SSD form: state 128, head dim 64, shared B and C)
+# ---------------------------------------------------------------------------
+
+def test_grouped_heads_match_bruteforce_per_head():
+    """Four heads, two q / k heads: head h is the brute-force gated linear
+    attention on q / k head h // 2, with a rectangular (d_k = 8, d_v = 5) state."""
+    rng = np.random.default_rng(9)
+    q, k, _, _, _, _ = _rand(rng, 1, 15, 2, 8, 5)
+    _, _, v, alpha, _, S0 = _rand(rng, 1, 15, 4, 8, 5)
+    o, S = oracle.recurrence(GLA, q, k, v, alpha, S0=S0)
+    for h in range(4):
+        ob, Sb = _gla_bruteforce(q[0, :, h // 2], k[0, :, h // 2], v[0, :, h], alpha[0, :, h], S0[0, h])
+        np.testing.assert_allclose(o[0, :, h], ob, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(S[0, h], Sb, rtol=1e-12, atol=1e-12)
+
+
+def test_heads_of_one_group_agree_and_groups_differ():
+    """With the same v and alpha for every head, the heads that share a q / k
+    head give identical outputs and heads of different groups do not: this
+    fixes which heads form a group (consecutive ones)."""
+    rng = np.random.default_rng(10)
+    q, k, v1, a1, _, _ = _rand(rng, 1, 12, 3, 6, 4, s0=False)
+    v = np.repeat(v1[:, :, :1], 6, axis=2)
+    alpha = np.repeat(a1[:, :, :1], 6, axis=2)
+    o, _ = oracle.recurrence(GLA, q, k, v, alpha)
+    for g in range(3):
+        np.testing.assert_array_equal(o[0, :, 2 * g], o[0, :, 2 * g + 1])
+    assert not np.allclose(o[0, :, 1], o[0, :, 2])
+    assert not np.allclose(o[0, :, 3], o[0, :, 4])
