@@ -15,6 +15,7 @@ namespace glinattn {
 struct RecurParams {
   int variant, in_bf16, out_bf16, qk_l2norm;
   int N, steps, H, pool_slots;  // pool_slots = 0 when states are not pooled
+  int Hq;                       // q / k heads (groups of H / Hq heads share them)
   int Cch;                      // conv channels per request, H * 3d
   const void *q, *k, *v;
   const float *alpha, *beta;
@@ -41,7 +42,7 @@ struct RecurParams {
   int state_every, nblocks;
 };
 
-glinattn_status launch_recurrent(const RecurParams &p, int d, cudaStream_t stream);
+glinattn_status launch_recurrent(const RecurParams &p, int dk, int dv, cudaStream_t stream);
 // conv caches at the emitted block boundaries of a prefill (checkpoint.cu)
 glinattn_status launch_conv_blocks(const glinattn_prefill_args &a, cudaStream_t stream);
 

@@ -997,7 +997,7 @@ Workspace carve(void *base, int B, int H, int Tp) {
 
 bool gdn_tc_supports(const glinattn_prefill_args &a) {
   return a.variant == GLINATTN_GDN && a.in_dtype == GLINATTN_BF16 && a.dk == kD && a.dv == kD &&
-         a.seqlen > 0;
+         (a.qk_heads == 0 || a.qk_heads == a.heads) && a.seqlen > 0;
 }
 
 size_t gdn_tc_workspace_bytes(const glinattn_prefill_args &a) {

@@ -28,7 +28,19 @@ glinattn_status check_common(int variant, int in_dtype, int out_dtype, int dk, i
       (out_dtype != GLINATTN_F32 && out_dtype != GLINATTN_BF16))
     return GLINATTN_ERR_INVALID_ARG;
   if (heads <= 0 || dk <= 0 || dv <= 0) return GLINATTN_ERR_INVALID_ARG;
-  if (dk != dv || !supported_head(dk)) return GLINATTN_ERR_UNSUPPORTED;
+  // square heads, or the 128 x 64 state of the SSD form (state 128, head dim 64)
+  const bool shape_ok = (dk == dv && supported_head(dk)) || (dk == 128 && dv == 64);
+  if (!shape_ok) return GLINATTN_ERR_UNSUPPORTED;
+  return GLINATTN_OK;
+}
+
+// q / k heads: 0 means one per head; otherwise a divisor of heads (groups of
+// heads share q and k).  Grouped heads take no convolution.
+glinattn_status check_qk_heads(int qk_heads, int heads, bool conv, int *out) {
+  const int hq = qk_heads == 0 ? heads : qk_heads;
+  if (hq < 0 || hq > heads || heads % hq != 0) return GLINATTN_ERR_INVALID_ARG;
+  if (hq != heads && conv) return GLINATTN_ERR_UNSUPPORTED;
+  *out = hq;
   return GLINATTN_OK;
 }
 
@@ -68,11 +80,14 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
   glinattn_status st = check_common(a->variant, a->in_dtype, a->out_dtype, a->dk, a->dv, a->heads);
   if (st != GLINATTN_OK) return st;
   if (a->batch < 0 || a->seqlen < 0) return GLINATTN_ERR_INVALID_ARG;
-  const int B = a->batch, T = a->seqlen, H = a->heads, d = a->dk;
+  const int B = a->batch, T = a->seqlen, H = a->heads, dk = a->dk, dv = a->dv;
+  int Hq = H;
+  st = check_qk_heads(a->qk_heads, H, a->conv_w != nullptr, &Hq);
+  if (st != GLINATTN_OK) return st;
   if ((long long)B * H > (1ll << 30) || (long long)T > (1ll << 30)) return GLINATTN_ERR_INVALID_ARG;
   if (B == 0) return GLINATTN_OK;
   const size_t act = a->in_dtype == GLINATTN_BF16 ? 2 : 4;
-  const size_t state_bytes = (size_t)B * H * d * d * sizeof(float);
+  const size_t state_bytes = (size_t)B * H * dk * dv * sizeof(float);
   if (!a->S_T) return GLINATTN_ERR_INVALID_ARG;
   if (a->state_every < 0) return GLINATTN_ERR_INVALID_ARG;
   const bool emit_blocks = a->state_every > 0 && T / a->state_every > 0;
@@ -85,7 +100,7 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
                    a->conv_in, a->conv_out))
     return GLINATTN_ERR_INVALID_ARG;
   if (partial_overlap(a->S0, state_bytes, a->S_T, state_bytes)) return GLINATTN_ERR_INVALID_ARG;
-  const int Cch = H * 3 * d;
+  const int Cch = H * (2 * dk + dv);
   if (a->conv_w) {
     const size_t cb = (size_t)B * 3 * Cch * act;
     if (partial_overlap(a->conv_in, cb, a->conv_out, cb)) return GLINATTN_ERR_INVALID_ARG;
@@ -120,6 +135,7 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
   p.N = B;
   p.steps = T;
   p.H = H;
+  p.Hq = Hq;
   p.pool_slots = 0;
   p.Cch = Cch;
   p.q = a->q;
@@ -139,7 +155,7 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
     p.state_every = a->state_every;
     p.nblocks = T / a->state_every;
   }
-  return glinattn::launch_recurrent(p, d, (cudaStream_t)stream);
+  return glinattn::launch_recurrent(p, dk, dv, (cudaStream_t)stream);
 }
 
 size_t glinattn_prefill_workspace_size(const glinattn_prefill_args *a) {
@@ -152,6 +168,9 @@ size_t glinattn_prefill_workspace_size(const glinattn_prefill_args *a) {
 glinattn_status glinattn_decode(const glinattn_decode_args *a, glinattn_stream_t stream) {
   if (!a) return GLINATTN_ERR_INVALID_ARG;
   glinattn_status st = check_common(a->variant, a->in_dtype, a->out_dtype, a->dk, a->dv, a->heads);
+  if (st != GLINATTN_OK) return st;
+  int Hq = a->heads;
+  st = check_qk_heads(a->qk_heads, a->heads, a->conv_w != nullptr, &Hq);
   if (st != GLINATTN_OK) return st;
   if (a->num_req < 0 || a->pool_slots <= 0) return GLINATTN_ERR_INVALID_ARG;
   if ((long long)a->num_req * a->heads > (1ll << 30)) return GLINATTN_ERR_INVALID_ARG;
@@ -170,8 +189,9 @@ glinattn_status glinattn_decode(const glinattn_decode_args *a, glinattn_stream_t
   p.N = a->num_req;
   p.steps = 1;
   p.H = a->heads;
+  p.Hq = Hq;
   p.pool_slots = a->pool_slots;
-  p.Cch = a->heads * 3 * a->dk;
+  p.Cch = a->heads * (2 * a->dk + a->dv);
   p.q = a->q;
   p.k = a->k;
   p.v = a->v;
@@ -187,12 +207,15 @@ glinattn_status glinattn_decode(const glinattn_decode_args *a, glinattn_stream_t
   p.conv_src = a->conv_w ? a->conv_pool : nullptr;
   p.conv_dst = a->conv_w ? a->conv_pool : nullptr;
   p.dev_status = a->dev_status;
-  return glinattn::launch_recurrent(p, a->dk, (cudaStream_t)stream);
+  return glinattn::launch_recurrent(p, a->dk, a->dv, (cudaStream_t)stream);
 }
 
 glinattn_status glinattn_spec_decode(const glinattn_spec_args *a, glinattn_stream_t stream) {
   if (!a) return GLINATTN_ERR_INVALID_ARG;
   glinattn_status st = check_common(a->variant, a->in_dtype, a->out_dtype, a->dk, a->dv, a->heads);
+  if (st != GLINATTN_OK) return st;
+  int Hq = a->heads;
+  st = check_qk_heads(a->qk_heads, a->heads, a->conv_w != nullptr, &Hq);
   if (st != GLINATTN_OK) return st;
   if (a->num_req < 0 || a->draft_len <= 0 || a->pool_slots <= 0) return GLINATTN_ERR_INVALID_ARG;
   if ((long long)a->num_req * a->heads > (1ll << 30) || a->draft_len > (1 << 20))
@@ -212,8 +235,9 @@ glinattn_status glinattn_spec_decode(const glinattn_spec_args *a, glinattn_strea
   p.N = a->num_req;
   p.steps = a->draft_len;
   p.H = a->heads;
+  p.Hq = Hq;
   p.pool_slots = a->pool_slots;
-  p.Cch = a->heads * 3 * a->dk;
+  p.Cch = a->heads * (2 * a->dk + a->dv);
   p.q = a->q;
   p.k = a->k;
   p.v = a->v;
@@ -230,12 +254,15 @@ glinattn_status glinattn_spec_decode(const glinattn_spec_args *a, glinattn_strea
   p.conv_src = a->conv_w ? a->conv_pool : nullptr;
   p.conv_dst = a->conv_w && !verify_only ? a->conv_pool : nullptr;
   p.dev_status = a->dev_status;
-  return glinattn::launch_recurrent(p, a->dk, (cudaStream_t)stream);
+  return glinattn::launch_recurrent(p, a->dk, a->dv, (cudaStream_t)stream);
 }
 
 glinattn_status glinattn_replay(const glinattn_replay_args *a, glinattn_stream_t stream) {
   if (!a) return GLINATTN_ERR_INVALID_ARG;
   glinattn_status st = check_common(a->variant, a->in_dtype, GLINATTN_F32, a->dk, a->dv, a->heads);
+  if (st != GLINATTN_OK) return st;
+  int Hq = a->heads;
+  st = check_qk_heads(a->qk_heads, a->heads, a->conv_w != nullptr, &Hq);
   if (st != GLINATTN_OK) return st;
   if (a->num_req < 0 || a->draft_len <= 0 || a->pool_slots <= 0) return GLINATTN_ERR_INVALID_ARG;
   if ((long long)a->num_req * a->heads > (1ll << 30) || a->draft_len > (1 << 20))
@@ -254,8 +281,9 @@ glinattn_status glinattn_replay(const glinattn_replay_args *a, glinattn_stream_t
   p.N = a->num_req;
   p.steps = a->draft_len;
   p.H = a->heads;
+  p.Hq = Hq;
   p.pool_slots = a->pool_slots;
-  p.Cch = a->heads * 3 * a->dk;
+  p.Cch = a->heads * (2 * a->dk + a->dv);
   p.q = a->q;
   p.k = a->k;
   p.v = a->v;
@@ -272,7 +300,7 @@ glinattn_status glinattn_replay(const glinattn_replay_args *a, glinattn_stream_t
   p.conv_src = a->conv_w ? a->conv_pool : nullptr;
   p.conv_dst = a->conv_w ? a->conv_pool : nullptr;
   p.dev_status = a->dev_status;
-  return glinattn::launch_recurrent(p, a->dk, (cudaStream_t)stream);
+  return glinattn::launch_recurrent(p, a->dk, a->dv, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -14,7 +14,9 @@
 // is applied to V's rows here instead of K's, which is the same product).
 //
 // Kernel design (sm_103a):
-//   * one CTA per (batch, head, 64-wide slice of d_v); the state slice
+//   * one CTA per (batch, head, 64-wide slice of d_v: two slices at d_v = 128,
+//     one in the SSD form's d_v = 64); groups of heads may share q and k
+//     (the q / k tiles come from head h / (H / Hq)); the state slice
 //     S[128 x 64] is fp32 and lives in the registers of the epilogue warps
 //     for the whole sequence, one d_k row per thread;
 //   * warp 0 streams Q, K (64 x 128) and V (64 x 64) chunk tiles with TMA
@@ -79,6 +81,8 @@ constexpr uint32_t kColQK = 0, kColO1 = 128, kColO2 = 256, kColDS = 384;
 
 struct GlaParams {
   int B, T, H, nchunks, out_bf16;
+  int rep;   // heads per q / k head
+  int DV;    // value head size: 128 (two CTAs per head) or 64 (one)
   int state_every, nblocks;  // states emitted after every state_every tokens (a multiple of 64)
   float *S_blocks;
   const float *alpha;
@@ -118,9 +122,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort = &bars->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int vblk = blockIdx.x & 1;
-  const int bh = blockIdx.x >> 1;
+  const int nvb = p.DV / kBV;
+  const int vblk = blockIdx.x % nvb;
+  const int bh = blockIdx.x / nvb;
   const int b = bh / p.H, h = bh - b * p.H;
+  const int hq = h / p.rep;  // the q / k head of head h
   const int T = p.T, nchunks = p.nchunks;
 
   // ---- the unit is skipped when a gate is outside (0, 1] ---------------------
@@ -169,10 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto prefetch = [&](int c) {  // chunk c's tiles into L2, ahead of the ring
       if (c >= nchunks) return;
       const int t0 = c * kC;
-      tma_prefetch_l2_4d(&tq, 0, h, t0, b);
-      tma_prefetch_l2_4d(&tq, 64, h, t0, b);
-      tma_prefetch_l2_4d(&tk, 0, h, t0, b);
-      tma_prefetch_l2_4d(&tk, 64, h, t0, b);
+      tma_prefetch_l2_4d(&tq, 0, hq, t0, b);
+      tma_prefetch_l2_4d(&tq, 64, hq, t0, b);
+      tma_prefetch_l2_4d(&tk, 0, hq, t0, b);
+      tma_prefetch_l2_4d(&tk, 64, hq, t0, b);
       tma_prefetch_l2_4d(&tv, vblk * kBV, h, t0, b);
     };
     if (lane == 0) {
@@ -198,10 +204,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *st = smem + kOffStage + s * kStageBytes;
         mbar_arrive_expect_tx(&bars->full[s], kStageBytes);
         const int t0 = c * kC;
-        tma_load_4d(st, &tq, &bars->full[s], 0, h, t0, b);
-        tma_load_4d(st + kTileQ / 2, &tq, &bars->full[s], 64, h, t0, b);
-        tma_load_4d(st + kTileQ, &tk, &bars->full[s], 0, h, t0, b);
-        tma_load_4d(st + kTileQ + kTileK / 2, &tk, &bars->full[s], 64, h, t0, b);
+        tma_load_4d(st, &tq, &bars->full[s], 0, hq, t0, b);
+        tma_load_4d(st + kTileQ / 2, &tq, &bars->full[s], 64, hq, t0, b);
+        tma_load_4d(st + kTileQ, &tk, &bars->full[s], 0, hq, t0, b);
+        tma_load_4d(st + kTileQ + kTileK / 2, &tk, &bars->full[s], 64, hq, t0, b);
         tma_load_4d(st + kTileQ + kTileK, &tv, &bars->full[s], vblk * kBV, h, t0, b);
       }
       const float l0 = log2f(a0n), l1 = log2f(a1n);
@@ -385,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the state slice S[srow, vblk*64 .. +64) in fp32 registers
     float S[kBV];
     {
-      const float *src = p.S0 ? p.S0 + (((size_t)b * p.H + h) * kDK + srow) * kDK + vblk * kBV : nullptr;
+      const float *src = p.S0 ? p.S0 + (((size_t)b * p.H + h) * kDK + srow) * p.DV + vblk * kBV : nullptr;
 #pragma unroll
       for (int j = 0; j < kBV; j += 4) {
         const float4 v4 = src ? *reinterpret_cast<const float4 *>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -431,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.state_every && ((c + 1) * kC) % p.state_every == 0 && (c + 1) * kC <= T) {
         // the state after this chunk closes a block: this thread's row slice goes out
         float *dst = p.S_blocks +
-                     ((((size_t)b * p.nblocks + (c + 1) * kC / p.state_every - 1) * p.H + h) * kDK + srow) * kDK +
+                     ((((size_t)b * p.nblocks + (c + 1) * kC / p.state_every - 1) * p.H + h) * kDK + srow) * p.DV +
                      vblk * kBV;
 #pragma unroll
         for (int j = 0; j < kBV; j += 4)
@@ -445,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float gi = eg_tok;
         const int t = t0 + tok;
         const bool store = has_tok && t < T;
-        const size_t obase = (((size_t)b * T + t) * p.H + h) * kDK + vblk * kBV;
+        const size_t obase = (((size_t)b * T + t) * p.H + h) * p.DV + vblk * kBV;
 #pragma unroll
         for (int qt = 0; qt < 4; ++qt) {
           float o1[16], o1l[16], o2[16];
@@ -479,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&bars->o_free[tb]);
     }
     if (ok) {
-      float *dst = p.S_T + (((size_t)b * p.H + h) * kDK + srow) * kDK + vblk * kBV;
+      float *dst = p.S_T + (((size_t)b * p.H + h) * kDK + srow) * p.DV + vblk * kBV;
 #pragma unroll
       for (int j = 0; j < kBV; j += 4)
         *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
@@ -604,17 +610,20 @@ bool encode_rows_map(CUtensorMap *m, const void *base, CUtensorMapDataType type,
 bool prefill_tc_available() { return encode_fn() != nullptr; }
 
 bool prefill_tc_supports(const glinattn_prefill_args &a) {
-  return a.variant == GLINATTN_GLA && a.in_dtype == GLINATTN_BF16 && a.dk == kDK && a.dv == kDK &&
-         a.conv_w == nullptr && !a.qk_l2norm && a.seqlen > 0;
+  return a.variant == GLINATTN_GLA && a.in_dtype == GLINATTN_BF16 && a.dk == kDK &&
+         (a.dv == kDK || a.dv == kBV) && a.conv_w == nullptr && !a.qk_l2norm && a.seqlen > 0;
 }
 
 glinattn_status launch_prefill_tc(const glinattn_prefill_args &a, cudaStream_t stream) {
   CUtensorMap tq, tk, tv;
-  if (!make_act_map(&tq, a.q, a.batch, a.seqlen, a.heads, kDK) ||
-      !make_act_map(&tk, a.k, a.batch, a.seqlen, a.heads, kDK) ||
-      !make_act_map(&tv, a.v, a.batch, a.seqlen, a.heads, kDK))
+  const int Hq = a.qk_heads > 0 ? a.qk_heads : a.heads;
+  if (!make_act_map(&tq, a.q, a.batch, a.seqlen, Hq, kDK) ||
+      !make_act_map(&tk, a.k, a.batch, a.seqlen, Hq, kDK) ||
+      !make_act_map(&tv, a.v, a.batch, a.seqlen, a.heads, a.dv))
     return GLINATTN_ERR_CUDA;
   GlaParams p;
+  p.rep = a.heads / Hq;
+  p.DV = a.dv;
   p.B = a.batch;
   p.T = a.seqlen;
   p.H = a.heads;
@@ -631,7 +640,7 @@ glinattn_status launch_prefill_tc(const glinattn_prefill_args &a, cudaStream_t s
   if (cudaFuncSetAttribute(gla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kSmemBytes) != cudaSuccess)
     return GLINATTN_ERR_CUDA;
-  const unsigned grid = (unsigned)a.batch * (unsigned)a.heads * (kDK / kBV);
+  const unsigned grid = (unsigned)a.batch * (unsigned)a.heads * (unsigned)(a.dv / kBV);
   gla_prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? GLINATTN_OK : GLINATTN_ERR_CUDA;
 }

@@ -37,16 +37,16 @@ namespace {
 
 using namespace sm100;
 
-template <int D>
+template <int DK, int DV>
 struct Shape {
-  static constexpr int NSPLIT = D == 128 ? 2 : 1;  // column slices per state
-  static constexpr int DC = D / NSPLIT;             // columns per CTA
-  static constexpr int NT = D == 128 ? 128 : ((D * D / 4 < 256) ? D * D / 4 : 256);
+  static constexpr int NSPLIT = DV == 128 ? 2 : 1;  // column slices per state
+  static constexpr int DC = DV / NSPLIT;             // columns per CTA
+  static constexpr int NT = DK == 128 ? 128 : ((DK * DV / 4 < 256) ? DK * DV / 4 : 256);
   static constexpr int COLG = DC / 4;               // 16-byte column groups
   static constexpr int ROWG = NT / COLG;            // row groups
-  static constexpr int RPT = D / ROWG;              // rows per thread
-  static constexpr int NCH = 2 * D + DC;            // front-end channels: q, k, own v slice
-  static_assert(RPT >= 1 && ROWG * RPT == D, "shape");
+  static constexpr int RPT = DK / ROWG;             // rows per thread
+  static constexpr int NCH = 2 * DK + DC;           // front-end channels: q, k, own v slice
+  static_assert(RPT >= 1 && ROWG * RPT == DK, "shape");
 };
 
 __device__ __forceinline__ float load_act(const void *base, size_t idx, int bf16) {
@@ -71,23 +71,24 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-template <int D>
-__global__ void __launch_bounds__(Shape<D>::NT)
+template <int DK, int DV>
+__global__ void __launch_bounds__(Shape<DK, DV>::NT)
     recurrent_kernel(const __grid_constant__ CUtensorMap tstate, const RecurParams p) {
-  using Sh = Shape<D>;
+  using Sh = Shape<DK, DV>;
   constexpr int NW = (Sh::NT + 31) / 32;
   constexpr int NCH = Sh::NCH;
   constexpr int MAXC = (NCH + Sh::NT - 1) / Sh::NT;  // front-end channels per thread
-  constexpr uint32_t kSliceBytes = D * Sh::DC * 4;
+  constexpr uint32_t kSliceBytes = DK * Sh::DC * 4;
   const int half = blockIdx.x % Sh::NSPLIT;
   const int unit = blockIdx.x / Sh::NSPLIT;
   const int n = unit / p.H, h = unit - n * p.H;
   const int tid = threadIdx.x;
   const int cg = tid % Sh::COLG, rg = tid / Sh::COLG;
   const int col0 = half * Sh::DC;  // first state column of this CTA
-  const size_t DD = (size_t)D * D;
+  const size_t DD = (size_t)DK * DV;
+  const int hq = h / (p.H / p.Hq);  // the q / k head (group) of head h
 
-  extern __shared__ __align__(128) float4 s_state4[];  // D rows x DC columns, row-major
+  extern __shared__ __align__(128) float4 s_state4[];  // DK rows x DC columns, row-major
   __shared__ float s_act[NCH];                          // q | k | own v slice after the front end
   __shared__ float s_red[Sh::ROWG][2][Sh::DC];
   __shared__ float s_wsum[2][NW];
@@ -95,19 +96,20 @@ __global__ void __launch_bounds__(Shape<D>::NT)
   __shared__ int s_bad;
   __shared__ __align__(8) uint64_t s_bar;
 
-  // global channel of local front-end channel c: q (0..D-1), k (D..2D-1), own v slice
+  // global channel of local front-end channel c: q (0..DK-1), k (DK..2DK-1), own v slice
   auto chan = [&](int c) {
-    if (c < 2 * D) return (c / D) * p.H * D + h * D + (c % D);
-    return 2 * p.H * D + h * D + col0 + (c - 2 * D);
+    if (c < 2 * DK) return (c / DK) * p.H * DK + h * DK + (c % DK);
+    return 2 * p.H * DK + h * DV + col0 + (c - 2 * DK);
   };
-  // input element of local channel c for token row `row` (index of (n, t, h))
+  // input element of local channel c for token row `row` (index of (n, t, h));
+  // q and k rows are indexed by (n, t, hq)
   auto act_at = [&](int c, size_t row) {
-    const void *src = c < D ? p.q : (c < 2 * D ? p.k : p.v);
-    const int i = c < 2 * D ? (c % D) : col0 + (c - 2 * D);
-    return load_act(src, row * D + i, p.in_bf16);
+    if (c >= 2 * DK) return load_act(p.v, row * DV + col0 + (c - 2 * DK), p.in_bf16);
+    const size_t rq = (row / p.H) * p.Hq + hq;
+    return load_act(c < DK ? p.q : p.k, rq * DK + (c % DK), p.in_bf16);
   };
   // conv-cache channels written by this CTA: q and k by slice 0, each v slice by its owner
-  auto writes_chan = [&](int c) { return c >= 2 * D || half == 0; };
+  auto writes_chan = [&](int c) { return c >= 2 * DK || half == 0; };
 
   // steps applied by this request: all, or its accepted length (replay)
   int steps_n = p.steps;
@@ -225,8 +227,8 @@ __global__ void __launch_bounds__(Shape<D>::NT)
       const float y = conv ? wr[i][0] * hr[i][0] + wr[i][1] * hr[i][1] + wr[i][2] * hr[i][2] + wr[i][3] * x
                            : x;
       yv[i] = y;
-      if (c < D) sq += y * y;
-      else if (c < 2 * D) sk += y * y;
+      if (c < DK) sq += y * y;
+      else if (c < 2 * DK) sk += y * y;
       hr[i][0] = hr[i][1];
       hr[i][1] = hr[i][2];
       hr[i][2] = x;
@@ -256,8 +258,8 @@ __global__ void __launch_bounds__(Shape<D>::NT)
       const int c = tid + i * Sh::NT;
       if (c < NCH) {
         float y = yv[i];
-        if (c < D) y *= iq;
-        else if (c < 2 * D) y *= ik;
+        if (c < DK) y *= iq;
+        else if (c < 2 * DK) y *= ik;
         s_act[c] = round_act ? round_bf16(y) : y;
       }
     }
@@ -275,11 +277,11 @@ __global__ void __launch_bounds__(Shape<D>::NT)
     // ---- q.k (one warp, fixed order) and the partial k S, q S ------------------
     if (tid < 32) {
       float acc = 0.f;
-      for (int i = tid; i < D; i += 32) acc += s_act[i] * s_act[D + i];
+      for (int i = tid; i < DK; i += 32) acc += s_act[i] * s_act[DK + i];
       acc = warp_sum(acc);
       if (tid == 0) s_qk = acc;
     }
-    const float *sqa = s_act, *ska = s_act + D, *sva = s_act + 2 * D;
+    const float *sqa = s_act, *ska = s_act + DK, *sva = s_act + 2 * DK;
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
 #pragma unroll
     for (int i = 0; i < Sh::RPT; ++i) {
@@ -330,12 +332,12 @@ __global__ void __launch_bounds__(Shape<D>::NT)
       S.z = a * S.z + kr * u.z;
       S.w = a * S.w + kr * u.w;
       if (!last) s_state4[r * Sh::COLG + cg] = S;
-      if (emit) *reinterpret_cast<float4 *>(dst + (size_t)r * D + 4 * cg) = S;
-      if (bdst) *reinterpret_cast<float4 *>(bdst + (size_t)r * D + 4 * cg) = S;
+      if (emit) *reinterpret_cast<float4 *>(dst + (size_t)r * DV + 4 * cg) = S;
+      if (bdst) *reinterpret_cast<float4 *>(bdst + (size_t)r * DV + 4 * cg) = S;
     }
     if (rg == 0 && p.o) {
       const float qk = s_qk;
-      const size_t ob = row * D + col0 + 4 * cg;
+      const size_t ob = row * DV + col0 + 4 * cg;
       store_act(p.o, ob + 0, a * y.x + qk * u.x, p.out_bf16);
       store_act(p.o, ob + 1, a * y.y + qk * u.y, p.out_bf16);
       store_act(p.o, ob + 2, a * y.z + qk * u.z, p.out_bf16);
@@ -366,7 +368,7 @@ __global__ void __launch_bounds__(Shape<D>::NT)
 #pragma unroll
     for (int i = 0; i < Sh::RPT; ++i) {
       const int r = rg + Sh::ROWG * i;
-      *reinterpret_cast<float4 *>(dst + (size_t)r * D + 4 * cg) = s_state4[r * Sh::COLG + cg];
+      *reinterpret_cast<float4 *>(dst + (size_t)r * DV + 4 * cg) = s_state4[r * Sh::COLG + cg];
     }
     if (conv && p.conv_dst) {
 #pragma unroll
@@ -382,23 +384,23 @@ __global__ void __launch_bounds__(Shape<D>::NT)
   release_history();
 }
 
-template <int D>
+template <int DK, int DV>
 cudaError_t launch(const RecurParams &p, cudaStream_t stream) {
-  using Sh = Shape<D>;
+  using Sh = Shape<DK, DV>;
   const unsigned grid = (unsigned)p.N * (unsigned)p.H * Sh::NSPLIT;
-  constexpr int smem = D * Sh::DC * 4;
+  constexpr int smem = DK * Sh::DC * 4;
   CUtensorMap tmap;
   memset(&tmap, 0, sizeof(tmap));
   if (p.S_src) {
     // the state source as (columns, rows, slot * H + head) planes; box = one column slice
     const long long planes = (long long)(p.src_slot ? p.pool_slots : p.N) * p.H;
-    const long long dims[3] = {D, D, planes};
-    const int box[3] = {Sh::DC, D, 1};
+    const long long dims[3] = {DV, DK, planes};
+    const int box[3] = {Sh::DC, DK, 1};
     if (!encode_3d_map(&tmap, p.S_src, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dims, box, false))
       return cudaErrorInvalidValue;
   }
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(recurrent_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(recurrent_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -413,22 +415,28 @@ cudaError_t launch(const RecurParams &p, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, recurrent_kernel<D>, tmap, p);
+  return cudaLaunchKernelEx(&cfg, recurrent_kernel<DK, DV>, tmap, p);
 }
 
 }  // namespace
 
-glinattn_status launch_recurrent(const RecurParams &p, int d, cudaStream_t stream) {
+glinattn_status launch_recurrent(const RecurParams &p, int dk, int dv, cudaStream_t stream) {
   if ((long long)p.N * p.H == 0) return GLINATTN_OK;
-  if (decode128_supports(p, d))
+  if (dk == dv && decode128_supports(p, dk))
     return launch_decode128(p, stream) == cudaSuccess ? GLINATTN_OK : GLINATTN_ERR_CUDA;
   cudaError_t e;
-  switch (d) {
-    case 16: e = launch<16>(p, stream); break;
-    case 32: e = launch<32>(p, stream); break;
-    case 64: e = launch<64>(p, stream); break;
-    case 128: e = launch<128>(p, stream); break;
-    default: return GLINATTN_ERR_UNSUPPORTED;
+  if (dk == 128 && dv == 64) {
+    e = launch<128, 64>(p, stream);
+  } else if (dk != dv) {
+    return GLINATTN_ERR_UNSUPPORTED;
+  } else {
+    switch (dk) {
+      case 16: e = launch<16, 16>(p, stream); break;
+      case 32: e = launch<32, 32>(p, stream); break;
+      case 64: e = launch<64, 64>(p, stream); break;
+      case 128: e = launch<128, 128>(p, stream); break;
+      default: return GLINATTN_ERR_UNSUPPORTED;
+    }
   }
   return e == cudaSuccess ? GLINATTN_OK : GLINATTN_ERR_CUDA;
 }

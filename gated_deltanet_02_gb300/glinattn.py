@@ -50,13 +50,13 @@ class PrefillArgs(ctypes.Structure):
                 ("q", _vp), ("k", _vp), ("v", _vp), ("alpha", _vp), ("beta", _vp), ("S0", _vp),
                 ("S_T", _vp), ("o", _vp), ("conv_w", _vp), ("conv_in", _vp), ("conv_out", _vp),
                 ("dev_status", _vp), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
-                ("S_blocks", _vp), ("conv_blocks", _vp)]
+                ("S_blocks", _vp), ("conv_blocks", _vp), ("qk_heads", _i32)]
 
 
 class DecodeArgs(ctypes.Structure):
     _fields_ = [("variant", _i32), ("in_dtype", _i32), ("out_dtype", _i32), ("qk_l2norm", _i32),
                 ("num_req", _i32), ("heads", _i32), ("dk", _i32), ("dv", _i32),
-                ("pool_slots", _i32), ("reserved0", _i32),
+                ("pool_slots", _i32), ("qk_heads", _i32),
                 ("q", _vp), ("k", _vp), ("v", _vp), ("alpha", _vp), ("beta", _vp),
                 ("state_pool", _vp), ("slot_ids", _vp), ("o", _vp), ("conv_w", _vp),
                 ("conv_pool", _vp), ("dev_status", _vp)]
@@ -68,13 +68,13 @@ class SpecArgs(ctypes.Structure):
                 ("dv", _i32), ("pool_slots", _i32),
                 ("q", _vp), ("k", _vp), ("v", _vp), ("alpha", _vp), ("beta", _vp),
                 ("state_pool", _vp), ("src_slots", _vp), ("dst_slots", _vp), ("o", _vp),
-                ("conv_w", _vp), ("conv_pool", _vp), ("dev_status", _vp)]
+                ("conv_w", _vp), ("conv_pool", _vp), ("dev_status", _vp), ("qk_heads", _i32)]
 
 
 class ReplayArgs(ctypes.Structure):
     _fields_ = [("variant", _i32), ("in_dtype", _i32), ("qk_l2norm", _i32), ("num_req", _i32),
                 ("draft_len", _i32), ("heads", _i32), ("dk", _i32), ("dv", _i32), ("pool_slots", _i32),
-                ("reserved0", _i32),
+                ("qk_heads", _i32),
                 ("q", _vp), ("k", _vp), ("v", _vp), ("alpha", _vp), ("beta", _vp),
                 ("state_pool", _vp), ("slot_ids", _vp), ("accept", _vp), ("conv_w", _vp),
                 ("conv_pool", _vp), ("dev_status", _vp)]
@@ -155,19 +155,20 @@ def glinattn_prefill(q, k, v, alpha, beta=None, S0=None, *, variant=GLA, conv_w=
                      conv_in=None, qk_l2norm=False, out_dtype=None, o=None, S_T=None,
                      conv_out=None, dev_status=None, stream=None, workspace=None,
                      state_every=0, S_blocks=None, conv_blocks=None):
-    """Prefill one segment.  q, k [B,T,H,dk], v [B,T,H,dv] (bf16 or fp32);
+    """Prefill one segment.  q, k [B,T,Hq,dk], v [B,T,H,dv] (bf16 or fp32;
+    Hq < H shares q, k across groups of H // Hq heads);
     alpha/beta [B,T,H] fp32; S0 [B,H,dk,dv] fp32 or None.  Outputs, and the
     scratch space the chunked Gated DeltaNet kernels need, are allocated when
     not given.  Returns (o, S_T, conv_out); with state_every > 0 also
     S_blocks [B, T // state_every, H, dk, dv], the state after every
     state_every tokens of the segment, and conv_blocks [B, T // state_every,
     3, Cch], the conv cache at the same points (None without a conv)."""
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
+    B, T, Hq, dk = q.shape
+    H, dv = v.shape[2], v.shape[3]
     dev = q.device
     act = q.dtype
-    _need(q, "q", act, (B, T, H, dk), dev)
-    _need(k, "k", act, (B, T, H, dk), dev)
+    _need(q, "q", act, (B, T, Hq, dk), dev)
+    _need(k, "k", act, (B, T, Hq, dk), dev)
     _need(v, "v", act, (B, T, H, dv), dev)
     _need(alpha, "alpha", torch.float32, (B, T, H), dev)
     _need(beta, "beta", torch.float32, (B, T, H), dev)
@@ -205,7 +206,7 @@ def glinattn_prefill(q, k, v, alpha, beta=None, S0=None, *, variant=GLA, conv_w=
                     S0=_ptr(S0), S_T=_ptr(S_T), o=_ptr(o), conv_w=_ptr(conv_w),
                     conv_in=_ptr(conv_in), conv_out=_ptr(conv_out), dev_status=_ptr(dev_status),
                     state_every=state_every, S_blocks=_ptr(S_blocks) if nblk else None,
-                    conv_blocks=_ptr(conv_blocks) if nblk else None)
+                    conv_blocks=_ptr(conv_blocks) if nblk else None, qk_heads=Hq)
     ws_bytes = library().glinattn_prefill_workspace_size(ctypes.byref(a))
     ws = None
     if ws_bytes:
@@ -224,16 +225,16 @@ def glinattn_prefill(q, k, v, alpha, beta=None, S0=None, *, variant=GLA, conv_w=
 def glinattn_decode(q, k, v, alpha, beta, state_pool, slot_ids, *, variant=GDN, conv_w=None,
                     conv_pool=None, qk_l2norm=False, out_dtype=None, o=None, dev_status=None,
                     stream=None):
-    """One decode step.  q, k [N,H,dk], v [N,H,dv]; alpha/beta [N,H];
+    """One decode step.  q, k [N,Hq,dk], v [N,H,dv]; alpha/beta [N,H];
     state_pool [P,H,dk,dv] fp32 and conv_pool [P,3,Cch] updated in place at
     slot_ids [N] int32.  Returns o [N,H,dv]."""
-    N, H, dk = q.shape
-    dv = v.shape[-1]
+    N, Hq, dk = q.shape
+    H, dv = v.shape[1], v.shape[2]
     dev = q.device
     act = q.dtype
     P = state_pool.shape[0]
-    _need(q, "q", act, (N, H, dk), dev)
-    _need(k, "k", act, (N, H, dk), dev)
+    _need(q, "q", act, (N, Hq, dk), dev)
+    _need(k, "k", act, (N, Hq, dk), dev)
     _need(v, "v", act, (N, H, dv), dev)
     _need(alpha, "alpha", torch.float32, (N, H), dev)
     _need(beta, "beta", torch.float32, (N, H), dev)
@@ -249,7 +250,7 @@ def glinattn_decode(q, k, v, alpha, beta, state_pool, slot_ids, *, variant=GDN, 
     _need(o, "o", out_dtype, (N, H, dv), dev)
     a = DecodeArgs(variant=variant, in_dtype=_dtype_code(q), out_dtype=_dtype_code(o),
                    qk_l2norm=int(bool(qk_l2norm)), num_req=N, heads=H, dk=dk, dv=dv,
-                   pool_slots=P, q=_ptr(q), k=_ptr(k), v=_ptr(v), alpha=_ptr(alpha),
+                   pool_slots=P, qk_heads=Hq, q=_ptr(q), k=_ptr(k), v=_ptr(v), alpha=_ptr(alpha),
                    beta=_ptr(beta), state_pool=_ptr(state_pool), slot_ids=_ptr(slot_ids),
                    o=_ptr(o), conv_w=_ptr(conv_w), conv_pool=_ptr(conv_pool) if conv_w is not None else None,
                    dev_status=_ptr(dev_status))
@@ -260,18 +261,18 @@ def glinattn_decode(q, k, v, alpha, beta, state_pool, slot_ids, *, variant=GDN, 
 def glinattn_spec_decode(q, k, v, alpha, beta, state_pool, src_slots, dst_slots, *, variant=GDN,
                          conv_w=None, conv_pool=None, qk_l2norm=False, out_dtype=None, o=None,
                          dev_status=None, stream=None):
-    """D draft steps per request.  q, k [N,D,H,dk], v [N,D,H,dv];
+    """D draft steps per request.  q, k [N,D,Hq,dk], v [N,D,H,dv];
     alpha/beta [N,D,H]; src_slots [N], dst_slots [N,D] int32.  The state after
     draft i is written to state_pool[dst_slots[n, i]]; dst_slots=None only
     verifies (outputs, no state written: see glinattn_replay).  Returns
     o [N,D,H,dv]."""
-    N, D, H, dk = q.shape
-    dv = v.shape[-1]
+    N, D, Hq, dk = q.shape
+    H, dv = v.shape[2], v.shape[3]
     dev = q.device
     act = q.dtype
     P = state_pool.shape[0]
-    _need(q, "q", act, (N, D, H, dk), dev)
-    _need(k, "k", act, (N, D, H, dk), dev)
+    _need(q, "q", act, (N, D, Hq, dk), dev)
+    _need(k, "k", act, (N, D, Hq, dk), dev)
     _need(v, "v", act, (N, D, H, dv), dev)
     _need(alpha, "alpha", torch.float32, (N, D, H), dev)
     _need(beta, "beta", torch.float32, (N, D, H), dev)
@@ -288,8 +289,9 @@ def glinattn_spec_decode(q, k, v, alpha, beta, state_pool, src_slots, dst_slots,
     _need(o, "o", out_dtype, (N, D, H, dv), dev)
     a = SpecArgs(variant=variant, in_dtype=_dtype_code(q), out_dtype=_dtype_code(o),
                  qk_l2norm=int(bool(qk_l2norm)), num_req=N, draft_len=D, heads=H, dk=dk, dv=dv,
-                 pool_slots=P, q=_ptr(q), k=_ptr(k), v=_ptr(v), alpha=_ptr(alpha), beta=_ptr(beta),
-                 state_pool=_ptr(state_pool), src_slots=_ptr(src_slots), dst_slots=_ptr(dst_slots),
+                 pool_slots=P, qk_heads=Hq, q=_ptr(q), k=_ptr(k), v=_ptr(v), alpha=_ptr(alpha),
+                 beta=_ptr(beta), state_pool=_ptr(state_pool), src_slots=_ptr(src_slots),
+                 dst_slots=_ptr(dst_slots),
                  o=_ptr(o), conv_w=_ptr(conv_w), conv_pool=_ptr(conv_pool) if conv_w is not None else None,
                  dev_status=_ptr(dev_status))
     _call("glinattn_spec_decode", a, _stream_handle(stream, dev))
@@ -299,11 +301,11 @@ def glinattn_spec_decode(q, k, v, alpha, beta, state_pool, src_slots, dst_slots,
 def glinattn_replay(k, v, alpha, beta, state_pool, slot_ids, accept, *, q=None, variant=GDN,
                     conv_w=None, conv_pool=None, qk_l2norm=False, dev_status=None, stream=None):
     """Apply the first accept[n] recorded draft steps to state_pool[slot_ids[n]]
-    (and its conv cache) in place.  k [N,D,H,dk], v [N,D,H,dv], alpha/beta
-    [N,D,H], q [N,D,H,dk] (its raw values enter the conv cache; defaults to k
+    (and its conv cache) in place.  k [N,D,Hq,dk], v [N,D,H,dv], alpha/beta
+    [N,D,H], q [N,D,Hq,dk] (its raw values enter the conv cache; defaults to k
     when there is no conv); slot_ids, accept [N] int32."""
-    N, D, H, dk = k.shape
-    dv = v.shape[-1]
+    N, D, Hq, dk = k.shape
+    H, dv = v.shape[2], v.shape[3]
     dev = k.device
     act = k.dtype
     P = state_pool.shape[0]
@@ -311,8 +313,8 @@ def glinattn_replay(k, v, alpha, beta, state_pool, slot_ids, accept, *, q=None, 
         if conv_w is not None:
             raise ValueError("q is needed with a conv: its raw values enter the conv cache")
         q = k
-    _need(q, "q", act, (N, D, H, dk), dev)
-    _need(k, "k", act, (N, D, H, dk), dev)
+    _need(q, "q", act, (N, D, Hq, dk), dev)
+    _need(k, "k", act, (N, D, Hq, dk), dev)
     _need(v, "v", act, (N, D, H, dv), dev)
     _need(alpha, "alpha", torch.float32, (N, D, H), dev)
     _need(beta, "beta", torch.float32, (N, D, H), dev)
@@ -324,7 +326,8 @@ def glinattn_replay(k, v, alpha, beta, state_pool, slot_ids, accept, *, q=None, 
         _need(conv_w, "conv_w", torch.float32, (Cch, 4), dev)
         _need(conv_pool, "conv_pool", act, (P, 3, Cch), dev)
     a = ReplayArgs(variant=variant, in_dtype=_dtype_code(k), qk_l2norm=int(bool(qk_l2norm)), num_req=N,
-                   draft_len=D, heads=H, dk=dk, dv=dv, pool_slots=P, q=_ptr(q), k=_ptr(k), v=_ptr(v),
+                   draft_len=D, heads=H, dk=dk, dv=dv, pool_slots=P, qk_heads=Hq, q=_ptr(q), k=_ptr(k),
+                   v=_ptr(v),
                    alpha=_ptr(alpha), beta=_ptr(beta), state_pool=_ptr(state_pool), slot_ids=_ptr(slot_ids),
                    accept=_ptr(accept), conv_w=_ptr(conv_w),
                    conv_pool=_ptr(conv_pool) if conv_w is not None else None, dev_status=_ptr(dev_status))

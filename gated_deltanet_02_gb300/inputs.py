@@ -22,6 +22,10 @@ measured on; "N(m, s)" means mean m, standard deviation s):
   first N entries of a random permutation of the P slots.
 * ``spec_drafts``     -- D draft tokens per request and an accepted prefix
   length drawn uniformly from 0..D.
+* ``ssd_prefill`` / ``ssd_decode`` -- the SSD form of Mamba2 as gated linear
+  attention: G groups of q / k heads (C and B) of size d_k = 128 (the state
+  size) shared by H heads of value size d_v = 64 (the head dim); q, k ~
+  N(0,1)/sqrt(d_k), v ~ N(0,1) in bf16, alpha = sigmoid(N(0,1) + 3).
 """
 from __future__ import annotations
 
@@ -112,6 +116,30 @@ def spec_drafts(N, D, H, d, seed=0, device="cpu", dtype=torch.bfloat16):
     alpha = torch.sigmoid(_randn((N, D, H), g, device) + 3.0)
     accept = torch.randint(0, D + 1, (N,), generator=g, device=device, dtype=torch.int32)
     return dict(q=q, k=k, v=v, alpha=alpha, beta=beta, accept=accept)
+
+
+def ssd_prefill(B, H, G, T, dk=128, dv=64, seed=0, device="cpu", dtype=torch.bfloat16, s0_std=0.0):
+    g = _gen(seed, device)
+    q = _randn((B, T, G, dk), g, device, dk ** -0.5, dtype)
+    k = _randn((B, T, G, dk), g, device, dk ** -0.5, dtype)
+    v = _randn((B, T, H, dv), g, device, 1.0, dtype)
+    alpha = torch.sigmoid(_randn((B, T, H), g, device) + 3.0)
+    S0 = _randn((B, H, dk, dv), g, device, s0_std) if s0_std > 0 else None
+    return dict(q=q, k=k, v=v, alpha=alpha, beta=None, S0=S0)
+
+
+def ssd_decode(N, H, G, P, dk=128, dv=64, seed=0, device="cpu", dtype=torch.bfloat16, D=None):
+    """One token (D=None) or D draft tokens per request, and a pool of P states."""
+    g = _gen(seed, device)
+    pool = _randn((P, H, dk, dv), g, device, 0.01)
+    perm = torch.randperm(P, generator=g, device=device)
+    slot_ids = perm[:N].to(torch.int32)
+    lead = (N,) if D is None else (N, D)
+    q = _randn(lead + (G, dk), g, device, dk ** -0.5, dtype)
+    k = _randn(lead + (G, dk), g, device, dk ** -0.5, dtype)
+    v = _randn(lead + (H, dv), g, device, 1.0, dtype)
+    alpha = torch.sigmoid(_randn(lead + (H,), g, device) + 3.0)
+    return dict(q=q, k=k, v=v, alpha=alpha, beta=None, pool=pool, slot_ids=slot_ids, perm=perm)
 
 
 def segment_lengths(T: int, fractions=(0.20, 0.35)):

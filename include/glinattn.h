@@ -27,7 +27,12 @@
  *   - dev_status (nullable) is a device word the kernels OR error bits into
  *     (GLINATTN_DEV_*); a unit that raises a bit skips its writes.  The caller
  *     zeroes it and reads it after synchronising.
- *   - Head sizes: dk == dv, one of 16, 32, 64, 128.  Activations (q, k, v,
+ *   - Head sizes: dk == dv, one of 16, 32, 64, 128; or dk = 128, dv = 64, the
+ *     SSD form of Mamba2 (state size 128, head dim 64: "Long context, fast
+ *     inference, smart decoding, and life beyond attention", section
+ *     "Mamba and hybrid SSMs, the real packages"; the linear-attention page's
+ *     section "Two ways to write the same computation" lists the SSD form
+ *     among the gated linear attention recurrences).  Activations (q, k, v,
  *     conv cache) are all GLINATTN_BF16 or all GLINATTN_F32; gates alpha and
  *     beta, states and conv weights are fp32.  alpha must lie in (0, 1],
  *     beta in [0, 1].
@@ -36,6 +41,11 @@
  *     part_offset + h * d + i.  Weight w[c][j] multiplies input x_{t-3+j}
  *     (tap 3 is the current token); no bias, no activation.  The conv cache
  *     holds the last 3 RAW inputs per channel, oldest first: [.., 3, Cch].
+ *   - Grouped q / k heads (qk_heads = Hq, 0 meaning Hq = H): q and k are
+ *     [.., Hq, dk] and consecutive groups of H / Hq heads share them, head h
+ *     reading q / k head h / (H / Hq) (the SSD form's B and C shared by the
+ *     heads of a group).  Hq must divide H; grouped heads take no
+ *     convolution (GLINATTN_ERR_UNSUPPORTED).  Everything else stays per head.
  *   - qk_l2norm != 0 rescales each q and k row of each head to
  *     x / sqrt(sum x^2 + 1e-6) after the convolution.  With bf16 activations
  *     the convolved / normalised values are rounded to bf16 before use.
@@ -77,7 +87,7 @@ typedef enum { GLINATTN_F32 = 0, GLINATTN_BF16 = 1 } glinattn_dtype;
  *   (or zero history).  Feeding S_T and conv_out of one call as S0 and
  *   conv_in of the next continues the sequence exactly (segmented prefill).
  *
- *   q, k   [B, T, H, dk]   v [B, T, H, dv]       activations (in_dtype)
+ *   q, k   [B, T, Hq, dk]  v [B, T, H, dv]       activations (in_dtype)
  *   alpha  [B, T, H]       beta [B, T, H] (GDN only, else NULL)       fp32
  *   S0     [B, H, dk, dv]  fp32 or NULL (zero state)
  *   S_T    [B, H, dk, dv]  fp32 output; may alias S0 exactly
@@ -98,9 +108,11 @@ typedef enum { GLINATTN_F32 = 0, GLINATTN_BF16 = 1 } glinattn_dtype;
  *   (when not NULL) [B, T / state_every, 3, Cch] (in_dtype) receives the conv
  *   cache at the same boundaries, so that (S_blocks[:, j], conv_blocks[:, j])
  *   is a whole checkpoint a later prefill or decode can start from.
- *   bf16 activations with dk == dv == 128 run the tensor-core chunked kernels
- *   (chunk 64; Gated DeltaNet also needs `workspace`, see below, else
- *   GLINATTN_ERR_INVALID_ARG); every other supported combination runs the
+ *   bf16 activations with dk = 128 run the tensor-core chunked kernels (chunk
+ *   64): gated linear attention with dv = 128 or 64, grouped q / k heads
+ *   allowed, no convolution or L2 norm; Gated DeltaNet with dv = 128 and one
+ *   q / k head per head (it also needs `workspace`, see below, else
+ *   GLINATTN_ERR_INVALID_ARG).  Every other supported combination runs the
  *   fp32 token-serial kernel, which is exact to fp32 rounding but not fast.
  */
 typedef struct {
@@ -123,6 +135,7 @@ typedef struct {
   size_t workspace_bytes; /* its size; may be 0 when the size query returns 0 */
   float *S_blocks;        /* [B, T / state_every, H, dk, dv] fp32 when state_every > 0 */
   void *conv_blocks;      /* [B, T / state_every, 3, Cch] (in_dtype) or NULL */
+  int32_t qk_heads;       /* q / k heads Hq (0: Hq = H), see "Grouped q / k heads" above */
 } glinattn_prefill_args;
 
 glinattn_status glinattn_prefill(const glinattn_prefill_args *args, glinattn_stream_t stream);
@@ -177,14 +190,14 @@ glinattn_status glinattn_prefill_static_scratch(const glinattn_prefill_args *arg
  *   the device: duplicates race); ids outside [0, pool_slots) set
  *   GLINATTN_DEV_BAD_SLOT and skip that request.
  *
- *   q, k [N, H, dk]   v [N, H, dv]   alpha, beta [N, H]   slot_ids [N] int32
+ *   q, k [N, Hq, dk]   v [N, H, dv]   alpha, beta [N, H]   slot_ids [N] int32
  *   state_pool [P, H, dk, dv] fp32 (read/write)   o [N, H, dv]
  *   conv_w [Cch, 4] or NULL;  conv_pool [P, 3, Cch] (in_dtype, read/write)
  */
 typedef struct {
   int32_t variant, in_dtype, out_dtype, qk_l2norm;
   int32_t num_req, heads, dk, dv, pool_slots;
-  int32_t reserved0;
+  int32_t qk_heads; /* q / k heads Hq (0: Hq = H) */
   const void *q, *k, *v;
   const float *alpha, *beta;
   float *state_pool;
@@ -212,7 +225,7 @@ glinattn_status glinattn_decode(const glinattn_decode_args *args, glinattn_strea
  *   conv cache, and the pool keeps one state per request; glinattn_replay
  *   then applies the accepted drafts (the replay-buffer alternative).
  *
- *   q, k [N, D, H, dk]   v [N, D, H, dv]   alpha, beta [N, D, H]
+ *   q, k [N, D, Hq, dk]   v [N, D, H, dv]   alpha, beta [N, D, H]
  *   src_slots [N]  dst_slots [N, D] or NULL  int32    o [N, D, H, dv]
  */
 typedef struct {
@@ -227,6 +240,7 @@ typedef struct {
   const float *conv_w;
   void *conv_pool;
   uint32_t *dev_status;
+  int32_t qk_heads; /* q / k heads Hq (0: Hq = H) */
 } glinattn_spec_args;
 
 glinattn_status glinattn_spec_decode(const glinattn_spec_args *args, glinattn_stream_t stream);
@@ -245,14 +259,14 @@ glinattn_status glinattn_spec_decode(const glinattn_spec_args *args, glinattn_st
  *   request; slot ids outside [0, pool_slots) set GLINATTN_DEV_BAD_SLOT.
  *   Only the applied steps' gates are checked.  No outputs are written.
  *
- *   q, k [N, D, H, dk]   v [N, D, H, dv]   alpha, beta [N, D, H]   (in_dtype / fp32)
+ *   q, k [N, D, Hq, dk]   v [N, D, H, dv]   alpha, beta [N, D, H]   (in_dtype / fp32)
  *   slot_ids [N] int32 (distinct)   accept [N] int32
  *   state_pool [P, H, dk, dv] fp32 and conv_pool [P, 3, Cch] (read/write)
  */
 typedef struct {
   int32_t variant, in_dtype, qk_l2norm;
   int32_t num_req, draft_len, heads, dk, dv, pool_slots;
-  int32_t reserved0;
+  int32_t qk_heads; /* q / k heads Hq (0: Hq = H) */
   const void *q, *k, *v;
   const float *alpha, *beta;
   float *state_pool;

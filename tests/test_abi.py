@@ -112,7 +112,11 @@ INVALID, UNSUPPORTED = 1, 2
     (dict(in_dtype=5), INVALID),
     (dict(out_dtype=-1), INVALID),
     (dict(dk=96, dv=96), UNSUPPORTED),
-    (dict(dk=128, dv=64), UNSUPPORTED),
+    (dict(dk=128, dv=32), UNSUPPORTED),
+    (dict(dk=64, dv=128), UNSUPPORTED),
+    (dict(qk_heads=3), INVALID),         # does not divide heads = 4
+    (dict(qk_heads=-1), INVALID),
+    (dict(qk_heads=2, conv_w=A * 9), UNSUPPORTED),  # grouped heads take no convolution
     (dict(heads=0), INVALID),
     (dict(batch=-1), INVALID),
     (dict(seqlen=-5), INVALID),
@@ -147,6 +151,8 @@ def test_prefill_null_args_and_empty_batch():
     (dict(dk=48, dv=48), UNSUPPORTED),
     (dict(conv_w=A * 9, conv_pool=None), INVALID),
     (dict(num_req=-1), INVALID),
+    (dict(qk_heads=3), INVALID),
+    (dict(qk_heads=1, conv_w=A * 9, conv_pool=A * 10), UNSUPPORTED),
 ])
 def test_decode_rejects(kw, code):
     assert G.library().glinattn_decode(ctypes.byref(_decode(**kw)), None) == code
