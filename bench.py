@@ -293,6 +293,9 @@ def run_ours(args):
     # ---- long context: 3-segment prefill, then 64 x 4 speculative decode -------------
     lc = long_context_run(args, dist, dev, rank)
 
+    # ---- the SSD form: state 128 x head dim 64, one q / k group for 32 heads ---------
+    ssd = ssd_run(args, dist, dev, rank)
+
     # ---- CPU baseline: the oracle on this host's cores (rank 0) -----------------------
     cpu = cpu_baseline_run(ex, budget_s=args.cpu_seconds) if rank == 0 and not args.no_cpu else None
 
@@ -354,6 +357,7 @@ def run_ours(args):
                                              "checkpoint_bytes": ck_bytes,
                                              "overhead_frac": ck_ms / gdn_ms - 1.0}},
         "long_context": lc,
+        "ssd": ssd,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))
@@ -459,6 +463,49 @@ def long_context_run(args, dist, dev, rank):
                                        "peak": pk["hbm_gbs"], "unit": "GB/s",
                                        "frac": copy_bytes / (statistics.mean(copy_per) / 1e3) / 1e9
                                        / pk["hbm_gbs"], "algorithmic_bytes": copy_bytes}}}
+
+
+def ssd_run(args, dist, dev, rank):
+    """The SSD form of Mamba2 as gated linear attention: a B=2, T=4096 prefill
+    of 32 heads (head dim 64, state size 128) sharing one q / k group, and a
+    decode step of 256 requests x 32 heads from a 512-slot pool."""
+    import torch
+
+    from gated_deltanet_02_gb300 import GLA, glinattn_decode, glinattn_prefill, inputs
+    pk, _ = peaks()
+    B, H, G, T, dk, dv = 2, 32, 1, 4096, 128, 64
+    ex = inputs.ssd_prefill(B, H, G, T, seed=rank, device=dev)
+    o = torch.empty(B, T, H, dv, dtype=torch.bfloat16, device=dev)
+    S = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+
+    def step_prefill():
+        glinattn_prefill(ex["q"], ex["k"], ex["v"], ex["alpha"], None, None, variant=GLA, o=o, S_T=S)
+
+    pre_ms, pre_per = timed_steps(step_prefill, max(3, min(args.steps, 10)), 2, dist, dev)
+    pre_bytes = B * T * G * dk * 2 * 2 + B * T * H * (dv * 2 * 2 + 4) + B * H * dk * dv * 4
+    N, P = 256, 512
+    dx = inputs.ssd_decode(N, H, G, P, seed=rank, device=dev)
+    od = torch.empty(N, H, dv, dtype=torch.bfloat16, device=dev)
+
+    def step_dec():
+        glinattn_decode(dx["q"], dx["k"], dx["v"], dx["alpha"], None, dx["pool"], dx["slot_ids"], variant=GLA,
+                        o=od)
+
+    dec_ms, dec_per = timed_steps(step_dec, max(10, args.steps), 3, dist, dev)
+    dec_bytes = N * H * dk * dv * 4 * 2
+    hbm = pk["hbm_gbs"]
+    return {"config": "SSD form as gated linear attention: B=2 T=4096, 32 heads of head dim 64, state size 128, "
+                      "one shared q / k group, bf16; decode 256 requests x 32 heads, 512-slot fp32 pool",
+            "prefill_tokens_per_s": B * T / (pre_ms / 1e3), "prefill_ms": pre_ms,
+            "prefill_roofline": {"bound": "hbm", "achieved": pre_bytes / (statistics.mean(pre_per) / 1e3) / 1e9,
+                                 "peak": hbm, "unit": "GB/s",
+                                 "frac": pre_bytes / (statistics.mean(pre_per) / 1e3) / 1e9 / hbm,
+                                 "algorithmic_bytes": pre_bytes},
+            "decode_tokens_per_s": N / (dec_ms / 1e3), "decode_ms": dec_ms,
+            "decode_roofline": {"bound": "hbm", "achieved": dec_bytes / (statistics.mean(dec_per) / 1e3) / 1e9,
+                                "peak": hbm, "unit": "GB/s",
+                                "frac": dec_bytes / (statistics.mean(dec_per) / 1e3) / 1e9 / hbm,
+                                "algorithmic_bytes": dec_bytes}}
 
 
 # ----------------------------------------------------------------------------

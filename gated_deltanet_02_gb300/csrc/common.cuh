@@ -21,6 +21,10 @@ struct RecurParams {
   const float *alpha, *beta;
   // state source: S_src + (slot or n) * H*d*d + h*d*d; NULL means zeros
   const float *S_src;
+  // normalised linear attention: normaliser source / destination, indexed
+  // like the states ([.., H, dk] fp32)
+  const float *z_src;
+  float *z_dst;
   const int32_t *src_slot;  // [N] or NULL (index by n)
   // state destination(s)
   float *S_dst;

@@ -525,7 +525,7 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
 bool decode128_supports(const RecurParams &p, int d) {
   return d == kD && p.src_slot != nullptr && (p.dst_slot != nullptr || p.S_dst == nullptr) && p.S_src != nullptr &&
          p.steps >= 1 && p.pool_slots > 0 && (p.conv_w == nullptr || p.conv_src != nullptr) &&
-         p.S_blocks == nullptr && p.Hq == p.H;
+         p.S_blocks == nullptr && p.Hq == p.H && p.variant != GLINATTN_NLA;
 }
 
 cudaError_t launch_decode128(const RecurParams &p, cudaStream_t stream) {

@@ -23,7 +23,8 @@ bool partial_overlap(const void *a, size_t na, const void *b, size_t nb) {
 
 glinattn_status check_common(int variant, int in_dtype, int out_dtype, int dk, int dv,
                              int heads) {
-  if (variant != GLINATTN_GLA && variant != GLINATTN_GDN) return GLINATTN_ERR_INVALID_ARG;
+  if (variant != GLINATTN_GLA && variant != GLINATTN_GDN && variant != GLINATTN_NLA)
+    return GLINATTN_ERR_INVALID_ARG;
   if ((in_dtype != GLINATTN_F32 && in_dtype != GLINATTN_BF16) ||
       (out_dtype != GLINATTN_F32 && out_dtype != GLINATTN_BF16))
     return GLINATTN_ERR_INVALID_ARG;
@@ -90,16 +91,24 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
   const size_t state_bytes = (size_t)B * H * dk * dv * sizeof(float);
   if (!a->S_T) return GLINATTN_ERR_INVALID_ARG;
   if (a->state_every < 0) return GLINATTN_ERR_INVALID_ARG;
+  const bool nla = a->variant == GLINATTN_NLA;
+  if (nla) {  // no convolution, L2 norm or checkpoints; the normaliser goes out
+    if (a->conv_w || a->qk_l2norm || a->state_every) return GLINATTN_ERR_UNSUPPORTED;
+    if (!a->z_T) return GLINATTN_ERR_INVALID_ARG;
+  }
   const bool emit_blocks = a->state_every > 0 && T / a->state_every > 0;
   if (emit_blocks && (!a->S_blocks || !aligned16(a->S_blocks))) return GLINATTN_ERR_INVALID_ARG;
   if (T > 0) {
-    if (!a->q || !a->k || !a->v || !a->alpha || !a->o) return GLINATTN_ERR_INVALID_ARG;
+    if (!a->q || !a->k || !a->v || (!a->alpha && !nla) || !a->o) return GLINATTN_ERR_INVALID_ARG;
     if (a->variant == GLINATTN_GDN && !a->beta) return GLINATTN_ERR_INVALID_ARG;
   }
   if (!all_aligned(a->q, a->k, a->v, a->alpha, a->beta, a->S0, a->S_T, a->o, a->conv_w,
                    a->conv_in, a->conv_out))
     return GLINATTN_ERR_INVALID_ARG;
+  if (nla && !all_aligned(a->z0, a->z_T)) return GLINATTN_ERR_INVALID_ARG;
   if (partial_overlap(a->S0, state_bytes, a->S_T, state_bytes)) return GLINATTN_ERR_INVALID_ARG;
+  if (nla && partial_overlap(a->z0, (size_t)B * H * dk * 4, a->z_T, (size_t)B * H * dk * 4))
+    return GLINATTN_ERR_INVALID_ARG;
   const int Cch = H * (2 * dk + dv);
   if (a->conv_w) {
     const size_t cb = (size_t)B * 3 * Cch * act;
@@ -141,10 +150,12 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
   p.q = a->q;
   p.k = a->k;
   p.v = a->v;
-  p.alpha = a->alpha;
+  p.alpha = nla ? nullptr : a->alpha;
   p.beta = a->beta;
   p.S_src = a->S0;
   p.S_dst = a->S_T;
+  p.z_src = nla ? a->z0 : nullptr;
+  p.z_dst = nla ? a->z_T : nullptr;
   p.o = a->o;
   p.conv_w = a->conv_w;
   p.conv_src = a->conv_w ? a->conv_in : nullptr;
@@ -175,7 +186,10 @@ glinattn_status glinattn_decode(const glinattn_decode_args *a, glinattn_stream_t
   if (a->num_req < 0 || a->pool_slots <= 0) return GLINATTN_ERR_INVALID_ARG;
   if ((long long)a->num_req * a->heads > (1ll << 30)) return GLINATTN_ERR_INVALID_ARG;
   if (a->num_req == 0) return GLINATTN_OK;
-  if (!a->q || !a->k || !a->v || !a->alpha || !a->o || !a->state_pool || !a->slot_ids)
+  const bool nla = a->variant == GLINATTN_NLA;
+  if (nla && (a->conv_w || a->qk_l2norm)) return GLINATTN_ERR_UNSUPPORTED;
+  if (nla && (!a->z_pool || !aligned16(a->z_pool))) return GLINATTN_ERR_INVALID_ARG;
+  if (!a->q || !a->k || !a->v || (!a->alpha && !nla) || !a->o || !a->state_pool || !a->slot_ids)
     return GLINATTN_ERR_INVALID_ARG;
   if (a->variant == GLINATTN_GDN && !a->beta) return GLINATTN_ERR_INVALID_ARG;
   if (a->conv_w && !a->conv_pool) return GLINATTN_ERR_INVALID_ARG;
@@ -195,9 +209,11 @@ glinattn_status glinattn_decode(const glinattn_decode_args *a, glinattn_stream_t
   p.q = a->q;
   p.k = a->k;
   p.v = a->v;
-  p.alpha = a->alpha;
+  p.alpha = nla ? nullptr : a->alpha;
   p.beta = a->beta;
   p.S_src = a->state_pool;
+  p.z_src = nla ? a->z_pool : nullptr;
+  p.z_dst = nla ? a->z_pool : nullptr;
   p.src_slot = a->slot_ids;
   p.S_dst = a->state_pool;
   p.dst_slot = a->slot_ids;
@@ -221,7 +237,10 @@ glinattn_status glinattn_spec_decode(const glinattn_spec_args *a, glinattn_strea
   if ((long long)a->num_req * a->heads > (1ll << 30) || a->draft_len > (1 << 20))
     return GLINATTN_ERR_INVALID_ARG;
   if (a->num_req == 0) return GLINATTN_OK;
-  if (!a->q || !a->k || !a->v || !a->alpha || !a->o || !a->state_pool || !a->src_slots)
+  const bool nla = a->variant == GLINATTN_NLA;
+  if (nla && (a->conv_w || a->qk_l2norm)) return GLINATTN_ERR_UNSUPPORTED;
+  if (nla && (!a->z_pool || !aligned16(a->z_pool))) return GLINATTN_ERR_INVALID_ARG;
+  if (!a->q || !a->k || !a->v || (!a->alpha && !nla) || !a->o || !a->state_pool || !a->src_slots)
     return GLINATTN_ERR_INVALID_ARG;
   if (a->variant == GLINATTN_GDN && !a->beta) return GLINATTN_ERR_INVALID_ARG;
   if (a->conv_w && !a->conv_pool) return GLINATTN_ERR_INVALID_ARG;
@@ -241,9 +260,11 @@ glinattn_status glinattn_spec_decode(const glinattn_spec_args *a, glinattn_strea
   p.q = a->q;
   p.k = a->k;
   p.v = a->v;
-  p.alpha = a->alpha;
+  p.alpha = nla ? nullptr : a->alpha;
   p.beta = a->beta;
   p.S_src = a->state_pool;
+  p.z_src = nla ? a->z_pool : nullptr;
+  p.z_dst = nla ? a->z_pool : nullptr;
   p.src_slot = a->src_slots;
   const bool verify_only = a->dst_slots == nullptr;  // outputs only, the pool is not written
   p.S_dst = verify_only ? nullptr : a->state_pool;
@@ -268,7 +289,10 @@ glinattn_status glinattn_replay(const glinattn_replay_args *a, glinattn_stream_t
   if ((long long)a->num_req * a->heads > (1ll << 30) || a->draft_len > (1 << 20))
     return GLINATTN_ERR_INVALID_ARG;
   if (a->num_req == 0) return GLINATTN_OK;
-  if (!a->q || !a->k || !a->v || !a->alpha || !a->state_pool || !a->slot_ids || !a->accept)
+  const bool nla = a->variant == GLINATTN_NLA;
+  if (nla && (a->conv_w || a->qk_l2norm)) return GLINATTN_ERR_UNSUPPORTED;
+  if (nla && (!a->z_pool || !aligned16(a->z_pool))) return GLINATTN_ERR_INVALID_ARG;
+  if (!a->q || !a->k || !a->v || (!a->alpha && !nla) || !a->state_pool || !a->slot_ids || !a->accept)
     return GLINATTN_ERR_INVALID_ARG;
   if (a->variant == GLINATTN_GDN && !a->beta) return GLINATTN_ERR_INVALID_ARG;
   if (a->conv_w && !a->conv_pool) return GLINATTN_ERR_INVALID_ARG;
@@ -287,9 +311,11 @@ glinattn_status glinattn_replay(const glinattn_replay_args *a, glinattn_stream_t
   p.q = a->q;
   p.k = a->k;
   p.v = a->v;
-  p.alpha = a->alpha;
+  p.alpha = nla ? nullptr : a->alpha;
   p.beta = a->beta;
   p.S_src = a->state_pool;
+  p.z_src = nla ? a->z_pool : nullptr;
+  p.z_dst = nla ? a->z_pool : nullptr;
   p.src_slot = a->slot_ids;
   p.S_dst = a->state_pool;  // in place, the final state only
   p.dst_slot = a->slot_ids;

@@ -65,6 +65,9 @@ __device__ __forceinline__ float round_bf16(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
 
+// phi(x) = elu(x) + 1, the positive feature map of normalised linear attention
+__device__ __forceinline__ float feature_map(float x) { return x > 0.f ? x + 1.f : expf(x); }
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -87,12 +90,15 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
   const int col0 = half * Sh::DC;  // first state column of this CTA
   const size_t DD = (size_t)DK * DV;
   const int hq = h / (p.H / p.Hq);  // the q / k head (group) of head h
+  const bool nla = p.variant == GLINATTN_NLA;  // no gates; phi(q), phi(k); normaliser z
 
   extern __shared__ __align__(128) float4 s_state4[];  // DK rows x DC columns, row-major
   __shared__ float s_act[NCH];                          // q | k | own v slice after the front end
   __shared__ float s_red[Sh::ROWG][2][Sh::DC];
   __shared__ float s_wsum[2][NW];
   __shared__ float s_qk;
+  __shared__ float s_z[DK];  // normalised linear attention: the normaliser z
+  __shared__ float s_qz;     // and phi(q) . z before this step's update
   __shared__ int s_bad;
   __shared__ __align__(8) uint64_t s_bar;
 
@@ -144,7 +150,7 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
   int dslot_next = n;
   if (p.steps > 0) {
     const size_t row0 = ((size_t)n * p.steps) * p.H + h;
-    a_next = p.alpha[row0];
+    a_next = nla ? 1.f : p.alpha[row0];
     if (p.variant == GLINATTN_GDN) b_next = p.beta[row0];
     if (p.dst_slot) dslot_next = p.dst_slot[(size_t)n * (p.dst_per_step ? p.steps : 1)];
   }
@@ -180,7 +186,7 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
       if (s < 0 || s >= p.pool_slots) bad |= GLINATTN_DEV_BAD_SLOT;
     }
   }
-  for (int t = tid; t < steps_n; t += Sh::NT) {
+  for (int t = tid; t < steps_n && !nla; t += Sh::NT) {
     const float a = p.alpha[((size_t)n * p.steps + t) * p.H + h];
     if (!(a > 0.f && a <= 1.f)) bad |= GLINATTN_DEV_BAD_GATE;
   }
@@ -197,6 +203,9 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
     for (int i = 0; i < Sh::RPT; ++i)
       s_state4[(rg + Sh::ROWG * i) * Sh::COLG + cg] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  if (nla)  // read by warp 0 after the first step's barrier
+    for (int i = tid; i < DK; i += Sh::NT)
+      s_z[i] = p.z_src && slot_ok ? p.z_src[((size_t)slot * p.H + h) * DK + i] : 0.f;
   // The slices of one state share the q / k conv history, and slice 0 writes it
   // back (in place for decode): every slice has read it before any writes it.
   bool history_released = Sh::NSPLIT == 1;
@@ -213,7 +222,7 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
     const float a = a_next, bgate = b_next;
     const int dslot_t = dslot_next;
     if (t + 1 < steps_n) {
-      a_next = p.alpha[row + p.H];
+      a_next = nla ? 1.f : p.alpha[row + p.H];
       if (p.variant == GLINATTN_GDN) b_next = p.beta[row + p.H];
       if (p.dst_slot && p.dst_per_step) dslot_next = p.dst_slot[(size_t)n * p.steps + t + 1];
     }
@@ -224,8 +233,8 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
     for (int i = 0; i < MAXC; ++i) {
       const int c = tid + i * Sh::NT;
       const float x = xr[i];
-      const float y = conv ? wr[i][0] * hr[i][0] + wr[i][1] * hr[i][1] + wr[i][2] * hr[i][2] + wr[i][3] * x
-                           : x;
+      float y = conv ? wr[i][0] * hr[i][0] + wr[i][1] * hr[i][1] + wr[i][2] * hr[i][2] + wr[i][3] * x : x;
+      if (nla && c < 2 * DK) y = feature_map(y);
       yv[i] = y;
       if (c < DK) sq += y * y;
       else if (c < 2 * DK) sk += y * y;
@@ -252,7 +261,7 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
       iq = 1.f / sqrtf(tq + 1e-6f);
       ik = 1.f / sqrtf(tk + 1e-6f);
     }
-    const bool round_act = p.in_bf16 && (conv || p.qk_l2norm);
+    const bool round_act = p.in_bf16 && (conv || p.qk_l2norm || nla);
 #pragma unroll
     for (int i = 0; i < MAXC; ++i) {
       const int c = tid + i * Sh::NT;
@@ -276,10 +285,17 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
 
     // ---- q.k (one warp, fixed order) and the partial k S, q S ------------------
     if (tid < 32) {
-      float acc = 0.f;
-      for (int i = tid; i < DK; i += 32) acc += s_act[i] * s_act[DK + i];
+      float acc = 0.f, accz = 0.f;
+      for (int i = tid; i < DK; i += 32) {
+        acc += s_act[i] * s_act[DK + i];
+        if (nla) accz += s_act[i] * s_z[i];
+      }
       acc = warp_sum(acc);
-      if (tid == 0) s_qk = acc;
+      if (nla) accz = warp_sum(accz);
+      if (tid == 0) {
+        s_qk = acc;
+        s_qz = accz;
+      }
     }
     const float *sqa = s_act, *ska = s_act + DK, *sva = s_act + 2 * DK;
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
@@ -335,13 +351,22 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
       if (emit) *reinterpret_cast<float4 *>(dst + (size_t)r * DV + 4 * cg) = S;
       if (bdst) *reinterpret_cast<float4 *>(bdst + (size_t)r * DV + 4 * cg) = S;
     }
+    if (nla && tid < DK) {  // z <- z + phi(k); every reader of the old z is past the barrier
+      s_z[tid] += ska[tid];
+      if (emit && half == 0 && p.z_dst) {
+        release_history();  // the other slice has read the source normaliser (it may be this slot)
+        p.z_dst[(dslot * p.H + h) * DK + tid] = s_z[tid];
+      }
+    }
     if (rg == 0 && p.o) {
       const float qk = s_qk;
+      // normalised linear attention divides by phi(q) . z_t = phi(q) . z_{t-1} + phi(q) . phi(k)
+      const float inv = nla ? 1.f / (s_qz + qk + 1e-6f) : 1.f;
       const size_t ob = row * DV + col0 + 4 * cg;
-      store_act(p.o, ob + 0, a * y.x + qk * u.x, p.out_bf16);
-      store_act(p.o, ob + 1, a * y.y + qk * u.y, p.out_bf16);
-      store_act(p.o, ob + 2, a * y.z + qk * u.z, p.out_bf16);
-      store_act(p.o, ob + 3, a * y.w + qk * u.w, p.out_bf16);
+      store_act(p.o, ob + 0, (a * y.x + qk * u.x) * inv, p.out_bf16);
+      store_act(p.o, ob + 1, (a * y.y + qk * u.y) * inv, p.out_bf16);
+      store_act(p.o, ob + 2, (a * y.z + qk * u.z) * inv, p.out_bf16);
+      store_act(p.o, ob + 3, (a * y.w + qk * u.w) * inv, p.out_bf16);
     }
     if (emit && conv && p.conv_dst) {
       release_history();
@@ -380,6 +405,8 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
             store_act(p.conv_dst, ((size_t)n * 3 + j) * p.Cch + chan(c), hr[i][j], p.in_bf16);
       }
     }
+    if (nla && half == 0 && p.z_dst)
+      for (int i = tid; i < DK; i += Sh::NT) p.z_dst[((size_t)n * p.H + h) * DK + i] = s_z[i];
   }
   release_history();
 }

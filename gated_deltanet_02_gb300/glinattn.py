@@ -21,7 +21,7 @@ import torch
 
 from . import build as _build
 
-GLA, GDN = 0, 1
+GLA, GDN, NLA = 0, 1, 2
 F32, BF16 = 0, 1
 
 DEV_BAD_SLOT = 0x1
@@ -50,7 +50,7 @@ class PrefillArgs(ctypes.Structure):
                 ("q", _vp), ("k", _vp), ("v", _vp), ("alpha", _vp), ("beta", _vp), ("S0", _vp),
                 ("S_T", _vp), ("o", _vp), ("conv_w", _vp), ("conv_in", _vp), ("conv_out", _vp),
                 ("dev_status", _vp), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
-                ("S_blocks", _vp), ("conv_blocks", _vp), ("qk_heads", _i32)]
+                ("S_blocks", _vp), ("conv_blocks", _vp), ("qk_heads", _i32), ("z0", _vp), ("z_T", _vp)]
 
 
 class DecodeArgs(ctypes.Structure):
@@ -59,7 +59,7 @@ class DecodeArgs(ctypes.Structure):
                 ("pool_slots", _i32), ("qk_heads", _i32),
                 ("q", _vp), ("k", _vp), ("v", _vp), ("alpha", _vp), ("beta", _vp),
                 ("state_pool", _vp), ("slot_ids", _vp), ("o", _vp), ("conv_w", _vp),
-                ("conv_pool", _vp), ("dev_status", _vp)]
+                ("conv_pool", _vp), ("dev_status", _vp), ("z_pool", _vp)]
 
 
 class SpecArgs(ctypes.Structure):
@@ -68,7 +68,8 @@ class SpecArgs(ctypes.Structure):
                 ("dv", _i32), ("pool_slots", _i32),
                 ("q", _vp), ("k", _vp), ("v", _vp), ("alpha", _vp), ("beta", _vp),
                 ("state_pool", _vp), ("src_slots", _vp), ("dst_slots", _vp), ("o", _vp),
-                ("conv_w", _vp), ("conv_pool", _vp), ("dev_status", _vp), ("qk_heads", _i32)]
+                ("conv_w", _vp), ("conv_pool", _vp), ("dev_status", _vp), ("qk_heads", _i32),
+                ("z_pool", _vp)]
 
 
 class ReplayArgs(ctypes.Structure):
@@ -77,7 +78,7 @@ class ReplayArgs(ctypes.Structure):
                 ("qk_heads", _i32),
                 ("q", _vp), ("k", _vp), ("v", _vp), ("alpha", _vp), ("beta", _vp),
                 ("state_pool", _vp), ("slot_ids", _vp), ("accept", _vp), ("conv_w", _vp),
-                ("conv_pool", _vp), ("dev_status", _vp)]
+                ("conv_pool", _vp), ("dev_status", _vp), ("z_pool", _vp)]
 
 
 class CopyArgs(ctypes.Structure):
@@ -154,7 +155,7 @@ def _call(name, args, stream_handle):
 def glinattn_prefill(q, k, v, alpha, beta=None, S0=None, *, variant=GLA, conv_w=None,
                      conv_in=None, qk_l2norm=False, out_dtype=None, o=None, S_T=None,
                      conv_out=None, dev_status=None, stream=None, workspace=None,
-                     state_every=0, S_blocks=None, conv_blocks=None):
+                     state_every=0, S_blocks=None, conv_blocks=None, z0=None, z_T=None):
     """Prefill one segment.  q, k [B,T,Hq,dk], v [B,T,H,dv] (bf16 or fp32;
     Hq < H shares q, k across groups of H // Hq heads);
     alpha/beta [B,T,H] fp32; S0 [B,H,dk,dv] fp32 or None.  Outputs, and the
@@ -162,7 +163,9 @@ def glinattn_prefill(q, k, v, alpha, beta=None, S0=None, *, variant=GLA, conv_w=
     not given.  Returns (o, S_T, conv_out); with state_every > 0 also
     S_blocks [B, T // state_every, H, dk, dv], the state after every
     state_every tokens of the segment, and conv_blocks [B, T // state_every,
-    3, Cch], the conv cache at the same points (None without a conv)."""
+    3, Cch], the conv cache at the same points (None without a conv).
+    variant=NLA (normalised linear attention: no gates, alpha may be None)
+    returns (o, S_T, None, z_T), the normaliser z [B,H,dk] beside the state."""
     B, T, Hq, dk = q.shape
     H, dv = v.shape[2], v.shape[3]
     dev = q.device
@@ -187,6 +190,12 @@ def glinattn_prefill(q, k, v, alpha, beta=None, S0=None, *, variant=GLA, conv_w=
         _need(conv_out, "conv_out", act, (B, 3, Cch), dev)
     _need(o, "o", out_dtype, (B, T, H, dv), dev)
     _need(S_T, "S_T", torch.float32, (B, H, dk, dv), dev)
+    nla = variant == NLA
+    if nla:
+        _need(z0, "z0", torch.float32, (B, H, dk), dev)
+        if z_T is None:
+            z_T = torch.empty((B, H, dk), dtype=torch.float32, device=dev)
+        _need(z_T, "z_T", torch.float32, (B, H, dk), dev)
     if state_every < 0:
         raise ValueError("state_every must be >= 0")
     nblk = T // state_every if state_every else 0
@@ -206,7 +215,8 @@ def glinattn_prefill(q, k, v, alpha, beta=None, S0=None, *, variant=GLA, conv_w=
                     S0=_ptr(S0), S_T=_ptr(S_T), o=_ptr(o), conv_w=_ptr(conv_w),
                     conv_in=_ptr(conv_in), conv_out=_ptr(conv_out), dev_status=_ptr(dev_status),
                     state_every=state_every, S_blocks=_ptr(S_blocks) if nblk else None,
-                    conv_blocks=_ptr(conv_blocks) if nblk else None, qk_heads=Hq)
+                    conv_blocks=_ptr(conv_blocks) if nblk else None, qk_heads=Hq,
+                    z0=_ptr(z0) if nla else None, z_T=_ptr(z_T) if nla else None)
     ws_bytes = library().glinattn_prefill_workspace_size(ctypes.byref(a))
     ws = None
     if ws_bytes:
@@ -217,6 +227,8 @@ def glinattn_prefill(q, k, v, alpha, beta=None, S0=None, *, variant=GLA, conv_w=
         a.workspace = _ptr(ws)
         a.workspace_bytes = ws_bytes
     _call("glinattn_prefill", a, _stream_handle(stream, dev))
+    if nla:
+        return o, S_T, None, z_T
     if state_every:
         return o, S_T, conv_out, S_blocks, conv_blocks
     return o, S_T, conv_out
@@ -224,7 +236,7 @@ def glinattn_prefill(q, k, v, alpha, beta=None, S0=None, *, variant=GLA, conv_w=
 
 def glinattn_decode(q, k, v, alpha, beta, state_pool, slot_ids, *, variant=GDN, conv_w=None,
                     conv_pool=None, qk_l2norm=False, out_dtype=None, o=None, dev_status=None,
-                    stream=None):
+                    stream=None, z_pool=None):
     """One decode step.  q, k [N,Hq,dk], v [N,H,dv]; alpha/beta [N,H];
     state_pool [P,H,dk,dv] fp32 and conv_pool [P,3,Cch] updated in place at
     slot_ids [N] int32.  Returns o [N,H,dv]."""
@@ -239,6 +251,7 @@ def glinattn_decode(q, k, v, alpha, beta, state_pool, slot_ids, *, variant=GDN, 
     _need(alpha, "alpha", torch.float32, (N, H), dev)
     _need(beta, "beta", torch.float32, (N, H), dev)
     _need(state_pool, "state_pool", torch.float32, (P, H, dk, dv), dev)
+    _need(z_pool, "z_pool", torch.float32, (P, H, dk), dev)
     _need(slot_ids, "slot_ids", torch.int32, (N,), dev)
     Cch = H * (2 * dk + dv)
     if conv_w is not None:
@@ -253,14 +266,14 @@ def glinattn_decode(q, k, v, alpha, beta, state_pool, slot_ids, *, variant=GDN, 
                    pool_slots=P, qk_heads=Hq, q=_ptr(q), k=_ptr(k), v=_ptr(v), alpha=_ptr(alpha),
                    beta=_ptr(beta), state_pool=_ptr(state_pool), slot_ids=_ptr(slot_ids),
                    o=_ptr(o), conv_w=_ptr(conv_w), conv_pool=_ptr(conv_pool) if conv_w is not None else None,
-                   dev_status=_ptr(dev_status))
+                   dev_status=_ptr(dev_status), z_pool=_ptr(z_pool))
     _call("glinattn_decode", a, _stream_handle(stream, dev))
     return o
 
 
 def glinattn_spec_decode(q, k, v, alpha, beta, state_pool, src_slots, dst_slots, *, variant=GDN,
                          conv_w=None, conv_pool=None, qk_l2norm=False, out_dtype=None, o=None,
-                         dev_status=None, stream=None):
+                         dev_status=None, stream=None, z_pool=None):
     """D draft steps per request.  q, k [N,D,Hq,dk], v [N,D,H,dv];
     alpha/beta [N,D,H]; src_slots [N], dst_slots [N,D] int32.  The state after
     draft i is written to state_pool[dst_slots[n, i]]; dst_slots=None only
@@ -277,6 +290,7 @@ def glinattn_spec_decode(q, k, v, alpha, beta, state_pool, src_slots, dst_slots,
     _need(alpha, "alpha", torch.float32, (N, D, H), dev)
     _need(beta, "beta", torch.float32, (N, D, H), dev)
     _need(state_pool, "state_pool", torch.float32, (P, H, dk, dv), dev)
+    _need(z_pool, "z_pool", torch.float32, (P, H, dk), dev)
     _need(src_slots, "src_slots", torch.int32, (N,), dev)
     _need(dst_slots, "dst_slots", torch.int32, (N, D), dev)
     Cch = H * (2 * dk + dv)
@@ -293,13 +307,14 @@ def glinattn_spec_decode(q, k, v, alpha, beta, state_pool, src_slots, dst_slots,
                  beta=_ptr(beta), state_pool=_ptr(state_pool), src_slots=_ptr(src_slots),
                  dst_slots=_ptr(dst_slots),
                  o=_ptr(o), conv_w=_ptr(conv_w), conv_pool=_ptr(conv_pool) if conv_w is not None else None,
-                 dev_status=_ptr(dev_status))
+                 dev_status=_ptr(dev_status), z_pool=_ptr(z_pool))
     _call("glinattn_spec_decode", a, _stream_handle(stream, dev))
     return o
 
 
 def glinattn_replay(k, v, alpha, beta, state_pool, slot_ids, accept, *, q=None, variant=GDN,
-                    conv_w=None, conv_pool=None, qk_l2norm=False, dev_status=None, stream=None):
+                    conv_w=None, conv_pool=None, qk_l2norm=False, dev_status=None, stream=None,
+                    z_pool=None):
     """Apply the first accept[n] recorded draft steps to state_pool[slot_ids[n]]
     (and its conv cache) in place.  k [N,D,Hq,dk], v [N,D,H,dv], alpha/beta
     [N,D,H], q [N,D,Hq,dk] (its raw values enter the conv cache; defaults to k
@@ -319,6 +334,7 @@ def glinattn_replay(k, v, alpha, beta, state_pool, slot_ids, accept, *, q=None, 
     _need(alpha, "alpha", torch.float32, (N, D, H), dev)
     _need(beta, "beta", torch.float32, (N, D, H), dev)
     _need(state_pool, "state_pool", torch.float32, (P, H, dk, dv), dev)
+    _need(z_pool, "z_pool", torch.float32, (P, H, dk), dev)
     _need(slot_ids, "slot_ids", torch.int32, (N,), dev)
     _need(accept, "accept", torch.int32, (N,), dev)
     Cch = H * (2 * dk + dv)
@@ -330,7 +346,8 @@ def glinattn_replay(k, v, alpha, beta, state_pool, slot_ids, accept, *, q=None, 
                    v=_ptr(v),
                    alpha=_ptr(alpha), beta=_ptr(beta), state_pool=_ptr(state_pool), slot_ids=_ptr(slot_ids),
                    accept=_ptr(accept), conv_w=_ptr(conv_w),
-                   conv_pool=_ptr(conv_pool) if conv_w is not None else None, dev_status=_ptr(dev_status))
+                   conv_pool=_ptr(conv_pool) if conv_w is not None else None, dev_status=_ptr(dev_status),
+                   z_pool=_ptr(z_pool))
     _call("glinattn_replay", a, _stream_handle(stream, dev))
     return state_pool
 

@@ -26,6 +26,9 @@ measured on; "N(m, s)" means mean m, standard deviation s):
   attention: G groups of q / k heads (C and B) of size d_k = 128 (the state
   size) shared by H heads of value size d_v = 64 (the head dim); q, k ~
   N(0,1)/sqrt(d_k), v ~ N(0,1) in bf16, alpha = sigmoid(N(0,1) + 3).
+* ``nla_prefill`` / ``nla_decode`` -- normalised kernelised linear attention:
+  raw q, k, v ~ N(0,1) (the feature map is applied inside the layer); a start
+  state ~ N(0, 0.05) and a positive start normaliser |N(0,1)| * 8 when asked.
 """
 from __future__ import annotations
 
@@ -140,6 +143,33 @@ def ssd_decode(N, H, G, P, dk=128, dv=64, seed=0, device="cpu", dtype=torch.bflo
     v = _randn(lead + (H, dv), g, device, 1.0, dtype)
     alpha = torch.sigmoid(_randn(lead + (H,), g, device) + 3.0)
     return dict(q=q, k=k, v=v, alpha=alpha, beta=None, pool=pool, slot_ids=slot_ids, perm=perm)
+
+
+def nla_prefill(B, H, T, d, Hq=None, seed=0, device="cpu", dtype=torch.bfloat16, start=False, dv=None):
+    g = _gen(seed, device)
+    Hq = H if Hq is None else Hq
+    dv = d if dv is None else dv
+    q = _randn((B, T, Hq, d), g, device, 1.0, dtype)
+    k = _randn((B, T, Hq, d), g, device, 1.0, dtype)
+    v = _randn((B, T, H, dv), g, device, 1.0, dtype)
+    S0 = _randn((B, H, d, dv), g, device, 0.05) if start else None
+    z0 = _randn((B, H, d), g, device).abs() * 8.0 if start else None
+    return dict(q=q, k=k, v=v, alpha=None, beta=None, S0=S0, z0=z0)
+
+
+def nla_decode(N, H, d, P, Hq=None, seed=0, device="cpu", dtype=torch.bfloat16, D=None):
+    """One token (D=None) or D draft tokens per request; pools of P states and
+    positive normalisers."""
+    g = _gen(seed, device)
+    Hq = H if Hq is None else Hq
+    pool = _randn((P, H, d, d), g, device, 0.05)
+    zpool = _randn((P, H, d), g, device).abs() * 8.0
+    perm = torch.randperm(P, generator=g, device=device)
+    lead = (N,) if D is None else (N, D)
+    q = _randn(lead + (Hq, d), g, device, 1.0, dtype)
+    k = _randn(lead + (Hq, d), g, device, 1.0, dtype)
+    v = _randn(lead + (H, d), g, device, 1.0, dtype)
+    return dict(q=q, k=k, v=v, pool=pool, zpool=zpool, slot_ids=perm[:N].to(torch.int32), perm=perm)
 
 
 def segment_lengths(T: int, fractions=(0.20, 0.35)):

@@ -71,7 +71,17 @@ typedef enum {
   GLINATTN_ERR_TIMEOUT = 5      /* reserved: a bounded device wait gave up */
 } glinattn_status;
 
-typedef enum { GLINATTN_GLA = 0, GLINATTN_GDN = 1 } glinattn_variant;
+/*
+ * GLINATTN_NLA: normalised kernelised linear attention ("Long context, fast
+ * inference, smart decoding, and life beyond attention", section "Linear
+ * attention: removing softmax entirely"): with phi(x) = elu(x) + 1 applied to
+ * q and k inside the layer,
+ *   S_t = S_{t-1} + phi(k_t)^T v_t,  z_t = z_{t-1} + phi(k_t),
+ *   o_t = phi(q_t) S_t / (phi(q_t) . z_t + 1e-6).
+ * No gates (alpha and beta are ignored and may be NULL), no convolution, no
+ * L2 norm; the normaliser z [.., H, dk] fp32 travels beside the state.
+ */
+typedef enum { GLINATTN_GLA = 0, GLINATTN_GDN = 1, GLINATTN_NLA = 2 } glinattn_variant;
 typedef enum { GLINATTN_F32 = 0, GLINATTN_BF16 = 1 } glinattn_dtype;
 
 /* Bits OR-ed into *dev_status by the kernels. */
@@ -136,6 +146,8 @@ typedef struct {
   float *S_blocks;        /* [B, T / state_every, H, dk, dv] fp32 when state_every > 0 */
   void *conv_blocks;      /* [B, T / state_every, 3, Cch] (in_dtype) or NULL */
   int32_t qk_heads;       /* q / k heads Hq (0: Hq = H), see "Grouped q / k heads" above */
+  const float *z0;        /* GLINATTN_NLA: normaliser in [B, H, dk] fp32, or NULL (zeros) */
+  float *z_T;             /* GLINATTN_NLA: normaliser out [B, H, dk] fp32 (may alias z0) */
 } glinattn_prefill_args;
 
 glinattn_status glinattn_prefill(const glinattn_prefill_args *args, glinattn_stream_t stream);
@@ -206,6 +218,7 @@ typedef struct {
   const float *conv_w;
   void *conv_pool;
   uint32_t *dev_status;
+  float *z_pool; /* GLINATTN_NLA: normalisers [P, H, dk] fp32, indexed like state_pool */
 } glinattn_decode_args;
 
 glinattn_status glinattn_decode(const glinattn_decode_args *args, glinattn_stream_t stream);
@@ -241,6 +254,7 @@ typedef struct {
   void *conv_pool;
   uint32_t *dev_status;
   int32_t qk_heads; /* q / k heads Hq (0: Hq = H) */
+  float *z_pool; /* GLINATTN_NLA: normalisers [P, H, dk] fp32, indexed like state_pool */
 } glinattn_spec_args;
 
 glinattn_status glinattn_spec_decode(const glinattn_spec_args *args, glinattn_stream_t stream);
@@ -275,6 +289,7 @@ typedef struct {
   const float *conv_w;
   void *conv_pool;
   uint32_t *dev_status;
+  float *z_pool; /* GLINATTN_NLA: normalisers [P, H, dk] fp32, indexed like state_pool */
 } glinattn_replay_args;
 
 glinattn_status glinattn_replay(const glinattn_replay_args *args, glinattn_stream_t stream);

@@ -117,6 +117,11 @@ INVALID, UNSUPPORTED = 1, 2
     (dict(qk_heads=3), INVALID),         # does not divide heads = 4
     (dict(qk_heads=-1), INVALID),
     (dict(qk_heads=2, conv_w=A * 9), UNSUPPORTED),  # grouped heads take no convolution
+    (dict(variant=3), INVALID),
+    (dict(variant=G.NLA, qk_l2norm=0, z_T=None), INVALID),   # the normaliser must go somewhere
+    (dict(variant=G.NLA, qk_l2norm=0, z_T=A * 10, conv_w=A * 9), UNSUPPORTED),
+    (dict(variant=G.NLA, qk_l2norm=0, z_T=A * 10, state_every=64, S_blocks=A * 11), UNSUPPORTED),
+    (dict(variant=G.NLA, qk_l2norm=0, z_T=A * 10 + 4), INVALID),
     (dict(heads=0), INVALID),
     (dict(batch=-1), INVALID),
     (dict(seqlen=-5), INVALID),
@@ -153,6 +158,8 @@ def test_prefill_null_args_and_empty_batch():
     (dict(num_req=-1), INVALID),
     (dict(qk_heads=3), INVALID),
     (dict(qk_heads=1, conv_w=A * 9, conv_pool=A * 10), UNSUPPORTED),
+    (dict(variant=G.NLA, qk_l2norm=0), INVALID),              # no normaliser pool
+    (dict(variant=G.NLA, z_pool=A * 11, conv_w=A * 9, conv_pool=A * 10), UNSUPPORTED),
 ])
 def test_decode_rejects(kw, code):
     assert G.library().glinattn_decode(ctypes.byref(_decode(**kw)), None) == code

@@ -1,0 +1,124 @@
+"""GPU parity of normalised kernelised linear attention against the oracle.
+
+"Long context, fast inference, smart decoding, and life beyond attention",
+section "Linear attention: removing softmax entirely": phi = elu + 1 on q and
+k, a running state S and normaliser z, o = phi(q) S / (phi(q) . z + 1e-6).
+Prefill (chunked and token-serial), segments handing (S, z) on, decode,
+speculative decode and replay are checked.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gated_deltanet_02_gb300 import (NLA, glinattn_decode, glinattn_prefill, glinattn_replay,
+                                     glinattn_spec_decode, inputs)
+from oracle.normalized import nla_decode, nla_prefill, nla_spec_decode
+
+from helpers import TOL_F32, TOL_O_BF16, TOL_S_BF16, f64, relerr, to
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def _prefill(g, S0=None, z0=None, out_dtype=torch.float32):
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o, S, _, z = glinattn_prefill(g["q"], g["k"], g["v"], None, None, S0, variant=NLA, z0=z0,
+                                  out_dtype=out_dtype, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return o, S, z
+
+
+def _ref(ex, start=True):
+    return nla_prefill(f64(ex["q"]), f64(ex["k"]), f64(ex["v"]), f64(ex["S0"]) if start else None,
+                       f64(ex["z0"]) if start else None, act_bf16=ex["q"].dtype == torch.bfloat16)
+
+
+@pytest.mark.parametrize("d,Hq", [(16, 2), (64, 2), (128, 2), (128, 1)])
+def test_nla_prefill_fp32(d, Hq):
+    ex = inputs.nla_prefill(2, 2, 77, d, Hq=Hq, seed=d + Hq, dtype=torch.float32, start=True)
+    g = to(ex, DEV)
+    o, S, z = _prefill(g, g["S0"], g["z0"])
+    o_ref, S_ref, z_ref = _ref(ex)
+    assert relerr(o, o_ref) <= TOL_F32 and relerr(S, S_ref) <= TOL_F32 and relerr(z, z_ref) <= TOL_F32
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 200, 300])
+def test_nla_prefill_bf16(T):
+    ex = inputs.nla_prefill(2, 3, T, 128, seed=T, start=T % 2 == 0)
+    g = to(ex, DEV)
+    start = T % 2 == 0
+    o, S, z = _prefill(g, g["S0"], g["z0"])
+    o_ref, S_ref, z_ref = _ref(ex, start)
+    assert relerr(o, o_ref) <= TOL_O_BF16
+    assert relerr(S, S_ref) <= TOL_S_BF16 and relerr(z, z_ref) <= TOL_S_BF16
+
+
+def test_nla_segments_hand_state_and_normaliser_on():
+    T = 333
+    ex = inputs.nla_prefill(1, 2, T, 128, seed=4)
+    g = to(ex, DEV)
+    S, z, outs = None, None, []
+    for s, e in ((0, 70), (70, 72), (72, T)):
+        seg = {key: (val[:, s:e].contiguous() if key in ("q", "k", "v") else val) for key, val in g.items()}
+        o, S, z = _prefill(seg, S, z)
+        outs.append(o)
+    o_ref, S_ref, z_ref = _ref(ex, start=False)
+    assert relerr(torch.cat(outs, 1), o_ref) <= TOL_O_BF16
+    assert relerr(S, S_ref) <= TOL_S_BF16 and relerr(z, z_ref) <= TOL_S_BF16
+
+
+@pytest.mark.parametrize("d,dtype", [(64, torch.bfloat16), (128, torch.bfloat16), (128, torch.float32)])
+def test_nla_decode(d, dtype):
+    N, H, P = 10, 3, 24
+    dx = inputs.nla_decode(N, H, d, P, seed=d, dtype=dtype)
+    g = to(dx, DEV)
+    pool, zpool = g["pool"].clone(), g["zpool"].clone()
+    o = glinattn_decode(g["q"], g["k"], g["v"], None, None, pool, g["slot_ids"], variant=NLA, z_pool=zpool,
+                        out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    o_ref, pool_ref, zpool_ref = nla_decode(f64(dx["q"]), f64(dx["k"]), f64(dx["v"]), f64(dx["pool"]),
+                                            f64(dx["zpool"]), dx["slot_ids"].tolist(),
+                                            act_bf16=dtype == torch.bfloat16)
+    tol_o, tol_s = (TOL_O_BF16, TOL_S_BF16) if dtype == torch.bfloat16 else (TOL_F32, TOL_F32)
+    sl = dx["slot_ids"].long()
+    assert relerr(o, o_ref) <= tol_o
+    assert relerr(pool[sl.to(DEV)], pool_ref[sl.numpy()]) <= tol_s
+    assert relerr(zpool[sl.to(DEV)], zpool_ref[sl.numpy()]) <= tol_s
+    untouched = torch.ones(P, dtype=torch.bool)
+    untouched[sl] = False
+    assert torch.equal(zpool.cpu()[untouched], dx["zpool"][untouched])
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_nla_spec_decode_and_replay(d):
+    N, D, H = 5, 4, 2
+    P = N * (1 + D)
+    dx = inputs.nla_decode(N, H, d, P, seed=11 + d, D=D)
+    g = to(dx, DEV)
+    src = dx["perm"][:N].to(torch.int32)
+    dst = dx["perm"][N:N + N * D].to(torch.int32).reshape(N, D)
+    pool, zpool = g["pool"].clone(), g["zpool"].clone()
+    o = glinattn_spec_decode(g["q"], g["k"], g["v"], None, None, pool, src.to(DEV), dst.to(DEV), variant=NLA,
+                             z_pool=zpool, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    o_ref, pool_ref, zpool_ref = nla_spec_decode(f64(dx["q"]), f64(dx["k"]), f64(dx["v"]), f64(dx["pool"]),
+                                                 f64(dx["zpool"]), src.tolist(), dst.tolist())
+    dl = dst.long()
+    assert relerr(o, o_ref) <= TOL_O_BF16
+    assert relerr(pool[dl.to(DEV)], pool_ref[dl.numpy()]) <= TOL_S_BF16
+    assert relerr(zpool[dl.to(DEV)], zpool_ref[dl.numpy()]) <= TOL_S_BF16
+    # verify only + replay lands on the per-draft states bit for bit
+    pool2, zpool2 = g["pool"].clone(), g["zpool"].clone()
+    o2 = glinattn_spec_decode(g["q"], g["k"], g["v"], None, None, pool2, src.to(DEV), None, variant=NLA,
+                              z_pool=zpool2, out_dtype=torch.float32)
+    accept = torch.tensor([0, 4, 1, 3, 2], dtype=torch.int32)
+    glinattn_replay(g["k"], g["v"], None, None, pool2, src.to(DEV), accept.to(DEV), q=g["q"], variant=NLA,
+                    z_pool=zpool2)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2)
+    for n, a in enumerate(accept.tolist()):
+        s = int(src[n])
+        want_S = g["pool"][s] if a == 0 else pool[int(dst[n, a - 1])]
+        want_z = g["zpool"][s] if a == 0 else zpool[int(dst[n, a - 1])]
+        assert torch.equal(pool2[s], want_S) and torch.equal(zpool2[s], want_z), (n, a)
