@@ -123,6 +123,9 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
   if (tc_device && glinattn::gdn_tc_supports(*a) &&
       (!a->workspace || a->workspace_bytes < glinattn::gdn_tc_workspace_bytes(*a) || !aligned16(a->workspace)))
     return GLINATTN_ERR_INVALID_ARG;
+  if (tc_device && glinattn::nla_tc_supports(*a) &&
+      (!a->workspace || a->workspace_bytes < glinattn::nla_tc_workspace_bytes(*a) || !aligned16(a->workspace)))
+    return GLINATTN_ERR_INVALID_ARG;
   // conv caches at the block boundaries: taken before the layer runs, since
   // conv_out may alias conv_in
   const bool conv_blocks = a->conv_w && a->conv_blocks && emit_blocks;
@@ -134,6 +137,7 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
   if (tc_device) {
     if (glinattn::prefill_tc_supports(*a)) return glinattn::launch_prefill_tc(*a, (cudaStream_t)stream);
     if (glinattn::gdn_tc_supports(*a)) return glinattn::launch_gdn_tc(*a, (cudaStream_t)stream);
+    if (glinattn::nla_tc_supports(*a)) return glinattn::launch_nla_tc(*a, (cudaStream_t)stream);
   }
 
   RecurParams p = {};
@@ -172,6 +176,7 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
 size_t glinattn_prefill_workspace_size(const glinattn_prefill_args *a) {
   if (!a || a->batch <= 0 || a->seqlen <= 0 || a->heads <= 0) return 0;
   if (check_common(a->variant, a->in_dtype, a->out_dtype, a->dk, a->dv, a->heads) != GLINATTN_OK) return 0;
+  if (glinattn::nla_tc_supports(*a)) return glinattn::nla_tc_workspace_bytes(*a);
   if (!glinattn::gdn_tc_supports(*a)) return 0;
   return glinattn::gdn_tc_workspace_bytes(*a);
 }

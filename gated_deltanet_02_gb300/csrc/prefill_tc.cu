@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- the unit is skipped when a gate is outside (0, 1] ---------------------
   {
     int bad = 0;
-    for (int t = tid; t < T; t += kThreads) {
+    for (int t = tid; t < T && p.alpha; t += kThreads) {  // no gates: alpha = 1
       const float a = p.alpha[((size_t)b * T + t) * p.H + h];
       bad |= !(a > 0.f && a <= 1.f);
     }
@@ -190,8 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // lane l holds the alphas of tokens 2l and 2l + 1 of the next chunk
     auto alphas = [&](int c, float &a0, float &a1) {
       const int ta = c * kC + 2 * lane, tb2 = ta + 1;
-      a0 = ta < T ? p.alpha[((size_t)b * T + ta) * p.H + h] : 1.f;
-      a1 = tb2 < T ? p.alpha[((size_t)b * T + tb2) * p.H + h] : 1.f;
+      a0 = ta < T && p.alpha ? p.alpha[((size_t)b * T + ta) * p.H + h] : 1.f;
+      a1 = tb2 < T && p.alpha ? p.alpha[((size_t)b * T + tb2) * p.H + h] : 1.f;
     };
     float a0n, a1n;
     alphas(0, a0n, a1n);

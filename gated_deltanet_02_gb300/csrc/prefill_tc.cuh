@@ -23,6 +23,12 @@ bool gdn_tc_supports(const glinattn_prefill_args &a);
 size_t gdn_tc_workspace_bytes(const glinattn_prefill_args &a);
 glinattn_status launch_gdn_tc(const glinattn_prefill_args &a, cudaStream_t stream);
 
+// Chunked normalised linear attention (features, gate-free chunked numerator,
+// normalisation) through a caller-provided workspace.
+bool nla_tc_supports(const glinattn_prefill_args &a);
+size_t nla_tc_workspace_bytes(const glinattn_prefill_args &a);
+glinattn_status launch_nla_tc(const glinattn_prefill_args &a, cudaStream_t stream);
+
 // [B, T, H, d] bf16 activations as a 4-D map (d, H, T, B); box 64 x 1 x 64 x 1
 // (64 channels of one head for 64 tokens), 128-byte swizzle.
 bool make_act_map(CUtensorMap *m, const void *base, int B, int T, int H, int d);

@@ -122,3 +122,42 @@ def test_nla_spec_decode_and_replay(d):
         want_S = g["pool"][s] if a == 0 else pool[int(dst[n, a - 1])]
         want_z = g["zpool"][s] if a == 0 else zpool[int(dst[n, a - 1])]
         assert torch.equal(pool2[s], want_S) and torch.equal(zpool2[s], want_z), (n, a)
+
+
+def test_nla_chunked_grouped_head_dim_64():
+    """Chunked path with two q / k heads for four heads of value size 64."""
+    ex = inputs.nla_prefill(2, 4, 150, 128, Hq=2, dv=64, seed=31, start=True)
+    g = to(ex, DEV)
+    o, S, z = _prefill(g, g["S0"], g["z0"])
+    o_ref, S_ref, z_ref = _ref(ex)
+    assert relerr(o, o_ref) <= TOL_O_BF16
+    assert relerr(S, S_ref) <= TOL_S_BF16 and relerr(z, z_ref) <= TOL_S_BF16
+
+
+def test_nla_bf16_output_and_normaliser_in_place():
+    """bf16 outputs (one rounding of the normalised value), z_T over z0."""
+    ex = inputs.nla_prefill(1, 2, 190, 128, seed=32, start=True)
+    g = to(ex, DEV)
+    z = g["z0"].clone()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o, S, _, z_out = glinattn_prefill(g["q"], g["k"], g["v"], None, None, g["S0"], variant=NLA, z0=z, z_T=z,
+                                      out_dtype=torch.bfloat16, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and z_out.data_ptr() == z.data_ptr()
+    o_ref, S_ref, z_ref = _ref(ex)
+    err = np.abs(f64(o) - o_ref)
+    assert (err <= np.abs(o_ref) * 2.0 ** -8 + TOL_O_BF16 * np.abs(o_ref).max()).all()
+    assert relerr(z, z_ref) <= TOL_S_BF16
+
+
+def test_nla_full_size_sampled():
+    """B=4, H=16, T=4096, d=128 (the gated linear attention prefill shape);
+    units (0, 0) and (3, 15) in full."""
+    ex = inputs.nla_prefill(4, 16, 4096, 128, seed=0, device=DEV)
+    o, S, z = _prefill(ex)
+    for b, h in ((0, 0), (3, 15)):
+        sub = {key: ex[key][b:b + 1, :, h:h + 1] for key in ("q", "k", "v")}
+        o_ref, S_ref, z_ref = nla_prefill(f64(sub["q"]), f64(sub["k"]), f64(sub["v"]))
+        assert relerr(o[b:b + 1, :, h:h + 1], o_ref) <= TOL_O_BF16, (b, h)
+        assert relerr(S[b:b + 1, h:h + 1], S_ref) <= TOL_S_BF16, (b, h)
+        assert relerr(z[b:b + 1, h:h + 1], z_ref) <= TOL_S_BF16, (b, h)
