@@ -11,6 +11,8 @@ The three entry points keep the C names:
 * ``glinattn_spec_decode`` -- D draft steps, one state per draft position
 * ``glinattn_replay``      -- apply the accepted drafts to the pool in place
 * ``glinattn_state_copy``  -- whole-slot copies inside a state pool (copy on write)
+* ``glinattn_selective_scan`` / ``glinattn_selective_scan_decode`` -- Mamba's
+  selective scan (chunked prefill; one step from a slot-indexed pool)
 """
 from __future__ import annotations
 
@@ -81,6 +83,19 @@ class ReplayArgs(ctypes.Structure):
                 ("conv_pool", _vp), ("dev_status", _vp), ("z_pool", _vp)]
 
 
+class ScanArgs(ctypes.Structure):
+    _fields_ = [("in_dtype", _i32), ("out_dtype", _i32), ("batch", _i32), ("seqlen", _i32),
+                ("channels", _i32), ("state", _i32), ("x", _vp), ("delta", _vp), ("Bm", _vp), ("Cm", _vp),
+                ("A", _vp), ("h0", _vp), ("h_T", _vp), ("y", _vp), ("workspace", _vp),
+                ("workspace_bytes", ctypes.c_size_t), ("dev_status", _vp)]
+
+
+class ScanDecodeArgs(ctypes.Structure):
+    _fields_ = [("in_dtype", _i32), ("out_dtype", _i32), ("num_req", _i32), ("channels", _i32),
+                ("state", _i32), ("pool_slots", _i32), ("x", _vp), ("delta", _vp), ("Bm", _vp), ("Cm", _vp),
+                ("A", _vp), ("state_pool", _vp), ("slot_ids", _vp), ("y", _vp), ("dev_status", _vp)]
+
+
 class CopyArgs(ctypes.Structure):
     _fields_ = [("n", _i32), ("pool_slots", _i32), ("heads", _i32), ("dk", _i32), ("dv", _i32),
                 ("in_dtype", _i32), ("state_pool", _vp), ("conv_pool", _vp), ("src_slots", _vp),
@@ -100,7 +115,8 @@ def library() -> ctypes.CDLL:
             lib = ctypes.CDLL(path)
             for name, argt in (("glinattn_prefill", PrefillArgs), ("glinattn_decode", DecodeArgs),
                                ("glinattn_spec_decode", SpecArgs), ("glinattn_replay", ReplayArgs),
-                               ("glinattn_state_copy", CopyArgs)):
+                               ("glinattn_state_copy", CopyArgs), ("glinattn_selective_scan", ScanArgs),
+                               ("glinattn_selective_scan_decode", ScanDecodeArgs)):
                 f = getattr(lib, name)
                 f.argtypes = [ctypes.POINTER(argt), _vp]
                 f.restype = ctypes.c_int
@@ -111,6 +127,8 @@ def library() -> ctypes.CDLL:
             lib.glinattn_state_bytes.restype = ctypes.c_size_t
             lib.glinattn_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs)]
             lib.glinattn_prefill_workspace_size.restype = ctypes.c_size_t
+            lib.glinattn_selective_scan_workspace_size.argtypes = [ctypes.POINTER(ScanArgs)]
+            lib.glinattn_selective_scan_workspace_size.restype = ctypes.c_size_t
             _lib = lib
     return _lib
 
@@ -373,6 +391,69 @@ def glinattn_state_copy(state_pool, src_slots, dst_slots, *, conv_pool=None, dev
                  dst_slots=_ptr(dst_slots), dev_status=_ptr(dev_status))
     _call("glinattn_state_copy", a, _stream_handle(stream, dev))
     return state_pool
+
+
+def glinattn_selective_scan(x, delta, Bm, Cm, A, h0=None, *, out_dtype=None, y=None, h_T=None,
+                            workspace=None, dev_status=None, stream=None):
+    """Mamba's selective scan over a segment.  x, delta [B,T,D], Bm, Cm
+    [B,T,N] (bf16 or fp32); A [D,N] fp32; h0 [B,D,N] fp32 or None.  Returns
+    (y [B,T,D], h_T [B,D,N])."""
+    B, T, D = x.shape
+    N = Bm.shape[-1]
+    dev = x.device
+    act = x.dtype
+    _need(x, "x", act, (B, T, D), dev)
+    _need(delta, "delta", act, (B, T, D), dev)
+    _need(Bm, "Bm", act, (B, T, N), dev)
+    _need(Cm, "Cm", act, (B, T, N), dev)
+    _need(A, "A", torch.float32, (D, N), dev)
+    _need(h0, "h0", torch.float32, (B, D, N), dev)
+    out_dtype = act if out_dtype is None else out_dtype
+    if y is None:
+        y = torch.empty((B, T, D), dtype=out_dtype, device=dev)
+    if h_T is None:
+        h_T = torch.empty((B, D, N), dtype=torch.float32, device=dev)
+    _need(y, "y", out_dtype, (B, T, D), dev)
+    _need(h_T, "h_T", torch.float32, (B, D, N), dev)
+    a = ScanArgs(in_dtype=_dtype_code(x), out_dtype=_dtype_code(y), batch=B, seqlen=T, channels=D, state=N,
+                 x=_ptr(x), delta=_ptr(delta), Bm=_ptr(Bm), Cm=_ptr(Cm), A=_ptr(A), h0=_ptr(h0), h_T=_ptr(h_T),
+                 y=_ptr(y), dev_status=_ptr(dev_status))
+    need = library().glinattn_selective_scan_workspace_size(ctypes.byref(a))
+    if need:
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        a.workspace = _ptr(workspace)
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
+    _call("glinattn_selective_scan", a, _stream_handle(stream, dev))
+    return y, h_T
+
+
+def glinattn_selective_scan_decode(x, delta, Bm, Cm, A, state_pool, slot_ids, *, out_dtype=None, y=None,
+                                   dev_status=None, stream=None):
+    """One selective-scan step for R requests: x, delta [R,D], Bm, Cm [R,N];
+    state_pool [P,D,N] fp32 updated in place at slot_ids [R] int32.  Returns y [R,D]."""
+    R, D = x.shape
+    N = Bm.shape[-1]
+    P = state_pool.shape[0]
+    dev = x.device
+    act = x.dtype
+    _need(x, "x", act, (R, D), dev)
+    _need(delta, "delta", act, (R, D), dev)
+    _need(Bm, "Bm", act, (R, N), dev)
+    _need(Cm, "Cm", act, (R, N), dev)
+    _need(A, "A", torch.float32, (D, N), dev)
+    _need(state_pool, "state_pool", torch.float32, (P, D, N), dev)
+    _need(slot_ids, "slot_ids", torch.int32, (R,), dev)
+    out_dtype = act if out_dtype is None else out_dtype
+    if y is None:
+        y = torch.empty((R, D), dtype=out_dtype, device=dev)
+    _need(y, "y", out_dtype, (R, D), dev)
+    a = ScanDecodeArgs(in_dtype=_dtype_code(x), out_dtype=_dtype_code(y), num_req=R, channels=D, state=N,
+                       pool_slots=P, x=_ptr(x), delta=_ptr(delta), Bm=_ptr(Bm), Cm=_ptr(Cm), A=_ptr(A),
+                       state_pool=_ptr(state_pool), slot_ids=_ptr(slot_ids), y=_ptr(y),
+                       dev_status=_ptr(dev_status))
+    _call("glinattn_selective_scan_decode", a, _stream_handle(stream, dev))
+    return y
 
 
 def version() -> int:

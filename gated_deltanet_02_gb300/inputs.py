@@ -26,6 +26,8 @@ measured on; "N(m, s)" means mean m, standard deviation s):
   attention: G groups of q / k heads (C and B) of size d_k = 128 (the state
   size) shared by H heads of value size d_v = 64 (the head dim); q, k ~
   N(0,1)/sqrt(d_k), v ~ N(0,1) in bf16, alpha = sigmoid(N(0,1) + 3).
+* ``selective_scan_inputs`` -- Mamba's selective scan: x ~ N(0,1), delta ~
+  N(-2,1), B, C ~ N(0,1), A = -exp(U(0,1)), h0 ~ N(0, 0.1) when asked.
 * ``nla_prefill`` / ``nla_decode`` -- normalised kernelised linear attention:
   raw q, k, v ~ N(0,1) (the feature map is applied inside the layer); a start
   state ~ N(0, 0.05) and a positive start normaliser |N(0,1)| * 8 when asked.
@@ -170,6 +172,20 @@ def nla_decode(N, H, d, P, Hq=None, seed=0, device="cpu", dtype=torch.bfloat16, 
     k = _randn(lead + (Hq, d), g, device, 1.0, dtype)
     v = _randn(lead + (H, d), g, device, 1.0, dtype)
     return dict(q=q, k=k, v=v, pool=pool, zpool=zpool, slot_ids=perm[:N].to(torch.int32), perm=perm)
+
+
+def selective_scan_inputs(B, T, D, N, seed=0, device="cpu", dtype=torch.float32, start=False):
+    """Mamba's selective scan: x ~ N(0,1), delta ~ N(-2,1) (softplus(delta)
+    mostly in 0.05..0.5), B, C ~ N(0,1), A = -exp(U(0,1)) per channel and state
+    index (the stable construction of the page's block); h0 ~ N(0, 0.1)."""
+    g = _gen(seed, device)
+    x = _randn((B, T, D), g, device, 1.0, dtype)
+    delta = (_randn((B, T, D), g, device) - 2.0).to(dtype)
+    Bm = _randn((B, T, N), g, device, 1.0, dtype)
+    Cm = _randn((B, T, N), g, device, 1.0, dtype)
+    A = -torch.exp(torch.rand((D, N), generator=g, device=device))
+    h0 = _randn((B, D, N), g, device, 0.1) if start else None
+    return dict(x=x, delta=delta, Bm=Bm, Cm=Cm, A=A, h0=h0)
 
 
 def segment_lengths(T: int, fractions=(0.20, 0.35)):

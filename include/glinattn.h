@@ -322,6 +322,64 @@ typedef struct {
 
 glinattn_status glinattn_state_copy(const glinattn_copy_args *args, glinattn_stream_t stream);
 
+/*
+ * glinattn_selective_scan -- Mamba's selective state-space scan over one
+ *   segment ("Long context, fast inference, smart decoding, and life beyond
+ *   attention", chapter "05 · State-space models: the architectural
+ *   alternative", section "Mamba: making the recurrence input-dependent, and
+ *   the engineering that makes that fast anyway").  For channel d and state
+ *   index n, with dt = softplus(delta) = log(1 + e^delta):
+ *     h_t[d, n] = exp(dt_t[d] A[d, n]) h_{t-1}[d, n] + dt_t[d] Bm_t[n] x_t[d]
+ *     y_t[d]    = sum_n h_t[d, n] Cm_t[n]
+ *   The projections producing delta, Bm and Cm are the caller's; the scan
+ *   applies the softplus.  All arithmetic is fp32.
+ *
+ *   x, delta [B, T, D] and Bm, Cm [B, T, N]   (in_dtype)
+ *   A [D, N] fp32     h0 [B, D, N] fp32 or NULL (zeros)
+ *   h_T [B, D, N] fp32 output (may alias h0 exactly)     y [B, T, D] (out_dtype)
+ *   N (state) in {8, 16, 32}; any D >= 1.  T == 0 copies h0 to h_T.
+ *   workspace: at least glinattn_selective_scan_workspace_size() bytes (the
+ *   chunk end states, step sums and start states), 16-byte aligned.
+ */
+typedef struct {
+  int32_t in_dtype, out_dtype;
+  int32_t batch, seqlen, channels, state;
+  const void *x, *delta, *Bm, *Cm;
+  const float *A;
+  const float *h0;
+  float *h_T;
+  void *y;
+  void *workspace;
+  size_t workspace_bytes;
+  uint32_t *dev_status;
+} glinattn_scan_args;
+
+size_t glinattn_selective_scan_workspace_size(const glinattn_scan_args *args);
+glinattn_status glinattn_selective_scan(const glinattn_scan_args *args, glinattn_stream_t stream);
+
+/*
+ * glinattn_selective_scan_decode -- one step of the selective scan for R
+ *   requests, the states in a slot-indexed pool updated in place:
+ *   state_pool[slot_ids[r]] is h of request r.  An id outside
+ *   [0, pool_slots) sets GLINATTN_DEV_BAD_SLOT and skips the request; ids must
+ *   be distinct.
+ *
+ *   x, delta [R, D]   Bm, Cm [R, N]   (in_dtype)    A [D, N] fp32
+ *   state_pool [P, D, N] fp32 (read/write)   slot_ids [R] int32   y [R, D] (out_dtype)
+ */
+typedef struct {
+  int32_t in_dtype, out_dtype;
+  int32_t num_req, channels, state, pool_slots;
+  const void *x, *delta, *Bm, *Cm;
+  const float *A;
+  float *state_pool;
+  const int32_t *slot_ids;
+  void *y;
+  uint32_t *dev_status;
+} glinattn_scan_decode_args;
+
+glinattn_status glinattn_selective_scan_decode(const glinattn_scan_decode_args *args, glinattn_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *glinattn_status_string(glinattn_status status);
 

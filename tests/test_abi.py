@@ -35,7 +35,8 @@ def test_library_exports_every_declared_symbol():
 
 STRUCTS = ((G.PrefillArgs, "glinattn_prefill_args"), (G.DecodeArgs, "glinattn_decode_args"),
            (G.SpecArgs, "glinattn_spec_args"), (G.ReplayArgs, "glinattn_replay_args"),
-           (G.CopyArgs, "glinattn_copy_args"))
+           (G.CopyArgs, "glinattn_copy_args"), (G.ScanArgs, "glinattn_scan_args"),
+           (G.ScanDecodeArgs, "glinattn_scan_decode_args"))
 
 
 def test_struct_layout_matches_header(tmp_path):
@@ -238,3 +239,53 @@ def test_replay_zero_requests_is_a_noop():
     lib = G.library()
     assert lib.glinattn_replay(None, None) == INVALID
     assert lib.glinattn_replay(ctypes.byref(_replay(num_req=0, k=None)), None) == 0
+
+
+def _scan(**kw):
+    base = dict(in_dtype=G.F32, out_dtype=G.F32, batch=2, seqlen=100, channels=64, state=16, x=A, delta=A * 2,
+                Bm=A * 3, Cm=A * 4, A=A * 5, h0=None, h_T=A * 6, y=A * 7)
+    base.update(kw)
+    return G.ScanArgs(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(in_dtype=5), INVALID),
+    (dict(state=12), UNSUPPORTED),
+    (dict(state=64), UNSUPPORTED),
+    (dict(channels=0), INVALID),
+    (dict(A=None), INVALID),
+    (dict(h_T=None), INVALID),
+    (dict(x=None), INVALID),
+    (dict(h_T=A * 6 + 4), INVALID),
+    (dict(h0=A * 6 + 64), INVALID),      # partial overlap with h_T
+    (dict(), INVALID),                   # no workspace for a non-empty segment
+])
+def test_selective_scan_rejects(kw, code):
+    assert G.library().glinattn_selective_scan(ctypes.byref(_scan(**kw)), None) == code
+
+
+def test_selective_scan_workspace_and_empty_batch():
+    lib = G.library()
+    a = _scan(batch=2, seqlen=130, channels=64, state=16)
+    nc = 3  # chunks of 64
+    assert lib.glinattn_selective_scan_workspace_size(ctypes.byref(a)) >= 2 * 2 * nc * 64 * 16 * 4
+    assert lib.glinattn_selective_scan(ctypes.byref(_scan(batch=0, x=None)), None) == 0
+    assert lib.glinattn_selective_scan(None, None) == INVALID
+
+
+def _scan_dec(**kw):
+    base = dict(in_dtype=G.BF16, out_dtype=G.F32, num_req=4, channels=64, state=16, pool_slots=8, x=A,
+                delta=A * 2, Bm=A * 3, Cm=A * 4, A=A * 5, state_pool=A * 6, slot_ids=A * 7, y=A * 8)
+    base.update(kw)
+    return G.ScanDecodeArgs(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(slot_ids=None), INVALID),
+    (dict(state_pool=A * 6 + 8), INVALID),
+    (dict(pool_slots=0), INVALID),
+    (dict(state=4), UNSUPPORTED),
+    (dict(num_req=70000), UNSUPPORTED),
+])
+def test_selective_scan_decode_rejects(kw, code):
+    assert G.library().glinattn_selective_scan_decode(ctypes.byref(_scan_dec(**kw)), None) == code
