@@ -296,6 +296,12 @@ def run_ours(args):
     # ---- the SSD form: state 128 x head dim 64, one q / k group for 32 heads ---------
     ssd = ssd_run(args, dist, dev, rank)
 
+    # ---- normalised kernelised linear attention ---------------------------------------
+    nla = nla_run(args, dist, dev, rank)
+
+    # ---- Mamba's selective scan -----------------------------------------------------------
+    scan = scan_run(args, dist, dev, rank)
+
     # ---- CPU baseline: the oracle on this host's cores (rank 0) -----------------------
     cpu = cpu_baseline_run(ex, budget_s=args.cpu_seconds) if rank == 0 and not args.no_cpu else None
 
@@ -358,6 +364,8 @@ def run_ours(args):
                                              "overhead_frac": ck_ms / gdn_ms - 1.0}},
         "long_context": lc,
         "ssd": ssd,
+        "normalized_linear_attention": nla,
+        "selective_scan": scan,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))
@@ -501,6 +509,105 @@ def ssd_run(args, dist, dev, rank):
                                  "peak": hbm, "unit": "GB/s",
                                  "frac": pre_bytes / (statistics.mean(pre_per) / 1e3) / 1e9 / hbm,
                                  "algorithmic_bytes": pre_bytes},
+            "decode_tokens_per_s": N / (dec_ms / 1e3), "decode_ms": dec_ms,
+            "decode_roofline": {"bound": "hbm", "achieved": dec_bytes / (statistics.mean(dec_per) / 1e3) / 1e9,
+                                "peak": hbm, "unit": "GB/s",
+                                "frac": dec_bytes / (statistics.mean(dec_per) / 1e3) / 1e9 / hbm,
+                                "algorithmic_bytes": dec_bytes}}
+
+
+def scan_run(args, dist, dev, rank):
+    """Mamba's selective scan on B=2, T=4096, D=2048 channels (d_model 1024
+    expanded twice), N=16 states, bf16 in and out; decode of 256 requests from
+    a 512-slot fp32 pool."""
+    import torch
+
+    from gated_deltanet_02_gb300 import glinattn_selective_scan, glinattn_selective_scan_decode, inputs
+    pk, _ = peaks()
+    B, T, D, N = 2, 4096, 2048, 16
+    ex = inputs.selective_scan_inputs(B, T, D, N, seed=rank, device=dev, dtype=torch.bfloat16)
+    y = torch.empty(B, T, D, dtype=torch.bfloat16, device=dev)
+    h = torch.empty(B, D, N, dtype=torch.float32, device=dev)
+    ws = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+
+    def step_scan():
+        glinattn_selective_scan(ex["x"], ex["delta"], ex["Bm"], ex["Cm"], ex["A"], None, y=y, h_T=h, workspace=ws)
+
+    sc_ms, sc_per = timed_steps(step_scan, max(3, min(args.steps, 10)), 2, dist, dev)
+    sc_bytes = B * T * (2 * D + 2 * N) * 2 + B * T * D * 2 + B * D * N * 4 + D * N * 4
+    R, P = 256, 512
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(rank + 7)
+    dx = inputs.selective_scan_inputs(R, 1, D, N, seed=rank + 3, device=dev, dtype=torch.bfloat16)
+    pool = torch.randn(P, D, N, device=dev, generator=gen) * 0.1
+    slots = torch.randperm(P, device=dev, generator=gen)[:R].to(torch.int32)
+    xd, dd, bd, cd = (dx[k][:, 0].contiguous() for k in ("x", "delta", "Bm", "Cm"))
+    yd = torch.empty(R, D, dtype=torch.bfloat16, device=dev)
+
+    def step_dec():
+        glinattn_selective_scan_decode(xd, dd, bd, cd, dx["A"], pool, slots, y=yd)
+
+    dec_ms, dec_per = timed_steps(step_dec, max(10, args.steps), 3, dist, dev)
+    dec_bytes = R * D * N * 4 * 2
+    hbm = pk["hbm_gbs"]
+    exps = B * T * D * N
+    return {"config": "selective scan B=2 T=4096 D=2048 N=16, bf16 x / delta / B / C / y, fp32 A and state; "
+                      "decode 256 requests x 2048 channels x 16 states from a 512-slot fp32 pool",
+            "tokens_per_s": B * T / (sc_ms / 1e3), "ms_per_step": sc_ms,
+            "roofline": {"bound": "hbm", "achieved": sc_bytes / (statistics.mean(sc_per) / 1e3) / 1e9, "peak": hbm,
+                         "unit": "GB/s", "frac": sc_bytes / (statistics.mean(sc_per) / 1e3) / 1e9 / hbm,
+                         "algorithmic_bytes": sc_bytes,
+                         "kernels": "ssm_chunk_kernel x2 + ssm_carry_kernel"},
+            "exp_per_s": 2 * exps / (statistics.mean(sc_per) / 1e3),
+            "decode_tokens_per_s": R / (dec_ms / 1e3), "decode_ms": dec_ms,
+            "decode_roofline": {"bound": "hbm", "achieved": dec_bytes / (statistics.mean(dec_per) / 1e3) / 1e9,
+                                "peak": hbm, "unit": "GB/s",
+                                "frac": dec_bytes / (statistics.mean(dec_per) / 1e3) / 1e9 / hbm,
+                                "algorithmic_bytes": dec_bytes}}
+
+
+def nla_run(args, dist, dev, rank):
+    """Normalised kernelised linear attention (phi = elu + 1): prefill on the
+    gated linear attention shape B=4 H=16 T=4096 d=128, and decode of 256
+    requests x 16 heads from a 512-slot pool of states and normalisers."""
+    import torch
+
+    from gated_deltanet_02_gb300 import NLA, glinattn_decode, glinattn_prefill, inputs
+    from gated_deltanet_02_gb300.glinattn import prefill_workspace_size
+    pk, _ = peaks()
+    B, H, T, d = 4, 16, 4096, 128
+    ex = inputs.nla_prefill(B, H, T, d, seed=rank, device=dev)
+    o = torch.empty(B, T, H, d, dtype=torch.bfloat16, device=dev)
+    S = torch.empty(B, H, d, d, dtype=torch.float32, device=dev)
+    z = torch.empty(B, H, d, dtype=torch.float32, device=dev)
+    ws = torch.empty(prefill_workspace_size(B, T, H, d, variant=NLA, out_dtype=1), dtype=torch.uint8, device=dev)
+
+    def step_prefill():
+        glinattn_prefill(ex["q"], ex["k"], ex["v"], None, None, None, variant=NLA, o=o, S_T=S, z_T=z,
+                         workspace=ws)
+
+    pre_ms, pre_per = timed_steps(step_prefill, max(3, min(args.steps, 10)), 2, dist, dev)
+    # q, k, v in (bf16), o out (bf16), S_T and z_T out: the layer's own bytes
+    pre_bytes = B * T * H * d * 2 * 4 + B * H * (d * d + d) * 4
+    N, P = 256, 512
+    dx = inputs.nla_decode(N, H, d, P, seed=rank, device=dev)
+    od = torch.empty(N, H, d, dtype=torch.bfloat16, device=dev)
+
+    def step_dec():
+        glinattn_decode(dx["q"], dx["k"], dx["v"], None, None, dx["pool"], dx["slot_ids"], variant=NLA,
+                        z_pool=dx["zpool"], o=od)
+
+    dec_ms, dec_per = timed_steps(step_dec, max(10, args.steps), 3, dist, dev)
+    dec_bytes = N * H * (d * d + d) * 4 * 2
+    hbm = pk["hbm_gbs"]
+    return {"config": "normalised linear attention (phi = elu + 1, eps = 1e-6): prefill B=4 H=16 T=4096 d=128 bf16; "
+                      "decode 256 requests x 16 heads, 512-slot fp32 pool of states and normalisers",
+            "prefill_tokens_per_s": B * T / (pre_ms / 1e3), "prefill_ms": pre_ms,
+            "prefill_roofline": {"bound": "hbm", "achieved": pre_bytes / (statistics.mean(pre_per) / 1e3) / 1e9,
+                                 "peak": hbm, "unit": "GB/s",
+                                 "frac": pre_bytes / (statistics.mean(pre_per) / 1e3) / 1e9 / hbm,
+                                 "algorithmic_bytes": pre_bytes,
+                                 "kernels": "nla_feature_kernel + gla_prefill_kernel + nla_normalize_kernel"},
             "decode_tokens_per_s": N / (dec_ms / 1e3), "decode_ms": dec_ms,
             "decode_roofline": {"bound": "hbm", "achieved": dec_bytes / (statistics.mean(dec_per) / 1e3) / 1e9,
                                 "peak": hbm, "unit": "GB/s",

@@ -14,9 +14,11 @@
 //      also copy the start normaliser, so that z_T may overwrite it;
 //   2. gla_prefill_kernel without gates: phi(q) S_t, written in fp32 (into o
 //      itself when o is fp32, else into the workspace);
-//   3. nla_normalize_kernel, one CTA per (chunk, head, sequence): z at the
-//      chunk start from the earlier chunks' sums, the 64 denominators of the
-//      chunk, the division, and z_T from the last chunk.
+//   3. nla_zscan_kernel, one thread per (sequence, q / k head, channel): the
+//      exclusive prefix of the chunk sums, i.e. z at every chunk start;
+//   4. nla_normalize_kernel, one CTA per (chunk, head, sequence): the 64
+//      denominators of the chunk from z at its start (a warp per 16 tokens),
+//      the division, and z_T from the last chunk.
 //
 // The denominators use the same bf16 feature values as the numerator.
 #include <cuda_bf16.h>
@@ -30,7 +32,9 @@ namespace {
 constexpr int kC = 64;    // chunk length (the tensor-core kernel's)
 constexpr int kDK = 128;  // key head size
 
-__device__ __forceinline__ float feature_map(float x) { return x > 0.f ? x + 1.f : expf(x); }
+// exp of a non-positive argument through the fast exponential: its relative
+// error (a few units of 2^-22) vanishes in the bf16 rounding that follows
+__device__ __forceinline__ float feature_map(float x) { return x > 0.f ? x + 1.f : __expf(x); }
 
 struct FeatureParams {
   const __nv_bfloat16 *q, *k;
@@ -41,80 +45,200 @@ struct FeatureParams {
   int T, H, Hq, nchunks;
 };
 
-__global__ void __launch_bounds__(kDK) nla_feature_kernel(const FeatureParams p) {
-  const int c = blockIdx.x, hq = blockIdx.y, b = blockIdx.z, d = threadIdx.x;
-  const int t0 = c * kC, n = min(kC, p.T - t0);
-  float zsum = 0.f;
-  for (int i = 0; i < n; ++i) {
-    const size_t e = (((size_t)b * p.T + t0 + i) * p.Hq + hq) * kDK + d;
-    p.fq[e] = __float2bfloat16_rn(feature_map(__bfloat162float(p.q[e])));
-    const __nv_bfloat16 fk = __float2bfloat16_rn(feature_map(__bfloat162float(p.k[e])));
-    p.fk[e] = fk;
-    zsum += __bfloat162float(fk);
+constexpr int kFeatThreads = 256;  // 16 token rows x 16 groups of 8 channels
+
+__device__ __forceinline__ uint4 features8(uint4 raw, float *rounded) {
+  const __nv_bfloat162 *x = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+  uint4 out;
+  uint32_t *o = reinterpret_cast<uint32_t *>(&out);
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const float2 f = __bfloat1622float2(x[m]);
+    const __nv_bfloat162 y = __floats2bfloat162_rn(feature_map(f.x), feature_map(f.y));
+    o[m] = *reinterpret_cast<const uint32_t *>(&y);
+    if (rounded) {
+      const float2 r = __bfloat1622float2(y);
+      rounded[2 * m] = r.x;
+      rounded[2 * m + 1] = r.y;
+    }
   }
-  p.dz[(((size_t)b * p.Hq + hq) * p.nchunks + c) * kDK + d] = zsum;
-  if (c == 0) {
-    const int rep = p.H / p.Hq;
-    for (int h = hq * rep; h < (hq + 1) * rep; ++h) {
-      const size_t e = ((size_t)b * p.H + h) * kDK + d;
-      p.z0w[e] = p.z0 ? p.z0[e] : 0.f;
+  return out;
+}
+
+// phi(q), phi(k) of one chunk of one q / k head, 16-byte accesses; the
+// chunk's column sums of phi(k) are reduced across token rows in shared memory.
+__global__ void __launch_bounds__(kFeatThreads, 4) nla_feature_kernel(const FeatureParams p) {
+  __shared__ float red[16][kDK];
+  const int c = blockIdx.x, hq = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, cg = tid & 15, rg = tid >> 4;
+  const int t0 = c * kC;
+  uint4 qv[4], kv[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {  // every load issued before any store
+    const int t = t0 + rg + 16 * j;
+    if (t < p.T) {
+      const size_t e = (((size_t)b * p.T + t) * p.Hq + hq) * kDK + 8 * cg;
+      qv[j] = *reinterpret_cast<const uint4 *>(p.q + e);
+      kv[j] = *reinterpret_cast<const uint4 *>(p.k + e);
+    }
+  }
+  float zs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int t = t0 + rg + 16 * j;
+    if (t < p.T) {
+      const size_t e = (((size_t)b * p.T + t) * p.Hq + hq) * kDK + 8 * cg;
+      float r[8];
+      *reinterpret_cast<uint4 *>(p.fq + e) = features8(qv[j], nullptr);
+      *reinterpret_cast<uint4 *>(p.fk + e) = features8(kv[j], r);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) zs[m] += r[m];
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < 8; ++m) red[rg][8 * cg + m] = zs[m];
+  __syncthreads();
+  if (tid < kDK) {
+    float z = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) z += red[r][tid];
+    p.dz[(((size_t)b * p.Hq + hq) * p.nchunks + c) * kDK + tid] = z;
+    if (c == 0) {
+      const int rep = p.H / p.Hq;
+      for (int h = hq * rep; h < (hq + 1) * rep; ++h) {
+        const size_t e = ((size_t)b * p.H + h) * kDK + tid;
+        p.z0w[e] = p.z0 ? p.z0[e] : 0.f;
+      }
+    }
+  }
+}
+
+// z at every chunk start (without the start normaliser): zstart[c] = sum of
+// the chunk sums before c.  The loads are independent; 8 are in flight.
+__global__ void __launch_bounds__(kDK) nla_zscan_kernel(const float *__restrict__ dz, float *__restrict__ zstart,
+                                                        int nchunks) {
+  const size_t base = (size_t)blockIdx.x * nchunks * kDK + threadIdx.x;  // blockIdx.x = b * Hq + hq
+  float z = 0.f;
+  for (int c0 = 0; c0 < nchunks; c0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) v[m] = c0 + m < nchunks ? dz[base + (size_t)(c0 + m) * kDK] : 0.f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      if (c0 + m < nchunks) zstart[base + (size_t)(c0 + m) * kDK] = z;
+      z += v[m];
     }
   }
 }
 
 struct NormParams {
   const __nv_bfloat16 *fq, *fk;
-  const float *dz, *z0;  // z0: the copy taken by the feature kernel
+  const float *zstart, *z0;  // z0: the copy taken by the feature kernel
   float *z_T;
   const float *num;  // [B, T, H, dv] fp32 numerators
   void *o;           // [B, T, H, dv] out_dtype (may be num itself when fp32)
   int T, H, Hq, dv, nchunks, out_bf16;
 };
 
+// Warp w owns tokens 16w .. 16w+15 of the chunk and lane l the channels
+// l + 32m: the lane first adds up phi(k) of the tokens before the warp's
+// range, then for each of its tokens extends z and reduces phi(q) . z across
+// the warp.  No shared-memory matrix, so many CTAs fit on an SM.
 __global__ void __launch_bounds__(kDK) nla_normalize_kernel(const NormParams p) {
-  __shared__ float red[kC][kDK + 1];  // padded: row i, column j in bank (i + j) % 32
   __shared__ float inv_den[kC];
-  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, d = threadIdx.x;
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
   const int hq = h / (p.H / p.Hq);
   const int t0 = c * kC, n = min(kC, p.T - t0);
-  // z at the start of the chunk: the start normaliser and the earlier chunks' sums
-  float z = p.z0[((size_t)b * p.H + h) * kDK + d];
-  for (int cc = 0; cc < c; ++cc) z += p.dz[(((size_t)b * p.Hq + hq) * p.nchunks + cc) * kDK + d];
-  for (int i = 0; i < n; ++i) {
-    const size_t e = (((size_t)b * p.T + t0 + i) * p.Hq + hq) * kDK + d;
-    z += __bfloat162float(p.fk[e]);
-    red[i][d] = __bfloat162float(p.fq[e]) * z;
+  float zl[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int d = lane + 32 * m;
+    zl[m] = p.z0[((size_t)b * p.H + h) * kDK + d] + p.zstart[(((size_t)b * p.Hq + hq) * p.nchunks + c) * kDK + d];
   }
-  if (c == p.nchunks - 1 && p.z_T) p.z_T[((size_t)b * p.H + h) * kDK + d] = z;
-  __syncthreads();
-  if (d < n) {
-    float s = 0.f;
-    for (int j = 0; j < kDK; ++j) s += red[d][j];
-    inv_den[d] = 1.f / (s + 1e-6f);
+  auto row = [&](int i) { return (((size_t)b * p.T + t0 + i) * p.Hq + hq) * kDK + lane; };
+  const int first = 16 * warp;
+  // phi(k) of the tokens before this warp's range, 8 rows of loads in flight
+  for (int j0 = 0; j0 < min(first, n); j0 += 8) {
+    float v[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) v[j][m] = j0 + j < n ? __bfloat162float(p.fk[row(j0 + j) + 32 * m]) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) zl[m] += v[j][m];
   }
+  // this warp's tokens, 8 at a time
+#pragma unroll
+  for (int j0 = 0; j0 < 16; j0 += 8) {
+    float fq[8][4], fk[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const bool in = first + j0 + j < n;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        fq[j][m] = in ? __bfloat162float(p.fq[row(first + j0 + j) + 32 * m]) : 0.f;
+        fk[j][m] = in ? __bfloat162float(p.fk[row(first + j0 + j) + 32 * m]) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float s = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        zl[m] += fk[j][m];
+        s += fq[j][m] * zl[m];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) inv_den[first + j0 + j] = 1.f / (s + 1e-6f);
+    }
+  }
+  // the last warp's z covers every token of the chunk
+  if (warp == 3 && c == p.nchunks - 1 && p.z_T)
+#pragma unroll
+    for (int m = 0; m < 4; ++m) p.z_T[((size_t)b * p.H + h) * kDK + lane + 32 * m] = zl[m];
   __syncthreads();
+  const int d = tid;
   const int nv4 = p.dv / 4;
-  for (int e = d; e < n * nv4; e += kDK) {
-    const int i = e / nv4, j = 4 * (e - i * nv4);
-    const size_t off = (((size_t)b * p.T + t0 + i) * p.H + h) * p.dv + j;
-    float4 x = *reinterpret_cast<const float4 *>(p.num + off);
-    const float r = inv_den[i];
-    x.x *= r; x.y *= r; x.z *= r; x.w *= r;
-    if (p.out_bf16) {
-      const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
-      uint2 pk;
-      pk.x = *reinterpret_cast<const uint32_t *>(&lo);
-      pk.y = *reinterpret_cast<const uint32_t *>(&hi);
-      *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + off) = pk;
-    } else {
-      *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + off) = x;
+  const int total = n * nv4;
+  for (int e0 = 0; e0 < total; e0 += 8 * kDK) {
+    float4 x[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {  // all loads first: num may be o itself
+      const int e = e0 + m * kDK + d;
+      if (e < total) {
+        const int i = e / nv4, j = 4 * (e - i * nv4);
+        x[m] = *reinterpret_cast<const float4 *>(p.num + (((size_t)b * p.T + t0 + i) * p.H + h) * p.dv + j);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int e = e0 + m * kDK + d;
+      if (e < total) {
+        const int i = e / nv4, j = 4 * (e - i * nv4);
+        const size_t off = (((size_t)b * p.T + t0 + i) * p.H + h) * p.dv + j;
+        const float r = inv_den[i];
+        const float4 y = make_float4(x[m].x * r, x[m].y * r, x[m].z * r, x[m].w * r);
+        if (p.out_bf16) {
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(y.x, y.y), hi = __floats2bfloat162_rn(y.z, y.w);
+          uint2 pk;
+          pk.x = *reinterpret_cast<const uint32_t *>(&lo);
+          pk.y = *reinterpret_cast<const uint32_t *>(&hi);
+          *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + off) = pk;
+        } else {
+          *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + off) = y;
+        }
+      }
     }
   }
 }
 
 struct Carve {
   __nv_bfloat16 *fq, *fk;
-  float *dz, *z0w, *num;
+  float *dz, *zstart, *z0w, *num;
   size_t bytes;
 };
 
@@ -132,9 +256,10 @@ Carve carve(void *base, const glinattn_prefill_args &a) {
   c.fq = reinterpret_cast<__nv_bfloat16 *>(p);
   c.fk = reinterpret_cast<__nv_bfloat16 *>(p + feat);
   c.dz = reinterpret_cast<float *>(p + 2 * feat);
-  c.z0w = reinterpret_cast<float *>(p + 2 * feat + dz);
-  c.num = num ? reinterpret_cast<float *>(p + 2 * feat + dz + zw) : nullptr;
-  c.bytes = 2 * feat + dz + zw + num;
+  c.zstart = reinterpret_cast<float *>(p + 2 * feat + dz);
+  c.z0w = reinterpret_cast<float *>(p + 2 * feat + 2 * dz);
+  c.num = num ? reinterpret_cast<float *>(p + 2 * feat + 2 * dz + zw) : nullptr;
+  c.bytes = 2 * feat + 2 * dz + zw + num;
   return c;
 }
 
@@ -166,7 +291,7 @@ glinattn_status launch_nla_tc(const glinattn_prefill_args &a, cudaStream_t strea
   fp.H = H;
   fp.Hq = Hq;
   fp.nchunks = nchunks;
-  nla_feature_kernel<<<dim3((unsigned)nchunks, (unsigned)Hq, (unsigned)B), kDK, 0, stream>>>(fp);
+  nla_feature_kernel<<<dim3((unsigned)nchunks, (unsigned)Hq, (unsigned)B), kFeatThreads, 0, stream>>>(fp);
   if (cudaGetLastError() != cudaSuccess) return GLINATTN_ERR_CUDA;
 
   // the numerator: gated linear attention with every gate 1, in fp32
@@ -183,10 +308,13 @@ glinattn_status launch_nla_tc(const glinattn_prefill_args &a, cudaStream_t strea
   const glinattn_status st = launch_prefill_tc(g, stream);
   if (st != GLINATTN_OK) return st;
 
+  nla_zscan_kernel<<<(unsigned)(B * Hq), kDK, 0, stream>>>(w.dz, w.zstart, nchunks);
+  if (cudaGetLastError() != cudaSuccess) return GLINATTN_ERR_CUDA;
+
   NormParams np;
   np.fq = w.fq;
   np.fk = w.fk;
-  np.dz = w.dz;
+  np.zstart = w.zstart;
   np.z0 = w.z0w;
   np.z_T = a.z_T;
   np.num = num;
