@@ -711,6 +711,36 @@ def run_profile(args):
             glinattn_decode(dx["q"], dx["k"], dx["v"], dx["alpha"], dx["beta"], dx["pool"], dx["slot_ids"],
                             variant=GDN, conv_w=dx["conv_w"], conv_pool=dx["conv_pool"], qk_l2norm=True,
                             o=od)
+    elif args.profile == "ssd":
+        ex = inputs.ssd_prefill(2, 32, 1, 4096, seed=0, device=dev)
+        o = torch.empty(2, 4096, 32, 64, dtype=torch.bfloat16, device=dev)
+        S = torch.empty(2, 32, 128, 64, dtype=torch.float32, device=dev)
+
+        def step():
+            glinattn_prefill(ex["q"], ex["k"], ex["v"], ex["alpha"], None, None, variant=GLA, o=o, S_T=S)
+    elif args.profile == "nla":
+        from gated_deltanet_02_gb300 import NLA
+        from gated_deltanet_02_gb300.glinattn import prefill_workspace_size
+        ex = inputs.nla_prefill(4, 16, 4096, 128, seed=0, device=dev)
+        o = torch.empty(4, 4096, 16, 128, dtype=torch.bfloat16, device=dev)
+        S = torch.empty(4, 16, 128, 128, dtype=torch.float32, device=dev)
+        z = torch.empty(4, 16, 128, dtype=torch.float32, device=dev)
+        ws = torch.empty(prefill_workspace_size(4, 4096, 16, 128, variant=NLA, out_dtype=1), dtype=torch.uint8,
+                         device=dev)
+
+        def step():
+            glinattn_prefill(ex["q"], ex["k"], ex["v"], None, None, None, variant=NLA, o=o, S_T=S, z_T=z,
+                             workspace=ws)
+    elif args.profile == "scan":
+        from gated_deltanet_02_gb300 import glinattn_selective_scan
+        ex = inputs.selective_scan_inputs(2, 4096, 2048, 16, seed=0, device=dev, dtype=torch.bfloat16)
+        y = torch.empty(2, 4096, 2048, dtype=torch.bfloat16, device=dev)
+        h = torch.empty(2, 2048, 16, dtype=torch.float32, device=dev)
+        ws = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+
+        def step():
+            glinattn_selective_scan(ex["x"], ex["delta"], ex["Bm"], ex["Cm"], ex["A"], None, y=y, h_T=h,
+                                    workspace=ws)
     else:
         g = GDN_CFG
         gx = inputs.gdn_prefill(g["B"], g["H"], g["T"], g["d"], seed=0, device=dev)
@@ -731,7 +761,7 @@ def run_profile(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["gla", "decode", "gdn"], default=None,
+    ap.add_argument("--profile", choices=["gla", "decode", "gdn", "ssd", "nla", "scan"], default=None,
                     help="run one workload's kernel a few times for a profiler, then exit")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)
