@@ -109,17 +109,27 @@ class ClockSampler:
 # helpers
 # ----------------------------------------------------------------------------
 
-def dist_setup():
+def dist_setup(backend="nccl"):
+    """One process per GPU from the launcher's environment.  The replicas
+    exchange nothing on the data path: the process group only carries the
+    barriers around the timed region and the max over ranks of its time."""
     import torch
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
         return dist, rank, ws, local
     return None, 0, 1, 0
+
+
+def aggregate(units_per_rank, world_size, ms_max):
+    """Whole-job throughput of weak-scaled replicas: every rank processes the
+    same number of units; the job takes as long as its slowest rank."""
+    return units_per_rank * world_size / (ms_max / 1e3)
 
 
 def barrier(dist):
@@ -230,7 +240,7 @@ def run_ours(args):
     tokens = c["B"] * c["T"]
     gbytes, gflops = gla_bytes_flops(**c)
     kern_ms = statistics.mean(per)
-    value = tokens * ws / (ms / 1e3)
+    value = aggregate(tokens, ws, ms)
 
     # ---- end to end through the C ABI with host buffers -------------------------
     host = {k: ex[k].cpu().pin_memory() for k in ("q", "k", "v", "alpha")}
