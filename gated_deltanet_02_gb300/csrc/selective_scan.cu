@@ -21,8 +21,11 @@
 //
 // A thread owns one channel and its N states in registers; the chunk's B and C
 // rows (shared by all channels) are staged in shared memory, and x, delta are
-// read 16 tokens ahead in one batch so their loads overlap.  exp is exp2f of
-// a pre-scaled A.
+// read 16 tokens ahead in one batch so their loads overlap.  The work is
+// bound by the special-function unit (one exp per token, channel and state),
+// so the exponentials use the fast hardware path: the decays exp(dt A) have
+// non-positive arguments, where its relative error (a few units of 2^-22
+// plus |dt A| 2^-24) is far inside the fp32 tolerance of the scan.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -46,8 +49,15 @@ __device__ __forceinline__ void act_st(void *base, size_t i, float v, int bf16) 
     reinterpret_cast<float *>(base)[i] = v;
 }
 
-// log(1 + e^x), finite for any x
-__device__ __forceinline__ float softplus(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
+// softplus(x) = log(1 + e^x) = max(x, 0) + log(1 + e^-|x|).  With e = e^-|x|
+// in (0, 1]: below 1e-3 the series e - e^2/2 (truncation e^3/3, relative
+// < 4e-7) avoids the cancellation of log(1 + e); above it the fast log of
+// 1 + e in [1.001, 2] is accurate to about 1e-7 absolute.
+__device__ __forceinline__ float softplus(float x) {
+  const float e = __expf(-fabsf(x));
+  const float l = e < 1e-3f ? e * (1.f - 0.5f * e) : __logf(1.f + e);
+  return fmaxf(x, 0.f) + l;
+}
 
 struct ScanParams {
   const void *x, *delta, *Bm, *Cm;
@@ -80,10 +90,10 @@ __global__ void __launch_bounds__(kCT) ssm_chunk_kernel(const ScanParams p) {
   const int t0 = c * kL, n = min(kL, p.T - t0);
   stage_bc<N>(p, b, t0, n, sB, sC, OUT);
   const bool active = d < p.D;
-  float A2[N], h[N];
+  float Ad[N], h[N];
 #pragma unroll
   for (int j = 0; j < N; ++j) {
-    A2[j] = active ? p.A[(size_t)d * N + j] * 1.4426950408889634f : 0.f;  // A log2(e)
+    Ad[j] = active ? p.A[(size_t)d * N + j] : 0.f;
     h[j] = 0.f;
   }
   if (OUT && active) {
@@ -113,7 +123,7 @@ __global__ void __launch_bounds__(kCT) ssm_chunk_kernel(const ScanParams p) {
       float yv = 0.f;
 #pragma unroll
       for (int j = 0; j < N; ++j) {
-        h[j] = exp2f(dt * A2[j]) * h[j] + dtx * sB[i0 + i][j];
+        h[j] = __expf(dt * Ad[j]) * h[j] + dtx * sB[i0 + i][j];
         if (OUT) yv += h[j] * sC[i0 + i][j];
       }
       if (OUT) {
@@ -140,12 +150,25 @@ __global__ void __launch_bounds__(256) ssm_carry_kernel(const ScanParams p) {
   const int b = (int)(e / per);
   const size_t dn = e - (size_t)b * per;
   const int d = (int)(dn / N);
-  const float A2 = p.A[dn] * 1.4426950408889634f;
+  const float A = p.A[dn];
   float h = p.h0 ? p.h0[(size_t)b * per + dn] : 0.f;
-  for (int c = 0; c < p.nc; ++c) {
-    const size_t s = ((size_t)b * p.nc + c) * per + dn;
-    p.h_start[s] = h;
-    h = exp2f(A2 * p.sdt[((size_t)b * p.nc + c) * p.D + d]) * h + p.h_end[s];
+  // the end states and step sums of 8 chunks are loaded together
+  for (int c0 = 0; c0 < p.nc; c0 += 8) {
+    float he[8], sd[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int c = c0 + m;
+      he[m] = c < p.nc ? p.h_end[((size_t)b * p.nc + c) * per + dn] : 0.f;
+      sd[m] = c < p.nc ? p.sdt[((size_t)b * p.nc + c) * p.D + d] : 0.f;
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int c = c0 + m;
+      if (c < p.nc) {
+        p.h_start[((size_t)b * p.nc + c) * per + dn] = h;
+        h = __expf(A * sd[m]) * h + he[m];
+      }
+    }
   }
   p.h_T[(size_t)b * per + dn] = h;
 }
@@ -184,7 +207,7 @@ __global__ void __launch_bounds__(256) ssm_decode_kernel(const ScanDecodeParams 
   float yv = 0.f;
 #pragma unroll
   for (int j = 0; j < N; ++j) {
-    const float a = exp2f(dt * p.A[(size_t)d * N + j] * 1.4426950408889634f);
+    const float a = __expf(dt * p.A[(size_t)d * N + j]);
     h[j] = a * h[j] + dtx * act_ld(p.Bm, (size_t)r * N + j, p.in_bf16);
     yv += h[j] * act_ld(p.Cm, (size_t)r * N + j, p.in_bf16);
   }
