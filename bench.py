@@ -721,6 +721,22 @@ def run_profile(args):
             glinattn_decode(dx["q"], dx["k"], dx["v"], dx["alpha"], dx["beta"], dx["pool"], dx["slot_ids"],
                             variant=GDN, conv_w=dx["conv_w"], conv_pool=dx["conv_pool"], qk_l2norm=True,
                             o=od)
+    elif args.profile == "spec":
+        from gated_deltanet_02_gb300 import glinattn_spec_decode
+        N, D, H, d = 64, 4, 32, 128
+        g = torch.Generator(device=dev)
+        g.manual_seed(0)
+        pool = torch.randn(N * (1 + D), H, d, d, device=dev, generator=g) * 0.01
+        cpool = torch.randn(N * (1 + D), 3, 3 * H * d, device=dev, generator=g).to(torch.bfloat16)
+        conv_w = torch.randn(3 * H * d, 4, device=dev, generator=g) * 0.5
+        src = torch.arange(N, dtype=torch.int32, device=dev)
+        dst = (N + torch.arange(N * D, dtype=torch.int32, device=dev)).view(N, D)
+        dr = inputs.spec_drafts(N, D, H, d, seed=1, device=dev)
+        od = torch.empty(N, D, H, d, dtype=torch.bfloat16, device=dev)
+
+        def step():
+            glinattn_spec_decode(dr["q"], dr["k"], dr["v"], dr["alpha"], dr["beta"], pool, src, dst, variant=GDN,
+                                 conv_w=conv_w, conv_pool=cpool, qk_l2norm=True, o=od)
     elif args.profile == "ssd":
         ex = inputs.ssd_prefill(2, 32, 1, 4096, seed=0, device=dev)
         o = torch.empty(2, 4096, 32, 64, dtype=torch.bfloat16, device=dev)
@@ -771,7 +787,7 @@ def run_profile(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["gla", "decode", "gdn", "ssd", "nla", "scan"], default=None,
+    ap.add_argument("--profile", choices=["gla", "decode", "gdn", "spec", "ssd", "nla", "scan"], default=None,
                     help="run one workload's kernel a few times for a profiler, then exit")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)
