@@ -161,3 +161,26 @@ def test_nla_full_size_sampled():
         assert relerr(o[b:b + 1, :, h:h + 1], o_ref) <= TOL_O_BF16, (b, h)
         assert relerr(S[b:b + 1, h:h + 1], S_ref) <= TOL_S_BF16, (b, h)
         assert relerr(z[b:b + 1, h:h + 1], z_ref) <= TOL_S_BF16, (b, h)
+
+
+def test_nla_zero_length_segment_hands_state_and_normaliser_on():
+    ex = inputs.nla_prefill(2, 2, 0, 64, seed=40, dtype=torch.float32, start=True)
+    g = to(ex, DEV)
+    o, S, z = _prefill(g, g["S0"], g["z0"])
+    assert o.numel() == 0
+    assert torch.equal(S, g["S0"]) and torch.equal(z, g["z0"])
+
+
+def test_nla_decode_bad_slot_is_flagged_and_skipped():
+    from gated_deltanet_02_gb300.glinattn import DEV_BAD_SLOT
+    dx = inputs.nla_decode(3, 2, 64, 6, seed=41)
+    g = to(dx, DEV)
+    pool, zpool = g["pool"].clone(), g["zpool"].clone()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    glinattn_decode(g["q"], g["k"], g["v"], None, None, pool, torch.tensor([1, 9, 4], dtype=torch.int32,
+                    device=DEV), variant=NLA, z_pool=zpool, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & DEV_BAD_SLOT
+    for s in (0, 2, 3, 5):
+        assert torch.equal(pool[s], g["pool"][s]) and torch.equal(zpool[s], g["zpool"][s])
+    assert not torch.equal(zpool[1], g["zpool"][1])

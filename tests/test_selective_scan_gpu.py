@@ -122,3 +122,12 @@ def test_scan_decode_bad_slot_is_flagged_and_skipped():
     assert int(status.item()) & DEV_BAD_SLOT
     assert torch.equal(pool[[0, 2, 3, 4]], before[[0, 2, 3, 4]])
     assert not torch.equal(pool[1], before[1])
+
+
+def test_scan_zero_length_segment_copies_the_state():
+    ex = inputs.selective_scan_inputs(2, 0, 96, 8, seed=12, start=True)
+    g = to(ex, DEV)
+    y, h = _run(g, g["h0"])
+    assert y.numel() == 0 and torch.equal(h, g["h0"])
+    y, h = _run(g)  # no start state: zeros
+    assert torch.equal(h, torch.zeros_like(h))
