@@ -23,9 +23,12 @@
 // rows (shared by all channels) are staged in shared memory, and x, delta are
 // read 16 tokens ahead in one batch so their loads overlap.  The work is
 // bound by the special-function unit (one exp per token, channel and state),
-// so the exponentials use the fast hardware path: the decays exp(dt A) have
-// non-positive arguments, where its relative error (a few units of 2^-22
-// plus |dt A| 2^-24) is far inside the fp32 tolerance of the scan.
+// so this file is compiled with fast math and the decays are exp2 of A log2(e)
+// pre-scaled once per thread: one hardware exp2 per state element.  The
+// arguments are non-positive, where its relative error (a few units of 2^-22)
+// is far inside the fp32 tolerance of the scan; results below the normal
+// range flush to zero, i.e. a state element that has decayed below 1e-38 is
+// dropped.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -93,7 +96,7 @@ __global__ void __launch_bounds__(kCT) ssm_chunk_kernel(const ScanParams p) {
   float Ad[N], h[N];
 #pragma unroll
   for (int j = 0; j < N; ++j) {
-    Ad[j] = active ? p.A[(size_t)d * N + j] : 0.f;
+    Ad[j] = active ? p.A[(size_t)d * N + j] * 1.4426950408889634f : 0.f;  // A log2(e)
     h[j] = 0.f;
   }
   if (OUT && active) {
@@ -123,7 +126,7 @@ __global__ void __launch_bounds__(kCT) ssm_chunk_kernel(const ScanParams p) {
       float yv = 0.f;
 #pragma unroll
       for (int j = 0; j < N; ++j) {
-        h[j] = __expf(dt * Ad[j]) * h[j] + dtx * sB[i0 + i][j];
+        h[j] = exp2f(dt * Ad[j]) * h[j] + dtx * sB[i0 + i][j];
         if (OUT) yv += h[j] * sC[i0 + i][j];
       }
       if (OUT) {
@@ -183,37 +186,43 @@ struct ScanDecodeParams {
   int R, D, P, in_bf16, out_bf16;
 };
 
-// One step per (request, channel): the N states move through registers once.
+// One step per (request, channel): N / 4 consecutive threads share a channel,
+// each moving one float4 of its states, so a warp reads and writes whole
+// contiguous state rows; y is reduced across the channel's threads.
 template <int N>
 __global__ void __launch_bounds__(256) ssm_decode_kernel(const ScanDecodeParams p) {
+  constexpr int kQ = N / 4;           // threads per channel
+  constexpr int kCh = 256 / kQ;       // channels per CTA
   const int r = blockIdx.y;
-  const int d = blockIdx.x * 256 + threadIdx.x;
-  if (d >= p.D) return;
+  const int q = threadIdx.x % kQ;
+  const int d = blockIdx.x * kCh + threadIdx.x / kQ;
+  const bool valid = d < p.D;
   const int slot = p.slot_ids[r];
-  if (slot < 0 || slot >= p.P) {
-    if (d == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_BAD_SLOT);
+  if (slot < 0 || slot >= p.P) {  // uniform over the CTA
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_BAD_SLOT);
     return;
   }
-  float4 *hp = reinterpret_cast<float4 *>(p.pool + ((size_t)slot * p.D + d) * N);
-  float h[N];
-#pragma unroll
-  for (int j = 0; j < N / 4; ++j) {
-    const float4 v = hp[j];
-    h[4 * j] = v.x; h[4 * j + 1] = v.y; h[4 * j + 2] = v.z; h[4 * j + 3] = v.w;
-  }
-  const size_t g = (size_t)r * p.D + d;
+  float4 *hp = reinterpret_cast<float4 *>(p.pool + ((size_t)slot * p.D + d) * N) + q;
+  const float4 h4 = valid ? *hp : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 a4 = valid ? reinterpret_cast<const float4 *>(p.A + (size_t)d * N)[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+  const size_t g = (size_t)r * p.D + (valid ? d : 0);
   const float dt = softplus(act_ld(p.delta, g, p.in_bf16));
   const float dtx = dt * act_ld(p.x, g, p.in_bf16);
+  float h[4] = {h4.x, h4.y, h4.z, h4.w};
+  const float av[4] = {a4.x, a4.y, a4.z, a4.w};
   float yv = 0.f;
 #pragma unroll
-  for (int j = 0; j < N; ++j) {
-    const float a = __expf(dt * p.A[(size_t)d * N + j]);
-    h[j] = a * h[j] + dtx * act_ld(p.Bm, (size_t)r * N + j, p.in_bf16);
-    yv += h[j] * act_ld(p.Cm, (size_t)r * N + j, p.in_bf16);
+  for (int j = 0; j < 4; ++j) {
+    const int n = 4 * q + j;
+    h[j] = __expf(dt * av[j]) * h[j] + dtx * act_ld(p.Bm, (size_t)r * N + n, p.in_bf16);
+    yv += h[j] * act_ld(p.Cm, (size_t)r * N + n, p.in_bf16);
   }
 #pragma unroll
-  for (int j = 0; j < N / 4; ++j) hp[j] = make_float4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-  act_st(p.y, g, yv, p.out_bf16);
+  for (int o = kQ / 2; o > 0; o >>= 1) yv += __shfl_xor_sync(0xffffffffu, yv, o);
+  if (valid) {
+    *hp = make_float4(h[0], h[1], h[2], h[3]);
+    if (q == 0) act_st(p.y, g, yv, p.out_bf16);
+  }
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -352,7 +361,8 @@ extern "C" glinattn_status glinattn_selective_scan_decode(const glinattn_scan_de
   p.P = a->pool_slots;
   p.in_bf16 = a->in_dtype == GLINATTN_BF16;
   p.out_bf16 = a->out_dtype == GLINATTN_BF16;
-  const dim3 grid((unsigned)((a->channels + 255) / 256), (unsigned)a->num_req);
+  const unsigned per_cta = 256u / (unsigned)(a->state / 4);  // channels per CTA
+  const dim3 grid((unsigned)((a->channels + per_cta - 1) / per_cta), (unsigned)a->num_req);
   cudaStream_t s = (cudaStream_t)stream;
   switch (a->state) {
     case 8: glinattn::ssm_decode_kernel<8><<<grid, 256, 0, s>>>(p); break;
