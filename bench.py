@@ -346,7 +346,9 @@ def run_ours(args):
                      "algorithmic_bytes": gbytes, "kernel": "gla_prefill_kernel"},
         "tensor": {"flops": gflops, "achieved_tflops": gflops / (kern_ms / 1e3) / 1e12,
                    "peak_tflops": tc, "frac": gflops / (kern_ms / 1e3) / 1e12 / tc,
-                   "peak_kind": f"{pk_kind} bf16 burst"},
+                   "peak_kind": f"{pk_kind} bf16 burst",
+                   # time at the roofline, max(FLOPs / tensor peak, bytes / HBM), over the measured time
+                   "attainable_frac": max(gflops / (tc * 1e12), gbytes / (hbm * 1e9)) / (kern_ms / 1e3)},
         "e2e": {"value": tokens * ws / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
@@ -647,11 +649,12 @@ def cpu_baseline_run(ex, budget_s=10.0):
         oracle.recurrence(oracle.GLA, qs, ks, vs, al, nthreads=cores)
         return time.perf_counter() - t0, bs * hs
 
-    dt, nu = run(1)
-    target = int(budget_s * cores / max(dt / nu, 1e-9))
+    dt1, nu1 = run(1)  # one (batch, head) unit: one thread
+    target = int(budget_s * cores / max(dt1 / nu1, 1e-9))
     target = max(1, min(B * H, target))
     dt, nu = run(target)
     return {"value": nu * T / H / dt, "unit": "tokens/s", "cores": min(cores, nu), "kind": "oracle",
+            "one_thread_value": nu1 * T / H / dt1,
             "sample": f"fp64 recurrence over {nu} of {B * H} (batch, head) units, full T={T}, "
                       f"of the GLA prefill workload ({dt:.1f} s)"}
 
