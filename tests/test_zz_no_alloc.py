@@ -79,3 +79,25 @@ def test_static_scratch_refuses_oversized_calls():
                       heads=H, dk=d, dv=d, q=fake, k=fake, v=fake, alpha=fake, beta=fake,
                       S_T=fake, o=fake)
     assert _entry()(ctypes.byref(a), None) == UNSUPPORTED
+
+
+def test_static_scratch_runs_normalised_linear_attention():
+    """The chunked normalised linear attention takes its scratch (features,
+    chunk sums, the fp32 numerator) from the same array."""
+    B, T, H, d = 1, 300, 2, 128
+    ex = inputs.nla_prefill(B, H, T, d, seed=4, device=DEV, start=True)
+    o = torch.empty(B, T, H, d, dtype=torch.bfloat16, device=DEV)
+    S = torch.empty(B, H, d, d, dtype=torch.float32, device=DEV)
+    z = torch.empty(B, H, d, dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    a = G.PrefillArgs(variant=G.NLA, in_dtype=G.BF16, out_dtype=G.BF16, batch=B, seqlen=T, heads=H, dk=d,
+                      dv=d, q=_ptr(ex["q"]), k=_ptr(ex["k"]), v=_ptr(ex["v"]), S0=_ptr(ex["S0"]), S_T=_ptr(S),
+                      o=_ptr(o), dev_status=_ptr(status), z0=_ptr(ex["z0"]), z_T=_ptr(z))
+    assert 0 < G.library().glinattn_prefill_workspace_size(ctypes.byref(a)) <= 32 << 20
+    stream = ctypes.c_void_p(torch.cuda.current_stream(DEV).cuda_stream)
+    assert _entry()(ctypes.byref(a), stream) == 0
+    o_ref, S_ref, _, z_ref = G.glinattn_prefill(ex["q"], ex["k"], ex["v"], None, None, ex["S0"], variant=G.NLA,
+                                                z0=ex["z0"], out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(o, o_ref) and torch.equal(S, S_ref) and torch.equal(z, z_ref)
