@@ -274,27 +274,25 @@ __global__ void __launch_bounds__(kPrepThreads)
     const int k = 32 * warp + lane;
     colbg[k] = betas[k] * exp2f(g2s[k]);
   }
-  if (ok && (warp == 2 || warp == 3)) {
-    const int i = 32 * (warp - 2) + lane;
-    float kk[64];
-    {
-      float part[32];
-      tmem_ld32(tm + ((uint32_t)(32 * warp) << 16), part);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) kk[j] = part[j];
-      tmem_ld32(tm + ((uint32_t)(32 * warp) << 16) + 32, part);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) kk[32 + j] = part[j];
-    }
+  // warps 2 and 6 read TMEM lanes 64-95 (K'K'^T rows 0-31), warps 3 and 7
+  // lanes 96-127 (rows 32-63); warp w >> 2 takes column half w >> 2.  Rows
+  // 0-31 x columns 32-63 form the zero block A01, so warp 6 has no work.
+  if (ok && (warp & 3) >= 2 && warp != 6) {
+    const int lq = warp & 3, half = warp >> 2;
+    const int i = 32 * (lq - 2) + lane;
+    float kk[32];
+    tmem_ld32(tm + ((uint32_t)(32 * lq) << 16) + 32 * half, kk);
     const float gi = g2s[i], bi = betas[i];
-    if (warp == 2) {
+    if (lq == 2) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) A00[lane * kLd + j] = (j < i) ? bi * exp2f(gi - g2s[j]) * kk[j] : 0.f;
-    } else {
+    } else if (half == 0) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) A10[lane * kLd + j] = bi * exp2f(gi - g2s[j]) * kk[j];
+    } else {
 #pragma unroll
-      for (int j = 32; j < 64; ++j) A11[lane * kLd + j - 32] = (j < i) ? bi * exp2f(gi - g2s[j]) * kk[j] : 0.f;
+      for (int j = 0; j < 32; ++j)
+        A11[lane * kLd + j] = (32 + j < i) ? bi * exp2f(gi - g2s[32 + j]) * kk[j] : 0.f;
     }
   }
   __syncthreads();
