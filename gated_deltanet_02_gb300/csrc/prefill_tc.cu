@@ -112,6 +112,9 @@ struct __align__(16) GateRing {
 };
 static_assert(sizeof(GateRing) <= kGateBytes, "gate ring entry");
 
+// kOutBf16: the output dtype is a template parameter so that each instance
+// carries only its own store path in the epilogue loop.
+template <bool kOutBf16>
 __global__ void __launch_bounds__(kThreads, 1)
     gla_prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, const GlaParams p) {
@@ -461,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) ov[jj] = gi * (o1[jj] + o1l[jj]) + o2[jj];
           if (store) {
-            if (p.out_bf16) {
+            if (kOutBf16) {
               uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + obase + 16 * qt);
 #pragma unroll
               for (int k = 0; k < 2; ++k) {
@@ -637,11 +640,12 @@ glinattn_status launch_prefill_tc(const glinattn_prefill_args &a, cudaStream_t s
   p.state_every = a.state_every > 0 && a.seqlen / a.state_every > 0 ? a.state_every : 0;
   p.nblocks = p.state_every ? a.seqlen / p.state_every : 0;
   p.S_blocks = a.S_blocks;
-  if (cudaFuncSetAttribute(gla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kernel = p.out_bf16 ? gla_prefill_kernel<true> : gla_prefill_kernel<false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kSmemBytes) != cudaSuccess)
     return GLINATTN_ERR_CUDA;
   const unsigned grid = (unsigned)a.batch * (unsigned)a.heads * (unsigned)(a.dv / kBV);
-  gla_prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? GLINATTN_OK : GLINATTN_ERR_CUDA;
 }
 
