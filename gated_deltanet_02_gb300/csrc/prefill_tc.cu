@@ -112,9 +112,10 @@ struct __align__(16) GateRing {
 };
 static_assert(sizeof(GateRing) <= kGateBytes, "gate ring entry");
 
-// kOutBf16: the output dtype is a template parameter so that each instance
-// carries only its own store path in the epilogue loop.
-template <bool kOutBf16>
+// kOutBf16, kEmit: the output dtype and whether block states are emitted are
+// template parameters, so that each instance carries only its own paths in
+// the epilogue loop (a compact loop measured faster than runtime branches).
+template <bool kOutBf16, bool kEmit>
 __global__ void __launch_bounds__(kThreads, 1)
     gla_prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, const GlaParams p) {
@@ -437,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars->ds_free);
       if (c + 1 < nchunks) write_state((c + 1) & 1);
-      if (p.state_every && ((c + 1) * kC) % p.state_every == 0 && (c + 1) * kC <= T) {
+      if (kEmit && ((c + 1) * kC) % p.state_every == 0 && (c + 1) * kC <= T) {
         // the state after this chunk closes a block: this thread's row slice goes out
         float *dst = p.S_blocks +
                      ((((size_t)b * p.nblocks + (c + 1) * kC / p.state_every - 1) * p.H + h) * kDK + srow) * p.DV +
@@ -640,7 +641,8 @@ glinattn_status launch_prefill_tc(const glinattn_prefill_args &a, cudaStream_t s
   p.state_every = a.state_every > 0 && a.seqlen / a.state_every > 0 ? a.state_every : 0;
   p.nblocks = p.state_every ? a.seqlen / p.state_every : 0;
   p.S_blocks = a.S_blocks;
-  auto kernel = p.out_bf16 ? gla_prefill_kernel<true> : gla_prefill_kernel<false>;
+  auto kernel = p.out_bf16 ? (p.state_every ? gla_prefill_kernel<true, true> : gla_prefill_kernel<true, false>)
+                           : (p.state_every ? gla_prefill_kernel<false, true> : gla_prefill_kernel<false, false>);
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kSmemBytes) != cudaSuccess)
     return GLINATTN_ERR_CUDA;
