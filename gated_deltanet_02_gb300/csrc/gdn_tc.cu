@@ -522,6 +522,9 @@ __device__ __forceinline__ float grow_chunk(GateRow &G, const ScanParams &p, siz
   return row[kC - 1];
 }
 
+// kOutBf16, kEmit: output dtype and block-state emission as template
+// parameters, so each instance carries only its own epilogue paths
+template <bool kOutBf16, bool kEmit>
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_scan_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tu,
@@ -851,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // buffer (c + 1) & 1 was last read by W S (done: ds_ready of chunk c - 1)
       // and Q' S (done: o_ready of chunk c - 1) of the previous chunk
       if (c + 1 < nchunks) write_state((c + 1) & 1);
-      if (p.state_every && ((c + 1) * kC) % p.state_every == 0 && (c + 1) * kC <= T) {
+      if (kEmit && ((c + 1) * kC) % p.state_every == 0 && (c + 1) * kC <= T) {
         // the state after this chunk closes a block: this thread's row slice goes out
         float *dst = p.S_blocks +
                      ((((size_t)b * p.nblocks + (c + 1) * kC / p.state_every - 1) * p.H + h) * kD + srow) * kD +
@@ -880,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) ov[jj] = gi * (a1[jj] + a2[jj]) + (b1[jj] + b2[jj]);
           if (store) {
-            if (p.out_bf16) {
+            if (kOutBf16) {
               uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + obase + 16 * qt);
 #pragma unroll
               for (int k = 0; k < 2; ++k) dst[k] = pack8_rn(ov + 8 * k);
@@ -1048,10 +1051,12 @@ glinattn_status launch_gdn_tc(const glinattn_prefill_args &a, cudaStream_t strea
   sp.state_every = a.state_every > 0 && T / a.state_every > 0 ? a.state_every : 0;
   sp.nblocks = sp.state_every ? T / sp.state_every : 0;
   sp.S_blocks = a.S_blocks;
-  if (cudaFuncSetAttribute(gdn_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto scan = sp.out_bf16 ? (sp.state_every ? gdn_scan_kernel<true, true> : gdn_scan_kernel<true, false>)
+                          : (sp.state_every ? gdn_scan_kernel<false, true> : gdn_scan_kernel<false, false>);
+  if (cudaFuncSetAttribute(scan, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kScanSmem) != cudaSuccess)
     return GLINATTN_ERR_CUDA;
-  gdn_scan_kernel<<<(unsigned)(B * H * kNV), kThreads, kScanSmem, stream>>>(tq, tk, tw, tu, sp);
+  scan<<<(unsigned)(B * H * kNV), kThreads, kScanSmem, stream>>>(tq, tk, tw, tu, sp);
   return cudaGetLastError() == cudaSuccess ? GLINATTN_OK : GLINATTN_ERR_CUDA;
 }
 
