@@ -88,6 +88,9 @@ struct PrepParams {
   uint32_t *dev_status;
 };
 
+// kConv, kL2: the front end's convolution and L2 norm as template parameters
+// (one code path per instance)
+template <bool kConv, bool kL2>
 __global__ void __launch_bounds__(kPrepThreads)
     gdn_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const PrepParams p) {
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(kPrepThreads)
       if (r0 == 0) {
         if (t >= 0)
           v = *reinterpret_cast<const uint2 *>(src + (((size_t)b * T + t) * H + h) * kD + 4 * lane);
-        else if (p.has_conv && p.conv_in)
+        else if (kConv && p.conv_in)
           v = *reinterpret_cast<const uint2 *>(p.conv_in + ((size_t)b * 3 + (t + 3)) * Cch + part * H * kD +
                                                h * kD + 4 * lane);
       }
@@ -154,7 +157,7 @@ __global__ void __launch_bounds__(kPrepThreads)
     }
 #pragma unroll
     for (int c2 = 0; c2 < 4; ++c2)
-      f.w[c2] = p.has_conv ? *reinterpret_cast<const float4 *>(
+      f.w[c2] = kConv ? *reinterpret_cast<const float4 *>(
                                  p.conv_w + ((size_t)part * H * kD + h * kD + 4 * lane + c2) * 4)
                            : make_float4(0.f, 0.f, 0.f, 1.f);
   };
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(kPrepThreads)
         const float4 wc = f.w[c2];
         y[c2] = wc.x * xv(r) + wc.y * xv(r + 1) + wc.z * xv(r + 2) + wc.w * xv(r + 3);
       }
-      if (part < 2 && p.qk_l2norm) {
+      if (part < 2 && kL2) {
         float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -1023,14 +1026,16 @@ glinattn_status launch_gdn_tc(const glinattn_prefill_args &a, cudaStream_t strea
   pp.conv_in = static_cast<const __nv_bfloat16 *>(a.conv_in);
   pp.Qp = w.Qp; pp.Kp = w.Kp; pp.Wp = w.Wp; pp.Up = w.Up; pp.Gp = w.Gp;
   pp.dev_status = a.dev_status;
-  if (cudaFuncSetAttribute(gdn_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto prep = pp.has_conv ? (pp.qk_l2norm ? gdn_prep_kernel<true, true> : gdn_prep_kernel<true, false>)
+                          : (pp.qk_l2norm ? gdn_prep_kernel<false, true> : gdn_prep_kernel<false, false>);
+  if (cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)kPrepSmem) != cudaSuccess)
     return GLINATTN_ERR_CUDA;
   CUtensorMap rq, rk, rv;  // raw activations, 64-token x 64-channel boxes
   if (!make_act_map(&rq, a.q, B, T, H, kD) || !make_act_map(&rk, a.k, B, T, H, kD) ||
       !make_act_map(&rv, a.v, B, T, H, kD))
     return GLINATTN_ERR_CUDA;
-  gdn_prep_kernel<<<dim3(nchunks, H, B), kPrepThreads, kPrepSmem, stream>>>(rq, rk, rv, pp);
+  prep<<<dim3(nchunks, H, B), kPrepThreads, kPrepSmem, stream>>>(rq, rk, rv, pp);
   if (cudaGetLastError() != cudaSuccess) return GLINATTN_ERR_CUDA;
 
   CUtensorMap tq, tk, tw, tu;
