@@ -74,7 +74,12 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-template <int DK, int DV>
+// kVar: the variant (GLINATTN_GLA or GLINATTN_GDN) as a template parameter, so
+// each instance carries only its own update path; kAnyVariant reads it at run
+// time (normalised linear attention, measured faster that way).
+constexpr int kAnyVariant = -1;
+
+template <int DK, int DV, int kVar>
 __global__ void __launch_bounds__(Shape<DK, DV>::NT)
     recurrent_kernel(const __grid_constant__ CUtensorMap tstate, const RecurParams p) {
   using Sh = Shape<DK, DV>;
@@ -90,7 +95,8 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
   const int col0 = half * Sh::DC;  // first state column of this CTA
   const size_t DD = (size_t)DK * DV;
   const int hq = h / (p.H / p.Hq);  // the q / k head (group) of head h
-  const bool nla = p.variant == GLINATTN_NLA;  // no gates; phi(q), phi(k); normaliser z
+  const bool nla = kVar == kAnyVariant && p.variant == GLINATTN_NLA;  // no gates; phi(q), phi(k); z
+  const bool gdn = kVar == kAnyVariant ? p.variant == GLINATTN_GDN : kVar == GLINATTN_GDN;
 
   extern __shared__ __align__(128) float4 s_state4[];  // DK rows x DC columns, row-major
   __shared__ float s_act[NCH];                          // q | k | own v slice after the front end
@@ -151,7 +157,7 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
   if (p.steps > 0) {
     const size_t row0 = ((size_t)n * p.steps) * p.H + h;
     a_next = nla ? 1.f : p.alpha[row0];
-    if (p.variant == GLINATTN_GDN) b_next = p.beta[row0];
+    if (gdn) b_next = p.beta[row0];
     if (p.dst_slot) dslot_next = p.dst_slot[(size_t)n * (p.dst_per_step ? p.steps : 1)];
   }
   float xr[MAXC], wr[MAXC][4], hr[MAXC][3];
@@ -223,7 +229,7 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
     const int dslot_t = dslot_next;
     if (t + 1 < steps_n) {
       a_next = nla ? 1.f : p.alpha[row + p.H];
-      if (p.variant == GLINATTN_GDN) b_next = p.beta[row + p.H];
+      if (gdn) b_next = p.beta[row + p.H];
       if (p.dst_slot && p.dst_per_step) dslot_next = p.dst_slot[(size_t)n * p.steps + t + 1];
     }
     // ---- front end in registers: conv, history shift, next token prefetch -------
@@ -323,7 +329,7 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
     // ---- update: shared memory copy for the next step, global copy if due ------
     const float4 vv = *reinterpret_cast<const float4 *>(sva + 4 * cg);
     float4 u = vv;
-    if (p.variant == GLINATTN_GDN) {
+    if (gdn) {
       const float b = bgate;
       u.x = b * (vv.x - a * x.x);
       u.y = b * (vv.y - a * x.y);
@@ -411,8 +417,8 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
   release_history();
 }
 
-template <int DK, int DV>
-cudaError_t launch(const RecurParams &p, cudaStream_t stream) {
+template <int DK, int DV, int kVar>
+cudaError_t launch_variant(const RecurParams &p, cudaStream_t stream) {
   using Sh = Shape<DK, DV>;
   const unsigned grid = (unsigned)p.N * (unsigned)p.H * Sh::NSPLIT;
   constexpr int smem = DK * Sh::DC * 4;
@@ -427,7 +433,7 @@ cudaError_t launch(const RecurParams &p, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   }
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(recurrent_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(recurrent_kernel<DK, DV, kVar>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
@@ -442,7 +448,14 @@ cudaError_t launch(const RecurParams &p, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, recurrent_kernel<DK, DV>, tmap, p);
+  return cudaLaunchKernelEx(&cfg, recurrent_kernel<DK, DV, kVar>, tmap, p);
+}
+
+template <int DK, int DV>
+cudaError_t launch(const RecurParams &p, cudaStream_t stream) {
+  if (p.variant == GLINATTN_GDN) return launch_variant<DK, DV, GLINATTN_GDN>(p, stream);
+  if (p.variant == GLINATTN_GLA) return launch_variant<DK, DV, GLINATTN_GLA>(p, stream);
+  return launch_variant<DK, DV, kAnyVariant>(p, stream);
 }
 
 }  // namespace
