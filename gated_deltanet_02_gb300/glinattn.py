@@ -4,7 +4,7 @@ Argument marshalling only: every step of the layer runs in the CUDA kernels of
 ``libglinattn.so``.  PyTorch supplies device memory and streams.  There is no
 CPU fallback: if the library cannot be built or loaded, every call raises.
 
-The three entry points keep the C names:
+The entry points keep the C names:
 
 * ``glinattn_prefill``     -- chunked prefill of a segment (state hand-over in/out)
 * ``glinattn_decode``      -- one recurrent step per request, state pool by slot id
