@@ -135,7 +135,13 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *a, glinattn_stream
     if (st != GLINATTN_OK) return st;
   }
   if (tc_device) {
-    if (glinattn::prefill_tc_supports(*a)) return glinattn::launch_prefill_tc(*a, (cudaStream_t)stream);
+    if (glinattn::prefill_tc_supports(*a)) {
+      // few (batch, head) units: split the sequence when the caller gave the scratch for it
+      const size_t split = glinattn::gla_split_workspace_bytes(*a);
+      if (split && a->workspace && a->workspace_bytes >= split && aligned16(a->workspace))
+        return glinattn::launch_gla_split(*a, (cudaStream_t)stream);
+      return glinattn::launch_prefill_tc(*a, (cudaStream_t)stream);
+    }
     if (glinattn::gdn_tc_supports(*a)) return glinattn::launch_gdn_tc(*a, (cudaStream_t)stream);
     if (glinattn::nla_tc_supports(*a)) return glinattn::launch_nla_tc(*a, (cudaStream_t)stream);
   }
@@ -177,6 +183,7 @@ size_t glinattn_prefill_workspace_size(const glinattn_prefill_args *a) {
   if (!a || a->batch <= 0 || a->seqlen <= 0 || a->heads <= 0) return 0;
   if (check_common(a->variant, a->in_dtype, a->out_dtype, a->dk, a->dv, a->heads) != GLINATTN_OK) return 0;
   if (glinattn::nla_tc_supports(*a)) return glinattn::nla_tc_workspace_bytes(*a);
+  if (glinattn::prefill_tc_supports(*a)) return glinattn::gla_split_workspace_bytes(*a);
   if (!glinattn::gdn_tc_supports(*a)) return 0;
   return glinattn::gdn_tc_workspace_bytes(*a);
 }

@@ -83,6 +83,7 @@ struct GlaParams {
   int B, T, H, nchunks, out_bf16;
   int rep;   // heads per q / k head
   int DV;    // value head size: 128 (two CTAs per head) or 64 (one)
+  const int *skip;  // [B, H] or NULL: units to skip (a gate elsewhere in a split sequence is invalid)
   int state_every, nblocks;  // states emitted after every state_every tokens (a multiple of 64)
   float *S_blocks;
   const float *alpha;
@@ -142,6 +143,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (__syncthreads_or(bad)) {
       if (tid == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_BAD_GATE);
+      return;
+    }
+    if (p.skip && p.skip[bh]) {  // uniform over the CTA
       return;
     }
   }
@@ -619,6 +623,10 @@ bool prefill_tc_supports(const glinattn_prefill_args &a) {
 }
 
 glinattn_status launch_prefill_tc(const glinattn_prefill_args &a, cudaStream_t stream) {
+  return launch_prefill_tc_skip(a, stream, nullptr);
+}
+
+glinattn_status launch_prefill_tc_skip(const glinattn_prefill_args &a, cudaStream_t stream, const int *skip) {
   CUtensorMap tq, tk, tv;
   const int Hq = a.qk_heads > 0 ? a.qk_heads : a.heads;
   if (!make_act_map(&tq, a.q, a.batch, a.seqlen, Hq, kDK) ||
@@ -628,6 +636,7 @@ glinattn_status launch_prefill_tc(const glinattn_prefill_args &a, cudaStream_t s
   GlaParams p;
   p.rep = a.heads / Hq;
   p.DV = a.dv;
+  p.skip = skip;
   p.B = a.batch;
   p.T = a.seqlen;
   p.H = a.heads;

@@ -17,6 +17,15 @@ bool prefill_tc_supports(const glinattn_prefill_args &a);
 
 // bf16 activations, dk == dv == 128, chunk 64.  Arguments already validated.
 glinattn_status launch_prefill_tc(const glinattn_prefill_args &a, cudaStream_t stream);
+// The same with a per-unit skip flag array [B, H] (NULL: none).
+glinattn_status launch_prefill_tc_skip(const glinattn_prefill_args &a, cudaStream_t stream, const int *skip);
+
+// Gated linear attention split along the sequence when B * H * (d_v / 64)
+// leaves more than half of the SMs idle (gla_split.cu): the number of pieces
+// (1 = no split), the workspace it needs, and the launch.
+int gla_split_pieces(const glinattn_prefill_args &a);
+size_t gla_split_workspace_bytes(const glinattn_prefill_args &a);
+glinattn_status launch_gla_split(const glinattn_prefill_args &a, cudaStream_t stream);
 
 // Chunked Gated DeltaNet (two passes through a caller-provided workspace).
 bool gdn_tc_supports(const glinattn_prefill_args &a);
