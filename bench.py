@@ -10,8 +10,11 @@ then 64 requests x 4-token speculative decode), each with its roofline.
 
 Timing: W untimed warm-up steps, then K steps between a barrier and
 torch.cuda.synchronize() on both sides, CUDA events on the launching stream,
-max over ranks.  Every input set is larger than L2 (129 MB), so no flush is
-needed.  Multi-GPU runs are replicas: each rank runs the same per-GPU workload
+max over ranks.  No step finds the previous step's data in L2 (129 MB): the
+working set of a step is larger than L2, or, where it is smaller (the SSD-form
+prefill, the selective scan, the replay round), consecutive steps cycle over
+disjoint copies of their buffers whose combined footprint is about three times
+L2, so no flush is needed.  Multi-GPU runs are replicas: each rank runs the same per-GPU workload
 ("scaling": "weak"); there is no data-path collective.
 
 ``--impl reference`` times the plain fp64 CPU oracle on the host cores on a
@@ -165,6 +168,26 @@ def timed_steps(fn, steps, warmup, dist, device):
     per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
     total = ev[0].elapsed_time(ev[steps])
     return max_over_ranks(dist, total / steps, device), per
+
+
+L2_BYTES = 129 * 10**6
+
+
+def rotation(step_bytes, most=8):
+    """Number of disjoint buffer copies for a step touching ``step_bytes``, so
+    that the memory touched between two uses of one copy is about 3x L2."""
+    return max(1, min(most, -(-3 * L2_BYTES // max(1, step_bytes))))
+
+
+def cycling(fns):
+    """A step that runs the next of several equivalent steps (each on its own
+    buffers) on every call."""
+    state = {"i": 0}
+
+    def step():
+        fns[state["i"] % len(fns)]()
+        state["i"] += 1
+    return step
 
 
 def source_hash(*names):
@@ -339,7 +362,8 @@ def run_ours(args):
         "config": {"workload": "gated linear attention prefill, B=4 H=16 T=4096 d_k=d_v=128 C=64, "
                                "bf16 q/k/v/o, fp32 alpha and state, S0 = 0",
                    "global_batch": c["B"] * ws, "seq_len": c["T"], "parallelism": f"replicas x{ws}",
-                   "l2": "inputs larger than L2 (no flush needed)"},
+                   "l2": "inputs larger than L2 (no flush needed); smaller sub-benchmarks cycle over "
+                         "disjoint buffer copies totalling ~3x L2"},
         "roofline": {"bound": "hbm", "achieved": gbytes / (kern_ms / 1e3) / 1e9, "peak": hbm,
                      "unit": "GB/s", "frac": gbytes / (kern_ms / 1e3) / 1e9 / hbm,
                      "traffic": traffic, "peak_kind": f"{pk_kind} burst copy",
@@ -439,13 +463,18 @@ def long_context_run(args, dist, dev, rank):
     # the replay-buffer alternative: verify without per-draft states, then apply
     # each request's accepted drafts (a ~ U{0..4}) to its own slot in place
     accept = dr["accept"].to(torch.int32)
+    # the 64 slots a round touches (134 MB) cycle over disjoint slot sets of the
+    # pool (the states the speculative round above left in them)
+    rsets = [torch.arange(i * N, (i + 1) * N, dtype=torch.int32, device=dev)
+             for i in range(rotation(N * H * d * d * 4, most=P // N))]
 
-    def step_replay():
-        glinattn_spec_decode(dr["q"], dr["k"], dr["v"], dr["alpha"], dr["beta"], pool, src, None,
+    def replay_round(rs):
+        glinattn_spec_decode(dr["q"], dr["k"], dr["v"], dr["alpha"], dr["beta"], pool, rs, None,
                              variant=GDN, conv_w=ex["conv_w"], conv_pool=cpool, qk_l2norm=True, o=od)
-        glinattn_replay(dr["k"], dr["v"], dr["alpha"], dr["beta"], pool, src, accept, q=dr["q"], variant=GDN,
+        glinattn_replay(dr["k"], dr["v"], dr["alpha"], dr["beta"], pool, rs, accept, q=dr["q"], variant=GDN,
                         conv_w=ex["conv_w"], conv_pool=cpool, qk_l2norm=True)
 
+    step_replay = cycling([lambda rs=rs: replay_round(rs) for rs in rsets])
     rep_ms, rep_per = timed_steps(step_replay, max(10, args.steps), 3, dist, dev)
     n_acc = int((accept > 0).sum().item())
     rep_bytes = N * H * d * d * 4 + 2 * n_acc * H * d * d * 4
@@ -494,15 +523,15 @@ def ssd_run(args, dist, dev, rank):
     from gated_deltanet_02_gb300 import GLA, glinattn_decode, glinattn_prefill, inputs
     pk, _ = peaks()
     B, H, G, T, dk, dv = 2, 32, 1, 4096, 128, 64
-    ex = inputs.ssd_prefill(B, H, G, T, seed=rank, device=dev)
-    o = torch.empty(B, T, H, dv, dtype=torch.bfloat16, device=dev)
-    S = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
-
-    def step_prefill():
-        glinattn_prefill(ex["q"], ex["k"], ex["v"], ex["alpha"], None, None, variant=GLA, o=o, S_T=S)
-
-    pre_ms, pre_per = timed_steps(step_prefill, max(3, min(args.steps, 10)), 2, dist, dev)
     pre_bytes = B * T * G * dk * 2 * 2 + B * T * H * (dv * 2 * 2 + 4) + B * H * dk * dv * 4
+    steps = []
+    for i in range(rotation(pre_bytes)):  # a step's 71 MB fit in L2: cycle over disjoint copies
+        ex = inputs.ssd_prefill(B, H, G, T, seed=rank + 1000 * i, device=dev)
+        o = torch.empty(B, T, H, dv, dtype=torch.bfloat16, device=dev)
+        S = torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev)
+        steps.append(lambda ex=ex, o=o, S=S: glinattn_prefill(ex["q"], ex["k"], ex["v"], ex["alpha"], None, None,
+                                                              variant=GLA, o=o, S_T=S))
+    pre_ms, pre_per = timed_steps(cycling(steps), max(3, min(args.steps, 10)), 2, dist, dev)
     N, P = 256, 512
     dx = inputs.ssd_decode(N, H, G, P, seed=rank, device=dev)
     od = torch.empty(N, H, dv, dtype=torch.bfloat16, device=dev)
@@ -537,34 +566,38 @@ def scan_run(args, dist, dev, rank):
     from gated_deltanet_02_gb300 import glinattn_selective_scan, glinattn_selective_scan_decode, inputs
     pk, _ = peaks()
     B, T, D, N = 2, 4096, 2048, 16
-    ex = inputs.selective_scan_inputs(B, T, D, N, seed=rank, device=dev, dtype=torch.bfloat16)
-    y = torch.empty(B, T, D, dtype=torch.bfloat16, device=dev)
-    h = torch.empty(B, D, N, dtype=torch.float32, device=dev)
-    ws = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
-
-    def step_scan():
-        glinattn_selective_scan(ex["x"], ex["delta"], ex["Bm"], ex["Cm"], ex["A"], None, y=y, h_T=h, workspace=ws)
-
-    sc_ms, sc_per = timed_steps(step_scan, max(3, min(args.steps, 10)), 2, dist, dev)
     sc_bytes = B * T * (2 * D + 2 * N) * 2 + B * T * D * 2 + B * D * N * 4 + D * N * 4
-    R, P = 256, 512
+    # a step touches ~135 MB (inputs, y and the chunk states of the workspace):
+    # cycle over disjoint copies
+    steps = []
+    for i in range(rotation(sc_bytes + 2 * B * 64 * D * N * 4)):
+        ex = inputs.selective_scan_inputs(B, T, D, N, seed=rank + 1000 * i, device=dev, dtype=torch.bfloat16)
+        y = torch.empty(B, T, D, dtype=torch.bfloat16, device=dev)
+        h = torch.empty(B, D, N, dtype=torch.float32, device=dev)
+        ws = torch.empty(64 << 20, dtype=torch.uint8, device=dev)
+        steps.append(lambda ex=ex, y=y, h=h, ws=ws: glinattn_selective_scan(ex["x"], ex["delta"], ex["Bm"], ex["Cm"],
+                                                                           ex["A"], None, y=y, h_T=h, workspace=ws))
+    sc_ms, sc_per = timed_steps(cycling(steps), max(3, min(args.steps, 10)), 2, dist, dev)
+    R = 256
+    dec_bytes = R * D * N * 4 * 2
+    # a step's 256 state rows (34 MB) fit in L2: cycle over disjoint slot sets
+    # of a pool holding rotation(...) x 256 slots
+    nsets = rotation(dec_bytes)
+    P = R * nsets
     gen = torch.Generator(device=dev)
     gen.manual_seed(rank + 7)
     dx = inputs.selective_scan_inputs(R, 1, D, N, seed=rank + 3, device=dev, dtype=torch.bfloat16)
     pool = torch.randn(P, D, N, device=dev, generator=gen) * 0.1
-    slots = torch.randperm(P, device=dev, generator=gen)[:R].to(torch.int32)
+    slot_sets = torch.randperm(P, device=dev, generator=gen).to(torch.int32).view(nsets, R)
     xd, dd, bd, cd = (dx[k][:, 0].contiguous() for k in ("x", "delta", "Bm", "Cm"))
     yd = torch.empty(R, D, dtype=torch.bfloat16, device=dev)
-
-    def step_dec():
-        glinattn_selective_scan_decode(xd, dd, bd, cd, dx["A"], pool, slots, y=yd)
-
+    step_dec = cycling([lambda sl=sl: glinattn_selective_scan_decode(xd, dd, bd, cd, dx["A"], pool, sl, y=yd)
+                        for sl in slot_sets])
     dec_ms, dec_per = timed_steps(step_dec, max(10, args.steps), 3, dist, dev)
-    dec_bytes = R * D * N * 4 * 2
     hbm = pk["hbm_gbs"]
     exps = B * T * D * N
     return {"config": "selective scan B=2 T=4096 D=2048 N=16, bf16 x / delta / B / C / y, fp32 A and state; "
-                      "decode 256 requests x 2048 channels x 16 states from a 512-slot fp32 pool",
+                      f"decode 256 requests x 2048 channels x 16 states from a {P}-slot fp32 pool",
             "tokens_per_s": B * T / (sc_ms / 1e3), "ms_per_step": sc_ms,
             "roofline": {"bound": "hbm", "achieved": sc_bytes / (statistics.mean(sc_per) / 1e3) / 1e9, "peak": hbm,
                          "unit": "GB/s", "frac": sc_bytes / (statistics.mean(sc_per) / 1e3) / 1e9 / hbm,
