@@ -5,20 +5,22 @@
 //   S_t = S_{t-1} + phi(k_t)^T v_t,   z_t = z_{t-1} + phi(k_t),
 //   o_t = phi(q_t) S_t / (phi(q_t) . z_t + 1e-6).
 // The numerator is gated linear attention with every gate equal to 1 on the
-// features phi(q), phi(k), so it runs on the chunked tensor-core kernel; the
-// denominator is a prefix sum of phi(k) dotted with phi(q).  Three launches:
+// features phi(q), phi(k), so it runs on the chunked tensor-core kernel.
+// Inside a chunk the denominator splits the same way as the numerator:
+// phi(q_t) . z_t = phi(q_t) . z_start + sum over s <= t of phi(q_t) . phi(k_s),
+// and the second term is the row sum of the masked phi(Q) phi(K)^T tile that
+// the kernel already forms.  Three launches:
 //
 //   1. nla_feature_kernel, one CTA per (chunk, q / k head, sequence): phi(q)
 //      and phi(k) rounded to bf16 (the tensor-core operands) into the
 //      workspace, and the chunk's column sums of phi(k); the chunk-0 CTAs
 //      also copy the start normaliser, so that z_T may overwrite it;
-//   2. gla_prefill_kernel without gates: phi(q) S_t, written in fp32 (into o
-//      itself when o is fp32, else into the workspace);
-//   3. nla_zscan_kernel, one thread per (sequence, q / k head, channel): the
-//      exclusive prefix of the chunk sums, i.e. z at every chunk start;
-//   4. nla_normalize_kernel, one CTA per (chunk, head, sequence): the 64
-//      denominators of the chunk from z at its start (a warp per 16 tokens),
-//      the division, and z_T from the last chunk.
+//   2. nla_zscan_kernel, one thread per (sequence, q / k head, channel): z at
+//      every chunk start of every value head (start normaliser plus the
+//      exclusive prefix of the chunk sums), and z_T;
+//   3. gla_prefill_kernel, normalised instance: no gates; each token's
+//      denominator from z at its chunk start and the row sum, the outputs
+//      divided by it in the epilogue and written in the output dtype.
 //
 // The denominators use the same bf16 feature values as the numerator.
 #include <cuda_bf16.h>
@@ -113,132 +115,37 @@ __global__ void __launch_bounds__(kFeatThreads, 4) nla_feature_kernel(const Feat
   }
 }
 
-// z at every chunk start (without the start normaliser): zstart[c] = sum of
-// the chunk sums before c.  The loads are independent; 8 are in flight.
-__global__ void __launch_bounds__(kDK) nla_zscan_kernel(const float *__restrict__ dz, float *__restrict__ zstart,
+// z at every chunk start for each value head of the q / k head: the start
+// normaliser plus the chunk sums of phi(k) before the chunk; then z_T.  The
+// loads are independent; 8 are in flight.
+__global__ void __launch_bounds__(kDK) nla_zscan_kernel(const float *__restrict__ dz, const float *__restrict__ z0w,
+                                                        float *__restrict__ zstart, float *z_T, int H, int Hq,
                                                         int nchunks) {
-  const size_t base = (size_t)blockIdx.x * nchunks * kDK + threadIdx.x;  // blockIdx.x = b * Hq + hq
+  const int bq = blockIdx.x;  // b * Hq + hq
+  const int b = bq / Hq, hq = bq - b * Hq, rep = H / Hq;
+  const int d = threadIdx.x;
+  const size_t src = (size_t)bq * nchunks * kDK + d;
   float z = 0.f;
   for (int c0 = 0; c0 < nchunks; c0 += 8) {
     float v[8];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) v[m] = c0 + m < nchunks ? dz[base + (size_t)(c0 + m) * kDK] : 0.f;
+    for (int m = 0; m < 8; ++m) v[m] = c0 + m < nchunks ? dz[src + (size_t)(c0 + m) * kDK] : 0.f;
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      if (c0 + m < nchunks) zstart[base + (size_t)(c0 + m) * kDK] = z;
+      if (c0 + m < nchunks)
+        for (int h = hq * rep; h < (hq + 1) * rep; ++h)
+          zstart[(((size_t)b * H + h) * nchunks + c0 + m) * kDK + d] = z0w[((size_t)b * H + h) * kDK + d] + z;
       z += v[m];
     }
   }
-}
-
-struct NormParams {
-  const __nv_bfloat16 *fq, *fk;
-  const float *zstart, *z0;  // z0: the copy taken by the feature kernel
-  float *z_T;
-  const float *num;  // [B, T, H, dv] fp32 numerators
-  void *o;           // [B, T, H, dv] out_dtype (may be num itself when fp32)
-  int T, H, Hq, dv, nchunks, out_bf16;
-};
-
-// Warp w owns tokens 16w .. 16w+15 of the chunk and lane l the channels
-// l + 32m: the lane first adds up phi(k) of the tokens before the warp's
-// range, then for each of its tokens extends z and reduces phi(q) . z across
-// the warp.  No shared-memory matrix, so many CTAs fit on an SM.
-__global__ void __launch_bounds__(kDK) nla_normalize_kernel(const NormParams p) {
-  __shared__ float inv_den[kC];
-  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int hq = h / (p.H / p.Hq);
-  const int t0 = c * kC, n = min(kC, p.T - t0);
-  float zl[4];
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const int d = lane + 32 * m;
-    zl[m] = p.z0[((size_t)b * p.H + h) * kDK + d] + p.zstart[(((size_t)b * p.Hq + hq) * p.nchunks + c) * kDK + d];
-  }
-  auto row = [&](int i) { return (((size_t)b * p.T + t0 + i) * p.Hq + hq) * kDK + lane; };
-  const int first = 16 * warp;
-  // phi(k) of the tokens before this warp's range, 8 rows of loads in flight
-  for (int j0 = 0; j0 < min(first, n); j0 += 8) {
-    float v[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int m = 0; m < 4; ++m) v[j][m] = j0 + j < n ? __bfloat162float(p.fk[row(j0 + j) + 32 * m]) : 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int m = 0; m < 4; ++m) zl[m] += v[j][m];
-  }
-  // this warp's tokens, 8 at a time
-#pragma unroll
-  for (int j0 = 0; j0 < 16; j0 += 8) {
-    float fq[8][4], fk[8][4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const bool in = first + j0 + j < n;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        fq[j][m] = in ? __bfloat162float(p.fq[row(first + j0 + j) + 32 * m]) : 0.f;
-        fk[j][m] = in ? __bfloat162float(p.fk[row(first + j0 + j) + 32 * m]) : 0.f;
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float s = 0.f;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        zl[m] += fk[j][m];
-        s += fq[j][m] * zl[m];
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) inv_den[first + j0 + j] = 1.f / (s + 1e-6f);
-    }
-  }
-  // the last warp's z covers every token of the chunk
-  if (warp == 3 && c == p.nchunks - 1 && p.z_T)
-#pragma unroll
-    for (int m = 0; m < 4; ++m) p.z_T[((size_t)b * p.H + h) * kDK + lane + 32 * m] = zl[m];
-  __syncthreads();
-  const int d = tid;
-  const int nv4 = p.dv / 4;
-  const int total = n * nv4;
-  for (int e0 = 0; e0 < total; e0 += 8 * kDK) {
-    float4 x[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {  // all loads first: num may be o itself
-      const int e = e0 + m * kDK + d;
-      if (e < total) {
-        const int i = e / nv4, j = 4 * (e - i * nv4);
-        x[m] = *reinterpret_cast<const float4 *>(p.num + (((size_t)b * p.T + t0 + i) * p.H + h) * p.dv + j);
-      }
-    }
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const int e = e0 + m * kDK + d;
-      if (e < total) {
-        const int i = e / nv4, j = 4 * (e - i * nv4);
-        const size_t off = (((size_t)b * p.T + t0 + i) * p.H + h) * p.dv + j;
-        const float r = inv_den[i];
-        const float4 y = make_float4(x[m].x * r, x[m].y * r, x[m].z * r, x[m].w * r);
-        if (p.out_bf16) {
-          const __nv_bfloat162 lo = __floats2bfloat162_rn(y.x, y.y), hi = __floats2bfloat162_rn(y.z, y.w);
-          uint2 pk;
-          pk.x = *reinterpret_cast<const uint32_t *>(&lo);
-          pk.y = *reinterpret_cast<const uint32_t *>(&hi);
-          *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + off) = pk;
-        } else {
-          *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + off) = y;
-        }
-      }
-    }
-  }
+  if (z_T)
+    for (int h = hq * rep; h < (hq + 1) * rep; ++h)
+      z_T[((size_t)b * H + h) * kDK + d] = z0w[((size_t)b * H + h) * kDK + d] + z;
 }
 
 struct Carve {
   __nv_bfloat16 *fq, *fk;
-  float *dz, *zstart, *z0w, *num;
+  float *dz, *zstart, *z0w;
   size_t bytes;
 };
 
@@ -249,17 +156,16 @@ Carve carve(void *base, const glinattn_prefill_args &a) {
   const int nchunks = (a.seqlen + kC - 1) / kC;
   const size_t feat = align256((size_t)a.batch * a.seqlen * Hq * kDK * 2);
   const size_t dz = align256((size_t)a.batch * Hq * nchunks * kDK * 4);
+  const size_t zs = align256((size_t)a.batch * a.heads * nchunks * kDK * 4);
   const size_t zw = align256((size_t)a.batch * a.heads * kDK * 4);
-  const size_t num = a.out_dtype == GLINATTN_BF16 ? align256((size_t)a.batch * a.seqlen * a.heads * a.dv * 4) : 0;
   uint8_t *p = static_cast<uint8_t *>(base);
   Carve c;
   c.fq = reinterpret_cast<__nv_bfloat16 *>(p);
   c.fk = reinterpret_cast<__nv_bfloat16 *>(p + feat);
   c.dz = reinterpret_cast<float *>(p + 2 * feat);
   c.zstart = reinterpret_cast<float *>(p + 2 * feat + dz);
-  c.z0w = reinterpret_cast<float *>(p + 2 * feat + 2 * dz);
-  c.num = num ? reinterpret_cast<float *>(p + 2 * feat + 2 * dz + zw) : nullptr;
-  c.bytes = 2 * feat + 2 * dz + zw + num;
+  c.z0w = reinterpret_cast<float *>(p + 2 * feat + dz + zs);
+  c.bytes = 2 * feat + dz + zs + zw;
   return c;
 }
 
@@ -294,39 +200,19 @@ glinattn_status launch_nla_tc(const glinattn_prefill_args &a, cudaStream_t strea
   nla_feature_kernel<<<dim3((unsigned)nchunks, (unsigned)Hq, (unsigned)B), kFeatThreads, 0, stream>>>(fp);
   if (cudaGetLastError() != cudaSuccess) return GLINATTN_ERR_CUDA;
 
-  // the numerator: gated linear attention with every gate 1, in fp32
-  float *num = a.out_dtype == GLINATTN_BF16 ? w.num : static_cast<float *>(a.o);
+  nla_zscan_kernel<<<(unsigned)(B * Hq), kDK, 0, stream>>>(w.dz, w.z0w, w.zstart, a.z_T, H, Hq, nchunks);
+  if (cudaGetLastError() != cudaSuccess) return GLINATTN_ERR_CUDA;
+
+  // gated linear attention with every gate 1 on the features, normalised in
+  // its epilogue
   glinattn_prefill_args g = a;
   g.variant = GLINATTN_GLA;
   g.q = w.fq;
   g.k = w.fk;
   g.alpha = nullptr;
   g.beta = nullptr;
-  g.o = num;
-  g.out_dtype = GLINATTN_F32;
   g.state_every = 0;
-  const glinattn_status st = launch_prefill_tc(g, stream);
-  if (st != GLINATTN_OK) return st;
-
-  nla_zscan_kernel<<<(unsigned)(B * Hq), kDK, 0, stream>>>(w.dz, w.zstart, nchunks);
-  if (cudaGetLastError() != cudaSuccess) return GLINATTN_ERR_CUDA;
-
-  NormParams np;
-  np.fq = w.fq;
-  np.fk = w.fk;
-  np.zstart = w.zstart;
-  np.z0 = w.z0w;
-  np.z_T = a.z_T;
-  np.num = num;
-  np.o = a.o;
-  np.T = T;
-  np.H = H;
-  np.Hq = Hq;
-  np.dv = a.dv;
-  np.nchunks = nchunks;
-  np.out_bf16 = a.out_dtype == GLINATTN_BF16;
-  nla_normalize_kernel<<<dim3((unsigned)nchunks, (unsigned)H, (unsigned)B), kDK, 0, stream>>>(np);
-  return cudaGetLastError() == cudaSuccess ? GLINATTN_OK : GLINATTN_ERR_CUDA;
+  return launch_prefill_tc_nla(g, stream, nullptr, w.zstart);
 }
 
 }  // namespace glinattn

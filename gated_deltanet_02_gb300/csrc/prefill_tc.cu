@@ -72,7 +72,14 @@ constexpr uint32_t kOffG = kOffS + 4 * kTileS;                 // gate ring [sta
 constexpr uint32_t kGateBytes = 1088;                          // one GateRing entry
 constexpr uint32_t kOffBar = kOffG + kStages * kGateBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+// the normalised variant only, past the barriers: 1 / denominator ring
+// [slot][token] and z at the chunk start [stage][d_k]
+constexpr int kDenSlots = 4;
+constexpr uint32_t kOffDen = kOffBar + 256;
+constexpr uint32_t kOffZ = kOffDen + kDenSlots * kC * 4;
+constexpr uint32_t kZBytes = kDK * 4;
+constexpr uint32_t kSmemBytesNla = kOffZ + kStages * kZBytes + 1024;
+static_assert(kSmemBytesNla <= 232448, "shared memory budget");
 
 // TMEM columns: QK^T double-buffered (64 each), Q[S_hi|S_lo] (128), P V
 // double-buffered (64 each), K^T[V~hi|V~lo] (128).
@@ -86,6 +93,10 @@ struct GlaParams {
   const int *skip;  // [B, H] or NULL: units to skip (a gate elsewhere in a split sequence is invalid)
   int state_every, nblocks;  // states emitted after every state_every tokens (a multiple of 64)
   float *S_blocks;
+  // normalised linear attention: z at every chunk start, including the start
+  // normaliser, [B, H, nchunks, d_k]; the outputs are divided by
+  // phi(q_t) . z_t + 1e-6 (the kNla instances only)
+  const float *nla_z;
   const float *alpha;
   const float *S0;
   float *S_T;
@@ -97,6 +108,7 @@ struct Bars {
   uint64_t full[kStages], empty[kStages];
   uint64_t qk_ready[2], qk_free[2], p_ready[2], p_free;
   uint64_t ds_ready, ds_free, o_ready[2], o_free[2], s_ready[2];
+  uint64_t den_ready[kDenSlots];
   uint32_t tmem_base;
   int abort;
 };
@@ -116,7 +128,11 @@ static_assert(sizeof(GateRing) <= kGateBytes, "gate ring entry");
 // kOutBf16, kEmit: the output dtype and whether block states are emitted are
 // template parameters, so that each instance carries only its own paths in
 // the epilogue loop (a compact loop measured faster than runtime branches).
-template <bool kOutBf16, bool kEmit>
+// kNla: normalised linear attention (gates 1, q and k already the features):
+// warpgroup A also forms each token's denominator phi(q_t) . z_t from z at the
+// chunk start and the row sum of the masked phi(Q) phi(K)^T, and warpgroup B
+// divides the outputs by it.
+template <bool kOutBf16, bool kEmit, bool kNla>
 __global__ void __launch_bounds__(kThreads, 1)
     gla_prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, const GlaParams p) {
@@ -163,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->o_free[i], kEpiThreads);
       mbar_init(&bars->s_ready[i], kEpiThreads);
     }
+    for (int i = 0; i < kDenSlots; ++i) mbar_init(&bars->den_ready[i], kEpiThreads);
     mbar_init(&bars->p_free, 2);
     mbar_init(&bars->ds_ready, 1);
     mbar_init(&bars->ds_free, kEpiThreads);
@@ -210,8 +227,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_bar_warp(&bars->empty[s], (use & 1u) ^ 1u, abort)) break;
       if (lane == 0) {
         uint8_t *st = smem + kOffStage + s * kStageBytes;
-        mbar_arrive_expect_tx(&bars->full[s], kStageBytes);
+        mbar_arrive_expect_tx(&bars->full[s], kNla ? kStageBytes + kZBytes : kStageBytes);
         const int t0 = c * kC;
+        if (kNla)  // z at this chunk's start travels with its tiles
+          bulk_load(smem + kOffZ + s * kZBytes, p.nla_z + (((size_t)b * p.H + h) * nchunks + c) * kDK, kZBytes,
+                    &bars->full[s]);
         tma_load_4d(st, &tq, &bars->full[s], 0, hq, t0, b);
         tma_load_4d(st + kTileQ / 2, &tq, &bars->full[s], 64, hq, t0, b);
         tma_load_4d(st + kTileQ, &tk, &bars->full[s], 0, hq, t0, b);
@@ -346,6 +366,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             qk[jj] = (j <= row) ? qk[jj] * exp2f(gi - gr.g[j]) : 0.f;
           }
         }
+        if (kNla) {
+          // phi(q_row) . z over this lane's 64 channels (its half of the Q
+          // tile), plus its half of the masked row of phi(Q) phi(K)^T
+          const int half = lane >> 4;
+          const uint32_t qrow = smem_u32(smem + kOffStage + s * kStageBytes) + half * (kTileQ / 2);
+          const float4 *zh = reinterpret_cast<const float4 *>(smem + kOffZ + s * kZBytes) + 16 * half;
+          float den = 0.f;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) den += qk[jj];
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            float x[8];
+            unpack8(lds128(qrow + swz(row, ch)), x);
+            const float4 za = zh[2 * ch], zb = zh[2 * ch + 1];
+            den = fmaf(x[0], za.x, den);
+            den = fmaf(x[1], za.y, den);
+            den = fmaf(x[2], za.z, den);
+            den = fmaf(x[3], za.w, den);
+            den = fmaf(x[4], zb.x, den);
+            den = fmaf(x[5], zb.y, den);
+            den = fmaf(x[6], zb.z, den);
+            den = fmaf(x[7], zb.w, den);
+          }
+          den += __shfl_xor_sync(0xffffffffu, den, 16);
+          if (lane < 16) reinterpret_cast<float *>(smem + kOffDen)[(c & (kDenSlots - 1)) * kC + row] = 1.f / (den + 1e-6f);
+          mbar_arrive(&bars->den_ready[c & (kDenSlots - 1)]);
+        }
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           uint4 uh, ul;
@@ -454,6 +501,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---- o = gamma_i (Q S) + P V ----------------------------------------------
       if (!wait_bar_warp(&bars->o_ready[tb], ph, abort)) { ok = false; break; }
+      float inv_den = 1.f;
+      if (kNla) {
+        const int ds = c & (kDenSlots - 1);
+        if (!wait_bar_warp(&bars->den_ready[ds], (uint32_t)(c / kDenSlots) & 1u, abort)) { ok = false; break; }
+        inv_den = reinterpret_cast<const float *>(smem + kOffDen)[ds * kC + (tok & (kC - 1))];
+      }
       tc_fence_after();
       {
         const float gi = eg_tok;
@@ -468,6 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           float ov[16];
 #pragma unroll
           for (int jj = 0; jj < 16; ++jj) ov[jj] = gi * (o1[jj] + o1l[jj]) + o2[jj];
+          if (kNla) {
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) ov[jj] *= inv_den;
+          }
           if (store) {
             if (kOutBf16) {
               uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + obase + 16 * qt);
@@ -627,6 +684,11 @@ glinattn_status launch_prefill_tc(const glinattn_prefill_args &a, cudaStream_t s
 }
 
 glinattn_status launch_prefill_tc_skip(const glinattn_prefill_args &a, cudaStream_t stream, const int *skip) {
+  return launch_prefill_tc_nla(a, stream, skip, nullptr);
+}
+
+glinattn_status launch_prefill_tc_nla(const glinattn_prefill_args &a, cudaStream_t stream, const int *skip,
+                                      const float *nla_z) {
   CUtensorMap tq, tk, tv;
   const int Hq = a.qk_heads > 0 ? a.qk_heads : a.heads;
   if (!make_act_map(&tq, a.q, a.batch, a.seqlen, Hq, kDK) ||
@@ -650,13 +712,15 @@ glinattn_status launch_prefill_tc_skip(const glinattn_prefill_args &a, cudaStrea
   p.state_every = a.state_every > 0 && a.seqlen / a.state_every > 0 ? a.state_every : 0;
   p.nblocks = p.state_every ? a.seqlen / p.state_every : 0;
   p.S_blocks = a.S_blocks;
-  auto kernel = p.out_bf16 ? (p.state_every ? gla_prefill_kernel<true, true> : gla_prefill_kernel<true, false>)
-                           : (p.state_every ? gla_prefill_kernel<false, true> : gla_prefill_kernel<false, false>);
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kSmemBytes) != cudaSuccess)
+  p.nla_z = nla_z;
+  auto kernel = nla_z ? (p.out_bf16 ? gla_prefill_kernel<true, false, true> : gla_prefill_kernel<false, false, true>)
+                : p.out_bf16 ? (p.state_every ? gla_prefill_kernel<true, true, false> : gla_prefill_kernel<true, false, false>)
+                             : (p.state_every ? gla_prefill_kernel<false, true, false> : gla_prefill_kernel<false, false, false>);
+  const uint32_t smem_bytes = nla_z ? kSmemBytesNla : kSmemBytes;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes) != cudaSuccess)
     return GLINATTN_ERR_CUDA;
   const unsigned grid = (unsigned)a.batch * (unsigned)a.heads * (unsigned)(a.dv / kBV);
-  kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  kernel<<<grid, kThreads, smem_bytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? GLINATTN_OK : GLINATTN_ERR_CUDA;
 }
 
