@@ -38,8 +38,9 @@ bool gdn_tc_supports(const glinattn_prefill_args &a);
 size_t gdn_tc_workspace_bytes(const glinattn_prefill_args &a);
 glinattn_status launch_gdn_tc(const glinattn_prefill_args &a, cudaStream_t stream);
 
-// Chunked normalised linear attention (features, gate-free chunked numerator,
-// normalisation) through a caller-provided workspace.
+// Chunked normalised linear attention (features, z at chunk starts, then the
+// gate-free chunked kernel dividing in its epilogue) through a caller-provided
+// workspace.
 bool nla_tc_supports(const glinattn_prefill_args &a);
 size_t nla_tc_workspace_bytes(const glinattn_prefill_args &a);
 glinattn_status launch_nla_tc(const glinattn_prefill_args &a, cudaStream_t stream);
