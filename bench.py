@@ -567,10 +567,11 @@ def scan_run(args, dist, dev, rank):
     pk, _ = peaks()
     B, T, D, N = 2, 4096, 2048, 16
     sc_bytes = B * T * (2 * D + 2 * N) * 2 + B * T * D * 2 + B * D * N * 4 + D * N * 4
-    # a step touches ~135 MB (inputs, y and the chunk states of the workspace):
-    # cycle over disjoint copies
+    # a step touches ~135 MB (inputs, y and the chunk end / start states the
+    # workspace holds for its 64-token chunks): cycle over disjoint copies
+    chunk_states = 2 * B * (T // 64) * D * N * 4
     steps = []
-    for i in range(rotation(sc_bytes + 2 * B * 64 * D * N * 4)):
+    for i in range(rotation(sc_bytes + chunk_states)):
         ex = inputs.selective_scan_inputs(B, T, D, N, seed=rank + 1000 * i, device=dev, dtype=torch.bfloat16)
         y = torch.empty(B, T, D, dtype=torch.bfloat16, device=dev)
         h = torch.empty(B, D, N, dtype=torch.float32, device=dev)
