@@ -34,7 +34,7 @@ def _worker(rank, ws, port, out):
 
 @pytest.mark.parametrize("ws", [2, 3])
 def test_replicas_take_the_slowest_rank(ws):
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()  # no fork of a multi-threaded process
     mp.spawn(_worker, args=(ws, _free_port(), out), nprocs=ws, join=True)
     for rank in range(ws):
         slowest, value = out[rank]
