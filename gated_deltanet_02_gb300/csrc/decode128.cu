@@ -31,6 +31,7 @@
 #include <string.h>
 
 #include "common.cuh"
+#include "frontend.cuh"
 #include "prefill_tc.cuh"
 #include "sm100.cuh"
 
@@ -353,11 +354,12 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
         for (int i = 0; i < kMaxC; ++i) {
           const int c = tid + i * kNT;
           const float x = xr[i];
-          const float y = conv ? wr[i][0] * hr[i][0] + wr[i][1] * hr[i][1] + wr[i][2] * hr[i][2] + wr[i][3] * x
+          const float y = conv ? fe::conv4(wr[i][0], wr[i][1], wr[i][2], wr[i][3], hr[i][0], hr[i][1], hr[i][2], x)
                                : x;
           yv[i] = y;
-          if (c < kD) sq += y * y;
-          else if (c < 2 * kD) sk += y * y;
+          // one q and one k channel per thread (channel tid of each)
+          if (c < kD) sq = __fmul_rn(y, y);
+          else if (c < 2 * kD) sk = __fmul_rn(y, y);
           hr[i][0] = hr[i][1];
           hr[i][1] = hr[i][2];
           hr[i][2] = x;
@@ -368,22 +370,16 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
           }
         }
         float iq = 1.f, ik = 1.f;
-        if (p.qk_l2norm) {
-          sq = warp_sum(sq);
-          sk = warp_sum(sk);
+        if (p.qk_l2norm) {  // pairwise sums of squares: lanes, then warps
+          sq = fe::warp_pairwise_sum(sq);
+          sk = fe::warp_pairwise_sum(sk);
           if (lane == 0) {
             s_wsum[warp] = sq;
             s_wsum[kNW + warp] = sk;
           }
           __syncthreads();
-          float tq = 0.f, tk = 0.f;
-#pragma unroll
-          for (int w = 0; w < kNW; ++w) {
-            tq += s_wsum[w];
-            tk += s_wsum[kNW + w];
-          }
-          iq = 1.f / sqrtf(tq + 1e-6f);
-          ik = 1.f / sqrtf(tk + 1e-6f);
+          iq = fe::inv_norm(fe::pairwise_sum<kNW>(s_wsum));
+          ik = fe::inv_norm(fe::pairwise_sum<kNW>(s_wsum + kNW));
         }
         const bool round_act = in_bf16 && (conv || p.qk_l2norm);
         float qk_part = 0.f;
@@ -394,8 +390,8 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
             const int c = tid + i * kNT;
             if (c < kNCH) {
               float y = yv[i];
-              if (c < kD) y *= iq;
-              else if (c < 2 * kD) y *= ik;
+              if (c < kD) y = __fmul_rn(y, iq);
+              else if (c < 2 * kD) y = __fmul_rn(y, ik);
               if (round_act) y = __bfloat162float(__float2bfloat16_rn(y));
               s_act[c] = y;
               if (c < kD) qv = y;

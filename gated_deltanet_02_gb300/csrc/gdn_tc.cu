@@ -32,6 +32,7 @@
 #include <string.h>
 
 #include "common.cuh"
+#include "frontend.cuh"
 #include "prefill_tc.cuh"
 #include "sm100.cuh"
 #include "tc_common.cuh"
@@ -185,15 +186,15 @@ __global__ void __launch_bounds__(kPrepThreads)
           return __uint_as_float((c2 & 1) ? (wd & 0xffff0000u) : (wd << 16));
         };
         const float4 wc = f.w[c2];
-        y[c2] = wc.x * xv(r) + wc.y * xv(r + 1) + wc.z * xv(r + 2) + wc.w * xv(r + 3);
+        y[c2] = fe::conv4(wc.x, wc.y, wc.z, wc.w, xv(r), xv(r + 1), xv(r + 2), xv(r + 3));
       }
       if (part < 2 && kL2) {
-        float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
+        // pairwise sum of squares: this lane's 4 channels, then adjacent lanes
+        const float ss = fe::warp_pairwise_sum(__fadd_rn(__fadd_rn(__fmul_rn(y[0], y[0]), __fmul_rn(y[1], y[1])),
+                                                         __fadd_rn(__fmul_rn(y[2], y[2]), __fmul_rn(y[3], y[3]))));
+        const float inv = fe::inv_norm(ss);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float inv = 1.f / sqrtf(ss + 1e-6f);
-#pragma unroll
-        for (int c2 = 0; c2 < 4; ++c2) y[c2] *= inv;
+        for (int c2 = 0; c2 < 4; ++c2) y[c2] = __fmul_rn(y[c2], inv);
       }
       const bool valid = t0 + r0 + r < T;
       uint2 pk;

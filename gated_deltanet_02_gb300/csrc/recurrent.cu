@@ -29,6 +29,7 @@
 #include <string.h>
 
 #include "common.cuh"
+#include "frontend.cuh"
 #include "prefill_tc.cuh"
 #include "sm100.cuh"
 
@@ -84,6 +85,8 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
     recurrent_kernel(const __grid_constant__ CUtensorMap tstate, const RecurParams p) {
   using Sh = Shape<DK, DV>;
   constexpr int NW = (Sh::NT + 31) / 32;
+  static_assert(Sh::NT >= DK && Sh::NT % 32 == 0 && (NW & (NW - 1)) == 0,
+                "the L2 norm's pairwise sum wants one q and one k channel per thread and 2^m warps");
   constexpr int NCH = Sh::NCH;
   constexpr int MAXC = (NCH + Sh::NT - 1) / Sh::NT;  // front-end channels per thread
   constexpr uint32_t kSliceBytes = DK * Sh::DC * 4;
@@ -239,33 +242,28 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
     for (int i = 0; i < MAXC; ++i) {
       const int c = tid + i * Sh::NT;
       const float x = xr[i];
-      float y = conv ? wr[i][0] * hr[i][0] + wr[i][1] * hr[i][1] + wr[i][2] * hr[i][2] + wr[i][3] * x : x;
+      float y = conv ? fe::conv4(wr[i][0], wr[i][1], wr[i][2], wr[i][3], hr[i][0], hr[i][1], hr[i][2], x) : x;
       if (nla && c < 2 * DK) y = feature_map(y);
       yv[i] = y;
-      if (c < DK) sq += y * y;
-      else if (c < 2 * DK) sk += y * y;
+      // at most one q and one k channel per thread (NT >= DK)
+      if (c < DK) sq = __fmul_rn(y, y);
+      else if (c < 2 * DK) sk = __fmul_rn(y, y);
       hr[i][0] = hr[i][1];
       hr[i][1] = hr[i][2];
       hr[i][2] = x;
       if (c < NCH && t + 1 < steps_n) xr[i] = act_at(c, row + p.H);
     }
     float iq = 1.f, ik = 1.f;
-    if (p.qk_l2norm) {
-      sq = warp_sum(sq);
-      sk = warp_sum(sk);
+    if (p.qk_l2norm) {  // pairwise sums of squares: lanes, then warps
+      sq = fe::warp_pairwise_sum(sq);
+      sk = fe::warp_pairwise_sum(sk);
       if ((tid & 31) == 0) {
         s_wsum[0][tid >> 5] = sq;
         s_wsum[1][tid >> 5] = sk;
       }
       __syncthreads();
-      float tq = 0.f, tk = 0.f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        tq += s_wsum[0][w];
-        tk += s_wsum[1][w];
-      }
-      iq = 1.f / sqrtf(tq + 1e-6f);
-      ik = 1.f / sqrtf(tk + 1e-6f);
+      iq = fe::inv_norm(fe::pairwise_sum<NW>(s_wsum[0]));
+      ik = fe::inv_norm(fe::pairwise_sum<NW>(s_wsum[1]));
     }
     const bool round_act = p.in_bf16 && (conv || p.qk_l2norm || nla);
 #pragma unroll
@@ -273,8 +271,8 @@ __global__ void __launch_bounds__(Shape<DK, DV>::NT)
       const int c = tid + i * Sh::NT;
       if (c < NCH) {
         float y = yv[i];
-        if (c < DK) y *= iq;
-        else if (c < 2 * DK) y *= ik;
+        if (c < DK) y = __fmul_rn(y, iq);
+        else if (c < 2 * DK) y = __fmul_rn(y, ik);
         s_act[c] = round_act ? round_bf16(y) : y;
       }
     }

@@ -24,7 +24,10 @@ gcc on first use and composes the layer from it:
 ``oracle.chunked`` holds the second, independent fp64 path (the chunked form).
 
 Inputs are float64 numpy arrays holding exactly the values the GPU receives
-(bf16 values are exact in float64).  Outputs are float64.
+(bf16 values are exact in float64).  Outputs are float64.  The recurrences
+run in double precision; the front end of bf16 activations (conv, L2 norm,
+then the rounding to bf16, which decides a bf16 code) runs in single
+precision in the order its definitions read, see ``frontend``.
 """
 from __future__ import annotations
 
@@ -53,7 +56,8 @@ def build(force: bool = False) -> str:
              or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
     if force or stale:
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+        # -ffp-contract=off: no product and sum fused into one rounding
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
                                "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -69,8 +73,10 @@ def _load():
             lib.oracle_causal_conv.argtypes = [ctypes.c_int] * 3 + [dp] * 5
             lib.oracle_l2norm_rows.argtypes = [ctypes.c_longlong, ctypes.c_int, dp, ctypes.c_double]
             lib.oracle_round_bf16.argtypes = [ctypes.c_longlong, dp]
+            lib.oracle_causal_conv_f32.argtypes = [ctypes.c_int] * 3 + [dp] * 5
+            lib.oracle_l2norm_rows_f32.argtypes = [ctypes.c_longlong, ctypes.c_int, dp, ctypes.c_double]
             for f in (lib.oracle_recurrence, lib.oracle_causal_conv, lib.oracle_l2norm_rows,
-                      lib.oracle_round_bf16):
+                      lib.oracle_round_bf16, lib.oracle_causal_conv_f32, lib.oracle_l2norm_rows_f32):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -150,9 +156,11 @@ def recurrence(variant, q, k, v, alpha, beta=None, S0=None, return_states=False,
 # The front end: short causal convolution, L2 norm, bf16 activations
 # --------------------------------------------------------------------------
 
-def causal_conv(x, w, cache_in=None):
+def causal_conv(x, w, cache_in=None, single=False):
     """Depthwise causal conv, width 4: x [B,T,Cch], w [Cch,4], cache [B,3,Cch].
-    Returns (y [B,T,Cch], cache_out [B,3,Cch])."""
+    Returns (y [B,T,Cch], cache_out [B,3,Cch]).  ``single``: evaluated in
+    single precision, each product and sum rounded, taps oldest first (the
+    values then fit a float exactly; see ``frontend``)."""
     x, w = _f64(x), _f64(w)
     B, T, Cch = x.shape
     if w.shape != (Cch, 4):
@@ -162,16 +170,19 @@ def causal_conv(x, w, cache_in=None):
         raise ValueError("conv cache shape")
     y = np.zeros_like(x)
     cout = np.zeros((B, 3, Cch))
-    _check(_load().oracle_causal_conv(B, T, Cch, _ptr(x), _ptr(w), _ptr(cin), _ptr(y),
-                                      _ptr(cout)), "causal_conv")
+    fn = _load().oracle_causal_conv_f32 if single else _load().oracle_causal_conv
+    _check(fn(B, T, Cch, _ptr(x), _ptr(w), _ptr(cin), _ptr(y), _ptr(cout)), "causal_conv")
     return y, cout
 
 
-def l2norm_rows(x, eps=L2_EPS):
-    """Normalise the last axis: x / sqrt(sum x^2 + eps)."""
+def l2norm_rows(x, eps=L2_EPS, single=False):
+    """Normalise the last axis: x / sqrt(sum x^2 + eps).  ``single``: in single
+    precision, the sum of squares by pairwise summation, then each element
+    times 1 / sqrt(s + eps)."""
     x = _f64(x).copy()
     d = x.shape[-1]
-    _check(_load().oracle_l2norm_rows(x.size // d, d, _ptr(x), eps), "l2norm")
+    fn = _load().oracle_l2norm_rows_f32 if single else _load().oracle_l2norm_rows
+    _check(fn(x.size // d, d, _ptr(x), eps), "l2norm")
     return x
 
 
@@ -190,22 +201,29 @@ def frontend(q, k, v, conv_w=None, conv_in=None, qk_l2norm=False, act_bf16=True)
     [B, 3, H*(2dk+dv)].  Steps: optional conv (with conv_in as the history, or
     zeros), then optional L2 norm of each q and k row per head, then rounding to
     bf16 when activations are bf16.  Returns (q, k, v, conv_out or None).
+
+    With bf16 activations the rounding to bf16 decides an integer (the bf16
+    code), so the steps before it are taken in the precision the layer
+    computes them in, single precision, in the order the definitions read
+    (``causal_conv`` / ``l2norm_rows`` with ``single``); with fp32 activations
+    nothing is decided and they stay in double precision.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     conv_out = None
     changed = False
+    single = bool(act_bf16)
     if conv_w is not None:
         x = np.concatenate([q.reshape(B, T, H * dk), k.reshape(B, T, H * dk),
                             v.reshape(B, T, H * dv)], axis=-1)
-        y, conv_out = causal_conv(x, conv_w, conv_in)
+        y, conv_out = causal_conv(x, conv_w, conv_in, single=single)
         q = y[..., :H * dk].reshape(B, T, H, dk)
         k = y[..., H * dk:2 * H * dk].reshape(B, T, H, dk)
         v = y[..., 2 * H * dk:].reshape(B, T, H, dv)
         changed = True
     if qk_l2norm:
-        q, k = l2norm_rows(q), l2norm_rows(k)
+        q, k = l2norm_rows(q, single=single), l2norm_rows(k, single=single)
         changed = True
     if act_bf16 and changed:
         q, k, v = round_bf16(q), round_bf16(k), round_bf16(v)

@@ -6,7 +6,10 @@
  * baseline leg may load this library. The CUDA product path never links, loads
  * or calls it, and it shares no code, header or constant with that path.
  *
- * Every function is the plain definition, token by token, in double precision:
+ * Every function is the plain definition, token by token, in double precision
+ * (the front end has a single-precision twin, oracle_causal_conv_f32 and
+ * oracle_l2norm_rows_f32, for bf16 activations, whose rounding to bf16 is a
+ * decision taken in the precision the layer computes its front end in):
  *
  *   "Inference for linear attention and hybrid architectures",
  *   section "Two ways to write the same computation":
@@ -214,6 +217,70 @@ int oracle_l2norm_rows(long long n, int d, double *x, double eps) {
     const double inv = 1.0 / sqrt(ss + eps);
     for (int i = 0; i < d; ++i) xr[i] *= inv;
   }
+  return ORACLE_OK;
+}
+
+/*
+ * Single-precision front end.  With bf16 activations the convolution and the
+ * L2 norm end in a rounding to bf16: the value decides an integer (the bf16
+ * code), so this step is evaluated in the precision the layer computes its
+ * front end in, single precision, in the order the definitions read, every
+ * product and sum rounded on its own (no fused multiply-add):
+ *   y = ((w0 x_{t-3} + w1 x_{t-2}) + w2 x_{t-1}) + w3 x_t
+ *   s = sum of y_i^2 by pairwise summation (the row split in halves,
+ *       recursively), r = 1 / sqrt(s + eps), y_i <- y_i r.
+ * Inputs and outputs are doubles holding single-precision values.
+ */
+int oracle_causal_conv_f32(int B, int T, int Cch, const double *x, const double *w,
+                           const double *cache_in, double *y, double *cache_out) {
+  if (B < 0 || T < 0 || Cch <= 0) return ORACLE_EBADARG;
+  float *hist = (float *)malloc(sizeof(float) * (size_t)(T + 3) * (size_t)Cch);
+  if (!hist) return ORACLE_ENOMEM;
+  for (int b = 0; b < B; ++b) {
+    for (int s = 0; s < 3; ++s)
+      for (int c = 0; c < Cch; ++c)
+        hist[(size_t)s * Cch + c] = cache_in ? (float)cache_in[((size_t)b * 3 + s) * Cch + c] : 0.0f;
+    for (int t = 0; t < T; ++t)
+      for (int c = 0; c < Cch; ++c) hist[(size_t)(t + 3) * Cch + c] = (float)x[((size_t)b * T + t) * Cch + c];
+    for (int t = 0; t < T; ++t)
+      for (int c = 0; c < Cch; ++c) {
+        float acc = 0.0f;
+        for (int j = 0; j < 4; ++j) {
+          const float prod = (float)w[(size_t)c * 4 + j] * hist[(size_t)(t + j) * Cch + c];
+          acc = j == 0 ? prod : acc + prod;
+        }
+        y[((size_t)b * T + t) * Cch + c] = (double)acc;
+      }
+    if (cache_out)
+      for (int s = 0; s < 3; ++s)
+        for (int c = 0; c < Cch; ++c)
+          cache_out[((size_t)b * 3 + s) * Cch + c] = (double)hist[(size_t)(T + s) * Cch + c];
+  }
+  free(hist);
+  return ORACLE_OK;
+}
+
+static float pairwise_sum_f32(const float *a, int n) {
+  if (n == 1) return a[0];
+  const int h = n / 2;
+  return pairwise_sum_f32(a, h) + pairwise_sum_f32(a + h, n - h);
+}
+
+int oracle_l2norm_rows_f32(long long n, int d, double *x, double eps) {
+  if (n < 0 || d <= 0) return ORACLE_EBADARG;
+  float *sq = (float *)malloc(sizeof(float) * (size_t)d);
+  if (!sq) return ORACLE_ENOMEM;
+  const float epsf = (float)eps;
+  for (long long r = 0; r < n; ++r) {
+    double *xr = x + r * d;
+    for (int i = 0; i < d; ++i) {
+      const float v = (float)xr[i];
+      sq[i] = v * v;
+    }
+    const float inv = 1.0f / sqrtf(pairwise_sum_f32(sq, d) + epsf);
+    for (int i = 0; i < d; ++i) xr[i] = (double)((float)xr[i] * inv);
+  }
+  free(sq);
   return ORACLE_OK;
 }
 

@@ -328,6 +328,81 @@ def test_l2norm_and_bf16_rounding():
 
 
 # ---------------------------------------------------------------------------
+# the single-precision front end (bf16 activations): the same definitions
+# evaluated in float, checked against the double-precision ones
+# ---------------------------------------------------------------------------
+
+U32 = 2.0 ** -24  # unit roundoff of float
+
+
+def _bf16_exact(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def test_single_precision_conv_is_double_conv_rounded():
+    rng = np.random.default_rng(42)
+    B, T, Cch = 2, 37, 24
+    x = _bf16_exact(rng.standard_normal((B, T, Cch)))
+    w = rng.standard_normal((Cch, 4)).astype(np.float32).astype(np.float64)
+    cache = _bf16_exact(rng.standard_normal((B, 3, Cch)))
+    y32, c32 = oracle.causal_conv(x, w, cache, single=True)
+    y64, c64 = oracle.causal_conv(x, w, cache)
+    np.testing.assert_array_equal(c32, c64)
+    hist = np.concatenate([cache, x], axis=1)
+    absp = sum(np.abs(w[:, j]) * np.abs(hist[:, j:j + T]) for j in range(4))
+    # 4 rounded products and 3 rounded sums: at most 7 units of roundoff of sum |w x|
+    assert (np.abs(y32 - y64) <= 7 * U32 * absp).all()
+    assert (y32 == y32.astype(np.float32)).all()  # float values
+    # small integers: every product and partial sum is exact in float
+    xi = rng.integers(-8, 9, (1, 9, 5)).astype(np.float64)
+    wi = rng.integers(-8, 9, (5, 4)).astype(np.float64)
+    np.testing.assert_array_equal(oracle.causal_conv(xi, wi, single=True)[0], oracle.causal_conv(xi, wi)[0])
+
+
+def test_single_precision_l2norm_is_double_l2norm_rounded():
+    rng = np.random.default_rng(43)
+    for d in (16, 32, 64, 128):
+        x = rng.standard_normal((7, d)).astype(np.float32).astype(np.float64) * 3
+        y32 = oracle.l2norm_rows(x, single=True)
+        y64 = oracle.l2norm_rows(x)
+        assert (np.abs(y32 - y64) <= (np.log2(d) + 6) * U32 * np.abs(y64).max(axis=-1, keepdims=True)).all()
+
+
+def test_single_precision_sum_of_squares_keeps_small_terms():
+    """Pairwise summation: 127 squares of 2^-26 beside one square of 1 are not
+    lost (added one by one to 1 in float, each would round away), so the
+    normalised 1 comes out below 1 / sqrt(1 + eps)."""
+    x = np.full((1, 128), 2.0 ** -13)
+    x[0, 0] = 1.0
+    y = oracle.l2norm_rows(x, single=True)
+    swallowed = np.float32(1.0) / np.sqrt(np.float32(1.0) + np.float32(oracle.L2_EPS))
+    assert y[0, 0] < swallowed
+    np.testing.assert_allclose(y, oracle.l2norm_rows(x), rtol=4 * U32)
+
+
+def test_single_precision_front_end_rounds_like_double_except_at_ties():
+    """Conv, L2 norm and the rounding to bf16: the bf16 values agree with the
+    double-precision front end except where the exact value lies within float
+    rounding of a bf16 rounding boundary (there either neighbour is right)."""
+    B, H, T, d = 2, 3, 50, 128
+    ex = inputs.gdn_prefill(B, H, T, d, seed=44)
+    q, k, v, w = (ex[n].double().numpy() for n in ("q", "k", "v", "conv_w"))
+    q32, k32, v32, _ = oracle.frontend(q, k, v, w, None, True, act_bf16=True)
+    q64, k64, v64, _ = oracle.frontend(q, k, v, w, None, True, act_bf16=False)  # unrounded, double
+    for a32, a64 in ((q32, q64), (k32, k64), (v32, v64)):
+        r64 = oracle.round_bf16(a64)
+        diff = a32 != r64
+        assert diff.mean() < 1e-3
+        # a differing element sits next to the midpoint of its two bf16
+        # neighbours, within float rounding of the terms that produced it (a
+        # small result of a cancelling conv carries the absolute error of its
+        # larger terms)
+        lo, hi = np.minimum(a32, r64)[diff], np.maximum(a32, r64)[diff]
+        mid = (lo + hi) / 2
+        assert (np.abs(a64[diff] - mid) <= 1e-5 * np.abs(a64[diff]) + 1e-6 * np.abs(a64).max()).all()
+
+
+# ---------------------------------------------------------------------------
 # grouped q / k heads (the SSD form: state 128, head dim 64, shared B and C)
 # ---------------------------------------------------------------------------
 
