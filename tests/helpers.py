@@ -4,10 +4,14 @@ Error metric: normwise max relative error, max|x - ref| / max|ref| over the
 whole tensor (elementwise relative error is undefined near zero).  Tolerances
 for bf16 inputs: outputs 2e-3, final fp32 states 1e-3; fp32 inputs: 1e-5.
 """
+import os
+
 import numpy as np
 import torch
 
 TOL_O_BF16, TOL_S_BF16, TOL_F32 = 2e-3, 1e-3, 1e-5
+# oracle threads: every host core
+NT = os.cpu_count() or 1
 
 
 def relerr(x, ref):

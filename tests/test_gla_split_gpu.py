@@ -16,7 +16,7 @@ from gated_deltanet_02_gb300 import GLA, glinattn_prefill, inputs
 from gated_deltanet_02_gb300 import glinattn as G
 from gated_deltanet_02_gb300.glinattn import DEV_BAD_GATE
 
-from helpers import TOL_O_BF16, TOL_S_BF16, f64, relerr, to
+from helpers import TOL_O_BF16, TOL_S_BF16, NT, f64, relerr, to
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -37,7 +37,7 @@ def test_split_prefill_matches_oracle(B, H, G_, T, dv):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     o_ref, S_ref = oracle.recurrence(GLA, f64(ex["q"]), f64(ex["k"]), f64(ex["v"]), f64(ex["alpha"]),
-                                     S0=f64(ex["S0"]), nthreads=8)
+                                     S0=f64(ex["S0"]), nthreads=NT)
     assert relerr(o, o_ref) <= TOL_O_BF16 and relerr(S, S_ref) <= TOL_S_BF16
 
 

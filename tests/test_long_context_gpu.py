@@ -16,7 +16,7 @@ import torch
 import oracle
 from gated_deltanet_02_gb300 import GDN, glinattn_prefill, glinattn_spec_decode, inputs
 
-from helpers import TOL_O_BF16, TOL_S_BF16, f64, relerr
+from helpers import TOL_O_BF16, TOL_S_BF16, NT, f64, relerr
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -43,22 +43,18 @@ def prefilled():
     return ex, torch.cat(outs, dim=1), S, conv
 
 
-def _head_weights(ex, h):
-    return ex["conv_w"].view(3, H, D_HEAD, 4)[:, h].reshape(3 * D_HEAD, 4)
-
-
 def test_segmented_long_prefill_matches_oracle(prefilled):
+    """Every one of the 32 heads of the three-segment prefill against the
+    oracle's one-shot prefill (all host cores)."""
     ex, o, S, conv = prefilled
-    for h in (0, 31):
-        sub = {k: ex[k][:, :, h:h + 1] for k in ("q", "k", "v", "alpha", "beta")}
-        o_ref, S_ref, c_ref = oracle.layer_prefill(GDN, *(f64(sub[k]) for k in ("q", "k", "v", "alpha",
-                                                                                 "beta")),
-                                                   None, f64(_head_weights(ex, h)), None, True)
-        assert relerr(o[:, :, h:h + 1], o_ref) <= TOL_O_BF16, h
-        assert relerr(S[:, h:h + 1], S_ref) <= TOL_S_BF16, h
-        Cq = [p * H * D_HEAD + h * D_HEAD for p in range(3)]
-        got = torch.cat([conv[:, :, c:c + D_HEAD] for c in Cq], dim=-1)
-        assert np.array_equal(f64(got), c_ref)
+    cpu = {k: ex[k].cpu() for k in ("q", "k", "v", "alpha", "beta", "conv_w")}
+    o_ref, S_ref, c_ref = oracle.layer_prefill(GDN, *(f64(cpu[k]) for k in ("q", "k", "v", "alpha", "beta")),
+                                               None, f64(cpu["conv_w"]), None, True, nthreads=NT)
+    o64, S64 = f64(o), f64(S)
+    for h in range(H):
+        assert relerr(o64[:, :, h], o_ref[:, :, h]) <= TOL_O_BF16, h
+        assert relerr(S64[:, h], S_ref[:, h]) <= TOL_S_BF16, h
+    assert np.array_equal(f64(conv), c_ref)
 
 
 def test_segmented_equals_one_shot_long(prefilled):
@@ -91,8 +87,8 @@ def test_spec_decode_rollback_long_context(prefilled):
     accept = dr["accept"].tolist()
     # rollback: the kept state of request n is src (a = 0) or dst[n, a-1]
     kept = [int(src[n]) if a == 0 else int(dst[n, a - 1]) for n, a in enumerate(accept)]
-    # oracle on sampled requests, all heads, from the prefilled state
-    for n in (0, 17, 63):
+    # the oracle for every request, all heads, from the prefilled state
+    for n in range(N_REQ):
         mini_pool = f64(S)  # slot 0: the request's copy of the prefilled state
         o_ref, pool_ref, cpool_ref = oracle.spec_decode(
             GDN, f64(dr["q"][n:n + 1]), f64(dr["k"][n:n + 1]), f64(dr["v"][n:n + 1]),

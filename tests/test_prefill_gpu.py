@@ -14,7 +14,7 @@ import oracle
 from gated_deltanet_02_gb300 import GDN, GLA, glinattn_prefill, inputs
 from oracle.chunked import chunked
 
-from helpers import TOL_F32, TOL_O_BF16, TOL_S_BF16, f64, relerr, to
+from helpers import TOL_F32, TOL_O_BF16, TOL_S_BF16, NT, f64, relerr, to
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -38,7 +38,7 @@ def _oracle_prefill(ex, variant, conv, S0=None, conv_in=None, sl=slice(None), he
     a = cut(ex["alpha"])
     b = cut(ex.get("beta")) if variant == GDN else None
     return oracle.layer_prefill(variant, q, k, v, a, b, S0, f64(ex.get("conv_w")) if conv else None,
-                                conv_in, conv, nthreads=8)
+                                conv_in, conv, nthreads=NT)
 
 
 def test_worked_example_fp32():
@@ -125,34 +125,38 @@ def test_bf16_output():
     assert (err <= np.abs(o_ref) * 2.0 ** -8 + TOL_O_BF16 * np.abs(o_ref).max()).all()
 
 
-def _sampled_full(ex, variant, conv, heads):
-    """Run the full workload on the GPU; check the listed (b, h) units in full
-    against the oracle."""
+def _full_all_units(ex, variant, conv):
+    """Run the full workload on the GPU and check every (b, h) unit in full
+    against the oracle (run over the whole batch on all host cores)."""
     g = to(ex, DEV)
     o, S, c = _gpu_prefill(g, variant, conv, S0=g.get("S0"), out_dtype=torch.float32)
-    for b, h in heads:
-        sub = {k: (v[b:b + 1, :, h:h + 1] if k in ("q", "k", "v", "alpha", "beta") and v is not None
-                   else v) for k, v in ex.items()}
-        S0 = None if ex.get("S0") is None else f64(ex["S0"][b:b + 1, h:h + 1])
-        if conv:  # the conv weights of head h only
-            H, d = ex["q"].shape[2], ex["q"].shape[3]
-            w = ex["conv_w"].view(3, H, d, 4)[:, h].reshape(3 * d, 4)
-            sub["conv_w"] = w
-        o_ref, S_ref, _ = _oracle_prefill(sub, variant, conv, S0=S0)
-        assert relerr(o[b:b + 1, :, h:h + 1], o_ref) <= TOL_O_BF16, (b, h)
-        assert relerr(S[b:b + 1, h:h + 1], S_ref) <= TOL_S_BF16, (b, h)
+    del g
+    cpu = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in ex.items()}
+    S0 = None if cpu.get("S0") is None else f64(cpu["S0"])
+    o_ref, S_ref, c_ref = oracle.layer_prefill(
+        variant, f64(cpu["q"]), f64(cpu["k"]), f64(cpu["v"]), f64(cpu["alpha"]),
+        f64(cpu.get("beta")) if variant == GDN else None, S0, f64(cpu.get("conv_w")) if conv else None,
+        None, conv, nthreads=NT)
+    o64, S64 = f64(o), f64(S)
+    B, H = S64.shape[:2]
+    for b in range(B):
+        for h in range(H):
+            assert relerr(o64[b, :, h], o_ref[b, :, h]) <= TOL_O_BF16, (b, h)
+            assert relerr(S64[b, h], S_ref[b, h]) <= TOL_S_BF16, (b, h)
+    if conv:
+        assert np.array_equal(f64(c), c_ref)
 
 
-def test_gla_prefill_full_size_sampled():
-    """B=4, H=16, T=4096, d=128, bf16; units (0,0) and (3,15) in full."""
+def test_gla_prefill_full_size_all_units():
+    """B=4, H=16, T=4096, d=128, bf16: all 64 (batch, head) units in full."""
     ex = inputs.gla_prefill(4, 16, 4096, 128, seed=0, device=DEV)
-    _sampled_full(ex, GLA, False, [(0, 0), (3, 15)])
+    _full_all_units(ex, GLA, False)
 
 
-def test_gdn_prefill_full_size_sampled():
-    """B=2, H=16, T=8192, d=128, conv + L2 norm, S0 ~ N(0, 0.01)."""
+def test_gdn_prefill_full_size_all_units():
+    """B=2, H=16, T=8192, d=128, conv + L2 norm, S0 ~ N(0, 0.01): all 32 units."""
     ex = inputs.gdn_prefill(2, 16, 8192, 128, seed=0, device=DEV)
-    _sampled_full(ex, GDN, True, [(0, 5), (1, 15)])
+    _full_all_units(ex, GDN, True)
 
 
 @pytest.mark.parametrize("variant", [GLA, GDN])

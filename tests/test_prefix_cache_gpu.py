@@ -16,7 +16,7 @@ import oracle
 from gated_deltanet_02_gb300 import GDN, GLA, glinattn_decode, glinattn_prefill, glinattn_state_copy, inputs
 from gated_deltanet_02_gb300.glinattn import DEV_BAD_SLOT
 
-from helpers import TOL_F32, TOL_O_BF16, TOL_S_BF16, f64, relerr, to
+from helpers import TOL_F32, TOL_O_BF16, TOL_S_BF16, NT, f64, relerr, to
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -29,7 +29,7 @@ def _oracle_states(ex, variant, conv, conv_in=None):
                                  act_bf16=ex["q"].dtype == torch.bfloat16)
     beta = f64(ex["beta"]) if variant == GDN else None
     o, S, states = oracle.recurrence(variant, q, k, v, f64(ex["alpha"]), beta, f64(ex.get("S0")),
-                                     return_states=True, nthreads=8)
+                                     return_states=True, nthreads=NT)
     return o, S, states
 
 
@@ -101,7 +101,7 @@ def test_block_length_longer_than_segment_emits_nothing():
     o, S, _, Sb, cb = _prefill(g, GLA, False, 128)
     assert Sb.shape[1] == 0 and cb is None
     o_ref, S_ref, _ = oracle.layer_prefill(GLA, f64(ex["q"]), f64(ex["k"]), f64(ex["v"]), f64(ex["alpha"]),
-                                           nthreads=8)
+                                           nthreads=NT)
     assert relerr(o, o_ref) <= TOL_O_BF16 and relerr(S, S_ref) <= TOL_S_BF16
 
 
@@ -117,7 +117,7 @@ def test_resume_from_checkpoint_equals_one_shot(variant):
     o_ref, S_ref, c_ref = oracle.layer_prefill(variant, f64(ex["q"]), f64(ex["k"]), f64(ex["v"]),
                                                f64(ex["alpha"]), f64(ex.get("beta")) if conv else None,
                                                f64(ex.get("S0")), f64(ex.get("conv_w")) if conv else None,
-                                               None, conv, nthreads=8)
+                                               None, conv, nthreads=NT)
     for j in (0, 2, 3):
         P = (j + 1) * every
         rest = {key: (val[:, P:].contiguous() if key in ("q", "k", "v", "alpha", "beta") and val is not None
@@ -199,7 +199,7 @@ def test_copy_on_write_decode_leaves_checkpoint_intact():
     assert torch.equal(pool[ck], saved) and torch.equal(cpool[ck], csaved)
     _, S_ref, c_ref = oracle.layer_prefill(GDN, f64(ex["q"]), f64(ex["k"]), f64(ex["v"]), f64(ex["alpha"]),
                                            f64(ex["beta"]), f64(ex["S0"]), f64(ex["conv_w"]), None, True,
-                                           nthreads=8)
+                                           nthreads=NT)
     pool_ref = np.zeros((P, H, d, d))
     cpool_ref = np.zeros((P, 3, 3 * H * d))
     pool_ref[[2, 5]] = S_ref[0]

@@ -17,7 +17,7 @@ import oracle
 from gated_deltanet_02_gb300 import (GLA, glinattn_decode, glinattn_prefill, glinattn_replay,
                                      glinattn_spec_decode, inputs)
 
-from helpers import TOL_F32, TOL_O_BF16, TOL_S_BF16, f64, relerr, to
+from helpers import TOL_F32, TOL_O_BF16, TOL_S_BF16, NT, f64, relerr, to
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -40,7 +40,7 @@ def test_ssd_prefill_bf16(T, G):
     g = to(ex, DEV)
     o, S, _ = _prefill(g, g["S0"])
     o_ref, S_ref = oracle.recurrence(GLA, f64(ex["q"]), f64(ex["k"]), f64(ex["v"]), f64(ex["alpha"]),
-                                     S0=f64(ex["S0"]), nthreads=8)
+                                     S0=f64(ex["S0"]), nthreads=NT)
     assert o.shape == (2, T, 4, 64) and S.shape == (2, 4, 128, 64)
     assert relerr(o, o_ref) <= TOL_O_BF16
     assert relerr(S, S_ref) <= TOL_S_BF16
@@ -52,7 +52,7 @@ def test_grouped_gla_with_square_heads():
     g = to(ex, DEV)
     o, S, _ = _prefill(g, g["S0"])
     o_ref, S_ref = oracle.recurrence(GLA, f64(ex["q"]), f64(ex["k"]), f64(ex["v"]), f64(ex["alpha"]),
-                                     S0=f64(ex["S0"]), nthreads=8)
+                                     S0=f64(ex["S0"]), nthreads=NT)
     assert relerr(o, o_ref) <= TOL_O_BF16 and relerr(S, S_ref) <= TOL_S_BF16
 
 
@@ -74,7 +74,7 @@ def test_ssd_segments_and_checkpoints():
     g = to(ex, DEV)
     o_all, S_all, _, Sb, _ = _prefill(g, None, state_every=64)
     _, _, states = oracle.recurrence(GLA, f64(ex["q"]), f64(ex["k"]), f64(ex["v"]), f64(ex["alpha"]),
-                                     return_states=True, nthreads=8)
+                                     return_states=True, nthreads=NT)
     for j in range(T // 64):
         assert relerr(Sb[:, j], states[:, 64 * (j + 1) - 1]) <= TOL_S_BF16, j
     S, outs = None, []
