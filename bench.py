@@ -302,9 +302,12 @@ def run_ours(args):
     og = torch.empty(g["B"], g["T"], g["H"], g["d"], dtype=torch.bfloat16, device=dev)
     Sg = torch.empty(g["B"], g["H"], g["d"], g["d"], dtype=torch.float32, device=dev)
 
+    from gated_deltanet_02_gb300.glinattn import prefill_workspace_size
+    gws = torch.empty(max(1, prefill_workspace_size(g["B"], g["T"], g["H"], g["d"])), dtype=torch.uint8, device=dev)
+
     def step_gdn():
         glinattn_prefill(gx["q"], gx["k"], gx["v"], gx["alpha"], gx["beta"], gx["S0"], variant=GDN,
-                         conv_w=gx["conv_w"], qk_l2norm=True, o=og, S_T=Sg)
+                         conv_w=gx["conv_w"], qk_l2norm=True, o=og, S_T=Sg, workspace=gws)
 
     gdn_ms, gdn_per = timed_steps(step_gdn, max(2, min(args.steps, 5)), 1, dist, dev)
     gdn_bytes, gdn_flops = gdn_bytes_flops(**g)
@@ -318,7 +321,7 @@ def run_ours(args):
     def step_gdn_ck():
         glinattn_prefill(gx["q"], gx["k"], gx["v"], gx["alpha"], gx["beta"], gx["S0"], variant=GDN,
                          conv_w=gx["conv_w"], qk_l2norm=True, o=og, S_T=Sg, state_every=every, S_blocks=Sb,
-                         conv_blocks=cb)
+                         conv_blocks=cb, workspace=gws)
 
     ck_ms, _ = timed_steps(step_gdn_ck, max(2, min(args.steps, 5)), 1, dist, dev)
     ck_bytes = Sb.numel() * 4 + cb.numel() * 2
@@ -377,6 +380,11 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
+        "long_context": lc,
+        "ssd": ssd,
+        "normalized_linear_attention": nla,
+        "selective_scan": scan,
+        "cpu_baseline": cpu,
         "decode": {"value": dc["N"] * ws / (dec_ms / 1e3), "unit": "tokens/s",
                    "config": "Gated DeltaNet decode, 256 requests x 16 heads, d=128, 512-slot fp32 pool, "
                              "conv cache + L2 norm, in place",
@@ -397,12 +405,7 @@ def run_ours(args):
                         "tensor_frac": gdn_flops / (statistics.mean(gdn_per) / 1e3) / 1e12 / tc,
                         "with_checkpoints": {"state_every": every, "ms_per_step": ck_ms,
                                              "checkpoint_bytes": ck_bytes,
-                                             "overhead_frac": ck_ms / gdn_ms - 1.0}},
-        "long_context": lc,
-        "ssd": ssd,
-        "normalized_linear_attention": nla,
-        "selective_scan": scan,
-        "cpu_baseline": cpu,
+                                             "overhead_frac": ck_ms / gdn_ms - 1.0}}
     }
     print(json.dumps(line))
     if dist is not None:

@@ -20,6 +20,8 @@
 // Used when B * H * (d_v / 64) leaves more than half of the SMs idle and T
 // splits into equal pieces of at least four chunks; otherwise the prefill
 // runs unsplit.
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <string.h>
@@ -304,14 +306,17 @@ struct SplitPlan {
   int P, L;
 };
 
+// SMs of the current device, looked up once per device (the split decision,
+// and so the queried scratch size, follows the device the call runs on).
 int sm_count() {
-  static int n = [] {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return 0;
-    return v;
-  }();
-  return n;
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices && (v = cache[dev].load(std::memory_order_relaxed)) > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(v, std::memory_order_relaxed);
+  return v;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }

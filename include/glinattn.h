@@ -155,12 +155,23 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *args, glinattn_str
 /*
  * glinattn_prefill_workspace_size -- bytes of device scratch the call needs
  *   for these arguments (only sizes, variant and dtypes are read).  The
- *   chunked Gated DeltaNet kernels run in two passes: a parallel pass over all
- *   chunks stores the front-end outputs q', k', the state-independent chunk
- *   products W = (I+A)^-1 diag(beta gamma) K' and U~ = (I+A)^-1 diag(beta) V'
- *   and the gates there, about 1.3 KB per (batch, head, token); the serial
- *   pass reads them.  Every other configuration needs 0 bytes.  The caller
- *   owns the buffer; calls on one stream may reuse it.
+ *   caller owns the buffer; calls on one stream may reuse it.  Nonzero for:
+ *   - chunked Gated DeltaNet (required): a parallel pass over all chunks
+ *     stores the front-end outputs q', k', the state-independent chunk
+ *     products W = (I+A)^-1 diag(beta gamma) K' and U~ = (I+A)^-1 diag(beta) V'
+ *     and the gates there, about 1.3 KB per (batch, head, token); the serial
+ *     pass reads them;
+ *   - chunked normalised linear attention (required): the features, the
+ *     chunk sums of phi(k) and the normaliser at every chunk start;
+ *   - chunked gated linear attention when so few (batch, head) units would
+ *     leave more than half of the SMs idle (optional): with the scratch the
+ *     sequence is split into pieces -- a pass computes every piece's end
+ *     state from a zero start, a combine gives every piece its start state,
+ *     and the usual kernel then runs the pieces in parallel.  Without it (or
+ *     with a smaller one) the call runs the unsplit kernel; both orders of
+ *     summation are within the stated tolerance but can differ in the last
+ *     bits.
+ *   Every other configuration needs 0 bytes.
  */
 size_t glinattn_prefill_workspace_size(const glinattn_prefill_args *args);
 
@@ -175,8 +186,10 @@ size_t glinattn_prefill_workspace_size(const glinattn_prefill_args *args);
  *   library's device image instead.
  *
  *   - args->workspace and args->workspace_bytes are ignored; every other field
- *     means what it means for glinattn_prefill, with the same validation and
- *     the same results.
+ *     means what it means for glinattn_prefill, with the same validation.  The
+ *     results are bit for bit those of glinattn_prefill given a workspace of
+ *     at least glinattn_prefill_workspace_size() bytes (for gated linear
+ *     attention with few units that is the split path, see above).
  *   - A call whose glinattn_prefill_workspace_size() exceeds 32 MiB (about
  *     26,000 batch x head x token positions of chunked Gated DeltaNet prefill)
  *     returns GLINATTN_ERR_UNSUPPORTED and launches nothing.
