@@ -20,12 +20,20 @@
 //     rounding to bf16), [Q; K] K^T as one M = 128 MMA, A, the unit-lower
 //     inverse (I + A)^-1 in fp32, and W and U~ as MMAs.  Q', K', W (bf16), U~
 //     (fp32) and the log2 gates go to a caller-provided workspace.
-//   pass B (gdn_scan_kernel), one CTA per (batch, head, 64-wide d_v slice),
+//   pass B (gdn_scan_kernel), one CTA per (batch, head, 32-wide d_v slice),
 //     serial over chunks with the fp32 state in registers: U = U~ - W S, the
-//     outputs and the state carry, with the same warp roles as the gated
-//     linear attention kernel.
+//     outputs and the state carry.  The two output terms share one
+//     accumulator, O = c_i (Q' S + P'' U) with P''_ij = (Q'K'^T)_ij
+//     exp(g_i - g_j) / c_i and the row scale c_i = gamma_i (2^-100 for a row
+//     whose own decay is below that: its Q' S term then carries 2^-100 in
+//     place of gamma_i, a difference below 2^-100 |Q' S|).  Three threads
+//     issue MMAs: one the state chain (W S, K'^T r U), one Q'K'^T as soon as
+//     a chunk lands, one the outputs -- Q'S once W S of the chunk is done and
+//     P''U once K'^T r U is done, so the chain's MMAs never wait behind the
+//     outputs' in the tensor pipe.  The M = 64 accumulators are read with the
+//     16x256b TMEM shape (every lane of a warp holds two rows).
 //
-// Operands derived in fp32 (S, P, U, r U, the inverse) enter the MMAs as a
+// Operands derived in fp32 (S, P'', U, r U, the inverse) enter the MMAs as a
 // bf16 high part plus a bf16 remainder.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -50,14 +58,6 @@ constexpr int kD = 128;  // head size (d_k = d_v)
 // arithmetic so the compiler keeps accesses through it in the shared space.
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
-}
-
-// bf16 round-to-nearest-even of 8 floats, packed as 16 bytes.
-__device__ __forceinline__ uint4 pack8_rn(const float *x) {
-  uint32_t w[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) w[k] = bits(__floats2bfloat162_rn(x[2 * k], x[2 * k + 1]));
-  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // ================================ pass A ====================================
@@ -314,11 +314,13 @@ __global__ void __launch_bounds__(kPrepThreads)
     for (int m = 0; m < 8; ++m) xs[m] = 0.f;
 #pragma unroll
     for (int i = 0; i < kBlk; ++i) {
+      // x_j of rows not solved yet are still 0 and A is strictly lower, so
+      // the bounds can be the compile-time 4m < i: every index stays static
       float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-      for (int m = 0; 4 * m + sub < i && m < 8; m += 2) {
-        s0 += Ab[i * kLd + 4 * m + sub] * xs[m];
-        if (4 * (m + 1) + sub < i) s1 += Ab[i * kLd + 4 * (m + 1) + sub] * xs[m + 1];
+      for (int m = 0; m < 8; m += 2) {
+        if (4 * m < i) s0 = fmaf(Ab[i * kLd + 4 * m + sub], xs[m], s0);
+        if (4 * (m + 1) < i) s1 = fmaf(Ab[i * kLd + 4 * (m + 1) + sub], xs[m + 1], s1);
       }
       float sum = s0 + s1;
       sum += __shfl_xor_sync(0xffffffffu, sum, 1);
@@ -417,23 +419,29 @@ __global__ void __launch_bounds__(kPrepThreads)
 
   // ---- W (bf16) and U~ (fp32) rows to the workspace ----------------------------
   if (ok) {
-    const int q4 = warp & 3, i = 16 * q4 + lane;
+    // 16x256b reads of the M = 64 accumulators: rows r0 and r0 + 8, columns
+    // 8m + cq and + 1 of each 64-column half
+    const int q4 = warp & 3, r0 = 16 * q4 + (lane >> 2), cq = 2 * (lane & 3);
     const uint32_t base = tm + ((uint32_t)(32 * q4) << 16) + (warp < 4 ? 0u : 128u);
-    const size_t row = unit * p.Tp + t0 + i;
+    const size_t row0 = unit * p.Tp + t0 + r0, row1 = row0 + 8;
+    float v0[32], v1[32];
+    tmem_ld16x256b_x8x2(base, base + 64, v0, v1);
+    if (warp < 4) {
 #pragma unroll
-    for (int blk = 0; blk < 4; ++blk) {
-      float v[32];
-      tmem_ld32(base + 32 * blk, v);
-      if (lane < 16) {
-        if (warp < 4) {
-          uint4 *dst = reinterpret_cast<uint4 *>(p.Wp + row * kD + 32 * blk);
+      for (int m = 0; m < 16; ++m) {
+        const float *v = m < 8 ? v0 : v1;
+        const int mm = m & 7, col = 8 * m + cq;
+        *reinterpret_cast<__nv_bfloat162 *>(p.Wp + row0 * kD + col) = __floats2bfloat162_rn(v[4 * mm], v[4 * mm + 1]);
+        *reinterpret_cast<__nv_bfloat162 *>(p.Wp + row1 * kD + col) =
+            __floats2bfloat162_rn(v[4 * mm + 2], v[4 * mm + 3]);
+      }
+    } else {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) dst[k] = pack8_rn(v + 8 * k);
-        } else {
-          float4 *dst = reinterpret_cast<float4 *>(p.Up + row * kD + 32 * blk);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-        }
+      for (int m = 0; m < 16; ++m) {
+        const float *v = m < 8 ? v0 : v1;
+        const int mm = m & 7, col = 8 * m + cq;
+        *reinterpret_cast<float2 *>(p.Up + row0 * kD + col) = make_float2(v[4 * mm], v[4 * mm + 1]);
+        *reinterpret_cast<float2 *>(p.Up + row1 * kD + col) = make_float2(v[4 * mm + 2], v[4 * mm + 3]);
       }
     }
   }
@@ -453,9 +461,10 @@ constexpr int kNV = kD / kBV;    // CTAs per (batch, head)
 constexpr int kStages = 2;
 constexpr int kPrefetch = 3;  // chunks prefetched into L2 beyond the shared-memory ring
 // warp 0 TMA, warp 1 MMA issuer of the state chain (W S, K'^T r U), warps 2-5 P,
-// warps 6-9 U / state / outputs, warp 10 MMA issuer of Q'K'^T, Q'S and P U
-constexpr int kThreads = 352;
-constexpr int kEpiThreads = 128;
+// warps 6-9 U / state / outputs, warp 10 MMA issuer of the outputs (Q'S + P U),
+// warp 11 MMA issuer of Q'K'^T (a thread issues one small MMA about every 85
+// cycles, so the MMAs of a chunk are spread over three issuers)
+constexpr int kThreads = 384;
 constexpr uint32_t kTile = kC * kD * 2;        // Q', K' or W tile: 16 KiB (2 column blocks)
 constexpr uint32_t kTileU = kC * kBV * 4;      // U~ slice, fp32: 8 KiB
 constexpr uint32_t kStageBytes = 3 * kTile + kTileU;
@@ -475,8 +484,9 @@ constexpr uint32_t kScanSmem = kOffBar + 256 + 1024;
 static_assert(kScanSmem <= 232448, "shared memory budget");
 static_assert(kOffP % 1024 == 0 && kOffU % 1024 == 0 && kOffRU % 1024 == 0 && kOffS % 1024 == 0, "alignment");
 // TMEM (64 columns each, the hi and lo products side by side): Q'K'^T,
-// W[S_hi|S_lo], K'^T[rU_hi|rU_lo], Q'[S_hi|S_lo], P[U_hi|U_lo]
-constexpr uint32_t kColQK = 0, kColWS = 64, kColDS = 128, kColQS = 192, kColPU = 256;
+// W[S_hi|S_lo], K'^T[rU_hi|rU_lo], and the outputs Q'[S_hi|S_lo] + P''[U_hi|U_lo]
+constexpr uint32_t kColQK = 0, kColWS = 64, kColDS = 128, kColO = 192;
+constexpr uint32_t kScanTmCols = 256;
 
 struct ScanParams {
   int B, T, H, nchunks, Tp, out_bf16;
@@ -586,23 +596,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 2);  // one commit from each MMA issuer
+      mbar_init(&bars->empty[s], 3);  // one commit from each MMA issuer
     }
+    // arrivals: one commit, or one per warp of a warpgroup
     mbar_init(&bars->qk_ready, 1);
     mbar_init(&bars->o_ready, 1);
-    mbar_init(&bars->qk_free, kEpiThreads);
-    mbar_init(&bars->p_ready, kEpiThreads);
-    mbar_init(&bars->o_free, kEpiThreads);
+    mbar_init(&bars->qk_free, 4);
+    mbar_init(&bars->p_ready, 4);
+    mbar_init(&bars->o_free, 4);
     mbar_init(&bars->ws_ready, 1);
     mbar_init(&bars->ds_ready, 1);
     mbar_init(&bars->p_free, 2);
-    mbar_init(&bars->u_ready, kEpiThreads);
-    mbar_init(&bars->s_ready, kEpiThreads);
+    mbar_init(&bars->u_ready, 4);
+    mbar_init(&bars->s_ready, 4);
     bars->abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, 512);
+    tmem_alloc(&bars->tmem_base, kScanTmCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -685,9 +696,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 6) {
-    // ============ warpgroup A: P = (Q' K'^T) * D ============
+    // ============ warpgroup A: P'' = (Q' K'^T) masked and scaled ============
+    // P''_ij = (Q'K'^T)_ij 2^(g_i - g_j) / c_i for j <= i with the row scale
+    // c_i = 2^max(g_i, -100): the outputs are c_i (Q' S + P'' U), both terms in
+    // one accumulator.  16x256b layout: rows r0, r0 + 8, columns 8m + cq, + 1.
     const int q4 = warp & 3;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    const int r0 = 16 * q4 + (lane >> 2), cq = 2 * (lane & 3);
+    const uint32_t phi = smem_u32(smem + kOffP), plo = phi + kTileP;
     float *grow = s_g + warp * 2 * kC;
     GateRow G;
     grow_prefetch(G, p, unit, 0, lane);
@@ -696,68 +712,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float gC = grow_chunk(G, p, unit, c, lane, grow);
       if (!wait_bar_warp(&bars->qk_ready, pc, abort)) break;
       tc_fence_after();
-      // lane l < 16 holds row 16*q4 + l (M = 64 layout); it keeps columns 0..31
-      // and hands columns 32..63 to lane l + 16
       float qk[32];
-      {
-        float lo32[32], hi32[32];
-        tmem_ld32(tmem + kColQK + lane_base, lo32);
-        tmem_ld32(tmem + kColQK + 32 + lane_base, hi32);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float x = __shfl_sync(0xffffffffu, hi32[j], lane & 15);
-          qk[j] = lane < 16 ? lo32[j] : x;
-        }
-      }
+      tmem_ld16x256b_x8(tmem + kColQK + lane_base, qk);
       tc_fence_before();
-      mbar_arrive(&bars->qk_free);
-      const bool factored = gC > -100.f;
+      warp_arrive(&bars->qk_free);
+      const bool factored = gC > kRowScaleFloor;  // 2^-g <= 2^100: no overflow
       float *cfrow = grow + kC;
       if (factored) {
         cfrow[2 * lane] = exp2f(-grow[2 * lane]);
         cfrow[2 * lane + 1] = exp2f(-grow[2 * lane + 1]);
       }
       __syncwarp();
-      if (!wait_bar_warp(&bars->p_free, pc ^ 1u, abort)) break;
-      {
-        const int row = 16 * q4 + (lane & 15), jb = 32 * (lane >> 4);
-        const uint32_t phi = smem_u32(smem + kOffP), plo = phi + kTileP;
-        const float gi = grow[row];
-        if (factored) {
-          const float rf = exp2f(gi);
+      if (factored) {
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int j = jb + jj;
-            qk[jj] = (j <= row) ? qk[jj] * rf * cfrow[j] : 0.f;
-          }
-        } else {
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int j = jb + jj;
-            qk[jj] = (j <= row) ? qk[jj] * exp2f(gi - grow[j]) : 0.f;
-          }
+        for (int m = 0; m < 8; ++m) {
+          const int col = 8 * m + cq;
+          const float f0 = cfrow[col], f1 = cfrow[col + 1];
+          qk[4 * m + 0] = col <= r0 ? qk[4 * m + 0] * f0 : 0.f;
+          qk[4 * m + 1] = col + 1 <= r0 ? qk[4 * m + 1] * f1 : 0.f;
+          qk[4 * m + 2] = col <= r0 + 8 ? qk[4 * m + 2] * f0 : 0.f;
+          qk[4 * m + 3] = col + 1 <= r0 + 8 ? qk[4 * m + 3] * f1 : 0.f;
         }
+      } else {
+        const float g0 = grow[r0], g1 = grow[r0 + 8];
+        const float m0 = fmaxf(g0, kRowScaleFloor), m1 = fmaxf(g1, kRowScaleFloor);  // log2 c_i
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint4 uh, ul;
-          split8(&qk[8 * c4], uh, ul);
-          const int ch = 4 * (lane >> 4) + c4;
-          sts128(phi + swz(row, ch), uh);
-          sts128(plo + swz(row, ch), ul);
+        for (int m = 0; m < 8; ++m) {
+          const int col = 8 * m + cq;
+          const float ga = grow[col], gb = grow[col + 1];
+          qk[4 * m + 0] = col <= r0 ? qk[4 * m + 0] * exp2f((g0 - ga) - m0) : 0.f;
+          qk[4 * m + 1] = col + 1 <= r0 ? qk[4 * m + 1] * exp2f((g0 - gb) - m0) : 0.f;
+          qk[4 * m + 2] = col <= r0 + 8 ? qk[4 * m + 2] * exp2f((g1 - ga) - m1) : 0.f;
+          qk[4 * m + 3] = col + 1 <= r0 + 8 ? qk[4 * m + 3] * exp2f((g1 - gb) - m1) : 0.f;
         }
       }
+      if (!wait_bar_warp(&bars->p_free, pc ^ 1u, abort)) break;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        uint32_t h0, l0, h1, l1;
+        split2(qk[4 * m + 0], qk[4 * m + 1], h0, l0);
+        split2(qk[4 * m + 2], qk[4 * m + 3], h1, l1);
+        const uint32_t o0 = swz(r0, m) + 2 * cq, o1 = swz(r0 + 8, m) + 2 * cq;
+        sts32(phi + o0, h0);
+        sts32(plo + o0, l0);
+        sts32(phi + o1, h1);
+        sts32(plo + o1, l1);
+      }
       fence_proxy_async_smem();
-      mbar_arrive(&bars->p_ready);
+      warp_arrive(&bars->p_ready);
     }
   } else if (warp < 10) {
     // ============ warpgroup B: U, the state chain and the outputs ============
     const int q4 = warp & 3;
     const int srow = 32 * q4 + lane;
-    const bool has_tok = lane < 16;
-    const int tok = 16 * q4 + lane;
-    // U rows: lane l < 16 takes columns 0..15 of row 16*q4 + l, lane l + 16 columns 16..31
-    const int urow = 16 * q4 + (lane & 15), uh = lane >> 4;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    // the M = 64 accumulators in the 16x256b layout: rows r0, r0 + 8 and, of the
+    // 32 slice columns, 8m + cq and + 1 (m = 0..3: high parts; + 32: remainders)
+    const int r0 = 16 * q4 + (lane >> 2), cq = 2 * (lane & 3);
     float *grow = s_g + warp * 2 * kC;
     GateRow G;
     grow_prefetch(G, p, unit, 0, lane);
@@ -781,68 +792,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         sts128(sb + swz(srow, 4 + ch), vl);
       }
       fence_proxy_async_smem();
-      mbar_arrive(&bars->s_ready);
+      warp_arrive(&bars->s_ready);
     };
     write_state(0);
     bool ok = true;
+    const uint32_t ub = smem_u32(smem + kOffU), rb = smem_u32(smem + kOffRU);
     for (int c = 0; c < nchunks && ok; ++c) {
       const int s = c % kStages;
       const uint32_t pc = (uint32_t)c & 1u;
       const uint32_t sph = (uint32_t)(c / kStages) & 1u;
       const int t0 = c * kC;
       const float gC = grow_chunk(G, p, unit, c, lane, grow);
-      const float g_tok = grow[tok & (kC - 1)];
+      const float g0 = grow[r0], g1 = grow[r0 + 8];
 
-      // ---- U = U~ - W S (the hi and lo products summed) ---------------------------
+      // ---- U = U~ - W S (the hi and lo products summed), r U -----------------------
       if (!wait_bar_warp(&bars->ws_ready, pc, abort)) { ok = false; break; }
       tc_fence_after();
-      float u[16];
-      {
-        float hi[16], lo[16];
-        tmem_ld16(tmem + kColWS + lane_base, hi);        // W S_hi, columns 0..15
-        tmem_ld16(tmem + kColWS + kBV + lane_base, lo);  // W S_lo, columns 0..15
-#pragma unroll
-        for (int j = 0; j < 16; ++j) u[j] = hi[j] + lo[j];
-        tmem_ld16(tmem + kColWS + 16 + lane_base, hi);        // columns 16..31
-        tmem_ld16(tmem + kColWS + kBV + 16 + lane_base, lo);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float x = __shfl_sync(0xffffffffu, hi[j] + lo[j], lane & 15);
-          if (lane >= 16) u[j] = x;
-        }
-      }
+      float ws[32];
+      tmem_ld16x256b_x8(tmem + kColWS + lane_base, ws);
       if (!wait_bar_warp(&bars->full[s], sph, abort)) { ok = false; break; }
       if (!wait_bar_warp(&bars->p_free, pc ^ 1u, abort)) { ok = false; break; }
       {
         // the U~ slice rows are 128 bytes (32 fp32), loaded with the 128-byte swizzle
         const uint32_t ut = smem_u32(smem + kOffStage + s * kStageBytes + 3 * kTile);
+        const float ra = exp2f(gC - g0), rc = exp2f(gC - g1);
 #pragma unroll
-        for (int j = 0; j < 16; j += 4) {
-          const uint4 w4 = lds128(ut + swz(urow, 4 * uh + j / 4));
-          u[j] = __uint_as_float(w4.x) - u[j];
-          u[j + 1] = __uint_as_float(w4.y) - u[j + 1];
-          u[j + 2] = __uint_as_float(w4.z) - u[j + 2];
-          u[j + 3] = __uint_as_float(w4.w) - u[j + 3];
-        }
-        const float r = exp2f(gC - grow[urow]);
-        const uint32_t ub = smem_u32(smem + kOffU), rb = smem_u32(smem + kOffRU);
-#pragma unroll
-        for (int c8 = 0; c8 < 2; ++c8) {
-          const int ch = 2 * uh + c8;  // columns 16*uh + 8*c8 .. +7 of the slice
-          uint4 vh, vl;
-          split8(&u[8 * c8], vh, vl);
-          sts128(ub + swz(urow, ch), vh);
-          sts128(ub + swz(urow, 4 + ch), vl);
-          float ru[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) ru[i] = r * u[8 * c8 + i];
-          split8(ru, vh, vl);
-          sts128(rb + swz(urow, ch), vh);
-          sts128(rb + swz(urow, 4 + ch), vl);
+        for (int m = 0; m < 4; ++m) {
+          const int col = 8 * m + cq;
+          const uint32_t uo = 4 * (col & 3);
+          const float2 ua = lds64f(ut + swz(r0, col >> 2) + uo), uc = lds64f(ut + swz(r0 + 8, col >> 2) + uo);
+          const float a0 = ua.x - (ws[4 * m + 0] + ws[4 * m + 16]), a1 = ua.y - (ws[4 * m + 1] + ws[4 * m + 17]);
+          const float c0 = uc.x - (ws[4 * m + 2] + ws[4 * m + 18]), c1 = uc.y - (ws[4 * m + 3] + ws[4 * m + 19]);
+          uint32_t h, l;
+          split2(a0, a1, h, l);
+          sts32(ub + swz(r0, m) + 2 * cq, h);
+          sts32(ub + swz(r0, 4 + m) + 2 * cq, l);
+          split2(c0, c1, h, l);
+          sts32(ub + swz(r0 + 8, m) + 2 * cq, h);
+          sts32(ub + swz(r0 + 8, 4 + m) + 2 * cq, l);
+          split2(ra * a0, ra * a1, h, l);
+          sts32(rb + swz(r0, m) + 2 * cq, h);
+          sts32(rb + swz(r0, 4 + m) + 2 * cq, l);
+          split2(rc * c0, rc * c1, h, l);
+          sts32(rb + swz(r0 + 8, m) + 2 * cq, h);
+          sts32(rb + swz(r0 + 8, 4 + m) + 2 * cq, l);
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(&bars->u_ready);
+      warp_arrive(&bars->u_ready);
 
       // ---- S <- gamma_C S + K'^T diag(r) U (hi and lo products summed) -----------
       if (!wait_bar_warp(&bars->ds_ready, pc, abort)) { ok = false; break; }
@@ -850,13 +847,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const float gam = exp2f(gC);
         float dh[32], dl[32];
-        tmem_ld32(tmem + kColDS + lane_base, dh);
-        tmem_ld32(tmem + kColDS + kBV + lane_base, dl);
+        tmem_ld32x2(tmem + kColDS + lane_base, tmem + kColDS + kBV + lane_base, dh, dl);
 #pragma unroll
         for (int jj = 0; jj < kBV; ++jj) S[jj] = gam * S[jj] + (dh[jj] + dl[jj]);
       }
-      // buffer (c + 1) & 1 was last read by W S (done: ds_ready of chunk c - 1)
-      // and Q' S (done: o_ready of chunk c - 1) of the previous chunk
+      // buffer (c + 1) & 1 was last read by W S and Q' S of the previous chunk,
+      // both complete before that chunk's outputs were ready
       if (c + 1 < nchunks) write_state((c + 1) & 1);
       if (kEmit && ((c + 1) * kC) % p.state_every == 0 && (c + 1) * kC <= T) {
         // the state after this chunk closes a block: this thread's row slice goes out
@@ -868,40 +864,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
       }
 
-      // ---- o = gamma_i (Q' S) + P U -------------------------------------------------
+      // ---- o = c_i (Q' S + P'' U), the hi and lo columns summed -----------------------
       if (!wait_bar_warp(&bars->o_ready, pc, abort)) { ok = false; break; }
       tc_fence_after();
+      float ov[32];
+      tmem_ld16x256b_x8(tmem + kColO + lane_base, ov);
+      tc_fence_before();
+      warp_arrive(&bars->o_free);
       {
-        const float gi = exp2f(g_tok);
-        const int t = t0 + tok;
-        const bool store = has_tok && t < T;
-        const size_t obase = (((size_t)b * T + t) * p.H + h) * kD + vblk * kBV;
+        const float f0 = exp2f(fmaxf(g0, kRowScaleFloor)), f1 = exp2f(fmaxf(g1, kRowScaleFloor));
+        const int ta = t0 + r0, tb2 = ta + 8;
+        const size_t oa = (((size_t)b * T + ta) * p.H + h) * kD + vblk * kBV + cq;
+        const size_t ob2 = (((size_t)b * T + tb2) * p.H + h) * kD + vblk * kBV + cq;
 #pragma unroll
-        for (int qt = 0; qt < 2; ++qt) {
-          float a1[16], a2[16], b1[16], b2[16];
-          tmem_ld16(tmem + kColQS + 16 * qt + lane_base, a1);
-          tmem_ld16(tmem + kColQS + kBV + 16 * qt + lane_base, a2);
-          tmem_ld16(tmem + kColPU + 16 * qt + lane_base, b1);
-          tmem_ld16(tmem + kColPU + kBV + 16 * qt + lane_base, b2);
-          float ov[16];
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj) ov[jj] = gi * (a1[jj] + a2[jj]) + (b1[jj] + b2[jj]);
-          if (store) {
-            if (kOutBf16) {
-              uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + obase + 16 * qt);
-#pragma unroll
-              for (int k = 0; k < 2; ++k) dst[k] = pack8_rn(ov + 8 * k);
-            } else {
-              float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + obase + 16 * qt);
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                dst[k] = make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
-            }
+        for (int m = 0; m < 4; ++m) {
+          const float x0 = f0 * (ov[4 * m + 0] + ov[4 * m + 16]), x1 = f0 * (ov[4 * m + 1] + ov[4 * m + 17]);
+          const float y0 = f1 * (ov[4 * m + 2] + ov[4 * m + 18]), y1 = f1 * (ov[4 * m + 3] + ov[4 * m + 19]);
+          if (kOutBf16) {
+            __nv_bfloat16 *o16 = reinterpret_cast<__nv_bfloat16 *>(p.o);
+            if (ta < T) *reinterpret_cast<__nv_bfloat162 *>(o16 + oa + 8 * m) = __floats2bfloat162_rn(x0, x1);
+            if (tb2 < T) *reinterpret_cast<__nv_bfloat162 *>(o16 + ob2 + 8 * m) = __floats2bfloat162_rn(y0, y1);
+          } else {
+            float *o32 = reinterpret_cast<float *>(p.o);
+            if (ta < T) *reinterpret_cast<float2 *>(o32 + oa + 8 * m) = make_float2(x0, x1);
+            if (tb2 < T) *reinterpret_cast<float2 *>(o32 + ob2 + 8 * m) = make_float2(y0, y1);
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(&bars->o_free);
     }
     if (ok) {
       float *dst = p.S_T + ((unit * kD) + srow) * kD + vblk * kBV;
@@ -909,12 +898,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < kBV; j += 4)
         *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
-  } else {
-    // ============ MMA issuer B: Q' K'^T, Q' S and P U (off the state chain) ============
+  } else if (warp == 10) {
+    // ============ MMA issuer B: the outputs Q'S + P'' U ============
+    // Each output MMA group is issued right after the state-chain MMA it may
+    // not delay has completed (Q'S after W S, P''U after K'^T r U), so the
+    // chain's MMAs never wait behind the outputs' in the tensor pipe.
     if (lane == 0) {
-      constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);        // Q' K'^T
       constexpr uint32_t id_xs = idesc_bf16(64, 2 * kBV, false, true);    // Q' [S_hi|S_lo]
-      constexpr uint32_t id_pu = idesc_bf16(64, 2 * kBV, false, true);    // P [U_hi|U_lo]
+      constexpr uint32_t id_pu = idesc_bf16(64, 2 * kBV, false, true);    // P'' [U_hi|U_lo]
       const uint32_t sbase = smem_u32(smem);
       const uint64_t dP = desc_sw128(sbase + kOffP, 16, 1024);
       const uint64_t dU = desc_sw128(sbase + kOffU, 16, 1024);    // [U_hi | U_lo]
@@ -922,28 +913,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = c % kStages;
         const uint32_t pc = (uint32_t)c & 1u;
         const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
-        const uint64_t dQ = desc_sw128(aQ, 16, 1024), dK = desc_sw128(aQ + kTile, 16, 1024);
+        const uint64_t dQ = desc_sw128(aQ, 16, 1024);
         const uint64_t dS = desc_sw128(sbase + kOffS + (c & 1) * kTileS, 16, 1024);
-        // Q' K'^T: M = 64 tokens, N = 64 tokens, K = d_k
-        if (!wait_bar(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) break;
-        if (!wait_bar(&bars->qk_free, pc ^ 1u, abort)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
-          umma_bf16(tmem + kColQK, dQ + off, dK + off, id_qk, ks > 0);
-        }
-        umma_commit(&bars->qk_ready);
-        // Q' [S_hi | S_lo] (its accumulator is read by the previous chunk's outputs)
-        if (!wait_bar(&bars->s_ready, pc, abort)) break;
+        // Q' [S_hi | S_lo] once W S of this chunk is done (S_c is in place), and
+        // the previous chunk's outputs are read
+        if (!wait_bar(&bars->ws_ready, pc, abort)) break;
         if (!wait_bar(&bars->o_free, pc ^ 1u, abort)) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t aoff = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
-          umma_bf16(tmem + kColQS, dQ + aoff, dS + ((ks * 2048) >> 4), id_xs, ks > 0);
+          umma_bf16(tmem + kColO, dQ + aoff, dS + ((ks * 2048) >> 4), id_xs, ks > 0);
         }
-        // (Phi + Plo) [U_hi | U_lo]: M = 64, N = 64, K = 64 tokens
+        // (P''hi + P''lo) [U_hi | U_lo] into the same columns, once K'^T r U is done
+        if (!wait_bar(&bars->ds_ready, pc, abort)) break;
         if (!wait_bar(&bars->p_ready, pc, abort)) break;
         if (!wait_bar(&bars->u_ready, pc, abort)) break;
         tc_fence_after();
@@ -951,11 +934,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int part = 0; part < 2; ++part)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(tmem + kColPU, dP + ((part * kTileP + ks * 32) >> 4), dU + ((ks * 2048) >> 4), id_pu,
-                      (part | ks) != 0);
+            umma_bf16(tmem + kColO, dP + ((part * kTileP + ks * 32) >> 4), dU + ((ks * 2048) >> 4), id_pu, 1u);
         umma_commit(&bars->o_ready);
-        umma_commit(&bars->p_free);    // P and U may be rewritten
-        umma_commit(&bars->empty[s]);  // Q' and K' of this stage are read
+        umma_commit(&bars->p_free);    // P'' and U may be rewritten
+        umma_commit(&bars->empty[s]);  // Q' of this stage is read
+      }
+    }
+  } else {
+    // ============ MMA issuer QK: Q'K'^T of each chunk as soon as it may ============
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_bf16(64, 64, false, false);        // Q' K'^T
+      const uint32_t sbase = smem_u32(smem);
+      for (int c = 0; c < nchunks; ++c) {  // M = 64 tokens, N = 64 tokens, K = d_k
+        const int s = c % kStages;
+        if (!wait_bar(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) break;
+        if (!wait_bar(&bars->qk_free, ((uint32_t)c & 1u) ^ 1u, abort)) break;
+        tc_fence_after();
+        const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
+        const uint64_t dQ = desc_sw128(aQ, 16, 1024), dK = desc_sw128(aQ + kTile, 16, 1024);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = ((ks >> 2) * (kTile / 2) + (ks & 3) * 32) >> 4;
+          umma_bf16(tmem + kColQK, dQ + off, dK + off, id_qk, ks > 0);
+        }
+        umma_commit(&bars->qk_ready);
+        umma_commit(&bars->empty[s]);  // Q' and K' of this stage are read by Q'K'^T
       }
     }
   }
@@ -965,7 +968,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (*abort && tid == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_WAIT_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, kScanTmCols);
   }
 }
 

@@ -69,5 +69,26 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float *x) {
   }
 }
 
+// bf16 high parts (top 16 bits) and remainders of a pair, packed as 32 bits
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  const uint32_t u0 = __float_as_uint(x0), u1 = __float_as_uint(x1);
+  const float r0 = x0 - __uint_as_float(u0 & 0xffff0000u);
+  const float r1 = x1 - __uint_as_float(u1 & 0xffff0000u);
+  hi = __byte_perm(u0, u1, 0x7632);
+  lo = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+}
+
+// Arrive once per warp, after the warp's own work: __syncwarp orders the
+// lanes' shared-memory and TMEM accesses before lane 0's arrival.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// log2 of the smallest per-row output scale c_i of the chunked kernels: the
+// outputs are c_i (Q S + P'' V) with P''_ij = (Q K^T)_ij 2^(g_i - g_j) / c_i
+// and c_i = 2^max(g_i, -100), so no factor of P'' exceeds 2^100
+constexpr float kRowScaleFloor = -100.f;
+
 }  // namespace tc
 }  // namespace glinattn
