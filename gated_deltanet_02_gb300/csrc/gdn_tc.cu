@@ -61,22 +61,44 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 }
 
 // ================================ pass A ====================================
+//
+// Persistent: one CTA per SM walks the chunks (batch, head, chunk) w =
+// blockIdx.x, + gridDim.x, ..., heads fastest, and its warps form a pipeline
+// over consecutive chunks:
+//   warp 0       TMA: the chunk's raw q, k, v rows (64 x 3 x 128 bf16, rows
+//                past T zero-filled) into a 2-stage ring;
+//   warp 1       MMA issuer (one thread): K'K'^T of a chunk once its front
+//                end is done, W = T diag(beta gamma) K' and U~ = T diag(beta) V'
+//                of a chunk once its inverse is done;
+//   warps 2-7    front end: conv, L2 norm, bf16; Q' rows straight to global
+//                memory, K' and V' tiles into a 2-stage ring (K' also to global
+//                memory), the chunk's gates;
+//   warps 8-11   A = strict_lower(diag(beta) (K'K'^T * D)) from tensor
+//                memory, T = (I + A)^-1 in 32 x 32 blocks (the diagonal blocks
+//                by forward substitution, lane = column; T10 = -T11 A10 T00),
+//                then T diag(beta gamma) and T diag(beta) as bf16 hi / lo tiles;
+//   warps 12-15  W (bf16) and U~ (fp32) from tensor memory to global memory.
 
-constexpr int kPrepThreads = 256;
-constexpr int kBlk = 32;                         // the inverse works on 32 x 32 blocks
-constexpr uint32_t kBlkBytes = kBlk * (kBlk + 1) * 4;  // one fp32 block, rows padded to 33
-constexpr uint32_t kOffRaw = 0;                  // the chunk's raw q, k, v rows: 3 x 2 swizzled 8 KiB blocks
-constexpr uint32_t kRawBytes = 3 * 16384;        // (dead after the front end; A, T, Tm reuse it)
-constexpr uint32_t kOffA = 0;                    // A00, A10, A11 (A00 later holds X = A10 T00)
-constexpr uint32_t kOffT = 3 * kBlkBytes;        // T00, T10, T11 of T = (I + A)^-1
-constexpr uint32_t kOffTm = 25600;               // T diag(beta gamma) hi, lo and T diag(beta) hi, lo: 4 x 8 KiB
-constexpr uint32_t kOffQK = 61440;               // stacked [Q'; K']: 2 column blocks x 128 rows x 128 B
-constexpr uint32_t kOffVp = kOffQK + 32768;      // V': 2 column blocks x 64 rows x 128 B
-constexpr uint32_t kOffMisc = kOffVp + 16384;    // g2[64], beta[64], barrier, TMEM slot
-constexpr uint32_t kPrepSmem = kOffMisc + 1024 + 1024;
-static_assert(kOffT + 3 * kBlkBytes <= kOffTm && kOffTm + 4 * 8192 <= kOffQK, "pass A layout");
-static_assert(kOffRaw + kRawBytes <= kOffQK, "raw tile");
-static_assert(kOffQK % 1024 == 0 && kOffVp % 1024 == 0 && kOffTm % 1024 == 0, "alignment");
+constexpr int kPrepThreads = 512;  // 16 warps
+constexpr int kFeWarp0 = 2, kFeWarps = 6, kInvWarp0 = 8, kEpiWarp0 = 12;
+static_assert(kInvWarp0 % 4 == 0 && kEpiWarp0 % 4 == 0, "a warpgroup per role covers the four TMEM lane quarters");
+constexpr int kBlk = 32;                               // the inverse works on 32 x 32 blocks
+constexpr int kLd = kBlk + 4;                          // fp32 block rows padded to 36 (16-byte aligned)
+constexpr uint32_t kBlkBytes = kBlk * kLd * 4;
+constexpr uint32_t kRawBytes = 3 * 16384;              // q, k, v: two swizzled 8 KiB column blocks each
+constexpr uint32_t kPrepTile = 16384;                  // K' or V': two swizzled 8 KiB column blocks
+constexpr uint32_t kOffRaw = 0;                        // [2][q | k | v]
+constexpr uint32_t kOffPrep = kOffRaw + 2 * kRawBytes;  // [2][K' | V']
+constexpr uint32_t kOffPG = kOffPrep + 4 * kPrepTile;  // [2][g2[64] | beta[64]]
+constexpr uint32_t kOffTm = kOffPG + 1024;             // T diag(beta gamma) hi, lo, T diag(beta) hi, lo
+constexpr uint32_t kOffAT = kOffTm + 4 * 8192;         // A00^T, A10, A11^T, T00, T10, T11 (X reuses A00^T)
+constexpr uint32_t kOffCol = kOffAT + 6 * kBlkBytes;   // beta_k 2^g_k [64], beta_k [64]
+constexpr uint32_t kOffPBar = kOffCol + 512;
+constexpr uint32_t kPrepSmem = kOffPBar + 256 + 1024;
+static_assert(kOffPrep % 1024 == 0 && kOffTm % 1024 == 0, "swizzle atoms");
+static_assert(kPrepSmem <= 232448, "shared memory budget");
+// TMEM: K'K'^T double-buffered (64 each), W (128), U~ (128)
+constexpr uint32_t kColKK = 0, kColW = 128, kColU = 256, kPrepTmCols = 512;
 
 struct PrepParams {
   int B, T, H, nchunks, Tp, qk_l2norm, has_conv;
@@ -89,344 +111,488 @@ struct PrepParams {
   uint32_t *dev_status;
 };
 
+// Arrivals: raw_empty, prep_full one per front-end warp; kk_free, tm_ready one
+// per inverse warp; wu_free one per epilogue warp; the rest the TMA
+// transaction or one MMA commit.
+struct PrepBars {
+  uint64_t raw_full[2], raw_empty[2], prep_full[2], prep_empty[2], kk_ready[2], kk_free[2];
+  uint64_t tm_ready, tm_free, wu_ready, wu_free;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(PrepBars) <= 256, "barrier block");
+
+// AND of a predicate over the 128 threads of named barrier 1 (the inverse
+// warps), so that they leave their loop together
+__device__ __forceinline__ bool inv_all(bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+      "bar.red.and.pred p, 1, 128, p;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)ok)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void inv_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 // kConv, kL2: the front end's convolution and L2 norm as template parameters
 // (one code path per instance)
 template <bool kConv, bool kL2>
-__global__ void __launch_bounds__(kPrepThreads)
+__global__ void __launch_bounds__(kPrepThreads, 1)
     gdn_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const PrepParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  PrepBars *bars = reinterpret_cast<PrepBars *>(smem + kOffPBar);
+  volatile int *abort = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t0 = c * kC, H = p.H, T = p.T;
+  const int H = p.H, T = p.T, nch = p.nchunks;
   const int Cch = 3 * H * kD;
-  const size_t unit = (size_t)b * H + h;
-  float *g2s = reinterpret_cast<float *>(smem + kOffMisc);
-  float *betas = g2s + kC;
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kOffMisc + 512);
-  uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffMisc + 520);
-  uint64_t *bar_raw = reinterpret_cast<uint64_t *>(smem + kOffMisc + 528);
-  float *colbg = reinterpret_cast<float *>(smem + kOffMisc + 768);  // beta_k 2^g_k, 64 columns
-  uint8_t *raw = smem + kOffRaw;
+  const int nitems = p.B * H * nch;
+  // item w: head fastest, then chunk, then batch
+  auto decode = [&](int w, int &b, int &h, int &c) {
+    h = w % H;
+    const int r = w / H;
+    c = r % nch;
+    b = r / nch;
+  };
 
-  // the chunk's 64 raw rows of q, k and v by TMA (rows past T arrive as zeros)
   if (tid == 0) {
-    mbar_init(bar, 1);
-    mbar_init(bar_raw, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->raw_full[i], 1);
+      mbar_init(&bars->raw_empty[i], kFeWarps);
+      mbar_init(&bars->prep_full[i], kFeWarps);
+      mbar_init(&bars->prep_empty[i], 1);
+      mbar_init(&bars->kk_ready[i], 1);
+      mbar_init(&bars->kk_free[i], 4);
+    }
+    mbar_init(&bars->tm_ready, 4);
+    mbar_init(&bars->tm_free, 1);
+    mbar_init(&bars->wu_ready, 1);
+    mbar_init(&bars->wu_free, 4);
+    bars->abort = 0;
     fence_mbar_init();
-    mbar_arrive_expect_tx(bar_raw, kRawBytes);
-    const CUtensorMap *maps[3] = {&tq, &tk, &tv};
-#pragma unroll
-    for (int part = 0; part < 3; ++part)
-#pragma unroll
-      for (int blk = 0; blk < 2; ++blk)
-        tma_load_4d(raw + part * 16384 + blk * 8192, maps[part], bar_raw, 64 * blk, h, t0, b);
   }
-  if (warp == 0) {
-    tmem_alloc(tslot, 256);
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kPrepTmCols);
     tmem_relinquish();
   }
-  __syncthreads();  // both mbarriers are initialised before any thread waits on them
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
 
-  // ---- front end: y_t = sum_j w_j x_{t-3+j}; L2 norm of q, k rows; bf16 -------
-  // A task is (part, 8 consecutive tokens) of the chunk: a warp slides the
-  // 4-tap window along its tokens, lane l owning channels 4l .. 4l+3, so every
-  // access is 8 bytes per lane and the L2 norm is one warp reduction.  The
-  // chunk's rows come from the TMA tile; the 3 rows before the chunk (first
-  // task of each part only) from global memory, or conv_in before the
-  // sequence (zero without it).
-  struct FeTask {
-    uint2 hist[3];  // rows -3, -2, -1 of the chunk when r0 == 0
-    float4 w[4];    // the 4 taps of channels 4l .. 4l+3
-  };
-  auto fe_load = [&](int task, FeTask &f) {
-    const int part = task % 3, r0 = (task / 3) * 8;
-    const __nv_bfloat16 *src = part == 0 ? p.q : (part == 1 ? p.k : p.v);
+  if (warp == 0) {
+    // ======================= TMA: raw q, k, v rows =======================
+    if (lane == 0) {
+      prefetch_tensormap(&tq);
+      prefetch_tensormap(&tk);
+      prefetch_tensormap(&tv);
+      const CUtensorMap *maps[3] = {&tq, &tk, &tv};
+      int it = 0;
+      for (int w = blockIdx.x; w < nitems; w += gridDim.x, ++it) {
+        int b, h, c;
+        decode(w, b, h, c);
+        const int slot = it & 1;
+        if (!wait_bar(&bars->raw_empty[slot], ((uint32_t)(it >> 1) & 1u) ^ 1u, abort)) break;
+        uint8_t *raw = smem + kOffRaw + slot * kRawBytes;
+        mbar_arrive_expect_tx(&bars->raw_full[slot], kRawBytes);
 #pragma unroll
-    for (int m = 0; m < 3; ++m) {
-      const int t = t0 - 3 + m;
-      uint2 v = make_uint2(0u, 0u);
-      if (r0 == 0) {
-        if (t >= 0)
-          v = *reinterpret_cast<const uint2 *>(src + (((size_t)b * T + t) * H + h) * kD + 4 * lane);
-        else if (kConv && p.conv_in)
-          v = *reinterpret_cast<const uint2 *>(p.conv_in + ((size_t)b * 3 + (t + 3)) * Cch + part * H * kD +
-                                               h * kD + 4 * lane);
+        for (int part = 0; part < 3; ++part)
+#pragma unroll
+          for (int blk = 0; blk < 2; ++blk)
+            tma_load_4d(raw + part * 16384 + blk * 8192, maps[part], &bars->raw_full[slot], 64 * blk, h, c * kC, b);
+        // the next item's rows into L2 while this one is in flight
+        const int wn = w + gridDim.x;
+        if (wn < nitems) {
+          int bn, hn, cn;
+          decode(wn, bn, hn, cn);
+#pragma unroll
+          for (int part = 0; part < 3; ++part) {
+            tma_prefetch_l2_4d(maps[part], 0, hn, cn * kC, bn);
+            tma_prefetch_l2_4d(maps[part], 64, hn, cn * kC, bn);
+          }
+        }
       }
-      f.hist[m] = v;
     }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      constexpr uint32_t id_kk = idesc_bf16(64, 64, false, false);   // K' K'^T
+      constexpr uint32_t id_wu = idesc_bf16(64, 128, false, true);   // Tm K' and Tm V'
+      const uint32_t sbase = smem_u32(smem);
+      // Two streams of MMAs, issued in whichever order their inputs land:
+      // K'K'^T of item ik once its front end is done, W and U~ of item iu once
+      // its inverse is done (K'K'^T of item iu + 1 never waits for W, U~ of iu).
+      const int nmine = blockIdx.x < (unsigned)nitems ? (nitems - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+      int ik = 0, iu = 0;
+      uint64_t t0 = global_timer_ns();
+      while (iu < nmine) {
+        bool progressed = false;
+        if (ik < nmine && ik <= iu + 1) {
+          const int slot = ik & 1;
+          const uint32_t ph = (uint32_t)(ik >> 1) & 1u;
+          if (mbar_test(&bars->prep_full[slot], ph) && mbar_test(&bars->kk_free[slot], ph ^ 1u)) {
+            tc_fence_after();
+            // K' K'^T: M = 64, N = 64, K = d_k
+            const uint64_t dK = desc_sw128(sbase + kOffPrep + slot * 2 * kPrepTile, 16, 1024);
 #pragma unroll
-    for (int c2 = 0; c2 < 4; ++c2)
-      f.w[c2] = kConv ? *reinterpret_cast<const float4 *>(
-                                 p.conv_w + ((size_t)part * H * kD + h * kD + 4 * lane + c2) * 4)
-                           : make_float4(0.f, 0.f, 0.f, 1.f);
-  };
-  uint8_t *qk = smem + kOffQK;
-  uint8_t *vp = smem + kOffVp;
-  auto fe_compute = [&](int task, const FeTask &f) {
-    const int part = task % 3, r0 = (task / 3) * 8;
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint32_t off = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
+              umma_bf16(tmem + kColKK + slot * 64, dK + off, dK + off, id_kk, ks > 0);
+            }
+            umma_commit(&bars->kk_ready[slot]);
+            ++ik;
+            progressed = true;
+          }
+        }
+        if (iu < ik) {
+          const int slot = iu & 1;
+          const uint32_t pt = (uint32_t)iu & 1u;
+          if (mbar_test(&bars->tm_ready, pt) && mbar_test(&bars->wu_free, pt ^ 1u)) {
+            tc_fence_after();
+            // W = [Tm1_hi | Tm1_lo] K', U~ = [Tm2_hi | Tm2_lo] V': M = 64, N = 128, K = 2 x 64 tokens
+            const uint64_t dT1 = desc_sw128(sbase + kOffTm, 16, 1024);
+            const uint64_t dT2 = desc_sw128(sbase + kOffTm + 16384, 16, 1024);
+            const uint64_t dK = desc_sw128(sbase + kOffPrep + slot * 2 * kPrepTile, 8192, 1024);
+            const uint64_t dV = desc_sw128(sbase + kOffPrep + slot * 2 * kPrepTile + kPrepTile, 8192, 1024);
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint32_t aoff = (part * 8192 + ks * 32) >> 4, boff = (ks * 2048) >> 4;
+                umma_bf16(tmem + kColW, dT1 + aoff, dK + boff, id_wu, (part | ks) != 0);
+                umma_bf16(tmem + kColU, dT2 + aoff, dV + boff, id_wu, (part | ks) != 0);
+              }
+            umma_commit(&bars->wu_ready);
+            umma_commit(&bars->tm_free);
+            umma_commit(&bars->prep_empty[slot]);
+            ++iu;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t0 = global_timer_ns();
+        } else {
+          if (*abort) break;
+          if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            break;
+          }
+          __nanosleep(32);
+        }
+      }
+    }
+  } else if (warp < kInvWarp0) {
+    // ======================= front end =======================
+    // A task is (part, 8 consecutive tokens) of the chunk: the warp slides the
+    // 4-tap window along its tokens, lane l owning channels 4l .. 4l+3, so every
+    // access is 8 bytes per lane and the L2 norm is one warp reduction.  The
+    // chunk's rows come from the TMA tile; the 3 rows before the chunk (first
+    // task of each part only) from global memory, or conv_in before the
+    // sequence (zero without it).
+    // Warp fw takes the tasks fw + 6k (k = 0..3), all of part fw % 3 (the
+    // part's conv taps are loaded once per chunk), row groups fw / 3 + 2k.
+    const int fw = warp - kFeWarp0;
+    const int part = fw % 3;
+    static_assert(kFeWarps % 3 == 0 && 24 % kFeWarps == 0, "a warp's tasks share one part");
+    const __nv_bfloat16 *src = part == 0 ? p.q : (part == 1 ? p.k : p.v);
     // channels 4l .. 4l+3: column block l / 16, 16-byte chunk (l % 16) / 2, half l % 2
     const uint32_t cb = (uint32_t)(lane >> 4), ch = (uint32_t)((lane & 15) >> 1), hb = (uint32_t)(lane & 1) * 8;
-    uint2 xrow[11];  // rows r0 - 3 .. r0 + 7
+    int it = 0;
+    for (int w = blockIdx.x; w < nitems; w += gridDim.x, ++it) {
+      int b, h, c;
+      decode(w, b, h, c);
+      const int t0 = c * kC;
+      const size_t unit = (size_t)b * H + h;
+      const int slot = it & 1;
+      const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+      // the 4 taps of channels 4l .. 4l+3, as (4l, 4l + 2) and (4l + 1, 4l + 3) pairs
+      float4 wt[4];
 #pragma unroll
-    for (int m = 0; m < 11; ++m) {
-      const int tr = r0 - 3 + m;
-      xrow[m] = tr >= 0 ? *reinterpret_cast<const uint2 *>(raw + part * 16384 + cb * 8192 + swz(tr, ch) + hb)
-                        : f.hist[m < 3 ? m : 0];
+      for (int c2 = 0; c2 < 4; ++c2)
+        wt[c2] = kConv ? *reinterpret_cast<const float4 *>(p.conv_w + ((size_t)part * H * kD + h * kD + 4 * lane + c2) * 4)
+                       : make_float4(0.f, 0.f, 0.f, 1.f);
+      const fe::f2 we[4] = {fe::f2_pack(wt[0].x, wt[2].x), fe::f2_pack(wt[0].y, wt[2].y), fe::f2_pack(wt[0].z, wt[2].z),
+                            fe::f2_pack(wt[0].w, wt[2].w)};
+      const fe::f2 wo[4] = {fe::f2_pack(wt[1].x, wt[3].x), fe::f2_pack(wt[1].y, wt[3].y), fe::f2_pack(wt[1].z, wt[3].z),
+                            fe::f2_pack(wt[1].w, wt[3].w)};
+      uint2 hist[3];  // rows -3, -2, -1 of the chunk (row group 0 only)
+#pragma unroll
+      for (int m = 0; m < 3; ++m) {
+        const int t = t0 - 3 + m;
+        uint2 v = make_uint2(0u, 0u);
+        if (fw < 3) {
+          if (t >= 0)
+            v = *reinterpret_cast<const uint2 *>(src + (((size_t)b * T + t) * H + h) * kD + 4 * lane);
+          else if (kConv && p.conv_in)
+            v = *reinterpret_cast<const uint2 *>(p.conv_in + ((size_t)b * 3 + (t + 3)) * Cch + part * H * kD +
+                                                 h * kD + 4 * lane);
+        }
+        hist[m] = v;
+      }
+      if (!wait_bar_warp(&bars->prep_empty[slot], ph ^ 1u, abort)) break;  // W, U~ of chunk it - 2 are issued
+      if (fw == 0) {
+        // gates of the chunk: g2 = cumsum(log2 alpha); alpha = 1, beta = 0 past T
+        float *g2s = reinterpret_cast<float *>(smem + kOffPG + slot * 512);
+        float *betas = g2s + kC;
+        const int ta = t0 + 2 * lane, tb = ta + 1;
+        const size_t ia = ((size_t)b * T + ta) * H + h, ib = ((size_t)b * T + tb) * H + h;
+        const float a0 = ta < T ? p.alpha[ia] : 1.f, a1 = tb < T ? p.alpha[ib] : 1.f;
+        const float l0 = log2f(a0), l1 = log2f(a1);
+        float incl = l0 + l1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) excl = 0.f;
+        const float ga = excl + l0, gb = ga + l1;
+        g2s[2 * lane] = ga;
+        g2s[2 * lane + 1] = gb;
+        betas[2 * lane] = ta < T ? p.beta[ia] : 0.f;
+        betas[2 * lane + 1] = tb < T ? p.beta[ib] : 0.f;
+        p.Gp[unit * p.Tp + t0 + 2 * lane] = ga;
+        p.Gp[unit * p.Tp + t0 + 2 * lane + 1] = gb;
+      }
+      if (!wait_bar_warp(&bars->raw_full[slot], ph, abort)) break;
+      const uint8_t *raw = smem + kOffRaw + slot * kRawBytes + part * 16384 + cb * 8192;
+      uint8_t *dst_tile = part == 1 ? smem + kOffPrep + slot * 2 * kPrepTile
+                                    : smem + kOffPrep + slot * 2 * kPrepTile + kPrepTile;
+#pragma unroll 1
+      for (int k = 0; k < 4; ++k) {
+        const int r0 = (fw / 3 + 2 * k) * 8;  // the task's 8 tokens
+        // channels (4l, 4l + 2) and (4l + 1, 4l + 3) of rows r0 - 3 .. r0 + 7 as
+        // fp32 pairs: the even and the odd channels of the lane's 8 bytes
+        fe::f2 xe[11], xo[11];
+#pragma unroll
+        for (int m = 0; m < 11; ++m) {
+          const int tr = r0 - 3 + m;
+          const uint2 v = tr >= 0 ? *reinterpret_cast<const uint2 *>(raw + swz(tr, ch) + hb) : hist[m < 3 ? m : 0];
+          xe[m] = fe::bf16_lows(v.x, v.y);
+          xo[m] = fe::bf16_highs(v.x, v.y);
+        }
+        // the 8 rows are independent: each step runs over all of them
+        fe::f2 ye[8], yo[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          ye[r] = fe::conv4x2(we[0], we[1], we[2], we[3], xe[r], xe[r + 1], xe[r + 2], xe[r + 3]);
+          yo[r] = fe::conv4x2(wo[0], wo[1], wo[2], wo[3], xo[r], xo[r + 1], xo[r + 2], xo[r + 3]);
+        }
+        if (part < 2 && kL2) {
+          // this lane's ((y0^2 + y1^2) + (y2^2 + y3^2)), then across the lanes
+          float ss[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            float a, c;
+            fe::f2_unpack(fe::f2_add(fe::f2_mul(ye[r], ye[r]), fe::f2_mul(yo[r], yo[r])), a, c);
+            ss[r] = __fadd_rn(a, c);
+          }
+          const float inv = fe::inv_norm(fe::warp_pairwise_sum8(ss, lane));
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const float ir = __shfl_sync(0xffffffffu, inv, fe::row_lane(r));
+            const fe::f2 i2 = fe::f2_pack(ir, ir);
+            ye[r] = fe::f2_mul(ye[r], i2);
+            yo[r] = fe::f2_mul(yo[r], i2);
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const bool valid = t0 + r0 + r < T;
+          float y0, y1, y2, y3;
+          fe::f2_unpack(ye[r], y0, y2);
+          fe::f2_unpack(yo[r], y1, y3);
+          uint2 pk = make_uint2(0u, 0u);
+          if (valid) {
+            pk.x = bits(__floats2bfloat162_rn(y0, y1));
+            pk.y = bits(__floats2bfloat162_rn(y2, y3));
+          }
+          const int t = r0 + r;
+          const size_t grow = (unit * p.Tp + t0 + t) * kD + 4 * lane;
+          if (part == 0) {
+            *reinterpret_cast<uint2 *>(p.Qp + grow) = pk;
+          } else {
+            *reinterpret_cast<uint2 *>(dst_tile + cb * 8192 + swz(t, ch) + hb) = pk;
+            if (part == 1) *reinterpret_cast<uint2 *>(p.Kp + grow) = pk;
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      warp_arrive(&bars->prep_full[slot]);
+      warp_arrive(&bars->raw_empty[slot]);
     }
+  } else if (warp < kEpiWarp0) {
+    // ======================= A, the inverse and the T tiles =======================
+    const int iw = warp - kInvWarp0, itid = tid - 32 * kInvWarp0;  // 0..3, 0..127
+    const int q4 = warp & 3;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    const int r0 = 16 * q4 + (lane >> 2), cq = 2 * (lane & 3);
+    float *A00 = reinterpret_cast<float *>(smem + kOffAT);
+    float *A10 = A00 + kBlk * kLd;
+    float *A11 = A10 + kBlk * kLd;
+    float *T00 = A11 + kBlk * kLd;
+    float *T10 = T00 + kBlk * kLd;
+    float *T11 = T10 + kBlk * kLd;
+    float *colbg = reinterpret_cast<float *>(smem + kOffCol);
+    float *colb = colbg + kC;
+    int it = 0;
+    for (int w = blockIdx.x; w < nitems; w += gridDim.x, ++it) {
+      const int slot = it & 1;
+      const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+      bool ok = wait_bar_warp(&bars->prep_full[slot], ph, abort) && wait_bar_warp(&bars->kk_ready[slot], ph, abort);
+      if (!inv_all(ok)) break;
+      const float *g2s = reinterpret_cast<const float *>(smem + kOffPG + slot * 512);
+      const float *betas = g2s + kC;
+      tc_fence_after();
+      // ---- A_ij = beta_i 2^(g_i - g_j) (k_i . k_j) for j < i, as the blocks A00, A10, A11
+      {
+        float kk[32];
+        tmem_ld16x256b_x8(tmem + kColKK + slot * 64 + lane_base, kk);
+        tc_fence_before();
+        warp_arrive(&bars->kk_free[slot]);
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      float y[4];
+        for (int e = 0; e < 32; e += 2) {  // the pair of columns j, j + 1 of row i
+          const int i = (e & 2) ? r0 + 8 : r0, j = 8 * (e >> 2) + cq;
+          const float gi = g2s[i], bi = betas[i];
+          const float a0 = j < i ? bi * exp2f(gi - g2s[j]) * kk[e] : 0.f;
+          const float a1 = j + 1 < i ? bi * exp2f(gi - g2s[j + 1]) * kk[e + 1] : 0.f;
+          // the diagonal blocks transposed (the solve walks their columns), A10 by rows
+          if (i < kBlk) {
+            if (j < kBlk) {
+              A00[j * kLd + i] = a0;
+              A00[(j + 1) * kLd + i] = a1;
+            }
+          } else if (j < kBlk) {
+            *reinterpret_cast<float2 *>(A10 + (i - kBlk) * kLd + j) = make_float2(a0, a1);
+          } else {
+            A11[(j - kBlk) * kLd + (i - kBlk)] = a0;
+            A11[(j + 1 - kBlk) * kLd + (i - kBlk)] = a1;
+          }
+        }
+      }
+      inv_sync();
+      // ---- T00 = (I + A00)^-1 (warp 0) and T11 = (I + A11)^-1 (warp 1) by forward
+      // substitution, lane = column c, right-looking: x = e_c, then for i = 0, 1,
+      // ...: x_i is final and x_m -= A_mi x_i for m > i.  Row i of the stored
+      // transpose holds column i of A; its entries m <= i are 0 and skipped.
+      if (iw < 2) {
+        const float *At = iw ? A11 : A00;
+        float *Tb = iw ? T11 : T00;
+        float x[kBlk];
 #pragma unroll
-      for (int c2 = 0; c2 < 4; ++c2) {
-        // bf16 channel c2 of row m: low or high half of word c2 / 2
-        auto xv = [&](int m) {
-          const uint32_t wd = (c2 >> 1) ? xrow[m].y : xrow[m].x;
-          return __uint_as_float((c2 & 1) ? (wd & 0xffff0000u) : (wd << 16));
+        for (int m = 0; m < kBlk; ++m) x[m] = m == lane ? 1.f : 0.f;
+#pragma unroll
+        for (int i = 0; i < kBlk - 1; ++i) {
+#pragma unroll
+          for (int m4 = ((i + 1) / 4) * 4; m4 < kBlk; m4 += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(At + i * kLd + m4);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (m4 + e > i) x[m4 + e] = fmaf(-av[e], x[i], x[m4 + e]);
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < kBlk; ++m) Tb[m * kLd + lane] = x[m];
+      } else {
+        // column scales of T diag(beta gamma) and T diag(beta)
+        const int k = 32 * (iw - 2) + lane;
+        colbg[k] = betas[k] * exp2f(g2s[k]);
+        colb[k] = betas[k];
+      }
+      inv_sync();
+      // ---- T10 = -T11 (A10 T00): X = A10 T00 in A00's place, then T10 = -T11 X;
+      // thread: row itid >> 2, columns 8 (itid & 3) .. + 7
+      float *X = A00;
+      {
+        const int r = itid >> 2, c0 = 8 * (itid & 3);
+        // acc[0..7] += sum_m L[r][m] R[m][c0 .. c0 + 7], rows of 16-byte groups
+        auto rowprod = [&](const float *L, const float *R, float (&acc)[8]) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+#pragma unroll
+          for (int m4 = 0; m4 < kBlk; m4 += 4) {
+            const float4 l = *reinterpret_cast<const float4 *>(L + r * kLd + m4);
+            const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+              const float4 ra = *reinterpret_cast<const float4 *>(R + (m4 + mm) * kLd + c0);
+              const float4 rb = *reinterpret_cast<const float4 *>(R + (m4 + mm) * kLd + c0 + 4);
+              acc[0] = fmaf(lv[mm], ra.x, acc[0]); acc[1] = fmaf(lv[mm], ra.y, acc[1]);
+              acc[2] = fmaf(lv[mm], ra.z, acc[2]); acc[3] = fmaf(lv[mm], ra.w, acc[3]);
+              acc[4] = fmaf(lv[mm], rb.x, acc[4]); acc[5] = fmaf(lv[mm], rb.y, acc[5]);
+              acc[6] = fmaf(lv[mm], rb.z, acc[6]); acc[7] = fmaf(lv[mm], rb.w, acc[7]);
+            }
+          }
         };
-        const float4 wc = f.w[c2];
-        y[c2] = fe::conv4(wc.x, wc.y, wc.z, wc.w, xv(r), xv(r + 1), xv(r + 2), xv(r + 3));
+        float acc[8];
+        rowprod(A10, T00, acc);
+        *reinterpret_cast<float4 *>(X + r * kLd + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4 *>(X + r * kLd + c0 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        inv_sync();
+        rowprod(T11, X, acc);
+        *reinterpret_cast<float4 *>(T10 + r * kLd + c0) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+        *reinterpret_cast<float4 *>(T10 + r * kLd + c0 + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
       }
-      if (part < 2 && kL2) {
-        // pairwise sum of squares: this lane's 4 channels, then adjacent lanes
-        const float ss = fe::warp_pairwise_sum(__fadd_rn(__fadd_rn(__fmul_rn(y[0], y[0]), __fmul_rn(y[1], y[1])),
-                                                         __fadd_rn(__fmul_rn(y[2], y[2]), __fmul_rn(y[3], y[3]))));
-        const float inv = fe::inv_norm(ss);
+      // ---- T diag(beta gamma) and T diag(beta) as bf16 hi / lo MMA tiles (once
+      // the previous chunk's W and U~ MMAs have read them)
+      ok = wait_bar_warp(&bars->tm_free, ((uint32_t)it & 1u) ^ 1u, abort);
+      if (!inv_all(ok)) break;  // also orders T10's writes before the reads below
+      {
+        uint8_t *tm1 = smem + kOffTm;  // T diag(beta gamma): hi, lo
+        uint8_t *tm2 = tm1 + 16384;    // T diag(beta): hi, lo
 #pragma unroll
-        for (int c2 = 0; c2 < 4; ++c2) y[c2] = __fmul_rn(y[c2], inv);
+        for (int rep = 0; rep < 4; ++rep) {  // (row i, 8-column chunk): 512 items, 4 per thread
+          const int item = itid + 128 * rep, i = item >> 3, chk = item & 7;
+          // T[i][8 chk .. + 7]: from T00, T10 or T11 (T01 = 0)
+          const int k0 = 8 * chk;
+          const float *src = i < kBlk ? (k0 < kBlk ? T00 + i * kLd + k0 : nullptr)
+                                      : (k0 < kBlk ? T10 + (i - kBlk) * kLd + k0 : T11 + (i - kBlk) * kLd + (k0 - kBlk));
+          float tv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          if (src) {
+            const float4 ta = *reinterpret_cast<const float4 *>(src), tb = *reinterpret_cast<const float4 *>(src + 4);
+            tv[0] = ta.x; tv[1] = ta.y; tv[2] = ta.z; tv[3] = ta.w;
+            tv[4] = tb.x; tv[5] = tb.y; tv[6] = tb.z; tv[7] = tb.w;
+          }
+          float w1[8], w2[8];
+#pragma unroll
+          for (int e2 = 0; e2 < 8; ++e2) {
+            w1[e2] = tv[e2] * colbg[k0 + e2];
+            w2[e2] = tv[e2] * colb[k0 + e2];
+          }
+          uint4 h1, l1, h2, l2;
+          split8(w1, h1, l1);
+          split8(w2, h2, l2);
+          const uint32_t off = swz(i, chk);
+          *reinterpret_cast<uint4 *>(tm1 + off) = h1;
+          *reinterpret_cast<uint4 *>(tm1 + 8192 + off) = l1;
+          *reinterpret_cast<uint4 *>(tm2 + off) = h2;
+          *reinterpret_cast<uint4 *>(tm2 + 8192 + off) = l2;
+        }
       }
-      const bool valid = t0 + r0 + r < T;
-      uint2 pk;
-      pk.x = bits(__floats2bfloat162_rn(valid ? y[0] : 0.f, valid ? y[1] : 0.f));
-      pk.y = bits(__floats2bfloat162_rn(valid ? y[2] : 0.f, valid ? y[3] : 0.f));
-      const int t = r0 + r;
-      if (part < 2)
-        *reinterpret_cast<uint2 *>(qk + cb * 16384 + swz(part * kC + t, ch) + hb) = pk;
-      else
-        *reinterpret_cast<uint2 *>(vp + cb * 8192 + swz(t, ch) + hb) = pk;
+      fence_proxy_async_smem();
+      warp_arrive(&bars->tm_ready);
+      inv_sync();  // the next chunk's A may overwrite the blocks read above
     }
-  };
-  FeTask fa, fb;
-  fe_load(warp, fa);  // 24 tasks, three per warp
-  // ---- gates of the chunk (warp 0): g2 = cumsum(log2 alpha); alpha = 1, beta = 0 past T
-  if (warp == 0) {
-    const int ta = t0 + 2 * lane, tb = ta + 1;
-    const size_t ia = ((size_t)b * T + ta) * H + h, ib = ((size_t)b * T + tb) * H + h;
-    const float a0 = ta < T ? p.alpha[ia] : 1.f, a1 = tb < T ? p.alpha[ib] : 1.f;
-    const float l0 = log2f(a0), l1 = log2f(a1);
-    float incl = l0 + l1;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) excl = 0.f;
-    const float ga = excl + l0, gb = ga + l1;
-    g2s[2 * lane] = ga;
-    g2s[2 * lane + 1] = gb;
-    betas[2 * lane] = ta < T ? p.beta[ia] : 0.f;
-    betas[2 * lane + 1] = tb < T ? p.beta[ib] : 0.f;
-    p.Gp[unit * p.Tp + t0 + 2 * lane] = ga;
-    p.Gp[unit * p.Tp + t0 + 2 * lane + 1] = gb;
-  }
-
-  const bool raw_ok = mbar_wait(bar_raw, 0);  // visibility of the raw tile to this thread
-  fe_load(warp + 8, fb);
-  fe_compute(warp, fa);
-  fe_load(warp + 16, fa);
-  fe_compute(warp + 8, fb);
-  fe_compute(warp + 16, fa);
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tm = *tslot;
-  // Q', K' rows to the workspace: 2 x 64 rows x 16 chunks of 16 bytes
-  for (int it = tid; it < 2 * kC * 16; it += kPrepThreads) {
-    const int part = it >> 10, rem = it & 1023, t = rem >> 4, ch = rem & 15;
-    const uint4 v = *reinterpret_cast<const uint4 *>(qk + (ch >> 3) * 16384 + swz(part * kC + t, ch & 7));
-    __nv_bfloat16 *dst = (part == 0 ? p.Qp : p.Kp) + (unit * p.Tp + t0 + t) * kD + ch * 8;
-    *reinterpret_cast<uint4 *>(dst) = v;
-  }
-
-  // ---- [Q'; K'] K'^T: M = 128 (rows 0-63 Q'K'^T, rows 64-127 K'K'^T), N = 64
-  if (tid == 0) {
-    const uint64_t dA = desc_sw128(smem_u32(qk), 16, 1024);
-    const uint64_t dB = desc_sw128(smem_u32(qk + 8192), 16, 1024);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t off = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-      umma_bf16(tm, dA + off, dB + off, idesc_bf16(128, 64, false, false), ks > 0);
-    }
-    umma_commit(bar);
-  }
-  bool ok = __syncthreads_and(mbar_wait(bar, 0) && raw_ok);
-  tc_fence_after();
-
-  // ---- A_ij = beta_i 2^(g_i - g_j) (k_i . k_j) for j < i (rows from TMEM lanes 64..127)
-  // stored as the blocks A00, A10, A11 of 32 x 32 (A01 is zero)
-  float *A00 = reinterpret_cast<float *>(smem + kOffA);
-  float *A10 = A00 + kBlk * (kBlk + 1);
-  float *A11 = A10 + kBlk * (kBlk + 1);
-  float *T00 = reinterpret_cast<float *>(smem + kOffT);
-  float *T10 = T00 + kBlk * (kBlk + 1);
-  float *T11 = T10 + kBlk * (kBlk + 1);
-  constexpr int kLd = kBlk + 1;
-  if (ok && warp < 2) {  // column scales of T diag(beta gamma)
-    const int k = 32 * warp + lane;
-    colbg[k] = betas[k] * exp2f(g2s[k]);
-  }
-  // warps 2 and 6 read TMEM lanes 64-95 (K'K'^T rows 0-31), warps 3 and 7
-  // lanes 96-127 (rows 32-63); warp w >> 2 takes column half w >> 2.  Rows
-  // 0-31 x columns 32-63 form the zero block A01, so warp 6 has no work.
-  if (ok && (warp & 3) >= 2 && warp != 6) {
-    const int lq = warp & 3, half = warp >> 2;
-    const int i = 32 * (lq - 2) + lane;
-    float kk[32];
-    tmem_ld32(tm + ((uint32_t)(32 * lq) << 16) + 32 * half, kk);
-    const float gi = g2s[i], bi = betas[i];
-    if (lq == 2) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) A00[lane * kLd + j] = (j < i) ? bi * exp2f(gi - g2s[j]) * kk[j] : 0.f;
-    } else if (half == 0) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) A10[lane * kLd + j] = bi * exp2f(gi - g2s[j]) * kk[j];
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        A11[lane * kLd + j] = (32 + j < i) ? bi * exp2f(gi - g2s[32 + j]) * kk[j] : 0.f;
-    }
-  }
-  __syncthreads();
-
-  // ---- T = (I + A)^-1 in 32 x 32 blocks ---------------------------------------
-  // T00 = (I + A00)^-1 and T11 = (I + A11)^-1 by forward substitution, both at
-  // once: 4 lanes solve column kc of one block, lane `sub` holding x_j for
-  // j = sub (mod 4), the partial sums combined with two shuffles per row.
-  // Then T10 = -T11 A10 T00 as two fp32 products (T01 = 0).
-  if (ok) {
-    const int k = tid >> 2, sub = tid & 3, blk = k >> 5, kc = k & 31;
-    const float *Ab = blk ? A11 : A00;
-    float xs[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) xs[m] = 0.f;
-#pragma unroll
-    for (int i = 0; i < kBlk; ++i) {
-      // x_j of rows not solved yet are still 0 and A is strictly lower, so
-      // the bounds can be the compile-time 4m < i: every index stays static
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int m = 0; m < 8; m += 2) {
-        if (4 * m < i) s0 = fmaf(Ab[i * kLd + 4 * m + sub], xs[m], s0);
-        if (4 * (m + 1) < i) s1 = fmaf(Ab[i * kLd + 4 * (m + 1) + sub], xs[m + 1], s1);
-      }
-      float sum = s0 + s1;
-      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-      if ((i & 3) == sub) xs[i >> 2] = (i == kc ? 1.f : 0.f) - sum;
-    }
-    float *Tb = blk ? T11 : T00;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) Tb[(4 * m + sub) * kLd + kc] = xs[m];
-  }
-  __syncthreads();
-  float *X = A00;  // A00 is no longer needed: X = A10 T00 takes its place
-  // a warp computes rows warp, warp + 8, +16, +24 of a product, lane = column;
-  // each element of the right factor is loaded once for the four rows
-  if (ok) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int j = 0; j < kBlk; ++j) {
-      const float t = T00[j * kLd + lane];
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) acc[rr] += A10[(warp + 8 * rr) * kLd + j] * t;
-    }
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) X[(warp + 8 * rr) * kLd + lane] = acc[rr];
-  }
-  __syncthreads();
-  if (ok) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int j = 0; j < kBlk; ++j) {
-      const float x = X[j * kLd + lane];
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) acc[rr] += T11[(warp + 8 * rr) * kLd + j] * x;
-    }
-#pragma unroll
-    for (int rr = 0; rr < 4; ++rr) T10[(warp + 8 * rr) * kLd + lane] = -acc[rr];
-  }
-  __syncthreads();
-  // ---- T diag(beta gamma) and T diag(beta) as bf16 hi / lo MMA tiles ------------
-  if (ok) {
-    uint8_t *tm1 = smem + kOffTm;  // T diag(beta gamma): hi, lo
-    uint8_t *tm2 = tm1 + 16384;    // T diag(beta): hi, lo
-    for (int it = tid; it < kC * 8; it += kPrepThreads) {  // (row i, 8-column chunk)
-      const int i = it >> 3, chk = it & 7;
-      float w1[8], w2[8];
-#pragma unroll
-      for (int e2 = 0; e2 < 8; ++e2) {
-        const int k = 8 * chk + e2;
-        float tv;
-        if (i < kBlk) tv = k < kBlk ? T00[i * kLd + k] : 0.f;
-        else tv = k < kBlk ? T10[(i - kBlk) * kLd + k] : T11[(i - kBlk) * kLd + (k - kBlk)];
-        w1[e2] = tv * colbg[k];
-        w2[e2] = tv * betas[k];
-      }
-      uint32_t h1[4], l1[4], h2[4], l2[4];
-#pragma unroll
-      for (int q2 = 0; q2 < 4; ++q2) {
-        const __nv_bfloat162 a = __floats2bfloat162_rn(w1[2 * q2], w1[2 * q2 + 1]);
-        const __nv_bfloat162 c2 = __floats2bfloat162_rn(w2[2 * q2], w2[2 * q2 + 1]);
-        h1[q2] = bits(a);
-        h2[q2] = bits(c2);
-        l1[q2] = bits(__floats2bfloat162_rn(w1[2 * q2] - __low2float(a), w1[2 * q2 + 1] - __high2float(a)));
-        l2[q2] = bits(__floats2bfloat162_rn(w2[2 * q2] - __low2float(c2), w2[2 * q2 + 1] - __high2float(c2)));
-      }
-      const uint32_t off = swz(i, chk);
-      *reinterpret_cast<uint4 *>(tm1 + off) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
-      *reinterpret_cast<uint4 *>(tm1 + 8192 + off) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
-      *reinterpret_cast<uint4 *>(tm2 + off) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
-      *reinterpret_cast<uint4 *>(tm2 + 8192 + off) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
-    }
-  }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-
-  // ---- W = Tm1 K' (TMEM cols 0-127), U~ = Tm2 V' (cols 128-255): M = 64, N = 128
-  if (ok && tid == 0) {
-    const uint32_t id = idesc_bf16(64, 128, false, true);
-    const uint64_t dT1 = desc_sw128(smem_u32(smem + kOffTm), 16, 1024);
-    const uint64_t dT2 = desc_sw128(smem_u32(smem + kOffTm + 16384), 16, 1024);
-    const uint64_t dK = desc_sw128(smem_u32(qk + 8192), 16384, 1024);
-    const uint64_t dV = desc_sw128(smem_u32(vp), 8192, 1024);
-#pragma unroll
-    for (int part = 0; part < 2; ++part)
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        const uint32_t aoff = (part * 8192 + ks * 32) >> 4, boff = (ks * 2048) >> 4;
-        umma_bf16(tm, dT1 + aoff, dK + boff, id, (part | ks) != 0);
-        umma_bf16(tm + 128, dT2 + aoff, dV + boff, id, (part | ks) != 0);
-      }
-    umma_commit(bar);
-  }
-  if (ok) ok = __syncthreads_and(mbar_wait(bar, 1));
-  tc_fence_after();
-
-  // ---- W (bf16) and U~ (fp32) rows to the workspace ----------------------------
-  if (ok) {
-    // 16x256b reads of the M = 64 accumulators: rows r0 and r0 + 8, columns
-    // 8m + cq and + 1 of each 64-column half
-    const int q4 = warp & 3, r0 = 16 * q4 + (lane >> 2), cq = 2 * (lane & 3);
-    const uint32_t base = tm + ((uint32_t)(32 * q4) << 16) + (warp < 4 ? 0u : 128u);
-    const size_t row0 = unit * p.Tp + t0 + r0, row1 = row0 + 8;
-    float v0[32], v1[32];
-    tmem_ld16x256b_x8x2(base, base + 64, v0, v1);
-    if (warp < 4) {
+  } else {
+    // ======================= W (bf16) and U~ (fp32) to global memory =======================
+    const int q4 = warp & 3;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    const int r0 = 16 * q4 + (lane >> 2), cq = 2 * (lane & 3);
+    int it = 0;
+    for (int w = blockIdx.x; w < nitems; w += gridDim.x, ++it) {
+      int b, h, c;
+      decode(w, b, h, c);
+      const size_t unit = (size_t)b * H + h;
+      const size_t row0 = unit * p.Tp + c * kC + r0, row1 = row0 + 8;
+      if (!wait_bar_warp(&bars->wu_ready, (uint32_t)it & 1u, abort)) break;
+      tc_fence_after();
+      float v0[32], v1[32];
+      tmem_ld16x256b_x8x2(tmem + kColW + lane_base, tmem + kColW + 64 + lane_base, v0, v1);
 #pragma unroll
       for (int m = 0; m < 16; ++m) {
         const float *v = m < 8 ? v0 : v1;
@@ -435,7 +601,9 @@ __global__ void __launch_bounds__(kPrepThreads)
         *reinterpret_cast<__nv_bfloat162 *>(p.Wp + row1 * kD + col) =
             __floats2bfloat162_rn(v[4 * mm + 2], v[4 * mm + 3]);
       }
-    } else {
+      tmem_ld16x256b_x8x2(tmem + kColU + lane_base, tmem + kColU + 64 + lane_base, v0, v1);
+      tc_fence_before();
+      warp_arrive(&bars->wu_free);
 #pragma unroll
       for (int m = 0; m < 16; ++m) {
         const float *v = m < 8 ? v0 : v1;
@@ -445,12 +613,13 @@ __global__ void __launch_bounds__(kPrepThreads)
       }
     }
   }
+
   tc_fence_before();
   __syncthreads();
-  if (!ok && tid == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_WAIT_TIMEOUT);
-  if (warp == 0) {
+  if (*abort && tid == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_WAIT_TIMEOUT);
+  if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tm, 256);
+    tmem_dealloc(tmem, kPrepTmCols);
   }
 }
 
@@ -1039,7 +1208,13 @@ glinattn_status launch_gdn_tc(const glinattn_prefill_args &a, cudaStream_t strea
   if (!make_act_map(&rq, a.q, B, T, H, kD) || !make_act_map(&rk, a.k, B, T, H, kD) ||
       !make_act_map(&rv, a.v, B, T, H, kD))
     return GLINATTN_ERR_CUDA;
-  prep<<<dim3(nchunks, H, B), kPrepThreads, kPrepSmem, stream>>>(rq, rk, rv, pp);
+  // persistent: one CTA per SM (or per item when there are fewer)
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return GLINATTN_ERR_CUDA;
+  const long long items = (long long)B * H * nchunks;
+  const unsigned grid = (unsigned)(items < sms ? items : sms);
+  prep<<<grid, kPrepThreads, kPrepSmem, stream>>>(rq, rk, rv, pp);
   if (cudaGetLastError() != cudaSuccess) return GLINATTN_ERR_CUDA;
 
   CUtensorMap tq, tk, tw, tu;
