@@ -75,9 +75,9 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 //                memory), the chunk's gates;
 //   warps 8-11   A = strict_lower(diag(beta) (K'K'^T * D)) from tensor
 //                memory, T = (I + A)^-1 in 32 x 32 blocks (the diagonal blocks
-//                by forward substitution, lane = column; T10 = -T11 A10 T00),
-//                then T diag(beta gamma) and T diag(beta) as bf16 hi / lo tiles;
-//   warps 12-15  W (bf16) and U~ (fp32) from tensor memory to global memory.
+//                by forward substitution, lane = column; T10 = -T11 A10 T00);
+//   warps 12-15  T diag(beta gamma) and T diag(beta) as bf16 hi / lo tiles, then
+//                W (bf16) and U~ (fp32) from tensor memory to global memory.
 
 constexpr int kPrepThreads = 512;  // 16 warps
 constexpr int kFeWarp0 = 2, kFeWarps = 6, kInvWarp0 = 8, kEpiWarp0 = 12;
@@ -88,17 +88,19 @@ constexpr uint32_t kBlkBytes = kBlk * kLd * 4;
 constexpr uint32_t kRawBytes = 3 * 16384;              // q, k, v: two swizzled 8 KiB column blocks each
 constexpr uint32_t kPrepTile = 16384;                  // K' or V': two swizzled 8 KiB column blocks
 constexpr uint32_t kOffRaw = 0;                        // [2][q | k | v]
-constexpr uint32_t kOffPrep = kOffRaw + 2 * kRawBytes;  // [2][K' | V']
-constexpr uint32_t kOffPG = kOffPrep + 4 * kPrepTile;  // [2][g2[64] | beta[64]]
-constexpr uint32_t kOffTm = kOffPG + 1024;             // T diag(beta gamma) hi, lo, T diag(beta) hi, lo
-constexpr uint32_t kOffAT = kOffTm + 4 * 8192;         // A00^T, A10, A11^T, T00, T10, T11 (X reuses A00^T)
-constexpr uint32_t kOffCol = kOffAT + 6 * kBlkBytes;   // beta_k 2^g_k [64], beta_k [64]
-constexpr uint32_t kOffPBar = kOffCol + 512;
+constexpr int kPrepSlots = 3;                          // K' / V' ring depth
+constexpr uint32_t kOffPrep = kOffRaw + 2 * kRawBytes;  // [3][K' | V']
+constexpr uint32_t kOffPG = kOffPrep + kPrepSlots * 2 * kPrepTile;  // [3][g2[64] | beta[64]]
+constexpr uint32_t kOffAT = kOffPG + kPrepSlots * 512;  // A00^T, A10, A11^T, T00, T10, T11 (X reuses A00^T)
+constexpr uint32_t kOffCol = kOffAT + 6 * kBlkBytes;   // [2][beta_k 2^g_k [64], beta_k [64]]
+constexpr uint32_t kOffPBar = kOffCol + 1024;
 constexpr uint32_t kPrepSmem = kOffPBar + 256 + 1024;
-static_assert(kOffPrep % 1024 == 0 && kOffTm % 1024 == 0, "swizzle atoms");
+static_assert(kOffPrep % 1024 == 0, "swizzle atoms");
 static_assert(kPrepSmem <= 232448, "shared memory budget");
-// TMEM: K'K'^T double-buffered (64 each), W (128), U~ (128)
-constexpr uint32_t kColKK = 0, kColW = 128, kColU = 256, kPrepTmCols = 512;
+// TMEM: K'K'^T double-buffered (64 each), W (128), U~ (128), and the A operands
+// of the W and U~ MMAs: T diag(beta gamma) hi, lo, T diag(beta) hi, lo (32
+// columns each: bf16 pairs (k, k + 1) per column, rows in the M = 64 lanes)
+constexpr uint32_t kColKK = 0, kColW = 128, kColU = 256, kColTm = 384, kPrepTmCols = 512;
 
 struct PrepParams {
   int B, T, H, nchunks, Tp, qk_l2norm, has_conv;
@@ -111,12 +113,12 @@ struct PrepParams {
   uint32_t *dev_status;
 };
 
-// Arrivals: raw_empty, prep_full one per front-end warp; kk_free, tm_ready one
-// per inverse warp; wu_free one per epilogue warp; the rest the TMA
-// transaction or one MMA commit.
+// Arrivals: raw_empty, prep_full one per front-end warp; kk_free, t_ready one
+// per inverse warp; t_free, tm_ready, wu_free one per epilogue warp; the rest
+// the TMA transaction or one MMA commit.
 struct PrepBars {
-  uint64_t raw_full[2], raw_empty[2], prep_full[2], prep_empty[2], kk_ready[2], kk_free[2];
-  uint64_t tm_ready, tm_free, wu_ready, wu_free;
+  uint64_t raw_full[2], raw_empty[2], prep_full[kPrepSlots], prep_empty[kPrepSlots], kk_ready[2], kk_free[2];
+  uint64_t tm_ready, tm_free, wu_ready, wu_free, t_ready, t_free;
   uint32_t tmem_base;
   int abort;
 };
@@ -136,6 +138,8 @@ __device__ __forceinline__ bool inv_all(bool ok) {
 }
 
 __device__ __forceinline__ void inv_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// the 128 threads of the epilogue warps
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 // kConv, kL2: the front end's convolution and L2 norm as template parameters
 // (one code path per instance)
@@ -163,15 +167,19 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->raw_full[i], 1);
       mbar_init(&bars->raw_empty[i], kFeWarps);
-      mbar_init(&bars->prep_full[i], kFeWarps);
-      mbar_init(&bars->prep_empty[i], 1);
       mbar_init(&bars->kk_ready[i], 1);
       mbar_init(&bars->kk_free[i], 4);
+    }
+    for (int i = 0; i < kPrepSlots; ++i) {
+      mbar_init(&bars->prep_full[i], kFeWarps);
+      mbar_init(&bars->prep_empty[i], 1);
     }
     mbar_init(&bars->tm_ready, 4);
     mbar_init(&bars->tm_free, 1);
     mbar_init(&bars->wu_ready, 1);
     mbar_init(&bars->wu_free, 4);
+    mbar_init(&bars->t_ready, 4);
+    mbar_init(&bars->t_free, 4);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -231,44 +239,43 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       uint64_t t0 = global_timer_ns();
       while (iu < nmine) {
         bool progressed = false;
-        if (ik < nmine && ik <= iu + 1) {
-          const int slot = ik & 1;
-          const uint32_t ph = (uint32_t)(ik >> 1) & 1u;
-          if (mbar_test(&bars->prep_full[slot], ph) && mbar_test(&bars->kk_free[slot], ph ^ 1u)) {
+        if (ik < nmine) {
+          const int ps = ik % kPrepSlots, ks2 = ik & 1;
+          if (mbar_test(&bars->prep_full[ps], (uint32_t)(ik / kPrepSlots) & 1u) &&
+              mbar_test(&bars->kk_free[ks2], ((uint32_t)(ik >> 1) & 1u) ^ 1u)) {
             tc_fence_after();
             // K' K'^T: M = 64, N = 64, K = d_k
-            const uint64_t dK = desc_sw128(sbase + kOffPrep + slot * 2 * kPrepTile, 16, 1024);
+            const uint64_t dK = desc_sw128(sbase + kOffPrep + ps * 2 * kPrepTile, 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               const uint32_t off = ((ks >> 2) * 8192 + (ks & 3) * 32) >> 4;
-              umma_bf16(tmem + kColKK + slot * 64, dK + off, dK + off, id_kk, ks > 0);
+              umma_bf16(tmem + kColKK + ks2 * 64, dK + off, dK + off, id_kk, ks > 0);
             }
-            umma_commit(&bars->kk_ready[slot]);
+            umma_commit(&bars->kk_ready[ks2]);
             ++ik;
             progressed = true;
           }
         }
         if (iu < ik) {
-          const int slot = iu & 1;
+          const int ps = iu % kPrepSlots;
           const uint32_t pt = (uint32_t)iu & 1u;
           if (mbar_test(&bars->tm_ready, pt) && mbar_test(&bars->wu_free, pt ^ 1u)) {
             tc_fence_after();
-            // W = [Tm1_hi | Tm1_lo] K', U~ = [Tm2_hi | Tm2_lo] V': M = 64, N = 128, K = 2 x 64 tokens
-            const uint64_t dT1 = desc_sw128(sbase + kOffTm, 16, 1024);
-            const uint64_t dT2 = desc_sw128(sbase + kOffTm + 16384, 16, 1024);
-            const uint64_t dK = desc_sw128(sbase + kOffPrep + slot * 2 * kPrepTile, 8192, 1024);
-            const uint64_t dV = desc_sw128(sbase + kOffPrep + slot * 2 * kPrepTile + kPrepTile, 8192, 1024);
+            // W = [Tm1_hi | Tm1_lo] K', U~ = [Tm2_hi | Tm2_lo] V': M = 64, N = 128, K = 2 x 64
+            // tokens, the A operands in tensor memory (8 columns per 16 tokens)
+            const uint64_t dK = desc_sw128(sbase + kOffPrep + ps * 2 * kPrepTile, 8192, 1024);
+            const uint64_t dV = desc_sw128(sbase + kOffPrep + ps * 2 * kPrepTile + kPrepTile, 8192, 1024);
 #pragma unroll
             for (int part = 0; part < 2; ++part)
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks) {
-                const uint32_t aoff = (part * 8192 + ks * 32) >> 4, boff = (ks * 2048) >> 4;
-                umma_bf16(tmem + kColW, dT1 + aoff, dK + boff, id_wu, (part | ks) != 0);
-                umma_bf16(tmem + kColU, dT2 + aoff, dV + boff, id_wu, (part | ks) != 0);
+                const uint32_t acol = kColTm + part * 32 + ks * 8, boff = (ks * 2048) >> 4;
+                umma_bf16_tmem_a(tmem + kColW, tmem + acol, dK + boff, id_wu, (part | ks) != 0);
+                umma_bf16_tmem_a(tmem + kColU, tmem + acol + 64, dV + boff, id_wu, (part | ks) != 0);
               }
             umma_commit(&bars->wu_ready);
             umma_commit(&bars->tm_free);
-            umma_commit(&bars->prep_empty[slot]);
+            umma_commit(&bars->prep_empty[ps]);
             ++iu;
             progressed = true;
           }
@@ -301,25 +308,19 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     const __nv_bfloat16 *src = part == 0 ? p.q : (part == 1 ? p.k : p.v);
     // channels 4l .. 4l+3: column block l / 16, 16-byte chunk (l % 16) / 2, half l % 2
     const uint32_t cb = (uint32_t)(lane >> 4), ch = (uint32_t)((lane & 15) >> 1), hb = (uint32_t)(lane & 1) * 8;
-    int it = 0;
-    for (int w = blockIdx.x; w < nitems; w += gridDim.x, ++it) {
+    // the conv taps of the chunk's head, the 3 rows before the chunk (row group
+    // 0 only) and its gates (warp 0 only)
+    float4 nwt[4];
+    uint2 nhist[3];
+    float2 nga = make_float2(1.f, 1.f), ngb = make_float2(0.f, 0.f);
+    auto prefetch = [&](int wn) {
       int b, h, c;
-      decode(w, b, h, c);
+      decode(wn, b, h, c);
       const int t0 = c * kC;
-      const size_t unit = (size_t)b * H + h;
-      const int slot = it & 1;
-      const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-      // the 4 taps of channels 4l .. 4l+3, as (4l, 4l + 2) and (4l + 1, 4l + 3) pairs
-      float4 wt[4];
 #pragma unroll
       for (int c2 = 0; c2 < 4; ++c2)
-        wt[c2] = kConv ? *reinterpret_cast<const float4 *>(p.conv_w + ((size_t)part * H * kD + h * kD + 4 * lane + c2) * 4)
-                       : make_float4(0.f, 0.f, 0.f, 1.f);
-      const fe::f2 we[4] = {fe::f2_pack(wt[0].x, wt[2].x), fe::f2_pack(wt[0].y, wt[2].y), fe::f2_pack(wt[0].z, wt[2].z),
-                            fe::f2_pack(wt[0].w, wt[2].w)};
-      const fe::f2 wo[4] = {fe::f2_pack(wt[1].x, wt[3].x), fe::f2_pack(wt[1].y, wt[3].y), fe::f2_pack(wt[1].z, wt[3].z),
-                            fe::f2_pack(wt[1].w, wt[3].w)};
-      uint2 hist[3];  // rows -3, -2, -1 of the chunk (row group 0 only)
+        nwt[c2] = kConv ? *reinterpret_cast<const float4 *>(p.conv_w + ((size_t)part * H * kD + h * kD + 4 * lane + c2) * 4)
+                        : make_float4(0.f, 0.f, 0.f, 1.f);
 #pragma unroll
       for (int m = 0; m < 3; ++m) {
         const int t = t0 - 3 + m;
@@ -331,16 +332,42 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             v = *reinterpret_cast<const uint2 *>(p.conv_in + ((size_t)b * 3 + (t + 3)) * Cch + part * H * kD +
                                                  h * kD + 4 * lane);
         }
-        hist[m] = v;
+        nhist[m] = v;
       }
-      if (!wait_bar_warp(&bars->prep_empty[slot], ph ^ 1u, abort)) break;  // W, U~ of chunk it - 2 are issued
       if (fw == 0) {
-        // gates of the chunk: g2 = cumsum(log2 alpha); alpha = 1, beta = 0 past T
-        float *g2s = reinterpret_cast<float *>(smem + kOffPG + slot * 512);
-        float *betas = g2s + kC;
         const int ta = t0 + 2 * lane, tb = ta + 1;
         const size_t ia = ((size_t)b * T + ta) * H + h, ib = ((size_t)b * T + tb) * H + h;
-        const float a0 = ta < T ? p.alpha[ia] : 1.f, a1 = tb < T ? p.alpha[ib] : 1.f;
+        nga = make_float2(ta < T ? p.alpha[ia] : 1.f, tb < T ? p.alpha[ib] : 1.f);
+        ngb = make_float2(ta < T ? p.beta[ia] : 0.f, tb < T ? p.beta[ib] : 0.f);
+      }
+    };
+    if (blockIdx.x < (unsigned)nitems) prefetch(blockIdx.x);
+    int it = 0;
+    for (int w = blockIdx.x; w < nitems; w += gridDim.x, ++it) {
+      int b, h, c;
+      decode(w, b, h, c);
+      const int t0 = c * kC;
+      const size_t unit = (size_t)b * H + h;
+      const int slot = it & 1, ps = it % kPrepSlots;
+      const uint32_t ph = (uint32_t)(it >> 1) & 1u, pph = (uint32_t)(it / kPrepSlots) & 1u;
+      // the 4 taps of channels 4l .. 4l+3, as (4l, 4l + 2) and (4l + 1, 4l + 3) pairs
+      float4 wt[4];
+#pragma unroll
+      for (int c2 = 0; c2 < 4; ++c2) wt[c2] = nwt[c2];
+      const fe::f2 we[4] = {fe::f2_pack(wt[0].x, wt[2].x), fe::f2_pack(wt[0].y, wt[2].y), fe::f2_pack(wt[0].z, wt[2].z),
+                            fe::f2_pack(wt[0].w, wt[2].w)};
+      const fe::f2 wo[4] = {fe::f2_pack(wt[1].x, wt[3].x), fe::f2_pack(wt[1].y, wt[3].y), fe::f2_pack(wt[1].z, wt[3].z),
+                            fe::f2_pack(wt[1].w, wt[3].w)};
+      // this chunk's history rows and gates were loaded one chunk ahead
+      const uint2 hist[3] = {nhist[0], nhist[1], nhist[2]};
+      const float a0 = nga.x, a1 = nga.y, be0 = ngb.x, be1 = ngb.y;
+      if (w + (int)gridDim.x < nitems) prefetch(w + gridDim.x);
+      // W, U~ of chunk it - 3 are done
+      if (!wait_bar_warp(&bars->prep_empty[ps], pph ^ 1u, abort)) break;
+      if (fw == 0) {
+        // gates of the chunk: g2 = cumsum(log2 alpha); alpha = 1, beta = 0 past T
+        float *g2s = reinterpret_cast<float *>(smem + kOffPG + ps * 512);
+        float *betas = g2s + kC;
         const float l0 = log2f(a0), l1 = log2f(a1);
         float incl = l0 + l1;
 #pragma unroll
@@ -353,15 +380,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         const float ga = excl + l0, gb = ga + l1;
         g2s[2 * lane] = ga;
         g2s[2 * lane + 1] = gb;
-        betas[2 * lane] = ta < T ? p.beta[ia] : 0.f;
-        betas[2 * lane + 1] = tb < T ? p.beta[ib] : 0.f;
+        betas[2 * lane] = be0;
+        betas[2 * lane + 1] = be1;
         p.Gp[unit * p.Tp + t0 + 2 * lane] = ga;
         p.Gp[unit * p.Tp + t0 + 2 * lane + 1] = gb;
       }
       if (!wait_bar_warp(&bars->raw_full[slot], ph, abort)) break;
       const uint8_t *raw = smem + kOffRaw + slot * kRawBytes + part * 16384 + cb * 8192;
-      uint8_t *dst_tile = part == 1 ? smem + kOffPrep + slot * 2 * kPrepTile
-                                    : smem + kOffPrep + slot * 2 * kPrepTile + kPrepTile;
+      uint8_t *dst_tile = smem + kOffPrep + ps * 2 * kPrepTile + (part == 1 ? 0 : kPrepTile);
 #pragma unroll 1
       for (int k = 0; k < 4; ++k) {
         const int r0 = (fw / 3 + 2 * k) * 8;  // the task's 8 tokens
@@ -422,7 +448,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
       }
       fence_proxy_async_smem();
-      warp_arrive(&bars->prep_full[slot]);
+      warp_arrive(&bars->prep_full[ps]);
       warp_arrive(&bars->raw_empty[slot]);
     }
   } else if (warp < kEpiWarp0) {
@@ -437,15 +463,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     float *T00 = A11 + kBlk * kLd;
     float *T10 = T00 + kBlk * kLd;
     float *T11 = T10 + kBlk * kLd;
-    float *colbg = reinterpret_cast<float *>(smem + kOffCol);
-    float *colb = colbg + kC;
     int it = 0;
     for (int w = blockIdx.x; w < nitems; w += gridDim.x, ++it) {
-      const int slot = it & 1;
+      const int slot = it & 1, ps = it % kPrepSlots;
       const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-      bool ok = wait_bar_warp(&bars->prep_full[slot], ph, abort) && wait_bar_warp(&bars->kk_ready[slot], ph, abort);
+      bool ok = wait_bar_warp(&bars->prep_full[ps], (uint32_t)(it / kPrepSlots) & 1u, abort) &&
+                wait_bar_warp(&bars->kk_ready[slot], ph, abort);
       if (!inv_all(ok)) break;
-      const float *g2s = reinterpret_cast<const float *>(smem + kOffPG + slot * 512);
+      const float *g2s = reinterpret_cast<const float *>(smem + kOffPG + ps * 512);
       const float *betas = g2s + kC;
       tc_fence_after();
       // ---- A_ij = beta_i 2^(g_i - g_j) (k_i . k_j) for j < i, as the blocks A00, A10, A11
@@ -454,55 +479,106 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         tmem_ld16x256b_x8(tmem + kColKK + slot * 64 + lane_base, kk);
         tc_fence_before();
         warp_arrive(&bars->kk_free[slot]);
+        const float gr[2] = {g2s[r0], g2s[r0 + 8]}, br[2] = {betas[r0], betas[r0 + 8]};
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {  // the pair of columns j, j + 1 of row i
-          const int i = (e & 2) ? r0 + 8 : r0, j = 8 * (e >> 2) + cq;
-          const float gi = g2s[i], bi = betas[i];
-          const float a0 = j < i ? bi * exp2f(gi - g2s[j]) * kk[e] : 0.f;
-          const float a1 = j + 1 < i ? bi * exp2f(gi - g2s[j + 1]) * kk[e + 1] : 0.f;
-          // the diagonal blocks transposed (the solve walks their columns), A10 by rows
-          if (i < kBlk) {
-            if (j < kBlk) {
-              A00[j * kLd + i] = a0;
-              A00[(j + 1) * kLd + i] = a1;
+        for (int m = 0; m < 8; ++m) {  // the pair of columns j, j + 1 of rows r0, r0 + 8
+          const int j = 8 * m + cq;
+          const float2 gj = *reinterpret_cast<const float2 *>(g2s + j);
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int i = r0 + 8 * rr;
+            // computed for every (i, j), then selected: no divergent branches
+            const float d0 = exp2f(fminf(gr[rr] - gj.x, 0.f)), d1 = exp2f(fminf(gr[rr] - gj.y, 0.f));
+            const float a0 = j < i ? br[rr] * d0 * kk[4 * m + 2 * rr] : 0.f;
+            const float a1 = j + 1 < i ? br[rr] * d1 * kk[4 * m + 2 * rr + 1] : 0.f;
+            // the diagonal blocks transposed (the solve walks their columns), A10 by rows
+            if (i < kBlk) {
+              if (j < kBlk) {
+                A00[j * kLd + i] = a0;
+                A00[(j + 1) * kLd + i] = a1;
+              }
+            } else if (j < kBlk) {
+              *reinterpret_cast<float2 *>(A10 + (i - kBlk) * kLd + j) = make_float2(a0, a1);
+            } else {
+              A11[(j - kBlk) * kLd + (i - kBlk)] = a0;
+              A11[(j + 1 - kBlk) * kLd + (i - kBlk)] = a1;
             }
-          } else if (j < kBlk) {
-            *reinterpret_cast<float2 *>(A10 + (i - kBlk) * kLd + j) = make_float2(a0, a1);
-          } else {
-            A11[(j - kBlk) * kLd + (i - kBlk)] = a0;
-            A11[(j + 1 - kBlk) * kLd + (i - kBlk)] = a1;
           }
         }
       }
-      inv_sync();
-      // ---- T00 = (I + A00)^-1 (warp 0) and T11 = (I + A11)^-1 (warp 1) by forward
-      // substitution, lane = column c, right-looking: x = e_c, then for i = 0, 1,
-      // ...: x_i is final and x_m -= A_mi x_i for m > i.  Row i of the stored
-      // transpose holds column i of A; its entries m <= i are 0 and skipped.
+      // the epilogue warps have read T of the previous chunk
+      ok = wait_bar_warp(&bars->t_free, ((uint32_t)it & 1u) ^ 1u, abort);
+      if (!inv_all(ok)) break;  // also orders the writes of A before the reads below
+      // ---- T00 = (I + A00)^-1 (warp 0) and T11 = (I + A11)^-1 (warp 1), each in
+      // 16 x 16 sub-blocks [Ta 0; Tb Tc]: the diagonal ones by forward
+      // substitution (lanes 0-15 Ta, 16-31 Tc, lane = column c), right-looking:
+      // x = e_c, then for i = 0, 1, ...: x_i is final and x_m -= A_mi x_i for
+      // m > i (row i of the stored transpose holds column i of A; its entries
+      // m <= i are 0 and skipped); then Tb = -Tc (Ab Ta).
       if (iw < 2) {
         const float *At = iw ? A11 : A00;
         float *Tb = iw ? T11 : T00;
-        float x[kBlk];
+        const int hf = lane >> 4, c = lane & 15, base = 16 * hf;
+        float x[16];
 #pragma unroll
-        for (int m = 0; m < kBlk; ++m) x[m] = m == lane ? 1.f : 0.f;
+        for (int m = 0; m < 16; ++m) x[m] = m == c ? 1.f : 0.f;
 #pragma unroll
-        for (int i = 0; i < kBlk - 1; ++i) {
+        for (int i = 0; i < 15; ++i) {
 #pragma unroll
-          for (int m4 = ((i + 1) / 4) * 4; m4 < kBlk; m4 += 4) {
-            const float4 a = *reinterpret_cast<const float4 *>(At + i * kLd + m4);
+          for (int m4 = ((i + 1) / 4) * 4; m4 < 16; m4 += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(At + (base + i) * kLd + base + m4);
             const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               if (m4 + e > i) x[m4 + e] = fmaf(-av[e], x[i], x[m4 + e]);
           }
         }
+        // Ta, Tc by rows, and the zero block above Tc
 #pragma unroll
-        for (int m = 0; m < kBlk; ++m) Tb[m * kLd + lane] = x[m];
-      } else {
-        // column scales of T diag(beta gamma) and T diag(beta)
-        const int k = 32 * (iw - 2) + lane;
-        colbg[k] = betas[k] * exp2f(g2s[k]);
-        colb[k] = betas[k];
+        for (int m = 0; m < 16; ++m) {
+          Tb[(base + m) * kLd + base + c] = x[m];
+          if (hf) Tb[m * kLd + 16 + c] = 0.f;
+        }
+        // P = Ab Ta (Ab = A[16..31][0..15], i.e. rows 0-15, columns 16-31 of the
+        // transpose): column c, rows 8 hf .. 8 hf + 7 in this lane
+        float ta[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) ta[m] = __shfl_sync(0xffffffffu, x[m], c);
+        float pr[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) pr[r] = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float4 u = *reinterpret_cast<const float4 *>(At + m * kLd + 16 + 8 * hf);
+          const float4 v = *reinterpret_cast<const float4 *>(At + m * kLd + 20 + 8 * hf);
+          pr[0] = fmaf(u.x, ta[m], pr[0]); pr[1] = fmaf(u.y, ta[m], pr[1]);
+          pr[2] = fmaf(u.z, ta[m], pr[2]); pr[3] = fmaf(u.w, ta[m], pr[3]);
+          pr[4] = fmaf(v.x, ta[m], pr[4]); pr[5] = fmaf(v.y, ta[m], pr[5]);
+          pr[6] = fmaf(v.z, ta[m], pr[6]); pr[7] = fmaf(v.w, ta[m], pr[7]);
+        }
+        float pc[16];  // column c of P
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const float o = __shfl_xor_sync(0xffffffffu, pr[r], 16);
+          pc[r] = hf ? o : pr[r];
+          pc[8 + r] = hf ? pr[r] : o;
+        }
+        __syncwarp();  // Tc's rows are stored
+        // Tb = -Tc P: rows 8 hf .. 8 hf + 7 of column c
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const float *tc = Tb + (16 + 8 * hf + r) * kLd + 16;
+          float acc = 0.f;
+#pragma unroll
+          for (int m4 = 0; m4 < 16; m4 += 4) {
+            const float4 t4 = *reinterpret_cast<const float4 *>(tc + m4);
+            acc = fmaf(t4.x, pc[m4], acc);
+            acc = fmaf(t4.y, pc[m4 + 1], acc);
+            acc = fmaf(t4.z, pc[m4 + 2], acc);
+            acc = fmaf(t4.w, pc[m4 + 3], acc);
+          }
+          Tb[(16 + 8 * hf + r) * kLd + c] = -acc;
+        }
       }
       inv_sync();
       // ---- T10 = -T11 (A10 T00): X = A10 T00 in A00's place, then T10 = -T11 X;
@@ -538,48 +614,15 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         *reinterpret_cast<float4 *>(T10 + r * kLd + c0) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
         *reinterpret_cast<float4 *>(T10 + r * kLd + c0 + 4) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
       }
-      // ---- T diag(beta gamma) and T diag(beta) as bf16 hi / lo MMA tiles (once
-      // the previous chunk's W and U~ MMAs have read them)
-      ok = wait_bar_warp(&bars->tm_free, ((uint32_t)it & 1u) ^ 1u, abort);
-      if (!inv_all(ok)) break;  // also orders T10's writes before the reads below
-      {
-        uint8_t *tm1 = smem + kOffTm;  // T diag(beta gamma): hi, lo
-        uint8_t *tm2 = tm1 + 16384;    // T diag(beta): hi, lo
-#pragma unroll
-        for (int rep = 0; rep < 4; ++rep) {  // (row i, 8-column chunk): 512 items, 4 per thread
-          const int item = itid + 128 * rep, i = item >> 3, chk = item & 7;
-          // T[i][8 chk .. + 7]: from T00, T10 or T11 (T01 = 0)
-          const int k0 = 8 * chk;
-          const float *src = i < kBlk ? (k0 < kBlk ? T00 + i * kLd + k0 : nullptr)
-                                      : (k0 < kBlk ? T10 + (i - kBlk) * kLd + k0 : T11 + (i - kBlk) * kLd + (k0 - kBlk));
-          float tv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          if (src) {
-            const float4 ta = *reinterpret_cast<const float4 *>(src), tb = *reinterpret_cast<const float4 *>(src + 4);
-            tv[0] = ta.x; tv[1] = ta.y; tv[2] = ta.z; tv[3] = ta.w;
-            tv[4] = tb.x; tv[5] = tb.y; tv[6] = tb.z; tv[7] = tb.w;
-          }
-          float w1[8], w2[8];
-#pragma unroll
-          for (int e2 = 0; e2 < 8; ++e2) {
-            w1[e2] = tv[e2] * colbg[k0 + e2];
-            w2[e2] = tv[e2] * colb[k0 + e2];
-          }
-          uint4 h1, l1, h2, l2;
-          split8(w1, h1, l1);
-          split8(w2, h2, l2);
-          const uint32_t off = swz(i, chk);
-          *reinterpret_cast<uint4 *>(tm1 + off) = h1;
-          *reinterpret_cast<uint4 *>(tm1 + 8192 + off) = l1;
-          *reinterpret_cast<uint4 *>(tm2 + off) = h2;
-          *reinterpret_cast<uint4 *>(tm2 + 8192 + off) = l2;
-        }
-      }
-      fence_proxy_async_smem();
-      warp_arrive(&bars->tm_ready);
+      warp_arrive(&bars->t_ready);
       inv_sync();  // the next chunk's A may overwrite the blocks read above
     }
   } else {
-    // ======================= W (bf16) and U~ (fp32) to global memory =======================
+    // ============ the T tiles, then W (bf16) and U~ (fp32) to global memory ============
+    const int etid = tid - 32 * kEpiWarp0;  // 0..127
+    const float *T00 = reinterpret_cast<const float *>(smem + kOffAT) + 3 * kBlk * kLd;
+    const float *T10 = T00 + kBlk * kLd;
+    const float *T11 = T10 + kBlk * kLd;
     const int q4 = warp & 3;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     const int r0 = 16 * q4 + (lane >> 2), cq = 2 * (lane & 3);
@@ -589,6 +632,60 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       decode(w, b, h, c);
       const size_t unit = (size_t)b * H + h;
       const size_t row0 = unit * p.Tp + c * kC + r0, row1 = row0 + 8;
+      const int slot = it & 1;
+      // ---- T diag(beta gamma) and T diag(beta) as bf16 hi / lo MMA operands in
+      // tensor memory, once the inverse is done and the previous chunk's W and U~
+      // MMAs have read them
+      if (!wait_bar_warp(&bars->t_ready, (uint32_t)it & 1u, abort)) break;
+      if (!wait_bar_warp(&bars->tm_free, ((uint32_t)it & 1u) ^ 1u, abort)) break;
+      float *colbg = reinterpret_cast<float *>(smem + kOffCol) + slot * 2 * kC;
+      float *colb = colbg + kC;
+      if (etid < kC) {
+        const float *g2s = reinterpret_cast<const float *>(smem + kOffPG + (it % kPrepSlots) * 512);
+        const float bk = g2s[kC + etid];
+        colbg[etid] = bk * exp2f(g2s[etid]);
+        colb[etid] = bk;
+      }
+      epi_sync();
+      tc_fence_after();
+      {
+        // 16x256b fragment: rows r0, r0 + 8; column pairs k = 16m + 4(lane & 3) .. + 3
+        // (T01 = 0; T00, T10 or T11 otherwise)
+        const int q = lane & 3;
+        float tv[2][4][4];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int i = r0 + 8 * rr;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int k = 16 * m + 4 * q;
+            const float *src = i < kBlk ? (k < kBlk ? T00 + i * kLd + k : nullptr)
+                                        : (k < kBlk ? T10 + (i - kBlk) * kLd + k : T11 + (i - kBlk) * kLd + (k - kBlk));
+            const float4 t4 = src ? *reinterpret_cast<const float4 *>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+            tv[rr][m][0] = t4.x; tv[rr][m][1] = t4.y; tv[rr][m][2] = t4.z; tv[rr][m][3] = t4.w;
+          }
+        }
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {  // T diag(beta gamma), T diag(beta)
+          const float *col = part ? colb : colbg;
+          uint32_t vh[16], vl[16];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const float4 cs = *reinterpret_cast<const float4 *>(col + 16 * m + 4 * q);
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+              split2(tv[rr][m][0] * cs.x, tv[rr][m][1] * cs.y, vh[4 * m + 2 * rr], vl[4 * m + 2 * rr]);
+              split2(tv[rr][m][2] * cs.z, tv[rr][m][3] * cs.w, vh[4 * m + 2 * rr + 1], vl[4 * m + 2 * rr + 1]);
+            }
+          }
+          tmem_st16x256b_x4(tmem + kColTm + part * 64 + lane_base, vh);
+          tmem_st16x256b_x4(tmem + kColTm + part * 64 + 32 + lane_base, vl);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      warp_arrive(&bars->tm_ready);
+      warp_arrive(&bars->t_free);
       if (!wait_bar_warp(&bars->wu_ready, (uint32_t)it & 1u, abort)) break;
       tc_fence_after();
       float v0[32], v1[32];

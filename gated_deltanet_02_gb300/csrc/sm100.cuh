@@ -243,6 +243,19 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       : "memory");
 }
 
+// 16x256b store of 4 x 8 columns (the M = 64 accumulator fragment: rows t >> 2
+// and + 8 of the warp's 16-lane block, columns 8m + 2(t & 3), + 1 in v[4m ..]);
+// tmem_wait_st() completes it.
+__device__ __forceinline__ void tmem_st16x256b_x4(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16};\n" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Arrive once on the mbarrier when every MMA issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
   asm volatile(
