@@ -18,17 +18,24 @@
 //     one in the SSD form's d_v = 64); groups of heads may share q and k
 //     (the q / k tiles come from head h / (H / Hq)); the state slice
 //     S[128 x 64] is fp32 and lives in the registers of the epilogue warps
-//     for the whole sequence, one d_k row per thread;
+//     for the whole sequence, one d_k row per thread of warpgroup B;
 //   * warp 0 streams Q, K (64 x 128) and V (64 x 64) chunk tiles with TMA
-//     (128-byte swizzle, 2-stage ring, out-of-range rows of a ragged last
-//     chunk are zero-filled by the copy engine);
-//   * warp 1 (one thread) issues tcgen05.mma: QK^T, K^T V~, P V and Q S into
-//     double-buffered TMEM accumulators (4 x 64 columns per chunk);
-//   * warps 2-5 form P = (QK^T)*D, V~ = diag(r) V and the next state, and
-//     write the outputs.  Operands derived in fp32 (P, V~, S) are split into
-//     a bf16 high part and a bf16 remainder and multiplied twice, so the
-//     products keep ~16 bits instead of bf16's 8 (one bf16 rounding of these
-//     operands alone costs ~2e-3 relative error in o and S).
+//     (128-byte swizzle, 3-stage ring, out-of-range rows of a ragged last
+//     chunk are zero-filled by the copy engine) and the chunk's gates into a
+//     ring beside them, prefetching 3 more chunks into L2;
+//   * two threads issue tcgen05.mma (a thread issues one small MMA about every
+//     85 cycles, so the chunk's MMAs are spread over two issuers): warp 1 the
+//     state chain, K^T V~ and then Q S; warp 10 Q K^T one chunk ahead and P V.
+//     Accumulators in TMEM: Q K^T and P V double-buffered (64 columns each),
+//     Q [S_hi | S_lo] and K^T [V~hi | V~lo] (128 columns each);
+//   * warpgroup A (warps 2-5) forms P = (QK^T)*D and V~ = diag(r) V as bf16
+//     hi / lo tiles; warpgroup B (warps 6-9) holds the state, folds the
+//     K^T V~ accumulator into it, writes the next state's hi / lo tile and
+//     writes the outputs gamma_i (Q S)_i + (P V)_i.  Operands derived in fp32
+//     (P, V~, S) are split into a bf16 high part and a bf16 remainder and
+//     multiplied twice, so the products keep ~16 bits instead of bf16's 8 (one
+//     bf16 rounding of these operands alone costs ~2e-3 relative error in o
+//     and S).
 //   Every mbarrier wait is bounded; on timeout the CTA raises
 //   GLINATTN_DEV_WAIT_TIMEOUT and all roles leave their loops.
 #include <cuda.h>
