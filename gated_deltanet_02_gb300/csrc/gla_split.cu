@@ -10,8 +10,10 @@
 // of whole chunks that run side by side:
 //
 //   1. gla_state_kernel, one CTA per (piece, head, d_v slice): S_local and
-//      Gamma of its piece (only K^T diag(r) V per chunk: no scores, no
-//      outputs), and whether any gate of the whole sequence is invalid;
+//      Gamma of its piece, S_local as one accumulation of K^T diag(w) V over
+//      the piece's chunks (w_t the decay from token t to the piece end; no
+//      scores, no outputs, no chain through the state), and whether any gate
+//      of the whole sequence is invalid;
 //   2. gla_combine_kernel: S_start of every piece, serially over the P
 //      pieces (one multiply-add per state element and piece), and S_T;
 //   3. gla_prefill_kernel on the pieces as separate sequences, each from its
@@ -40,18 +42,20 @@ using namespace tc;
 constexpr int kC = 64;     // chunk length
 constexpr int kDK = 128;   // key head size
 constexpr int kBV = 64;    // d_v columns per CTA
-constexpr int kStages = 3;
-constexpr int kThreads = 192;  // warp 0 TMA + gates, warp 1 MMA issuer, warps 2-5 V~ and the state
+constexpr int kStages = 4;
+constexpr int kPrefetch = 4;  // chunks prefetched into L2 beyond the shared-memory ring
+constexpr int kThreads = 192;  // warp 0 TMA + weights, warp 1 MMA issuer, warps 2-5 V~ and the end state
 constexpr uint32_t kTileK = kC * kDK * 2;   // 16 KiB: two 64-column swizzled blocks
 constexpr uint32_t kTileV = kC * kBV * 2;   // 8 KiB
 constexpr uint32_t kStageBytes = kTileK + kTileV;
 constexpr uint32_t kOffStage = 0;
-constexpr uint32_t kOffVt = kStages * kStageBytes;     // V~ [hi | lo], double-buffered
-constexpr uint32_t kOffG = kOffVt + 2 * 2 * kTileV;    // gates [stage]: r[64], 2^g_C
+constexpr int kVtBufs = 2;                             // V~ [hi | lo] buffers
+constexpr uint32_t kOffVt = kStages * kStageBytes;
+constexpr uint32_t kOffG = kOffVt + kVtBufs * 2 * kTileV;  // weights [stage]: w[64]
 constexpr uint32_t kGateFloats = kC + 4;
 constexpr uint32_t kOffBar = kOffG + kStages * kGateFloats * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
-constexpr uint32_t kTmCols = 256;  // K^T [V~hi | V~lo], double-buffered
+constexpr uint32_t kTmCols = 128;  // S_local as K^T [V~hi | V~lo], one accumulator
 
 struct StateParams {
   int BP, P, L, T, H, rep, DV, nchunks;  // BP = B * P sequences of L tokens
@@ -64,7 +68,7 @@ struct StateParams {
 
 struct StateBars {
   uint64_t full[kStages], empty[kStages];
-  uint64_t vt_ready[2], vt_free[2], ds_ready[2], ds_free[2];
+  uint64_t vt_ready[kVtBufs], vt_free[kVtBufs], ds_ready;
   uint32_t tmem_base;
   int abort;
 };
@@ -108,12 +112,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->full[s], 1 + 32);  // the TMA transaction and the 32 gate lanes
       mbar_init(&bars->empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kVtBufs; ++i) {
       mbar_init(&bars->vt_ready[i], 128);
       mbar_init(&bars->vt_free[i], 1);
-      mbar_init(&bars->ds_ready[i], 1);
-      mbar_init(&bars->ds_free[i], 128);
     }
+    mbar_init(&bars->ds_ready, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -128,16 +131,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tb0 = (bp % p.P) * L;  // first token of the piece in the whole sequence (for alpha)
   const size_t arow = (size_t)b * p.T;
 
+  // The piece's end state from a zero start is a plain sum,
+  //   S_local = sum_t w_t k_t^T v_t,  w_t = prod_{s > t in the piece} alpha_s,
+  // so it is one accumulation of K^T [V~hi | V~lo] over all chunks (V~ = diag(w) V)
+  // with no chain through the state.  The chunks are taken from the last to
+  // the first, so w comes from a running suffix sum of log2 alpha.
   if (warp == 0) {
-    // ============ TMA producer (lane 0) and the gates of each chunk (all lanes) ============
+    // ============ TMA producer (lane 0) and the weights w of each chunk (all lanes) ============
+    // chunk k of the loop (counted from the last) into L2, ahead of the ring
+    auto prefetch = [&](int k) {
+      if (k >= nchunks) return;
+      const int t0 = (nchunks - 1 - k) * kC;
+      tma_prefetch_l2_4d(&tk, 0, hq, t0, bp);
+      tma_prefetch_l2_4d(&tk, 64, hq, t0, bp);
+      tma_prefetch_l2_4d(&tv, vblk * kBV, h, t0, bp);
+    };
     if (lane == 0) {
       prefetch_tensormap(&tk);
       prefetch_tensormap(&tv);
+      for (int k = 0; k < kPrefetch; ++k) prefetch(kStages + k);
     }
-    for (int c = 0; c < nchunks; ++c) {
-      const int s = c % kStages;
-      const uint32_t use = (uint32_t)(c / kStages);
-      if (!wait_bar_warp(&bars->empty[s], (use & 1u) ^ 1u, abort)) break;
+    float gsuf = 0.f;  // sum of log2 alpha over the chunks after this one
+    bool ok = true;
+    // lane l: tokens 2l, 2l + 1 of a chunk; their gates are loaded one chunk
+    // ahead, so the loads' latency does not sit in the chunk loop
+    auto load_gates = [&](int c, float &x0, float &x1) {
+      const int ta = c * kC + 2 * lane, tb = ta + 1;
+      x0 = ta < L ? p.alpha[(arow + tb0 + ta) * p.H + h] : 1.f;
+      x1 = tb < L ? p.alpha[(arow + tb0 + tb) * p.H + h] : 1.f;
+    };
+    float na0 = 1.f, na1 = 1.f;
+    if (nchunks > 0) load_gates(nchunks - 1, na0, na1);
+    for (int k = 0; k < nchunks; ++k) {
+      const int c = nchunks - 1 - k, s = k % kStages;
+      const float a0 = na0, a1 = na1;
+      if (c > 0) load_gates(c - 1, na0, na1);
+      if (lane == 0) prefetch(k + kStages + kPrefetch);
+      const uint32_t use = (uint32_t)(k / kStages);
+      if (!wait_bar_warp(&bars->empty[s], (use & 1u) ^ 1u, abort)) { ok = false; break; }
       if (lane == 0) {
         uint8_t *st = smem + kOffStage + s * kStageBytes;
         mbar_arrive_expect_tx(&bars->full[s], kStageBytes);
@@ -146,10 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(st + kTileK / 2, &tk, &bars->full[s], 64, hq, t0, bp);
         tma_load_4d(st + kTileK, &tv, &bars->full[s], vblk * kBV, h, t0, bp);
       }
-      // lane l: tokens 2l, 2l + 1 of the chunk; g = cumsum(log2 alpha), r = 2^(g_C - g)
-      const int ta = c * kC + 2 * lane, tb = ta + 1;
-      const float a0 = ta < L ? p.alpha[(arow + tb0 + ta) * p.H + h] : 1.f;
-      const float a1 = tb < L ? p.alpha[(arow + tb0 + tb) * p.H + h] : 1.f;
+      // g = cumsum(log2 alpha) inside the chunk, w = 2^(gsuf + g_C - g)
       const float l0 = log2f(a0), l1 = log2f(a1);
       float incl = l0 + l1;
 #pragma unroll
@@ -162,112 +190,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float ga = excl + l0, gb = excl + l0 + l1;
       const float gC = __shfl_sync(0xffffffffu, gb, 31);
       float *gr = gates + s * kGateFloats;
-      gr[2 * lane] = exp2f(gC - ga);
-      gr[2 * lane + 1] = exp2f(gC - gb);
-      if (lane == 0) gr[kC] = exp2f(gC);
-      mbar_arrive(&bars->full[s]);  // releases this lane's gate writes
+      gr[2 * lane] = exp2f(gsuf + (gC - ga));
+      gr[2 * lane + 1] = exp2f(gsuf + (gC - gb));
+      mbar_arrive(&bars->full[s]);  // releases this lane's weight writes
+      gsuf += gC;
     }
+    if (ok && lane == 0 && vblk == 0) p.gamma[bph] = exp2f(gsuf);  // the piece's total decay
   } else if (warp == 1) {
-    // ============ MMA issuer: dS = K^T [V~hi | V~lo] per chunk ============
+    // ============ MMA issuer: S_local += K^T [V~hi | V~lo], one accumulator ============
     if (lane == 0) {
       constexpr uint32_t id_ds = idesc_bf16(128, 2 * kBV, true, true);
       const uint32_t sbase = smem_u32(smem);
-      for (int c = 0; c < nchunks; ++c) {
-        const int s = c % kStages, vb = c & 1;
-        const uint32_t ph = (uint32_t)(c >> 1) & 1u;
-        if (!wait_bar(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) break;
-        if (!wait_bar(&bars->vt_ready[vb], ph, abort)) break;
-        if (!wait_bar(&bars->ds_free[vb], ph ^ 1u, abort)) break;
+      bool ok = true;
+      for (int k = 0; k < nchunks; ++k) {
+        const int s = k % kStages, vb = k % kVtBufs;
+        const uint32_t ph = (uint32_t)(k / kVtBufs) & 1u;
+        if (!wait_bar(&bars->full[s], (uint32_t)(k / kStages) & 1u, abort) ||
+            !wait_bar(&bars->vt_ready[vb], ph, abort)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint64_t dKm = desc_sw128(sbase + kOffStage + s * kStageBytes, kTileK / 2, 1024);
         const uint64_t dVt = desc_sw128(sbase + kOffVt + vb * 2 * kTileV, kTileV, 1024);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tmem + vb * 128, dKm + ((ks * 2048) >> 4), dVt + ((ks * 2048) >> 4), id_ds, ks > 0);
-        umma_commit(&bars->ds_ready[vb]);
+          umma_bf16(tmem, dKm + ((ks * 2048) >> 4), dVt + ((ks * 2048) >> 4), id_ds, (k | ks) != 0);
         umma_commit(&bars->vt_free[vb]);
         umma_commit(&bars->empty[s]);
       }
+      if (ok) umma_commit(&bars->ds_ready);
     }
   } else {
-    // ============ warps 2-5: V~ = diag(r) V, then the state S <- 2^g_C S + dS ============
+    // ============ warps 2-5: V~ = diag(w) V per chunk, then S_local from TMEM ============
     const int e = tid - 64;  // 0..127
     const int q4 = warp & 3;
     const int srow = 32 * q4 + lane;  // d_k row of the state held by this thread
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-    float S[kBV];
-#pragma unroll
-    for (int j = 0; j < kBV; ++j) S[j] = 0.f;
-    float gam = 1.f, eg_prev = 1.f;
     bool ok = true;
-    for (int c = 0; c <= nchunks && ok; ++c) {
-      if (c < nchunks) {
-        const int s = c % kStages, vb = c & 1;
-        const uint32_t ph = (uint32_t)(c >> 1) & 1u;
-        if (!wait_bar_warp(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) { ok = false; break; }
-        if (!wait_bar_warp(&bars->vt_free[vb], ph ^ 1u, abort)) { ok = false; break; }
-        const float *gr = gates + s * kGateFloats;
-        const uint32_t vt = smem_u32(smem + kOffStage + s * kStageBytes + kTileK);
-        const uint32_t vhi = smem_u32(smem + kOffVt + vb * 2 * kTileV), vlo = vhi + kTileV;
-        const int t = e >> 1, half = e & 1;
-        const float r = gr[t];
+    for (int k = 0; k < nchunks && ok; ++k) {
+      const int s = k % kStages, vb = k % kVtBufs;
+      const uint32_t ph = (uint32_t)(k / kVtBufs) & 1u;
+      if (!wait_bar_warp(&bars->full[s], (uint32_t)(k / kStages) & 1u, abort)) { ok = false; break; }
+      if (!wait_bar_warp(&bars->vt_free[vb], ph ^ 1u, abort)) { ok = false; break; }
+      const float *gr = gates + s * kGateFloats;
+      const uint32_t vt = smem_u32(smem + kOffStage + s * kStageBytes + kTileK);
+      const uint32_t vhi = smem_u32(smem + kOffVt + vb * 2 * kTileV), vlo = vhi + kTileV;
+      const int t = e >> 1, half = e & 1;
+      const float w = gr[t];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t ch = 4 * half + k;
-          float x[8];
-          unpack8(lds128(vt + swz(t, ch)), x);
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint32_t ch = 4 * half + kk;
+        float x[8];
+        unpack8(lds128(vt + swz(t, ch)), x);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) x[i] *= r;
-          uint4 uh, ul;
-          split8(x, uh, ul);
-          sts128(vhi + swz(t, ch), uh);
-          sts128(vlo + swz(t, ch), ul);
-        }
-        const float eg = gr[kC];
-        fence_proxy_async_smem();
-        mbar_arrive(&bars->vt_ready[vb]);
-        if (c > 0) {  // the state update of the previous chunk below uses its own gate
-          const float tmp = eg_prev;
-          eg_prev = eg;
-          gam *= tmp;
-          // previous chunk's update
-          const int db = (c - 1) & 1;
-          if (!wait_bar_warp(&bars->ds_ready[db], (uint32_t)((c - 1) >> 1) & 1u, abort)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            float dh[32], dl[32];
-            tmem_ld32x2(tmem + db * 128 + 32 * hf + lane_base, tmem + db * 128 + kBV + 32 * hf + lane_base, dh, dl);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) S[32 * hf + jj] = tmp * S[32 * hf + jj] + (dh[jj] + dl[jj]);
-          }
-          tc_fence_before();
-          mbar_arrive(&bars->ds_free[db]);
-        } else {
-          eg_prev = eg;
-        }
-      } else {  // the last chunk's update
-        const int db = (c - 1) & 1;
-        gam *= eg_prev;
-        if (!wait_bar_warp(&bars->ds_ready[db], (uint32_t)((c - 1) >> 1) & 1u, abort)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float dh[32], dl[32];
-          tmem_ld32x2(tmem + db * 128 + 32 * hf + lane_base, tmem + db * 128 + kBV + 32 * hf + lane_base, dh, dl);
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) S[32 * hf + jj] = eg_prev * S[32 * hf + jj] + (dh[jj] + dl[jj]);
-        }
-        tc_fence_before();
-        mbar_arrive(&bars->ds_free[db]);
+        for (int i = 0; i < 8; ++i) x[i] *= w;
+        uint4 uh, ul;
+        split8(x, uh, ul);
+        sts128(vhi + swz(t, ch), uh);
+        sts128(vlo + swz(t, ch), ul);
       }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->vt_ready[vb]);
     }
-    if (ok) {
+    if (ok && wait_bar_warp(&bars->ds_ready, 0u, abort)) {
+      tc_fence_after();
       float *dst = p.S_local + (((size_t)bph * kDK) + srow) * p.DV + vblk * kBV;
 #pragma unroll
-      for (int j = 0; j < kBV; j += 4)
-        *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-      if (e == 0 && vblk == 0) p.gamma[bph] = gam;
+      for (int hf = 0; hf < 2; ++hf) {
+        float dh[32], dl[32];
+        tmem_ld32x2(tmem + 32 * hf + lane_base, tmem + kBV + 32 * hf + lane_base, dh, dl);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4 *>(dst + 32 * hf + j) =
+              make_float4(dh[j] + dl[j], dh[j + 1] + dl[j + 1], dh[j + 2] + dl[j + 2], dh[j + 3] + dl[j + 3]);
+      }
     }
   }
 
