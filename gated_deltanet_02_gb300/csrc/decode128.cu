@@ -49,24 +49,31 @@ constexpr int kRowG = kNT / kColG;    // 8 row groups
 constexpr int kRPT = kD / kRowG;      // 16 rows per thread
 constexpr int kNCH = 2 * kD + kDC;    // front-end channels: q, k, own v slice
 constexpr int kMaxC = (kNCH + kNT - 1) / kNT;
-constexpr int kRing = 2;              // units in flight per CTA
 constexpr int kTab = 4;               // unit table entries
 constexpr int kTabSteps = 8;          // per-step scalars kept in a table entry
 constexpr int kTabWords = 32;         // [0] src slot, [1..8] dst slots, [9..16] alpha, [17..24] beta,
                                       // [25] steps applied (replay)
 constexpr uint32_t kStateBytes = kD * kDC * 4;
-constexpr uint32_t kMiscBytes = kNCH * 4 + kNW * 2 * kDC * 4 + 3 * kNW * 4 + kTab * kTabWords * 4 + kRing * 8;
+// units in flight per CTA (the ring depth): two for decode, whose one step per
+// unit is short next to a state's copy; one for several steps per unit, where
+// the smaller footprint lets 5 CTAs (20 warps) share an SM to hide the latency
+// of each step's reductions
+__host__ __device__ constexpr uint32_t misc_bytes(int kr) {
+  return kNCH * 4 + kNW * 2 * kDC * 4 + 3 * kNW * 4 + kTab * kTabWords * 4 + kr * 8;
+}
 
-constexpr int kRingSteps = 2;         // token rows of a unit carried in its ring slot (3 CTAs per SM)
+// token rows of a unit carried in its ring slot: 2 with two slots (3 CTAs per
+// SM), 4 with one (5 CTAs per SM); later rows come from global memory
+__host__ __device__ constexpr int ring_steps(int kr) { return kr == 1 ? 4 : 2; }
 // ring slot: the state half, then the conv history (3 rows) and the first
 // `xrows` token rows of the unit, each row kNCH channels of `esz` bytes
-__host__ __device__ constexpr int ring_xrows(int steps) { return steps < kRingSteps ? steps : kRingSteps; }
+__host__ __device__ constexpr int ring_xrows(int steps, int kr) { return steps < ring_steps(kr) ? steps : ring_steps(kr); }
 __host__ __device__ constexpr uint32_t small_bytes(int esz, int xrows) { return (3u + xrows) * kNCH * esz; }
 __host__ __device__ constexpr uint32_t slot_bytes(int esz, int xrows) {
   return kStateBytes + small_bytes(esz, xrows);
 }
-__host__ __device__ constexpr uint32_t smem_bytes(int esz, int xrows) {
-  return 128 + kRing * slot_bytes(esz, xrows) + kMiscBytes;
+__host__ __device__ constexpr uint32_t smem_bytes(int esz, int xrows, int kr) {
+  return 128 + kr * slot_bytes(esz, xrows) + misc_bytes(kr);
 }
 
 __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
@@ -94,7 +101,8 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-__global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ CUtensorMap tstate,
+template <int kRing>
+__global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(const __grid_constant__ CUtensorMap tstate,
                                                         const RecurParams p) {
   extern __shared__ uint8_t smem_raw[];
   // 128-byte aligned base derived from the shared array itself, so the compiler
@@ -102,7 +110,7 @@ __global__ void __launch_bounds__(kNT) decode128_kernel(const __grid_constant__ 
   uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   const int in_bf16 = p.in_bf16;
   const int esz = in_bf16 ? 2 : 4;
-  const int xrows = ring_xrows(p.steps);
+  const int xrows = ring_xrows(p.steps, kRing);
   const uint32_t sbytes = slot_bytes(esz, xrows);
   float *s_act = reinterpret_cast<float *>(smem + kRing * sbytes);  // q | k | own v slice
   float *s_red = s_act + kNCH;                                      // [warp][k S | q S][kDC]
@@ -524,9 +532,10 @@ bool decode128_supports(const RecurParams &p, int d) {
          p.S_blocks == nullptr && p.Hq == p.H && p.variant != GLINATTN_NLA;
 }
 
-cudaError_t launch_decode128(const RecurParams &p, cudaStream_t stream) {
+template <int kRing>
+cudaError_t launch_ring(const RecurParams &p, cudaStream_t stream) {
   const int esz = p.in_bf16 ? 2 : 4;
-  const int smem = (int)smem_bytes(esz, ring_xrows(p.steps));
+  const int smem = (int)smem_bytes(esz, ring_xrows(p.steps, kRing), kRing);
   CUtensorMap tmap;
   memset(&tmap, 0, sizeof(tmap));
   {
@@ -536,9 +545,9 @@ cudaError_t launch_decode128(const RecurParams &p, cudaStream_t stream) {
     if (!encode_3d_map(&tmap, p.S_src, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dims, box, false))
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(decode128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(decode128_kernel<kRing>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode128_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(decode128_kernel<kRing>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -558,12 +567,16 @@ cudaError_t launch_decode128(const RecurParams &p, cudaStream_t stream) {
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   int max_clusters = 0;
   cfg.gridDim = dim3(2 * (unsigned)sms);
-  if ((e = cudaOccupancyMaxActiveClusters(&max_clusters, decode128_kernel, &cfg)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveClusters(&max_clusters, decode128_kernel<kRing>, &cfg)) != cudaSuccess) return e;
   if (max_clusters < 1) max_clusters = 1;
   const long long units = (long long)p.N * p.H;
   const long long clusters = units < max_clusters ? units : max_clusters;
   cfg.gridDim = dim3((unsigned)(2 * clusters));
-  return cudaLaunchKernelEx(&cfg, decode128_kernel, tmap, p);
+  return cudaLaunchKernelEx(&cfg, decode128_kernel<kRing>, tmap, p);
+}
+
+cudaError_t launch_decode128(const RecurParams &p, cudaStream_t stream) {
+  return p.steps > 1 ? launch_ring<1>(p, stream) : launch_ring<2>(p, stream);
 }
 
 }  // namespace glinattn
