@@ -8,6 +8,9 @@
 //   GLA:  S <- alpha S + k^T v                      o = q S = alpha (q S_old) + (q.k) v
 //   GDN:  u = beta (v - alpha (k S_old))            S <- alpha S_old + k^T u
 //         o = q S = alpha (q S_old) + (q.k) u
+//   NLA:  (normalised linear attention, phi = elu + 1, no gates, normaliser z)
+//         S <- S + phi(k)^T v,  z <- z + phi(k),
+//         o = phi(q) S / (phi(q) . z + 1e-6) = (phi(q) S_old + (q.k) v) / (phi(q) . z_old + q.k + 1e-6)
 // Section "Speculative decoding and PD disaggregation": requests address their
 // states by slot, and speculative decode keeps one state per draft position.
 //
@@ -59,7 +62,7 @@ constexpr uint32_t kStateBytes = kD * kDC * 4;
 // the smaller footprint lets 5 CTAs (20 warps) share an SM to hide the latency
 // of each step's reductions
 __host__ __device__ constexpr uint32_t misc_bytes(int kr) {
-  return kNCH * 4 + kNW * 2 * kDC * 4 + 3 * kNW * 4 + kTab * kTabWords * 4 + kr * 8;
+  return kNCH * 4 + kNW * 2 * kDC * 4 + 4 * kNW * 4 + kTab * kTabWords * 4 + kr * 8;
 }
 
 // token rows of a unit carried in its ring slot: 2 with two slots (3 CTAs per
@@ -69,11 +72,13 @@ __host__ __device__ constexpr int ring_steps(int kr) { return kr == 1 ? 4 : 2; }
 // `xrows` token rows of the unit, each row kNCH channels of `esz` bytes
 __host__ __device__ constexpr int ring_xrows(int steps, int kr) { return steps < ring_steps(kr) ? steps : ring_steps(kr); }
 __host__ __device__ constexpr uint32_t small_bytes(int esz, int xrows) { return (3u + xrows) * kNCH * esz; }
-__host__ __device__ constexpr uint32_t slot_bytes(int esz, int xrows) {
-  return kStateBytes + small_bytes(esz, xrows);
+// the state slice, the small rows, then (normalised linear attention only) the
+// normaliser z: 512 bytes, a multiple of 128 like the rest
+__host__ __device__ constexpr uint32_t slot_bytes(int esz, int xrows, bool nla) {
+  return kStateBytes + small_bytes(esz, xrows) + (nla ? kD * 4 : 0);
 }
-__host__ __device__ constexpr uint32_t smem_bytes(int esz, int xrows, int kr) {
-  return 128 + kr * slot_bytes(esz, xrows) + misc_bytes(kr);
+__host__ __device__ constexpr uint32_t smem_bytes(int esz, int xrows, int kr, bool nla) {
+  return 128 + kr * slot_bytes(esz, xrows, nla) + misc_bytes(kr);
 }
 
 __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
@@ -95,6 +100,9 @@ __device__ __forceinline__ void st_act(void *base, size_t idx, float x, int bf16
     reinterpret_cast<float *>(base)[idx] = x;
 }
 
+// phi(x) = elu(x) + 1, the positive feature map of normalised linear attention
+__device__ __forceinline__ float feature_map(float x) { return x > 0.f ? x + 1.f : expf(x); }
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -111,11 +119,11 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
   const int in_bf16 = p.in_bf16;
   const int esz = in_bf16 ? 2 : 4;
   const int xrows = ring_xrows(p.steps, kRing);
-  const uint32_t sbytes = slot_bytes(esz, xrows);
+  const uint32_t sbytes = slot_bytes(esz, xrows, p.variant == GLINATTN_NLA);
   float *s_act = reinterpret_cast<float *>(smem + kRing * sbytes);  // q | k | own v slice
   float *s_red = s_act + kNCH;                                      // [warp][k S | q S][kDC]
-  float *s_wsum = s_red + kNW * 2 * kDC;                            // [|q|^2, |k|^2, q.k][warp]
-  int *s_tab = reinterpret_cast<int *>(s_wsum + 3 * kNW);           // [kTab][kTabWords]
+  float *s_wsum = s_red + kNW * 2 * kDC;                            // [|q|^2, |k|^2, q.k, q.z][warp]
+  int *s_tab = reinterpret_cast<int *>(s_wsum + 4 * kNW);           // [kTab][kTabWords]
   uint64_t *s_full = reinterpret_cast<uint64_t *>(s_tab + kTab * kTabWords);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -129,6 +137,7 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
   const int K = (int)(U * (cluster + 1) / nclusters) - u0;
   const bool conv = p.conv_w != nullptr;
   const bool gdn = p.variant == GLINATTN_GDN;
+  const bool nla = p.variant == GLINATTN_NLA;  // no gates; phi(q), phi(k); z beside the state
   const int tsteps = steps < kTabSteps ? steps : kTabSteps;
   const int ndst = p.dst_per_step ? steps : 1;
   const size_t DD = (size_t)kD * kD;
@@ -155,7 +164,7 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
         if (t < tsteps && t < ndst && p.dst_slot) cp_async4(&e[lane], &p.dst_slot[(size_t)n * ndst + t]);
       } else if (lane <= 2 * kTabSteps) {
         const int t = lane - 1 - kTabSteps;
-        if (t < tsteps) cp_async4(&e[lane], &p.alpha[((size_t)n * steps + t) * H + h]);
+        if (t < tsteps && !nla) cp_async4(&e[lane], &p.alpha[((size_t)n * steps + t) * H + h]);
       } else if (lane <= 3 * kTabSteps) {
         const int t = lane - 1 - 2 * kTabSteps;
         if (t < tsteps && gdn) cp_async4(&e[lane], &p.beta[((size_t)n * steps + t) * H + h]);
@@ -179,9 +188,11 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
     const int n = unit_n(k), h = unit_h(k);
     uint8_t *st = smem + (k % kRing) * sbytes;
     uint8_t *small = st + kStateBytes;
-    const uint32_t bytes = kStateBytes + (conv ? 3u : 0u) * kNCH * esz + (uint32_t)xrows * kNCH * esz;
+    const uint32_t bytes = kStateBytes + (conv ? 3u : 0u) * kNCH * esz + (uint32_t)xrows * kNCH * esz +
+                           (nla ? kD * 4u : 0u);
     mbar_arrive_expect_tx(bar, bytes);
     tma_load_3d(st, &tstate, bar, col0, 0, slot * H + h);
+    if (nla) bulk_load(small + small_bytes(esz, xrows), p.z_src + ((size_t)slot * H + h) * kD, kD * 4, bar);
     if (conv) {
 #pragma unroll
       for (int j = 0; j < 3; ++j) {
@@ -283,14 +294,14 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
         const int d = e[1 + t];
         if (d < 0 || d >= p.pool_slots) bad |= GLINATTN_DEV_BAD_SLOT;
       }
-      for (int t = 0; t < tsteps && t < su; ++t) {
+      for (int t = 0; t < tsteps && t < su && !nla; ++t) {
         const float a = __int_as_float(e[1 + kTabSteps + t]);
         if (!(a > 0.f && a <= 1.f)) bad |= GLINATTN_DEV_BAD_GATE;
       }
       if (steps > kTabSteps) {  // the steps beyond the table, checked in global memory
         int b2 = 0;
         for (int t = kTabSteps + tid; t < steps; t += kNT) {
-          const float a = p.alpha[((size_t)n * steps + t) * H + h];
+          const float a = nla ? 1.f : p.alpha[((size_t)n * steps + t) * H + h];
           if (t < su && !(a > 0.f && a <= 1.f)) b2 |= GLINATTN_DEV_BAD_GATE;
           if (t < ndst && p.dst_slot) {
             const int d = p.dst_slot[(size_t)n * ndst + t];
@@ -308,6 +319,7 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
       float *sst = reinterpret_cast<float *>(smem + s * sbytes);
       float4 *st4 = reinterpret_cast<float4 *>(sst);
       const uint8_t *small = smem + s * sbytes + kStateBytes;
+      float *zs = reinterpret_cast<float *>(smem + s * sbytes + kStateBytes + small_bytes(esz, xrows));  // z (NLA)
       // raw input of local channel c at step st: the ring slot's rows for the
       // first xrows steps, global memory after that
       auto x_at = [&](int st, int c) -> float {
@@ -333,7 +345,7 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
             for (int j = 0; j < 3; ++j) hr[i][j] = ld_act(small, j * kNCH + c, in_bf16);
         }
       }
-      float a_nx = __int_as_float(e[1 + kTabSteps]);
+      float a_nx = nla ? 1.f : __int_as_float(e[1 + kTabSteps]);
       float b_nx = gdn ? __int_as_float(e[1 + 2 * kTabSteps]) : 0.f;
       int d_nx = e[1];
 
@@ -346,11 +358,11 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
         if (!last) {  // next step's scalars: table, else global memory
           const int t1 = t + 1;
           if (t1 < kTabSteps) {
-            a_nx = __int_as_float(e[1 + kTabSteps + t1]);
+            a_nx = nla ? 1.f : __int_as_float(e[1 + kTabSteps + t1]);
             if (gdn) b_nx = __int_as_float(e[1 + 2 * kTabSteps + t1]);
             if (p.dst_per_step) d_nx = e[1 + t1];
           } else {
-            a_nx = p.alpha[row + H];
+            a_nx = nla ? 1.f : p.alpha[row + H];
             if (gdn) b_nx = p.beta[row + H];
             if (p.dst_per_step && p.dst_slot) d_nx = p.dst_slot[(size_t)n * ndst + t1];
           }
@@ -362,8 +374,8 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
         for (int i = 0; i < kMaxC; ++i) {
           const int c = tid + i * kNT;
           const float x = xr[i];
-          const float y = conv ? fe::conv4(wr[i][0], wr[i][1], wr[i][2], wr[i][3], hr[i][0], hr[i][1], hr[i][2], x)
-                               : x;
+          float y = conv ? fe::conv4(wr[i][0], wr[i][1], wr[i][2], wr[i][3], hr[i][0], hr[i][1], hr[i][2], x) : x;
+          if (nla && c < 2 * kD) y = feature_map(y);
           yv[i] = y;
           // one q and one k channel per thread (channel tid of each)
           if (c < kD) sq = __fmul_rn(y, y);
@@ -389,8 +401,8 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
           iq = fe::inv_norm(fe::pairwise_sum<kNW>(s_wsum));
           ik = fe::inv_norm(fe::pairwise_sum<kNW>(s_wsum + kNW));
         }
-        const bool round_act = in_bf16 && (conv || p.qk_l2norm);
-        float qk_part = 0.f;
+        const bool round_act = in_bf16 && (conv || p.qk_l2norm || nla);
+        float qk_part = 0.f, qz_part = 0.f;
         {
           float qv = 0.f;
 #pragma unroll
@@ -402,20 +414,34 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
               else if (c < 2 * kD) y = __fmul_rn(y, ik);
               if (round_act) y = __bfloat162float(__float2bfloat16_rn(y));
               s_act[c] = y;
-              if (c < kD) qv = y;
-              else if (c < 2 * kD) qk_part = qv * y;  // q_c * k_c: same thread, same c % kD
+              if (c < kD) {
+                qv = y;
+                if (nla) qz_part = y * zs[c];
+              } else if (c < 2 * kD) {
+                qk_part = qv * y;  // q_c * k_c: same thread, same c % kD
+              }
             }
           }
         }
         qk_part = warp_sum(qk_part);
         if (lane == 0) s_wsum[2 * kNW + warp] = qk_part;
+        if (nla) {
+          qz_part = warp_sum(qz_part);
+          if (lane == 0) s_wsum[3 * kNW + warp] = qz_part;
+        }
         if (!__syncthreads_and(ok)) {
           dead = true;
           break;
         }
-        float qk = 0.f;
+        float qk = 0.f, qz = 0.f;
 #pragma unroll
         for (int w = 0; w < kNW; ++w) qk += s_wsum[2 * kNW + w];
+        if (nla) {
+#pragma unroll
+          for (int w = 0; w < kNW; ++w) qz += s_wsum[3 * kNW + w];
+          // z <- z + phi(k): channel tid, read above only by this thread
+          zs[tid] += s_act[kD + tid];
+        }
 
         // ---- partial k S and q S over this thread's rows, then across rows ------
         const float *sqa = s_act, *ska = s_act + kD, *sva = s_act + 2 * kD;
@@ -475,8 +501,10 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
           if (emit) *reinterpret_cast<float4 *>(dst + (size_t)r * kD + 4 * cg) = S;
         }
         if (rg == 0 && p.o) {
-          const float o0 = a * y.x + qk * u.x, o1 = a * y.y + qk * u.y;
-          const float o2 = a * y.z + qk * u.z, o3 = a * y.w + qk * u.w;
+          // normalised linear attention divides by phi(q) . z_{t-1} + phi(q) . phi(k) + eps
+          const float inv = nla ? 1.f / (qz + qk + 1e-6f) : 1.f;
+          const float o0 = (a * y.x + qk * u.x) * inv, o1 = (a * y.y + qk * u.y) * inv;
+          const float o2 = (a * y.z + qk * u.z) * inv, o3 = (a * y.w + qk * u.w) * inv;
           const size_t ob = row * kD + col0 + 4 * cg;
           if (p.out_bf16) {
             const __nv_bfloat162 lo = __floats2bfloat162_rn(o0, o1), hi = __floats2bfloat162_rn(o2, o3);
@@ -487,6 +515,13 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
           } else {
             *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + ob) = make_float4(o0, o1, o2, o3);
           }
+        }
+        if (emit && nla && half == 0 && p.z_dst) {  // z after this step (the other half has its copy)
+          if (!hist_waited) {
+            cluster_wait();
+            hist_waited = true;
+          }
+          p.z_dst[((size_t)dslot * H + h) * kD + tid] = zs[tid];
         }
         if (emit && conv && p.conv_dst) {
           if (!hist_waited) {
@@ -529,13 +564,15 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
 bool decode128_supports(const RecurParams &p, int d) {
   return d == kD && p.src_slot != nullptr && (p.dst_slot != nullptr || p.S_dst == nullptr) && p.S_src != nullptr &&
          p.steps >= 1 && p.pool_slots > 0 && (p.conv_w == nullptr || p.conv_src != nullptr) &&
-         p.S_blocks == nullptr && p.Hq == p.H && p.variant != GLINATTN_NLA;
+         p.S_blocks == nullptr && p.Hq == p.H &&
+         (p.variant != GLINATTN_NLA ||  // the normaliser pool is copied in with the state
+          (p.z_src != nullptr && ((uintptr_t)p.z_src & 15u) == 0 && ((uintptr_t)p.z_dst & 15u) == 0));
 }
 
 template <int kRing>
 cudaError_t launch_ring(const RecurParams &p, cudaStream_t stream) {
   const int esz = p.in_bf16 ? 2 : 4;
-  const int smem = (int)smem_bytes(esz, ring_xrows(p.steps, kRing), kRing);
+  const int smem = (int)smem_bytes(esz, ring_xrows(p.steps, kRing), kRing, p.variant == GLINATTN_NLA);
   CUtensorMap tmap;
   memset(&tmap, 0, sizeof(tmap));
   {
