@@ -109,7 +109,9 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-template <int kRing>
+// kNla: normalised linear attention as a template parameter, so the gated
+// instances carry none of its code
+template <int kRing, bool kNla>
 __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(const __grid_constant__ CUtensorMap tstate,
                                                         const RecurParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
   const int in_bf16 = p.in_bf16;
   const int esz = in_bf16 ? 2 : 4;
   const int xrows = ring_xrows(p.steps, kRing);
-  const uint32_t sbytes = slot_bytes(esz, xrows, p.variant == GLINATTN_NLA);
+  const uint32_t sbytes = slot_bytes(esz, xrows, kNla);
   float *s_act = reinterpret_cast<float *>(smem + kRing * sbytes);  // q | k | own v slice
   float *s_red = s_act + kNCH;                                      // [warp][k S | q S][kDC]
   float *s_wsum = s_red + kNW * 2 * kDC;                            // [|q|^2, |k|^2, q.k, q.z][warp]
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
   const int K = (int)(U * (cluster + 1) / nclusters) - u0;
   const bool conv = p.conv_w != nullptr;
   const bool gdn = p.variant == GLINATTN_GDN;
-  const bool nla = p.variant == GLINATTN_NLA;  // no gates; phi(q), phi(k); z beside the state
+  constexpr bool nla = kNla;  // no gates; phi(q), phi(k); z beside the state
   const int tsteps = steps < kTabSteps ? steps : kTabSteps;
   const int ndst = p.dst_per_step ? steps : 1;
   const size_t DD = (size_t)kD * kD;
@@ -569,10 +571,10 @@ bool decode128_supports(const RecurParams &p, int d) {
           (p.z_src != nullptr && ((uintptr_t)p.z_src & 15u) == 0 && ((uintptr_t)p.z_dst & 15u) == 0));
 }
 
-template <int kRing>
+template <int kRing, bool kNla>
 cudaError_t launch_ring(const RecurParams &p, cudaStream_t stream) {
   const int esz = p.in_bf16 ? 2 : 4;
-  const int smem = (int)smem_bytes(esz, ring_xrows(p.steps, kRing), kRing, p.variant == GLINATTN_NLA);
+  const int smem = (int)smem_bytes(esz, ring_xrows(p.steps, kRing), kRing, kNla);
   CUtensorMap tmap;
   memset(&tmap, 0, sizeof(tmap));
   {
@@ -582,9 +584,9 @@ cudaError_t launch_ring(const RecurParams &p, cudaStream_t stream) {
     if (!encode_3d_map(&tmap, p.S_src, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dims, box, false))
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(decode128_kernel<kRing>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(decode128_kernel<kRing, kNla>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode128_kernel<kRing>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(decode128_kernel<kRing, kNla>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -604,16 +606,17 @@ cudaError_t launch_ring(const RecurParams &p, cudaStream_t stream) {
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   int max_clusters = 0;
   cfg.gridDim = dim3(2 * (unsigned)sms);
-  if ((e = cudaOccupancyMaxActiveClusters(&max_clusters, decode128_kernel<kRing>, &cfg)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveClusters(&max_clusters, decode128_kernel<kRing, kNla>, &cfg)) != cudaSuccess) return e;
   if (max_clusters < 1) max_clusters = 1;
   const long long units = (long long)p.N * p.H;
   const long long clusters = units < max_clusters ? units : max_clusters;
   cfg.gridDim = dim3((unsigned)(2 * clusters));
-  return cudaLaunchKernelEx(&cfg, decode128_kernel<kRing>, tmap, p);
+  return cudaLaunchKernelEx(&cfg, decode128_kernel<kRing, kNla>, tmap, p);
 }
 
 cudaError_t launch_decode128(const RecurParams &p, cudaStream_t stream) {
-  return p.steps > 1 ? launch_ring<1>(p, stream) : launch_ring<2>(p, stream);
+  if (p.variant == GLINATTN_NLA) return p.steps > 1 ? launch_ring<1, true>(p, stream) : launch_ring<2, true>(p, stream);
+  return p.steps > 1 ? launch_ring<1, false>(p, stream) : launch_ring<2, false>(p, stream);
 }
 
 }  // namespace glinattn
