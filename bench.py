@@ -807,6 +807,27 @@ def run_profile(args):
         def step():
             glinattn_selective_scan(ex["x"], ex["delta"], ex["Bm"], ex["Cm"], ex["A"], None, y=y, h_T=h,
                                     workspace=ws)
+    elif args.profile == "nla_decode":
+        from gated_deltanet_02_gb300 import NLA
+        dx = inputs.nla_decode(256, 16, 128, 512, seed=0, device=dev)
+        od = torch.empty(256, 16, 128, dtype=torch.bfloat16, device=dev)
+
+        def step():
+            glinattn_decode(dx["q"], dx["k"], dx["v"], None, None, dx["pool"], dx["slot_ids"], variant=NLA,
+                            z_pool=dx["zpool"], o=od)
+    elif args.profile == "scan_decode":
+        from gated_deltanet_02_gb300 import glinattn_selective_scan_decode
+        R, D, N, P = 256, 2048, 16, 1536
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(7)
+        dx = inputs.selective_scan_inputs(R, 1, D, N, seed=3, device=dev, dtype=torch.bfloat16)
+        pool = torch.randn(P, D, N, device=dev, generator=gen) * 0.1
+        slots = torch.randperm(P, device=dev, generator=gen)[:R].to(torch.int32)
+        xd, dd, bd, cd = (dx[k][:, 0].contiguous() for k in ("x", "delta", "Bm", "Cm"))
+        yd = torch.empty(R, D, dtype=torch.bfloat16, device=dev)
+
+        def step():
+            glinattn_selective_scan_decode(xd, dd, bd, cd, dx["A"], pool, slots, y=yd)
     else:
         g = GDN_CFG
         gx = inputs.gdn_prefill(g["B"], g["H"], g["T"], g["d"], seed=0, device=dev)
@@ -827,7 +848,8 @@ def run_profile(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["gla", "decode", "gdn", "spec", "ssd", "nla", "scan"], default=None,
+    ap.add_argument("--profile", choices=["gla", "decode", "gdn", "spec", "ssd", "nla", "scan", "nla_decode",
+                                          "scan_decode"], default=None,
                     help="run one workload's kernel a few times for a profiler, then exit")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)
