@@ -45,6 +45,30 @@ def test_scan_fp32(T, N):
     assert relerr(y, y_ref) <= TOL_F32 and relerr(h, h_ref) <= TOL_F32
 
 
+@pytest.mark.parametrize("T", [1, 63, 65, 130])
+@pytest.mark.parametrize("N", [8, 16, 32])
+def test_scan_many_channels(T, N):
+    """B = 4 sequences of D = 1000 channels (a ragged last block of channels),
+    T ending inside, at and past a 64-token chunk."""
+    ex = inputs.selective_scan_inputs(4, T, 1000, N, seed=40 + T + N, start=True)
+    g = to(ex, DEV)
+    y, h = _run(g, g["h0"])
+    y_ref, h_ref = _ref(ex, f64(ex["h0"]))
+    assert relerr(y, y_ref) <= TOL_F32 and relerr(h, h_ref) <= TOL_F32
+
+
+def test_scan_many_channels_bf16_state_in_place():
+    ex = inputs.selective_scan_inputs(4, 70, 1024, 16, seed=44, dtype=torch.bfloat16, start=True)
+    g = to(ex, DEV)
+    h = g["h0"].clone()
+    yb, h2 = _run(g, h, out_dtype=torch.bfloat16, h_T=h)
+    assert h2.data_ptr() == h.data_ptr()
+    y_ref, h_ref = _ref(ex, f64(ex["h0"]))
+    err = np.abs(f64(yb) - y_ref)
+    assert (err <= np.abs(y_ref) * 2.0 ** -8 + TOL_O_BF16 * np.abs(y_ref).max()).all()
+    assert relerr(h, h_ref) <= TOL_F32
+
+
 def test_scan_bf16_inputs_and_outputs():
     ex = inputs.selective_scan_inputs(2, 150, 256, 16, seed=3, dtype=torch.bfloat16)
     g = to(ex, DEV)
