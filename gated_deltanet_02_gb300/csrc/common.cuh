@@ -53,5 +53,9 @@ glinattn_status launch_conv_blocks(const glinattn_prefill_args &a, cudaStream_t 
 // Persistent pipelined decode / speculative decode for 128 x 128 pooled states.
 bool decode128_supports(const RecurParams &p, int d);
 cudaError_t launch_decode128(const RecurParams &p, cudaStream_t stream);
+// Verify-only speculative decode (outputs, no states) from one read of each
+// start state, in the chunked form over the drafts.
+bool verify128_supports(const RecurParams &p, int d);
+cudaError_t launch_verify128(const RecurParams &p, cudaStream_t stream);
 
 }  // namespace glinattn

@@ -460,6 +460,8 @@ cudaError_t launch(const RecurParams &p, cudaStream_t stream) {
 
 glinattn_status launch_recurrent(const RecurParams &p, int dk, int dv, cudaStream_t stream) {
   if ((long long)p.N * p.H == 0) return GLINATTN_OK;
+  if (dk == dv && verify128_supports(p, dk))
+    return launch_verify128(p, stream) == cudaSuccess ? GLINATTN_OK : GLINATTN_ERR_CUDA;
   if (dk == dv && decode128_supports(p, dk))
     return launch_decode128(p, stream) == cudaSuccess ? GLINATTN_OK : GLINATTN_ERR_CUDA;
   cudaError_t e;

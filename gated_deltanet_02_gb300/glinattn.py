@@ -295,7 +295,9 @@ def glinattn_spec_decode(q, k, v, alpha, beta, state_pool, src_slots, dst_slots,
     """D draft steps per request.  q, k [N,D,Hq,dk], v [N,D,H,dv];
     alpha/beta [N,D,H]; src_slots [N], dst_slots [N,D] int32.  The state after
     draft i is written to state_pool[dst_slots[n, i]]; dst_slots=None only
-    verifies (outputs, no state written: see glinattn_replay).  Returns
+    verifies (outputs, no state written: see glinattn_replay; at d = 128 the
+    gated forms compute them in the chunked form over the drafts, equal to the
+    per-draft outputs up to fp32 rounding).  Returns
     o [N,D,H,dv]."""
     N, D, Hq, dk = q.shape
     H, dv = v.shape[2], v.shape[3]

@@ -249,7 +249,13 @@ glinattn_status glinattn_decode(const glinattn_decode_args *args, glinattn_strea
  *   and from every source slot (not checked on the device).
  *   dst_slots == NULL verifies only: the outputs are written, no state and no
  *   conv cache, and the pool keeps one state per request; glinattn_replay
- *   then applies the accepted drafts (the replay-buffer alternative).
+ *   then applies the accepted drafts (the replay-buffer alternative).  For
+ *   GLA and Gated DeltaNet with dk = dv = 128, q / k heads = heads and
+ *   draft_len <= 16, the verify-only outputs come from the chunked form of
+ *   the section "Two ways to write the same computation" over the D drafts
+ *   (one read of the start state), so they equal the per-draft outputs up to
+ *   fp32 rounding rather than bit for bit; the front end (conv, L2 norm, bf16
+ *   rounding of q, k, v) is the decode step's, bit for bit.
  *
  *   q, k [N, D, Hq, dk]   v [N, D, H, dv]   alpha, beta [N, D, H]
  *   src_slots [N]  dst_slots [N, D] or NULL  int32    o [N, D, H, dv]
