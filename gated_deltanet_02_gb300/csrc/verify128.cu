@@ -196,10 +196,16 @@ __global__ void __launch_bounds__(kVT, 2) verify128_kernel(const RecurParams p) 
       }
     }
     __syncthreads();
+    // the inverse norms, once per token: warp 0, lane t (q) and 16 + t (k)
+    float *s_inv = vsm + kOffKS;  // free until the row products
+    if (p.qk_l2norm && warp == 0 && (lane & 15) < D) {
+      const int t = lane & 15;
+      s_inv[lane] = fe::inv_norm(fe::pairwise_sum<4>(vsm + kOffWsum + t * 8 + (lane < 16 ? 0 : 4)));
+    }
+    if (p.qk_l2norm) __syncthreads();
     for (int t = 0; t < D; ++t) {
       float y = act[t * 3 * kD + ca];
-      const float inv = p.qk_l2norm ? fe::inv_norm(fe::pairwise_sum<4>(vsm + kOffWsum + t * 8 + (ca < kD ? 0 : 4)))
-                                    : 1.f;
+      const float inv = p.qk_l2norm ? s_inv[(ca < kD ? 0 : 16) + t] : 1.f;
       y = __fmul_rn(y, inv);
       if (round_act) y = __bfloat162float(__float2bfloat16_rn(y));
       act[t * 3 * kD + ca] = y;
@@ -261,59 +267,61 @@ __global__ void __launch_bounds__(kVT, 2) verify128_kernel(const RecurParams p) 
       red4[((warp * 2 * kG) + 2 * i + 1) * (kD / 4) + lane] = qp[i];
     }
     __syncthreads();
-    for (int e = tid; e < 2 * kG * kD; e += kVT) {
-      const int v = e / kD, c = e - (e / kD) * kD, t = g0 + v / 2;
-      float s = 0.f;
+    // the sums over the warps; in the last group warp 0 forms the D x D scalars
+    // (lane = draft) meanwhile and warps 1-7 add
+    const bool last = g0 + kG >= D;
+    if (last && warp == 0) {
+      const float a = lane < D ? ga : 1.f;
+      float g = log2f(a);
 #pragma unroll
-      for (int w = 0; w < 8; ++w) s += vsm[kOffRed + (w * 2 * kG + v) * kD + c];
-      if (t < D) vsm[((v & 1) ? kOffQS : kOffKS) + t * kD + c] = s;
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, g, o);
+        if (lane >= o) g += y;
+      }
+      if (lane < D) {
+        vsm[kOffGam + lane] = exp2f(g);
+        vsm[kOffBet + lane] = kGdn ? gb : 0.f;
+      }
+      // P_ij = (q_i . k_j) 2^(g_i - g_j) for j <= i: lane j of row i
+      for (int i = 0; i < D; ++i) {
+        const float gi = __shfl_sync(0xffffffffu, g, i);
+        if (lane <= i) vsm[kOffP + i * kMaxD + lane] = vsm[kOffGqk + i * kMaxD + lane] * exp2f(gi - g);
+      }
+      if (kGdn) {
+        // A_ij = beta_i 2^(g_i - g_j) (k_i . k_j), j < i; T = (I + A)^-1 by forward
+        // substitution, lane = column j: x = e_j, then x_m -= A_mi x_i for m > i
+        const float bl = lane < D ? gb : 0.f;
+        float x[kMaxD];
+#pragma unroll
+        for (int m = 0; m < kMaxD; ++m) x[m] = m == lane ? 1.f : 0.f;
+#pragma unroll
+        for (int i = 0; i < kMaxD; ++i) {
+          if (i >= D) break;
+          const float gi = __shfl_sync(0xffffffffu, g, i);
+#pragma unroll
+          for (int m = i + 1; m < kMaxD; ++m) {
+            if (m >= D) break;
+            const float gm = __shfl_sync(0xffffffffu, g, m), bm = __shfl_sync(0xffffffffu, bl, m);
+            const float amj = bm * exp2f(gm - gi) * vsm[kOffGkk + m * kMaxD + i];
+            x[m] = fmaf(-amj, x[i], x[m]);
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < kMaxD; ++m)
+          if (m < D && lane < D) vsm[kOffT + m * kMaxD + lane] = x[m];
+      }
+    } else {
+      const int e0 = last ? tid - 32 : tid, step = last ? kVT - 32 : kVT;
+      for (int e = e0; e < 2 * kG * kD; e += step) {
+        const int v = e / kD, c = e - (e / kD) * kD, t = g0 + v / 2;
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) s += vsm[kOffRed + (w * 2 * kG + v) * kD + c];
+        if (t < D) vsm[((v & 1) ? kOffQS : kOffKS) + t * kD + c] = s;
+      }
     }
     __syncthreads();
   }
-
-  // ---- the D x D scalars (warp 0; lane = draft) ----------------------------------
-  if (warp == 0) {
-    const float a = lane < D ? ga : 1.f;
-    float g = log2f(a);
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, g, o);
-      if (lane >= o) g += y;
-    }
-    if (lane < D) {
-      vsm[kOffGam + lane] = exp2f(g);
-      vsm[kOffBet + lane] = kGdn ? gb : 0.f;
-    }
-    // P_ij = (q_i . k_j) 2^(g_i - g_j) for j <= i: lane j of row i
-    for (int i = 0; i < D; ++i) {
-      const float gi = __shfl_sync(0xffffffffu, g, i);
-      if (lane <= i) vsm[kOffP + i * kMaxD + lane] = vsm[kOffGqk + i * kMaxD + lane] * exp2f(gi - g);
-    }
-    if (kGdn) {
-      // A_ij = beta_i 2^(g_i - g_j) (k_i . k_j), j < i; T = (I + A)^-1 by forward
-      // substitution, lane = column j: x = e_j, then x_m -= A_mi x_i for m > i
-      const float bl = lane < D ? gb : 0.f;
-      float x[kMaxD];
-#pragma unroll
-      for (int m = 0; m < kMaxD; ++m) x[m] = m == lane ? 1.f : 0.f;
-#pragma unroll
-      for (int i = 0; i < kMaxD; ++i) {
-        if (i >= D) break;
-        const float gi = __shfl_sync(0xffffffffu, g, i);
-#pragma unroll
-        for (int m = i + 1; m < kMaxD; ++m) {
-          if (m >= D) break;
-          const float gm = __shfl_sync(0xffffffffu, g, m), bm = __shfl_sync(0xffffffffu, bl, m);
-          const float amj = bm * exp2f(gm - gi) * vsm[kOffGkk + m * kMaxD + i];
-          x[m] = fmaf(-amj, x[i], x[m]);
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < kMaxD; ++m)
-        if (m < D && lane < D) vsm[kOffT + m * kMaxD + lane] = x[m];
-    }
-  }
-  __syncthreads();
 
   // ---- outputs: column c, drafts of parity tid >> 7 ---------------------------------
   {
