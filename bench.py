@@ -761,7 +761,7 @@ def run_profile(args):
             glinattn_decode(dx["q"], dx["k"], dx["v"], dx["alpha"], dx["beta"], dx["pool"], dx["slot_ids"],
                             variant=GDN, conv_w=dx["conv_w"], conv_pool=dx["conv_pool"], qk_l2norm=True,
                             o=od)
-    elif args.profile == "spec":
+    elif args.profile in ("spec", "verify"):
         from gated_deltanet_02_gb300 import glinattn_spec_decode
         N, D, H, d = 64, 4, 32, 128
         g = torch.Generator(device=dev)
@@ -771,6 +771,8 @@ def run_profile(args):
         conv_w = torch.randn(3 * H * d, 4, device=dev, generator=g) * 0.5
         src = torch.arange(N, dtype=torch.int32, device=dev)
         dst = (N + torch.arange(N * D, dtype=torch.int32, device=dev)).view(N, D)
+        if args.profile == "verify":  # verify only: outputs, no per-draft states
+            dst = None
         dr = inputs.spec_drafts(N, D, H, d, seed=1, device=dev)
         od = torch.empty(N, D, H, d, dtype=torch.bfloat16, device=dev)
 
@@ -848,8 +850,8 @@ def run_profile(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["gla", "decode", "gdn", "spec", "ssd", "nla", "scan", "nla_decode",
-                                          "scan_decode"], default=None,
+    ap.add_argument("--profile", choices=["gla", "decode", "gdn", "spec", "verify", "ssd", "nla", "scan",
+                                          "nla_decode", "scan_decode"], default=None,
                     help="run one workload's kernel a few times for a profiler, then exit")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)
