@@ -159,11 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- the unit is skipped when a gate is outside (0, 1] ---------------------
   {
-    int bad = 0;
-    for (int t = tid; t < T && p.alpha; t += kThreads) {  // no gates: alpha = 1
-      const float a = p.alpha[((size_t)b * T + t) * p.H + h];
-      bad |= !(a > 0.f && a <= 1.f);
-    }
+    const int bad = p.alpha ? gates_bad(p.alpha + (size_t)b * T * p.H + h, T, p.H, tid, kThreads) : 0;  // no gates: 1
     if (__syncthreads_or(bad)) {
       if (tid == 0 && p.dev_status) atomicOr(p.dev_status, GLINATTN_DEV_BAD_GATE);
       return;

@@ -26,6 +26,23 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
   }
 }
 
+// Whether any of a unit's T gates (alpha at a[t * stride]) is outside (0, 1]:
+// this thread's share, eight independent loads in flight per round.
+__device__ __forceinline__ int gates_bad(const float *a, int T, size_t stride, int tid, int nthreads) {
+  int bad = 0;
+  for (int t0 = tid; t0 < T; t0 += 8 * nthreads) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int t = t0 + j * nthreads;
+      v[j] = t < T ? a[(size_t)t * stride] : 1.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) bad |= !(v[j] > 0.f && v[j] <= 1.f);
+  }
+  return bad;
+}
+
 // Warp-uniform version for warps that go on to warp-collective tcgen05.ld.
 __device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort) {
   const bool ok = wait_bar(bar, parity, abort);
