@@ -15,9 +15,10 @@
 //      and phi(k) rounded to bf16 (the tensor-core operands) into the
 //      workspace, and the chunk's column sums of phi(k); the chunk-0 CTAs
 //      also copy the start normaliser, so that z_T may overwrite it;
-//   2. nla_zscan_kernel, one thread per (sequence, q / k head, channel): z at
-//      every chunk start of every value head (start normaliser plus the
-//      exclusive prefix of the chunk sums), and z_T;
+//   2. nla_zscan_kernel, one CTA per (sequence, q / k head), a thread per
+//      channel and group of chunks: z at every chunk start of every value
+//      head (start normaliser plus the exclusive prefix of the chunk sums),
+//      and z_T;
 //   3. gla_prefill_kernel, normalised instance: no gates; each token's
 //      denominator from z at its chunk start and the row sum, the outputs
 //      divided by it in the epilogue and written in the output dtype.
@@ -117,30 +118,53 @@ __global__ void __launch_bounds__(kFeatThreads, 4) nla_feature_kernel(const Feat
 
 // z at every chunk start for each value head of the q / k head: the start
 // normaliser plus the chunk sums of phi(k) before the chunk; then z_T.  The
-// loads are independent; 8 are in flight.
-__global__ void __launch_bounds__(kDK) nla_zscan_kernel(const float *__restrict__ dz, const float *__restrict__ z0w,
-                                                        float *__restrict__ zstart, float *z_T, int H, int Hq,
-                                                        int nchunks) {
+// chunks are split into kZG groups, one per 128-thread slice of the CTA: each
+// slice sums its group's chunk sums, the slices exchange their totals, then
+// each walks its group again (the second reads hit L2) writing z at every
+// chunk start.  Loads are independent, 8 in flight per thread.
+constexpr int kZG = 4;
+
+__global__ void __launch_bounds__(kDK * kZG) nla_zscan_kernel(const float *__restrict__ dz,
+                                                              const float *__restrict__ z0w,
+                                                              float *__restrict__ zstart, float *z_T, int H, int Hq,
+                                                              int nchunks) {
+  __shared__ float tot[kZG][kDK];
   const int bq = blockIdx.x;  // b * Hq + hq
   const int b = bq / Hq, hq = bq - b * Hq, rep = H / Hq;
-  const int d = threadIdx.x;
+  const int d = threadIdx.x % kDK, grp = threadIdx.x / kDK;
+  const int per = (nchunks + kZG - 1) / kZG;
+  const int c_begin = grp * per, c_end = min(nchunks, c_begin + per);
   const size_t src = (size_t)bq * nchunks * kDK + d;
-  float z = 0.f;
-  for (int c0 = 0; c0 < nchunks; c0 += 8) {
+  float s = 0.f;
+  for (int c0 = c_begin; c0 < c_end; c0 += 8) {
     float v[8];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) v[m] = c0 + m < nchunks ? dz[src + (size_t)(c0 + m) * kDK] : 0.f;
+    for (int m = 0; m < 8; ++m) v[m] = c0 + m < c_end ? dz[src + (size_t)(c0 + m) * kDK] : 0.f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) s += v[m];
+  }
+  tot[grp][d] = s;
+  __syncthreads();
+  float z = 0.f;
+  for (int g = 0; g < grp; ++g) z += tot[g][d];
+  for (int c0 = c_begin; c0 < c_end; c0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) v[m] = c0 + m < c_end ? dz[src + (size_t)(c0 + m) * kDK] : 0.f;
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      if (c0 + m < nchunks)
+      if (c0 + m < c_end)
         for (int h = hq * rep; h < (hq + 1) * rep; ++h)
           zstart[(((size_t)b * H + h) * nchunks + c0 + m) * kDK + d] = z0w[((size_t)b * H + h) * kDK + d] + z;
       z += v[m];
     }
   }
-  if (z_T)
+  if (z_T && grp == kZG - 1) {
+    float zt = 0.f;
+    for (int g = 0; g < kZG; ++g) zt += tot[g][d];
     for (int h = hq * rep; h < (hq + 1) * rep; ++h)
-      z_T[((size_t)b * H + h) * kDK + d] = z0w[((size_t)b * H + h) * kDK + d] + z;
+      z_T[((size_t)b * H + h) * kDK + d] = z0w[((size_t)b * H + h) * kDK + d] + zt;
+  }
 }
 
 struct Carve {
@@ -200,7 +224,7 @@ glinattn_status launch_nla_tc(const glinattn_prefill_args &a, cudaStream_t strea
   nla_feature_kernel<<<dim3((unsigned)nchunks, (unsigned)Hq, (unsigned)B), kFeatThreads, 0, stream>>>(fp);
   if (cudaGetLastError() != cudaSuccess) return GLINATTN_ERR_CUDA;
 
-  nla_zscan_kernel<<<(unsigned)(B * Hq), kDK, 0, stream>>>(w.dz, w.z0w, w.zstart, a.z_T, H, Hq, nchunks);
+  nla_zscan_kernel<<<(unsigned)(B * Hq), kDK * kZG, 0, stream>>>(w.dz, w.z0w, w.zstart, a.z_T, H, Hq, nchunks);
   if (cudaGetLastError() != cudaSuccess) return GLINATTN_ERR_CUDA;
 
   // gated linear attention with every gate 1 on the features, normalised in
