@@ -175,24 +175,36 @@ __global__ void __launch_bounds__(kVT, 2) verify128_kernel(const RecurParams p) 
       }
     }
     float *act = vsm + kOffAct;
-    for (int t = 0; t < D; ++t) {
-      const float xa = ld_in(rawx, t * kRawRow + ca, in_bf16);
-      const float ya = conv ? fe::conv4(wa[0], wa[1], wa[2], wa[3], ha[0], ha[1], ha[2], xa) : xa;
-      ha[0] = ha[1];
-      ha[1] = ha[2];
-      ha[2] = xa;
-      act[t * 3 * kD + ca] = ya;
-      if (has_v) {
-        const float xv = ld_in(rawx, t * kRawRow + cv, in_bf16);
-        const float yv = conv ? fe::conv4(wv[0], wv[1], wv[2], wv[3], hv[0], hv[1], hv[2], xv) : xv;
-        hv[0] = hv[1];
-        hv[1] = hv[2];
-        hv[2] = xv;
-        act[t * 3 * kD + cv] = round_act ? __bfloat162float(__float2bfloat16_rn(yv)) : yv;
+    // tokens in groups of 8: their squares summed over the lanes together
+    // (the same pairwise tree per token as one reduction each)
+    for (int t0 = 0; t0 < D; t0 += 8) {
+      float sq[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int t = t0 + k;
+        sq[k] = 0.f;
+        if (t < D) {
+          const float xa = ld_in(rawx, t * kRawRow + ca, in_bf16);
+          const float ya = conv ? fe::conv4(wa[0], wa[1], wa[2], wa[3], ha[0], ha[1], ha[2], xa) : xa;
+          ha[0] = ha[1];
+          ha[1] = ha[2];
+          ha[2] = xa;
+          act[t * 3 * kD + ca] = ya;
+          sq[k] = __fmul_rn(ya, ya);
+          if (has_v) {
+            const float xv = ld_in(rawx, t * kRawRow + cv, in_bf16);
+            const float yv = conv ? fe::conv4(wv[0], wv[1], wv[2], wv[3], hv[0], hv[1], hv[2], xv) : xv;
+            hv[0] = hv[1];
+            hv[1] = hv[2];
+            hv[2] = xv;
+            act[t * 3 * kD + cv] = round_act ? __bfloat162float(__float2bfloat16_rn(yv)) : yv;
+          }
+        }
       }
       if (p.qk_l2norm) {  // pairwise sums of squares: lanes, then the 4 warps of q (or k)
-        const float sq = fe::warp_pairwise_sum(__fmul_rn(ya, ya));
-        if (lane == 0) vsm[kOffWsum + t * 8 + warp] = sq;
+        const float r = fe::warp_pairwise_sum8(sq, lane);
+        const int row = 4 * (lane & 1) + 2 * ((lane >> 1) & 1) + ((lane >> 2) & 1);  // the row lane l holds
+        if (lane < 8 && t0 + row < D) vsm[kOffWsum + (t0 + row) * 8 + warp] = r;
       }
     }
     __syncthreads();
