@@ -3,14 +3,23 @@
 // With bf16 activations the short convolution and the L2 norm end in a
 // rounding to bf16, i.e. in a decision: a value near a bf16 rounding boundary
 // goes one way or the other depending on the last bits of the fp32 result.
-// Every kernel therefore evaluates the front end in one fixed order, with
-// every product and sum rounded on its own (no fused multiply-add):
-//   conv:  y = ((w0 x_{t-3} + w1 x_{t-2}) + w2 x_{t-1}) + w3 x_t
+// Every kernel therefore evaluates the front end in one fixed order, each
+// step rounded once:
+//   conv:  y = w0 x_{t-3}, then y = fma(w_j, x_j, y) for the later taps
+//          x_{t-2}, x_{t-1}, x_t (exact product and sum, one rounding)
 //   norm:  s = sum of y_i^2 over the row by pairwise summation (the row split
-//          in halves, recursively: adjacent pairs first), r = 1 / sqrt(s + 1e-6),
-//          each element scaled by r
+//          in halves, recursively: adjacent pairs first), every square and
+//          sum rounded on its own, r = 1 / sqrt(s + 1e-6), each element
+//          scaled by r
 // so that the same inputs give the same bf16 activations in every kernel:
-// prefill, decode and speculative decode agree bit for bit on them.
+// prefill, decode and speculative decode agree bit for bit on them.  A
+// product that must round before a sum is never left for the compiler to
+// fuse: sums after products are scalar __fadd_rn.  The two-lane forms
+// (mul / add / fma on fp32 pairs) are used for the conv, whose sums are
+// explicit fused multiply-adds, and for products not followed by a sum; a
+// two-lane product followed by a two-lane sum was fused into one rounding
+// even when written with the _rn intrinsics, which moved about one activation
+// in 30,000 by a bf16 step.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -19,12 +28,14 @@
 namespace glinattn {
 namespace fe {
 
-// one output of the width-4 causal convolution, oldest tap first
+// one output of the width-4 causal convolution, oldest tap first, every later
+// tap added by one fused multiply-add
 __device__ __forceinline__ float conv4(float w0, float w1, float w2, float w3, float x0, float x1, float x2,
                                        float x3) {
-  float acc = __fadd_rn(__fmul_rn(w0, x0), __fmul_rn(w1, x1));
-  acc = __fadd_rn(acc, __fmul_rn(w2, x2));
-  return __fadd_rn(acc, __fmul_rn(w3, x3));
+  float acc = __fmul_rn(w0, x0);
+  acc = __fmaf_rn(w1, x1, acc);
+  acc = __fmaf_rn(w2, x2, acc);
+  return __fmaf_rn(w3, x3, acc);
 }
 
 // sum over the 32 lanes, adjacent lanes first (xor 1, 2, 4, 8, 16): the
@@ -48,37 +59,21 @@ __device__ __forceinline__ float pairwise_sum(const float *s) {
 // the inverse norm of a row whose sum of squares is s
 __device__ __forceinline__ float inv_norm(float s) { return __frcp_rn(__fsqrt_rn(__fadd_rn(s, 1e-6f))); }
 
-// ---- two channels at once: the packed fp32 pair instructions round each half
-// on its own, exactly as the scalar operations above do
-using f2 = unsigned long long;  // (low half, high half)
-
-__device__ __forceinline__ f2 f2_pack(float lo, float hi) {
-  f2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(f2 v, float &lo, float &hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
-  f2 r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
-  f2 r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-// conv4 on a pair of channels
-__device__ __forceinline__ f2 conv4x2(f2 w0, f2 w1, f2 w2, f2 w3, f2 x0, f2 x1, f2 x2, f2 x3) {
-  return f2_add(f2_add(f2_add(f2_mul(w0, x0), f2_mul(w1, x1)), f2_mul(w2, x2)), f2_mul(w3, x3));
+// ---- two channels at once: the conv of a pair of channels
+__device__ __forceinline__ float2 conv4x2(float2 w0, float2 w1, float2 w2, float2 w3, float2 x0, float2 x1, float2 x2,
+                                          float2 x3) {
+  float2 acc = __fmul2_rn(w0, x0);
+  acc = __ffma2_rn(w1, x1, acc);
+  acc = __ffma2_rn(w2, x2, acc);
+  return __ffma2_rn(w3, x3, acc);
 }
 // two bf16x2 words a, b as fp32 pairs: their low halves (a.lo, b.lo) and their
 // high halves (a.hi, b.hi)
-__device__ __forceinline__ f2 bf16_lows(uint32_t a, uint32_t b) { return f2_pack(__uint_as_float(a << 16), __uint_as_float(b << 16)); }
-__device__ __forceinline__ f2 bf16_highs(uint32_t a, uint32_t b) {
-  return f2_pack(__uint_as_float(a & 0xffff0000u), __uint_as_float(b & 0xffff0000u));
+__device__ __forceinline__ float2 bf16_lows(uint32_t a, uint32_t b) {
+  return make_float2(__uint_as_float(a << 16), __uint_as_float(b << 16));
+}
+__device__ __forceinline__ float2 bf16_highs(uint32_t a, uint32_t b) {
+  return make_float2(__uint_as_float(a & 0xffff0000u), __uint_as_float(b & 0xffff0000u));
 }
 
 // Pairwise row sums of 8 rows at once: s[r] is this lane's partial of row r;

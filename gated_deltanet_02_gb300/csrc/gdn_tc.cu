@@ -354,10 +354,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       float4 wt[4];
 #pragma unroll
       for (int c2 = 0; c2 < 4; ++c2) wt[c2] = nwt[c2];
-      const fe::f2 we[4] = {fe::f2_pack(wt[0].x, wt[2].x), fe::f2_pack(wt[0].y, wt[2].y), fe::f2_pack(wt[0].z, wt[2].z),
-                            fe::f2_pack(wt[0].w, wt[2].w)};
-      const fe::f2 wo[4] = {fe::f2_pack(wt[1].x, wt[3].x), fe::f2_pack(wt[1].y, wt[3].y), fe::f2_pack(wt[1].z, wt[3].z),
-                            fe::f2_pack(wt[1].w, wt[3].w)};
+      const float2 we[4] = {make_float2(wt[0].x, wt[2].x), make_float2(wt[0].y, wt[2].y), make_float2(wt[0].z, wt[2].z),
+                            make_float2(wt[0].w, wt[2].w)};
+      const float2 wo[4] = {make_float2(wt[1].x, wt[3].x), make_float2(wt[1].y, wt[3].y), make_float2(wt[1].z, wt[3].z),
+                            make_float2(wt[1].w, wt[3].w)};
       // this chunk's history rows and gates were loaded one chunk ahead
       const uint2 hist[3] = {nhist[0], nhist[1], nhist[2]};
       const float a0 = nga.x, a1 = nga.y, be0 = ngb.x, be1 = ngb.y;
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         const int r0 = (fw / 3 + 2 * k) * 8;  // the task's 8 tokens
         // channels (4l, 4l + 2) and (4l + 1, 4l + 3) of rows r0 - 3 .. r0 + 7 as
         // fp32 pairs: the even and the odd channels of the lane's 8 bytes
-        fe::f2 xe[11], xo[11];
+        float2 xe[11], xo[11];
 #pragma unroll
         for (int m = 0; m < 11; ++m) {
           const int tr = r0 - 3 + m;
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           xo[m] = fe::bf16_highs(v.x, v.y);
         }
         // the 8 rows are independent: each step runs over all of them
-        fe::f2 ye[8], yo[8];
+        float2 ye[8], yo[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
           ye[r] = fe::conv4x2(we[0], we[1], we[2], we[3], xe[r], xe[r + 1], xe[r + 2], xe[r + 3]);
@@ -413,29 +413,25 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
           float ss[8];
 #pragma unroll
           for (int r = 0; r < 8; ++r) {
-            float a, c;
-            fe::f2_unpack(fe::f2_add(fe::f2_mul(ye[r], ye[r]), fe::f2_mul(yo[r], yo[r])), a, c);
-            ss[r] = __fadd_rn(a, c);
+            const float2 pe = __fmul2_rn(ye[r], ye[r]), po = __fmul2_rn(yo[r], yo[r]);
+            ss[r] = __fadd_rn(__fadd_rn(pe.x, po.x), __fadd_rn(pe.y, po.y));
           }
           const float inv = fe::inv_norm(fe::warp_pairwise_sum8(ss, lane));
 #pragma unroll
           for (int r = 0; r < 8; ++r) {
             const float ir = __shfl_sync(0xffffffffu, inv, fe::row_lane(r));
-            const fe::f2 i2 = fe::f2_pack(ir, ir);
-            ye[r] = fe::f2_mul(ye[r], i2);
-            yo[r] = fe::f2_mul(yo[r], i2);
+            const float2 i2 = make_float2(ir, ir);
+            ye[r] = __fmul2_rn(ye[r], i2);
+            yo[r] = __fmul2_rn(yo[r], i2);
           }
         }
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
           const bool valid = t0 + r0 + r < T;
-          float y0, y1, y2, y3;
-          fe::f2_unpack(ye[r], y0, y2);
-          fe::f2_unpack(yo[r], y1, y3);
           uint2 pk = make_uint2(0u, 0u);
           if (valid) {
-            pk.x = bits(__floats2bfloat162_rn(y0, y1));
-            pk.y = bits(__floats2bfloat162_rn(y2, y3));
+            pk.x = bits(__floats2bfloat162_rn(ye[r].x, yo[r].x));
+            pk.y = bits(__floats2bfloat162_rn(ye[r].y, yo[r].y));
           }
           const int t = r0 + r;
           const size_t grow = (unit * p.Tp + t0 + t) * kD + 4 * lane;

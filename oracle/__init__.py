@@ -56,7 +56,8 @@ def build(force: bool = False) -> str:
              or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
     if force or stale:
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-        # -ffp-contract=off: no product and sum fused into one rounding
+        # -ffp-contract=off: a product and a sum fuse into one rounding only
+        # where the source calls fmaf
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
                                "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB_PATH)
@@ -159,8 +160,9 @@ def recurrence(variant, q, k, v, alpha, beta=None, S0=None, return_states=False,
 def causal_conv(x, w, cache_in=None, single=False):
     """Depthwise causal conv, width 4: x [B,T,Cch], w [Cch,4], cache [B,3,Cch].
     Returns (y [B,T,Cch], cache_out [B,3,Cch]).  ``single``: evaluated in
-    single precision, each product and sum rounded, taps oldest first (the
-    values then fit a float exactly; see ``frontend``)."""
+    single precision, taps oldest first, the first product rounded and each
+    later tap added by one fused multiply-add (the values then fit a float
+    exactly; see ``frontend``)."""
     x, w = _f64(x), _f64(w)
     B, T, Cch = x.shape
     if w.shape != (Cch, 4):

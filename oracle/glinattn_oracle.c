@@ -224,11 +224,13 @@ int oracle_l2norm_rows(long long n, int d, double *x, double eps) {
  * Single-precision front end.  With bf16 activations the convolution and the
  * L2 norm end in a rounding to bf16: the value decides an integer (the bf16
  * code), so this step is evaluated in the precision the layer computes its
- * front end in, single precision, in the order the definitions read, every
- * product and sum rounded on its own (no fused multiply-add):
- *   y = ((w0 x_{t-3} + w1 x_{t-2}) + w2 x_{t-1}) + w3 x_t
+ * front end in, single precision, in the order the definitions read:
+ *   y = w0 x_{t-3} rounded, then each later tap added by one fused
+ *       multiply-add (w1 x_{t-2}, w2 x_{t-1}, w3 x_t in turn: the exact
+ *       product and sum, rounded once);
  *   s = sum of y_i^2 by pairwise summation (the row split in halves,
- *       recursively), r = 1 / sqrt(s + eps), y_i <- y_i r.
+ *       recursively), every square and sum rounded on its own,
+ *       r = 1 / sqrt(s + eps), y_i <- y_i r.
  * Inputs and outputs are doubles holding single-precision values.
  */
 int oracle_causal_conv_f32(int B, int T, int Cch, const double *x, const double *w,
@@ -244,11 +246,8 @@ int oracle_causal_conv_f32(int B, int T, int Cch, const double *x, const double 
       for (int c = 0; c < Cch; ++c) hist[(size_t)(t + 3) * Cch + c] = (float)x[((size_t)b * T + t) * Cch + c];
     for (int t = 0; t < T; ++t)
       for (int c = 0; c < Cch; ++c) {
-        float acc = 0.0f;
-        for (int j = 0; j < 4; ++j) {
-          const float prod = (float)w[(size_t)c * 4 + j] * hist[(size_t)(t + j) * Cch + c];
-          acc = j == 0 ? prod : acc + prod;
-        }
+        float acc = (float)w[(size_t)c * 4] * hist[(size_t)t * Cch + c];
+        for (int j = 1; j < 4; ++j) acc = fmaf((float)w[(size_t)c * 4 + j], hist[(size_t)(t + j) * Cch + c], acc);
         y[((size_t)b * T + t) * Cch + c] = (double)acc;
       }
     if (cache_out)

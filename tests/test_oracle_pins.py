@@ -350,13 +350,35 @@ def test_single_precision_conv_is_double_conv_rounded():
     np.testing.assert_array_equal(c32, c64)
     hist = np.concatenate([cache, x], axis=1)
     absp = sum(np.abs(w[:, j]) * np.abs(hist[:, j:j + T]) for j in range(4))
-    # 4 rounded products and 3 rounded sums: at most 7 units of roundoff of sum |w x|
-    assert (np.abs(y32 - y64) <= 7 * U32 * absp).all()
+    # 1 rounded product and 3 fused multiply-adds: at most 4 units of roundoff of sum |w x|
+    assert (np.abs(y32 - y64) <= 4 * U32 * absp).all()
     assert (y32 == y32.astype(np.float32)).all()  # float values
     # small integers: every product and partial sum is exact in float
     xi = rng.integers(-8, 9, (1, 9, 5)).astype(np.float64)
     wi = rng.integers(-8, 9, (5, 4)).astype(np.float64)
     np.testing.assert_array_equal(oracle.causal_conv(xi, wi, single=True)[0], oracle.causal_conv(xi, wi)[0])
+
+
+def test_single_precision_conv_fuses_the_later_taps():
+    """A fused multiply-add rounds the exact w x + acc once, so a result that
+    fits a float comes out exact even when the product alone does not:
+    1 * (-1) + (1 + 2^-12)^2 = 2^-11 + 2^-24, while the rounded product
+    (a tie, to even: 1 + 2^-11) would leave 2^-11.  The same holds for every
+    later tap; the first tap is a plain rounded product."""
+    e = 1.0 + 2.0 ** -12
+    exact = 2.0 ** -11 + 2.0 ** -24
+    for j in (1, 2, 3):
+        x = np.zeros((1, 4, 1))
+        w = np.zeros((1, 4))
+        # output at t = 3 reads x_0 .. x_3 with taps 0 .. 3; tap 0 gives -1, tap j gives e^2
+        x[0, 0, 0], w[0, 0] = -1.0, 1.0
+        x[0, j, 0], w[0, j] = e, e
+        y32 = oracle.causal_conv(x, w, single=True)[0]
+        assert y32[0, 3, 0] == exact, j
+    # the first tap alone is the rounded product: (1 + 2^-12)^2 -> 1 + 2^-11
+    x = np.zeros((1, 4, 1)); w = np.zeros((1, 4))
+    x[0, 0, 0], w[0, 0] = e, e
+    assert oracle.causal_conv(x, w, single=True)[0][0, 3, 0] == 1.0 + 2.0 ** -11
 
 
 def test_single_precision_l2norm_is_double_l2norm_rounded():

@@ -12,6 +12,7 @@ import torch
 
 import oracle
 from gated_deltanet_02_gb300 import GDN, GLA, glinattn_prefill, inputs
+from gated_deltanet_02_gb300.glinattn import prefill_workspace_size
 from oracle.chunked import chunked
 
 from helpers import TOL_F32, TOL_O_BF16, TOL_S_BF16, NT, f64, relerr, to
@@ -194,3 +195,75 @@ def test_more_units_than_sms(variant):
         o_ref, S_ref, _ = _oracle_prefill(sub, variant, conv, S0=S0)
         assert relerr(o[b:b + 1, :, h:h + 1], o_ref) <= TOL_O_BF16, (b, h)
         assert relerr(S[b:b + 1, h:h + 1], S_ref) <= TOL_S_BF16, (b, h)
+
+
+# ------------------------------------------------------- random shapes ---------
+def _shapes(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        out.append((int(rng.integers(1, 4)), int(rng.integers(1, 6)), int(rng.integers(1, 700)),
+                    bool(rng.integers(0, 2)), bool(rng.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("B,H,T,with_s0,bf16_out", _shapes(8, 2024))
+@pytest.mark.parametrize("variant", [GLA, GDN])
+def test_random_shapes_match_oracle(variant, B, H, T, with_s0, bf16_out):
+    """Seeded random batch, head count and length (ragged last chunks, one to
+    five heads, start state or none, bf16 or fp32 outputs) for both forms at
+    d = 128, against the oracle."""
+    conv = variant == GDN
+    maker = inputs.gdn_prefill if conv else inputs.gla_prefill
+    ex = maker(B, H, T, 128, seed=B * 1000 + H * 100 + T, **({} if conv else {"s0_std": 0.05}))
+    g = to(ex, DEV)
+    S0 = g.get("S0") if with_s0 else None
+    o, S, c = _gpu_prefill(g, variant, conv, S0=S0, out_dtype=torch.bfloat16 if bf16_out else torch.float32)
+    o_ref, S_ref, c_ref = _oracle_prefill(ex, variant, conv, S0=f64(ex["S0"]) if with_s0 else None)
+    if bf16_out:
+        err = np.abs(f64(o) - o_ref)
+        assert (err <= np.abs(o_ref) * 2.0 ** -8 + TOL_O_BF16 * np.abs(o_ref).max()).all()
+    else:
+        assert relerr(o, o_ref) <= TOL_O_BF16
+    assert relerr(S, S_ref) <= TOL_S_BF16
+    if conv:
+        assert np.array_equal(f64(c), c_ref)
+
+
+# ------------------------------------------------ prepared activations ---------
+def _prepared_qk(ws, B, H, T):
+    """q', k' as the chunked Gated DeltaNet kernels leave them in the
+    workspace: bf16 rows [B*H, Tp, 128] (Tp = T rounded up to the 64-token
+    chunk), q' first, k' at the next 256-byte boundary."""
+    Tp = (T + 63) // 64 * 64
+    n = B * H * Tp * 128 * 2
+    kq = ws[:n].view(torch.bfloat16).view(B, H, Tp, 128)[:, :, :T]
+    off = (n + 255) // 256 * 256
+    kk = ws[off:off + n].view(torch.bfloat16).view(B, H, Tp, 128)[:, :, :T]
+    return f64(kq).transpose(0, 2, 1, 3), f64(kk).transpose(0, 2, 1, 3)
+
+
+@pytest.mark.parametrize("B,H,T,with_conv_in", [(3, 3, 418, False), (2, 4, 1000, True), (1, 2, 4096, False)])
+def test_prepared_activations_bit_exact(B, H, T, with_conv_in):
+    """The bf16 q' and k' the tensor-core passes read (conv, L2 norm, rounding)
+    equal the oracle's front end bit for bit: the rounding to bf16 is a
+    decision both sides take in single precision, every product and sum
+    rounded on its own."""
+    ex = inputs.gdn_prefill(B, H, T, 128, seed=31 * T + H)
+    g = to(ex, DEV)
+    conv_in = None
+    if with_conv_in:
+        gen = torch.Generator().manual_seed(T)
+        conv_in = torch.randn((B, 3, 3 * H * 128), generator=gen).to(torch.bfloat16)
+    ws = torch.zeros(int(prefill_workspace_size(B, T, H, 128)), dtype=torch.uint8, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    glinattn_prefill(g["q"], g["k"], g["v"], g["alpha"], g["beta"], None, variant=GDN, conv_w=g["conv_w"],
+                     conv_in=None if conv_in is None else conv_in.to(DEV), qk_l2norm=True,
+                     out_dtype=torch.float32, workspace=ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    qp, kp = _prepared_qk(ws, B, H, T)
+    qf, kf, _, _ = oracle.frontend(f64(ex["q"]), f64(ex["k"]), f64(ex["v"]), f64(ex["conv_w"]),
+                                   f64(conv_in), True, True)
+    assert np.array_equal(qp, qf), int((qp != qf).sum())
+    assert np.array_equal(kp, kf), int((kp != kf).sum())
