@@ -388,9 +388,9 @@ def run_ours(args):
         if dist is not None:
             dist.destroy_process_group()
         return
-    traffic = profiled_traffic("gla_prefill_kernel", ["prefill_tc.cu", "sm100.cuh"])
-    prep_t = profiled_traffic("gdn_prep_kernel", ["gdn_tc.cu", "sm100.cuh"])
-    scan_t = profiled_traffic("gdn_scan_kernel", ["gdn_tc.cu", "sm100.cuh"])
+    traffic = profiled_traffic("gla_prefill_kernel", ["prefill_tc.cu", "sm100.cuh", "tc_common.cuh"])
+    prep_t = profiled_traffic("gdn_prep_kernel", ["gdn_tc.cu", "sm100.cuh", "tc_common.cuh", "frontend.cuh"])
+    scan_t = profiled_traffic("gdn_scan_kernel", ["gdn_tc.cu", "sm100.cuh", "tc_common.cuh", "frontend.cuh"])
     gdn_traffic = prep_t + scan_t if prep_t is not None and scan_t is not None else None
     line = {
         "metric": METRIC,
@@ -434,7 +434,7 @@ def run_ours(args):
                    "ms_per_step": dec_ms,
                    "roofline": {"bound": "hbm", "achieved": dsb / (dec_kms / 1e3) / 1e9, "peak": hbm,
                                 "unit": "GB/s", "frac": dsb / (dec_kms / 1e3) / 1e9 / hbm,
-                                "traffic": profiled_traffic("decode128_kernel", ["decode128.cu", "sm100.cuh"]),
+                                "traffic": profiled_traffic("decode128_kernel", ["decode128.cu", "sm100.cuh", "frontend.cuh"]),
                                 "algorithmic_bytes": dsb, "kernel": "decode128_kernel"}},
         "gdn_prefill": {"value": g["B"] * g["T"] * ws / (gdn_ms / 1e3), "unit": "tokens/s",
                         "config": "Gated DeltaNet prefill, B=2 H=16 T=8192 d=128, conv + L2 norm",
