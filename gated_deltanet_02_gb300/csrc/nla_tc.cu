@@ -9,19 +9,19 @@
 // Inside a chunk the denominator splits the same way as the numerator:
 // phi(q_t) . z_t = phi(q_t) . z_start + sum over s <= t of phi(q_t) . phi(k_s),
 // and the second term is the row sum of the masked phi(Q) phi(K)^T tile that
-// the kernel already forms.  Three launches:
+// the kernel already forms.  Two launches:
 //
 //   1. nla_feature_kernel, one CTA per (chunk, q / k head, sequence): phi(q)
 //      and phi(k) rounded to bf16 (the tensor-core operands) into the
 //      workspace, and the chunk's column sums of phi(k); the chunk-0 CTAs
 //      also copy the start normaliser, so that z_T may overwrite it;
-//   2. nla_zscan_kernel, one CTA per (sequence, q / k head), a thread per
-//      channel and group of chunks: z at every chunk start of every value
-//      head (start normaliser plus the exclusive prefix of the chunk sums),
-//      and z_T;
-//   3. gla_prefill_kernel, normalised instance: no gates; each token's
-//      denominator from z at its chunk start and the row sum, the outputs
-//      divided by it in the epilogue and written in the output dtype.
+//   2. gla_prefill_kernel, normalised instance: no gates; z is the state of a
+//      value column that is 1 in every token, so warpgroup A carries it from
+//      chunk to chunk (the start normaliser plus each chunk's column sums,
+//      which travel with the chunk's tiles) and forms each token's
+//      denominator from z at its chunk start and the row sum; the outputs
+//      are divided by it in the epilogue and written in the output dtype,
+//      and z_T is written at the end.
 //
 // The denominators use the same bf16 feature values as the numerator.
 #include <cuda_bf16.h>
@@ -116,60 +116,9 @@ __global__ void __launch_bounds__(kFeatThreads, 4) nla_feature_kernel(const Feat
   }
 }
 
-// z at every chunk start for each value head of the q / k head: the start
-// normaliser plus the chunk sums of phi(k) before the chunk; then z_T.  The
-// chunks are split into kZG groups, one per 128-thread slice of the CTA: each
-// slice sums its group's chunk sums, the slices exchange their totals, then
-// each walks its group again (the second reads hit L2) writing z at every
-// chunk start.  Loads are independent, 8 in flight per thread.
-constexpr int kZG = 4;
-
-__global__ void __launch_bounds__(kDK * kZG) nla_zscan_kernel(const float *__restrict__ dz,
-                                                              const float *__restrict__ z0w,
-                                                              float *__restrict__ zstart, float *z_T, int H, int Hq,
-                                                              int nchunks) {
-  __shared__ float tot[kZG][kDK];
-  const int bq = blockIdx.x;  // b * Hq + hq
-  const int b = bq / Hq, hq = bq - b * Hq, rep = H / Hq;
-  const int d = threadIdx.x % kDK, grp = threadIdx.x / kDK;
-  const int per = (nchunks + kZG - 1) / kZG;
-  const int c_begin = grp * per, c_end = min(nchunks, c_begin + per);
-  const size_t src = (size_t)bq * nchunks * kDK + d;
-  float s = 0.f;
-  for (int c0 = c_begin; c0 < c_end; c0 += 8) {
-    float v[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) v[m] = c0 + m < c_end ? dz[src + (size_t)(c0 + m) * kDK] : 0.f;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) s += v[m];
-  }
-  tot[grp][d] = s;
-  __syncthreads();
-  float z = 0.f;
-  for (int g = 0; g < grp; ++g) z += tot[g][d];
-  for (int c0 = c_begin; c0 < c_end; c0 += 8) {
-    float v[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) v[m] = c0 + m < c_end ? dz[src + (size_t)(c0 + m) * kDK] : 0.f;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      if (c0 + m < c_end)
-        for (int h = hq * rep; h < (hq + 1) * rep; ++h)
-          zstart[(((size_t)b * H + h) * nchunks + c0 + m) * kDK + d] = z0w[((size_t)b * H + h) * kDK + d] + z;
-      z += v[m];
-    }
-  }
-  if (z_T && grp == kZG - 1) {
-    float zt = 0.f;
-    for (int g = 0; g < kZG; ++g) zt += tot[g][d];
-    for (int h = hq * rep; h < (hq + 1) * rep; ++h)
-      z_T[((size_t)b * H + h) * kDK + d] = z0w[((size_t)b * H + h) * kDK + d] + zt;
-  }
-}
-
 struct Carve {
   __nv_bfloat16 *fq, *fk;
-  float *dz, *zstart, *z0w;
+  float *dz, *z0w;
   size_t bytes;
 };
 
@@ -180,16 +129,14 @@ Carve carve(void *base, const glinattn_prefill_args &a) {
   const int nchunks = (a.seqlen + kC - 1) / kC;
   const size_t feat = align256((size_t)a.batch * a.seqlen * Hq * kDK * 2);
   const size_t dz = align256((size_t)a.batch * Hq * nchunks * kDK * 4);
-  const size_t zs = align256((size_t)a.batch * a.heads * nchunks * kDK * 4);
   const size_t zw = align256((size_t)a.batch * a.heads * kDK * 4);
   uint8_t *p = static_cast<uint8_t *>(base);
   Carve c;
   c.fq = reinterpret_cast<__nv_bfloat16 *>(p);
   c.fk = reinterpret_cast<__nv_bfloat16 *>(p + feat);
   c.dz = reinterpret_cast<float *>(p + 2 * feat);
-  c.zstart = reinterpret_cast<float *>(p + 2 * feat + dz);
-  c.z0w = reinterpret_cast<float *>(p + 2 * feat + dz + zs);
-  c.bytes = 2 * feat + dz + zs + zw;
+  c.z0w = reinterpret_cast<float *>(p + 2 * feat + dz);
+  c.bytes = 2 * feat + dz + zw;
   return c;
 }
 
@@ -224,9 +171,6 @@ glinattn_status launch_nla_tc(const glinattn_prefill_args &a, cudaStream_t strea
   nla_feature_kernel<<<dim3((unsigned)nchunks, (unsigned)Hq, (unsigned)B), kFeatThreads, 0, stream>>>(fp);
   if (cudaGetLastError() != cudaSuccess) return GLINATTN_ERR_CUDA;
 
-  nla_zscan_kernel<<<(unsigned)(B * Hq), kDK * kZG, 0, stream>>>(w.dz, w.z0w, w.zstart, a.z_T, H, Hq, nchunks);
-  if (cudaGetLastError() != cudaSuccess) return GLINATTN_ERR_CUDA;
-
   // gated linear attention with every gate 1 on the features, normalised in
   // its epilogue
   glinattn_prefill_args g = a;
@@ -236,7 +180,7 @@ glinattn_status launch_nla_tc(const glinattn_prefill_args &a, cudaStream_t strea
   g.alpha = nullptr;
   g.beta = nullptr;
   g.state_every = 0;
-  return launch_prefill_tc_nla(g, stream, nullptr, w.zstart);
+  return launch_prefill_tc_nla(g, stream, nullptr, w.dz, w.z0w, a.z_T);
 }
 
 }  // namespace glinattn

@@ -80,12 +80,14 @@ constexpr uint32_t kGateBytes = 1088;                          // one GateRing e
 constexpr uint32_t kOffBar = kOffG + kStages * kGateBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
 // the normalised variant only, past the barriers: 1 / denominator ring
-// [slot][token] and z at the chunk start [stage][d_k]
+// [slot][token], the chunk's column sums of phi(k) [stage][d_k] and z at the
+// chunk start, one copy per warp of warpgroup A [4][d_k]
 constexpr int kDenSlots = 4;
 constexpr uint32_t kOffDen = kOffBar + 256;
 constexpr uint32_t kOffZ = kOffDen + kDenSlots * kC * 4;
 constexpr uint32_t kZBytes = kDK * 4;
-constexpr uint32_t kSmemBytesNla = kOffZ + kStages * kZBytes + 1024;
+constexpr uint32_t kOffZrun = kOffZ + kStages * kZBytes;
+constexpr uint32_t kSmemBytesNla = kOffZrun + 4 * kZBytes + 1024;
 static_assert(kSmemBytesNla <= 232448, "shared memory budget");
 
 // TMEM columns: QK^T double-buffered (64 each), Q[S_hi|S_lo] (128), P V
@@ -100,10 +102,13 @@ struct GlaParams {
   const int *skip;  // [B, H] or NULL: units to skip (a gate elsewhere in a split sequence is invalid)
   int state_every, nblocks;  // states emitted after every state_every tokens (a multiple of 64)
   float *S_blocks;
-  // normalised linear attention: z at every chunk start, including the start
-  // normaliser, [B, H, nchunks, d_k]; the outputs are divided by
-  // phi(q_t) . z_t + 1e-6 (the kNla instances only)
-  const float *nla_z;
+  // normalised linear attention (the kNla instances only): the column sums
+  // of phi(k) of every chunk [B, Hq, nchunks, d_k], the start normaliser
+  // [B, H, d_k] and z_T [B, H, d_k] (NULL: not written); the outputs are
+  // divided by phi(q_t) . z_t + 1e-6
+  const float *nla_dz;
+  const float *nla_z0;
+  float *nla_zT;
   const float *alpha;
   const float *S0;
   float *S_T;
@@ -232,9 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *st = smem + kOffStage + s * kStageBytes;
         mbar_arrive_expect_tx(&bars->full[s], kNla ? kStageBytes + kZBytes : kStageBytes);
         const int t0 = c * kC;
-        if (kNla)  // z at this chunk's start travels with its tiles
-          bulk_load(smem + kOffZ + s * kZBytes, p.nla_z + (((size_t)b * p.H + h) * nchunks + c) * kDK, kZBytes,
-                    &bars->full[s]);
+        if (kNla)  // the chunk's column sums of phi(k) travel with its tiles
+          bulk_load(smem + kOffZ + s * kZBytes, p.nla_dz + (((size_t)b * (p.H / p.rep) + hq) * nchunks + c) * kDK,
+                    kZBytes, &bars->full[s]);
         tma_load_4d(st, &tq, &bars->full[s], 0, hq, t0, b);
         tma_load_4d(st + kTileQ / 2, &tq, &bars->full[s], 64, hq, t0, b);
         tma_load_4d(st + kTileQ, &tk, &bars->full[s], 0, hq, t0, b);
@@ -316,6 +321,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q4 = warp & 3;
     const int e = tid - 64;               // 0..127
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    // normalised instance: every warp carries z at the chunk start (lane l
+    // channels 4l .. 4l+3) and keeps a copy in shared memory for the
+    // denominators of its rows, so no other warp waits on it
+    float4 zl = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 *zw = reinterpret_cast<float4 *>(smem + kOffZrun + q4 * kZBytes);
+    if (kNla) {
+      zl = reinterpret_cast<const float4 *>(p.nla_z0 + ((size_t)b * p.H + h) * kDK)[lane];
+      zw[lane] = zl;
+      __syncwarp();
+    }
     for (int c = 0; c < nchunks; ++c) {
       const int s = c % kStages;
       const uint32_t sph = (uint32_t)(c / kStages) & 1u;
@@ -374,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // tile), plus its half of the masked row of phi(Q) phi(K)^T
           const int half = lane >> 4;
           const uint32_t qrow = smem_u32(smem + kOffStage + s * kStageBytes) + half * (kTileQ / 2);
-          const float4 *zh = reinterpret_cast<const float4 *>(smem + kOffZ + s * kZBytes) + 16 * half;
+          const float4 *zh = zw + 16 * half;
           float den = 0.f;
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) den += qk[jj];
@@ -395,6 +410,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           den += __shfl_xor_sync(0xffffffffu, den, 16);
           if (lane < 16) reinterpret_cast<float *>(smem + kOffDen)[(c & (kDenSlots - 1)) * kC + row] = 1.f / (den + 1e-6f);
           mbar_arrive(&bars->den_ready[c & (kDenSlots - 1)]);
+          // z at the next chunk start: plus the chunk's column sums of phi(k)
+          const float4 dz = reinterpret_cast<const float4 *>(smem + kOffZ + s * kZBytes)[lane];
+          zl.x += dz.x;
+          zl.y += dz.y;
+          zl.z += dz.z;
+          zl.w += dz.w;
+          __syncwarp();  // every lane has read this chunk's z
+          zw[lane] = zl;
+          __syncwarp();
         }
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
@@ -427,6 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(&bars->p_ready[tb]);
     }
+    if (kNla && q4 == 2 && vblk == 0 && p.nla_zT && !*abort)
+      reinterpret_cast<float4 *>(p.nla_zT + ((size_t)b * p.H + h) * kDK)[lane] = zl;
   } else if (warp < 10) {
     // ============ warpgroup B: the state chain and the outputs ============
     const int q4 = warp & 3;
@@ -687,11 +713,11 @@ glinattn_status launch_prefill_tc(const glinattn_prefill_args &a, cudaStream_t s
 }
 
 glinattn_status launch_prefill_tc_skip(const glinattn_prefill_args &a, cudaStream_t stream, const int *skip) {
-  return launch_prefill_tc_nla(a, stream, skip, nullptr);
+  return launch_prefill_tc_nla(a, stream, skip, nullptr, nullptr, nullptr);
 }
 
 glinattn_status launch_prefill_tc_nla(const glinattn_prefill_args &a, cudaStream_t stream, const int *skip,
-                                      const float *nla_z) {
+                                      const float *nla_dz, const float *nla_z0, float *nla_zT) {
   CUtensorMap tq, tk, tv;
   const int Hq = a.qk_heads > 0 ? a.qk_heads : a.heads;
   if (!make_act_map(&tq, a.q, a.batch, a.seqlen, Hq, kDK) ||
@@ -715,11 +741,13 @@ glinattn_status launch_prefill_tc_nla(const glinattn_prefill_args &a, cudaStream
   p.state_every = a.state_every > 0 && a.seqlen / a.state_every > 0 ? a.state_every : 0;
   p.nblocks = p.state_every ? a.seqlen / p.state_every : 0;
   p.S_blocks = a.S_blocks;
-  p.nla_z = nla_z;
-  auto kernel = nla_z ? (p.out_bf16 ? gla_prefill_kernel<true, false, true> : gla_prefill_kernel<false, false, true>)
+  p.nla_dz = nla_dz;
+  p.nla_z0 = nla_z0;
+  p.nla_zT = nla_zT;
+  auto kernel = nla_dz ? (p.out_bf16 ? gla_prefill_kernel<true, false, true> : gla_prefill_kernel<false, false, true>)
                 : p.out_bf16 ? (p.state_every ? gla_prefill_kernel<true, true, false> : gla_prefill_kernel<true, false, false>)
                              : (p.state_every ? gla_prefill_kernel<false, true, false> : gla_prefill_kernel<false, false, false>);
-  const uint32_t smem_bytes = nla_z ? kSmemBytesNla : kSmemBytes;
+  const uint32_t smem_bytes = nla_dz ? kSmemBytesNla : kSmemBytes;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes) != cudaSuccess)
     return GLINATTN_ERR_CUDA;
   const unsigned grid = (unsigned)a.batch * (unsigned)a.heads * (unsigned)(a.dv / kBV);

@@ -19,12 +19,13 @@ bool prefill_tc_supports(const glinattn_prefill_args &a);
 glinattn_status launch_prefill_tc(const glinattn_prefill_args &a, cudaStream_t stream);
 // The same with a per-unit skip flag array [B, H] (NULL: none).
 glinattn_status launch_prefill_tc_skip(const glinattn_prefill_args &a, cudaStream_t stream, const int *skip);
-// The same kernel for normalised linear attention: q and k are the features,
-// no gates; z_chunk [B, H, nchunks, d_k] holds z at every chunk start
-// (including the start normaliser) and the outputs are divided by
-// phi(q_t) . z_t + 1e-6.
+// The same kernel for normalised linear attention (nonzero dz): q and k are
+// the features, no gates; dz [B, Hq, nchunks, d_k] holds every chunk's column
+// sums of phi(k), z0 [B, H, d_k] the start normaliser (not overlapping z_T),
+// z_T [B, H, d_k] receives the final one (NULL: not written), and the outputs
+// are divided by phi(q_t) . z_t + 1e-6.
 glinattn_status launch_prefill_tc_nla(const glinattn_prefill_args &a, cudaStream_t stream, const int *skip,
-                                      const float *z_chunk);
+                                      const float *dz, const float *z0, float *z_T);
 
 // Gated linear attention split along the sequence when B * H * (d_v / 64)
 // leaves more than half of the SMs idle (gla_split.cu): the number of pieces

@@ -162,7 +162,7 @@ glinattn_status glinattn_prefill(const glinattn_prefill_args *args, glinattn_str
  *     and the gates there, about 1.3 KB per (batch, head, token); the serial
  *     pass reads them;
  *   - chunked normalised linear attention (required): the features, the
- *     chunk sums of phi(k) and the normaliser at every chunk start;
+ *     chunk sums of phi(k) and a copy of the start normaliser;
  *   - chunked gated linear attention when so few (batch, head) units would
  *     leave more than half of the SMs idle (optional): with the scratch the
  *     sequence is split into pieces -- a pass computes every piece's end
