@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         int b, h, c;
         decode(w, b, h, c);
         const int slot = it & 1;
-        if (!wait_bar(&bars->raw_empty[slot], ((uint32_t)(it >> 1) & 1u) ^ 1u, abort)) break;
+        if (!wait_bar<false>(&bars->raw_empty[slot], ((uint32_t)(it >> 1) & 1u) ^ 1u, abort)) break;
         uint8_t *raw = smem + kOffRaw + slot * kRawBytes;
         mbar_arrive_expect_tx(&bars->raw_full[slot], kRawBytes);
 #pragma unroll
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       const float a0 = nga.x, a1 = nga.y, be0 = ngb.x, be1 = ngb.y;
       if (w + (int)gridDim.x < nitems) prefetch(w + gridDim.x);
       // W, U~ of chunk it - 3 are done
-      if (!wait_bar_warp(&bars->prep_empty[ps], pph ^ 1u, abort)) break;
+      if (!wait_bar_warp<false>(&bars->prep_empty[ps], pph ^ 1u, abort)) break;
       if (fw == 0) {
         // gates of the chunk: g2 = cumsum(log2 alpha); alpha = 1, beta = 0 past T
         float *g2s = reinterpret_cast<float *>(smem + kOffPG + ps * 512);
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         p.Gp[unit * p.Tp + t0 + 2 * lane] = ga;
         p.Gp[unit * p.Tp + t0 + 2 * lane + 1] = gb;
       }
-      if (!wait_bar_warp(&bars->raw_full[slot], ph, abort)) break;
+      if (!wait_bar_warp<false>(&bars->raw_full[slot], ph, abort)) break;
       const uint8_t *raw = smem + kOffRaw + slot * kRawBytes + part * 16384 + cb * 8192;
       uint8_t *dst_tile = smem + kOffPrep + ps * 2 * kPrepTile + (part == 1 ? 0 : kPrepTile);
 #pragma unroll 1
@@ -463,8 +463,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     for (int w = blockIdx.x; w < nitems; w += gridDim.x, ++it) {
       const int slot = it & 1, ps = it % kPrepSlots;
       const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-      bool ok = wait_bar_warp(&bars->prep_full[ps], (uint32_t)(it / kPrepSlots) & 1u, abort) &&
-                wait_bar_warp(&bars->kk_ready[slot], ph, abort);
+      bool ok = wait_bar_warp<false>(&bars->prep_full[ps], (uint32_t)(it / kPrepSlots) & 1u, abort) &&
+                wait_bar_warp<false>(&bars->kk_ready[slot], ph, abort);
       if (!inv_all(ok)) break;
       const float *g2s = reinterpret_cast<const float *>(smem + kOffPG + ps * 512);
       const float *betas = g2s + kC;
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
       }
       // the epilogue warps have read T of the previous chunk
-      ok = wait_bar_warp(&bars->t_free, ((uint32_t)it & 1u) ^ 1u, abort);
+      ok = wait_bar_warp<false>(&bars->t_free, ((uint32_t)it & 1u) ^ 1u, abort);
       if (!inv_all(ok)) break;  // also orders the writes of A before the reads below
       // ---- T00 = (I + A00)^-1 (warp 0) and T11 = (I + A11)^-1 (warp 1), each in
       // 16 x 16 sub-blocks [Ta 0; Tb Tc]: the diagonal ones by forward
@@ -632,8 +632,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       // ---- T diag(beta gamma) and T diag(beta) as bf16 hi / lo MMA operands in
       // tensor memory, once the inverse is done and the previous chunk's W and U~
       // MMAs have read them
-      if (!wait_bar_warp(&bars->t_ready, (uint32_t)it & 1u, abort)) break;
-      if (!wait_bar_warp(&bars->tm_free, ((uint32_t)it & 1u) ^ 1u, abort)) break;
+      if (!wait_bar_warp<false>(&bars->t_ready, (uint32_t)it & 1u, abort)) break;
+      if (!wait_bar_warp<false>(&bars->tm_free, ((uint32_t)it & 1u) ^ 1u, abort)) break;
       float *colbg = reinterpret_cast<float *>(smem + kOffCol) + slot * 2 * kC;
       float *colb = colbg + kC;
       if (etid < kC) {
@@ -682,7 +682,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       tc_fence_before();
       warp_arrive(&bars->tm_ready);
       warp_arrive(&bars->t_free);
-      if (!wait_bar_warp(&bars->wu_ready, (uint32_t)it & 1u, abort)) break;
+      if (!wait_bar_warp<false>(&bars->wu_ready, (uint32_t)it & 1u, abort)) break;
       tc_fence_after();
       float v0[32], v1[32];
       tmem_ld16x256b_x8x2(tmem + kColW + lane_base, tmem + kColW + 64 + lane_base, v0, v1);
@@ -901,7 +901,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < nchunks; ++c) {
         const int s = c % kStages;
         prefetch(c + kStages + kPrefetch);
-        if (!wait_bar(&bars->empty[s], ((uint32_t)(c / kStages) & 1u) ^ 1u, abort)) break;
+        if (!wait_bar<false>(&bars->empty[s], ((uint32_t)(c / kStages) & 1u) ^ 1u, abort)) break;
         uint8_t *st = smem + kOffStage + s * kStageBytes;
         uint64_t *fb = &bars->full[s];
         mbar_arrive_expect_tx(fb, kStageBytes);
@@ -932,8 +932,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dKm = desc_sw128(aQ + kTile, kTile / 2, 1024);
         const uint64_t dW = desc_sw128(aQ + 2 * kTile, 16, 1024);
         const uint64_t dS = desc_sw128(sbase + kOffS + (c & 1) * kTileS, 16, 1024);  // [S_hi | S_lo]
-        if (!wait_bar(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) break;
-        if (!wait_bar(&bars->s_ready, pc, abort)) break;
+        if (!wait_bar<false>(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) break;
+        if (!wait_bar<false>(&bars->s_ready, pc, abort)) break;
         tc_fence_after();
         // W [S_hi | S_lo]: M = 64, N = 64, K = d_k (W tile K-major, S tile MN-major)
 #pragma unroll
@@ -942,7 +942,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16(tmem + kColWS, dW + aoff, dS + ((ks * 2048) >> 4), id_xs, ks > 0);
         }
         umma_commit(&bars->ws_ready);
-        if (!wait_bar(&bars->u_ready, pc, abort)) break;
+        if (!wait_bar<false>(&bars->u_ready, pc, abort)) break;
         tc_fence_after();
         // dS = K'^T [rU_hi | rU_lo]: M = d_k (K' tile read M-major), N = 64, K = 64 tokens
 #pragma unroll
@@ -968,7 +968,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < nchunks; ++c) {
       const uint32_t pc = (uint32_t)c & 1u;
       const float gC = grow_chunk(G, p, unit, c, lane, grow);
-      if (!wait_bar_warp(&bars->qk_ready, pc, abort)) break;
+      if (!wait_bar_warp<false>(&bars->qk_ready, pc, abort)) break;
       tc_fence_after();
       float qk[32];
       tmem_ld16x256b_x8(tmem + kColQK + lane_base, qk);
@@ -1004,7 +1004,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           qk[4 * m + 3] = col + 1 <= r0 + 8 ? qk[4 * m + 3] * exp2f((g1 - gb) - m1) : 0.f;
         }
       }
-      if (!wait_bar_warp(&bars->p_free, pc ^ 1u, abort)) break;
+      if (!wait_bar_warp<false>(&bars->p_free, pc ^ 1u, abort)) break;
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
         uint32_t h0, l0, h1, l1;
@@ -1064,12 +1064,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float g0 = grow[r0], g1 = grow[r0 + 8];
 
       // ---- U = U~ - W S (the hi and lo products summed), r U -----------------------
-      if (!wait_bar_warp(&bars->ws_ready, pc, abort)) { ok = false; break; }
+      if (!wait_bar_warp<false>(&bars->ws_ready, pc, abort)) { ok = false; break; }
       tc_fence_after();
       float ws[32];
       tmem_ld16x256b_x8(tmem + kColWS + lane_base, ws);
-      if (!wait_bar_warp(&bars->full[s], sph, abort)) { ok = false; break; }
-      if (!wait_bar_warp(&bars->p_free, pc ^ 1u, abort)) { ok = false; break; }
+      if (!wait_bar_warp<false>(&bars->full[s], sph, abort)) { ok = false; break; }
+      if (!wait_bar_warp<false>(&bars->p_free, pc ^ 1u, abort)) { ok = false; break; }
       {
         // the U~ slice rows are 128 bytes (32 fp32), loaded with the 128-byte swizzle
         const uint32_t ut = smem_u32(smem + kOffStage + s * kStageBytes + 3 * kTile);
@@ -1100,7 +1100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       warp_arrive(&bars->u_ready);
 
       // ---- S <- gamma_C S + K'^T diag(r) U (hi and lo products summed) -----------
-      if (!wait_bar_warp(&bars->ds_ready, pc, abort)) { ok = false; break; }
+      if (!wait_bar_warp<false>(&bars->ds_ready, pc, abort)) { ok = false; break; }
       tc_fence_after();
       {
         const float gam = exp2f(gC);
@@ -1123,7 +1123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // ---- o = c_i (Q' S + P'' U), the hi and lo columns summed -----------------------
-      if (!wait_bar_warp(&bars->o_ready, pc, abort)) { ok = false; break; }
+      if (!wait_bar_warp<false>(&bars->o_ready, pc, abort)) { ok = false; break; }
       tc_fence_after();
       float ov[32];
       tmem_ld16x256b_x8(tmem + kColO + lane_base, ov);
@@ -1175,8 +1175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dS = desc_sw128(sbase + kOffS + (c & 1) * kTileS, 16, 1024);
         // Q' [S_hi | S_lo] once W S of this chunk is done (S_c is in place), and
         // the previous chunk's outputs are read
-        if (!wait_bar(&bars->ws_ready, pc, abort)) break;
-        if (!wait_bar(&bars->o_free, pc ^ 1u, abort)) break;
+        if (!wait_bar<false>(&bars->ws_ready, pc, abort)) break;
+        if (!wait_bar<false>(&bars->o_free, pc ^ 1u, abort)) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
@@ -1184,9 +1184,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_bf16(tmem + kColO, dQ + aoff, dS + ((ks * 2048) >> 4), id_xs, ks > 0);
         }
         // (P''hi + P''lo) [U_hi | U_lo] into the same columns, once K'^T r U is done
-        if (!wait_bar(&bars->ds_ready, pc, abort)) break;
-        if (!wait_bar(&bars->p_ready, pc, abort)) break;
-        if (!wait_bar(&bars->u_ready, pc, abort)) break;
+        if (!wait_bar<false>(&bars->ds_ready, pc, abort)) break;
+        if (!wait_bar<false>(&bars->p_ready, pc, abort)) break;
+        if (!wait_bar<false>(&bars->u_ready, pc, abort)) break;
         tc_fence_after();
 #pragma unroll
         for (int part = 0; part < 2; ++part)
@@ -1205,8 +1205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sbase = smem_u32(smem);
       for (int c = 0; c < nchunks; ++c) {  // M = 64 tokens, N = 64 tokens, K = d_k
         const int s = c % kStages;
-        if (!wait_bar(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) break;
-        if (!wait_bar(&bars->qk_free, ((uint32_t)c & 1u) ^ 1u, abort)) break;
+        if (!wait_bar<false>(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) break;
+        if (!wait_bar<false>(&bars->qk_free, ((uint32_t)c & 1u) ^ 1u, abort)) break;
         tc_fence_after();
         const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
         const uint64_t dQ = desc_sw128(aQ, 16, 1024), dK = desc_sw128(aQ + kTile, 16, 1024);

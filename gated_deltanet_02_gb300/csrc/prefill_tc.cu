@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = c % kStages;
       const uint32_t use = (uint32_t)(c / kStages);
       if (lane == 0) prefetch(c + kStages + kPrefetch);
-      if (!wait_bar_warp(&bars->empty[s], (use & 1u) ^ 1u, abort)) break;
+      if (!wait_bar_warp<!kNla>(&bars->empty[s], (use & 1u) ^ 1u, abort)) break;
       if (lane == 0) {
         uint8_t *st = smem + kOffStage + s * kStageBytes;
         mbar_arrive_expect_tx(&bars->full[s], kNla ? kStageBytes + kZBytes : kStageBytes);
@@ -286,8 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = c % kStages;
         const int tb = c & 1;
         const uint32_t ph = (uint32_t)(c >> 1) & 1u;
-        if (!wait_bar(&bars->p_ready[tb], ph, abort)) break;  // V~ of chunk c
-        if (!wait_bar(&bars->ds_free, ((uint32_t)c & 1u) ^ 1u, abort)) break;
+        if (!wait_bar<!kNla>(&bars->p_ready[tb], ph, abort)) break;  // V~ of chunk c
+        if (!wait_bar<!kNla>(&bars->ds_free, ((uint32_t)c & 1u) ^ 1u, abort)) break;
         tc_fence_after();
         const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
         const uint32_t aK = aQ + kTileQ;
@@ -301,9 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&bars->ds_ready);
         umma_commit(&bars->p_free);  // V~ may be rewritten
         const int sb = c & 1;
-        if (!wait_bar(&bars->s_ready[sb], ph, abort)) break;
+        if (!wait_bar<!kNla>(&bars->s_ready[sb], ph, abort)) break;
         // Q S accumulator is single: the previous chunk's outputs must be read
-        if (c > 0 && !wait_bar(&bars->o_free[(c - 1) & 1], (uint32_t)((c - 1) >> 1) & 1u, abort)) break;
+        if (c > 0 && !wait_bar<!kNla>(&bars->o_free[(c - 1) & 1], (uint32_t)((c - 1) >> 1) & 1u, abort)) break;
         tc_fence_after();
         const uint64_t dS = desc_sw128(sbase + kOffS + sb * 2 * kTileS, kTileS, 1024);  // [hi | lo]
         // O1 = Q [S_hi | S_lo]: M = 64, N = 128, K = d_k (S tile rows = d_k, MN-major)
@@ -336,8 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sph = (uint32_t)(c / kStages) & 1u;
       const int tb = c & 1;
       const uint32_t ph = (uint32_t)(c >> 1) & 1u;
-      if (!wait_bar_warp(&bars->qk_ready[tb], ph, abort)) break;
-      if (!wait_bar_warp(&bars->full[s], sph, abort)) break;  // the chunk's gates and V tile
+      if (!wait_bar_warp<!kNla>(&bars->qk_ready[tb], ph, abort)) break;
+      if (!wait_bar_warp<!kNla>(&bars->full[s], sph, abort)) break;  // the chunk's gates and V tile
       const GateRing &gr = ring[s];
       tc_fence_after();
       // lane l < 16 holds row 16*q4 + l of QK^T (M = 64 layout); it keeps
@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&bars->qk_free[tb]);
-      if (!wait_bar_warp(&bars->p_free, ((uint32_t)c & 1u) ^ 1u, abort)) break;
+      if (!wait_bar_warp<!kNla>(&bars->p_free, ((uint32_t)c & 1u) ^ 1u, abort)) break;
       // D_ij = 2^(g_i - g_j).  When the chunk's total decay is moderate the
       // factors 2^g_i and 2^-g_j cannot overflow and D is their product (one
       // exp2 per token, done by the TMA warp); otherwise pairwise exp2.
@@ -466,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float egC = 1.f, eg_tok = 1.f;
     auto read_gates = [&](int c) -> bool {
       const int s = c % kStages;
-      if (!wait_bar_warp(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) return false;
+      if (!wait_bar_warp<!kNla>(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) return false;
       egC = ring[s].egC;
       eg_tok = ring[s].eg[tok & (kC - 1)];
       return true;
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t0 = c * kC;
 
       // ---- S <- gamma_C S + K^T V~ (the hi and lo column halves summed) -------
-      if (!wait_bar_warp(&bars->ds_ready, (uint32_t)c & 1u, abort)) { ok = false; break; }
+      if (!wait_bar_warp<!kNla>(&bars->ds_ready, (uint32_t)c & 1u, abort)) { ok = false; break; }
       tc_fence_after();
       {
         const float gam = egC;
@@ -529,11 +529,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // ---- o = gamma_i (Q S) + P V ----------------------------------------------
-      if (!wait_bar_warp(&bars->o_ready[tb], ph, abort)) { ok = false; break; }
+      if (!wait_bar_warp<!kNla>(&bars->o_ready[tb], ph, abort)) { ok = false; break; }
       float inv_den = 1.f;
       if (kNla) {
         const int ds = c & (kDenSlots - 1);
-        if (!wait_bar_warp(&bars->den_ready[ds], (uint32_t)(c / kDenSlots) & 1u, abort)) { ok = false; break; }
+        if (!wait_bar_warp<!kNla>(&bars->den_ready[ds], (uint32_t)(c / kDenSlots) & 1u, abort)) { ok = false; break; }
         inv_den = reinterpret_cast<const float *>(smem + kOffDen)[ds * kC + (tok & (kC - 1))];
       }
       tc_fence_after();
@@ -594,8 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Q K^T of chunk c: M = 64 tokens, N = 64 tokens, K = d_k (2 swizzle blocks x 4 steps)
       auto issue_qk = [&](int c) -> bool {
         const int s = c % kStages, tb = c & 1;
-        if (!wait_bar(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) return false;
-        if (!wait_bar(&bars->qk_free[tb], ((uint32_t)(c >> 1) & 1u) ^ 1u, abort)) return false;
+        if (!wait_bar<!kNla>(&bars->full[s], (uint32_t)(c / kStages) & 1u, abort)) return false;
+        if (!wait_bar<!kNla>(&bars->qk_free[tb], ((uint32_t)(c >> 1) & 1u) ^ 1u, abort)) return false;
         tc_fence_after();
         const uint32_t aQ = sbase + kOffStage + s * kStageBytes;
         const uint64_t dQ = desc_sw128(aQ, 16, 1024), dK = desc_sw128(aQ + kTileQ, 16, 1024);
@@ -613,8 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tb = c & 1;
         const uint32_t ph = (uint32_t)(c >> 1) & 1u;
         if (c + 1 < nchunks && !issue_qk(c + 1)) break;
-        if (!wait_bar(&bars->p_ready[tb], ph, abort)) break;
-        if (!wait_bar(&bars->o_free[tb], ph ^ 1u, abort)) break;   // P V buffer tb
+        if (!wait_bar<!kNla>(&bars->p_ready[tb], ph, abort)) break;
+        if (!wait_bar<!kNla>(&bars->o_free[tb], ph ^ 1u, abort)) break;   // P V buffer tb
         tc_fence_after();
         const uint64_t dV = desc_sw128(sbase + kOffStage + s * kStageBytes + kTileQ + kTileK, 16, 1024);
         // O2 = (Phi + Plo) V: M = 64, N = 64, K = 64 tokens

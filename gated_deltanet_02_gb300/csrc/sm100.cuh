@@ -45,19 +45,33 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 }
 
 // Test the phase; if it is not complete the thread is suspended until it
-// completes or about kSuspendHintNs pass, so waiting warps do not spin on the
-// issue slots that the working warps of the same sub-partition need.
+// completes or a time limit passes.  kHint: with a suspend-time hint of
+// kSuspendHintNs, so waiting warps do not spin on the issue slots that the
+// working warps of the same sub-partition need; without it the hardware's own
+// (shorter) limit applies, which measured faster in the Gated DeltaNet
+// kernels and the normalising prefill and slower in the gated one.
 constexpr uint32_t kSuspendHintNs = 1000000u;
 
+template <bool kHint = true>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
-      : "memory");
+  if constexpr (kHint) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 

@@ -13,11 +13,12 @@ namespace tc {
 using namespace sm100;
 
 // Bounded wait that also gives up as soon as another role has aborted.
+template <bool kHint = true>
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kHint>(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kHint>(bar, parity)) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       *abort = 1;
@@ -44,8 +45,9 @@ __device__ __forceinline__ int gates_bad(const float *a, int T, size_t stride, i
 }
 
 // Warp-uniform version for warps that go on to warp-collective tcgen05.ld.
+template <bool kHint = true>
 __device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort) {
-  const bool ok = wait_bar(bar, parity, abort);
+  const bool ok = wait_bar<kHint>(bar, parity, abort);
   return __all_sync(0xffffffffu, ok);
 }
 
