@@ -352,7 +352,7 @@ def run_ours(args):
         glinattn_prefill(gx["q"], gx["k"], gx["v"], gx["alpha"], gx["beta"], gx["S0"], variant=GDN,
                          conv_w=gx["conv_w"], qk_l2norm=True, o=og, S_T=Sg, workspace=gws)
 
-    gdn_ms, gdn_per = timed_steps(step_gdn, max(2, min(args.steps, 5)), 1, dist, dev)
+    gdn_ms, gdn_per = timed_steps(step_gdn, max(3, min(args.steps, 20)), 3, dist, dev)
     gdn_bytes, gdn_flops = gdn_bytes_flops(**g)
 
     # the same prefill keeping a prefix-cache checkpoint (state + conv cache) every 1024 tokens
@@ -366,7 +366,7 @@ def run_ours(args):
                          conv_w=gx["conv_w"], qk_l2norm=True, o=og, S_T=Sg, state_every=every, S_blocks=Sb,
                          conv_blocks=cb, workspace=gws)
 
-    ck_ms, _ = timed_steps(step_gdn_ck, max(2, min(args.steps, 5)), 1, dist, dev)
+    ck_ms, _ = timed_steps(step_gdn_ck, max(3, min(args.steps, 20)), 3, dist, dev)
     ck_bytes = Sb.numel() * 4 + cb.numel() * 2
 
     # ---- long context: 3-segment prefill, then 64 x 4 speculative decode -------------
@@ -678,7 +678,7 @@ def nla_run(args, dist, dev, rank):
         glinattn_prefill(ex["q"], ex["k"], ex["v"], None, None, None, variant=NLA, o=o, S_T=S, z_T=z,
                          workspace=ws)
 
-    pre_ms, pre_per = timed_steps(step_prefill, max(3, min(args.steps, 10)), 2, dist, dev)
+    pre_ms, pre_per = timed_steps(step_prefill, max(3, min(args.steps, 20)), 3, dist, dev)
     # q, k, v in (bf16), o out (bf16), S_T and z_T out: the layer's own bytes
     pre_bytes = B * T * H * d * 2 * 4 + B * H * (d * d + d) * 4
     N, P = 256, 512
