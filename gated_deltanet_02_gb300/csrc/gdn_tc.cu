@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         int b, h, c;
         decode(w, b, h, c);
         const int slot = it & 1;
-        if (!wait_bar<false>(&bars->raw_empty[slot], ((uint32_t)(it >> 1) & 1u) ^ 1u, abort)) break;
+        if (!wait_bar(&bars->raw_empty[slot], ((uint32_t)(it >> 1) & 1u) ^ 1u, abort)) break;
         uint8_t *raw = smem + kOffRaw + slot * kRawBytes;
         mbar_arrive_expect_tx(&bars->raw_full[slot], kRawBytes);
 #pragma unroll
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       const float a0 = nga.x, a1 = nga.y, be0 = ngb.x, be1 = ngb.y;
       if (w + (int)gridDim.x < nitems) prefetch(w + gridDim.x);
       // W, U~ of chunk it - 3 are done
-      if (!wait_bar_warp<false>(&bars->prep_empty[ps], pph ^ 1u, abort)) break;
+      if (!wait_bar_warp(&bars->prep_empty[ps], pph ^ 1u, abort)) break;
       if (fw == 0) {
         // gates of the chunk: g2 = cumsum(log2 alpha); alpha = 1, beta = 0 past T
         float *g2s = reinterpret_cast<float *>(smem + kOffPG + ps * 512);
@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         p.Gp[unit * p.Tp + t0 + 2 * lane] = ga;
         p.Gp[unit * p.Tp + t0 + 2 * lane + 1] = gb;
       }
-      if (!wait_bar_warp<false>(&bars->raw_full[slot], ph, abort)) break;
+      if (!wait_bar_warp(&bars->raw_full[slot], ph, abort)) break;
       const uint8_t *raw = smem + kOffRaw + slot * kRawBytes + part * 16384 + cb * 8192;
       uint8_t *dst_tile = smem + kOffPrep + ps * 2 * kPrepTile + (part == 1 ? 0 : kPrepTile);
 #pragma unroll 1
@@ -463,8 +463,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     for (int w = blockIdx.x; w < nitems; w += gridDim.x, ++it) {
       const int slot = it & 1, ps = it % kPrepSlots;
       const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-      bool ok = wait_bar_warp<false>(&bars->prep_full[ps], (uint32_t)(it / kPrepSlots) & 1u, abort) &&
-                wait_bar_warp<false>(&bars->kk_ready[slot], ph, abort);
+      bool ok = wait_bar_warp(&bars->prep_full[ps], (uint32_t)(it / kPrepSlots) & 1u, abort) &&
+                wait_bar_warp(&bars->kk_ready[slot], ph, abort);
       if (!inv_all(ok)) break;
       const float *g2s = reinterpret_cast<const float *>(smem + kOffPG + ps * 512);
       const float *betas = g2s + kC;
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
       }
       // the epilogue warps have read T of the previous chunk
-      ok = wait_bar_warp<false>(&bars->t_free, ((uint32_t)it & 1u) ^ 1u, abort);
+      ok = wait_bar_warp(&bars->t_free, ((uint32_t)it & 1u) ^ 1u, abort);
       if (!inv_all(ok)) break;  // also orders the writes of A before the reads below
       // ---- T00 = (I + A00)^-1 (warp 0) and T11 = (I + A11)^-1 (warp 1), each in
       // 16 x 16 sub-blocks [Ta 0; Tb Tc]: the diagonal ones by forward
@@ -632,8 +632,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       // ---- T diag(beta gamma) and T diag(beta) as bf16 hi / lo MMA operands in
       // tensor memory, once the inverse is done and the previous chunk's W and U~
       // MMAs have read them
-      if (!wait_bar_warp<false>(&bars->t_ready, (uint32_t)it & 1u, abort)) break;
-      if (!wait_bar_warp<false>(&bars->tm_free, ((uint32_t)it & 1u) ^ 1u, abort)) break;
+      if (!wait_bar_warp(&bars->t_ready, (uint32_t)it & 1u, abort)) break;
+      if (!wait_bar_warp(&bars->tm_free, ((uint32_t)it & 1u) ^ 1u, abort)) break;
       float *colbg = reinterpret_cast<float *>(smem + kOffCol) + slot * 2 * kC;
       float *colb = colbg + kC;
       if (etid < kC) {
@@ -682,7 +682,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       tc_fence_before();
       warp_arrive(&bars->tm_ready);
       warp_arrive(&bars->t_free);
-      if (!wait_bar_warp<false>(&bars->wu_ready, (uint32_t)it & 1u, abort)) break;
+      if (!wait_bar_warp(&bars->wu_ready, (uint32_t)it & 1u, abort)) break;
       tc_fence_after();
       float v0[32], v1[32];
       tmem_ld16x256b_x8x2(tmem + kColW + lane_base, tmem + kColW + 64 + lane_base, v0, v1);

@@ -48,8 +48,9 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 // completes or a time limit passes.  kHint: with a suspend-time hint of
 // kSuspendHintNs, so waiting warps do not spin on the issue slots that the
 // working warps of the same sub-partition need; without it the hardware's own
-// (shorter) limit applies, which measured faster in the Gated DeltaNet
-// kernels and the normalising prefill and slower in the gated one.
+// (shorter) limit applies, which measured faster in the Gated DeltaNet scan
+// and the normalising prefill and slower in the gated prefill and the Gated
+// DeltaNet preparation pass.
 constexpr uint32_t kSuspendHintNs = 1000000u;
 
 template <bool kHint = true>
