@@ -111,7 +111,9 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 // kNla: normalised linear attention as a template parameter, so the gated
 // instances carry none of its code
-template <int kRing, bool kNla>
+// kOut: the call writes outputs (a replay does not: then the q S row
+// products, the q . k scalars and their reductions are skipped)
+template <int kRing, bool kNla, bool kOut>
 __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(const __grid_constant__ CUtensorMap tstate,
                                                         const RecurParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -425,22 +427,28 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
             }
           }
         }
-        qk_part = warp_sum(qk_part);
-        if (lane == 0) s_wsum[2 * kNW + warp] = qk_part;
-        if (nla) {
-          qz_part = warp_sum(qz_part);
-          if (lane == 0) s_wsum[3 * kNW + warp] = qz_part;
+        if (kOut) {
+          qk_part = warp_sum(qk_part);
+          if (lane == 0) s_wsum[2 * kNW + warp] = qk_part;
+          if (nla) {
+            qz_part = warp_sum(qz_part);
+            if (lane == 0) s_wsum[3 * kNW + warp] = qz_part;
+          }
         }
         if (!__syncthreads_and(ok)) {
           dead = true;
           break;
         }
         float qk = 0.f, qz = 0.f;
+        if (kOut) {
 #pragma unroll
-        for (int w = 0; w < kNW; ++w) qk += s_wsum[2 * kNW + w];
+          for (int w = 0; w < kNW; ++w) qk += s_wsum[2 * kNW + w];
+        }
         if (nla) {
+          if (kOut) {
 #pragma unroll
-          for (int w = 0; w < kNW; ++w) qz += s_wsum[3 * kNW + w];
+            for (int w = 0; w < kNW; ++w) qz += s_wsum[3 * kNW + w];
+          }
           // z <- z + phi(k): channel tid, read above only by this thread
           zs[tid] += s_act[kD + tid];
         }
@@ -454,20 +462,24 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
           const float4 S = st4[r * kColG + cg];
           const float kr = ska[r], qr = sqa[r];
           x.x += kr * S.x; x.y += kr * S.y; x.z += kr * S.z; x.w += kr * S.w;
-          y.x += qr * S.x; y.y += qr * S.y; y.z += qr * S.z; y.w += qr * S.w;
+          if (kOut) {
+            y.x += qr * S.x; y.y += qr * S.y; y.z += qr * S.z; y.w += qr * S.w;
+          }
         }
         // the warp's two row groups (lanes l and l ^ 16 share a column group)
         x.x += __shfl_xor_sync(0xffffffffu, x.x, 16);
         x.y += __shfl_xor_sync(0xffffffffu, x.y, 16);
         x.z += __shfl_xor_sync(0xffffffffu, x.z, 16);
         x.w += __shfl_xor_sync(0xffffffffu, x.w, 16);
-        y.x += __shfl_xor_sync(0xffffffffu, y.x, 16);
-        y.y += __shfl_xor_sync(0xffffffffu, y.y, 16);
-        y.z += __shfl_xor_sync(0xffffffffu, y.z, 16);
-        y.w += __shfl_xor_sync(0xffffffffu, y.w, 16);
+        if (kOut) {
+          y.x += __shfl_xor_sync(0xffffffffu, y.x, 16);
+          y.y += __shfl_xor_sync(0xffffffffu, y.y, 16);
+          y.z += __shfl_xor_sync(0xffffffffu, y.z, 16);
+          y.w += __shfl_xor_sync(0xffffffffu, y.w, 16);
+        }
         if (lane < 16) {
           *reinterpret_cast<float4 *>(&s_red[(warp * 2 + 0) * kDC + 4 * cg]) = x;
-          *reinterpret_cast<float4 *>(&s_red[(warp * 2 + 1) * kDC + 4 * cg]) = y;
+          if (kOut) *reinterpret_cast<float4 *>(&s_red[(warp * 2 + 1) * kDC + 4 * cg]) = y;
         }
         __syncthreads();
         x = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -475,9 +487,11 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
 #pragma unroll
         for (int w = 0; w < kNW; ++w) {
           const float4 a4 = *reinterpret_cast<const float4 *>(&s_red[(w * 2 + 0) * kDC + 4 * cg]);
-          const float4 b4 = *reinterpret_cast<const float4 *>(&s_red[(w * 2 + 1) * kDC + 4 * cg]);
+          const float4 b4 = kOut ? *reinterpret_cast<const float4 *>(&s_red[(w * 2 + 1) * kDC + 4 * cg]) : a4;
           x.x += a4.x; x.y += a4.y; x.z += a4.z; x.w += a4.w;
-          y.x += b4.x; y.y += b4.y; y.z += b4.z; y.w += b4.w;
+          if (kOut) {
+            y.x += b4.x; y.y += b4.y; y.z += b4.z; y.w += b4.w;
+          }
         }
 
         // ---- update: shared copy for the next step, global copy when due --------
@@ -502,7 +516,7 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
           if (!last) st4[r * kColG + cg] = S;
           if (emit) *reinterpret_cast<float4 *>(dst + (size_t)r * kD + 4 * cg) = S;
         }
-        if (rg == 0 && p.o) {
+        if (kOut && rg == 0 && p.o) {
           // normalised linear attention divides by phi(q) . z_{t-1} + phi(q) . phi(k) + eps
           const float inv = nla ? 1.f / (qz + qk + 1e-6f) : 1.f;
           const float o0 = (a * y.x + qk * u.x) * inv, o1 = (a * y.y + qk * u.y) * inv;
@@ -571,7 +585,7 @@ bool decode128_supports(const RecurParams &p, int d) {
           (p.z_src != nullptr && ((uintptr_t)p.z_src & 15u) == 0 && ((uintptr_t)p.z_dst & 15u) == 0));
 }
 
-template <int kRing, bool kNla>
+template <int kRing, bool kNla, bool kOut>
 cudaError_t launch_ring(const RecurParams &p, cudaStream_t stream) {
   const int esz = p.in_bf16 ? 2 : 4;
   const int smem = (int)smem_bytes(esz, ring_xrows(p.steps, kRing), kRing, kNla);
@@ -584,9 +598,9 @@ cudaError_t launch_ring(const RecurParams &p, cudaStream_t stream) {
     if (!encode_3d_map(&tmap, p.S_src, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dims, box, false))
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(decode128_kernel<kRing, kNla>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(decode128_kernel<kRing, kNla, kOut>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode128_kernel<kRing, kNla>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(decode128_kernel<kRing, kNla, kOut>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -606,17 +620,23 @@ cudaError_t launch_ring(const RecurParams &p, cudaStream_t stream) {
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   int max_clusters = 0;
   cfg.gridDim = dim3(2 * (unsigned)sms);
-  if ((e = cudaOccupancyMaxActiveClusters(&max_clusters, decode128_kernel<kRing, kNla>, &cfg)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveClusters(&max_clusters, decode128_kernel<kRing, kNla, kOut>, &cfg)) != cudaSuccess) return e;
   if (max_clusters < 1) max_clusters = 1;
   const long long units = (long long)p.N * p.H;
   const long long clusters = units < max_clusters ? units : max_clusters;
   cfg.gridDim = dim3((unsigned)(2 * clusters));
-  return cudaLaunchKernelEx(&cfg, decode128_kernel<kRing, kNla>, tmap, p);
+  return cudaLaunchKernelEx(&cfg, decode128_kernel<kRing, kNla, kOut>, tmap, p);
+}
+
+template <bool kOut>
+cudaError_t launch_decode128_out(const RecurParams &p, cudaStream_t stream) {
+  if (p.variant == GLINATTN_NLA)
+    return p.steps > 1 ? launch_ring<1, true, kOut>(p, stream) : launch_ring<2, true, kOut>(p, stream);
+  return p.steps > 1 ? launch_ring<1, false, kOut>(p, stream) : launch_ring<2, false, kOut>(p, stream);
 }
 
 cudaError_t launch_decode128(const RecurParams &p, cudaStream_t stream) {
-  if (p.variant == GLINATTN_NLA) return p.steps > 1 ? launch_ring<1, true>(p, stream) : launch_ring<2, true>(p, stream);
-  return p.steps > 1 ? launch_ring<1, false>(p, stream) : launch_ring<2, false>(p, stream);
+  return p.o ? launch_decode128_out<true>(p, stream) : launch_decode128_out<false>(p, stream);
 }
 
 }  // namespace glinattn
