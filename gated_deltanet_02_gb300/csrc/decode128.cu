@@ -378,12 +378,19 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
         for (int i = 0; i < kMaxC; ++i) {
           const int c = tid + i * kNT;
           const float x = xr[i];
-          float y = conv ? fe::conv4(wr[i][0], wr[i][1], wr[i][2], wr[i][3], hr[i][0], hr[i][1], hr[i][2], x) : x;
-          if (nla && c < 2 * kD) y = feature_map(y);
+          // without outputs q' is not needed (i = 0 holds the q channels)
+          float y = 0.f;
+          if (kOut || i > 0) {
+            y = conv ? fe::conv4(wr[i][0], wr[i][1], wr[i][2], wr[i][3], hr[i][0], hr[i][1], hr[i][2], x) : x;
+            if (nla && c < 2 * kD) y = feature_map(y);
+          }
           yv[i] = y;
           // one q and one k channel per thread (channel tid of each)
-          if (c < kD) sq = __fmul_rn(y, y);
-          else if (c < 2 * kD) sk = __fmul_rn(y, y);
+          if (c < kD) {
+            if (kOut) sq = __fmul_rn(y, y);
+          } else if (c < 2 * kD) {
+            sk = __fmul_rn(y, y);
+          }
           hr[i][0] = hr[i][1];
           hr[i][1] = hr[i][2];
           hr[i][2] = x;
@@ -395,14 +402,14 @@ __global__ void __launch_bounds__(kNT, kRing == 1 ? 5 : 4) decode128_kernel(cons
         }
         float iq = 1.f, ik = 1.f;
         if (p.qk_l2norm) {  // pairwise sums of squares: lanes, then warps
-          sq = fe::warp_pairwise_sum(sq);
+          if (kOut) sq = fe::warp_pairwise_sum(sq);
           sk = fe::warp_pairwise_sum(sk);
           if (lane == 0) {
-            s_wsum[warp] = sq;
+            if (kOut) s_wsum[warp] = sq;
             s_wsum[kNW + warp] = sk;
           }
           __syncthreads();
-          iq = fe::inv_norm(fe::pairwise_sum<kNW>(s_wsum));
+          if (kOut) iq = fe::inv_norm(fe::pairwise_sum<kNW>(s_wsum));
           ik = fe::inv_norm(fe::pairwise_sum<kNW>(s_wsum + kNW));
         }
         const bool round_act = in_bf16 && (conv || p.qk_l2norm || nla);
