@@ -253,30 +253,32 @@ __global__ void __launch_bounds__(kVT, 2) verify128_kernel(const RecurParams p) 
 
   // ---- K S and Q S: this warp's 16 rows, then the sum over the 8 warps --------
   for (int g0 = 0; g0 < D; g0 += kG) {
-    float4 kp[kG], qp[kG];
+    // fused multiply-adds on column pairs (two lanes of one instruction)
+    float2 kp[kG][2], qp[kG][2];
 #pragma unroll
-    for (int i = 0; i < kG; ++i) {
-      kp[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      qp[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    for (int i = 0; i < kG; ++i)
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) kp[i][h2] = qp[i][h2] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
       const int row = 16 * warp + r;
+      const float2 s01 = make_float2(S[r].x, S[r].y), s23 = make_float2(S[r].z, S[r].w);
 #pragma unroll
       for (int i = 0; i < kG; ++i) {
         const int t = g0 + i < D ? g0 + i : D - 1;  // past D: a repeat, never used
         const float kv = act[t * 3 * kD + kD + row], qv = act[t * 3 * kD + row];
-        kp[i].x = fmaf(kv, S[r].x, kp[i].x); kp[i].y = fmaf(kv, S[r].y, kp[i].y);
-        kp[i].z = fmaf(kv, S[r].z, kp[i].z); kp[i].w = fmaf(kv, S[r].w, kp[i].w);
-        qp[i].x = fmaf(qv, S[r].x, qp[i].x); qp[i].y = fmaf(qv, S[r].y, qp[i].y);
-        qp[i].z = fmaf(qv, S[r].z, qp[i].z); qp[i].w = fmaf(qv, S[r].w, qp[i].w);
+        const float2 k2 = make_float2(kv, kv), q2 = make_float2(qv, qv);
+        kp[i][0] = __ffma2_rn(k2, s01, kp[i][0]);
+        kp[i][1] = __ffma2_rn(k2, s23, kp[i][1]);
+        qp[i][0] = __ffma2_rn(q2, s01, qp[i][0]);
+        qp[i][1] = __ffma2_rn(q2, s23, qp[i][1]);
       }
     }
     float4 *red4 = reinterpret_cast<float4 *>(vsm + kOffRed);
 #pragma unroll
     for (int i = 0; i < kG; ++i) {
-      red4[((warp * 2 * kG) + 2 * i) * (kD / 4) + lane] = kp[i];
-      red4[((warp * 2 * kG) + 2 * i + 1) * (kD / 4) + lane] = qp[i];
+      red4[((warp * 2 * kG) + 2 * i) * (kD / 4) + lane] = make_float4(kp[i][0].x, kp[i][0].y, kp[i][1].x, kp[i][1].y);
+      red4[((warp * 2 * kG) + 2 * i + 1) * (kD / 4) + lane] = make_float4(qp[i][0].x, qp[i][0].y, qp[i][1].x, qp[i][1].y);
     }
     __syncthreads();
     // the sums over the warps; in the last group warp 0 forms the D x D scalars
