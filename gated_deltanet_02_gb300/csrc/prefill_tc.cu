@@ -512,7 +512,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           float dh[32], dl[32];
           tmem_ld32x2(tmem + kColDS + 32 * half + lane_base, tmem + kColDS + kBV + 32 * half + lane_base, dh, dl);
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) S[32 * half + jj] = gam * S[32 * half + jj] + (dh[jj] + dl[jj]);
+          for (int jj = 0; jj < 32; jj += 2) {
+            if constexpr (kNla) {  // two-lane arithmetic: faster in this instance, slower in the gated ones
+              const float2 r = __ffma2_rn(make_float2(gam, gam), make_float2(S[32 * half + jj], S[32 * half + jj + 1]),
+                                          __fadd2_rn(make_float2(dh[jj], dh[jj + 1]), make_float2(dl[jj], dl[jj + 1])));
+              S[32 * half + jj] = r.x;
+              S[32 * half + jj + 1] = r.y;
+            } else {
+              S[32 * half + jj] = gam * S[32 * half + jj] + (dh[jj] + dl[jj]);
+              S[32 * half + jj + 1] = gam * S[32 * half + jj + 1] + (dh[jj + 1] + dl[jj + 1]);
+            }
+          }
         }
       }
       tc_fence_before();
@@ -549,7 +559,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                       tmem + kColO2 + tb * 64 + 16 * qt + lane_base, o1, o1l, o2);
           float ov[16];
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) ov[jj] = gi * (o1[jj] + o1l[jj]) + o2[jj];
+          for (int jj = 0; jj < 16; jj += 2) {
+            if constexpr (kNla) {
+              const float2 r = __ffma2_rn(make_float2(gi, gi),
+                                          __fadd2_rn(make_float2(o1[jj], o1[jj + 1]), make_float2(o1l[jj], o1l[jj + 1])),
+                                          make_float2(o2[jj], o2[jj + 1]));
+              ov[jj] = r.x;
+              ov[jj + 1] = r.y;
+            } else {
+              ov[jj] = gi * (o1[jj] + o1l[jj]) + o2[jj];
+              ov[jj + 1] = gi * (o1[jj + 1] + o1l[jj + 1]) + o2[jj + 1];
+            }
+          }
           if (kNla) {
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) ov[jj] *= inv_den;
