@@ -362,7 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = 16 * q4 + (lane & 15), jb = 32 * (lane >> 4);
         const uint32_t phi = smem_u32(smem + kOffP);
         const uint32_t plo = phi + kTileP;
-        if (gr.factored) {  // warp-uniform
+        if constexpr (kNla) {  // every gate is 1: D is the causal mask
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) qk[jj] = (jb + jj <= row) ? qk[jj] : 0.f;
+        } else if (gr.factored) {  // warp-uniform
           const float rf = gr.eg[row];
           const uint32_t cfa = smem_u32(&gr.ecg[jb]);
 #pragma unroll
@@ -390,23 +393,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int half = lane >> 4;
           const uint32_t qrow = smem_u32(smem + kOffStage + s * kStageBytes) + half * (kTileQ / 2);
           const float4 *zh = zw + 16 * half;
-          float den = 0.f;
+          // four two-lane partial sums, so the chain of additions stays short
+          float2 e[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) den += qk[jj];
+          for (int jj = 0; jj < 32; jj += 8) {
+#pragma unroll
+            for (int m = 0; m < 4; ++m) e[m] = __fadd2_rn(e[m], make_float2(qk[jj + 2 * m], qk[jj + 2 * m + 1]));
+          }
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {
             float x[8];
             unpack8(lds128(qrow + swz(row, ch)), x);
             const float4 za = zh[2 * ch], zb = zh[2 * ch + 1];
-            den = fmaf(x[0], za.x, den);
-            den = fmaf(x[1], za.y, den);
-            den = fmaf(x[2], za.z, den);
-            den = fmaf(x[3], za.w, den);
-            den = fmaf(x[4], zb.x, den);
-            den = fmaf(x[5], zb.y, den);
-            den = fmaf(x[6], zb.z, den);
-            den = fmaf(x[7], zb.w, den);
+            e[0] = __ffma2_rn(make_float2(x[0], x[1]), make_float2(za.x, za.y), e[0]);
+            e[1] = __ffma2_rn(make_float2(x[2], x[3]), make_float2(za.z, za.w), e[1]);
+            e[2] = __ffma2_rn(make_float2(x[4], x[5]), make_float2(zb.x, zb.y), e[2]);
+            e[3] = __ffma2_rn(make_float2(x[6], x[7]), make_float2(zb.z, zb.w), e[3]);
           }
+          float den = ((e[0].x + e[0].y) + (e[1].x + e[1].y)) + ((e[2].x + e[2].y) + (e[3].x + e[3].y));
           den += __shfl_xor_sync(0xffffffffu, den, 16);
           if (lane < 16) reinterpret_cast<float *>(smem + kOffDen)[(c & (kDenSlots - 1)) * kC + row] = 1.f / (den + 1e-6f);
           mbar_arrive(&bars->den_ready[c & (kDenSlots - 1)]);
@@ -440,8 +444,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ch = 4 * half + k;
           float x[8];
           unpack8(lds128(vt + swz(t, ch)), x);
+          if (!kNla) {  // r = 1 without gates
 #pragma unroll
-          for (int i = 0; i < 8; ++i) x[i] *= r;
+            for (int i = 0; i < 8; ++i) x[i] *= r;
+          }
           uint4 uh, ul;
           split8(x, uh, ul);
           sts128(vhi + swz(t, ch), uh);
