@@ -271,11 +271,25 @@ def run_ours(args):
     # the copies in and out on their own streams (both directions of the host
     # link and the kernel run side by side), so the figure is the whole job's
     # rate.  The copy in (202 MB a step) sets it: spreading it over three copy
-    # streams measured no faster.
-    host = {k: ex[k].cpu().pin_memory() for k in ("q", "k", "v", "alpha")}
+    # streams measured no faster.  The step's inputs sit in one pinned buffer
+    # (q, k, v, alpha back to back, each at a 16-byte boundary), so the copy
+    # in is one transfer; the prefill gets views into the device copy.
+    names = ("q", "k", "v", "alpha")
+    sizes = [ex[k].numel() * ex[k].element_size() for k in names]
+    offs = [sum((n + 255) // 256 * 256 for n in sizes[:i]) for i in range(len(sizes))]
+    total = offs[-1] + sizes[-1]
+
+    def views(buf):
+        return {k: buf[off:off + n].view(ex[k].dtype).view(ex[k].shape) for k, off, n in zip(names, offs, sizes)}
+
+    hraw = torch.empty(total, dtype=torch.uint8).pin_memory()
+    host = views(hraw)
+    for k in names:
+        host[k].copy_(ex[k].cpu())
     o_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
     S_h = [torch.empty(S.shape, dtype=S.dtype).pin_memory() for _ in range(2)]
-    dbuf = [{k: torch.empty_like(ex[k]) for k in host} for _ in range(2)]
+    draw = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+    dbuf = [views(d) for d in draw]
     o2 = [o, torch.empty_like(o)]
     S2 = [S, torch.empty_like(S)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -291,8 +305,7 @@ def run_ours(args):
         j = i % 2
         s_in.wait_event(ev_comp[j])  # buffer set j's last prefill has read its inputs
         with torch.cuda.stream(s_in):
-            for k in host:
-                dbuf[j][k].copy_(host[k], non_blocking=True)
+            draw[j].copy_(hraw, non_blocking=True)
             ev_in[j].record(s_in)
         comp.wait_event(ev_in[j])
         comp.wait_event(ev_out[j])  # and its last outputs are copied out
@@ -323,7 +336,7 @@ def run_ours(args):
         return max_over_ranks(dist, t0.elapsed_time(t1) / steps, dev)
 
     e2e_ms = e2e_timed(max(4, args.steps // 2), 2)
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = hraw.numel()  # the bytes the one copy in moves (inputs plus alignment gaps)
     d2h = o_h[0].numel() * o_h[0].element_size() + S_h[0].numel() * S_h[0].element_size()
 
     # ---- Gated DeltaNet decode, batch 256 -----------------------------------------
