@@ -141,9 +141,12 @@ static_assert(sizeof(GateRing) <= kGateBytes, "gate ring entry");
 // template parameters, so that each instance carries only its own paths in
 // the epilogue loop (a compact loop measured faster than runtime branches).
 // kNla: normalised linear attention (gates 1, q and k already the features):
-// warpgroup A also forms each token's denominator phi(q_t) . z_t from z at the
-// chunk start and the row sum of the masked phi(Q) phi(K)^T, and warpgroup B
-// divides the outputs by it.
+// warpgroup A also carries z from chunk to chunk (each warp its own copy, plus
+// the chunk's column sums of phi(k), which arrive with the tiles) and forms
+// each token's denominator phi(q_t) . z_t from z at the chunk start and the
+// row sum of the masked phi(Q) phi(K)^T; warpgroup B divides the outputs by
+// it.  This instance multiplies by no gate and uses two-lane arithmetic in
+// its state fold and outputs (faster here, slower in the gated instances).
 template <bool kOutBf16, bool kEmit, bool kNla>
 __global__ void __launch_bounds__(kThreads, 1)
     gla_prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
