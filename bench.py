@@ -835,6 +835,21 @@ def run_profile(args):
         def step():
             glinattn_spec_decode(dr["q"], dr["k"], dr["v"], dr["alpha"], dr["beta"], pool, src, dst, variant=GDN,
                                  conv_w=conv_w, conv_pool=cpool, qk_l2norm=True, o=od)
+    elif args.profile == "replay":  # the accepted drafts (0..4 per request, seeded) applied in place
+        from gated_deltanet_02_gb300 import glinattn_replay
+        N, D, H, d = 64, 4, 32, 128
+        g = torch.Generator(device=dev)
+        g.manual_seed(0)
+        pool = torch.randn(N, H, d, d, device=dev, generator=g) * 0.01
+        cpool = torch.randn(N, 3, 3 * H * d, device=dev, generator=g).to(torch.bfloat16)
+        conv_w = torch.randn(3 * H * d, 4, device=dev, generator=g) * 0.5
+        src = torch.arange(N, dtype=torch.int32, device=dev)
+        dr = inputs.spec_drafts(N, D, H, d, seed=1, device=dev)
+        accept = dr["accept"]
+
+        def step():
+            glinattn_replay(dr["k"], dr["v"], dr["alpha"], dr["beta"], pool, src, accept, q=dr["q"], variant=GDN,
+                            conv_w=conv_w, conv_pool=cpool, qk_l2norm=True)
     elif args.profile == "ssd":
         ex = inputs.ssd_prefill(2, 32, 1, 4096, seed=0, device=dev)
         o = torch.empty(2, 4096, 32, 64, dtype=torch.bfloat16, device=dev)
@@ -906,7 +921,7 @@ def run_profile(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["gla", "decode", "gdn", "spec", "verify", "ssd", "nla", "scan",
+    ap.add_argument("--profile", choices=["gla", "decode", "gdn", "spec", "verify", "replay", "ssd", "nla", "scan",
                                           "nla_decode", "scan_decode"], default=None,
                     help="run one workload's kernel a few times for a profiler, then exit")
     ap.add_argument("--launches", type=int, default=3)
